@@ -1,0 +1,138 @@
+"""Pins of the oracle's number-format codecs and quantisers against the format definitions,
+closed forms and torch's own conversions (independent library routines)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import codecs, moe
+
+
+def test_e4m3_table_matches_definition_landmarks():
+    t = codecs.E4M3_VALUES
+    assert t[0x00] == 0.0 and t[0x80] == 0.0
+    assert t[0x01] == 2.0 ** -9          # smallest subnormal: 1/8 * 2^-6
+    assert t[0x08] == 2.0 ** -6          # smallest normal
+    assert t[0x38] == 1.0                # exponent field 7 = bias
+    assert t[0x7E] == 448.0              # largest finite
+    assert math.isnan(t[0x7F]) and math.isnan(t[0xFF])
+    assert t[0xFE] == -448.0
+
+
+def test_e4m3_table_matches_torch_for_every_code():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    ours = codecs.E4M3_VALUES
+    both_nan = np.isnan(ref) & np.isnan(ours)
+    assert np.all(both_nan | (ref == ours))
+
+
+def test_e4m3_encode_matches_torch_rne():
+    rng = np.random.default_rng(7)
+    v = np.concatenate([rng.standard_normal(20000) * 50, rng.standard_normal(2000) * 0.01,
+                        codecs.E4M3_VALUES[:0x7F], -codecs.E4M3_VALUES[1:0x7F]])
+    # midpoints between neighbouring magnitudes: ties must go to the even code
+    mids = (codecs.E4M3_VALUES[1:0x7F] + codecs.E4M3_VALUES[0:0x7E]) / 2
+    v = np.concatenate([v, mids, -mids])
+    v = np.clip(v, -448, 448).astype(np.float32).astype(np.float64)
+    ref = torch.from_numpy(v).to(torch.float32).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    ours = codecs.e4m3_encode_rne_satfinite(v)
+    # +0 / -0 may differ in sign bit only
+    same = (ref == ours) | ((ref & 0x7F) == 0) & ((ours & 0x7F) == 0)
+    assert np.all(same)
+
+
+def test_e4m3_encode_saturates():
+    assert codecs.e4m3_encode_rne_satfinite(np.array([1e6]))[0] == 0x7E
+    assert codecs.e4m3_encode_rne_satfinite(np.array([-500.0]))[0] == 0xFE
+
+
+def test_e2m1_table_is_the_format():
+    mags = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    assert list(codecs.E2M1_VALUES[:8]) == mags
+    assert list(codecs.E2M1_VALUES[8:]) == [-m for m in mags]
+
+
+def test_e2m1_unpack_nibble_order():
+    # byte 0x21: low nibble code 1 (0.5) is element 0, high nibble code 2 (1.0) is element 1
+    out = codecs.e2m1_unpack_decode(np.array([[0x21, 0xF7]], dtype=np.uint8))
+    assert out.tolist() == [[0.5, 1.0, 6.0, -6.0]]
+
+
+def test_ue8m0():
+    s = np.array([0, 1, 127, 128, 254, 255], dtype=np.uint8)
+    d = codecs.ue8m0_decode(s)
+    assert d[0] == 2.0 ** -127 and d[1] == 2.0 ** -126 and d[2] == 1.0 and d[3] == 2.0
+    assert d[4] == 2.0 ** 127 and math.isnan(d[5])
+
+
+def test_bf16_rounding_matches_torch():
+    rng = np.random.default_rng(3)
+    v = np.concatenate([rng.standard_normal(50000), rng.standard_normal(5000) * 1e-30,
+                        rng.standard_normal(5000) * 1e30])
+    v32 = v.astype(np.float32)
+    # exact ties: bf16 value + half a spacing (low 16 bits = 0x8000)
+    ties = ((v32.view(np.uint32) & np.uint32(0xFFFF0000)) | np.uint32(0x8000)).view(np.float32)
+    v32 = np.concatenate([v32, ties])
+    ref = torch.from_numpy(v32).to(torch.bfloat16).to(torch.float64).numpy()
+    ours = codecs.round_to_bf16(v32.astype(np.float64))
+    assert np.array_equal(ref, ours)
+    assert np.array_equal(codecs.bf16_decode(codecs.bf16_encode(ours)), ours)
+
+
+def test_int8_row_quant_range_and_error():
+    rng = np.random.default_rng(5)
+    a = rng.standard_normal((64, 300)) * rng.uniform(0.01, 100, size=(64, 1))
+    q, s = moe.quant_int8_rows(a)
+    assert q.dtype == np.int8 and q.min() >= -127 and q.max() <= 127
+    assert (q != -128).all()
+    a32 = a.astype(np.float32).astype(np.float64)
+    arg = np.argmax(np.abs(a32), axis=1)
+    assert np.all(np.abs(q[np.arange(64), arg]) == 127)
+    err = np.abs(q * s[:, None].astype(np.float64) - a32)
+    assert np.all(err <= s[:, None] * 0.5 * (1 + 1e-6))
+
+
+def test_int8_row_quant_zero_row():
+    q, s = moe.quant_int8_rows(np.zeros((2, 8)))
+    assert np.all(q == 0) and np.all(s == np.float32(1e-8))
+
+
+def test_mx_exponent_rule():
+    am = np.array([448.0, 449.0, 224.0, 896.0, 1.0, 0.0, 3.0e-38], dtype=np.float32)
+    e = moe.mx_scale_exponent(am, 448.0)
+    assert e[0] == 0 and e[1] == 1 and e[2] == -1 and e[3] == 1
+    assert e[4] == math.ceil(math.log2(1.0 / 448.0)) and e[5] == -127
+    assert e[6] == -127  # clamped to the smallest UE8M0 exponent
+
+
+def test_mx_fp8_quant_properties():
+    rng = np.random.default_rng(9)
+    a = rng.standard_normal((16, 128)) * rng.uniform(1e-3, 1e3, size=(16, 1))
+    a[3, 32:64] = 0.0
+    codes, sc = moe.quant_mx_fp8(a)
+    vals = codecs.e4m3_decode(codes)
+    scale = codecs.ue8m0_decode(sc)
+    assert np.all(np.abs(vals) <= 448.0)
+    assert np.all(vals[3, 32:64] == 0.0)
+    deq = vals * np.repeat(scale, 32, axis=1)
+    a32 = a.astype(np.float32).astype(np.float64)
+    # the block's largest element lands in the top binade of e4m3: |amax/2^e| > 224
+    blocks = np.abs(a32).reshape(16, 4, 32).max(axis=2)
+    nz = blocks > 0
+    assert np.all((blocks / scale)[nz] > 224.0) and np.all((blocks / scale)[nz] <= 448.0)
+    # RNE error: at most half a spacing of the element's binade (relative 2^-4)
+    rel = np.abs(deq - a32) / np.maximum(np.abs(a32), 2.0 ** -6 * np.repeat(scale, 32, axis=1))
+    assert np.all(rel <= 2.0 ** -4 + 1e-12)
+
+
+def test_int32_accumulator_guard():
+    q = np.full((1, 200000), 127, dtype=np.int8)
+    w = np.full((200000, 1), 127, dtype=np.int8)
+    with pytest.raises(OverflowError):
+        moe._int_matmul_checked(q, w)
+    # the largest inner dimension of the configurations fits: 5120 * 127^2 < 2^31
+    q = np.full((1, 5120), -127, dtype=np.int8)
+    w = np.full((5120, 1), 127, dtype=np.int8)
+    assert moe._int_matmul_checked(q, w)[0, 0] == -5120 * 127 * 127

@@ -1,0 +1,209 @@
+"""Pins of the oracle's plan, SwiGLU and forward path against the pages' worked example,
+hand-derived closed forms, invariants, brute force and library routines."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+from oracle import codecs, moe
+from workloads import Workload, make_inputs, to_numpy
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _load(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------------------------------
+# plan
+# ---------------------------------------------------------------------------------------
+
+
+def test_plan_worked_example():
+    g = _load("plan_count_prefix_scatter.json")
+    counts, offsets, row_src = moe.plan(np.array(g["topk_ids"]), g["num_experts"])
+    assert counts.tolist() == g["counts"]
+    assert offsets.tolist() == g["offsets"]
+    assert row_src.tolist() == g["row_src"]
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_plan_invariants(seed):
+    rng = np.random.default_rng(seed)
+    T, E = int(rng.integers(1, 60)), int(rng.integers(1, 20))
+    K = int(rng.integers(1, min(E, 6) + 1))
+    ids = np.stack([rng.permutation(E)[:K] for _ in range(T)]).astype(np.int32)
+    if seed % 2:
+        ids[rng.random(ids.shape) < 0.2] = -1  # masked routes
+    counts, offsets, row_src = moe.plan(ids, E)
+    valid = ids.reshape(-1) >= 0
+    assert counts.sum() == valid.sum() == offsets[-1]
+    # brute-force count and N_e = |I_e| (ids unique per token)
+    for e in range(E):
+        assert counts[e] == np.sum(ids == e) == len({i for i in range(T) if e in ids[i]})
+    # (i,k) -> pool position is a bijection onto [0, R) and rows sit in their expert's range
+    assert sorted(row_src.tolist()) == sorted(np.flatnonzero(valid).tolist())
+    for e in range(E):
+        for p in range(offsets[e], offsets[e + 1]):
+            assert ids.reshape(-1)[row_src[p]] == e
+
+
+def test_plan_rejects_bad_ids():
+    with pytest.raises(ValueError):
+        moe.plan(np.array([[0, 4]]), 4)
+    with pytest.raises(ValueError):
+        moe.plan(np.array([[-2, 1]]), 4)
+
+
+# ---------------------------------------------------------------------------------------
+# SiLU / SwiGLU
+# ---------------------------------------------------------------------------------------
+
+
+def test_silu_closed_forms():
+    z = np.linspace(-30, 30, 6001)
+    s = moe.silu(z)
+    assert moe.silu(np.array([0.0]))[0] == 0.0
+    # SiLU(z) - SiLU(-z) = z  (z*sigma(z) - (-z)*sigma(-z) = z*(sigma(z)+sigma(-z)) = z)
+    assert np.allclose(s - moe.silu(-z), z, rtol=0, atol=1e-12)
+    assert abs(moe.silu(np.array([1.0]))[0] - 1.0 / (1.0 + math.exp(-1.0))) < 1e-15
+    assert abs(moe.silu(np.array([60.0]))[0] - 60.0) < 1e-20 * 60 + 1e-12
+    assert abs(moe.silu(np.array([-60.0]))[0]) < 1e-24
+    assert moe.silu(np.array([-1000.0]))[0] == 0.0
+    # the global minimum is at z* = -1.2784645 with value -0.2784645 (z* = -(1 + W(1/e)))
+    zs = -(1.0 + scipy.special.lambertw(1.0 / math.e).real)
+    assert abs(zs + 1.2784645428) < 1e-9
+    assert np.min(s) >= moe.silu(np.array([zs]))[0] - 1e-15
+    assert abs(moe.silu(np.array([zs]))[0] + 0.2784645428) < 1e-9
+    # sigmoid from scipy (an independent routine)
+    assert np.allclose(s, z * scipy.special.expit(z), rtol=1e-14, atol=1e-300)
+
+
+def test_swiglu_gate_is_first_half():
+    h = np.array([[1.0, -1.0]])  # gate = 1, up = -1
+    assert moe.swiglu(h, 1)[0, 0] == pytest.approx(-1.0 / (1.0 + math.exp(-1.0)), abs=1e-15)
+
+
+# ---------------------------------------------------------------------------------------
+# Closed-form examples
+# ---------------------------------------------------------------------------------------
+
+
+def test_closed_form_a16w16():
+    g = _load("ffn_closed_form_a16w16.json")
+    bf = lambda a: codecs.bf16_encode(np.array(a, dtype=np.float64))
+    y = moe.forward("a16w16", bf(g["x"]), None, np.array(g["topk_ids"]),
+                    np.array(g["topk_weights"], dtype=np.float32), bf(g["w1"]), None, bf(g["w2"]), None,
+                    num_experts=2, inter=g["intermediate"])
+    assert y.tolist() == g["y"]
+
+
+def test_closed_form_int8():
+    g = _load("ffn_closed_form_int8.json")
+    q = np.array(g["q"], dtype=np.int8)
+    w1 = np.array([g["w1_stored"]], dtype=np.int8)
+    w2 = np.array([g["w2_stored"]], dtype=np.int8)
+    y, rec = moe.expert_ffn("a8w8_int8", q.astype(np.float64), np.array(g["x_scale"], np.float32),
+                            moe.decode_weight("a8w8_int8", w1, None, 0),
+                            np.array(g["w1_scale"], np.float32),
+                            moe.decode_weight("a8w8_int8", w2, None, 0),
+                            np.array(g["w2_scale"], np.float32), inter=1)
+    assert rec["c"].tolist() == g["c"] and rec["h"].tolist() == g["h"]
+    assert rec["d"].tolist() == g["d"]
+    a = 12.0 / (1.0 + math.exp(-3.0))
+    assert rec["a"].tolist() == [[127]]
+    assert y[0, 0] == pytest.approx(a, rel=2e-7) and y[0, 1] == pytest.approx(-2 * a, rel=2e-7)
+
+
+# ---------------------------------------------------------------------------------------
+# Whole path: brute force, reductions, linearity
+# ---------------------------------------------------------------------------------------
+
+
+def _np(inp):
+    return to_numpy(inp)
+
+
+TINY = {
+    "a16w16": Workload("t", "a16w16", 12, 64, 64, 4, 2, 11, 0.1),
+    "a8w8_fp8": Workload("t", "a8w8_fp8", 12, 128, 64, 4, 2, 12, 0.1),
+    "a8w8_int8": Workload("t", "a8w8_int8", 12, 96, 64, 4, 3, 13, 0.1),
+    "a8w4_fp8_fp4": Workload("t", "a8w4_fp8_fp4", 12, 128, 64, 4, 2, 14, 0.1),
+}
+
+
+def _forward(mode, d, wl, **kw):
+    return moe.forward(mode, d["x"], d["x_scale"], d["topk_ids"], d["topk_weights"], d["w1"],
+                       d["w1_scale"], d["w2"], d["w2_scale"], num_experts=wl.E, inter=wl.I, **kw)
+
+
+@pytest.mark.parametrize("mode", list(TINY))
+def test_brute_force_per_token_equals_pooled_path(mode):
+    wl = TINY[mode]
+    d = _np(make_inputs(wl))
+    y = _forward(mode, d, wl)
+    yb = moe.forward_tokens(mode, range(wl.T), d["x"], d["x_scale"], d["topk_ids"], d["topk_weights"],
+                            d["w1"], d["w1_scale"], d["w2"], d["w2_scale"], inter=wl.I)
+    assert np.array_equal(y, yb)
+    assert np.all(np.isfinite(y)) and np.abs(y).max() > 0
+
+
+def test_dense_reduction_matches_library_routines():
+    """E=1, K=1, G=1: y = bf16(bf16(SwiGLU(x W1)) W2), computed with torch float64 matmul
+    and torch's SiLU, an implementation independent of the oracle's."""
+    wl = Workload("dense", "a16w16", 20, 64, 32, 1, 1, 21, 0.2)
+    inp = make_inputs(wl)
+    inp["topk_weights"] = torch.ones_like(inp["topk_weights"])
+    d = _np(inp)
+    y = _forward("a16w16", d, wl)
+    x = inp["x"].double()
+    h = x @ inp["w1"][0].double()
+    a = (torch.nn.functional.silu(h[:, :32]) * h[:, 32:]).to(torch.bfloat16).double()
+    ref = (a @ inp["w2"][0].double()).float().to(torch.bfloat16).double().numpy()
+    assert np.array_equal(y, ref)
+
+
+def test_linearity_in_gates_and_masking():
+    wl = TINY["a16w16"]
+    d = _np(make_inputs(wl))
+    d0 = dict(d, topk_weights=np.zeros_like(d["topk_weights"]))
+    assert np.all(_forward("a16w16", d0, wl) == 0.0)
+    # one-hot gates select slot 0 only; masking slot 1 gives the same result
+    g1 = np.zeros_like(d["topk_weights"])
+    g1[:, 0] = 1.0
+    y1 = _forward("a16w16", dict(d, topk_weights=g1), wl)
+    ids_m = d["topk_ids"].copy()
+    ids_m[:, 1] = -1
+    ym = _forward("a16w16", dict(d, topk_ids=ids_m), wl)
+    y1m = _forward("a16w16", dict(d, topk_ids=ids_m, topk_weights=g1), wl)
+    assert np.array_equal(y1, y1m)
+    _, rec = _forward("a16w16", dict(d, topk_ids=ids_m), wl, return_intermediates=True)
+    assert np.all(rec["comb"].reshape(wl.T, wl.K, -1)[:, 1] == 0.0)
+    assert ym.shape == y1.shape
+
+
+def test_int8_path_accumulators_are_integers_in_range():
+    wl = TINY["a8w8_int8"]
+    d = _np(make_inputs(wl))
+    _, rec = _forward("a8w8_int8", d, wl, return_intermediates=True)
+    for e, r in rec["experts"].items():
+        assert r["c"].dtype == np.int64 and r["d"].dtype == np.int64
+        assert np.abs(r["a"].astype(np.int64)).max() <= 127
+
+
+def test_fp8_mode_decoding_uses_block_scales():
+    """Scaling one 32-block's UE8M0 byte by +1 doubles exactly that block's contribution."""
+    wl = TINY["a8w8_fp8"]
+    d = _np(make_inputs(wl))
+    xd = moe.decode_x("a8w8_fp8", d["x"], d["x_scale"])
+    sc = d["x_scale"].copy()
+    sc[0, 1] += 1
+    xd2 = moe.decode_x("a8w8_fp8", d["x"], sc)
+    assert np.array_equal(xd2[0, 32:64], 2 * xd[0, 32:64])
+    assert np.array_equal(xd2[0, :32], xd[0, :32]) and np.array_equal(xd2[1:], xd[1:])
