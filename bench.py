@@ -1,0 +1,368 @@
+"""Benchmark of the fused MoE expert FFN (route -> dispatch -> L1+SwiGLU -> L2+gate -> combine).
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference] [--workload NAME]
+
+One step = one pass of the whole path (moe_plan, moe_dispatch, moe_expert_l1, moe_expert_l2,
+moe_combine -- the sequence moe_forward runs) over one batch of seeded synthetic inputs
+already resident in HBM. The default workload is the bf16 Mixtral-like prefill (4096 tokens,
+hidden 4096, intermediate 14336, 8 experts, top-2). Its weights (2.82 GB) are larger than the
+129 MB L2, so no L2 flush is needed between steps.
+
+Prints one JSON line (rank 0). value = TFLOP/s of algorithmic work (6*H*I per routed row)
+summed over ranks; under torchrun every rank runs an independent replica (weak scaling, no
+collective on the data path). `--impl reference` times the CPU oracle (float64 numpy) on the
+host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused MoE FFN TFLOP/s + routed rows/s, % of tensor/HBM roofline, 1xGB300"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+DTYPE = {"a16w16": "bf16", "a8w8_fp8": "e4m3", "a8w8_int8": "int8", "a8w4_fp8_fp4": "e4m3xe2m1"}
+LAUNCHES_PER_STEP = {"a16w16": 7, "a8w8_fp8": 7, "a8w8_int8": 8, "a8w4_fp8_fp4": 7}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="mixtral_bf16_prefill")
+    ap.add_argument("--flags", type=int, default=0, help="GEMM stage flags (1 = CUDA-core reference kernels)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def workload_config(wl):
+    return {"workload": wl.name, "mode": wl.mode, "tokens": wl.T, "hidden": wl.H, "intermediate": wl.I,
+            "experts": wl.E, "topk": wl.K, "routed_rows": wl.routed_rows, "seed": wl.seed,
+            "l2_policy": "inputs larger than L2 (no flush)"}
+
+
+# ---------------------------------------------------------------------------------------
+# CPU oracle (the reference arm and the cpu_baseline leg)
+# ---------------------------------------------------------------------------------------
+
+
+def oracle_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var):
+            return int(os.environ[var])
+    return os.cpu_count() or 1
+
+
+def oracle_sample(wl, inp_host, n_tokens, seed):
+    """Run the oracle, as it stands, on a seeded sample of n_tokens tokens; returns
+    (seconds, routed rows computed)."""
+    import numpy as np
+    from oracle import moe as omoe
+    rng = np.random.default_rng(seed)
+    tokens = np.sort(rng.choice(wl.T, size=n_tokens, replace=False))
+    h = inp_host
+    xs = None if h["x_scale"] is None else h["x_scale"][tokens]
+    ids = h["topk_ids"][tokens]
+    t0 = time.perf_counter()
+    omoe.forward(wl.mode, h["x"][tokens], xs, ids, h["topk_weights"][tokens], h["w1"], h["w1_scale"], h["w2"],
+                 h["w2_scale"], num_experts=wl.E, inter=wl.I)
+    dt = time.perf_counter() - t0
+    return dt, int((ids >= 0).sum())
+
+
+def cpu_tokens_per_sample(wl):
+    # a handful of tokens: the oracle's cost is dominated by decoding each touched expert
+    return 2 if wl.H * wl.I >= 4096 * 8192 else 8
+
+
+def host_inputs(wl):
+    from workloads import make_inputs, to_numpy
+    import torch
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    return to_numpy(make_inputs(wl, device=dev))
+
+
+def run_reference(args, wl, rank, world):
+    if rank != 0:
+        return None
+    h = host_inputs(wl)
+    n_tok = cpu_tokens_per_sample(wl)
+    for w in range(args.warmup):
+        oracle_sample(wl, h, n_tok, seed=1000 + w)
+    total_t, total_rows = 0.0, 0
+    for s in range(args.steps):
+        dt, rows = oracle_sample(wl, h, n_tok, seed=2000 + s)
+        total_t += dt
+        total_rows += rows
+    flops = 6.0 * wl.H * wl.I * total_rows
+    value = flops / total_t / 1e12
+    cores = oracle_threads()
+    sample = f"{n_tok} seeded tokens per step ({total_rows / args.steps:.0f} routed rows), float64 numpy oracle"
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(wl), "routed_rows_per_s": total_rows / total_t,
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# ---------------------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------------------
+
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu_index = gpu_index
+        self.out = os.path.join("/tmp", f"moe_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.out, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={CLOCK_FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.out):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.out):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]), "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())}
+
+
+# ---------------------------------------------------------------------------------------
+# the GB300 arm
+# ---------------------------------------------------------------------------------------
+
+
+def dominant_kernel_traffic(workload):
+    """DRAM bytes per launch of the L1 GEMM from the committed ncu summary, valid only while
+    the kernel sources are the ones the counters were taken on."""
+    path = os.path.join(ROOT, "profiles", f"l1_gemm_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*(\d+)", txt)
+    h = re.search(r"source_sha256:\s*([0-9a-f]{16,64})", txt)
+    if not m or not h:
+        return None
+    return int(m.group(1)) if h.group(1) == kernel_source_hash()[:len(h.group(1))] else None
+
+
+def kernel_source_hash():
+    d = os.path.join(ROOT, "moe_expert_ffn_topk_gb300", "csrc")
+    sha = hashlib.sha256()
+    for name in sorted(os.listdir(d)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            sha.update(open(os.path.join(d, name), "rb").read())
+    return sha.hexdigest()
+
+
+def run_gb300(args, wl, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import moe_expert_ffn_topk_gb300 as moe
+    from workloads import make_inputs
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream()
+    inp = make_inputs(wl, device=dev)
+    d = moe.dims(wl.T, wl.H, wl.I, wl.E, wl.K)
+    ws = moe.alloc_workspace(d, wl.mode, dev)
+    y = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=dev)
+
+    def step(ev_l1=None):
+        moe.moe_plan(inp["topk_ids"], d, ws, stream=stream)
+        moe.moe_dispatch(inp["x"], inp["x_scale"], d, wl.mode, ws, stream=stream)
+        if ev_l1:
+            ev_l1[0].record(stream)
+        moe.moe_expert_l1(inp["w1"], inp["w1_scale"], d, wl.mode, ws, args.flags, stream=stream)
+        if ev_l1:
+            ev_l1[1].record(stream)
+        moe.moe_expert_l2(inp["w2"], inp["w2_scale"], inp["topk_weights"], d, wl.mode, ws, args.flags, stream=stream)
+        moe.moe_combine(y, d, ws, stream=stream)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        step()
+    st = moe.moe_check_device_error(ws)
+    if st != 0:
+        raise RuntimeError(f"device error during warm-up: {moe.moe_status_string(st)}")
+
+    l1_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clocks:
+        barrier()
+        t0.record(stream)
+        for i in range(args.steps):
+            step(l1_events[i])
+        t1.record(stream)
+        barrier()
+    elapsed_ms = t0.elapsed_time(t1)
+    l1_ms = statistics.mean(a.elapsed_time(b) for a, b in l1_events)
+    st = moe.moe_check_device_error(ws)
+    if st != 0:
+        raise RuntimeError(f"device error in the timed region: {moe.moe_status_string(st)}")
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    # end to end through the public API with host buffers: H2D of the step's inputs from
+    # pinned memory, the forward call, D2H of y
+    host_in = {k: inp[k].cpu().pin_memory() for k in ("x", "x_scale", "topk_ids", "topk_weights")
+               if inp[k] is not None}
+    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
+    y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = y_host.numel() * y_host.element_size()
+
+    def e2e_step():
+        for k, v in host_in.items():
+            dev_in[k].copy_(v, non_blocking=True)
+        moe.moe_forward(dev_in["x"], dev_in.get("x_scale"), dev_in["topk_ids"], dev_in["topk_weights"], inp["w1"],
+                        inp["w1_scale"], inp["w2"], inp["w2_scale"], y, d, wl.mode, ws, args.flags, stream=stream)
+        y_host.copy_(y, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    if rank != 0:
+        return None, None
+    flops = float(wl.flops)
+    ms_per_step = elapsed_ms / args.steps
+    value = world * flops * args.steps / (elapsed_ms * 1e-3) / 1e12
+    pk, pk_src = peaks()
+    l1_flops = 4.0 * wl.H * wl.I * wl.routed_rows
+    achieved = l1_flops / (l1_ms * 1e-3) / 1e12
+    peak = float(pk.get("bf16_tflops_sustained", pk.get("bf16_tflops")))
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": DTYPE[wl.mode], "data": "synthetic (seeded; random-init weights)",
+        "config": workload_config(wl),
+        "routed_rows_per_s": world * wl.routed_rows * args.steps / (elapsed_ms * 1e-3),
+        "roofline": {"bound": "tensor", "kernel": "L1 grouped GEMM + SwiGLU (moe_expert_l1)",
+                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                     "peak_source": f"{pk_src} bf16 dense, sustained", "l1_ms": l1_ms,
+                     "traffic": dominant_kernel_traffic(wl.name)},
+        "e2e": {"value": world * flops * args.steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps},
+        "gpu_launches": LAUNCHES_PER_STEP[wl.mode] * args.steps,
+        "clocks": clocks.summary(),
+    }
+    return line, inp
+
+
+def main():
+    args = parse()
+    from workloads import WORKLOADS
+    wl = WORKLOADS[args.workload]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, wl, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    line, inp = run_gb300(args, wl, rank, world, local_rank)
+    if line is not None and not args.no_cpu_baseline:
+        from workloads import to_numpy
+        h = to_numpy(inp)
+        n_tok = cpu_tokens_per_sample(wl)
+        dt, rows = oracle_sample(wl, h, n_tok, seed=7)
+        line["cpu_baseline"] = {"value": 6.0 * wl.H * wl.I * rows / dt / 1e12, "unit": "TFLOP/s",
+                                "cores": oracle_threads(), "kind": "oracle",
+                                "sample": f"{n_tok} seeded tokens ({rows} routed rows) of {wl.name}, "
+                                          f"{dt:.1f} s, float64 numpy oracle"}
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

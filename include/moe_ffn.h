@@ -1,0 +1,196 @@
+/*
+ * moe_ffn.h -- C ABI of the GB300 fused MoE expert feed-forward with top-k combine.
+ *
+ * What the library computes (Ascend "mega_moe" page, "Computation Process", A16W16 use
+ * case, and its A8W8-INT / A8W8-FP use cases; DeepGEMM MegaMoE page §4 for the
+ * FP8-activation x FP4-weight recipe):
+ *
+ *     y_i = sum_{k<K} G[i,k] * Y_{e_ik}[row(i,k), :]
+ *     Y_e = SwiGLU(X_e . W1[e]) . W2[e],   SwiGLU(H) = SiLU(H[:, :I]) * H[:, I:]
+ *
+ * in five stages on one GPU: route metadata (count, prefix sum, scatter), dispatch (gather
+ * of the routed x rows into a per-expert pool), L1 grouped GEMM with SwiGLU and
+ * re-quantisation fused, L2 grouped GEMM with the gate weight applied, and the combine of
+ * the K weighted rows of each token in fixed slot order.
+ *
+ * Conventions shared by every entry point
+ *   - All tensors are row-major and contiguous. Pointers marked "device" must point to
+ *     device memory of the current CUDA device; the library reads inputs, writes outputs
+ *     and the caller's workspace, and keeps no pointer after the call returns.
+ *   - The library allocates nothing. The caller owns every buffer, including the workspace
+ *     of moe_workspace_bytes() bytes (256-byte aligned).
+ *   - Every call is asynchronous on `stream` (NULL = legacy default stream) and never
+ *     synchronises the host, except moe_check_device_error().
+ *   - Argument errors are found on the host before anything is launched and returned as a
+ *     status. Errors found on the device (an expert id outside [-1, E), a bounded wait
+ *     that ran out) are recorded in the workspace's error word; read them with
+ *     moe_check_device_error().
+ *   - Limits: 0 <= T, 1 <= K <= 32, K <= E <= 1024, H and I multiples of 128, and
+ *     T*K <= 2^24.
+ */
+#ifndef MOE_FFN_H
+#define MOE_FFN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+/* A CUDA stream (cudaStream_t / CUstream) without including CUDA headers. */
+typedef struct CUstream_st* moe_stream_t;
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* a size, pointer or alignment the op does not accept  */
+    MOE_ERR_UNSUPPORTED = 2,   /* a mode / shape combination this build does not run    */
+    MOE_ERR_CUDA = 3,          /* a CUDA runtime call or kernel launch failed           */
+    MOE_ERR_BAD_ROUTE = 4,     /* device: an expert id outside [-1, E); route skipped   */
+    MOE_ERR_TIMEOUT = 5,       /* device: a bounded wait ran out; results are invalid   */
+    MOE_ERR_WORKSPACE = 6      /* workspace missing, misaligned or too small            */
+} moe_status;
+
+/* Storage formats of the four use cases (Ascend mega_moe page, "Use Case / A / W" table;
+ * DeepGEMM page §1 for FP8 x FP4). T tokens, H hidden, I intermediate, E experts.
+ *
+ * MOE_A16W16        x bf16 [T,H]; w1 bf16 [E,H,2I]; w2 bf16 [E,I,H] (the page's math
+ *                   layout: hidden x 2*intermediate per expert). No scales.
+ * MOE_A8W8_FP8      x e4m3 [T,H] + UE8M0 bytes [T,H/32]; w1 e4m3 [E,2I,H] + UE8M0
+ *                   [E,2I,H/32]; w2 e4m3 [E,H,I] + UE8M0 [E,H,I/32] (the page's transposed
+ *                   FP8 layout; its (N, K/64, 2) scale shape is this (N, K/32)).
+ * MOE_A8W8_INT8     x int8 [T,H] in [-127,127] + fp32 [T] per-token scale; w1 int8
+ *                   [E,2I,H] + fp32 [E,2I]; w2 int8 [E,H,I] + fp32 [E,H] per output channel.
+ * MOE_A8W4_FP8_FP4  x e4m3 [T,H] + fp32 [T,H/128] power-of-two block scales; w1 e2m1
+ *                   [E,2I,H/2] + UE8M0 [E,2I,H/32]; w2 e2m1 [E,H,I/2] + UE8M0 [E,H,I/32];
+ *                   two e2m1 codes per byte, element 2j in the low nibble.
+ * In every mode the gate columns of w1 are the first I outputs and the up columns the
+ * last I; y is bf16 [T,H]. */
+typedef enum {
+    MOE_A16W16 = 0,
+    MOE_A8W8_FP8 = 1,
+    MOE_A8W8_INT8 = 2,
+    MOE_A8W4_FP8_FP4 = 3
+} moe_dtype_mode;
+
+typedef struct {
+    int32_t num_tokens;    /* T */
+    int32_t hidden;        /* H */
+    int32_t intermediate;  /* I: the width of A; w1 has 2*I outputs */
+    int32_t num_experts;   /* E */
+    int32_t topk;          /* K */
+} moe_dims;
+
+/* A quantised tensor: its codes and, where the mode has them, its scales (device). */
+typedef struct {
+    const void* data;
+    const void* scale;
+} moe_operand;
+
+/* Flags of the GEMM stages. */
+enum {
+    MOE_FLAG_NONE = 0u,
+    MOE_FLAG_SIMT = 1u   /* run the CUDA-core reference GEMMs instead of the tensor-core ones */
+};
+
+/* Bytes of workspace that moe_plan / moe_forward and the stage calls need for `d` and `m`.
+ * Returns 0 when `d` is outside the limits above. The caller allocates it (device memory,
+ * 256-byte aligned); its contents need no initialisation. */
+MOE_API size_t moe_workspace_bytes(const moe_dims* d, moe_dtype_mode m);
+
+/* Stage S1, route metadata (Ascend page, A16W16 "EP Dispatch": I_e, N_e = |I_e|, row(i,k);
+ * metadata page §1 and §3: count -> prefix sum -> scatter).
+ *   topk_ids  device int32 [T,K]: expert of each (token, slot); -1 = masked route (skipped);
+ *             other ids outside [0,E) set MOE_ERR_BAD_ROUTE and are skipped.
+ *   counts    device int32 [E]   or NULL: N_e, the routed rows of each expert (the page's
+ *             expert_token_nums output).
+ *   offsets   device int32 [E+1] or NULL: exclusive prefix sum of counts; offsets[E] = R.
+ *   row_src   device int32 [T*K] or NULL: row_src[p] = i*K+k for p < R, the (token, slot)
+ *             identity of routed row p; rows of expert e fill [offsets[e], offsets[e+1]),
+ *             in an order the call does not fix (the page allows any fixed order).
+ * The plan is also kept in the workspace for the stages that follow. */
+MOE_API moe_status moe_plan(const int32_t* topk_ids, const moe_dims* d, int32_t* counts, int32_t* offsets,
+                    int32_t* row_src, void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/* Stage S2, dispatch: copies x row i (and its scales) into the workspace's pool row of every
+ * routed (i, k), the single-GPU form of the page's EP Dispatch. Needs moe_plan first.
+ *   x  device operand in the mode's x format. */
+MOE_API moe_status moe_dispatch(moe_operand x, const moe_dims* d, moe_dtype_mode m, void* workspace,
+                        size_t workspace_bytes, moe_stream_t stream);
+
+/* Stages S3+S4, L1 grouped GEMM with SwiGLU and the L2-operand re-quantisation fused
+ * (Ascend page: "Linear1 Projection", "SwiGLU Activation", and the A8W8 activation
+ * quantisation of "Linear2"; DeepGEMM page §4 step 6). Needs moe_dispatch first.
+ *   w1  device operand in the mode's w1 format. Writes the L2 operand A into the workspace:
+ *       bf16 (A16W16), e4m3 + UE8M0 per 1x32 (both FP8 modes), int8 + fp32 per row (INT8). */
+MOE_API moe_status moe_expert_l1(moe_operand w1, const moe_dims* d, moe_dtype_mode m, uint32_t flags,
+                         void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/* Stage S5, L2 grouped GEMM with the gate weight applied (Ascend page "Linear2 Projection"
+ * and "Token Combine": w_k * Y_e[row(i,k)]). Needs moe_expert_l1 first.
+ *   w2            device operand in the mode's w2 format.
+ *   topk_weights  device fp32 [T,K] gate weights G.
+ * Writes bf16(G[i,k] * Y[row(i,k)]) (product in fp32) into the workspace's combine row i*K+k. */
+MOE_API moe_status moe_expert_l2(moe_operand w2, const float* topk_weights, const moe_dims* d, moe_dtype_mode m,
+                         uint32_t flags, void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/* Stage S6, combine (Ascend page "Token Combine"): y[i,:] = bf16( sum_{k=0..K-1} c[i,k,:] )
+ * summed in fp32 in slot order; masked slots contribute nothing. Needs moe_expert_l2 first.
+ *   y  device bf16 [T,H]; every row is written. */
+MOE_API moe_status moe_combine(void* y, const moe_dims* d, void* workspace, size_t workspace_bytes,
+                       moe_stream_t stream);
+
+/* The whole path: moe_plan, moe_dispatch, moe_expert_l1, moe_expert_l2, moe_combine in
+ * stream order. Deterministic: the same inputs give bit-identical y. */
+MOE_API moe_status moe_forward(moe_operand x, const int32_t* topk_ids, const float* topk_weights, moe_operand w1,
+                       moe_operand w2, void* y, const moe_dims* d, moe_dtype_mode m, uint32_t flags,
+                       void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/* Synchronises `stream`, returns the first device-side error recorded in the workspace
+ * (MOE_OK if none) and clears it. */
+MOE_API moe_status moe_check_device_error(void* workspace, moe_stream_t stream);
+
+/* Static text for a status code. */
+MOE_API const char* moe_status_string(moe_status s);
+
+/* Byte offsets of the workspace regions, for inspection of the intermediate stages. Rows of
+ * expert e in the pools start at pad_offsets[e] (a multiple of the 128-row tile) and the
+ * pool holds at most pool_rows rows. A region that a mode does not use has size 0. */
+typedef struct {
+    size_t header;        /* int32[16]: [0] error word, [1] R, [2] padded rows, [3] row tiles */
+    size_t counts;        /* int32[E]   */
+    size_t offsets;       /* int32[E+1] */
+    size_t pad_offsets;   /* int32[E+1] padded row offsets of the pools */
+    size_t tile_offsets;  /* int32[E+1] cumulative 128-row tiles */
+    size_t row_src;       /* int32[T*K] unpadded pool row -> i*K+k */
+    size_t pool_src;      /* int32[pool_rows] padded pool row -> i*K+k, -1 for padding */
+    size_t slot_row;      /* int32[T*K] i*K+k -> padded pool row, -1 if masked */
+    size_t x_pool;        /* gathered x codes [pool_rows, H] */
+    size_t x_pool_scale;  /* gathered x scales [pool_rows, *] */
+    size_t a_pool;        /* L2 operand codes [pool_rows, I] */
+    size_t a_pool_scale;  /* L2 operand scales [pool_rows, *] */
+    size_t a_f32;         /* fp32 A [pool_rows, I] (INT8 mode: before the per-row quantisation) */
+    size_t comb;          /* bf16 [T*K, H] weighted rows */
+    size_t total;         /* = moe_workspace_bytes() */
+    int64_t pool_rows;    /* rows reserved in each pool */
+} moe_workspace_layout_t;
+
+MOE_API moe_status moe_workspace_layout(const moe_dims* d, moe_dtype_mode m, moe_workspace_layout_t* out);
+
+/* Test hook for the failure path of a bounded device wait: launches one thread that waits
+ * on a workspace flag that nothing sets, gives up after `timeout_ns` nanoseconds, records
+ * MOE_ERR_TIMEOUT in the error word and returns. The device stays usable. */
+MOE_API moe_status moe_debug_bounded_wait(void* workspace, size_t workspace_bytes, uint64_t timeout_ns,
+                                  moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_FFN_H */

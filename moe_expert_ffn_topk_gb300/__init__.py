@@ -1,0 +1,21 @@
+"""GB300-native fused MoE expert feed-forward with top-k combine.
+
+The computation runs in the CUDA library ``_lib/libmoe_gb300.so`` (sources in ``csrc/``,
+C ABI in ``include/moe_ffn.h``); this package is its thin Python binding. Importing it
+without the built library raises ImportError: there is no fallback path.
+"""
+import torch
+
+from ._binding import (ABI_FUNCTIONS, MODES, MOE_FLAG_NONE, MOE_FLAG_SIMT, MoeDims, MoeError,  # noqa: F401
+                       dims, moe_check_device_error, moe_combine, moe_debug_bounded_wait, moe_dispatch,
+                       moe_expert_l1, moe_expert_l2, moe_forward, moe_plan, moe_status_string,
+                       moe_workspace_bytes, moe_workspace_layout)
+
+
+def alloc_workspace(d: MoeDims, mode, device="cuda") -> torch.Tensor:
+    """A device byte buffer of moe_workspace_bytes(d, mode) bytes (torch allocations are
+    at least 256-byte aligned)."""
+    n = moe_workspace_bytes(d, mode)
+    if n == 0:
+        raise ValueError("dimensions outside the library's limits")
+    return torch.empty(n, dtype=torch.uint8, device=device)

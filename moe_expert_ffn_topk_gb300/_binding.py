@@ -1,0 +1,184 @@
+"""ctypes binding of the C ABI in ``include/moe_ffn.h``.
+
+Argument marshalling only: each function takes torch tensors (device memory allocated by
+the caller), checks placement and contiguity, passes their addresses and the current CUDA
+stream to the library function of the same name, and turns a non-OK status into
+``MoeError``. Every stage of the computation runs in the library's CUDA kernels. When the
+library has not been built, importing this module raises ``ImportError``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libmoe_gb300.so")
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_BAD_ROUTE, MOE_ERR_TIMEOUT, \
+    MOE_ERR_WORKSPACE = range(7)
+MODES = {"a16w16": 0, "a8w8_fp8": 1, "a8w8_int8": 2, "a8w4_fp8_fp4": 3}
+MOE_FLAG_NONE, MOE_FLAG_SIMT = 0, 1
+
+ABI_FUNCTIONS = ("moe_workspace_bytes", "moe_plan", "moe_dispatch", "moe_expert_l1", "moe_expert_l2",
+                 "moe_combine", "moe_forward", "moe_check_device_error", "moe_status_string",
+                 "moe_workspace_layout", "moe_debug_bounded_wait")
+
+
+class MoeDims(ctypes.Structure):
+    _fields_ = [("num_tokens", ctypes.c_int32), ("hidden", ctypes.c_int32), ("intermediate", ctypes.c_int32),
+                ("num_experts", ctypes.c_int32), ("topk", ctypes.c_int32)]
+
+
+class MoeOperand(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("scale", ctypes.c_void_p)]
+
+
+class MoeWorkspaceLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in (
+        "header", "counts", "offsets", "pad_offsets", "tile_offsets", "row_src", "pool_src", "slot_row",
+        "x_pool", "x_pool_scale", "a_pool", "a_pool_scale", "a_f32", "comb", "total")] + \
+        [("pool_rows", ctypes.c_int64)]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {moe_status_string(status)} (status {status})")
+
+
+def _load():
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(f"CUDA library not built ({_LIB_PATH} is missing); run __graft_entry__.build()")
+    lib = ctypes.CDLL(_LIB_PATH)
+    vp, sz, u32, st = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_uint32, ctypes.c_int
+    dims_p = ctypes.POINTER(MoeDims)
+    sig = {
+        "moe_workspace_bytes": (sz, [dims_p, st]),
+        "moe_plan": (st, [vp, dims_p, vp, vp, vp, vp, sz, vp]),
+        "moe_dispatch": (st, [MoeOperand, dims_p, st, vp, sz, vp]),
+        "moe_expert_l1": (st, [MoeOperand, dims_p, st, u32, vp, sz, vp]),
+        "moe_expert_l2": (st, [MoeOperand, vp, dims_p, st, u32, vp, sz, vp]),
+        "moe_combine": (st, [vp, dims_p, vp, sz, vp]),
+        "moe_forward": (st, [MoeOperand, vp, vp, MoeOperand, MoeOperand, vp, dims_p, st, u32, vp, sz, vp]),
+        "moe_check_device_error": (st, [vp, vp]),
+        "moe_status_string": (ctypes.c_char_p, [st]),
+        "moe_workspace_layout": (st, [dims_p, st, ctypes.POINTER(MoeWorkspaceLayout)]),
+        "moe_debug_bounded_wait": (st, [vp, sz, ctypes.c_uint64, vp]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype, f.argtypes = res, args
+    return lib
+
+
+LIB = _load()
+
+
+# ---------------------------------------------------------------------------------------
+# marshalling helpers
+# ---------------------------------------------------------------------------------------
+
+
+def dims(T: int, H: int, I: int, E: int, K: int) -> MoeDims:  # noqa: E741
+    return MoeDims(T, H, I, E, K)
+
+
+def _mode(m) -> int:
+    return MODES[m] if isinstance(m, str) else int(m)
+
+
+def _ptr(t, what, dev=True):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{what} must be a torch.Tensor")
+    if dev and not t.is_cuda:
+        raise ValueError(f"{what} must be in device memory")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    return t.data_ptr() if t.numel() else None
+
+
+def _operand(data, scale, what):
+    return MoeOperand(_ptr(data, what), _ptr(scale, what + "_scale"))
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ws(workspace):
+    return _ptr(workspace, "workspace"), workspace.numel() * workspace.element_size()
+
+
+def _check(status, what):
+    if status != MOE_OK:
+        raise MoeError(status, what)
+
+
+# ---------------------------------------------------------------------------------------
+# the ABI, one function each
+# ---------------------------------------------------------------------------------------
+
+
+def moe_status_string(status: int) -> str:
+    return LIB.moe_status_string(int(status)).decode()
+
+
+def moe_workspace_bytes(d: MoeDims, mode) -> int:
+    return LIB.moe_workspace_bytes(ctypes.byref(d), _mode(mode))
+
+
+def moe_workspace_layout(d: MoeDims, mode) -> dict:
+    out = MoeWorkspaceLayout()
+    _check(LIB.moe_workspace_layout(ctypes.byref(d), _mode(mode), ctypes.byref(out)), "moe_workspace_layout")
+    return {name: getattr(out, name) for name, _ in MoeWorkspaceLayout._fields_}
+
+
+def moe_plan(topk_ids, d: MoeDims, workspace, counts=None, offsets=None, row_src=None, stream=None):
+    ws, nb = _ws(workspace)
+    _check(LIB.moe_plan(_ptr(topk_ids, "topk_ids"), ctypes.byref(d), _ptr(counts, "counts"),
+                        _ptr(offsets, "offsets"), _ptr(row_src, "row_src"), ws, nb, _stream(stream)), "moe_plan")
+
+
+def moe_dispatch(x, x_scale, d: MoeDims, mode, workspace, stream=None):
+    ws, nb = _ws(workspace)
+    _check(LIB.moe_dispatch(_operand(x, x_scale, "x"), ctypes.byref(d), _mode(mode), ws, nb, _stream(stream)),
+           "moe_dispatch")
+
+
+def moe_expert_l1(w1, w1_scale, d: MoeDims, mode, workspace, flags=0, stream=None):
+    ws, nb = _ws(workspace)
+    _check(LIB.moe_expert_l1(_operand(w1, w1_scale, "w1"), ctypes.byref(d), _mode(mode), flags, ws, nb,
+                             _stream(stream)), "moe_expert_l1")
+
+
+def moe_expert_l2(w2, w2_scale, topk_weights, d: MoeDims, mode, workspace, flags=0, stream=None):
+    ws, nb = _ws(workspace)
+    _check(LIB.moe_expert_l2(_operand(w2, w2_scale, "w2"), _ptr(topk_weights, "topk_weights"), ctypes.byref(d),
+                             _mode(mode), flags, ws, nb, _stream(stream)), "moe_expert_l2")
+
+
+def moe_combine(y, d: MoeDims, workspace, stream=None):
+    ws, nb = _ws(workspace)
+    _check(LIB.moe_combine(_ptr(y, "y"), ctypes.byref(d), ws, nb, _stream(stream)), "moe_combine")
+
+
+def moe_forward(x, x_scale, topk_ids, topk_weights, w1, w1_scale, w2, w2_scale, y, d: MoeDims, mode, workspace,
+                flags=0, stream=None):
+    ws, nb = _ws(workspace)
+    _check(LIB.moe_forward(_operand(x, x_scale, "x"), _ptr(topk_ids, "topk_ids"), _ptr(topk_weights, "topk_weights"),
+                           _operand(w1, w1_scale, "w1"), _operand(w2, w2_scale, "w2"), _ptr(y, "y"),
+                           ctypes.byref(d), _mode(mode), flags, ws, nb, _stream(stream)), "moe_forward")
+
+
+def moe_check_device_error(workspace, stream=None) -> int:
+    return LIB.moe_check_device_error(_ptr(workspace, "workspace"), _stream(stream))
+
+
+def moe_debug_bounded_wait(workspace, timeout_ns: int, stream=None):
+    ws, nb = _ws(workspace)
+    _check(LIB.moe_debug_bounded_wait(ws, nb, int(timeout_ns), _stream(stream)), "moe_debug_bounded_wait")

@@ -1,0 +1,250 @@
+// Host side of the C ABI: argument checks, workspace layout and the stage launch sequence.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+
+#include "internal.h"
+#include "moe_ffn.h"
+
+namespace moe {
+
+int x_elem_bytes(int mode) { return mode == MOE_A16W16 ? 2 : 1; }
+
+int64_t x_scale_row_bytes(int mode, int H) {
+    switch (mode) {
+        case MOE_A8W8_FP8: return H / 32;                // UE8M0 per 1x32
+        case MOE_A8W8_INT8: return 4;                    // fp32 per token
+        case MOE_A8W4_FP8_FP4: return (int64_t)(H / 128) * 4;  // fp32 per 1x128
+        default: return 0;
+    }
+}
+
+int a_elem_bytes(int mode) { return mode == MOE_A16W16 ? 2 : 1; }
+
+int64_t a_scale_row_bytes(int mode, int I) {
+    switch (mode) {
+        case MOE_A8W8_FP8:
+        case MOE_A8W4_FP8_FP4: return I / 32;            // UE8M0 per 1x32
+        case MOE_A8W8_INT8: return 4;                    // fp32 per row
+        default: return 0;
+    }
+}
+
+static bool dims_ok(const moe_dims* d, moe_dtype_mode m) {
+    if (!d) return false;
+    if (m < MOE_A16W16 || m > MOE_A8W4_FP8_FP4) return false;
+    if (d->num_tokens < 0 || d->topk < 1 || d->topk > 32) return false;
+    if (d->num_experts < d->topk || d->num_experts > 1024) return false;
+    if (d->hidden < 128 || d->hidden % 128 || d->intermediate < 128 || d->intermediate % 128) return false;
+    if ((int64_t)d->num_tokens * d->topk > (int64_t(1) << 24)) return false;
+    if ((int64_t)d->hidden > (1 << 16) || (int64_t)d->intermediate > (1 << 16)) return false;
+    return true;
+}
+
+static size_t align_up(size_t v) { return (v + 255) & ~size_t(255); }
+
+moe_status layout(const moe_dims* d, moe_dtype_mode m, moe_workspace_layout_t* out) {
+    if (!out || !dims_ok(d, m)) return MOE_ERR_INVALID_ARG;
+    const int64_t T = d->num_tokens, H = d->hidden, I = d->intermediate, E = d->num_experts, K = d->topk;
+    const int64_t R = T * K;
+    const int64_t pool_rows = R + std::min<int64_t>(E, R) * (kTileRows - 1);
+    moe_workspace_layout_t L;
+    std::memset(&L, 0, sizeof(L));
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t at = off;
+        off = align_up(off + bytes);
+        return at;
+    };
+    L.header = take(sizeof(int32_t) * kHeaderInts);
+    size_t claim = take(sizeof(int32_t) * E);
+    (void)claim;  // immediately after the header; not exported
+    L.counts = take(sizeof(int32_t) * E);
+    L.offsets = take(sizeof(int32_t) * (E + 1));
+    L.pad_offsets = take(sizeof(int32_t) * (E + 1));
+    L.tile_offsets = take(sizeof(int32_t) * (E + 1));
+    size_t pos = take(sizeof(int32_t) * R);
+    (void)pos;
+    L.row_src = take(sizeof(int32_t) * R);
+    L.pool_src = take(sizeof(int32_t) * pool_rows);
+    L.slot_row = take(sizeof(int32_t) * R);
+    L.comb = take((size_t)R * H * 2);
+    // everything above is the same for every mode; the pools below depend on it
+    L.x_pool = take((size_t)pool_rows * H * x_elem_bytes(m));
+    L.x_pool_scale = take((size_t)pool_rows * x_scale_row_bytes(m, (int)H));
+    L.a_pool = take((size_t)pool_rows * I * a_elem_bytes(m));
+    L.a_pool_scale = take((size_t)pool_rows * a_scale_row_bytes(m, (int)I));
+    L.a_f32 = take(m == MOE_A8W8_INT8 ? (size_t)pool_rows * I * 4 : 0);
+    L.total = off;
+    L.pool_rows = pool_rows;
+    *out = L;
+    return MOE_OK;
+}
+
+moe_status make_plan_view(const moe_dims* d, moe_dtype_mode m, void* ws, size_t ws_bytes, Plan* p, bool pools) {
+    moe_workspace_layout_t L;
+    moe_status st = layout(d, m, &L);
+    if (st != MOE_OK) return st;
+    const size_t need = pools ? L.total : L.x_pool;  // x_pool starts where the mode-free part ends
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < need) return MOE_ERR_WORKSPACE;
+    uint8_t* b = static_cast<uint8_t*>(ws);
+    p->T = d->num_tokens;
+    p->H = d->hidden;
+    p->I = d->intermediate;
+    p->E = d->num_experts;
+    p->K = d->topk;
+    p->mode = m;
+    p->pool_rows = L.pool_rows;
+    p->hdr = reinterpret_cast<int32_t*>(b + L.header);
+    p->claim = reinterpret_cast<int32_t*>(b + align_up(L.header + sizeof(int32_t) * kHeaderInts));
+    p->counts = reinterpret_cast<int32_t*>(b + L.counts);
+    p->offsets = reinterpret_cast<int32_t*>(b + L.offsets);
+    p->pad_off = reinterpret_cast<int32_t*>(b + L.pad_offsets);
+    p->tile_off = reinterpret_cast<int32_t*>(b + L.tile_offsets);
+    p->pos = reinterpret_cast<int32_t*>(b + align_up(L.tile_offsets + sizeof(int32_t) * (p->E + 1)));
+    p->row_src = reinterpret_cast<int32_t*>(b + L.row_src);
+    p->pool_src = reinterpret_cast<int32_t*>(b + L.pool_src);
+    p->slot_row = reinterpret_cast<int32_t*>(b + L.slot_row);
+    p->x_pool = b + L.x_pool;
+    p->x_pool_scale = b + L.x_pool_scale;
+    p->a_pool = b + L.a_pool;
+    p->a_pool_scale = b + L.a_pool_scale;
+    p->a_f32 = reinterpret_cast<float*>(b + L.a_f32);
+    p->comb = reinterpret_cast<uint16_t*>(b + L.comb);
+    return MOE_OK;
+}
+
+static moe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+static bool operand_ok(moe_operand o, bool needs_scale) {
+    if (!o.data) return false;
+    if (needs_scale && !o.scale) return false;
+    return true;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+size_t moe_workspace_bytes(const moe_dims* d, moe_dtype_mode m) {
+    moe_workspace_layout_t L;
+    if (layout(d, m, &L) != MOE_OK) return 0;
+    return L.total;
+}
+
+moe_status moe_workspace_layout(const moe_dims* d, moe_dtype_mode m, moe_workspace_layout_t* out) {
+    return layout(d, m, out);
+}
+
+moe_status moe_plan(const int32_t* topk_ids, const moe_dims* d, int32_t* counts, int32_t* offsets,
+                    int32_t* row_src, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+    Plan p;
+    moe_status st = make_plan_view(d, MOE_A16W16, workspace, workspace_bytes, &p, false);
+    if (st != MOE_OK) return st;
+    if (!topk_ids && d->num_tokens > 0) return MOE_ERR_INVALID_ARG;
+    return from_cuda(launch_route(p, topk_ids, counts, offsets, row_src, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_dispatch(moe_operand x, const moe_dims* d, moe_dtype_mode m, void* workspace, size_t workspace_bytes,
+                        moe_stream_t stream) {
+    Plan p;
+    moe_status st = make_plan_view(d, m, workspace, workspace_bytes, &p, true);
+    if (st != MOE_OK) return st;
+    if (d->num_tokens > 0 && !operand_ok(x, m != MOE_A16W16)) return MOE_ERR_INVALID_ARG;
+    return from_cuda(launch_dispatch(p, x.data, x.scale, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_expert_l1(moe_operand w1, const moe_dims* d, moe_dtype_mode m, uint32_t flags, void* workspace,
+                         size_t workspace_bytes, moe_stream_t stream) {
+    Plan p;
+    moe_status st = make_plan_view(d, m, workspace, workspace_bytes, &p, true);
+    if (st != MOE_OK) return st;
+    if (!operand_ok(w1, m != MOE_A16W16)) return MOE_ERR_INVALID_ARG;
+    if (d->num_tokens == 0) return MOE_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (!(flags & MOE_FLAG_SIMT) && tc_supported(p, 1)) {
+        e = launch_l1_tc(p, w1.data, w1.scale, s);
+    } else {
+        e = launch_l1_simt(p, w1.data, w1.scale, s);
+    }
+    if (e == cudaSuccess && m == MOE_A8W8_INT8) e = launch_int8_row_quant(p, s);
+    return from_cuda(e);
+}
+
+moe_status moe_expert_l2(moe_operand w2, const float* topk_weights, const moe_dims* d, moe_dtype_mode m,
+                         uint32_t flags, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+    Plan p;
+    moe_status st = make_plan_view(d, m, workspace, workspace_bytes, &p, true);
+    if (st != MOE_OK) return st;
+    if (!operand_ok(w2, m != MOE_A16W16)) return MOE_ERR_INVALID_ARG;
+    if (d->num_tokens == 0) return MOE_OK;
+    if (!topk_weights) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (!(flags & MOE_FLAG_SIMT) && tc_supported(p, 2))
+        return from_cuda(launch_l2_tc(p, w2.data, w2.scale, topk_weights, s));
+    return from_cuda(launch_l2_simt(p, w2.data, w2.scale, topk_weights, s));
+}
+
+moe_status moe_combine(void* y, const moe_dims* d, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+    Plan p;
+    moe_status st = make_plan_view(d, MOE_A16W16, workspace, workspace_bytes, &p, false);
+    if (st != MOE_OK) return st;
+    if (d->num_tokens == 0) return MOE_OK;
+    if (!y) return MOE_ERR_INVALID_ARG;
+    return from_cuda(launch_combine(p, static_cast<uint16_t*>(y), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_forward(moe_operand x, const int32_t* topk_ids, const float* topk_weights, moe_operand w1,
+                       moe_operand w2, void* y, const moe_dims* d, moe_dtype_mode m, uint32_t flags,
+                       void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+    Plan p;
+    moe_status st = make_plan_view(d, m, workspace, workspace_bytes, &p, true);
+    if (st != MOE_OK) return st;
+    const bool q = m != MOE_A16W16;
+    if (!operand_ok(w1, q) || !operand_ok(w2, q)) return MOE_ERR_INVALID_ARG;
+    if (d->num_tokens == 0) return MOE_OK;
+    if (!operand_ok(x, q) || !topk_ids || !topk_weights || !y) return MOE_ERR_INVALID_ARG;
+    if ((st = moe_plan(topk_ids, d, nullptr, nullptr, nullptr, workspace, workspace_bytes, stream)) != MOE_OK) return st;
+    if ((st = moe_dispatch(x, d, m, workspace, workspace_bytes, stream)) != MOE_OK) return st;
+    if ((st = moe_expert_l1(w1, d, m, flags, workspace, workspace_bytes, stream)) != MOE_OK) return st;
+    if ((st = moe_expert_l2(w2, topk_weights, d, m, flags, workspace, workspace_bytes, stream)) != MOE_OK) return st;
+    return moe_combine(y, d, workspace, workspace_bytes, stream);
+}
+
+moe_status moe_check_device_error(void* workspace, moe_stream_t stream) {
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255)) return MOE_ERR_WORKSPACE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int32_t err = 0;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemcpy(&err, workspace, sizeof(err), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+    const int32_t zero = 0;
+    if (cudaMemcpy(workspace, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return MOE_ERR_CUDA;
+    return static_cast<moe_status>(err);
+}
+
+const char* moe_status_string(moe_status s) {
+    switch (s) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "unsupported mode or shape";
+        case MOE_ERR_CUDA: return "CUDA error";
+        case MOE_ERR_BAD_ROUTE: return "expert id outside [-1, num_experts)";
+        case MOE_ERR_TIMEOUT: return "bounded device wait timed out";
+        case MOE_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        default: return "unknown status";
+    }
+}
+
+moe_status moe_debug_bounded_wait(void* workspace, size_t workspace_bytes, uint64_t timeout_ns, moe_stream_t stream) {
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255) || workspace_bytes < 256) return MOE_ERR_WORKSPACE;
+    Plan p;
+    std::memset(&p, 0, sizeof(p));
+    p.hdr = static_cast<int32_t*>(workspace);
+    return from_cuda(launch_debug_wait(p, timeout_ns, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

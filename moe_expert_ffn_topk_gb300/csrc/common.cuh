@@ -1,0 +1,82 @@
+// Device helpers shared by the kernels of the library.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+#include "internal.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------------------
+// Error word: the first error recorded wins.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ void record_error(int32_t* hdr, int code) {
+    atomicCAS(&hdr[kErrWord], 0, code);
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ---------------------------------------------------------------------------------------
+// Number formats (from the bit layouts of the formats)
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+    return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+__device__ __forceinline__ uint16_t float_to_bf16_bits(float v) {
+    __nv_bfloat16 h = __float2bfloat16_rn(v);
+    return *reinterpret_cast<uint16_t*>(&h);
+}
+
+// e4m3fn code -> float (exact), via the fp8 conversion of cuda_fp8.h
+__device__ __forceinline__ float e4m3_to_float(uint8_t c) {
+    __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(c), __NV_E4M3);
+    return __half2float(__half(h));
+}
+
+// float -> e4m3fn code, round to nearest even, saturating to +-448
+__device__ __forceinline__ uint8_t float_to_e4m3_satfinite(float v) {
+    return static_cast<uint8_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
+}
+
+// e2m1 code (low 4 bits) -> float: sign | 2 exponent bits (bias 1) | 1 mantissa bit
+__device__ __forceinline__ float e2m1_to_float(uint32_t c) {
+    const uint32_t e = (c >> 1) & 3u, m = c & 1u;
+    float mag = (e == 0) ? 0.5f * static_cast<float>(m)
+                         : (1.0f + 0.5f * static_cast<float>(m)) * static_cast<float>(1u << (e - 1));
+    return (c & 8u) ? -mag : mag;
+}
+
+// UE8M0 byte -> 2^(s-127) as float (s in [1, 254] is a normal float; s = 0 is 2^-127)
+__device__ __forceinline__ float ue8m0_to_float(uint8_t s) {
+    return s == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(static_cast<uint32_t>(s) << 23);
+}
+
+// Shared exponent of an MX block: the smallest e with amax <= emax * 2^e, clamped to
+// [-127, 127]; amax = 0 gives -127. For emax = 448 = 0.875 * 2^9: with amax = m * 2^x,
+// m in [0.5, 1), amax / 448 lies in (2^(x-10), 2^(x-9)] when m <= 0.875, else in
+// (2^(x-9), 2^(x-8)).
+__device__ __forceinline__ int mx_exponent_e4m3(float amax) {
+    if (!(amax > 0.0f)) return -127;
+    int x;
+    float m = frexpf(amax, &x);
+    int e = (m <= 0.875f) ? x - 9 : x - 8;
+    return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+// 2^-e as float for e in [-127, 126] (exact power of two)
+__device__ __forceinline__ float exp2_neg_int(int e) {
+    return __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+}
+
+__device__ __forceinline__ float silu(float z) {
+    return z / (1.0f + expf(-z));
+}
+
+}  // namespace moe

@@ -1,0 +1,68 @@
+// Internal declarations shared by the translation units of the library (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe_ffn.h"
+
+namespace moe {
+
+constexpr int kTileRows = 128;          // rows per pool tile; expert regions are padded to it
+constexpr int kHeaderInts = 16;         // workspace header: [0] error word, [1] R, [2] padded rows, [3] tiles
+constexpr int kErrWord = 0;
+constexpr int kHdrRows = 1;
+constexpr int kHdrPadRows = 2;
+constexpr int kHdrTiles = 3;
+constexpr int kHdrWaitFlag = 8;         // a flag that nothing sets (bounded-wait test hook)
+
+// Device view of the workspace for one (dims, mode).
+struct Plan {
+    int T, H, I, E, K;
+    int mode;
+    int64_t pool_rows;
+    int32_t* hdr;
+    int32_t* claim;        // [E] per-expert claim counters (zeroed at the start of each plan)
+    int32_t* counts;       // [E]
+    int32_t* offsets;      // [E+1]
+    int32_t* pad_off;      // [E+1]
+    int32_t* tile_off;     // [E+1]
+    int32_t* pos;          // [T*K] position of (i,k) inside its expert
+    int32_t* row_src;      // [T*K]
+    int32_t* pool_src;     // [pool_rows]
+    int32_t* slot_row;     // [T*K]
+    uint8_t* x_pool;       // [pool_rows, H * x elem bytes]
+    uint8_t* x_pool_scale;
+    uint8_t* a_pool;       // [pool_rows, I * a elem bytes]
+    uint8_t* a_pool_scale;
+    float* a_f32;          // [pool_rows, I] (INT8 mode)
+    uint16_t* comb;        // bf16 [T*K, H]
+};
+
+// x / A storage properties per mode
+int x_elem_bytes(int mode);            // bytes per x element (bf16 2, others 1)
+int64_t x_scale_row_bytes(int mode, int H);
+int a_elem_bytes(int mode);
+int64_t a_scale_row_bytes(int mode, int I);
+
+moe_status layout(const moe_dims* d, moe_dtype_mode m, moe_workspace_layout_t* out);
+moe_status make_plan_view(const moe_dims* d, moe_dtype_mode m, void* ws, size_t ws_bytes, Plan* p, bool pools);
+
+// Launchers (each returns cudaGetLastError() of its launches).
+cudaError_t launch_route(const Plan& p, const int32_t* topk_ids, int32_t* counts_out, int32_t* offsets_out,
+                         int32_t* row_src_out, cudaStream_t s);
+cudaError_t launch_dispatch(const Plan& p, const void* x, const void* x_scale, cudaStream_t s);
+cudaError_t launch_combine(const Plan& p, uint16_t* y, cudaStream_t s);
+cudaError_t launch_l1_simt(const Plan& p, const void* w1, const void* w1_scale, cudaStream_t s);
+cudaError_t launch_l2_simt(const Plan& p, const void* w2, const void* w2_scale, const float* topk_weights,
+                           cudaStream_t s);
+cudaError_t launch_int8_row_quant(const Plan& p, cudaStream_t s);
+cudaError_t launch_debug_wait(const Plan& p, uint64_t timeout_ns, cudaStream_t s);
+
+// Tensor-core path. Returns cudaErrorNotSupported when the mode / shape has no tcgen05 kernel.
+cudaError_t launch_l1_tc(const Plan& p, const void* w1, const void* w1_scale, cudaStream_t s);
+cudaError_t launch_l2_tc(const Plan& p, const void* w2, const void* w2_scale, const float* topk_weights,
+                         cudaStream_t s);
+bool tc_supported(const Plan& p, int stage);
+
+}  // namespace moe

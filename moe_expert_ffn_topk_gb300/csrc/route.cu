@@ -1,0 +1,269 @@
+// Stage S1 (route metadata), S2 (dispatch gather) and S6 (combine), plus the bounded-wait
+// test hook.
+//
+// Route metadata follows the count -> prefix sum -> scatter scheme of the layout-metadata
+// page (§1, §3.2-3.5): every CTA counts its ids per expert in shared memory with
+// warp-aggregated atomics, claims a contiguous range of each expert's rows with one global
+// atomicAdd per (CTA, expert) -- the returned old value is the CTA's base -- and a second
+// kernel scans the final counts into offsets. Unlike the prior art's single persistent
+// kernel with a grid barrier, the scan runs as its own tiny launch, so no CTA ever waits on
+// another.
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kRouteThreads = 256;
+constexpr int kRouteItems = 16;                       // ids per thread in the count kernel
+constexpr int kRouteChunk = kRouteThreads * kRouteItems;
+
+// Count ids per expert in shared memory (warp-aggregated), claim each expert's range with a
+// global atomicAdd and record every id's position inside its expert.
+__global__ void __launch_bounds__(kRouteThreads) route_count_claim_kernel(const int32_t* __restrict__ ids, int n_ids,
+                                                                          int E, int32_t* __restrict__ claim,
+                                                                          int32_t* __restrict__ pos,
+                                                                          int32_t* __restrict__ hdr) {
+    extern __shared__ int32_t smem[];
+    int32_t* hist = smem;      // [E] ids of this CTA per expert
+    int32_t* base = smem + E;  // [E] this CTA's first position in each expert
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+    __syncthreads();
+
+    const int lane = threadIdx.x & 31;
+    const int begin = blockIdx.x * kRouteChunk;
+    int expert[kRouteItems];
+    int rank[kRouteItems];
+#pragma unroll
+    for (int j = 0; j < kRouteItems; ++j) {
+        const int i = begin + j * kRouteThreads + threadIdx.x;
+        const bool in = i < n_ids;
+        int e = in ? ids[i] : -1;
+        const bool valid = in && e >= 0 && e < E;
+        if (in && !valid && e != -1) record_error(hdr, MOE_ERR_BAD_ROUTE);
+        expert[j] = valid ? e : -1;
+        rank[j] = -1;
+        const unsigned active = __ballot_sync(0xffffffffu, valid);
+        if (valid) {
+            const unsigned peers = __match_any_sync(active, e);   // lanes routed to the same expert
+            const int leader = __ffs(peers) - 1;
+            int b = 0;
+            if (lane == leader) b = atomicAdd(&hist[e], __popc(peers));
+            b = __shfl_sync(peers, b, leader);
+            rank[j] = b + __popc(peers & ((1u << lane) - 1u));
+        }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const int c = hist[e];
+        base[e] = c ? atomicAdd(&claim[e], c) : 0;               // global offset claim
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kRouteItems; ++j) {
+        const int i = begin + j * kRouteThreads + threadIdx.x;
+        if (i < n_ids) pos[i] = expert[j] >= 0 ? base[expert[j]] + rank[j] : -1;
+    }
+}
+
+// Exclusive scan over up to 1024 values, one per thread of a 1024-thread block.
+__device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, d);
+        if (lane >= d) x += y;
+    }
+    if (lane == 31) warp_sums[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = warp_sums[lane];
+        int s = w;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, s, d);
+            if (lane >= d) s += y;
+        }
+        warp_sums[lane] = s - w;  // exclusive prefix of the warp totals
+        if (lane == 31) *total = s;
+    }
+    __syncthreads();
+    const int out = x - v + warp_sums[warp];
+    __syncthreads();
+    return out;
+}
+
+// counts -> offsets, padded offsets and tile offsets; marks the padding rows of the pools.
+__global__ void __launch_bounds__(1024) route_scan_kernel(int E, const int32_t* __restrict__ claim,
+                                                          int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                                                          int32_t* __restrict__ pad_off, int32_t* __restrict__ tile_off,
+                                                          int32_t* __restrict__ pool_src, int32_t* __restrict__ hdr,
+                                                          int32_t* __restrict__ counts_out,
+                                                          int32_t* __restrict__ offsets_out) {
+    __shared__ int warp_sums[32];
+    __shared__ int total_rows, total_tiles;
+    const int e = threadIdx.x;
+    const int c = e < E ? claim[e] : 0;
+    const int tiles = (c + kTileRows - 1) / kTileRows;
+    const int off = block_exclusive_scan(c, warp_sums, &total_rows);
+    const int toff = block_exclusive_scan(tiles, warp_sums, &total_tiles);
+    if (e < E) {
+        counts[e] = c;
+        offsets[e] = off;
+        tile_off[e] = toff;
+        pad_off[e] = toff * kTileRows;
+        if (counts_out) counts_out[e] = c;
+        if (offsets_out) offsets_out[e] = off;
+        for (int r = toff * kTileRows + c; r < (toff + tiles) * kTileRows; ++r) pool_src[r] = -1;
+    }
+    if (e == 0) {
+        offsets[E] = total_rows;
+        tile_off[E] = total_tiles;
+        pad_off[E] = total_tiles * kTileRows;
+        if (offsets_out) offsets_out[E] = total_rows;
+        hdr[kHdrRows] = total_rows;
+        hdr[kHdrPadRows] = total_tiles * kTileRows;
+        hdr[kHdrTiles] = total_tiles;
+    }
+}
+
+// Scatter every routed (i,k) to its pool row and record both directions of the identity map.
+__global__ void route_scatter_kernel(const int32_t* __restrict__ ids, int n_ids, int E, const int32_t* __restrict__ pos,
+                                     const int32_t* __restrict__ offsets, const int32_t* __restrict__ pad_off,
+                                     int32_t* __restrict__ row_src, int32_t* __restrict__ pool_src,
+                                     int32_t* __restrict__ slot_row, int32_t* __restrict__ row_src_out) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n_ids) return;
+    const int e = ids[i];
+    const int p = pos[i];
+    if (e < 0 || e >= E || p < 0) {
+        slot_row[i] = -1;
+        return;
+    }
+    const int row = offsets[e] + p;
+    const int prow = pad_off[e] + p;
+    row_src[row] = i;
+    if (row_src_out) row_src_out[row] = i;
+    pool_src[prow] = i;
+    slot_row[i] = prow;
+}
+
+// S2: copy x row (token = src / K) and its scale row into every padded pool row; padding
+// rows get zeros.
+__global__ void __launch_bounds__(128) dispatch_gather_kernel(const uint4* __restrict__ x, const uint32_t* __restrict__ xs,
+                                                              const int32_t* __restrict__ pool_src,
+                                                              const int32_t* __restrict__ hdr, int K, int row_vecs,
+                                                              int scale_words, uint4* __restrict__ xp,
+                                                              uint32_t* __restrict__ xps) {
+    const int rows = hdr[kHdrPadRows];
+    for (int r = blockIdx.x; r < rows; r += gridDim.x) {
+        const int src = pool_src[r];
+        uint4* dst = xp + (size_t)r * row_vecs;
+        if (src >= 0) {
+            const uint4* s = x + (size_t)(src / K) * row_vecs;
+            for (int v = threadIdx.x; v < row_vecs; v += blockDim.x) dst[v] = s[v];
+            for (int w = threadIdx.x; w < scale_words; w += blockDim.x)
+                xps[(size_t)r * scale_words + w] = xs[(size_t)(src / K) * scale_words + w];
+        } else {
+            const uint4 z = make_uint4(0, 0, 0, 0);
+            for (int v = threadIdx.x; v < row_vecs; v += blockDim.x) dst[v] = z;
+            for (int w = threadIdx.x; w < scale_words; w += blockDim.x) xps[(size_t)r * scale_words + w] = 0u;
+        }
+    }
+}
+
+// S6: y[t, 8j..8j+7] = bf16( sum_k comb[t*K+k, 8j..8j+7] ), fp32 sum in slot order.
+__global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ comb, const int32_t* __restrict__ slot_row,
+                                                      int T, int K, int row_vecs, uint4* __restrict__ y) {
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (int64_t)T * row_vecs) return;
+    const int t = (int)(idx / row_vecs);
+    const int v = (int)(idx % row_vecs);
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+    for (int k = 0; k < K; ++k) {
+        if (slot_row[t * K + k] < 0) continue;   // masked route: contributes nothing
+        const uint4 c = comb[((size_t)t * K + k) * row_vecs + v];
+        const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            acc[2 * j] = __fadd_rn(acc[2 * j], __uint_as_float(w[j] << 16));
+            acc[2 * j + 1] = __fadd_rn(acc[2 * j + 1], __uint_as_float(w[j] & 0xffff0000u));
+        }
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        o[j] = (uint32_t)float_to_bf16_bits(acc[2 * j]) | ((uint32_t)float_to_bf16_bits(acc[2 * j + 1]) << 16);
+    y[(size_t)t * row_vecs + v] = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Waits for hdr[kHdrWaitFlag] to become non-zero, at most timeout_ns; on time-out records
+// MOE_ERR_TIMEOUT and returns.
+__global__ void debug_wait_kernel(int32_t* hdr, uint64_t timeout_ns) {
+    const uint64_t t0 = globaltimer_ns();
+    volatile int32_t* flag = hdr + kHdrWaitFlag;
+    while (*flag == 0) {
+        if (globaltimer_ns() - t0 > timeout_ns) {
+            record_error(hdr, MOE_ERR_TIMEOUT);
+            return;
+        }
+        __nanosleep(1000);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_route(const Plan& p, const int32_t* topk_ids, int32_t* counts_out, int32_t* offsets_out,
+                         int32_t* row_src_out, cudaStream_t s) {
+    const int n_ids = p.T * p.K;
+    cudaError_t e = cudaMemsetAsync(p.claim, 0, sizeof(int32_t) * p.E, s);
+    if (e != cudaSuccess) return e;
+    if (n_ids > 0) {
+        const int blocks = (n_ids + kRouteChunk - 1) / kRouteChunk;
+        route_count_claim_kernel<<<blocks, kRouteThreads, 2 * p.E * sizeof(int32_t), s>>>(topk_ids, n_ids, p.E, p.claim,
+                                                                                          p.pos, p.hdr);
+    }
+    route_scan_kernel<<<1, 1024, 0, s>>>(p.E, p.claim, p.counts, p.offsets, p.pad_off, p.tile_off, p.pool_src, p.hdr,
+                                         counts_out, offsets_out);
+    if (n_ids > 0) {
+        route_scatter_kernel<<<(n_ids + 255) / 256, 256, 0, s>>>(topk_ids, n_ids, p.E, p.pos, p.offsets, p.pad_off,
+                                                                 p.row_src, p.pool_src, p.slot_row, row_src_out);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch(const Plan& p, const void* x, const void* x_scale, cudaStream_t s) {
+    if (p.T == 0) return cudaSuccess;
+    const int row_vecs = p.H * x_elem_bytes(p.mode) / 16;
+    const int scale_words = (int)(x_scale_row_bytes(p.mode, p.H) / 4);
+    const int grid = (int)std::min<int64_t>(p.pool_rows, 152 * 16);
+    dispatch_gather_kernel<<<grid, 128, 0, s>>>(static_cast<const uint4*>(x), static_cast<const uint32_t*>(x_scale),
+                                                p.pool_src, p.hdr, p.K, row_vecs, scale_words,
+                                                reinterpret_cast<uint4*>(p.x_pool),
+                                                reinterpret_cast<uint32_t*>(p.x_pool_scale));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const Plan& p, uint16_t* y, cudaStream_t s) {
+    const int row_vecs = p.H / 8;
+    const int64_t n = (int64_t)p.T * row_vecs;
+    if (n == 0) return cudaSuccess;
+    combine_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(reinterpret_cast<const uint4*>(p.comb), p.slot_row, p.T,
+                                                               p.K, row_vecs, reinterpret_cast<uint4*>(y));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_debug_wait(const Plan& p, uint64_t timeout_ns, cudaStream_t s) {
+    cudaError_t e = cudaMemsetAsync(p.hdr + kHdrWaitFlag, 0, sizeof(int32_t), s);
+    if (e != cudaSuccess) return e;
+    debug_wait_kernel<<<1, 1, 0, s>>>(p.hdr, timeout_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,69 @@
+"""Helpers of the GPU tests: run the library's stages through the C-ABI binding and read
+back the workspace regions, and compare against the oracle."""
+import numpy as np
+import torch
+
+TOL = {"a16w16": 2e-2, "a8w8_int8": 2e-2, "a8w8_fp8": 6e-2, "a8w4_fp8_fp4": 6e-2}
+
+
+def lib():
+    from moe_expert_ffn_topk_gb300 import build
+    build.build()
+    import moe_expert_ffn_topk_gb300 as moe
+    return moe
+
+
+def run_forward(moe, wl, inp, flags=0, stages=False):
+    """One forward pass; returns y (and, with stages=True, the plan and workspace views)."""
+    dev = inp["topk_ids"].device
+    d = moe.dims(wl.T, wl.H, wl.I, wl.E, wl.K)
+    ws = moe.alloc_workspace(d, wl.mode, dev)
+    y = torch.full((wl.T, wl.H), float("nan"), dtype=torch.bfloat16, device=dev)
+    if stages:
+        E = wl.E
+        counts = torch.full((E,), -7, dtype=torch.int32, device=dev)
+        offsets = torch.full((E + 1,), -7, dtype=torch.int32, device=dev)
+        row_src = torch.full((max(wl.T * wl.K, 1),), -7, dtype=torch.int32, device=dev)
+        moe.moe_plan(inp["topk_ids"], d, ws, counts, offsets, row_src)
+        moe.moe_dispatch(inp["x"], inp["x_scale"], d, wl.mode, ws)
+        moe.moe_expert_l1(inp["w1"], inp["w1_scale"], d, wl.mode, ws, flags)
+        moe.moe_expert_l2(inp["w2"], inp["w2_scale"], inp["topk_weights"], d, wl.mode, ws, flags)
+        moe.moe_combine(y, d, ws)
+    else:
+        moe.moe_forward(inp["x"], inp["x_scale"], inp["topk_ids"], inp["topk_weights"], inp["w1"], inp["w1_scale"],
+                        inp["w2"], inp["w2_scale"], y, d, wl.mode, ws, flags)
+    status = moe.moe_check_device_error(ws)
+    out = {"y": y, "status": status, "ws": ws, "d": d}
+    if stages:
+        L = moe.moe_workspace_layout(d, wl.mode)
+        out.update(counts=counts, offsets=offsets, row_src=row_src[:wl.T * wl.K], layout=L)
+    return out
+
+
+def region(ws, L, name, dtype, count):
+    off = L[name]
+    nbytes = count * torch.tensor([], dtype=dtype).element_size()
+    return ws[off:off + nbytes].view(dtype)
+
+
+def y_numpy(y):
+    return y.float().cpu().double().numpy()
+
+
+def assert_close(got, ref, mode, what="y"):
+    err = np.abs(got - ref).max() if got.size else 0.0
+    bound = TOL[mode] * (np.abs(ref).max() if ref.size else 0.0)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite values"
+    assert err <= bound, f"{what}: max|got - ref| = {err:.4e} > {bound:.4e} ({TOL[mode]} * max|ref|)"
+    return err, bound
+
+
+def slice_tokens(inp, tokens):
+    """The inputs of a subset of tokens (tokens are independent problems)."""
+    idx = torch.as_tensor(tokens, device=inp["topk_ids"].device, dtype=torch.long)
+    out = dict(inp)
+    for k in ("x", "topk_ids", "topk_weights"):
+        out[k] = inp[k].index_select(0, idx).contiguous()
+    if inp["x_scale"] is not None:
+        out["x_scale"] = inp["x_scale"].index_select(0, idx).contiguous()
+    return out

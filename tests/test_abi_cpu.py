@@ -1,0 +1,107 @@
+"""The C-ABI library loads on the CPU host, exports every symbol its header declares, and its
+host-side logic (limits, workspace layout, argument checks) behaves without a GPU."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import __graft_entry__
+    from moe_expert_ffn_topk_gb300 import build
+    build.build()
+    del __graft_entry__
+    import moe_expert_ffn_topk_gb300 as m
+    return m
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        names |= set(re.findall(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", src))
+    return names
+
+
+def test_exports_every_declared_symbol(moe):
+    declared = _declared_functions()
+    assert declared == set(moe.ABI_FUNCTIONS), declared ^ set(moe.ABI_FUNCTIONS)
+    lib = ctypes.CDLL(moe._binding._LIB_PATH)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(moe):
+    assert moe.moe_status_string(0) == "ok"
+    assert "timed out" in moe.moe_status_string(5)
+    assert moe.moe_status_string(99) == "unknown status"
+
+
+CONFIGS = [(64, 256, 128, 8, 2), (4096, 4096, 14336, 8, 2), (128, 7168, 2048, 256, 8),
+           (8192, 7168, 2048, 256, 8), (2048, 5120, 1536, 64, 6), (0, 256, 128, 8, 2)]
+
+
+@pytest.mark.parametrize("cfg", CONFIGS)
+@pytest.mark.parametrize("mode", ["a16w16", "a8w8_fp8", "a8w8_int8", "a8w4_fp8_fp4"])
+def test_workspace_layout(moe, cfg, mode):
+    T, H, I, E, K = cfg
+    d = moe.dims(*cfg)
+    L = moe.moe_workspace_layout(d, mode)
+    assert L["total"] == moe.moe_workspace_bytes(d, mode) > 0
+    R = T * K
+    assert L["pool_rows"] == R + min(E, R) * 127
+    regions = {
+        "header": 64, "counts": 4 * E, "offsets": 4 * (E + 1), "pad_offsets": 4 * (E + 1),
+        "tile_offsets": 4 * (E + 1), "row_src": 4 * R, "pool_src": 4 * L["pool_rows"], "slot_row": 4 * R,
+        "comb": 2 * R * H, "x_pool": L["pool_rows"] * H * (2 if mode == "a16w16" else 1),
+        "a_pool": L["pool_rows"] * I * (2 if mode == "a16w16" else 1),
+    }
+    spans = sorted((L[k], L[k] + n) for k, n in regions.items() if n)
+    for (a0, a1), (b0, b1) in zip(spans, spans[1:]):
+        assert a1 <= b0
+    assert spans[-1][1] <= L["total"]
+    for k in regions:
+        assert L[k] % 256 == 0
+
+
+@pytest.mark.parametrize("bad", [(1, 100, 128, 8, 2), (1, 256, 96, 8, 2), (1, 256, 128, 8, 0),
+                                 (1, 256, 128, 8, 33), (1, 256, 128, 2000, 2), (1, 256, 128, 2, 4),
+                                 (-1, 256, 128, 8, 2)])
+def test_limits(moe, bad):
+    assert moe.moe_workspace_bytes(moe.dims(*bad), "a16w16") == 0
+
+
+def test_host_checks_return_before_launch(moe):
+    lib = moe._binding.LIB
+    d = moe.dims(64, 256, 128, 8, 2)
+    # no workspace
+    assert lib.moe_plan(ctypes.c_void_p(16), ctypes.byref(d), None, None, None, None, 0, None) == 6
+    # misaligned workspace
+    assert lib.moe_plan(ctypes.c_void_p(16), ctypes.byref(d), None, None, None, ctypes.c_void_p(4096 + 8),
+                        1 << 30, None) == 6
+    # workspace too small
+    assert lib.moe_plan(ctypes.c_void_p(16), ctypes.byref(d), None, None, None, ctypes.c_void_p(4096), 16,
+                        None) == 6
+    # bad dims
+    bad = moe.dims(64, 100, 128, 8, 2)
+    assert lib.moe_plan(ctypes.c_void_p(16), ctypes.byref(bad), None, None, None, ctypes.c_void_p(4096),
+                        1 << 30, None) == 1
+    # missing operands
+    op = moe._binding.MoeOperand(None, None)
+    assert lib.moe_expert_l1(op, ctypes.byref(d), 0, 0, ctypes.c_void_p(4096), 1 << 30, None) == 1
+    w = moe._binding.MoeOperand(ctypes.c_void_p(4096), None)
+    assert lib.moe_expert_l1(w, ctypes.byref(d), 3, 0, ctypes.c_void_p(4096), 1 << 30, None) == 1  # scale needed
+    assert lib.moe_forward(op, None, None, w, w, None, ctypes.byref(d), 9, 0, ctypes.c_void_p(4096), 1 << 30,
+                           None) == 1  # unknown mode
+
+
+def test_binding_rejects_host_tensors(moe):
+    import torch
+    d = moe.dims(64, 256, 128, 8, 2)
+    with pytest.raises(ValueError):
+        moe.moe_plan(torch.zeros((64, 2), dtype=torch.int32), d, torch.zeros(1 << 20, dtype=torch.uint8))

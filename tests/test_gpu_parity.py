@@ -1,0 +1,220 @@
+"""GPU parity of every stage of the path against the CPU oracle, through the C ABI.
+
+Bars: counts, offsets and the per-expert multiset of row identities bit-exact; floating
+point within max|y - y_ref| <= tol * max|y_ref| (2e-2 bf16 and INT8, 6e-2 for the FP8/FP4
+modes); INT8 L2 accumulators bit-exact given the kernel's own re-quantised operand.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import TOL, assert_close, lib, region, run_forward, slice_tokens, y_numpy
+from oracle import moe as omoe
+from workloads import WORKLOADS, Workload, make_inputs, to_numpy
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def moe():
+    return lib()
+
+
+def oracle_forward(wl, inp, **kw):
+    h = to_numpy(inp)
+    return omoe.forward(wl.mode, h["x"], h["x_scale"], h["topk_ids"], h["topk_weights"], h["w1"], h["w1_scale"],
+                        h["w2"], h["w2_scale"], num_experts=wl.E, inter=wl.I, **kw)
+
+
+# Small cases that still span several 128-row tiles, several column tiles and ragged tails.
+CASES = {
+    "a16w16": [WORKLOADS["tiny_bf16"], Workload("ragged_bf16", "a16w16", 300, 512, 384, 6, 2, 21, 0.05)],
+    "a8w8_fp8": [Workload("tiny_fp8", "a8w8_fp8", 64, 256, 128, 8, 2, 22, 0.02),
+                 Workload("ragged_fp8", "a8w8_fp8", 300, 512, 384, 6, 2, 23, 0.05)],
+    "a8w8_int8": [Workload("tiny_int8", "a8w8_int8", 64, 256, 128, 8, 2, 24, 0.02),
+                  Workload("ragged_int8", "a8w8_int8", 300, 512, 384, 6, 3, 25, 0.05)],
+    "a8w4_fp8_fp4": [Workload("tiny_fp4", "a8w4_fp8_fp4", 64, 256, 128, 8, 2, 26, 0.02),
+                     Workload("ragged_fp4", "a8w4_fp8_fp4", 300, 512, 384, 6, 2, 27, 0.05),
+                     Workload("skew_fp4", "a8w4_fp8_fp4", 257, 256, 256, 64, 8, 28, 0.05, zipf_s=1.2, zipf_empty=8)],
+}
+ALL = [(m, wl) for m, wls in CASES.items() for wl in wls]
+
+
+def check_plan(out, wl, ids):
+    ids_np = ids.cpu().numpy()
+    counts, offsets, row_src = omoe.plan(ids_np, wl.E)
+    assert out["counts"].cpu().numpy().tolist() == counts.tolist()
+    assert out["offsets"].cpu().numpy().tolist() == offsets.tolist()
+    got = out["row_src"].cpu().numpy()[:offsets[-1]]
+    for e in range(wl.E):
+        lo, hi = offsets[e], offsets[e + 1]
+        assert sorted(got[lo:hi].tolist()) == sorted(row_src[lo:hi].tolist()), f"expert {e}"
+
+
+@pytest.mark.parametrize("mode,wl", ALL, ids=[f"{m}-{w.name}" for m, w in ALL])
+@pytest.mark.parametrize("flags", [0, 1], ids=["default", "simt"])
+def test_forward_matches_oracle(moe, mode, wl, flags):
+    inp = make_inputs(wl, device=DEV)
+    out = run_forward(moe, wl, inp, flags=flags, stages=True)
+    assert out["status"] == 0
+    check_plan(out, wl, inp["topk_ids"])
+    ref, rec = oracle_forward(wl, inp, return_intermediates=True)
+    # weighted combine rows (stage S5) and the output (stage S6)
+    L = out["layout"]
+    comb = region(out["ws"], L, "comb", torch.bfloat16, wl.T * wl.K * wl.H).view(wl.T * wl.K, wl.H)
+    assert_close(y_numpy(comb), rec["comb"], mode, "combine rows")
+    assert_close(y_numpy(out["y"]), ref, mode)
+
+
+@pytest.mark.parametrize("mode,wl", ALL[:1] + ALL[2:3], ids=["bf16", "fp8"])
+def test_deterministic(moe, mode, wl):
+    inp = make_inputs(wl, device=DEV)
+    y1 = run_forward(moe, wl, inp)["y"]
+    y2 = run_forward(moe, wl, inp)["y"]
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+
+
+def test_dispatch_gathers_rows(moe):
+    wl = CASES["a8w4_fp8_fp4"][1]
+    inp = make_inputs(wl, device=DEV)
+    out = run_forward(moe, wl, inp, stages=True)
+    L = out["layout"]
+    rows = L["pool_rows"]
+    pool_src = region(out["ws"], L, "pool_src", torch.int32, rows).cpu().numpy()
+    xp = region(out["ws"], L, "x_pool", torch.uint8, rows * wl.H).view(rows, wl.H).cpu().numpy()
+    xs = region(out["ws"], L, "x_pool_scale", torch.float32, rows * wl.H // 128).view(rows, -1).cpu().numpy()
+    x = inp["x"].cpu().numpy()
+    xsc = inp["x_scale"].cpu().numpy()
+    hdr = region(out["ws"], L, "header", torch.int32, 16).cpu().numpy()
+    n_pad = hdr[2]
+    assert n_pad % 128 == 0 and n_pad >= wl.T * wl.K
+    for r in range(n_pad):
+        s = pool_src[r]
+        if s >= 0:
+            assert np.array_equal(xp[r], x[s // wl.K]) and np.array_equal(xs[r], xsc[s // wl.K])
+        else:
+            assert not xp[r].any()
+
+
+def test_int8_l2_accumulators_exact(moe):
+    """D = A^int8 . W2 must be the exact integer product: recompute the weighted rows from the
+    kernel's own A^int8 and s^A with the oracle's integer GEMM and the page's fp32 dequant
+    order, and require bit equality."""
+    wl = CASES["a8w8_int8"][1]
+    inp = make_inputs(wl, device=DEV)
+    out = run_forward(moe, wl, inp, stages=True)
+    L = out["layout"]
+    rows = L["pool_rows"]
+    ws = out["ws"]
+    pool_src = region(ws, L, "pool_src", torch.int32, rows).cpu().numpy()
+    pad_off = region(ws, L, "pad_offsets", torch.int32, wl.E + 1).cpu().numpy()
+    a_q = region(ws, L, "a_pool", torch.int8, rows * wl.I).view(rows, wl.I).cpu().numpy()
+    s_a = region(ws, L, "a_pool_scale", torch.float32, rows).cpu().numpy()
+    comb = region(ws, L, "comb", torch.int16, wl.T * wl.K * wl.H).view(wl.T * wl.K, wl.H).cpu().numpy()
+    h = to_numpy(inp)
+    g = h["topk_weights"].reshape(-1)
+    assert np.abs(a_q.astype(np.int32)).max() <= 127
+    for e in range(wl.E):
+        lo, hi = pad_off[e], pad_off[e + 1]
+        src = pool_src[lo:hi]
+        keep = src >= 0
+        if not keep.any():
+            continue
+        w2 = h["w2"][e].astype(np.int64).T  # [I, H]
+        d = a_q[lo:hi][keep].astype(np.int64) @ w2
+        y32 = (d.astype(np.float32) * h["w2_scale"][e][None, :]).astype(np.float32)
+        y32 = (y32 * s_a[lo:hi][keep][:, None]).astype(np.float32)
+        c = (g[src[keep]][:, None].astype(np.float32) * y32).astype(np.float32)
+        ref_bits = torch.from_numpy(c).to(torch.bfloat16).view(torch.int16).numpy()
+        assert np.array_equal(comb[src[keep]], ref_bits), f"expert {e}"
+
+
+EDGE = [
+    Workload("one_token", "a16w16", 1, 256, 128, 8, 2, 31, 0.05),
+    Workload("one_expert", "a16w16", 70, 256, 128, 1, 1, 32, 0.05),
+    Workload("topk1", "a8w4_fp8_fp4", 40, 256, 128, 16, 1, 33, 0.05),
+    Workload("many_empty", "a8w8_fp8", 20, 256, 128, 256, 2, 34, 0.05),
+    Workload("max_topk", "a16w16", 9, 128, 128, 40, 32, 35, 0.05),
+]
+
+
+@pytest.mark.parametrize("wl", EDGE, ids=[w.name for w in EDGE])
+def test_edge_shapes(moe, wl):
+    inp = make_inputs(wl, device=DEV)
+    out = run_forward(moe, wl, inp, stages=True)
+    assert out["status"] == 0
+    check_plan(out, wl, inp["topk_ids"])
+    assert_close(y_numpy(out["y"]), oracle_forward(wl, inp), wl.mode)
+
+
+def test_all_rows_to_one_expert_and_masked_routes(moe):
+    wl = Workload("skewed", "a16w16", 200, 256, 128, 4, 2, 36, 0.05)
+    inp = make_inputs(wl, device=DEV)
+    ids = inp["topk_ids"].clone()
+    ids[:, 0] = 2                     # every token's first slot goes to expert 2 (N_e = 200)
+    ids[:, 1] = torch.where(ids[:, 1] == 2, torch.full_like(ids[:, 1], 3), ids[:, 1])
+    ids[::3, 1] = -1                  # masked routes
+    inp["topk_ids"] = ids.contiguous()
+    out = run_forward(moe, wl, inp, stages=True)
+    assert out["status"] == 0
+    check_plan(out, wl, inp["topk_ids"])
+    assert_close(y_numpy(out["y"]), oracle_forward(wl, inp), wl.mode)
+
+
+def test_bad_route_is_reported_and_skipped(moe):
+    wl = Workload("bad", "a16w16", 16, 256, 128, 4, 2, 37, 0.05)
+    inp = make_inputs(wl, device=DEV)
+    ids = inp["topk_ids"].clone()
+    ids[3, 1] = 99
+    inp["topk_ids"] = ids
+    out = run_forward(moe, wl, inp)
+    assert out["status"] == 4  # MOE_ERR_BAD_ROUTE
+    ids_m = ids.clone()
+    ids_m[3, 1] = -1              # the bad route is skipped like a masked one
+    ref = oracle_forward(wl, dict(inp, topk_ids=ids_m))
+    assert_close(y_numpy(out["y"]), ref, wl.mode)
+
+
+def test_zero_tokens(moe):
+    wl = Workload("empty", "a16w16", 0, 256, 128, 8, 2, 38, 0.05)
+    inp = make_inputs(wl, device=DEV)
+    out = run_forward(moe, wl, inp, stages=True)
+    assert out["status"] == 0
+    assert out["counts"].cpu().numpy().tolist() == [0] * 8
+    assert out["offsets"].cpu().numpy().tolist() == [0] * 9
+
+
+def test_bounded_wait_times_out_and_device_stays_usable(moe):
+    ws = torch.zeros(1 << 16, dtype=torch.uint8, device=DEV)
+    moe.moe_debug_bounded_wait(ws, 20_000_000)  # 20 ms on a flag that nothing sets
+    assert moe.moe_check_device_error(ws) == 5  # MOE_ERR_TIMEOUT
+    assert moe.moe_check_device_error(ws) == 0  # cleared
+    wl = WORKLOADS["tiny_bf16"]
+    inp = make_inputs(wl, device=DEV)
+    out = run_forward(moe, wl, inp)
+    assert out["status"] == 0
+    assert_close(y_numpy(out["y"]), oracle_forward(wl, inp), wl.mode)
+
+
+FULL = ["mixtral_bf16_prefill", "dsv3_fp8fp4_decode", "dsv3_fp8fp4_prefill_zipf", "int8_a8w8"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled(moe, name):
+    """Full-size workload in the benchmark's launch configuration; the oracle checks a seeded
+    sample of tokens (every token is an independent problem) and the plan in full."""
+    wl = WORKLOADS[name]
+    inp = make_inputs(wl, device=DEV)
+    out = run_forward(moe, wl, inp, stages=True)
+    assert out["status"] == 0
+    check_plan(out, wl, inp["topk_ids"])
+    rng = np.random.default_rng(wl.seed)
+    tokens = sorted(rng.choice(wl.T, size=min(wl.T, 6), replace=False).tolist())
+    sub = slice_tokens(inp, tokens)
+    ref = oracle_forward(wl, sub)
+    got = y_numpy(out["y"])[tokens]
+    assert_close(got, ref, wl.mode)
+    # every row of the output is written and finite
+    assert torch.isfinite(out["y"].float()).all()
