@@ -7,8 +7,8 @@ TOL = {"a16w16": 2e-2, "a8w8_int8": 2e-2, "a8w8_fp8": 6e-2, "a8w4_fp8_fp4": 6e-2
 
 
 def lib():
-    from moe_expert_ffn_topk_gb300 import build
-    build.build()
+    import __graft_entry__
+    __graft_entry__.build_module().build()
     import moe_expert_ffn_topk_gb300 as moe
     return moe
 

@@ -13,9 +13,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 @pytest.fixture(scope="module")
 def moe():
     import __graft_entry__
-    from moe_expert_ffn_topk_gb300 import build
-    build.build()
-    del __graft_entry__
+    __graft_entry__.build_module().build()
     import moe_expert_ffn_topk_gb300 as m
     return m
 
