@@ -222,7 +222,9 @@ __global__ void debug_wait_kernel(int32_t* hdr, uint64_t timeout_ns) {
 cudaError_t launch_route(const Plan& p, const int32_t* topk_ids, int32_t* counts_out, int32_t* offsets_out,
                          int32_t* row_src_out, cudaStream_t s) {
     const int n_ids = p.T * p.K;
-    cudaError_t e = cudaMemsetAsync(p.claim, 0, sizeof(int32_t) * p.E, s);
+    // the header (error word, totals) and the per-expert claim counters are contiguous
+    const size_t clear = reinterpret_cast<const uint8_t*>(p.claim + p.E) - reinterpret_cast<const uint8_t*>(p.hdr);
+    cudaError_t e = cudaMemsetAsync(p.hdr, 0, clear, s);
     if (e != cudaSuccess) return e;
     if (n_ids > 0) {
         const int blocks = (n_ids + kRouteChunk - 1) / kRouteChunk;
@@ -260,7 +262,7 @@ cudaError_t launch_combine(const Plan& p, uint16_t* y, cudaStream_t s) {
 }
 
 cudaError_t launch_debug_wait(const Plan& p, uint64_t timeout_ns, cudaStream_t s) {
-    cudaError_t e = cudaMemsetAsync(p.hdr + kHdrWaitFlag, 0, sizeof(int32_t), s);
+    cudaError_t e = cudaMemsetAsync(p.hdr, 0, sizeof(int32_t) * kHeaderInts, s);
     if (e != cudaSuccess) return e;
     debug_wait_kernel<<<1, 1, 0, s>>>(p.hdr, timeout_ns);
     return cudaGetLastError();

@@ -1,15 +1,482 @@
-// Tensor-core (tcgen05) grouped GEMM kernels. Placeholder until the kernels land: every
-// mode reports "no tensor-core kernel" and the stages run the CUDA-core reference kernels.
+// Tensor-core grouped GEMM stages for bf16 operands on sm_103a: tcgen05.mma with fp32
+// accumulators in tensor memory, operands staged in shared memory by TMA, a 4-stage mbarrier
+// ring between the loader and the MMA issuer, and two TMEM accumulators so the epilogue of
+// one tile overlaps the main loop of the next.
+//
+// Work decomposition (one persistent CTA per SM, static round-robin over tiles):
+//   tile = (expert e, 128-row block m of e's padded pool rows, column block n)
+//   tiles are ordered expert-major, then n, then m, so the CTAs in flight share a few
+//   weight column blocks of one expert in L2 while the expert's rows stay resident.
+//
+// L1 (Ascend mega_moe page, "Linear1 Projection" + "SwiGLU Activation"): the B tile of a stage
+// is the gate column block [n*128, n*128+128) and the up column block [I+n*128, ...) of
+// W1[e] (two TMA boxes each), so one 128x256 accumulator holds the gate and up values of the
+// same 128 outputs and SwiGLU runs in the epilogue: A = SiLU(gate) * up -> bf16.
+// L2 ("Linear2 Projection" + the gate weight of "Token Combine"): 128x256 accumulator over
+// H columns; the epilogue multiplies row p by G[row_src[p]] in fp32 and stores bf16 to the
+// combine row of (token, slot).
+//
+// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer,
+// warps 2-5 = epilogue (warp w reads TMEM lanes 32*(w%4) .. 32*(w%4)+31).
+// Every mbarrier wait is bounded (2 s); on time-out the CTA records MOE_ERR_TIMEOUT, drains
+// what it has in flight (again bounded), frees its tensor memory and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "common.cuh"
 #include "internal.h"
 
 namespace moe {
 
-bool tc_supported(const Plan&, int) { return false; }
+namespace {
 
-cudaError_t launch_l1_tc(const Plan&, const void*, const void*, cudaStream_t) { return cudaErrorNotSupported; }
+constexpr int kBM = 128;                       // rows per tile (MMA M)
+constexpr int kBN = 256;                       // accumulator columns per tile (MMA N)
+constexpr int kBK = 64;                        // K per stage: 64 bf16 = one 128-byte swizzle row
+constexpr int kStages = 4;
+constexpr int kABytes = kBM * kBK * 2;         // 16 KB
+constexpr int kBBoxBytes = kBK * 64 * 2;       // one 64(K) x 64(N) box, 8 KB
+constexpr int kBBytes = 4 * kBBoxBytes;        // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes; // 48 KB
+constexpr int kThreads = 192;
+constexpr int kTmemCols = 512;                 // two 256-column fp32 accumulators
+constexpr int kMaxExperts = 1024;
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 
-cudaError_t launch_l2_tc(const Plan&, const void*, const void*, const float*, cudaStream_t) {
-    return cudaErrorNotSupported;
+// Instruction descriptor of tcgen05.mma.kind::f16: D fp32 (bits 4-5 = 1), A bf16 (bits 7-9 =
+// 1), B bf16 (bits 10-12 = 1), A K-major (bit 15 = 0), B MN-major (bit 16 = 1), N >> 3 in
+// bits 17-22, M >> 4 in bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (1u << 16) |
+                            ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+
+struct TcArgs {
+    Plan p;
+    const float* topk_weights;  // L2 only
+    int n_tiles;                // column blocks per expert
+    int k_blocks;               // K / 64
+    int k_rows;                 // rows of one expert's weight in its 2-D view (L1: H, L2: I)
+};
+
+// ---------------------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Bounded wait for the phase of `bar` with the given parity to complete. Returns false when
+// the CTA gave up (this thread timed out, or another role already aborted).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* hdr, volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+            record_error(hdr, MOE_ERR_TIMEOUT);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: start >> 4 (bits 0-13), leading byte offset >> 4 (16-29),
+// stride byte offset >> 4 (32-45), descriptor version 1 (46-47), base offset 0, swizzle
+// mode in bits 61-63 (2 = 128-byte swizzle).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// A tile: 128 rows x 64 K, K-major, 128-byte swizzle (the TMA box layout). 8-row groups are
+// 1024 bytes apart; the K extent of one MMA (16 elements, 32 bytes) stays inside a swizzle
+// row, so the leading byte offset is unused.
+__device__ __forceinline__ uint64_t a_desc(uint32_t tile, int kk) { return smem_desc(tile + kk * 32, 16, 1024); }
+
+// B tile: four 64(K) x 64(N) boxes, N contiguous (MN-major), 128-byte swizzle. The 64-column
+// groups are one box (8 KB) apart (leading byte offset); groups of 8 K rows are 1024 bytes
+// apart (stride byte offset). One MMA consumes 16 K rows = 2048 bytes of every box.
+__device__ __forceinline__ uint64_t b_desc(uint32_t tile, int kk) {
+    return smem_desc(tile + kk * 2048, kBBoxBytes, 1024);
+}
+
+struct Tile {
+    int e, m, n, row0;
+};
+
+// Tiles are ordered expert-major: expert e owns tiles [tile_off[e] * n_tiles, tile_off[e+1] * n_tiles).
+__device__ __forceinline__ Tile decode_tile(int t, const int* tile_off, int E, int n_tiles) {
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (tile_off[mid] * n_tiles <= t) lo = mid; else hi = mid - 1;
+    }
+    Tile tl;
+    tl.e = lo;
+    const int mt = tile_off[lo + 1] - tile_off[lo];
+    const int local = t - tile_off[lo] * n_tiles;
+    tl.n = local / mt;
+    tl.m = local % mt;
+    tl.row0 = (tile_off[lo] + tl.m) * kBM;
+    return tl;
+}
+
+template <bool kL1>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, TcArgs args) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* smem = smem_raw + (base - raw);
+    const uint32_t bar0 = base + kStages * kStageBytes;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kStages + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kStages + 2 + a); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
+    uint8_t* misc = smem + kStages * kStageBytes + 8 * (2 * kStages + 5);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(misc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
+    int* tile_off = reinterpret_cast<int*>(misc + 16);
+
+    const Plan& p = args.p;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i <= p.E; i += kThreads) tile_off[i] = p.tile_off[i];
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), 4);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (warp == 0 && lane == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    const int total = tile_off[p.E] * args.n_tiles;
+    const int KB = args.k_blocks;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer ----------------
+            int it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                const Tile tl = decode_tile(t, tile_off, p.E, args.n_tiles);
+                const int wrow = tl.e * args.k_rows;
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const int s = it % kStages;
+                    const uint32_t ph = (uint32_t)(it / kStages) & 1u;
+                    if (!mbar_wait(empty_bar(s), ph ^ 1u, p.hdr, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = base + s * kStageBytes, sb = sa + kABytes;
+                    mbar_arrive_expect_tx(full_bar(s), kStageBytes);
+                    tma_load_2d(sa, &tmA, kb * kBK, tl.row0, full_bar(s));
+                    const int y = wrow + kb * kBK;
+                    if (kL1) {
+                        const int g0 = tl.n * 128, u0 = p.I + tl.n * 128;
+                        tma_load_2d(sb, &tmB, g0, y, full_bar(s));
+                        tma_load_2d(sb + kBBoxBytes, &tmB, g0 + 64, y, full_bar(s));
+                        tma_load_2d(sb + 2 * kBBoxBytes, &tmB, u0, y, full_bar(s));
+                        tma_load_2d(sb + 3 * kBBoxBytes, &tmB, u0 + 64, y, full_bar(s));
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) tma_load_2d(sb + j * kBBoxBytes, &tmB, tl.n * kBN + j * 64, y, full_bar(s));
+                    }
+                }
+            }
+            // drain: wait until every load issued into a stage has landed (bounded)
+            for (int j = it - kStages < 0 ? 0 : it - kStages; j < it; ++j) {
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(full_bar(j % kStages), (uint32_t)(j / kStages) & 1u)) {
+                    if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+                        record_error(p.hdr, MOE_ERR_TIMEOUT);
+                        break;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer ----------------
+            int it = 0, tc = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tc) {
+                const int a = tc & 1;
+                if (!mbar_wait(tempty_bar(a), ((uint32_t)(tc >> 1) & 1u) ^ 1u, p.hdr, abort_flag)) break;
+                tc_fence_after();
+                const uint32_t d = tmem_base + (uint32_t)(a * kBN);
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const int s = it % kStages;
+                    if (!mbar_wait(full_bar(s), (uint32_t)(it / kStages) & 1u, p.hdr, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = base + s * kStageBytes, sb = sa + kABytes;
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        tc_mma(d, a_desc(sa, kk), b_desc(sb, kk), kIdesc, (kb | kk) != 0);
+                    tc_commit(empty_bar(s));  // frees the stage once these MMAs have read it
+                }
+                if (ok) tc_commit(tfull_bar(a));
+            }
+            // drain: every MMA issued so far has completed before tensor memory is freed
+            tc_commit(drain_bar);
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(drain_bar, 0)) {
+                if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+                    record_error(p.hdr, MOE_ERR_TIMEOUT);
+                    break;
+                }
+            }
+        }
+    } else {
+        // ---------------- epilogue (warps 2..5) ----------------
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        int tc = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x, ++tc) {
+            const int a = tc & 1;
+            // every lane waits; the warp goes on only if all of them saw the phase complete
+            const bool ok = mbar_wait(tfull_bar(a), (uint32_t)(tc >> 1) & 1u, p.hdr, abort_flag);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc_fence_after();
+            const Tile tl = decode_tile(t, tile_off, p.E, args.n_tiles);
+            const int64_t row = tl.row0 + q * 32 + lane;
+            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * kBN);
+            if (kL1) {
+                uint16_t* out = reinterpret_cast<uint16_t*>(p.a_pool) + row * p.I + tl.n * 128;
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t g[32], u[32];
+                    tmem_ld32(tbase + c * 32, g);
+                    tmem_ld32(tbase + 128 + c * 32, u);
+                    tmem_ld_wait();
+                    uint32_t packed[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float a0 = silu(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]);
+                        const float a1 = silu(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]);
+                        packed[j] = (uint32_t)float_to_bf16_bits(a0) | ((uint32_t)float_to_bf16_bits(a1) << 16);
+                    }
+                    uint4* dst = reinterpret_cast<uint4*>(out + c * 32);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+                }
+            } else {
+                const int src = p.pool_src[row];
+                const float gw = src >= 0 ? args.topk_weights[src] : 0.0f;
+                uint16_t* out = p.comb + (int64_t)(src >= 0 ? src : 0) * p.H + tl.n * kBN;
+#pragma unroll 1
+                for (int c = 0; c < kBN / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(tbase + c * 32, r);
+                    tmem_ld_wait();
+                    if (src >= 0) {
+                        uint32_t packed[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const float y0 = __fmul_rn(gw, __uint_as_float(r[2 * j]));
+                            const float y1 = __fmul_rn(gw, __uint_as_float(r[2 * j + 1]));
+                            packed[j] = (uint32_t)float_to_bf16_bits(y0) | ((uint32_t)float_to_bf16_bits(y1) << 16);
+                        }
+                        uint4* dst = reinterpret_cast<uint4*>(out + c * 32);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(a));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// 2-D bf16 tensor [outer, inner] (row-major), boxes of box_outer x 64 elements, 128-byte swizzle.
+bool make_map(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {64, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms() {
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0) n = 148;
+    }
+    return n;
+}
+
+constexpr size_t smem_bytes() {
+    return 1024 + (size_t)kStages * kStageBytes + 8 * (2 * kStages + 5) + 16 + 4 * (kMaxExperts + 1);
+}
+
+template <bool kL1>
+cudaError_t launch_tc(const Plan& p, const CUtensorMap& a, const CUtensorMap& b, TcArgs args, cudaStream_t s) {
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(tc_gemm_kernel<kL1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)smem_bytes());
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    const int64_t max_tiles = (p.pool_rows / kBM) * args.n_tiles;
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(max_tiles, num_sms()));
+    tc_gemm_kernel<kL1><<<grid, kThreads, smem_bytes(), s>>>(a, b, args);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_supported(const Plan& p, int stage) {
+    if (p.mode != MOE_A16W16 || p.E > kMaxExperts || encode_fn() == nullptr) return false;
+    if (stage == 1) return p.I % 128 == 0;
+    return p.H % kBN == 0;
+}
+
+cudaError_t launch_l1_tc(const Plan& p, const void* w1, const void*, cudaStream_t s) {
+    CUtensorMap a, b;
+    if (!make_map(&a, p.x_pool, (uint64_t)p.H, (uint64_t)p.pool_rows, kBM)) return cudaErrorInvalidValue;
+    if (!make_map(&b, w1, (uint64_t)2 * p.I, (uint64_t)p.E * p.H, kBK)) return cudaErrorInvalidValue;
+    TcArgs args{p, nullptr, p.I / 128, p.H / kBK, p.H};
+    return launch_tc<true>(p, a, b, args, s);
+}
+
+cudaError_t launch_l2_tc(const Plan& p, const void* w2, const void*, const float* topk_weights, cudaStream_t s) {
+    CUtensorMap a, b;
+    if (!make_map(&a, p.a_pool, (uint64_t)p.I, (uint64_t)p.pool_rows, kBM)) return cudaErrorInvalidValue;
+    if (!make_map(&b, w2, (uint64_t)p.H, (uint64_t)p.E * p.I, kBK)) return cudaErrorInvalidValue;
+    TcArgs args{p, topk_weights, p.H / kBN, p.I / kBK, p.I};
+    return launch_tc<false>(p, a, b, args, s);
 }
 
 }  // namespace moe
