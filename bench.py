@@ -37,12 +37,14 @@ LAUNCHES_PER_STEP = {"a16w16": 7, "a8w8_fp8": 7, "a8w8_int8": 8, "a8w4_fp8_fp4":
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="mixtral_bf16_prefill")
     ap.add_argument("--flags", type=int, default=0, help="GEMM stage flags (1 = CUDA-core reference kernels)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=None, help="override the workload's token count")
+    ap.add_argument("--experts", type=int, default=None, help="override the workload's expert count")
     return ap.parse_args()
 
 
@@ -138,22 +140,32 @@ def run_reference(args, wl, rank, world):
 # clocks during the timed region
 # ---------------------------------------------------------------------------------------
 
-CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+CLOCK_FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
 
 class ClockSampler:
+    """nvidia-smi samples every 50 ms while the context is open; summary() keeps the samples
+    taken between mark_start() and mark_end() (the timed region)."""
+
     def __init__(self, gpu_index):
         self.proc = None
         self.gpu_index = gpu_index
         self.out = os.path.join("/tmp", f"moe_clocks_{os.getpid()}.csv")
+        self.t_start = self.t_end = None
+
+    def mark_start(self):
+        self.t_start = time.time()
+
+    def mark_end(self):
+        self.t_end = time.time()
 
     def __enter__(self):
         try:
             self.f = open(self.out, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={CLOCK_FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                                          "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.f,
                                          stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except Exception:
@@ -170,20 +182,30 @@ class ClockSampler:
             self.f.close()
 
     def summary(self):
+        import datetime
         if self.proc is None or not os.path.exists(self.out):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         rows = []
         for line in open(self.out):
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
-                rows.append(parts)
+            if len(parts) >= 10 and parts[2].replace(".", "").isdigit():
+                try:
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                except ValueError:
+                    ts = None
+                rows.append((ts, parts[1:]))
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        sm = [float(r[1]) for r in rows]
+        inside = [r for ts, r in rows if ts is not None and self.t_start is not None and
+                  self.t_start <= ts <= self.t_end]
+        use = inside or [r for _, r in rows]
+        sm = [float(r[1]) for r in use]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]), "reasons": reasons,
-                "samples": len(rows), "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())}
+        reasons = sorted({names[i] for r in use for i in range(4) if r[5 + i].lower() == "active"})
+        power = [float(r[3]) for r in use if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(use[0][2]), "reasons": reasons,
+                "samples_in_timed_region": len(inside), "samples": len(use),
+                "power_w_median": statistics.median(power) if power else None}
 
 
 # ---------------------------------------------------------------------------------------
@@ -256,11 +278,13 @@ def run_gb300(args, wl, rank, world, local_rank):
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local_rank) as clocks:
         barrier()
+        clocks.mark_start()
         t0.record(stream)
         for i in range(args.steps):
             step(l1_events[i])
         t1.record(stream)
         barrier()
+        clocks.mark_end()
     elapsed_ms = t0.elapsed_time(t1)
     l1_ms = statistics.mean(a.elapsed_time(b) for a, b in l1_events)
     st = moe.moe_check_device_error(ws)
@@ -310,7 +334,10 @@ def run_gb300(args, wl, rank, world, local_rank):
     pk, pk_src = peaks()
     l1_flops = 4.0 * wl.H * wl.I * wl.routed_rows
     achieved = l1_flops / (l1_ms * 1e-3) / 1e12
-    peak = float(pk.get("bf16_tflops_sustained", pk.get("bf16_tflops")))
+    # a timed region of a second or more runs at the power-capped clock: sustained peak;
+    # a shorter one runs at burst clocks: burst peak
+    sustained = elapsed_ms >= 1000.0
+    peak = float(pk["bf16_tflops_sustained"] if sustained else pk["bf16_tflops"])
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -319,7 +346,8 @@ def run_gb300(args, wl, rank, world, local_rank):
         "routed_rows_per_s": world * wl.routed_rows * args.steps / (elapsed_ms * 1e-3),
         "roofline": {"bound": "tensor", "kernel": "L1 grouped GEMM + SwiGLU (moe_expert_l1)",
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                     "peak_source": f"{pk_src} bf16 dense, sustained", "l1_ms": l1_ms,
+                     "peak_source": f"{pk_src} bf16 dense, {'sustained' if sustained else 'burst'}",
+                     "l1_ms": l1_ms,
                      "traffic": dominant_kernel_traffic(wl.name)},
         "e2e": {"value": world * flops * args.steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps},
@@ -331,8 +359,11 @@ def run_gb300(args, wl, rank, world, local_rank):
 
 def main():
     args = parse()
-    from workloads import WORKLOADS
+    from workloads import WORKLOADS, scaled
     wl = WORKLOADS[args.workload]
+    if args.tokens is not None or args.experts is not None:
+        wl = scaled(wl, name=f"{wl.name}[T={args.tokens or wl.T},E={args.experts or wl.E}]",
+                    T=args.tokens or wl.T, E=args.experts or wl.E)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
@@ -350,7 +381,9 @@ def main():
     if line is not None and not args.no_cpu_baseline:
         from workloads import to_numpy
         h = to_numpy(inp)
-        n_tok = cpu_tokens_per_sample(wl)
+        # size the sample for about 10 s of oracle time from a 2-token probe
+        dt0, _ = oracle_sample(wl, h, min(2, wl.T), seed=6)
+        n_tok = int(max(2, min(wl.T, 64, round(2 * 10.0 / max(dt0, 1e-3)))))
         dt, rows = oracle_sample(wl, h, n_tok, seed=7)
         line["cpu_baseline"] = {"value": 6.0 * wl.H * wl.I * rows / dt / 1e12, "unit": "TFLOP/s",
                                 "cores": oracle_threads(), "kind": "oracle",
