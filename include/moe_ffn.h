@@ -183,6 +183,24 @@ typedef struct {
 
 MOE_API moe_status moe_workspace_layout(const moe_dims* d, moe_dtype_mode m, moe_workspace_layout_t* out);
 
+/* moe_plan without a workspace, for callers that cannot allocate device memory where they
+ * need the plan: a runtime that forbids cudaMalloc on its execution path, or a plugin host
+ * that passes an operator its inputs and outputs but no scratch buffer. (The pages have no
+ * counterpart of this call; it is an allocation-free variant of moe_plan.)
+ *   topk_ids, counts, offsets, row_src  as for moe_plan (device memory, owned by the caller;
+ *             counts and offsets are required, row_src is required when T*K > 0).
+ *   Limits: T*K <= 65536 and E <= 1024; larger sizes return MOE_ERR_INVALID_ARG and launch
+ *   nothing. The call allocates nothing: its scratch is one fixed 1,590,272-byte device array
+ *   inside the library that every GPU which loads the library holds until the process exits.
+ *   The first call on a device looks up that array's device address (cudaGetSymbolAddress)
+ *   with the device current; make that first call before any stream capture.
+ *   Every call shares the array and it keeps the last call's contents (the call clears what
+ *   must start at zero itself); calls that overlap on the GPU race on it, so order them on
+ *   one stream. Expert ids outside [-1, E) are skipped like masked routes; this call has no
+ *   error word to report them (moe_plan does). */
+MOE_API moe_status moe_plan_noalloc(const int32_t* topk_ids, const moe_dims* d, int32_t* counts, int32_t* offsets,
+                                    int32_t* row_src, moe_stream_t stream);
+
 /* Test hook for the failure path of a bounded device wait: launches one thread that waits
  * on a workspace flag that nothing sets, gives up after `timeout_ns` nanoseconds, records
  * MOE_ERR_TIMEOUT in the error word and returns. The device stays usable. */

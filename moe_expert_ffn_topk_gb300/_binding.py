@@ -22,7 +22,7 @@ MOE_FLAG_NONE, MOE_FLAG_SIMT = 0, 1
 
 ABI_FUNCTIONS = ("moe_workspace_bytes", "moe_plan", "moe_dispatch", "moe_expert_l1", "moe_expert_l2",
                  "moe_combine", "moe_forward", "moe_check_device_error", "moe_status_string",
-                 "moe_workspace_layout", "moe_debug_bounded_wait")
+                 "moe_workspace_layout", "moe_debug_bounded_wait", "moe_plan_noalloc")
 
 
 class MoeDims(ctypes.Structure):
@@ -65,6 +65,7 @@ def _load():
         "moe_status_string": (ctypes.c_char_p, [st]),
         "moe_workspace_layout": (st, [dims_p, st, ctypes.POINTER(MoeWorkspaceLayout)]),
         "moe_debug_bounded_wait": (st, [vp, sz, ctypes.c_uint64, vp]),
+        "moe_plan_noalloc": (st, [vp, dims_p, vp, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -182,3 +183,10 @@ def moe_check_device_error(workspace, stream=None) -> int:
 def moe_debug_bounded_wait(workspace, timeout_ns: int, stream=None):
     ws, nb = _ws(workspace)
     _check(LIB.moe_debug_bounded_wait(ws, nb, int(timeout_ns), _stream(stream)), "moe_debug_bounded_wait")
+
+
+def moe_plan_noalloc(topk_ids, d: MoeDims, counts, offsets, row_src, stream=None):
+    """moe_plan without a workspace (its scratch is a fixed device array inside the library)."""
+    _check(LIB.moe_plan_noalloc(_ptr(topk_ids, "topk_ids"), ctypes.byref(d), _ptr(counts, "counts"),
+                                _ptr(offsets, "offsets"), _ptr(row_src, "row_src"), _stream(stream)),
+           "moe_plan_noalloc")
