@@ -227,12 +227,15 @@ def dominant_kernel_traffic(workload):
     return int(m.group(1)) if h.group(1) == kernel_source_hash()[:len(h.group(1))] else None
 
 
+L1_KERNEL_SOURCES = ("tc_gemm.cu", "common.cuh", "internal.h")
+
+
 def kernel_source_hash():
+    """sha256 over the sources the tensor-core GEMM kernel is built from."""
     d = os.path.join(ROOT, "moe_expert_ffn_topk_gb300", "csrc")
     sha = hashlib.sha256()
-    for name in sorted(os.listdir(d)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            sha.update(open(os.path.join(d, name), "rb").read())
+    for name in L1_KERNEL_SOURCES:
+        sha.update(open(os.path.join(d, name), "rb").read())
     return sha.hexdigest()
 
 
