@@ -239,6 +239,23 @@ def kernel_source_hash():
     return sha.hexdigest()
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest value over all ranks (the slowest rank's time); identity on one rank."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_step: float, steps: int, elapsed_ms: float, world: int) -> float:
+    """Replicas: every rank runs the full step, so the job did world * steps steps in the
+    slowest rank's time."""
+    return world * flops_per_step * steps / (elapsed_ms * 1e-3) / 1e12
+
+
 def run_gb300(args, wl, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -293,10 +310,7 @@ def run_gb300(args, wl, rank, world, local_rank):
     st = moe.moe_check_device_error(ws)
     if st != 0:
         raise RuntimeError(f"device error in the timed region: {moe.moe_status_string(st)}")
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
 
     # end to end through the public API with host buffers: H2D of the step's inputs from
     # pinned memory, the forward call, D2H of y
@@ -323,17 +337,13 @@ def run_gb300(args, wl, rank, world, local_rank):
         e2e_step()
     e1.record(stream)
     barrier()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
 
     if rank != 0:
         return None, None
     flops = float(wl.flops)
     ms_per_step = elapsed_ms / args.steps
-    value = world * flops * args.steps / (elapsed_ms * 1e-3) / 1e12
+    value = whole_job_tflops(flops, args.steps, elapsed_ms, world)
     pk, pk_src = peaks()
     l1_flops = 4.0 * wl.H * wl.I * wl.routed_rows
     achieved = l1_flops / (l1_ms * 1e-3) / 1e12
@@ -352,7 +362,7 @@ def run_gb300(args, wl, rank, world, local_rank):
                      "peak_source": f"{pk_src} bf16 dense, {'sustained' if sustained else 'burst'}",
                      "l1_ms": l1_ms,
                      "traffic": dominant_kernel_traffic(wl.name)},
-        "e2e": {"value": world * flops * args.steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "e2e": {"value": whole_job_tflops(flops, args.steps, e2e_ms, world), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps},
         "gpu_launches": LAUNCHES_PER_STEP[wl.mode] * args.steps,
         "clocks": clocks.summary(),
