@@ -76,6 +76,9 @@ moe_status layout(const moe_dims* d, moe_dtype_mode m, moe_workspace_layout_t* o
     L.a_pool = take((size_t)pool_rows * I * a_elem_bytes(m));
     L.a_pool_scale = take((size_t)pool_rows * a_scale_row_bytes(m, (int)I));
     L.a_f32 = take(m == MOE_A8W8_INT8 ? (size_t)pool_rows * I * 4 : 0);
+    const int planes = m == MOE_A16W16 ? 0 : (m == MOE_A8W8_INT8 ? 2 : 1);
+    L.x_pool_bf16 = take((size_t)planes * pool_rows * H * 2);
+    L.a_pool_bf16 = take((size_t)planes * pool_rows * I * 2);
     L.total = off;
     L.pool_rows = pool_rows;
     *out = L;
@@ -111,6 +114,8 @@ moe_status make_plan_view(const moe_dims* d, moe_dtype_mode m, void* ws, size_t 
     p->a_pool = b + L.a_pool;
     p->a_pool_scale = b + L.a_pool_scale;
     p->a_f32 = reinterpret_cast<float*>(b + L.a_f32);
+    p->x_bf16 = reinterpret_cast<uint16_t*>(b + L.x_pool_bf16);
+    p->a_bf16 = reinterpret_cast<uint16_t*>(b + L.a_pool_bf16);
     p->comb = reinterpret_cast<uint16_t*>(b + L.comb);
     return MOE_OK;
 }
@@ -168,6 +173,8 @@ moe_status moe_expert_l1(moe_operand w1, const moe_dims* d, moe_dtype_mode m, ui
     cudaError_t e;
     if (!(flags & MOE_FLAG_SIMT) && tc_supported(p, 1)) {
         e = launch_l1_tc(p, w1.data, w1.scale, s);
+    } else if (!(flags & MOE_FLAG_SIMT) && wm_supported(p, 1)) {
+        e = launch_l1_wm(p, w1.data, w1.scale, s);
     } else {
         e = launch_l1_simt(p, w1.data, w1.scale, s);
     }
@@ -186,6 +193,8 @@ moe_status moe_expert_l2(moe_operand w2, const float* topk_weights, const moe_di
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (!(flags & MOE_FLAG_SIMT) && tc_supported(p, 2))
         return from_cuda(launch_l2_tc(p, w2.data, w2.scale, topk_weights, s));
+    if (!(flags & MOE_FLAG_SIMT) && wm_supported(p, 2))
+        return from_cuda(launch_l2_wm(p, w2.data, w2.scale, topk_weights, s));
     return from_cuda(launch_l2_simt(p, w2.data, w2.scale, topk_weights, s));
 }
 

@@ -176,6 +176,58 @@ __global__ void __launch_bounds__(128) dispatch_gather_kernel(const uint4* __res
     }
 }
 
+// S2 for the quantised modes: copies the codes and scales like dispatch_gather_kernel and also
+// writes the row dequantised to bf16 for the tensor-core GEMM (x~ = code * scale, exact in
+// bf16: e4m3 has 4 significant bits and the scales are powers of two). INT8 rows are written
+// as two planes, hi = floor(q/16) and lo = q mod 16 (q = 16*hi + lo, both exact in bf16), so
+// that every fp32 partial sum of the GEMM stays an exactly representable integer.
+template <int MODE>
+__global__ void __launch_bounds__(128) dispatch_gather_q_kernel(const uint8_t* __restrict__ x, const uint8_t* __restrict__ xs,
+                                                                const int32_t* __restrict__ pool_src,
+                                                                const int32_t* __restrict__ hdr, int K, int H,
+                                                                int scale_bytes, int64_t pool_rows, uint8_t* __restrict__ xp,
+                                                                uint8_t* __restrict__ xps, uint16_t* __restrict__ xb) {
+    const int rows = hdr[kHdrPadRows];
+    for (int r = blockIdx.x; r < rows; r += gridDim.x) {
+        const int src = pool_src[r];
+        const int64_t tok = src >= 0 ? src / K : 0;
+        for (int v = threadIdx.x; v < H / 16; v += blockDim.x) {
+            uint4 c = src >= 0 ? reinterpret_cast<const uint4*>(x + tok * H)[v] : make_uint4(0, 0, 0, 0);
+            reinterpret_cast<uint4*>(xp + (int64_t)r * H)[v] = c;
+            const uint8_t* b = reinterpret_cast<const uint8_t*>(&c);
+            uint32_t out[8], out_lo[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                float f0, f1;
+                if constexpr (MODE == MOE_A8W8_INT8) {
+                    const int q0 = (int8_t)b[2 * j], q1 = (int8_t)b[2 * j + 1];
+                    f0 = (float)(q0 >> 4);
+                    f1 = (float)(q1 >> 4);
+                    out_lo[j] = (uint32_t)float_to_bf16_bits((float)(q0 & 15)) |
+                                ((uint32_t)float_to_bf16_bits((float)(q1 & 15)) << 16);
+                } else {
+                    const int k = v * 16 + 2 * j;
+                    float s;
+                    if constexpr (MODE == MOE_A8W8_FP8) s = src >= 0 ? ue8m0_to_float(xs[tok * (H / 32) + k / 32]) : 0.f;
+                    else s = src >= 0 ? reinterpret_cast<const float*>(xs)[tok * (H / 128) + k / 128] : 0.f;
+                    f0 = e4m3_to_float(b[2 * j]) * s;
+                    f1 = e4m3_to_float(b[2 * j + 1]) * s;
+                }
+                out[j] = (uint32_t)float_to_bf16_bits(f0) | ((uint32_t)float_to_bf16_bits(f1) << 16);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(xb + (int64_t)r * H + v * 16);
+            dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
+            dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+            if constexpr (MODE == MOE_A8W8_INT8) {
+                uint4* lo = reinterpret_cast<uint4*>(xb + (pool_rows + r) * H + v * 16);
+                lo[0] = make_uint4(out_lo[0], out_lo[1], out_lo[2], out_lo[3]);
+                lo[1] = make_uint4(out_lo[4], out_lo[5], out_lo[6], out_lo[7]);
+            }
+        }
+        for (int w = threadIdx.x; w < scale_bytes; w += blockDim.x) xps[(int64_t)r * scale_bytes + w] = src >= 0 ? xs[tok * scale_bytes + w] : 0;
+    }
+}
+
 // S6: y[t, 8j..8j+7] = bf16( sum_k comb[t*K+k, 8j..8j+7] ), fp32 sum in slot order.
 __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ comb, const int32_t* __restrict__ slot_row,
                                                       int T, int K, int row_vecs, uint4* __restrict__ y) {
@@ -240,8 +292,24 @@ cudaError_t launch_route(const Plan& p, const int32_t* topk_ids, int32_t* counts
     return cudaGetLastError();
 }
 
+template <int MODE>
+static cudaError_t dispatch_q(const Plan& p, const void* x, const void* x_scale, cudaStream_t s) {
+    const int grid = (int)std::min<int64_t>(p.pool_rows, 152 * 16);
+    dispatch_gather_q_kernel<MODE><<<grid, 128, 0, s>>>(static_cast<const uint8_t*>(x),
+                                                        static_cast<const uint8_t*>(x_scale), p.pool_src, p.hdr, p.K,
+                                                        p.H, (int)x_scale_row_bytes(MODE, p.H), p.pool_rows, p.x_pool,
+                                                        p.x_pool_scale, p.x_bf16);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_dispatch(const Plan& p, const void* x, const void* x_scale, cudaStream_t s) {
     if (p.T == 0) return cudaSuccess;
+    switch (p.mode) {
+        case MOE_A8W8_FP8: return dispatch_q<MOE_A8W8_FP8>(p, x, x_scale, s);
+        case MOE_A8W8_INT8: return dispatch_q<MOE_A8W8_INT8>(p, x, x_scale, s);
+        case MOE_A8W4_FP8_FP4: return dispatch_q<MOE_A8W4_FP8_FP4>(p, x, x_scale, s);
+        default: break;
+    }
     const int row_vecs = p.H * x_elem_bytes(p.mode) / 16;
     const int scale_words = (int)(x_scale_row_bytes(p.mode, p.H) / 4);
     const int grid = (int)std::min<int64_t>(p.pool_rows, 152 * 16);

@@ -164,9 +164,14 @@ __global__ void __launch_bounds__(NT) l1_simt_kernel(Plan p, const uint8_t* __re
             for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
             const int ex = mx_exponent_e4m3(amax);
             const float inv = exp2_neg_int(ex);
-            p.a_pool[row * I + j0] = float_to_e4m3_satfinite(a[0] * inv);
-            p.a_pool[row * I + j0 + 1] = float_to_e4m3_satfinite(a[1] * inv);
+            const uint8_t c0 = float_to_e4m3_satfinite(a[0] * inv), c1 = float_to_e4m3_satfinite(a[1] * inv);
+            p.a_pool[row * I + j0] = c0;
+            p.a_pool[row * I + j0 + 1] = c1;
             if (tx == 0) p.a_pool_scale[row * (I / 32) + jb] = static_cast<uint8_t>(ex + 127);
+            // the same values dequantised (exact in bf16) for the tensor-core L2 GEMM
+            const float sc = ue8m0_to_float(static_cast<uint8_t>(ex + 127));
+            p.a_bf16[row * I + j0] = float_to_bf16_bits(e4m3_to_float(c0) * sc);
+            p.a_bf16[row * I + j0 + 1] = float_to_bf16_bits(e4m3_to_float(c1) * sc);
         }
     }
 }
@@ -255,10 +260,15 @@ __global__ void __launch_bounds__(256) int8_row_quant_kernel(Plan p) {
         __syncthreads();
         const float s = fmaxf(__fdiv_rn(amax, 127.0f), 1e-8f);
         int8_t* q = reinterpret_cast<int8_t*>(p.a_pool) + (int64_t)r * I;
+        uint16_t* hi = p.a_bf16 + (int64_t)r * I;               // plane 0: floor(q/16)
+        uint16_t* lo = p.a_bf16 + (p.pool_rows + r) * I;        // plane 1: q mod 16
         for (int j = threadIdx.x; j < I; j += blockDim.x) {
             float v = rintf(__fdiv_rn(a[j], s));
             v = fminf(fmaxf(v, -127.0f), 127.0f);
-            q[j] = static_cast<int8_t>(v);
+            const int qi = static_cast<int>(v);
+            q[j] = static_cast<int8_t>(qi);
+            hi[j] = float_to_bf16_bits((float)(qi >> 4));
+            lo[j] = float_to_bf16_bits((float)(qi & 15));
         }
         if (threadIdx.x == 0) reinterpret_cast<float*>(p.a_pool_scale)[r] = s;
     }

@@ -28,10 +28,13 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tc_common.cuh"
 
 namespace moe {
 
 namespace {
+
+using namespace tc;
 
 constexpr int kBM = 128;                       // rows per tile (MMA M)
 constexpr int kBN = 256;                       // accumulator columns per tile (MMA N)
@@ -44,7 +47,6 @@ constexpr int kStageBytes = kABytes + kBBytes; // 48 KB
 constexpr int kThreads = 192;
 constexpr int kTmemCols = 512;                 // two 256-column fp32 accumulators
 constexpr int kMaxExperts = 1024;
-constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 
 // Instruction descriptor of tcgen05.mma.kind::f16: D fp32 (bits 4-5 = 1), A bf16 (bits 7-9 =
 // 1), B bf16 (bits 10-12 = 1), A K-major (bit 15 = 0), B MN-major (bit 16 = 1), N >> 3 in
@@ -60,110 +62,10 @@ struct TcArgs {
     int k_rows;                 // rows of one expert's weight in its 2-D view (L1: H, L2: I)
 };
 
-// ---------------------------------------------------------------------------------------
-// PTX wrappers
-// ---------------------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar),
-                 "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return done != 0;
-}
-
-// Bounded wait for the phase of `bar` with the given parity to complete. Returns false when
-// the CTA gave up (this thread timed out, or another role already aborted).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* hdr, volatile int* abort_flag) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
-            record_error(hdr, MOE_ERR_TIMEOUT);
-            *abort_flag = 1;
-            return false;
-        }
-    }
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
-        : "memory");
-}
-
-// 32 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-}
-
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-// Shared-memory matrix descriptor: start >> 4 (bits 0-13), leading byte offset >> 4 (16-29),
-// stride byte offset >> 4 (32-45), descriptor version 1 (46-47), base offset 0, swizzle
-// mode in bits 61-63 (2 = 128-byte swizzle).
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-    uint64_t d = 0;
-    d |= (uint64_t)((addr >> 4) & 0x3FFFu);
-    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-    d |= (uint64_t)1 << 46;
-    d |= (uint64_t)2 << 61;
-    return d;
-}
-
 // A tile: 128 rows x 64 K, K-major, 128-byte swizzle (the TMA box layout). 8-row groups are
 // 1024 bytes apart; the K extent of one MMA (16 elements, 32 bytes) stays inside a swizzle
 // row, so the leading byte offset is unused.
-__device__ __forceinline__ uint64_t a_desc(uint32_t tile, int kk) { return smem_desc(tile + kk * 32, 16, 1024); }
+__device__ __forceinline__ uint64_t a_desc(uint32_t tile, int kk) { return kmajor_desc(tile, kk); }
 
 // B tile: four 64(K) x 64(N) boxes, N contiguous (MN-major), 128-byte swizzle. The 64-column
 // groups are one box (8 KB) apart (leading byte offset); groups of 8 K rows are 1024 bytes
@@ -398,42 +300,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // host side
 // ---------------------------------------------------------------------------------------
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    });
-    return fn;
-}
-
 // 2-D bf16 tensor [outer, inner] (row-major), boxes of box_outer x 64 elements, 128-byte swizzle.
 bool make_map(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_outer) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {inner * 2};
-    cuuint32_t box[2] = {64, box_outer};
-    cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-int num_sms() {
-    static int n = 0;
-    if (n == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        if (n <= 0) n = 148;
-    }
-    return n;
+    return tc_make_map_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, inner, outer, 64, box_outer,
+                          CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 constexpr size_t smem_bytes() {
@@ -450,7 +320,7 @@ cudaError_t launch_tc(const Plan& p, const CUtensorMap& a, const CUtensorMap& b,
     });
     if (attr_err != cudaSuccess) return attr_err;
     const int64_t max_tiles = (p.pool_rows / kBM) * args.n_tiles;
-    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(max_tiles, num_sms()));
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(max_tiles, tc_num_sms()));
     tc_gemm_kernel<kL1><<<grid, kThreads, smem_bytes(), s>>>(a, b, args);
     return cudaGetLastError();
 }
@@ -458,7 +328,7 @@ cudaError_t launch_tc(const Plan& p, const CUtensorMap& a, const CUtensorMap& b,
 }  // namespace
 
 bool tc_supported(const Plan& p, int stage) {
-    if (p.mode != MOE_A16W16 || p.E > kMaxExperts || encode_fn() == nullptr) return false;
+    if (p.mode != MOE_A16W16 || p.E > kMaxExperts || !tc_encode_available()) return false;
     if (stage == 1) return p.I % 128 == 0;
     return p.H % kBN == 0;
 }

@@ -246,3 +246,53 @@ def test_tensor_core_stages_match_reference_kernels(moe, wl):
     assert diff.max() <= 2 ** -7 * scale, f"A pool: max diff {diff.max():.3e} vs scale {scale:.3e}"
     c = [region(o["ws"], L, "comb", torch.bfloat16, wl.T * wl.K * wl.H).float().cpu().numpy() for o in outs]
     assert np.abs(c[0] - c[1]).max() <= 2e-2 * np.abs(c[1]).max()
+
+
+def test_int8_l1_accumulators_exact_on_adversarial_codes(moe):
+    """Every x and W1 code is +-127 and K = 5120, so the int32 accumulators reach 5120*127^2
+    = 82,580,480 > 2^24: a plain fp32 accumulation would round, the exact integer GEMM must
+    not. With unit scales H = C exactly and SiLU(H) is H or 0, so the fp32 A of the kernel must
+    equal the oracle's bit for bit."""
+    wl = Workload("adv_int8", "a8w8_int8", 96, 5120, 256, 2, 1, 51, 0.05)
+    inp = make_inputs(wl, device=DEV)
+    g = torch.Generator(device=DEV).manual_seed(5)
+    sign = lambda shape: (torch.randint(0, 2, shape, generator=g, device=DEV) * 2 - 1).to(torch.int8) * 127
+    inp["x"] = sign(inp["x"].shape)
+    inp["x"][:3] = 127                  # rows whose gate and up sums are exactly +-82,580,480
+    inp["x_scale"] = torch.ones_like(inp["x_scale"])
+    inp["w1"] = sign(inp["w1"].shape)
+    inp["w1"][0, :3] = 127
+    inp["w1"][0, wl.I:wl.I + 3] = 127
+    inp["w1_scale"] = torch.ones_like(inp["w1_scale"])
+    inp["topk_ids"][:3] = 0
+    out = run_forward(moe, wl, inp, stages=True)
+    assert out["status"] == 0
+    L = out["layout"]
+    rows = L["pool_rows"]
+    ws = out["ws"]
+    pool_src = region(ws, L, "pool_src", torch.int32, rows).cpu().numpy()
+    a_f32 = region(ws, L, "a_f32", torch.float32, rows * wl.I).view(rows, wl.I).cpu().numpy()
+    _, rec = oracle_forward(wl, inp, return_intermediates=True)
+    for e, r in rec["experts"].items():
+        h = r["h"]
+        assert np.abs(r["c"]).max() > 2 ** 24 or e != 0
+        a_ref = (omoe.swiglu(h, wl.I)).astype(np.float32)
+        got_rows = {int(s): i for i, s in enumerate(pool_src) if s >= 0}
+        got = np.stack([a_f32[got_rows[int(s)]] for s in r["src"]])
+        # |H| >= 32258 whenever it is non-zero, so SiLU(H) = H exactly for H > 0 on both sides;
+        # for H <= 0 SiLU(H) * H_up is 0 up to an fp32/float64 underflow difference
+        pos = h[:, :wl.I] > 0
+        assert np.array_equal(got[pos], a_ref[pos]), f"expert {e}: {np.abs(got - a_ref)[pos].max()}"
+        assert np.abs(got[~pos]).max(initial=0) < 1e-20 and np.abs(a_ref[~pos]).max(initial=0) < 1e-20
+
+
+@pytest.mark.parametrize("mode,wl", [(m, w) for m, w in ALL if m != "a16w16"],
+                         ids=[f"{m}-{w.name}" for m, w in ALL if m != "a16w16"])
+def test_quantised_tensor_core_path_matches_reference_kernels(moe, mode, wl):
+    """The weight-major tcgen05 path and the CUDA-core reference kernels give the same weighted
+    combine rows up to the fp32 summation order."""
+    inp = make_inputs(wl, device=DEV)
+    outs = [run_forward(moe, wl, inp, flags=f, stages=True) for f in (0, 1)]
+    L = outs[0]["layout"]
+    c = [region(o["ws"], L, "comb", torch.bfloat16, wl.T * wl.K * wl.H).float().cpu().numpy() for o in outs]
+    assert np.abs(c[0] - c[1]).max() <= TOL[mode] * np.abs(c[1]).max()
