@@ -256,6 +256,41 @@ def whole_job_tflops(flops_per_step: float, steps: int, elapsed_ms: float, world
     return world * flops_per_step * steps / (elapsed_ms * 1e-3) / 1e12
 
 
+WEIGHT_BYTES_PER_ELEM = {"a16w16": 2.0, "a8w8_fp8": 1.0 + 1 / 32, "a8w8_int8": 1.0, "a8w4_fp8_fp4": 0.5 + 1 / 32}
+X_BYTES_PER_ELEM = {"a16w16": 2.0, "a8w8_fp8": 1.0 + 1 / 32, "a8w8_int8": 1.0, "a8w4_fp8_fp4": 1.0 + 4 / 128}
+
+
+def is_decode(wl) -> bool:
+    """Few routed rows per expert: the step streams the weights (HBM-bound)."""
+    return wl.routed_rows / wl.E < 64
+
+
+def l1_roofline(wl, inp, l1_ms, pk, pk_src, sustained):
+    """Roofline of the dominant kernel, the L1 grouped GEMM (2/3 of the flops and of the weight
+    bytes). Tensor-bound workloads: algorithmic flops 4*H*I per routed row against the dense
+    bf16 peak (the tensor-core kind every GEMM here issues). Weight-streaming (decode)
+    workloads: algorithmic bytes = W1 (+ block scales) of every expert with N_e > 0 plus the x
+    rows, against the measured HBM copy bandwidth."""
+    import numpy as np
+    if is_decode(wl):
+        ids = inp["topk_ids"].cpu().numpy().reshape(-1)
+        touched = len(np.unique(ids[ids >= 0]))
+        nbytes = touched * 2 * wl.I * wl.H * WEIGHT_BYTES_PER_ELEM[wl.mode] + wl.T * wl.H * X_BYTES_PER_ELEM[wl.mode]
+        achieved = nbytes / (l1_ms * 1e-3) / 1e9
+        peak = float(pk["hbm_gbs"])
+        return {"bound": "hbm", "kernel": "L1 grouped GEMM + SwiGLU (moe_expert_l1)", "achieved": achieved,
+                "peak": peak, "unit": "GB/s", "frac": achieved / peak, "peak_source": f"{pk_src} HBM copy",
+                "l1_ms": l1_ms, "algorithmic_bytes": nbytes, "experts_touched": touched,
+                "traffic": dominant_kernel_traffic(wl.name)}
+    l1_flops = 4.0 * wl.H * wl.I * wl.routed_rows
+    achieved = l1_flops / (l1_ms * 1e-3) / 1e12
+    peak = float(pk["bf16_tflops_sustained"] if sustained else pk["bf16_tflops"])
+    return {"bound": "tensor", "kernel": "L1 grouped GEMM + SwiGLU (moe_expert_l1)", "achieved": achieved,
+            "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "peak_source": f"{pk_src} bf16 dense, {'sustained' if sustained else 'burst'}", "l1_ms": l1_ms,
+            "traffic": dominant_kernel_traffic(wl.name)}
+
+
 def run_gb300(args, wl, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -345,23 +380,17 @@ def run_gb300(args, wl, rank, world, local_rank):
     ms_per_step = elapsed_ms / args.steps
     value = whole_job_tflops(flops, args.steps, elapsed_ms, world)
     pk, pk_src = peaks()
-    l1_flops = 4.0 * wl.H * wl.I * wl.routed_rows
-    achieved = l1_flops / (l1_ms * 1e-3) / 1e12
     # a timed region of a second or more runs at the power-capped clock: sustained peak;
     # a shorter one runs at burst clocks: burst peak
     sustained = elapsed_ms >= 1000.0
-    peak = float(pk["bf16_tflops_sustained"] if sustained else pk["bf16_tflops"])
+    roof = l1_roofline(wl, inp, l1_ms, pk, pk_src, sustained)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": DTYPE[wl.mode], "data": "synthetic (seeded; random-init weights)",
         "config": workload_config(wl),
         "routed_rows_per_s": world * wl.routed_rows * args.steps / (elapsed_ms * 1e-3),
-        "roofline": {"bound": "tensor", "kernel": "L1 grouped GEMM + SwiGLU (moe_expert_l1)",
-                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                     "peak_source": f"{pk_src} bf16 dense, {'sustained' if sustained else 'burst'}",
-                     "l1_ms": l1_ms,
-                     "traffic": dominant_kernel_traffic(wl.name)},
+        "roofline": roof,
         "e2e": {"value": whole_job_tflops(flops, args.steps, e2e_ms, world), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps},
         "gpu_launches": LAUNCHES_PER_STEP[wl.mode] * args.steps,
