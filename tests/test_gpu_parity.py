@@ -270,7 +270,8 @@ def test_int8_l1_accumulators_exact_on_adversarial_codes(moe):
     L = out["layout"]
     rows = L["pool_rows"]
     ws = out["ws"]
-    pool_src = region(ws, L, "pool_src", torch.int32, rows).cpu().numpy()
+    n_pad = int(region(ws, L, "header", torch.int32, 16).cpu().numpy()[2])
+    pool_src = region(ws, L, "pool_src", torch.int32, rows).cpu().numpy()[:n_pad]
     a_f32 = region(ws, L, "a_f32", torch.float32, rows * wl.I).view(rows, wl.I).cpu().numpy()
     _, rec = oracle_forward(wl, inp, return_intermediates=True)
     for e, r in rec["experts"].items():
