@@ -53,30 +53,38 @@ constexpr int kThreads = 352;
 constexpr int kMaxExperts = 1024;
 constexpr int kABytes = 2 * kWR * 128;  // two 128-row bf16 weight blocks per stage
 
+// Three rings per CTA: raw weight codes (TMA), the weights converted to bf16 (converter warps)
+// and the bf16 token tiles (TMA). The token ring is separate so its loads run ahead of the
+// converters by its own depth.
 template <int MODE>
 struct WmCfg;
 template <>
 struct WmCfg<MOE_A8W8_FP8> {
-    static constexpr int kWRaw = 64, kBRows = 128, kAccCols = 128, kBufs = 2, kRawStages = 4, kBfStages = 3;
+    static constexpr int kWRaw = 64, kBRows = 128, kAccCols = 128, kBufs = 2;
+    static constexpr int kRawStages = 3, kBfStages = 3, kTokStages = 4;
 };
 template <>
 struct WmCfg<MOE_A8W4_FP8_FP4> {
-    static constexpr int kWRaw = 32, kBRows = 128, kAccCols = 128, kBufs = 2, kRawStages = 8, kBfStages = 3;
+    static constexpr int kWRaw = 32, kBRows = 128, kAccCols = 128, kBufs = 2;
+    static constexpr int kRawStages = 6, kBfStages = 3, kTokStages = 4;
 };
 template <>
 struct WmCfg<MOE_A8W8_INT8> {
-    static constexpr int kWRaw = 64, kBRows = 256, kAccCols = 256, kBufs = 1, kRawStages = 4, kBfStages = 2;
+    static constexpr int kWRaw = 64, kBRows = 256, kAccCols = 256, kBufs = 1;
+    static constexpr int kRawStages = 3, kBfStages = 2, kTokStages = 3;
 };
 
 template <int MODE>
 struct WmLayout {
     using C = WmCfg<MODE>;
-    static constexpr int kBfBytes = kABytes + C::kBRows * 128;
+    static constexpr int kBfBytes = kABytes;                // two bf16 weight blocks
+    static constexpr int kTokBytes = C::kBRows * 128;       // bf16 token tile (INT8: hi + lo rows)
     static constexpr int kRawBytes = 2 * kWR * C::kWRaw;
     static constexpr int kBfOff = 0;
-    static constexpr int kRawOff = kBfOff + C::kBfStages * kBfBytes;
+    static constexpr int kTokOff = kBfOff + C::kBfStages * kBfBytes;
+    static constexpr int kRawOff = kTokOff + C::kTokStages * kTokBytes;
     static constexpr int kBarOff = kRawOff + C::kRawStages * kRawBytes;
-    static constexpr int kNumBars = 2 * C::kRawStages + 2 * C::kBfStages + 4 + 1;
+    static constexpr int kNumBars = 2 * C::kRawStages + 2 * C::kBfStages + 2 * C::kTokStages + 4 + 1;
     static constexpr int kMiscOff = kBarOff + 8 * kNumBars;     // tmem holder, abort flag
     static constexpr int kLutOff = kMiscOff + 16;               // 256 x u32 (e2m1 byte -> bf16x2)
     static constexpr int kTileOff = kLutOff + 1024;             // int[E+1]
@@ -195,9 +203,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto raw_empty = [&](int i) { return bars + 8u * (C::kRawStages + i); };
     auto bf_full = [&](int i) { return bars + 8u * (2 * C::kRawStages + i); };
     auto bf_empty = [&](int i) { return bars + 8u * (2 * C::kRawStages + C::kBfStages + i); };
-    auto acc_full = [&](int i) { return bars + 8u * (2 * C::kRawStages + 2 * C::kBfStages + i); };
-    auto acc_empty = [&](int i) { return bars + 8u * (2 * C::kRawStages + 2 * C::kBfStages + 2 + i); };
-    const uint32_t drain_bar = bars + 8u * (2 * C::kRawStages + 2 * C::kBfStages + 4);
+    constexpr int kTokBar = 2 * C::kRawStages + 2 * C::kBfStages;
+    auto tok_full = [&](int i) { return bars + 8u * (kTokBar + i); };
+    auto tok_empty = [&](int i) { return bars + 8u * (kTokBar + C::kTokStages + i); };
+    constexpr int kAccBar = kTokBar + 2 * C::kTokStages;
+    auto acc_full = [&](int i) { return bars + 8u * (kAccBar + i); };
+    auto acc_empty = [&](int i) { return bars + 8u * (kAccBar + 2 + i); };
+    const uint32_t drain_bar = bars + 8u * (kAccBar + 4);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
     uint32_t* lut = reinterpret_cast<uint32_t*>(smem + L::kLutOff);
@@ -218,8 +230,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(raw_empty(i), 128);
         }
         for (int i = 0; i < C::kBfStages; ++i) {
-            mbar_init(bf_full(i), 128 + 1);  // 128 converter threads + the token TMA
+            mbar_init(bf_full(i), 128);      // the 128 converter threads
             mbar_init(bf_empty(i), 1);
+        }
+        for (int i = 0; i < C::kTokStages; ++i) {
+            mbar_init(tok_full(i), 1);       // the token TMA (arrive + bytes)
+            mbar_init(tok_empty(i), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(acc_full(i), 1);
@@ -274,22 +290,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int n = tile_n<MODE>(n_valid);
                 const int boxes = (MODE == MOE_A8W8_INT8 ? kTokTile : n) / kTokBox;
                 for (int kb = 0; kb < KB; ++kb, ++it) {
-                    const int b = it % C::kBfStages;
-                    if (!mbar_wait(bf_empty(b), ((uint32_t)(it / C::kBfStages) & 1u) ^ 1u, p.hdr, abort_flag)) {
+                    const int b = it % C::kTokStages;
+                    if (!mbar_wait(tok_empty(b), ((uint32_t)(it / C::kTokStages) & 1u) ^ 1u, p.hdr, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t dst = base + L::kBfOff + b * L::kBfBytes + kABytes;
+                    const uint32_t dst = base + L::kTokOff + b * L::kTokBytes;
                     const int planes = MODE == MOE_A8W8_INT8 ? 2 : 1;
-                    mbar_arrive_expect_tx(bf_full(b), (uint32_t)(planes * boxes * kTokBox * 128));
+                    mbar_arrive_expect_tx(tok_full(b), (uint32_t)(planes * boxes * kTokBox * 128));
                     for (int pl = 0; pl < planes; ++pl)
                         for (int i = 0; i < boxes; ++i)
                             tma_load_2d(dst + (pl * kTokTile + i * kTokBox) * 128, &tmX, kb * kBK,
-                                        (int)(pl * p.pool_rows) + tl.row0 + i * kTokBox, bf_full(b));
+                                        (int)(pl * p.pool_rows) + tl.row0 + i * kTokBox, tok_full(b));
                 }
             }
-            for (int j = it - C::kBfStages < 0 ? 0 : it - C::kBfStages; j < it; ++j)
-                mbar_drain(bf_full(j % C::kBfStages), (uint32_t)(j / C::kBfStages) & 1u, p.hdr);
+            for (int j = it - C::kTokStages < 0 ? 0 : it - C::kTokStages; j < it; ++j)
+                mbar_drain(tok_full(j % C::kTokStages), (uint32_t)(j / C::kTokStages) & 1u, p.hdr);
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
@@ -306,15 +322,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t d0 = tmem_base + (uint32_t)(a * 2 * C::kAccCols);
                 const uint32_t d1 = d0 + C::kAccCols;
                 for (int kb = 0; kb < KB; ++kb, ++it) {
-                    const int b = it % C::kBfStages;
-                    if (!mbar_wait(bf_full(b), (uint32_t)(it / C::kBfStages) & 1u, p.hdr, abort_flag)) {
+                    const int b = it % C::kBfStages, tb = it % C::kTokStages;
+                    if (!mbar_wait(bf_full(b), (uint32_t)(it / C::kBfStages) & 1u, p.hdr, abort_flag) ||
+                        !mbar_wait(tok_full(tb), (uint32_t)(it / C::kTokStages) & 1u, p.hdr, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t sa0 = base + L::kBfOff + b * L::kBfBytes;
                     const uint32_t sa1 = sa0 + kWR * 128;
-                    const uint32_t sb = sa0 + kABytes;
+                    const uint32_t sb = base + L::kTokOff + tb * L::kTokBytes;
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
                         const uint64_t bd = kmajor_desc(sb, kk);
@@ -322,6 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_mma(d1, kmajor_desc(sa1, kk), bd, idesc, (kb | kk) != 0);
                     }
                     tc_commit(bf_empty(b));
+                    tc_commit(tok_empty(tb));
                 }
                 if (ok) tc_commit(acc_full(a));
             }
@@ -331,19 +349,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp >= 6) {
         // ---------------- weight converters ----------------
         const int c = threadIdx.x - 192;  // row of each 128-row weight block
+        const int spr = args.kin / 32;    // scale bytes per weight row (a multiple of 4)
         int it = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
             const Tile tl = decode(t, tile_off, p.E, args.n_slabs);
             const int64_t g0 = (int64_t)tl.e * args.n_out + (kL1 ? tl.s * kWR : tl.s * 2 * kWR) + c;
             const int64_t g1 = kL1 ? g0 + I : g0 + kWR;
-            const int spr = args.kin / 32;  // scale bytes per weight row
+            // the scales of 8 k-blocks (16 bytes per row) are loaded one group ahead of use
+            uint32_t cur0[4] = {}, cur1[4] = {}, nxt0[4] = {}, nxt1[4] = {};
+            auto load_group = [&](int grp, uint32_t (&d0)[4], uint32_t (&d1)[4]) {
+                if constexpr (MODE != MOE_A8W8_INT8) {
+                    const uint32_t* r0 = reinterpret_cast<const uint32_t*>(args.w_scale + g0 * spr);
+                    const uint32_t* r1 = reinterpret_cast<const uint32_t*>(args.w_scale + g1 * spr);
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        const int word = grp * 4 + w;
+                        d0[w] = word < spr / 4 ? __ldg(r0 + word) : 0u;
+                        d1[w] = word < spr / 4 ? __ldg(r1 + word) : 0u;
+                    }
+                }
+            };
+            load_group(0, cur0, cur1);
+            load_group(1, nxt0, nxt1);
             for (int kb = 0; kb < KB; ++kb, ++it) {
                 const int r = it % C::kRawStages, b = it % C::kBfStages;
+                if (kb > 0 && (kb & 7) == 0) {
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        cur0[w] = nxt0[w];
+                        cur1[w] = nxt1[w];
+                    }
+                    load_group((kb >> 3) + 1, nxt0, nxt1);
+                }
+                const int sel = (kb & 7) >> 1, sh = 16 * (kb & 1);
                 uint32_t s0 = 0, s1 = 0;
-                if constexpr (MODE != MOE_A8W8_INT8) {
-                    s0 = *reinterpret_cast<const uint16_t*>(args.w_scale + g0 * spr + 2 * kb);
-                    s1 = *reinterpret_cast<const uint16_t*>(args.w_scale + g1 * spr + 2 * kb);
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    if (w == sel) {
+                        s0 = (cur0[w] >> sh) & 0xffffu;
+                        s1 = (cur1[w] >> sh) & 0xffffu;
+                    }
                 }
                 bool w_ok = mbar_wait(raw_full(r), (uint32_t)(it / C::kRawStages) & 1u, p.hdr, abort_flag);
                 w_ok = w_ok && mbar_wait(bf_empty(b), ((uint32_t)(it / C::kBfStages) & 1u) ^ 1u, p.hdr, abort_flag);
