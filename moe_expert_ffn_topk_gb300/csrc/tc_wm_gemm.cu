@@ -14,8 +14,8 @@
 //   them dequantised to bf16; x~ = e4m3 code * power-of-two scale is exact in bf16. TMA loads
 //   them straight into the 128-byte-swizzled K-major tile.
 // - weights stay in HBM in their compact storage format (e2m1, e4m3 or int8); TMA brings the
-//   raw bytes into a staging ring and four converter warps expand them, with their UE8M0 block
-//   scale, to bf16 in the swizzled layout (exact as well). This keeps the HBM stream at 0.5 or
+//   raw bytes into a staging ring (32- or 64-byte swizzled) and four converter warps expand
+//   them, with their UE8M0 block scale, to bf16 in the 128-byte-swizzled layout (exact as well). This keeps the HBM stream at 0.5 or
 //   1 byte per weight, which is what decode is bound by.
 // INT8: every product q_x * q_w is an integer, and the fp32 accumulator is exact while the
 // partial sums stay below 2^24. The token codes are split as q = 16*hi + lo with
@@ -30,6 +30,8 @@
 // Every wait is bounded; on time-out the CTA records MOE_ERR_TIMEOUT, drains and exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
@@ -86,8 +88,7 @@ struct WmLayout {
     static constexpr int kBarOff = kRawOff + C::kRawStages * kRawBytes;
     static constexpr int kNumBars = 2 * C::kRawStages + 2 * C::kBfStages + 2 * C::kTokStages + 4 + 1;
     static constexpr int kMiscOff = kBarOff + 8 * kNumBars;     // tmem holder, abort flag
-    static constexpr int kLutOff = kMiscOff + 16;               // 256 x u32 (e2m1 byte -> bf16x2)
-    static constexpr int kTileOff = kLutOff + 1024;             // int[E+1]
+    static constexpr int kTileOff = kMiscOff + 16;              // int[E+1]
     static constexpr int kCountsOff = kTileOff + 4 * (kMaxExperts + 1);
     static constexpr int kBytes = kCountsOff + 4 * kMaxExperts;
     static constexpr size_t kSmem = 1024 + (size_t)kBytes;
@@ -151,41 +152,86 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return (uint32_t)float_to_bf16_bits(lo) | ((uint32_t)float_to_bf16_bits(hi) << 16);
 }
 
-// Expand one weight row's K block (64 elements) into the 128-byte-swizzled bf16 row `r` of a
-// K-major tile starting at `tile` (1024-byte aligned).
+__device__ __forceinline__ void store_chunk(uint8_t* tile, int r, int ch, uint32_t a, uint32_t b, uint32_t c,
+                                            uint32_t d) {
+    *reinterpret_cast<uint4*>(tile + r * 128 + ((ch ^ (r & 7)) << 4)) = make_uint4(a, b, c, d);
+}
+
+// 8 e2m1 codes (one 32-bit word, element 2j in the low nibble of byte j) times a power-of-two
+// scale, as 4 bf16x2 words. e2m1 -> f16 is exact, the fp32 product is exact, and so is the
+// rounding to bf16.
+__device__ __forceinline__ void e2m1x8_to_bf16(uint32_t w, float sc, uint32_t (&o)[4]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const __half2_raw h = __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)((w >> (8 * j)) & 0xffu), __NV_E2M1);
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
+        o[j] = pack_bf16x2(f.x * sc, f.y * sc);
+    }
+}
+
+// 8 e4m3 codes (two 32-bit words) times a power-of-two scale, as 4 bf16x2 words (exact).
+__device__ __forceinline__ void e4m3x8_to_bf16(uint32_t w0, uint32_t w1, float sc, uint32_t (&o)[4]) {
+    const uint32_t ww[2] = {w0, w1};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t pair = (ww[j >> 1] >> (16 * (j & 1))) & 0xffffu;
+        const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)pair, __NV_E4M3);
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
+        o[j] = pack_bf16x2(f.x * sc, f.y * sc);
+    }
+}
+
+// 8 int8 codes (two 32-bit words) as 4 bf16x2 words (exact).
+__device__ __forceinline__ void int8x8_to_bf16(uint32_t w0, uint32_t w1, uint32_t (&o)[4]) {
+    const uint32_t ww[2] = {w0, w1};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t pair = ww[j >> 1] >> (16 * (j & 1));
+        o[j] = pack_bf16x2((float)(int8_t)(pair & 0xffu), (float)(int8_t)((pair >> 8) & 0xffu));
+    }
+}
+
+// Expand weight row r's K block (64 elements) from the raw tile, which TMA wrote with the
+// 32-byte (e2m1: 32-byte rows) or 64-byte (one-byte codes: 64-byte rows) swizzle, into the
+// 128-byte-swizzled bf16 row r of a K-major MMA tile. Reads and writes are 16-byte accesses
+// and, with the swizzles, free of bank conflicts across a warp.
 template <int MODE>
-__device__ __forceinline__ void convert_row(const uint8_t* raw, uint32_t scales2, const uint32_t* lut, uint8_t* tile,
-                                            int r) {
-    uint8_t* row = tile + r * 128;
+__device__ __forceinline__ void convert_row(const uint8_t* raw_tile, uint32_t scales2, uint8_t* tile, int r) {
+    const float s0 = ue8m0_to_float((uint8_t)(scales2 & 0xffu));
+    const float s1 = ue8m0_to_float((uint8_t)((scales2 >> 8) & 0xffu));
+    if constexpr (MODE == MOE_A8W4_FP8_FP4) {
+        const uint8_t* row = raw_tile + r * 32;
+        const int x = (r >> 2) & 1;  // 32-byte swizzle: chunk ^= address bit 7
 #pragma unroll
-    for (int ch = 0; ch < 8; ++ch) {
-        uint32_t o[4];
-        if constexpr (MODE == MOE_A8W4_FP8_FP4) {
-            const uint32_t w = reinterpret_cast<const uint32_t*>(raw)[ch];  // 8 codes
-            const uint32_t sc = ue8m0_bf16x2(ch < 4 ? (scales2 & 0xffu) : ((scales2 >> 8) & 0xffu));
+        for (int q = 0; q < 2; ++q) {
+            const uint4 c = *reinterpret_cast<const uint4*>(row + ((q ^ x) << 4));
+            const float sc = q == 0 ? s0 : s1;
+            const uint32_t w[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
-            for (int j = 0; j < 4; ++j) o[j] = bf16x2_mul(lut[(w >> (8 * j)) & 0xffu], sc);
-        } else if constexpr (MODE == MOE_A8W8_FP8) {
-            const uint2 w = reinterpret_cast<const uint2*>(raw)[ch];        // 8 codes
-            const float sc = ue8m0_to_float((uint8_t)(ch < 4 ? (scales2 & 0xffu) : ((scales2 >> 8) & 0xffu)));
-            const uint32_t ww[2] = {w.x, w.y};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t pair = (ww[j >> 1] >> (16 * (j & 1))) & 0xffffu;
-                const __half2_raw h2 = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)pair, __NV_E4M3);
-                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
-                o[j] = pack_bf16x2(f.x * sc, f.y * sc);
-            }
-        } else {
-            const uint2 w = reinterpret_cast<const uint2*>(raw)[ch];
-            const uint32_t ww[2] = {w.x, w.y};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t pair = (ww[j >> 1] >> (16 * (j & 1))) & 0xffffu;
-                o[j] = pack_bf16x2((float)(int8_t)(pair & 0xff), (float)(int8_t)(pair >> 8));
+            for (int k = 0; k < 4; ++k) {
+                uint32_t o[4];
+                e2m1x8_to_bf16(w[k], sc, o);
+                store_chunk(tile, r, q * 4 + k, o[0], o[1], o[2], o[3]);
             }
         }
-        *reinterpret_cast<uint4*>(row + ((ch ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+    } else {
+        const uint8_t* row = raw_tile + r * 64;
+        const int x = (r >> 1) & 3;  // 64-byte swizzle: chunk ^= address bits 7-8
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint4 c = *reinterpret_cast<const uint4*>(row + ((q ^ x) << 4));
+            uint32_t o[4], o2[4];
+            if constexpr (MODE == MOE_A8W8_FP8) {
+                const float sc = q < 2 ? s0 : s1;
+                e4m3x8_to_bf16(c.x, c.y, sc, o);
+                e4m3x8_to_bf16(c.z, c.w, sc, o2);
+            } else {
+                int8x8_to_bf16(c.x, c.y, o);
+                int8x8_to_bf16(c.z, c.w, o2);
+            }
+            store_chunk(tile, r, 2 * q, o[0], o[1], o[2], o[3]);
+            store_chunk(tile, r, 2 * q + 1, o2[0], o2[1], o2[2], o2[3]);
+        }
     }
 }
 
@@ -212,7 +258,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t drain_bar = bars + 8u * (kAccBar + 4);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
-    uint32_t* lut = reinterpret_cast<uint32_t*>(smem + L::kLutOff);
     int* tile_off = reinterpret_cast<int*>(smem + L::kTileOff);
     int* counts = reinterpret_cast<int*>(smem + L::kCountsOff);
 
@@ -220,10 +265,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int i = threadIdx.x; i <= p.E; i += kThreads) tile_off[i] = p.tile_off[i];
     for (int i = threadIdx.x; i < p.E; i += kThreads) counts[i] = p.counts[i];
-    if (MODE == MOE_A8W4_FP8_FP4) {
-        for (int b = threadIdx.x; b < 256; b += kThreads)
-            lut[b] = pack_bf16x2(e2m1_to_float(b & 15u), e2m1_to_float(b >> 4));
-    }
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kRawStages; ++i) {
             mbar_init(raw_full(i), 1);
@@ -399,8 +440,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const uint8_t* rw = smem + L::kRawOff + r * L::kRawBytes;
                 uint8_t* dst = smem + L::kBfOff + b * L::kBfBytes;
-                convert_row<MODE>(rw + c * C::kWRaw, s0, lut, dst, c);
-                convert_row<MODE>(rw + kWR * C::kWRaw + c * C::kWRaw, s1, lut, dst + kWR * 128, c);
+                convert_row<MODE>(rw, s0, dst, c);
+                convert_row<MODE>(rw + kWR * C::kWRaw, s1, dst + kWR * 128, c);
                 fence_proxy_async_smem();
                 mbar_arrive(raw_empty(r));
                 mbar_arrive(bf_full(b));
@@ -540,7 +581,7 @@ cudaError_t launch_wm(const Plan& p, const void* w, const void* w_scale, const f
     const int planes = MODE == MOE_A8W8_INT8 ? 2 : 1;
     CUtensorMap tmW, tmX;
     if (!tc_make_map_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w, (uint64_t)kin_bytes, (uint64_t)p.E * n_out,
-                        C::kWRaw, kWR, CU_TENSOR_MAP_SWIZZLE_NONE))
+                        C::kWRaw, kWR, C::kWRaw == 32 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
     if (!tc_make_map_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kL1 ? (const void*)p.x_bf16 : (const void*)p.a_bf16,
                         (uint64_t)kin, (uint64_t)planes * p.pool_rows, kBK, kTokBox, CU_TENSOR_MAP_SWIZZLE_128B))
