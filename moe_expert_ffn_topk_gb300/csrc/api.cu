@@ -76,7 +76,7 @@ moe_status layout(const moe_dims* d, moe_dtype_mode m, moe_workspace_layout_t* o
     L.a_pool = take((size_t)pool_rows * I * a_elem_bytes(m));
     L.a_pool_scale = take((size_t)pool_rows * a_scale_row_bytes(m, (int)I));
     L.a_f32 = take(m == MOE_A8W8_INT8 ? (size_t)pool_rows * I * 4 : 0);
-    const int planes = m == MOE_A16W16 ? 0 : (m == MOE_A8W8_INT8 ? 2 : 1);
+    const int planes = m == MOE_A8W8_INT8 ? 2 : 0;  // the INT8 tensor-core path's hi / lo operand planes
     L.x_pool_bf16 = take((size_t)planes * pool_rows * H * 2);
     L.a_pool_bf16 = take((size_t)planes * pool_rows * I * 2);
     L.total = off;
@@ -173,6 +173,8 @@ moe_status moe_expert_l1(moe_operand w1, const moe_dims* d, moe_dtype_mode m, ui
     cudaError_t e;
     if (!(flags & MOE_FLAG_SIMT) && tc_supported(p, 1)) {
         e = launch_l1_tc(p, w1.data, w1.scale, s);
+    } else if (!(flags & MOE_FLAG_SIMT) && bs_supported(p, 1)) {
+        e = launch_l1_bs(p, w1.data, w1.scale, s);
     } else if (!(flags & MOE_FLAG_SIMT) && wm_supported(p, 1)) {
         e = launch_l1_wm(p, w1.data, w1.scale, s);
     } else {
@@ -193,6 +195,8 @@ moe_status moe_expert_l2(moe_operand w2, const float* topk_weights, const moe_di
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (!(flags & MOE_FLAG_SIMT) && tc_supported(p, 2))
         return from_cuda(launch_l2_tc(p, w2.data, w2.scale, topk_weights, s));
+    if (!(flags & MOE_FLAG_SIMT) && bs_supported(p, 2))
+        return from_cuda(launch_l2_bs(p, w2.data, w2.scale, topk_weights, s));
     if (!(flags & MOE_FLAG_SIMT) && wm_supported(p, 2))
         return from_cuda(launch_l2_wm(p, w2.data, w2.scale, topk_weights, s));
     return from_cuda(launch_l2_simt(p, w2.data, w2.scale, topk_weights, s));

@@ -215,10 +215,10 @@ __global__ void __launch_bounds__(128) dispatch_gather_q_kernel(const uint8_t* _
                 }
                 out[j] = (uint32_t)float_to_bf16_bits(f0) | ((uint32_t)float_to_bf16_bits(f1) << 16);
             }
-            uint4* dst = reinterpret_cast<uint4*>(xb + (int64_t)r * H + v * 16);
-            dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
-            dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
             if constexpr (MODE == MOE_A8W8_INT8) {
+                uint4* dst = reinterpret_cast<uint4*>(xb + (int64_t)r * H + v * 16);
+                dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
+                dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
                 uint4* lo = reinterpret_cast<uint4*>(xb + (pool_rows + r) * H + v * 16);
                 lo[0] = make_uint4(out_lo[0], out_lo[1], out_lo[2], out_lo[3]);
                 lo[1] = make_uint4(out_lo[4], out_lo[5], out_lo[6], out_lo[7]);

@@ -168,10 +168,6 @@ __global__ void __launch_bounds__(NT) l1_simt_kernel(Plan p, const uint8_t* __re
             p.a_pool[row * I + j0] = c0;
             p.a_pool[row * I + j0 + 1] = c1;
             if (tx == 0) p.a_pool_scale[row * (I / 32) + jb] = static_cast<uint8_t>(ex + 127);
-            // the same values dequantised (exact in bf16) for the tensor-core L2 GEMM
-            const float sc = ue8m0_to_float(static_cast<uint8_t>(ex + 127));
-            p.a_bf16[row * I + j0] = float_to_bf16_bits(e4m3_to_float(c0) * sc);
-            p.a_bf16[row * I + j0 + 1] = float_to_bf16_bits(e4m3_to_float(c1) * sc);
         }
     }
 }

@@ -1,0 +1,411 @@
+// Block-scaled weight-major tensor-core grouped GEMM for the FP8 modes (A8W8-FP8: e4m3 weights,
+// A8W4: e2m1 weights; e4m3 tokens in both), on tcgen05.mma kind::mxf8f6f4.block_scale: the
+// tensor core consumes the stored codes and applies one UE8M0 scale per 32 elements of K to
+// each operand, so nothing is dequantised in software (the Ascend mega_moe page, A8W8-FP use
+// case: "DQ_MX ... implicitly performed inside matmul"; DeepGEMM page §4 step 5: block-scaled
+// MMA with UE8M0 scale factors in tensor memory).
+//
+// Orientation and tiles as in the weight-major kernel: M = 128 weight rows per block, two blocks
+// per tile (L1: the gate and the up rows of the same 128 outputs; L2: 256 hidden columns), N =
+// the tokens of one expert's 128-row tile rounded up to 16, K = 128 per stage (4 MMAs of K=32).
+//
+// Operand staging:
+// - weights: TMA, 128-byte swizzle; e2m1 uses the 16U4_ALIGN16B element type, which expands
+//   each packed 8-byte group of 16 codes into a 16-byte slot (the padded layout the MMA reads
+//   for 4-bit operands); e4m3 weights are plain bytes.
+// - tokens: TMA of the pool's e4m3 codes (x for L1, the re-quantised A for L2) in boxes of 16 rows.
+// - scales: four "scale warps" write the stage's UE8M0 bytes into tensor memory with tcgen05.st.
+//   Layout read by the MMA (measured on this GPU): the scale of A row r is in TMEM lane r,
+//   column base + r/32, byte = the K-group (a_sf_id); the scale of B row n is in lane
+//   32*q + n%32 of every lane quarter q, column base + n/32, byte = b_sf_id. Each 32-bit word
+//   holds the 4 scales of one row for the stage's 4 K-groups.
+//
+// Warp roles (320 threads): 0 TMA producer, 1 TMEM allocation + MMA issuer, 2-5 epilogue,
+// 6-9 scale writers. Tensor memory: columns [0, 256) hold the two 128 x N accumulators (one
+// buffer), [256, 256 + 16*stages) the scale ring. Every wait is bounded; on time-out the CTA
+// records MOE_ERR_TIMEOUT, drains and exits.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc_common.cuh"
+
+namespace moe {
+
+namespace {
+
+using namespace tc;
+
+constexpr int kWR = 128;          // weight rows per block (MMA M)
+constexpr int kTok = 128;         // tokens per tile
+constexpr int kBK = 128;          // K per stage
+constexpr int kTokBox = 16;       // token rows per TMA box
+constexpr int kStages = 4;
+constexpr int kThreads = 320;
+constexpr int kMaxExperts = 1024;
+constexpr int kABlockBytes = kWR * 128;            // one 128-row block, 128 smem bytes per row
+constexpr int kABytes = 2 * kABlockBytes;
+constexpr int kBBytes = kTok * 128;
+constexpr int kStageBytes = kABytes + kBBytes;     // 48 KB
+constexpr int kSfCol0 = 256;                       // first TMEM column of the scale ring
+constexpr int kSfColsPerStage = 16;                // SFA block 0 (4), SFA block 1 (4), SFB (4), spare
+constexpr int kLookahead = 3;                      // scale loads issued this many stages ahead
+
+constexpr int kBarOff = kStages * kStageBytes;
+constexpr int kNumBars = 2 * kStages + 2 + 1;
+constexpr int kMiscOff = kBarOff + 8 * kNumBars;
+constexpr int kTileOffOff = kMiscOff + 16;
+constexpr int kCountsOff = kTileOffOff + 4 * (kMaxExperts + 1);
+constexpr size_t kSmem = 1024 + (size_t)kCountsOff + 4 * kMaxExperts;
+
+struct BsArgs {
+    Plan p;
+    const uint8_t* w_scale;     // UE8M0 [E*n_out][kin/32]
+    const float* topk_weights;  // L2
+    int n_slabs, k_blocks, n_out, kin;
+};
+
+struct Tile {
+    int e, s, m, row0;
+};
+
+__device__ __forceinline__ Tile decode(int t, const int* tile_off, int E, int n_slabs) {
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (tile_off[mid] * n_slabs <= t) lo = mid; else hi = mid - 1;
+    }
+    Tile tl;
+    tl.e = lo;
+    const int mt = tile_off[lo + 1] - tile_off[lo];
+    const int local = t - tile_off[lo] * n_slabs;
+    tl.s = local / mt;
+    tl.m = local % mt;
+    tl.row0 = (tile_off[lo] + tl.m) * kTok;
+    return tl;
+}
+
+// Instruction descriptor of kind::mxf8f6f4.block_scale: B scale-factor id (bits 4-5), A and B
+// element types (7-9, 10-12: e4m3 = 0, e2m1 = 5), both K-major, N >> 3 (17-22), scale type
+// UE8M0 (bit 23), M >> 4 (24-28), A scale-factor id (29-30).
+__device__ __forceinline__ uint32_t bs_idesc(uint32_t afmt, int n, int sf_id) {
+    return ((uint32_t)sf_id << 4) | (afmt << 7) | (0u << 10) | ((uint32_t)(n >> 3) << 17) | (1u << 23) |
+           ((uint32_t)(kWR >> 4) << 24) | ((uint32_t)sf_id << 29);
+}
+
+__device__ __forceinline__ void tc_mma_bs(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa,
+                                          uint32_t sfb, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        ::"r"(d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+template <int MODE, bool kL1>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_bs_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, BsArgs args) {
+    constexpr bool kFp4 = MODE == MOE_A8W4_FP8_FP4;
+    constexpr uint32_t kAfmt = kFp4 ? 5u : 0u;
+    constexpr uint32_t kABoxTx = kFp4 ? kWR * kBK / 2 : kWR * kBK;  // TMA counts the packed global bytes
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_base = smem_u32(smem_raw);
+    const uint32_t base = (raw_base + 1023u) & ~1023u;
+    uint8_t* smem = smem_raw + (base - raw_base);
+    const uint32_t bars = base + kBarOff;
+    auto full_bar = [&](int s) { return bars + 8u * s; };
+    auto empty_bar = [&](int s) { return bars + 8u * (kStages + s); };
+    const uint32_t acc_full = bars + 8u * (2 * kStages), acc_empty = bars + 8u * (2 * kStages + 1);
+    const uint32_t drain_bar = bars + 8u * (2 * kStages + 2);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kMiscOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
+    int* tile_off = reinterpret_cast<int*>(smem + kTileOffOff);
+    int* counts = reinterpret_cast<int*>(smem + kCountsOff);
+
+    const Plan& p = args.p;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i <= p.E; i += kThreads) tile_off[i] = p.tile_off[i];
+    for (int i = threadIdx.x; i < p.E; i += kThreads) counts[i] = p.counts[i];
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full_bar(s), 1 + 128);  // TMA (arrive + bytes) + 128 scale writers
+            mbar_init(empty_bar(s), 1);
+        }
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, 4);
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) tmem_alloc(smem_u32(tmem_holder), 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    const int total = tile_off[p.E] * args.n_slabs;
+    const int KB = args.k_blocks;
+    const int I = p.I, H = p.H;
+    auto n_valid_of = [&](const Tile& tl) { return min(kTok, counts[tl.e] - tl.m * kTok); };
+    auto wrow0 = [&](const Tile& tl) { return tl.e * args.n_out + (kL1 ? tl.s * kWR : tl.s * 2 * kWR); };
+    auto wrow1 = [&](const Tile& tl) { return kL1 ? wrow0(tl) + I : wrow0(tl) + kWR; };
+
+    if (warp == 0) {
+        // ---------------- TMA producer: weights (2 blocks) and tokens ----------------
+        if (lane == 0) {
+            int it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                const Tile tl = decode(t, tile_off, p.E, args.n_slabs);
+                const int n = (n_valid_of(tl) + 15) & ~15;
+                const int w0 = wrow0(tl), w1 = wrow1(tl);
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const int s = it % kStages;
+                    if (!mbar_wait(empty_bar(s), ((uint32_t)(it / kStages) & 1u) ^ 1u, p.hdr, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = base + s * kStageBytes, sb = sa + kABytes;
+                    mbar_arrive_expect_tx(full_bar(s), 2 * kABoxTx + (uint32_t)n * 128u);
+                    tma_load_2d(sa, &tmW, kb * kBK, w0, full_bar(s));
+                    tma_load_2d(sa + kABlockBytes, &tmW, kb * kBK, w1, full_bar(s));
+                    for (int i = 0; i < n / kTokBox; ++i)
+                        tma_load_2d(sb + i * kTokBox * 128, &tmX, kb * kBK, tl.row0 + i * kTokBox, full_bar(s));
+                }
+            }
+            for (int j = it - kStages < 0 ? 0 : it - kStages; j < it; ++j)
+                mbar_drain(full_bar(j % kStages), (uint32_t)(j / kStages) & 1u, p.hdr);
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            int it = 0, tc = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tc) {
+                if (!mbar_wait(acc_empty, ((uint32_t)tc & 1u) ^ 1u, p.hdr, abort_flag)) break;
+                tc_fence_after();
+                const Tile tl = decode(t, tile_off, p.E, args.n_slabs);
+                const int n = (n_valid_of(tl) + 15) & ~15;
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const int s = it % kStages;
+                    if (!mbar_wait(full_bar(s), (uint32_t)(it / kStages) & 1u, p.hdr, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = base + s * kStageBytes, sb = sa + kABytes;
+                    const uint32_t sf = tmem_base + kSfCol0 + s * kSfColsPerStage;
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 32; ++kk) {
+                        const uint32_t idesc = bs_idesc(kAfmt, n, kk);
+                        const uint64_t bd = kmajor_desc(sb, kk);
+                        tc_mma_bs(tmem_base, kmajor_desc(sa, kk), bd, idesc, sf, sf + 8, (kb | kk) != 0);
+                        tc_mma_bs(tmem_base + kWR, kmajor_desc(sa + kABlockBytes, kk), bd, idesc, sf + 4, sf + 8,
+                                  (kb | kk) != 0);
+                    }
+                    tc_commit(empty_bar(s));
+                }
+                if (ok) tc_commit(acc_full);
+            }
+            tc_commit(drain_bar);
+            mbar_drain(drain_bar, 0, p.hdr);
+        }
+    } else if (warp >= 6) {
+        // ---------------- scale writers ----------------
+        const int q = warp & 3;  // lane quarter this warp writes
+        const int spr = args.kin / 32;
+        // scale words of one stage: SFA rows 32q+lane of both blocks, SFB tokens 32c+lane
+        struct Words {
+            uint32_t a0, a1, b[4];
+        };
+        auto load_words = [&](int t, int kb) {
+            Words w;
+            const Tile tl = decode(t, tile_off, p.E, args.n_slabs);
+            const int nv = n_valid_of(tl);
+            w.a0 = __ldg(reinterpret_cast<const uint32_t*>(args.w_scale + (int64_t)(wrow0(tl) + 32 * q + lane) * spr) + kb);
+            w.a1 = __ldg(reinterpret_cast<const uint32_t*>(args.w_scale + (int64_t)(wrow1(tl) + 32 * q + lane) * spr) + kb);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int n = 32 * c + lane;
+                uint32_t v = 0x7f7f7f7fu;  // 1.0 for the padding tokens
+                if (n < nv) {
+                    const int64_t row = tl.row0 + n;
+                    if constexpr (kL1 && kFp4) {
+                        const uint32_t bits = __float_as_uint(reinterpret_cast<const float*>(p.x_pool_scale)[row * (H / 128) + kb]);
+                        v = ((bits >> 23) & 0xffu) * 0x01010101u;  // power-of-two scale -> its UE8M0 byte, x4
+                    } else if constexpr (kL1) {
+                        v = __ldg(reinterpret_cast<const uint32_t*>(p.x_pool_scale + row * (H / 32)) + kb);
+                    } else {
+                        v = __ldg(reinterpret_cast<const uint32_t*>(p.a_pool_scale + row * (I / 32)) + kb);
+                    }
+                }
+                w.b[c] = v;
+            }
+            return w;
+        };
+        // a lookahead iterator over the same (tile, k-block) sequence as the producer
+        int lt = blockIdx.x, lkb = 0;
+        auto advance = [&]() {
+            if (++lkb == KB) {
+                lkb = 0;
+                lt += gridDim.x;
+            }
+        };
+        Words ring[kLookahead];
+#pragma unroll
+        for (int i = 0; i < kLookahead; ++i) {
+            if (lt < total) ring[i] = load_words(lt, lkb);
+            advance();
+        }
+        int it = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            for (int kb = 0; kb < KB; ++kb, ++it) {
+                const Words w = ring[0];
+#pragma unroll
+                for (int i = 0; i + 1 < kLookahead; ++i) ring[i] = ring[i + 1];
+                if (lt < total) ring[kLookahead - 1] = load_words(lt, lkb);
+                advance();
+                const int s = it % kStages;
+                const bool w_ok = mbar_wait(empty_bar(s), ((uint32_t)(it / kStages) & 1u) ^ 1u, p.hdr, abort_flag);
+                if (!__all_sync(0xffffffffu, w_ok)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t sf = tmem_base + ((uint32_t)(32 * q) << 16) + kSfCol0 + s * kSfColsPerStage;
+                tmem_st1(sf + q, w.a0);
+                tmem_st1(sf + 4 + q, w.a1);
+                tmem_st4(sf + 8, w.b[0], w.b[1], w.b[2], w.b[3]);
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(full_bar(s));
+            }
+        }
+    } else {
+        // ---------------- epilogue (warps 2..5) ----------------
+        const int q = warp & 3;
+        int tc = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x, ++tc) {
+            const bool w_ok = mbar_wait(acc_full, (uint32_t)tc & 1u, p.hdr, abort_flag);
+            if (!__all_sync(0xffffffffu, w_ok)) break;
+            tc_fence_after();
+            const Tile tl = decode(t, tile_off, p.E, args.n_slabs);
+            const int n_valid = n_valid_of(tl);
+            const int n = (n_valid + 15) & ~15;
+            const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16);
+            if constexpr (kL1) {
+                const int j = tl.s * kWR + q * 32 + lane;
+                for (int c0 = 0; c0 < n; c0 += 32) {
+                    uint32_t g[32], u[32];
+                    tmem_ld32(tb + c0, g);
+                    tmem_ld32(tb + kWR + c0, u);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int tt = 0; tt < 32; ++tt) {
+                        if (c0 + tt >= n) break;  // uniform across the warp
+                        const float av = silu(__uint_as_float(g[tt])) * __uint_as_float(u[tt]);
+                        float amax = fabsf(av);
+#pragma unroll
+                        for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+                        const int ex = mx_exponent_e4m3(amax);
+                        const int64_t row = tl.row0 + c0 + tt;
+                        p.a_pool[row * I + j] = float_to_e4m3_satfinite(av * exp2_neg_int(ex));
+                        if (lane == 0) p.a_pool_scale[row * (I / 32) + (tl.s * kWR + q * 32) / 32] = (uint8_t)(ex + 127);
+                    }
+                }
+            } else {
+                for (int c0 = 0; c0 < n_valid; c0 += 32) {
+                    const int src_l = c0 + lane < n_valid ? p.pool_src[tl.row0 + c0 + lane] : -1;
+                    const float g_l = src_l >= 0 ? args.topk_weights[src_l] : 0.0f;
+#pragma unroll 1
+                    for (int blk = 0; blk < 2; ++blk) {
+                        const int h = tl.s * 2 * kWR + blk * kWR + q * 32 + lane;
+                        uint32_t y[32];
+                        tmem_ld32(tb + blk * kWR + c0, y);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int tt = 0; tt < 32; ++tt) {
+                            if (c0 + tt >= n_valid) break;  // uniform across the warp
+                            const int src = __shfl_sync(0xffffffffu, src_l, tt);
+                            const float gw = __shfl_sync(0xffffffffu, g_l, tt);
+                            if (src >= 0)
+                                p.comb[(int64_t)src * H + h] = float_to_bf16_bits(__fmul_rn(gw, __uint_as_float(y[tt])));
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, 512);
+}
+
+template <int MODE, bool kL1>
+cudaError_t launch_bs(const Plan& p, const void* w, const void* w_scale, const float* topk_weights, cudaStream_t s) {
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(tc_bs_kernel<MODE, kL1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    const int n_out = kL1 ? 2 * p.I : p.H;
+    const int kin = kL1 ? p.H : p.I;
+    CUtensorMap tmW, tmX;
+    const bool ok_w = MODE == MOE_A8W4_FP8_FP4
+                          ? tc_make_map_2d_packed4(&tmW, w, (uint64_t)kin, (uint64_t)p.E * n_out, kBK, kWR)
+                          : tc_make_map_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w, (uint64_t)kin,
+                                           (uint64_t)p.E * n_out, kBK, kWR, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!ok_w) return cudaErrorInvalidValue;
+    if (!tc_make_map_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kL1 ? (const void*)p.x_pool : (const void*)p.a_pool,
+                        (uint64_t)kin, (uint64_t)p.pool_rows, kBK, kTokBox, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    BsArgs args{p, static_cast<const uint8_t*>(w_scale), topk_weights, kL1 ? p.I / kWR : p.H / (2 * kWR), kin / kBK,
+                n_out, kin};
+    const int64_t max_tiles = (p.pool_rows / kTok) * args.n_slabs;
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(max_tiles, tc_num_sms()));
+    tc_bs_kernel<MODE, kL1><<<grid, kThreads, kSmem, s>>>(tmW, tmX, args);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool bs_supported(const Plan& p, int stage) {
+    if ((p.mode != MOE_A8W8_FP8 && p.mode != MOE_A8W4_FP8_FP4) || p.E > kMaxExperts || !tc_encode_available())
+        return false;
+    if (stage == 1) return p.I % kWR == 0 && p.H % kBK == 0;
+    return p.H % (2 * kWR) == 0 && p.I % kBK == 0;
+}
+
+cudaError_t launch_l1_bs(const Plan& p, const void* w1, const void* w1_scale, cudaStream_t s) {
+    if (p.mode == MOE_A8W4_FP8_FP4) return launch_bs<MOE_A8W4_FP8_FP4, true>(p, w1, w1_scale, nullptr, s);
+    if (p.mode == MOE_A8W8_FP8) return launch_bs<MOE_A8W8_FP8, true>(p, w1, w1_scale, nullptr, s);
+    return cudaErrorNotSupported;
+}
+
+cudaError_t launch_l2_bs(const Plan& p, const void* w2, const void* w2_scale, const float* topk_weights, cudaStream_t s) {
+    if (p.mode == MOE_A8W4_FP8_FP4) return launch_bs<MOE_A8W4_FP8_FP4, false>(p, w2, w2_scale, topk_weights, s);
+    if (p.mode == MOE_A8W8_FP8) return launch_bs<MOE_A8W8_FP8, false>(p, w2, w2_scale, topk_weights, s);
+    return cudaErrorNotSupported;
+}
+
+}  // namespace moe

@@ -147,5 +147,10 @@ bool tc_make_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes,
                     uint64_t outer, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle);
 bool tc_encode_available();
 int tc_num_sms();
+// Packed e2m1 tensor [outer, inner_elems] (two codes per byte): TMA expands every 8-byte group of
+// 16 codes into a 16-byte slot of the 128-byte-swizzled shared tile (the 4-bit operand layout of
+// kind::mxf8f6f4); the transaction byte count is the packed size.
+bool tc_make_map_2d_packed4(CUtensorMap* map, const void* ptr, uint64_t inner_elems, uint64_t outer,
+                            uint32_t box_inner, uint32_t box_outer);
 
 }  // namespace moe

@@ -42,6 +42,19 @@ bool tc_make_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool tc_make_map_2d_packed4(CUtensorMap* map, const void* ptr, uint64_t inner_elems, uint64_t outer, uint32_t box_inner,
+                            uint32_t box_outer) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner_elems, outer};
+    cuuint64_t strides[1] = {inner_elems / 2};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int tc_num_sms() {
     static int n = 0;
     if (n == 0) {

@@ -1,4 +1,7 @@
-// Weight-major tensor-core grouped GEMM for the quantised modes (A8W8-FP8, FP8 x FP4, INT8).
+// Weight-major tensor-core grouped GEMM with in-kernel weight dequantisation. The INT8 mode runs
+// on it (sm_103a has no integer tcgen05.mma kind); the FP8 modes use the block-scaled kernel in
+// tc_bs_gemm.cu, and the FP8 / e2m1 converter branches below are kept as the template's other
+// instances of the same pipeline.
 //
 // Orientation: the MMA's M dimension runs over 128 weight rows and its N dimension over the
 // tokens routed to one expert (N = 16..128 per tile, or 256 for INT8, see below), so the same
@@ -60,16 +63,6 @@ constexpr int kABytes = 2 * kWR * 128;  // two 128-row bf16 weight blocks per st
 // converters by its own depth.
 template <int MODE>
 struct WmCfg;
-template <>
-struct WmCfg<MOE_A8W8_FP8> {
-    static constexpr int kWRaw = 64, kBRows = 128, kAccCols = 128, kBufs = 2;
-    static constexpr int kRawStages = 3, kBfStages = 3, kTokStages = 4;
-};
-template <>
-struct WmCfg<MOE_A8W4_FP8_FP4> {
-    static constexpr int kWRaw = 32, kBRows = 128, kAccCols = 128, kBufs = 2;
-    static constexpr int kRawStages = 6, kBfStages = 3, kTokStages = 4;
-};
 template <>
 struct WmCfg<MOE_A8W8_INT8> {
     static constexpr int kWRaw = 64, kBRows = 256, kAccCols = 256, kBufs = 1;
@@ -597,27 +590,19 @@ cudaError_t launch_wm(const Plan& p, const void* w, const void* w_scale, const f
 }  // namespace
 
 bool wm_supported(const Plan& p, int stage) {
-    if (p.mode == MOE_A16W16 || p.E > kMaxExperts || !tc_encode_available()) return false;
+    if (p.mode != MOE_A8W8_INT8 || p.E > kMaxExperts || !tc_encode_available()) return false;
     if (stage == 1) return p.I % kWR == 0 && p.H % kBK == 0;
     return p.H % (2 * kWR) == 0 && p.I % kBK == 0;
 }
 
 cudaError_t launch_l1_wm(const Plan& p, const void* w1, const void* w1_scale, cudaStream_t s) {
-    switch (p.mode) {
-        case MOE_A8W8_FP8: return launch_wm<MOE_A8W8_FP8, true>(p, w1, w1_scale, nullptr, s);
-        case MOE_A8W4_FP8_FP4: return launch_wm<MOE_A8W4_FP8_FP4, true>(p, w1, w1_scale, nullptr, s);
-        case MOE_A8W8_INT8: return launch_wm<MOE_A8W8_INT8, true>(p, w1, w1_scale, nullptr, s);
-        default: return cudaErrorNotSupported;
-    }
+    if (p.mode != MOE_A8W8_INT8) return cudaErrorNotSupported;
+    return launch_wm<MOE_A8W8_INT8, true>(p, w1, w1_scale, nullptr, s);
 }
 
 cudaError_t launch_l2_wm(const Plan& p, const void* w2, const void* w2_scale, const float* topk_weights, cudaStream_t s) {
-    switch (p.mode) {
-        case MOE_A8W8_FP8: return launch_wm<MOE_A8W8_FP8, false>(p, w2, w2_scale, topk_weights, s);
-        case MOE_A8W4_FP8_FP4: return launch_wm<MOE_A8W4_FP8_FP4, false>(p, w2, w2_scale, topk_weights, s);
-        case MOE_A8W8_INT8: return launch_wm<MOE_A8W8_INT8, false>(p, w2, w2_scale, topk_weights, s);
-        default: return cudaErrorNotSupported;
-    }
+    if (p.mode != MOE_A8W8_INT8) return cudaErrorNotSupported;
+    return launch_wm<MOE_A8W8_INT8, false>(p, w2, w2_scale, topk_weights, s);
 }
 
 }  // namespace moe
