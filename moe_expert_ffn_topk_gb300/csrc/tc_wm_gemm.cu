@@ -128,19 +128,6 @@ __device__ __forceinline__ int tile_n(int n_valid) {
     else return (n_valid + 15) & ~15;
 }
 
-// bf16 bits of 2^(s-127) for a UE8M0 byte (s = 0 is the subnormal 2^-127)
-__device__ __forceinline__ uint32_t ue8m0_bf16x2(uint32_t s) {
-    const uint32_t h = s == 0 ? 0x0040u : (s << 7);
-    return h | (h << 16);
-}
-
-__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
-    __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&a);
-    __nv_bfloat162 y = *reinterpret_cast<__nv_bfloat162*>(&b);
-    __nv_bfloat162 r = __hmul2(x, y);
-    return *reinterpret_cast<uint32_t*>(&r);
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return (uint32_t)float_to_bf16_bits(lo) | ((uint32_t)float_to_bf16_bits(hi) << 16);
 }
