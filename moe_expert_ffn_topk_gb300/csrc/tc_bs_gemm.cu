@@ -5,25 +5,29 @@
 // case: "DQ_MX ... implicitly performed inside matmul"; DeepGEMM page §4 step 5: block-scaled
 // MMA with UE8M0 scale factors in tensor memory).
 //
-// Orientation and tiles as in the weight-major kernel: M = 128 weight rows per block, two blocks
-// per tile (L1: the gate and the up rows of the same 128 outputs; L2: 256 hidden columns), N =
-// the tokens of one expert's 128-row tile rounded up to 16, K = 128 per stage (4 MMAs of K=32).
+// Tiles (M = 128 weight rows, N = tokens, K = 128 per stage as 4 MMAs of K = 32):
+// - L1: the 128 rows are 64 gate rows and the 64 up rows of the same 64 outputs of A, so the
+//   epilogue pairs lane r (gate) with lane r + 64 (up) through a small shared buffer and applies
+//   SwiGLU (Ascend page, "SwiGLU Activation") and the MX FP8 re-quantisation of A.
+// - L2: 128 rows of hidden columns.
+// - tokens: a sub-tile of kNT rows of one expert (kNT = 128 for prefill-sized experts, 32 for
+//   decode-sized ones, where the weights stream from HBM and deeper staging matters). The
+//   sub-tiles of every expert are counted in-kernel from the routed-row counts.
+// Accumulators are double-buffered in tensor memory, so the epilogue of a tile overlaps the
+// main loop of the next.
 //
-// Operand staging:
-// - weights: TMA, 128-byte swizzle; e2m1 uses the 16U4_ALIGN16B element type, which expands
-//   each packed 8-byte group of 16 codes into a 16-byte slot (the padded layout the MMA reads
-//   for 4-bit operands); e4m3 weights are plain bytes.
-// - tokens: TMA of the pool's e4m3 codes (x for L1, the re-quantised A for L2) in boxes of 16 rows.
-// - scales: four "scale warps" write the stage's UE8M0 bytes into tensor memory with tcgen05.st.
-//   Layout read by the MMA (measured on this GPU): the scale of A row r is in TMEM lane r,
-//   column base + r/32, byte = the K-group (a_sf_id); the scale of B row n is in lane
-//   32*q + n%32 of every lane quarter q, column base + n/32, byte = b_sf_id. Each 32-bit word
-//   holds the 4 scales of one row for the stage's 4 K-groups.
+// Operand staging: weights by TMA with 128-byte swizzle (e2m1 through the 16U4_ALIGN16B element
+// type, which expands each packed 8-byte group of 16 codes into a 16-byte slot: the 4-bit
+// operand layout of kind::mxf8f6f4; its transaction count is the packed size); tokens by TMA of
+// the pool's e4m3 codes in boxes of 16 rows; scales by four "scale warps" that write the stage's
+// UE8M0 bytes into tensor memory with tcgen05.st. Layout the MMA reads (measured on this GPU):
+// the scale of A row r is in TMEM lane r, column base + r/32, byte = the K group (a_sf_id); the
+// scale of B row n is in lane 32*q + n%32 of every lane quarter q, column base + n/32, byte =
+// b_sf_id; one 32-bit word holds a row's 4 scales of a stage.
 //
 // Warp roles (320 threads): 0 TMA producer, 1 TMEM allocation + MMA issuer, 2-5 epilogue,
-// 6-9 scale writers. Tensor memory: columns [0, 256) hold the two 128 x N accumulators (one
-// buffer), [256, 256 + 16*stages) the scale ring. Every wait is bounded; on time-out the CTA
-// records MOE_ERR_TIMEOUT, drains and exits.
+// 6-9 scale writers. Every wait is bounded; on time-out the CTA records MOE_ERR_TIMEOUT, drains
+// and exits.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -39,27 +43,33 @@ namespace {
 
 using namespace tc;
 
-constexpr int kWR = 128;          // weight rows per block (MMA M)
-constexpr int kTok = 128;         // tokens per tile
+constexpr int kWR = 128;          // weight rows per tile (MMA M)
+constexpr int kHalf = 64;         // L1: gate rows, then up rows
 constexpr int kBK = 128;          // K per stage
 constexpr int kTokBox = 16;       // token rows per TMA box
-constexpr int kStages = 4;
 constexpr int kThreads = 320;
 constexpr int kMaxExperts = 1024;
-constexpr int kABlockBytes = kWR * 128;            // one 128-row block, 128 smem bytes per row
-constexpr int kABytes = 2 * kABlockBytes;
-constexpr int kBBytes = kTok * 128;
-constexpr int kStageBytes = kABytes + kBBytes;     // 48 KB
-constexpr int kSfCol0 = 256;                       // first TMEM column of the scale ring
-constexpr int kSfColsPerStage = 16;                // SFA block 0 (4), SFA block 1 (4), SFB (4), spare
-constexpr int kLookahead = 3;                      // scale loads issued this many stages ahead
+constexpr int kABytes = kWR * 128;
+constexpr int kSfCol0 = 256;      // first TMEM column of the scale ring
+constexpr int kSfColsPerStage = 8;  // SFA 4 columns, SFB up to 4 columns
+constexpr int kLookahead = 3;     // scale loads issued this many stages ahead
+constexpr int kEpiBar = 1;        // named barrier of the 4 epilogue warps
 
-constexpr int kBarOff = kStages * kStageBytes;
-constexpr int kNumBars = 2 * kStages + 2 + 1;
-constexpr int kMiscOff = kBarOff + 8 * kNumBars;
-constexpr int kTileOffOff = kMiscOff + 16;
-constexpr int kCountsOff = kTileOffOff + 4 * (kMaxExperts + 1);
-constexpr size_t kSmem = 1024 + (size_t)kCountsOff + 4 * kMaxExperts;
+template <int kNT, int kStages>
+struct BsCfg {
+    static constexpr int kBBytes = kNT * 128;
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kBarOff = kStages * kStageBytes;
+    static constexpr int kNumBars = 2 * kStages + 4 + 1;
+    static constexpr int kXbufOff = kBarOff + 8 * kNumBars;           // 32 tokens x 64 up values (fp32)
+    static constexpr int kMiscOff = kXbufOff + 32 * kHalf * 4;
+    static constexpr int kTileOffOff = kMiscOff + 16;                 // int[E+1] 128-row tiles per expert
+    static constexpr int kSubOffOff = kTileOffOff + 4 * (kMaxExperts + 1);   // int[E+1] kNT sub-tiles
+    static constexpr int kCountsOff = kSubOffOff + 4 * (kMaxExperts + 1);    // int[E]
+    static constexpr size_t kSmem = 1024 + (size_t)kCountsOff + 4 * kMaxExperts;
+    static_assert(kSmem <= 232448, "shared memory");
+    static_assert(2 * kNT <= kSfCol0 && kSfCol0 + kStages * kSfColsPerStage <= 512, "tensor memory");
+};
 
 struct BsArgs {
     Plan p;
@@ -69,22 +79,26 @@ struct BsArgs {
 };
 
 struct Tile {
-    int e, s, m, row0;
+    int e, s, row0, n_valid;
 };
 
-__device__ __forceinline__ Tile decode(int t, const int* tile_off, int E, int n_slabs) {
+// Tiles are ordered expert-major, then weight slab, then token sub-tile.
+template <int kNT>
+__device__ __forceinline__ Tile decode(int t, const int* sub_off, const int* tile_off, const int* counts, int E,
+                                       int n_slabs) {
     int lo = 0, hi = E - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (tile_off[mid] * n_slabs <= t) lo = mid; else hi = mid - 1;
+        if (sub_off[mid] * n_slabs <= t) lo = mid; else hi = mid - 1;
     }
     Tile tl;
     tl.e = lo;
-    const int mt = tile_off[lo + 1] - tile_off[lo];
-    const int local = t - tile_off[lo] * n_slabs;
-    tl.s = local / mt;
-    tl.m = local % mt;
-    tl.row0 = (tile_off[lo] + tl.m) * kTok;
+    const int ns = sub_off[lo + 1] - sub_off[lo];
+    const int local = t - sub_off[lo] * n_slabs;
+    tl.s = local / ns;
+    const int j = local % ns;
+    tl.row0 = tile_off[lo] * 128 + j * kNT;
+    tl.n_valid = min(kNT, counts[lo] - j * kNT);
     return tl;
 }
 
@@ -109,44 +123,63 @@ __device__ __forceinline__ void tc_mma_bs(uint32_t d, uint64_t adesc, uint64_t b
 __device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
 }
-__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a), "r"(b), "r"(c),
-                 "r"(d)
-                 : "memory");
-}
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync %0, 128;" ::"n"(kEpiBar) : "memory"); }
 
-template <int MODE, bool kL1>
+template <int MODE, bool kL1, int kNT, int kStages>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bs_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, BsArgs args) {
+    using Cfg = BsCfg<kNT, kStages>;
     constexpr bool kFp4 = MODE == MOE_A8W4_FP8_FP4;
     constexpr uint32_t kAfmt = kFp4 ? 5u : 0u;
-    constexpr uint32_t kABoxTx = kFp4 ? kWR * kBK / 2 : kWR * kBK;  // TMA counts the packed global bytes
+    constexpr uint32_t kABoxTx = kFp4 ? kHalf * kBK / 2 : kHalf * kBK;  // TMA counts the packed global bytes
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = smem_u32(smem_raw);
     const uint32_t base = (raw_base + 1023u) & ~1023u;
     uint8_t* smem = smem_raw + (base - raw_base);
-    const uint32_t bars = base + kBarOff;
+    const uint32_t bars = base + Cfg::kBarOff;
     auto full_bar = [&](int s) { return bars + 8u * s; };
     auto empty_bar = [&](int s) { return bars + 8u * (kStages + s); };
-    const uint32_t acc_full = bars + 8u * (2 * kStages), acc_empty = bars + 8u * (2 * kStages + 1);
-    const uint32_t drain_bar = bars + 8u * (2 * kStages + 2);
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kMiscOff);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
-    int* tile_off = reinterpret_cast<int*>(smem + kTileOffOff);
-    int* counts = reinterpret_cast<int*>(smem + kCountsOff);
+    auto acc_full = [&](int a) { return bars + 8u * (2 * kStages + a); };
+    auto acc_empty = [&](int a) { return bars + 8u * (2 * kStages + 2 + a); };
+    const uint32_t drain_bar = bars + 8u * (2 * kStages + 4);
+    float* xbuf = reinterpret_cast<float*>(smem + Cfg::kXbufOff);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kMiscOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kMiscOff + 4);
+    int* tile_off = reinterpret_cast<int*>(smem + Cfg::kTileOffOff);
+    int* sub_off = reinterpret_cast<int*>(smem + Cfg::kSubOffOff);
+    int* counts = reinterpret_cast<int*>(smem + Cfg::kCountsOff);
 
     const Plan& p = args.p;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int i = threadIdx.x; i <= p.E; i += kThreads) tile_off[i] = p.tile_off[i];
     for (int i = threadIdx.x; i < p.E; i += kThreads) counts[i] = p.counts[i];
-    if (threadIdx.x == 0) {
+    if (warp == 0) {
+        // sub-tiles of kNT tokens per expert, exclusive prefix over the experts
+        int carry = 0;
+        for (int b = 0; b < p.E; b += 32) {
+            const int e = b + lane;
+            const int v = e < p.E ? (p.counts[e] + kNT - 1) / kNT : 0;
+            int x = v;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, d);
+                if (lane >= d) x += y;
+            }
+            if (e < p.E) sub_off[e] = carry + x - v;
+            carry += __shfl_sync(0xffffffffu, x, 31);
+        }
+        if (lane == 0) sub_off[p.E] = carry;
+    }
+    if (threadIdx.x == 32) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(full_bar(s), 1 + 128);  // TMA (arrive + bytes) + 128 scale writers
             mbar_init(empty_bar(s), 1);
         }
-        mbar_init(acc_full, 1);
-        mbar_init(acc_empty, 4);
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(acc_full(a), 1);
+            mbar_init(acc_empty(a), 4);
+        }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -157,32 +190,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
 
-    const int total = tile_off[p.E] * args.n_slabs;
+    const int total = sub_off[p.E] * args.n_slabs;
     const int KB = args.k_blocks;
     const int I = p.I, H = p.H;
-    auto n_valid_of = [&](const Tile& tl) { return min(kTok, counts[tl.e] - tl.m * kTok); };
-    auto wrow0 = [&](const Tile& tl) { return tl.e * args.n_out + (kL1 ? tl.s * kWR : tl.s * 2 * kWR); };
-    auto wrow1 = [&](const Tile& tl) { return kL1 ? wrow0(tl) + I : wrow0(tl) + kWR; };
+    auto tile_of = [&](int t) { return decode<kNT>(t, sub_off, tile_off, counts, p.E, args.n_slabs); };
+    // first global weight row of each 64-row half of the tile
+    auto wrow = [&](const Tile& tl, int half) {
+        if (kL1) return tl.e * args.n_out + (half ? I : 0) + tl.s * kHalf;
+        return tl.e * args.n_out + tl.s * kWR + half * kHalf;
+    };
 
     if (warp == 0) {
-        // ---------------- TMA producer: weights (2 blocks) and tokens ----------------
+        // ---------------- TMA producer: weights (two 64-row boxes) and tokens ----------------
         if (lane == 0) {
             int it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const Tile tl = decode(t, tile_off, p.E, args.n_slabs);
-                const int n = (n_valid_of(tl) + 15) & ~15;
-                const int w0 = wrow0(tl), w1 = wrow1(tl);
+                const Tile tl = tile_of(t);
+                const int n = (tl.n_valid + 15) & ~15;
+                const int w0 = wrow(tl, 0), w1 = wrow(tl, 1);
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int s = it % kStages;
                     if (!mbar_wait(empty_bar(s), ((uint32_t)(it / kStages) & 1u) ^ 1u, p.hdr, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t sa = base + s * kStageBytes, sb = sa + kABytes;
+                    const uint32_t sa = base + s * Cfg::kStageBytes, sb = sa + kABytes;
                     mbar_arrive_expect_tx(full_bar(s), 2 * kABoxTx + (uint32_t)n * 128u);
                     tma_load_2d(sa, &tmW, kb * kBK, w0, full_bar(s));
-                    tma_load_2d(sa + kABlockBytes, &tmW, kb * kBK, w1, full_bar(s));
+                    tma_load_2d(sa + kHalf * 128, &tmW, kb * kBK, w1, full_bar(s));
                     for (int i = 0; i < n / kTokBox; ++i)
                         tma_load_2d(sb + i * kTokBox * 128, &tmX, kb * kBK, tl.row0 + i * kTokBox, full_bar(s));
                 }
@@ -196,10 +232,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             int it = 0, tc = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tc) {
-                if (!mbar_wait(acc_empty, ((uint32_t)tc & 1u) ^ 1u, p.hdr, abort_flag)) break;
+                const int a = tc & 1;
+                if (!mbar_wait(acc_empty(a), ((uint32_t)(tc >> 1) & 1u) ^ 1u, p.hdr, abort_flag)) break;
                 tc_fence_after();
-                const Tile tl = decode(t, tile_off, p.E, args.n_slabs);
-                const int n = (n_valid_of(tl) + 15) & ~15;
+                const Tile tl = tile_of(t);
+                const int n = (tl.n_valid + 15) & ~15;
+                const uint32_t d = tmem_base + (uint32_t)(a * kNT);
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int s = it % kStages;
                     if (!mbar_wait(full_bar(s), (uint32_t)(it / kStages) & 1u, p.hdr, abort_flag)) {
@@ -207,19 +245,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = base + s * kStageBytes, sb = sa + kABytes;
+                    const uint32_t sa = base + s * Cfg::kStageBytes, sb = sa + kABytes;
                     const uint32_t sf = tmem_base + kSfCol0 + s * kSfColsPerStage;
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 32; ++kk) {
-                        const uint32_t idesc = bs_idesc(kAfmt, n, kk);
-                        const uint64_t bd = kmajor_desc(sb, kk);
-                        tc_mma_bs(tmem_base, kmajor_desc(sa, kk), bd, idesc, sf, sf + 8, (kb | kk) != 0);
-                        tc_mma_bs(tmem_base + kWR, kmajor_desc(sa + kABlockBytes, kk), bd, idesc, sf + 4, sf + 8,
+                    for (int kk = 0; kk < kBK / 32; ++kk)
+                        tc_mma_bs(d, kmajor_desc(sa, kk), kmajor_desc(sb, kk), bs_idesc(kAfmt, n, kk), sf, sf + 4,
                                   (kb | kk) != 0);
-                    }
                     tc_commit(empty_bar(s));
                 }
-                if (ok) tc_commit(acc_full);
+                if (ok) tc_commit(acc_full(a));
             }
             tc_commit(drain_bar);
             mbar_drain(drain_bar, 0, p.hdr);
@@ -228,21 +262,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------- scale writers ----------------
         const int q = warp & 3;  // lane quarter this warp writes
         const int spr = args.kin / 32;
-        // scale words of one stage: SFA rows 32q+lane of both blocks, SFB tokens 32c+lane
+        const int r = 32 * q + lane;  // weight row within the tile
         struct Words {
-            uint32_t a0, a1, b[4];
+            uint32_t a, b[kNT / 32];
         };
         auto load_words = [&](int t, int kb) {
             Words w;
-            const Tile tl = decode(t, tile_off, p.E, args.n_slabs);
-            const int nv = n_valid_of(tl);
-            w.a0 = __ldg(reinterpret_cast<const uint32_t*>(args.w_scale + (int64_t)(wrow0(tl) + 32 * q + lane) * spr) + kb);
-            w.a1 = __ldg(reinterpret_cast<const uint32_t*>(args.w_scale + (int64_t)(wrow1(tl) + 32 * q + lane) * spr) + kb);
+            const Tile tl = tile_of(t);
+            const int wr = wrow(tl, r >= kHalf) + (r & (kHalf - 1));
+            w.a = __ldg(reinterpret_cast<const uint32_t*>(args.w_scale + (int64_t)wr * spr) + kb);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < kNT / 32; ++c) {
                 const int n = 32 * c + lane;
                 uint32_t v = 0x7f7f7f7fu;  // 1.0 for the padding tokens
-                if (n < nv) {
+                if (n < tl.n_valid) {
                     const int64_t row = tl.row0 + n;
                     if constexpr (kL1 && kFp4) {
                         const uint32_t bits = __float_as_uint(reinterpret_cast<const float*>(p.x_pool_scale)[row * (H / 128) + kb]);
@@ -257,8 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             return w;
         };
-        // a lookahead iterator over the same (tile, k-block) sequence as the producer
-        int lt = blockIdx.x, lkb = 0;
+        int lt = blockIdx.x, lkb = 0;  // lookahead iterator over the producer's (tile, k-block) sequence
         auto advance = [&]() {
             if (++lkb == KB) {
                 lkb = 0;
@@ -287,9 +319,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 const uint32_t sf = tmem_base + ((uint32_t)(32 * q) << 16) + kSfCol0 + s * kSfColsPerStage;
-                tmem_st1(sf + q, w.a0);
-                tmem_st1(sf + 4 + q, w.a1);
-                tmem_st4(sf + 8, w.b[0], w.b[1], w.b[2], w.b[3]);
+                tmem_st1(sf + q, w.a);
+#pragma unroll
+                for (int c = 0; c < kNT / 32; ++c) tmem_st1(sf + 4 + c, w.b[c]);
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(full_bar(s));
@@ -300,57 +332,63 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3;
         int tc = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++tc) {
-            const bool w_ok = mbar_wait(acc_full, (uint32_t)tc & 1u, p.hdr, abort_flag);
+            const int a = tc & 1;
+            const bool w_ok = mbar_wait(acc_full(a), (uint32_t)(tc >> 1) & 1u, p.hdr, abort_flag);
             if (!__all_sync(0xffffffffu, w_ok)) break;
             tc_fence_after();
-            const Tile tl = decode(t, tile_off, p.E, args.n_slabs);
-            const int n_valid = n_valid_of(tl);
-            const int n = (n_valid + 15) & ~15;
-            const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16);
+            const Tile tl = tile_of(t);
+            const int n = (tl.n_valid + 15) & ~15;
+            const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * kNT);
             if constexpr (kL1) {
-                const int j = tl.s * kWR + q * 32 + lane;
+                // lanes 0-63: gate rows, lanes 64-127: up rows of the same 64 outputs j
+                const bool gate = q < 2;
+                const int jl = 32 * (q & 1) + lane;  // output within the tile
+                const int j = tl.s * kHalf + jl;
                 for (int c0 = 0; c0 < n; c0 += 32) {
-                    uint32_t g[32], u[32];
-                    tmem_ld32(tb + c0, g);
-                    tmem_ld32(tb + kWR + c0, u);
+                    uint32_t v[32];
+                    tmem_ld32(tb + c0, v);
+                    tmem_ld_wait();
+                    if (!gate) {
+#pragma unroll
+                        for (int tt = 0; tt < 32; ++tt) xbuf[tt * kHalf + jl] = __uint_as_float(v[tt]);
+                    }
+                    epi_sync();
+                    if (gate) {
+#pragma unroll
+                        for (int tt = 0; tt < 32; ++tt) {
+                            if (c0 + tt >= n) break;  // uniform across the warp
+                            const float av = silu(__uint_as_float(v[tt])) * xbuf[tt * kHalf + jl];
+                            float amax = fabsf(av);
+#pragma unroll
+                            for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+                            const int ex = mx_exponent_e4m3(amax);
+                            const int64_t row = tl.row0 + c0 + tt;
+                            p.a_pool[row * I + j] = float_to_e4m3_satfinite(av * exp2_neg_int(ex));
+                            if (lane == 0) p.a_pool_scale[row * (I / 32) + (j >> 5)] = (uint8_t)(ex + 127);
+                        }
+                    }
+                    epi_sync();
+                }
+            } else {
+                const int h = tl.s * kWR + q * 32 + lane;
+                for (int c0 = 0; c0 < tl.n_valid; c0 += 32) {
+                    const int src_l = c0 + lane < tl.n_valid ? p.pool_src[tl.row0 + c0 + lane] : -1;
+                    const float g_l = src_l >= 0 ? args.topk_weights[src_l] : 0.0f;
+                    uint32_t y[32];
+                    tmem_ld32(tb + c0, y);
                     tmem_ld_wait();
 #pragma unroll
                     for (int tt = 0; tt < 32; ++tt) {
-                        if (c0 + tt >= n) break;  // uniform across the warp
-                        const float av = silu(__uint_as_float(g[tt])) * __uint_as_float(u[tt]);
-                        float amax = fabsf(av);
-#pragma unroll
-                        for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-                        const int ex = mx_exponent_e4m3(amax);
-                        const int64_t row = tl.row0 + c0 + tt;
-                        p.a_pool[row * I + j] = float_to_e4m3_satfinite(av * exp2_neg_int(ex));
-                        if (lane == 0) p.a_pool_scale[row * (I / 32) + (tl.s * kWR + q * 32) / 32] = (uint8_t)(ex + 127);
-                    }
-                }
-            } else {
-                for (int c0 = 0; c0 < n_valid; c0 += 32) {
-                    const int src_l = c0 + lane < n_valid ? p.pool_src[tl.row0 + c0 + lane] : -1;
-                    const float g_l = src_l >= 0 ? args.topk_weights[src_l] : 0.0f;
-#pragma unroll 1
-                    for (int blk = 0; blk < 2; ++blk) {
-                        const int h = tl.s * 2 * kWR + blk * kWR + q * 32 + lane;
-                        uint32_t y[32];
-                        tmem_ld32(tb + blk * kWR + c0, y);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int tt = 0; tt < 32; ++tt) {
-                            if (c0 + tt >= n_valid) break;  // uniform across the warp
-                            const int src = __shfl_sync(0xffffffffu, src_l, tt);
-                            const float gw = __shfl_sync(0xffffffffu, g_l, tt);
-                            if (src >= 0)
-                                p.comb[(int64_t)src * H + h] = float_to_bf16_bits(__fmul_rn(gw, __uint_as_float(y[tt])));
-                        }
+                        if (c0 + tt >= tl.n_valid) break;  // uniform across the warp
+                        const int src = __shfl_sync(0xffffffffu, src_l, tt);
+                        const float gw = __shfl_sync(0xffffffffu, g_l, tt);
+                        if (src >= 0) p.comb[(int64_t)src * H + h] = float_to_bf16_bits(__fmul_rn(gw, __uint_as_float(y[tt])));
                     }
                 }
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(acc_empty);
+            if (lane == 0) mbar_arrive(acc_empty(a));
         }
     }
 
@@ -360,31 +398,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_dealloc(tmem_base, 512);
 }
 
-template <int MODE, bool kL1>
-cudaError_t launch_bs(const Plan& p, const void* w, const void* w_scale, const float* topk_weights, cudaStream_t s) {
+template <int MODE, bool kL1, int kNT, int kStages>
+cudaError_t launch_bs_cfg(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmX, const BsArgs& args,
+                          cudaStream_t s) {
+    using Cfg = BsCfg<kNT, kStages>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(tc_bs_kernel<MODE, kL1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+        attr_err = cudaFuncSetAttribute(tc_bs_kernel<MODE, kL1, kNT, kStages>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmem);
     });
     if (attr_err != cudaSuccess) return attr_err;
+    // sub-tiles: at most one per routed row, and one per 128-row tile times 128/kNT
+    const int64_t max_sub = std::min<int64_t>((int64_t)p.T * p.K, (p.pool_rows / 128) * (128 / kNT));
+    const int64_t max_tiles = std::max<int64_t>(1, max_sub) * args.n_slabs;
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(max_tiles, tc_num_sms()));
+    tc_bs_kernel<MODE, kL1, kNT, kStages><<<grid, kThreads, Cfg::kSmem, s>>>(tmW, tmX, args);
+    return cudaGetLastError();
+}
+
+template <int MODE, bool kL1>
+cudaError_t launch_bs(const Plan& p, const void* w, const void* w_scale, const float* topk_weights, cudaStream_t s) {
     const int n_out = kL1 ? 2 * p.I : p.H;
     const int kin = kL1 ? p.H : p.I;
     CUtensorMap tmW, tmX;
     const bool ok_w = MODE == MOE_A8W4_FP8_FP4
-                          ? tc_make_map_2d_packed4(&tmW, w, (uint64_t)kin, (uint64_t)p.E * n_out, kBK, kWR)
+                          ? tc_make_map_2d_packed4(&tmW, w, (uint64_t)kin, (uint64_t)p.E * n_out, kBK, kHalf)
                           : tc_make_map_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w, (uint64_t)kin,
-                                           (uint64_t)p.E * n_out, kBK, kWR, CU_TENSOR_MAP_SWIZZLE_128B);
+                                           (uint64_t)p.E * n_out, kBK, kHalf, CU_TENSOR_MAP_SWIZZLE_128B);
     if (!ok_w) return cudaErrorInvalidValue;
     if (!tc_make_map_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kL1 ? (const void*)p.x_pool : (const void*)p.a_pool,
                         (uint64_t)kin, (uint64_t)p.pool_rows, kBK, kTokBox, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    BsArgs args{p, static_cast<const uint8_t*>(w_scale), topk_weights, kL1 ? p.I / kWR : p.H / (2 * kWR), kin / kBK,
+    BsArgs args{p, static_cast<const uint8_t*>(w_scale), topk_weights, kL1 ? p.I / kHalf : p.H / kWR, kin / kBK,
                 n_out, kin};
-    const int64_t max_tiles = (p.pool_rows / kTok) * args.n_slabs;
-    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(max_tiles, tc_num_sms()));
-    tc_bs_kernel<MODE, kL1><<<grid, kThreads, kSmem, s>>>(tmW, tmX, args);
-    return cudaGetLastError();
+    // few routed rows per expert: the weights stream from HBM; small token sub-tiles and a deep ring
+    if ((int64_t)p.T * p.K <= (int64_t)32 * p.E) return launch_bs_cfg<MODE, kL1, 32, 10>(p, tmW, tmX, args, s);
+    return launch_bs_cfg<MODE, kL1, 128, 6>(p, tmW, tmX, args, s);
 }
 
 }  // namespace
@@ -392,8 +442,8 @@ cudaError_t launch_bs(const Plan& p, const void* w, const void* w_scale, const f
 bool bs_supported(const Plan& p, int stage) {
     if ((p.mode != MOE_A8W8_FP8 && p.mode != MOE_A8W4_FP8_FP4) || p.E > kMaxExperts || !tc_encode_available())
         return false;
-    if (stage == 1) return p.I % kWR == 0 && p.H % kBK == 0;
-    return p.H % (2 * kWR) == 0 && p.I % kBK == 0;
+    if (stage == 1) return p.I % kHalf == 0 && p.H % kBK == 0;
+    return p.H % kWR == 0 && p.I % kBK == 0;
 }
 
 cudaError_t launch_l1_bs(const Plan& p, const void* w1, const void* w1_scale, cudaStream_t s) {
