@@ -266,11 +266,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         struct Words {
             uint32_t a, b[kNT / 32];
         };
-        auto load_words = [&](int t, int kb) {
+        // the lookahead tile is decoded once per tile, not once per stage
+        Tile ltile{};
+        const uint32_t* wsrow = nullptr;
+        auto load_words = [&](int kb) {
             Words w;
-            const Tile tl = tile_of(t);
-            const int wr = wrow(tl, r >= kHalf) + (r & (kHalf - 1));
-            w.a = __ldg(reinterpret_cast<const uint32_t*>(args.w_scale + (int64_t)wr * spr) + kb);
+            const Tile& tl = ltile;
+            w.a = __ldg(wsrow + kb);
 #pragma unroll
             for (int c = 0; c < kNT / 32; ++c) {
                 const int n = 32 * c + lane;
@@ -291,16 +293,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             return w;
         };
         int lt = blockIdx.x, lkb = 0;  // lookahead iterator over the producer's (tile, k-block) sequence
+        auto set_tile = [&]() {
+            if (lt < total) {
+                ltile = tile_of(lt);
+                const int wr = wrow(ltile, r >= kHalf) + (r & (kHalf - 1));
+                wsrow = reinterpret_cast<const uint32_t*>(args.w_scale + (int64_t)wr * spr);
+            }
+        };
         auto advance = [&]() {
             if (++lkb == KB) {
                 lkb = 0;
                 lt += gridDim.x;
+                set_tile();
             }
         };
+        set_tile();
         Words ring[kLookahead];
 #pragma unroll
         for (int i = 0; i < kLookahead; ++i) {
-            if (lt < total) ring[i] = load_words(lt, lkb);
+            if (lt < total) ring[i] = load_words(lkb);
             advance();
         }
         int it = 0;
@@ -310,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const Words w = ring[0];
 #pragma unroll
                 for (int i = 0; i + 1 < kLookahead; ++i) ring[i] = ring[i + 1];
-                if (lt < total) ring[kLookahead - 1] = load_words(lt, lkb);
+                if (lt < total) ring[kLookahead - 1] = load_words(lkb);
                 advance();
                 const int s = it % kStages;
                 const bool w_ok = mbar_wait(empty_bar(s), ((uint32_t)(it / kStages) & 1u) ^ 1u, p.hdr, abort_flag);
