@@ -5,14 +5,15 @@
 // case: "DQ_MX ... implicitly performed inside matmul"; DeepGEMM page §4 step 5: block-scaled
 // MMA with UE8M0 scale factors in tensor memory).
 //
-// Tiles (M = 128 weight rows, N = tokens, K = 128 per stage as 4 MMAs of K = 32):
+// Tiles (M = 128 weight rows, N = tokens, K = 128 or 256 per stage, MMAs of K = 32):
 // - L1: the 128 rows are 64 gate rows and the 64 up rows of the same 64 outputs of A, so the
 //   epilogue pairs lane r (gate) with lane r + 64 (up) through a small shared buffer and applies
 //   SwiGLU (Ascend page, "SwiGLU Activation") and the MX FP8 re-quantisation of A.
 // - L2: 128 rows of hidden columns.
-// - tokens: a sub-tile of kNT rows of one expert (kNT = 128 for prefill-sized experts, 32 for
-//   decode-sized ones, where the weights stream from HBM and deeper staging matters). The
-//   sub-tiles of every expert are counted in-kernel from the routed-row counts.
+// - tokens: a sub-tile of kNT rows of one expert: kNT = 128 with K = 128 stages for
+//   prefill-sized experts; kNT = 16 with K = 256 stages for decode-sized ones, where the weights
+//   stream from HBM and each load should cover whole 128-byte lines. The sub-tiles of every
+//   expert are counted in-kernel from the routed-row counts.
 // Accumulators are double-buffered in tensor memory, so the epilogue of a tile overlaps the
 // main loop of the next.
 //
@@ -45,20 +46,20 @@ using namespace tc;
 
 constexpr int kWR = 128;          // weight rows per tile (MMA M)
 constexpr int kHalf = 64;         // L1: gate rows, then up rows
-constexpr int kBK = 128;          // K per stage
+constexpr int kAtomK = 128;       // K of one 128-byte swizzle atom (a stage holds kAtoms of them)
 constexpr int kTokBox = 16;       // token rows per TMA box
 constexpr int kThreads = 320;
 constexpr int kMaxExperts = 1024;
 constexpr int kABytes = kWR * 128;
 constexpr int kSfCol0 = 256;      // first TMEM column of the scale ring
-constexpr int kSfColsPerStage = 8;  // SFA 4 columns, SFB up to 4 columns
+constexpr int kSfColsPerStage = 16;  // per K atom: SFA 4 columns, SFB up to 4 columns
 constexpr int kLookahead = 3;     // scale loads issued this many stages ahead
 constexpr int kEpiBar = 1;        // named barrier of the 4 epilogue warps
 
-template <int kNT, int kStages>
+template <int kNT, int kStages, int kAtoms>
 struct BsCfg {
-    static constexpr int kBBytes = kNT * 128;
-    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kBBytes = kNT * 128;                          // one K atom of tokens
+    static constexpr int kStageBytes = kAtoms * (kABytes + kBBytes);   // [A atoms][B atoms]
     static constexpr int kBarOff = kStages * kStageBytes;
     static constexpr int kNumBars = 2 * kStages + 4 + 1;
     static constexpr int kXbufOff = kBarOff + 8 * kNumBars;           // 32 tokens x 64 up values (fp32)
@@ -69,13 +70,14 @@ struct BsCfg {
     static constexpr size_t kSmem = 1024 + (size_t)kCountsOff + 4 * kMaxExperts;
     static_assert(kSmem <= 232448, "shared memory");
     static_assert(2 * kNT <= kSfCol0 && kSfCol0 + kStages * kSfColsPerStage <= 512, "tensor memory");
+    static_assert(kAtoms == 1 || kAtoms == 2, "atoms per stage");
 };
 
 struct BsArgs {
     Plan p;
     const uint8_t* w_scale;     // UE8M0 [E*n_out][kin/32]
     const float* topk_weights;  // L2
-    int n_slabs, k_blocks, n_out, kin;
+    int n_slabs, k_blocks, n_out, kin;  // k_blocks = stages per tile; the last may hold one atom
 };
 
 struct Tile {
@@ -126,13 +128,14 @@ __device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync %0, 128;" ::"n"(kEpiBar) : "memory"); }
 
-template <int MODE, bool kL1, int kNT, int kStages>
+template <int MODE, bool kL1, int kNT, int kStages, int kAtoms>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bs_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, BsArgs args) {
-    using Cfg = BsCfg<kNT, kStages>;
+    using Cfg = BsCfg<kNT, kStages, kAtoms>;
+    constexpr int kBK = kAtoms * kAtomK;  // K per stage
     constexpr bool kFp4 = MODE == MOE_A8W4_FP8_FP4;
     constexpr uint32_t kAfmt = kFp4 ? 5u : 0u;
-    constexpr uint32_t kABoxTx = kFp4 ? kHalf * kBK / 2 : kHalf * kBK;  // TMA counts the packed global bytes
+    constexpr uint32_t kABoxTx = kFp4 ? kHalf * kAtomK / 2 : kHalf * kAtomK;  // TMA counts the packed global bytes
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = smem_u32(smem_raw);
     const uint32_t base = (raw_base + 1023u) & ~1023u;
@@ -193,6 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int total = sub_off[p.E] * args.n_slabs;
     const int KB = args.k_blocks;
     const int I = p.I, H = p.H;
+    auto atoms_of = [&](int kb) { return min(kAtoms, (args.kin - kb * kBK) / kAtomK); };
     auto tile_of = [&](int t) { return decode<kNT>(t, sub_off, tile_off, counts, p.E, args.n_slabs); };
     // first global weight row of each 64-row half of the tile
     auto wrow = [&](const Tile& tl, int half) {
@@ -215,12 +219,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    const uint32_t sa = base + s * Cfg::kStageBytes, sb = sa + kABytes;
-                    mbar_arrive_expect_tx(full_bar(s), 2 * kABoxTx + (uint32_t)n * 128u);
-                    tma_load_2d(sa, &tmW, kb * kBK, w0, full_bar(s));
-                    tma_load_2d(sa + kHalf * 128, &tmW, kb * kBK, w1, full_bar(s));
-                    for (int i = 0; i < n / kTokBox; ++i)
-                        tma_load_2d(sb + i * kTokBox * 128, &tmX, kb * kBK, tl.row0 + i * kTokBox, full_bar(s));
+                    const uint32_t sa = base + s * Cfg::kStageBytes, sb = sa + kAtoms * kABytes;
+                    const int na = atoms_of(kb);
+                    mbar_arrive_expect_tx(full_bar(s), (uint32_t)na * (2 * kABoxTx + (uint32_t)n * 128u));
+                    for (int at = 0; at < na; ++at) {
+                        const int x = kb * kBK + at * kAtomK;
+                        tma_load_2d(sa + at * kABytes, &tmW, x, w0, full_bar(s));
+                        tma_load_2d(sa + at * kABytes + kHalf * 128, &tmW, x, w1, full_bar(s));
+                        for (int i = 0; i < n / kTokBox; ++i)
+                            tma_load_2d(sb + at * Cfg::kBBytes + i * kTokBox * 128, &tmX, x, tl.row0 + i * kTokBox,
+                                        full_bar(s));
+                    }
                 }
             }
             for (int j = it - kStages < 0 ? 0 : it - kStages; j < it; ++j)
@@ -245,12 +254,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = base + s * Cfg::kStageBytes, sb = sa + kABytes;
+                    const uint32_t sa = base + s * Cfg::kStageBytes, sb = sa + kAtoms * kABytes;
                     const uint32_t sf = tmem_base + kSfCol0 + s * kSfColsPerStage;
+                    const int na = atoms_of(kb);
+                    for (int at = 0; at < na; ++at) {
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 32; ++kk)
-                        tc_mma_bs(d, kmajor_desc(sa, kk), kmajor_desc(sb, kk), bs_idesc(kAfmt, n, kk), sf, sf + 4,
-                                  (kb | kk) != 0);
+                        for (int kk = 0; kk < kAtomK / 32; ++kk)
+                            tc_mma_bs(d, kmajor_desc(sa + at * kABytes, kk), kmajor_desc(sb + at * Cfg::kBBytes, kk),
+                                      bs_idesc(kAfmt, n, kk), sf + 8 * at, sf + 8 * at + 4, (kb | at | kk) != 0);
+                    }
                     tc_commit(empty_bar(s));
                 }
                 if (ok) tc_commit(acc_full(a));
@@ -263,32 +275,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3;  // lane quarter this warp writes
         const int spr = args.kin / 32;
         const int r = 32 * q + lane;  // weight row within the tile
+        constexpr int kTokWords = kNT < 32 ? 1 : kNT / 32;
         struct Words {
-            uint32_t a, b[kNT / 32];
+            uint32_t a[kAtoms], b[kAtoms][kTokWords];
         };
         // the lookahead tile is decoded once per tile, not once per stage
         Tile ltile{};
         const uint32_t* wsrow = nullptr;
+        // word g = the 4 UE8M0 bytes of K atom g (elements 128g .. 128g+127) of a row
         auto load_words = [&](int kb) {
             Words w;
             const Tile& tl = ltile;
-            w.a = __ldg(wsrow + kb);
+            const int na = atoms_of(kb);
 #pragma unroll
-            for (int c = 0; c < kNT / 32; ++c) {
-                const int n = 32 * c + lane;
-                uint32_t v = 0x7f7f7f7fu;  // 1.0 for the padding tokens
-                if (n < tl.n_valid) {
-                    const int64_t row = tl.row0 + n;
-                    if constexpr (kL1 && kFp4) {
-                        const uint32_t bits = __float_as_uint(reinterpret_cast<const float*>(p.x_pool_scale)[row * (H / 128) + kb]);
-                        v = ((bits >> 23) & 0xffu) * 0x01010101u;  // power-of-two scale -> its UE8M0 byte, x4
-                    } else if constexpr (kL1) {
-                        v = __ldg(reinterpret_cast<const uint32_t*>(p.x_pool_scale + row * (H / 32)) + kb);
-                    } else {
-                        v = __ldg(reinterpret_cast<const uint32_t*>(p.a_pool_scale + row * (I / 32)) + kb);
+            for (int at = 0; at < kAtoms; ++at) {
+                const int g = kb * kAtoms + at;
+                w.a[at] = at < na ? __ldg(wsrow + g) : 0x7f7f7f7fu;
+#pragma unroll
+                for (int c = 0; c < kTokWords; ++c) {
+                    const int n = 32 * c + lane;
+                    uint32_t v = 0x7f7f7f7fu;  // 1.0 for the padding tokens
+                    if (at < na && n < tl.n_valid) {
+                        const int64_t row = tl.row0 + n;
+                        if constexpr (kL1 && kFp4) {
+                            const uint32_t bits =
+                                __float_as_uint(reinterpret_cast<const float*>(p.x_pool_scale)[row * (H / 128) + g]);
+                            v = ((bits >> 23) & 0xffu) * 0x01010101u;  // power-of-two scale -> its UE8M0 byte, x4
+                        } else if constexpr (kL1) {
+                            v = __ldg(reinterpret_cast<const uint32_t*>(p.x_pool_scale + row * (H / 32)) + g);
+                        } else {
+                            v = __ldg(reinterpret_cast<const uint32_t*>(p.a_pool_scale + row * (I / 32)) + g);
+                        }
                     }
+                    w.b[at][c] = v;
                 }
-                w.b[c] = v;
             }
             return w;
         };
@@ -330,9 +350,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 const uint32_t sf = tmem_base + ((uint32_t)(32 * q) << 16) + kSfCol0 + s * kSfColsPerStage;
-                tmem_st1(sf + q, w.a);
 #pragma unroll
-                for (int c = 0; c < kNT / 32; ++c) tmem_st1(sf + 4 + c, w.b[c]);
+                for (int at = 0; at < kAtoms; ++at) {
+                    tmem_st1(sf + 8 * at + q, w.a[at]);
+#pragma unroll
+                    for (int c = 0; c < kTokWords; ++c) tmem_st1(sf + 8 * at + 4 + c, w.b[at][c]);
+                }
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(full_bar(s));
@@ -409,14 +432,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_dealloc(tmem_base, 512);
 }
 
-template <int MODE, bool kL1, int kNT, int kStages>
-cudaError_t launch_bs_cfg(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmX, const BsArgs& args,
+template <int MODE, bool kL1, int kNT, int kStages, int kAtoms>
+cudaError_t launch_bs_cfg(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmX, BsArgs args,
                           cudaStream_t s) {
-    using Cfg = BsCfg<kNT, kStages>;
+    using Cfg = BsCfg<kNT, kStages, kAtoms>;
+    args.k_blocks = (args.kin + kAtoms * kAtomK - 1) / (kAtoms * kAtomK);
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(tc_bs_kernel<MODE, kL1, kNT, kStages>,
+        attr_err = cudaFuncSetAttribute(tc_bs_kernel<MODE, kL1, kNT, kStages, kAtoms>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmem);
     });
     if (attr_err != cudaSuccess) return attr_err;
@@ -424,7 +448,7 @@ cudaError_t launch_bs_cfg(const Plan& p, const CUtensorMap& tmW, const CUtensorM
     const int64_t max_sub = std::min<int64_t>((int64_t)p.T * p.K, (p.pool_rows / 128) * (128 / kNT));
     const int64_t max_tiles = std::max<int64_t>(1, max_sub) * args.n_slabs;
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(max_tiles, tc_num_sms()));
-    tc_bs_kernel<MODE, kL1, kNT, kStages><<<grid, kThreads, Cfg::kSmem, s>>>(tmW, tmX, args);
+    tc_bs_kernel<MODE, kL1, kNT, kStages, kAtoms><<<grid, kThreads, Cfg::kSmem, s>>>(tmW, tmX, args);
     return cudaGetLastError();
 }
 
@@ -434,18 +458,18 @@ cudaError_t launch_bs(const Plan& p, const void* w, const void* w_scale, const f
     const int kin = kL1 ? p.H : p.I;
     CUtensorMap tmW, tmX;
     const bool ok_w = MODE == MOE_A8W4_FP8_FP4
-                          ? tc_make_map_2d_packed4(&tmW, w, (uint64_t)kin, (uint64_t)p.E * n_out, kBK, kHalf)
+                          ? tc_make_map_2d_packed4(&tmW, w, (uint64_t)kin, (uint64_t)p.E * n_out, kAtomK, kHalf)
                           : tc_make_map_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w, (uint64_t)kin,
-                                           (uint64_t)p.E * n_out, kBK, kHalf, CU_TENSOR_MAP_SWIZZLE_128B);
+                                           (uint64_t)p.E * n_out, kAtomK, kHalf, CU_TENSOR_MAP_SWIZZLE_128B);
     if (!ok_w) return cudaErrorInvalidValue;
     if (!tc_make_map_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kL1 ? (const void*)p.x_pool : (const void*)p.a_pool,
-                        (uint64_t)kin, (uint64_t)p.pool_rows, kBK, kTokBox, CU_TENSOR_MAP_SWIZZLE_128B))
+                        (uint64_t)kin, (uint64_t)p.pool_rows, kAtomK, kTokBox, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    BsArgs args{p, static_cast<const uint8_t*>(w_scale), topk_weights, kL1 ? p.I / kHalf : p.H / kWR, kin / kBK,
-                n_out, kin};
-    // few routed rows per expert: the weights stream from HBM; small token sub-tiles and a deep ring
-    if ((int64_t)p.T * p.K <= (int64_t)32 * p.E) return launch_bs_cfg<MODE, kL1, 32, 10>(p, tmW, tmX, args, s);
-    return launch_bs_cfg<MODE, kL1, 128, 6>(p, tmW, tmX, args, s);
+    BsArgs args{p, static_cast<const uint8_t*>(w_scale), topk_weights, kL1 ? p.I / kHalf : p.H / kWR, 0, n_out, kin};
+    // few routed rows per expert: the weights stream from HBM; 16-token sub-tiles and K = 256
+    // stages (whole 128-byte lines of every weight row per load)
+    if ((int64_t)p.T * p.K <= (int64_t)16 * p.E) return launch_bs_cfg<MODE, kL1, 16, 5, 2>(p, tmW, tmX, args, s);
+    return launch_bs_cfg<MODE, kL1, 128, 6, 1>(p, tmW, tmX, args, s);
 }
 
 }  // namespace
@@ -453,8 +477,8 @@ cudaError_t launch_bs(const Plan& p, const void* w, const void* w_scale, const f
 bool bs_supported(const Plan& p, int stage) {
     if ((p.mode != MOE_A8W8_FP8 && p.mode != MOE_A8W4_FP8_FP4) || p.E > kMaxExperts || !tc_encode_available())
         return false;
-    if (stage == 1) return p.I % kHalf == 0 && p.H % kBK == 0;
-    return p.H % kWR == 0 && p.I % kBK == 0;
+    if (stage == 1) return p.I % kHalf == 0 && p.H % kAtomK == 0;
+    return p.H % kWR == 0 && p.I % kAtomK == 0;
 }
 
 cudaError_t launch_l1_bs(const Plan& p, const void* w1, const void* w1_scale, cudaStream_t s) {
