@@ -97,7 +97,8 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
     return out;
 }
 
-// counts -> offsets, padded offsets and tile offsets; marks the padding rows of the pools.
+// counts -> offsets, padded offsets and tile offsets (the padding rows of the pools keep the -1
+// that launch_route writes into pool_src before the scatter).
 __global__ void __launch_bounds__(1024) route_scan_kernel(int E, const int32_t* __restrict__ claim,
                                                           int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                                                           int32_t* __restrict__ pad_off, int32_t* __restrict__ tile_off,
@@ -118,7 +119,6 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int E, const int32_t* 
         pad_off[e] = toff * kTileRows;
         if (counts_out) counts_out[e] = c;
         if (offsets_out) offsets_out[e] = off;
-        for (int r = toff * kTileRows + c; r < (toff + tiles) * kTileRows; ++r) pool_src[r] = -1;
     }
     if (e == 0) {
         offsets[E] = total_rows;
@@ -152,8 +152,9 @@ __global__ void route_scatter_kernel(const int32_t* __restrict__ ids, int n_ids,
     slot_row[i] = prow;
 }
 
-// S2: copy x row (token = src / K) and its scale row into every padded pool row; padding
-// rows get zeros.
+// S2: copy x row (token = src / K) and its scale row into the pool row of every routed (i, k).
+// Padding rows are left as they are: every consumer computes rows (tokens) independently and
+// drops the padding rows' results.
 __global__ void __launch_bounds__(128) dispatch_gather_kernel(const uint4* __restrict__ x, const uint32_t* __restrict__ xs,
                                                               const int32_t* __restrict__ pool_src,
                                                               const int32_t* __restrict__ hdr, int K, int row_vecs,
@@ -162,25 +163,19 @@ __global__ void __launch_bounds__(128) dispatch_gather_kernel(const uint4* __res
     const int rows = hdr[kHdrPadRows];
     for (int r = blockIdx.x; r < rows; r += gridDim.x) {
         const int src = pool_src[r];
+        if (src < 0) continue;  // padding row
         uint4* dst = xp + (size_t)r * row_vecs;
-        if (src >= 0) {
-            const uint4* s = x + (size_t)(src / K) * row_vecs;
-            for (int v = threadIdx.x; v < row_vecs; v += blockDim.x) dst[v] = s[v];
-            for (int w = threadIdx.x; w < scale_words; w += blockDim.x)
-                xps[(size_t)r * scale_words + w] = xs[(size_t)(src / K) * scale_words + w];
-        } else {
-            const uint4 z = make_uint4(0, 0, 0, 0);
-            for (int v = threadIdx.x; v < row_vecs; v += blockDim.x) dst[v] = z;
-            for (int w = threadIdx.x; w < scale_words; w += blockDim.x) xps[(size_t)r * scale_words + w] = 0u;
-        }
+        const uint4* s = x + (size_t)(src / K) * row_vecs;
+        for (int v = threadIdx.x; v < row_vecs; v += blockDim.x) dst[v] = s[v];
+        for (int w = threadIdx.x; w < scale_words; w += blockDim.x)
+            xps[(size_t)r * scale_words + w] = xs[(size_t)(src / K) * scale_words + w];
     }
 }
 
-// S2 for the quantised modes: copies the codes and scales like dispatch_gather_kernel and also
-// writes the row dequantised to bf16 for the tensor-core GEMM (x~ = code * scale, exact in
-// bf16: e4m3 has 4 significant bits and the scales are powers of two). INT8 rows are written
-// as two planes, hi = floor(q/16) and lo = q mod 16 (q = 16*hi + lo, both exact in bf16), so
-// that every fp32 partial sum of the GEMM stays an exactly representable integer.
+// S2 for the quantised modes: copies the codes and scale rows like dispatch_gather_kernel. For
+// the INT8 mode it also writes the codes as two bf16 planes, hi = floor(q/16) and lo = q mod 16
+// (q = 16*hi + lo, both exact in bf16), the operand of the INT8 tensor-core GEMM: with them every
+// fp32 partial sum of that GEMM stays an exactly representable integer.
 template <int MODE>
 __global__ void __launch_bounds__(128) dispatch_gather_q_kernel(const uint8_t* __restrict__ x, const uint8_t* __restrict__ xs,
                                                                 const int32_t* __restrict__ pool_src,
@@ -190,41 +185,31 @@ __global__ void __launch_bounds__(128) dispatch_gather_q_kernel(const uint8_t* _
     const int rows = hdr[kHdrPadRows];
     for (int r = blockIdx.x; r < rows; r += gridDim.x) {
         const int src = pool_src[r];
-        const int64_t tok = src >= 0 ? src / K : 0;
+        if (src < 0) continue;  // padding row: left as it is (rows are independent everywhere)
+        const int64_t tok = src / K;
         for (int v = threadIdx.x; v < H / 16; v += blockDim.x) {
-            uint4 c = src >= 0 ? reinterpret_cast<const uint4*>(x + tok * H)[v] : make_uint4(0, 0, 0, 0);
+            const uint4 c = reinterpret_cast<const uint4*>(x + tok * H)[v];
             reinterpret_cast<uint4*>(xp + (int64_t)r * H)[v] = c;
-            const uint8_t* b = reinterpret_cast<const uint8_t*>(&c);
-            uint32_t out[8], out_lo[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                float f0, f1;
-                if constexpr (MODE == MOE_A8W8_INT8) {
-                    const int q0 = (int8_t)b[2 * j], q1 = (int8_t)b[2 * j + 1];
-                    f0 = (float)(q0 >> 4);
-                    f1 = (float)(q1 >> 4);
-                    out_lo[j] = (uint32_t)float_to_bf16_bits((float)(q0 & 15)) |
-                                ((uint32_t)float_to_bf16_bits((float)(q1 & 15)) << 16);
-                } else {
-                    const int k = v * 16 + 2 * j;
-                    float s;
-                    if constexpr (MODE == MOE_A8W8_FP8) s = src >= 0 ? ue8m0_to_float(xs[tok * (H / 32) + k / 32]) : 0.f;
-                    else s = src >= 0 ? reinterpret_cast<const float*>(xs)[tok * (H / 128) + k / 128] : 0.f;
-                    f0 = e4m3_to_float(b[2 * j]) * s;
-                    f1 = e4m3_to_float(b[2 * j + 1]) * s;
-                }
-                out[j] = (uint32_t)float_to_bf16_bits(f0) | ((uint32_t)float_to_bf16_bits(f1) << 16);
-            }
             if constexpr (MODE == MOE_A8W8_INT8) {
-                uint4* dst = reinterpret_cast<uint4*>(xb + (int64_t)r * H + v * 16);
-                dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
-                dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
-                uint4* lo = reinterpret_cast<uint4*>(xb + (pool_rows + r) * H + v * 16);
-                lo[0] = make_uint4(out_lo[0], out_lo[1], out_lo[2], out_lo[3]);
-                lo[1] = make_uint4(out_lo[4], out_lo[5], out_lo[6], out_lo[7]);
+                const uint8_t* b = reinterpret_cast<const uint8_t*>(&c);
+                uint32_t hi[8], lo[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int q0 = (int8_t)b[2 * j], q1 = (int8_t)b[2 * j + 1];
+                    hi[j] = (uint32_t)float_to_bf16_bits((float)(q0 >> 4)) |
+                            ((uint32_t)float_to_bf16_bits((float)(q1 >> 4)) << 16);
+                    lo[j] = (uint32_t)float_to_bf16_bits((float)(q0 & 15)) |
+                            ((uint32_t)float_to_bf16_bits((float)(q1 & 15)) << 16);
+                }
+                uint4* dh = reinterpret_cast<uint4*>(xb + (int64_t)r * H + v * 16);
+                uint4* dl = reinterpret_cast<uint4*>(xb + (pool_rows + r) * H + v * 16);
+                dh[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                dh[1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+                dl[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                dl[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
             }
         }
-        for (int w = threadIdx.x; w < scale_bytes; w += blockDim.x) xps[(int64_t)r * scale_bytes + w] = src >= 0 ? xs[tok * scale_bytes + w] : 0;
+        for (int w = threadIdx.x; w < scale_bytes; w += blockDim.x) xps[(int64_t)r * scale_bytes + w] = xs[tok * scale_bytes + w];
     }
 }
 
@@ -277,6 +262,8 @@ cudaError_t launch_route(const Plan& p, const int32_t* topk_ids, int32_t* counts
     // the header (error word, totals) and the per-expert claim counters are contiguous
     const size_t clear = reinterpret_cast<const uint8_t*>(p.claim + p.E) - reinterpret_cast<const uint8_t*>(p.hdr);
     cudaError_t e = cudaMemsetAsync(p.hdr, 0, clear, s);
+    if (e != cudaSuccess) return e;
+    e = cudaMemsetAsync(p.pool_src, 0xff, sizeof(int32_t) * (size_t)p.pool_rows, s);  // -1: padding row
     if (e != cudaSuccess) return e;
     if (n_ids > 0) {
         const int blocks = (n_ids + kRouteChunk - 1) / kRouteChunk;

@@ -94,8 +94,8 @@ def test_dispatch_gathers_rows(moe):
         s = pool_src[r]
         if s >= 0:
             assert np.array_equal(xp[r], x[s // wl.K]) and np.array_equal(xs[r], xsc[s // wl.K])
-        else:
-            assert not xp[r].any()
+    # every routed (i, k) has exactly one pool row
+    assert sorted(int(v) for v in pool_src[:n_pad] if v >= 0) == list(range(wl.T * wl.K))
 
 
 def test_int8_l2_accumulators_exact(moe):
