@@ -214,46 +214,28 @@ class ClockSampler:
 
 
 def dominant_kernel_traffic(workload):
-    """DRAM bytes per launch of the L1 GEMM from the committed ncu summary, valid only while
-    the kernel sources are the ones the counters were taken on."""
+    """DRAM bytes per launch of the L1 GEMM from the committed ncu summary of this workload,
+    valid only while the kernel sources the counters were taken on are unchanged (the summary
+    lists them and their sha256)."""
     path = os.path.join(ROOT, "profiles", f"l1_gemm_{workload}.md")
     if not os.path.exists(path):
         return None
     txt = open(path).read()
     m = re.search(r"traffic_bytes_per_launch:\s*(\d+)", txt)
-    h = re.search(r"source_sha256:\s*([0-9a-f]{16,64})", txt)
-    if not m or not h:
+    h = re.search(r"source_sha256:\s*([0-9a-f]{64})", txt)
+    f = re.search(r"source_files:\s*(.+)", txt)
+    if not m or not h or not f:
         return None
-    return int(m.group(1)) if h.group(1) == kernel_source_hash()[:len(h.group(1))] else None
+    return int(m.group(1)) if h.group(1) == kernel_source_hash(f.group(1).split()) else None
 
 
-L1_KERNEL_SOURCES = ("tc_gemm.cu", "common.cuh", "internal.h")
-
-
-def kernel_source_hash():
-    """sha256 over the sources the tensor-core GEMM kernel is built from."""
+def kernel_source_hash(files):
+    """sha256 over the given files of the CUDA sources, in order."""
     d = os.path.join(ROOT, "moe_expert_ffn_topk_gb300", "csrc")
     sha = hashlib.sha256()
-    for name in L1_KERNEL_SOURCES:
+    for name in files:
         sha.update(open(os.path.join(d, name), "rb").read())
     return sha.hexdigest()
-
-
-def max_over_ranks(x: float, world: int, device) -> float:
-    """The largest value over all ranks (the slowest rank's time); identity on one rank."""
-    if world <= 1:
-        return x
-    import torch
-    import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
-
-
-def whole_job_tflops(flops_per_step: float, steps: int, elapsed_ms: float, world: int) -> float:
-    """Replicas: every rank runs the full step, so the job did world * steps steps in the
-    slowest rank's time."""
-    return world * flops_per_step * steps / (elapsed_ms * 1e-3) / 1e12
 
 
 WEIGHT_BYTES_PER_ELEM = {"a16w16": 2.0, "a8w8_fp8": 1.0 + 1 / 32, "a8w8_int8": 1.0, "a8w4_fp8_fp4": 0.5 + 1 / 32}
