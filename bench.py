@@ -238,6 +238,23 @@ def kernel_source_hash(files):
     return sha.hexdigest()
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest value over all ranks (the slowest rank's time); identity on one rank."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_step: float, steps: int, elapsed_ms: float, world: int) -> float:
+    """Replicas: every rank runs the full step, so the job did world * steps steps in the
+    slowest rank's time."""
+    return world * flops_per_step * steps / (elapsed_ms * 1e-3) / 1e12
+
+
 WEIGHT_BYTES_PER_ELEM = {"a16w16": 2.0, "a8w8_fp8": 1.0 + 1 / 32, "a8w8_int8": 1.0, "a8w4_fp8_fp4": 0.5 + 1 / 32}
 X_BYTES_PER_ELEM = {"a16w16": 2.0, "a8w8_fp8": 1.0 + 1 / 32, "a8w8_int8": 1.0, "a8w4_fp8_fp4": 1.0 + 4 / 128}
 

@@ -176,9 +176,9 @@ typedef struct {
     size_t a_pool;        /* L2 operand codes [pool_rows, I] */
     size_t a_pool_scale;  /* L2 operand scales [pool_rows, *] */
     size_t a_f32;         /* fp32 A [pool_rows, I] (INT8 mode: before the per-row quantisation) */
-    size_t x_pool_bf16;   /* INT8 mode: the gathered x codes as two bf16 planes [2][pool_rows, H],
+    size_t x_pool_planes; /* INT8 mode: the gathered x codes as two f16 planes [2][pool_rows, H],
                              hi = floor(q/16) and lo = q mod 16 (other modes: size 0) */
-    size_t a_pool_bf16;   /* INT8 mode: the re-quantised A as two bf16 planes (hi, lo) [2][pool_rows, I] */
+    size_t a_pool_planes; /* INT8 mode: the re-quantised A as two f16 planes (hi, lo) [2][pool_rows, I] */
     size_t comb;          /* bf16 [T*K, H] weighted rows */
     size_t total;         /* = moe_workspace_bytes() */
     int64_t pool_rows;    /* rows reserved in each pool */

@@ -37,7 +37,7 @@ class MoeOperand(ctypes.Structure):
 class MoeWorkspaceLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
         "header", "counts", "offsets", "pad_offsets", "tile_offsets", "row_src", "pool_src", "slot_row",
-        "x_pool", "x_pool_scale", "a_pool", "a_pool_scale", "a_f32", "x_pool_bf16", "a_pool_bf16", "comb",
+        "x_pool", "x_pool_scale", "a_pool", "a_pool_scale", "a_f32", "x_pool_planes", "a_pool_planes", "comb",
         "total")] + \
         [("pool_rows", ctypes.c_int64)]
 

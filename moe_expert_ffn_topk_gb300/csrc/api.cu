@@ -77,8 +77,8 @@ moe_status layout(const moe_dims* d, moe_dtype_mode m, moe_workspace_layout_t* o
     L.a_pool_scale = take((size_t)pool_rows * a_scale_row_bytes(m, (int)I));
     L.a_f32 = take(m == MOE_A8W8_INT8 ? (size_t)pool_rows * I * 4 : 0);
     const int planes = m == MOE_A8W8_INT8 ? 2 : 0;  // the INT8 tensor-core path's hi / lo operand planes
-    L.x_pool_bf16 = take((size_t)planes * pool_rows * H * 2);
-    L.a_pool_bf16 = take((size_t)planes * pool_rows * I * 2);
+    L.x_pool_planes = take((size_t)planes * pool_rows * H * 2);
+    L.a_pool_planes = take((size_t)planes * pool_rows * I * 2);
     L.total = off;
     L.pool_rows = pool_rows;
     *out = L;
@@ -114,8 +114,8 @@ moe_status make_plan_view(const moe_dims* d, moe_dtype_mode m, void* ws, size_t 
     p->a_pool = b + L.a_pool;
     p->a_pool_scale = b + L.a_pool_scale;
     p->a_f32 = reinterpret_cast<float*>(b + L.a_f32);
-    p->x_bf16 = reinterpret_cast<uint16_t*>(b + L.x_pool_bf16);
-    p->a_bf16 = reinterpret_cast<uint16_t*>(b + L.a_pool_bf16);
+    p->x_planes = reinterpret_cast<uint16_t*>(b + L.x_pool_planes);
+    p->a_planes = reinterpret_cast<uint16_t*>(b + L.a_pool_planes);
     p->comb = reinterpret_cast<uint16_t*>(b + L.comb);
     return MOE_OK;
 }
@@ -175,8 +175,8 @@ moe_status moe_expert_l1(moe_operand w1, const moe_dims* d, moe_dtype_mode m, ui
         e = launch_l1_tc(p, w1.data, w1.scale, s);
     } else if (!(flags & MOE_FLAG_SIMT) && bs_supported(p, 1)) {
         e = launch_l1_bs(p, w1.data, w1.scale, s);
-    } else if (!(flags & MOE_FLAG_SIMT) && wm_supported(p, 1)) {
-        e = launch_l1_wm(p, w1.data, w1.scale, s);
+    } else if (!(flags & MOE_FLAG_SIMT) && int8_tc_supported(p, 1)) {
+        e = launch_l1_int8_tc(p, w1.data, w1.scale, s);
     } else {
         e = launch_l1_simt(p, w1.data, w1.scale, s);
     }
@@ -197,8 +197,8 @@ moe_status moe_expert_l2(moe_operand w2, const float* topk_weights, const moe_di
         return from_cuda(launch_l2_tc(p, w2.data, w2.scale, topk_weights, s));
     if (!(flags & MOE_FLAG_SIMT) && bs_supported(p, 2))
         return from_cuda(launch_l2_bs(p, w2.data, w2.scale, topk_weights, s));
-    if (!(flags & MOE_FLAG_SIMT) && wm_supported(p, 2))
-        return from_cuda(launch_l2_wm(p, w2.data, w2.scale, topk_weights, s));
+    if (!(flags & MOE_FLAG_SIMT) && int8_tc_supported(p, 2))
+        return from_cuda(launch_l2_int8_tc(p, w2.data, w2.scale, topk_weights, s));
     return from_cuda(launch_l2_simt(p, w2.data, w2.scale, topk_weights, s));
 }
 

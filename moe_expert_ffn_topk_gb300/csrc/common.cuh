@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_fp8.h>
 #include <stdint.h>
 
@@ -33,6 +34,8 @@ __device__ __forceinline__ uint16_t float_to_bf16_bits(float v) {
     __nv_bfloat16 h = __float2bfloat16_rn(v);
     return *reinterpret_cast<uint16_t*>(&h);
 }
+
+__device__ __forceinline__ uint16_t float_to_f16_bits(float v) { return __half_as_ushort(__float2half_rn(v)); }
 
 // e4m3fn code -> float (exact), via the fp8 conversion of cuda_fp8.h
 __device__ __forceinline__ float e4m3_to_float(uint8_t c) {

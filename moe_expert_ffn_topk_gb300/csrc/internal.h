@@ -36,8 +36,8 @@ struct Plan {
     uint8_t* a_pool;       // [pool_rows, I * a elem bytes]
     uint8_t* a_pool_scale;
     float* a_f32;          // [pool_rows, I] (INT8 mode)
-    uint16_t* x_bf16;      // INT8: bf16 [2][pool_rows, H] (hi, lo planes)
-    uint16_t* a_bf16;      // INT8: bf16 [2][pool_rows, I]
+    uint16_t* x_planes;    // INT8: f16 [2][pool_rows, H] (hi, lo planes of the codes)
+    uint16_t* a_planes;    // INT8: f16 [2][pool_rows, I]
     uint16_t* comb;        // bf16 [T*K, H]
 };
 
@@ -67,12 +67,12 @@ cudaError_t launch_l2_tc(const Plan& p, const void* w2, const void* w2_scale, co
                          cudaStream_t s);
 bool tc_supported(const Plan& p, int stage);
 
-// Weight-major tensor-core path of the INT8 mode (weights converted to bf16 in shared memory,
-// tokens split into exact hi/lo bf16 planes).
-cudaError_t launch_l1_wm(const Plan& p, const void* w1, const void* w1_scale, cudaStream_t s);
-cudaError_t launch_l2_wm(const Plan& p, const void* w2, const void* w2_scale, const float* topk_weights,
-                         cudaStream_t s);
-bool wm_supported(const Plan& p, int stage);
+// Tensor-core path of the INT8 mode (weights converted to f16 in shared memory, tokens split
+// into exact hi/lo f16 planes).
+cudaError_t launch_l1_int8_tc(const Plan& p, const void* w1, const void* w1_scale, cudaStream_t s);
+cudaError_t launch_l2_int8_tc(const Plan& p, const void* w2, const void* w2_scale, const float* topk_weights,
+                              cudaStream_t s);
+bool int8_tc_supported(const Plan& p, int stage);
 
 // Block-scaled tensor-core path of the FP8 modes (kind::mxf8f6f4.block_scale).
 cudaError_t launch_l1_bs(const Plan& p, const void* w1, const void* w1_scale, cudaStream_t s);

@@ -173,8 +173,8 @@ __global__ void __launch_bounds__(128) dispatch_gather_kernel(const uint4* __res
 }
 
 // S2 for the quantised modes: copies the codes and scale rows like dispatch_gather_kernel. For
-// the INT8 mode it also writes the codes as two bf16 planes, hi = floor(q/16) and lo = q mod 16
-// (q = 16*hi + lo, both exact in bf16), the operand of the INT8 tensor-core GEMM: with them every
+// the INT8 mode it also writes the codes as two f16 planes, hi = floor(q/16) and lo = q mod 16
+// (q = 16*hi + lo, both exact in f16), the operand of the INT8 tensor-core GEMM: with them every
 // fp32 partial sum of that GEMM stays an exactly representable integer.
 template <int MODE>
 __global__ void __launch_bounds__(128) dispatch_gather_q_kernel(const uint8_t* __restrict__ x, const uint8_t* __restrict__ xs,
@@ -196,10 +196,10 @@ __global__ void __launch_bounds__(128) dispatch_gather_q_kernel(const uint8_t* _
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const int q0 = (int8_t)b[2 * j], q1 = (int8_t)b[2 * j + 1];
-                    hi[j] = (uint32_t)float_to_bf16_bits((float)(q0 >> 4)) |
-                            ((uint32_t)float_to_bf16_bits((float)(q1 >> 4)) << 16);
-                    lo[j] = (uint32_t)float_to_bf16_bits((float)(q0 & 15)) |
-                            ((uint32_t)float_to_bf16_bits((float)(q1 & 15)) << 16);
+                    hi[j] = (uint32_t)float_to_f16_bits((float)(q0 >> 4)) |
+                            ((uint32_t)float_to_f16_bits((float)(q1 >> 4)) << 16);
+                    lo[j] = (uint32_t)float_to_f16_bits((float)(q0 & 15)) |
+                            ((uint32_t)float_to_f16_bits((float)(q1 & 15)) << 16);
                 }
                 uint4* dh = reinterpret_cast<uint4*>(xb + (int64_t)r * H + v * 16);
                 uint4* dl = reinterpret_cast<uint4*>(xb + (pool_rows + r) * H + v * 16);
@@ -285,7 +285,7 @@ static cudaError_t dispatch_q(const Plan& p, const void* x, const void* x_scale,
     dispatch_gather_q_kernel<MODE><<<grid, 128, 0, s>>>(static_cast<const uint8_t*>(x),
                                                         static_cast<const uint8_t*>(x_scale), p.pool_src, p.hdr, p.K,
                                                         p.H, (int)x_scale_row_bytes(MODE, p.H), p.pool_rows, p.x_pool,
-                                                        p.x_pool_scale, p.x_bf16);
+                                                        p.x_pool_scale, p.x_planes);
     return cudaGetLastError();
 }
 

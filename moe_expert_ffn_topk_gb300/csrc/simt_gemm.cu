@@ -256,15 +256,15 @@ __global__ void __launch_bounds__(256) int8_row_quant_kernel(Plan p) {
         __syncthreads();
         const float s = fmaxf(__fdiv_rn(amax, 127.0f), 1e-8f);
         int8_t* q = reinterpret_cast<int8_t*>(p.a_pool) + (int64_t)r * I;
-        uint16_t* hi = p.a_bf16 + (int64_t)r * I;               // plane 0: floor(q/16)
-        uint16_t* lo = p.a_bf16 + (p.pool_rows + r) * I;        // plane 1: q mod 16
+        uint16_t* hi = p.a_planes + (int64_t)r * I;             // plane 0: floor(q/16), f16
+        uint16_t* lo = p.a_planes + (p.pool_rows + r) * I;      // plane 1: q mod 16, f16
         for (int j = threadIdx.x; j < I; j += blockDim.x) {
             float v = rintf(__fdiv_rn(a[j], s));
             v = fminf(fmaxf(v, -127.0f), 127.0f);
             const int qi = static_cast<int>(v);
             q[j] = static_cast<int8_t>(qi);
-            hi[j] = float_to_bf16_bits((float)(qi >> 4));
-            lo[j] = float_to_bf16_bits((float)(qi & 15));
+            hi[j] = float_to_f16_bits((float)(qi >> 4));
+            lo[j] = float_to_f16_bits((float)(qi & 15));
         }
         if (threadIdx.x == 0) reinterpret_cast<float*>(p.a_pool_scale)[r] = s;
     }

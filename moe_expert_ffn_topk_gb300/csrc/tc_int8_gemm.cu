@@ -1,0 +1,404 @@
+// INT8 grouped GEMM on the tensor cores with exact int32 results (Ascend mega_moe page, A8W8-INT
+// use case: C = Q_e . W1^int8 and D = A^int8 . W2^int8 in int32, then (C * s^W) * s^X in fp32).
+//
+// sm_103a has no integer tcgen05.mma kind, so the integers travel as f16 (kind::f16, fp32
+// accumulation in TMEM), which is exact as long as every partial sum stays below 2^24:
+// - the token codes are split as q = 16*hi + lo with hi = floor(q/16) in [-8, 7] and
+//   lo = q mod 16 in [0, 15] (the identity of the page's A8W4-INT "MSD" scheme); the dispatch
+//   stage (x) and the row quantiser (A) store them as two f16 planes;
+// - the weights stay int8 in HBM; TMA brings them into a staging ring (64-byte swizzle) and four
+//   converter warps expand them to f16 (q ^ 0x80 placed under the exponent of 1024 gives
+//   1152 + q exactly; one f16 subtraction removes the 1152), in the 128-byte-swizzled K-major
+//   layout of the MMA;
+// - one tile is 128 weight rows x 128 tokens; its B tile holds the tokens' hi rows, then their
+//   lo rows (N = 256), so |partial sum| <= 15 * 127 * K < 2^24 for K <= 8800, and the epilogue
+//   rebuilds the exact accumulator as 16 * D_hi + D_lo in int32 before the fp32 dequantisation.
+// Weight-major orientation as in the block-scaled kernel: M = weight rows; L1 tiles carry the
+// gate block and the up block of the same 128 outputs (two accumulators sharing B), L2 tiles two
+// 128-row blocks of hidden columns.
+//
+// Warp roles (352 threads): warp 0 TMA of raw weights, warp 1 TMEM allocation + MMA issue,
+// warps 2-5 epilogue, warps 6-9 weight converters, warp 10 TMA of the token tiles.
+// Every wait is bounded; on time-out the CTA records MOE_ERR_TIMEOUT, drains and exits.
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc_common.cuh"
+
+namespace moe {
+
+namespace {
+
+using namespace tc;
+
+constexpr int kWR = 128;        // weight rows per block (MMA M)
+constexpr int kTok = 128;       // tokens per tile (one route tile)
+constexpr int kBK = 64;         // K per stage: 64 f16 = one 128-byte swizzle row
+constexpr int kTokBox = 16;     // token rows per TMA box
+constexpr int kThreads = 352;
+constexpr int kMaxExperts = 1024;
+constexpr int kRawStages = 3, kHfStages = 2, kTokStages = 3;
+constexpr int kABytes = 2 * kWR * 128;   // two f16 weight blocks
+constexpr int kTokBytes = 2 * kTok * 128;  // hi rows, then lo rows
+constexpr int kRawBytes = 2 * kWR * kBK;   // two int8 weight blocks
+constexpr int kHfOff = 0;
+constexpr int kTokOff = kHfOff + kHfStages * kABytes;
+constexpr int kRawOff = kTokOff + kTokStages * kTokBytes;
+constexpr int kBarOff = kRawOff + kRawStages * kRawBytes;
+constexpr int kNumBars = 2 * (kRawStages + kHfStages + kTokStages) + 2 + 1;
+constexpr int kMiscOff = kBarOff + 8 * kNumBars;
+constexpr int kTileOffOff = kMiscOff + 16;
+constexpr int kCountsOff = kTileOffOff + 4 * (kMaxExperts + 1);
+constexpr size_t kSmem = 1024 + (size_t)kCountsOff + 4 * kMaxExperts;
+static_assert(kSmem <= 232448, "shared memory");
+
+// kind::f16 instruction descriptor: D fp32 (bits 4-5 = 1), A and B f16 (formats 0), both
+// K-major, N = 256 (>> 3 in bits 17-22), M = 128 (>> 4 in bits 24-28).
+constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(256 >> 3) << 17) | ((uint32_t)(kWR >> 4) << 24);
+
+struct I8Args {
+    Plan p;
+    const float* w_scale;       // fp32 per output channel [E*n_out]
+    const float* topk_weights;  // L2
+    int n_slabs, k_blocks, n_out;
+};
+
+struct Tile {
+    int e, s, m, row0;
+};
+
+__device__ __forceinline__ Tile decode(int t, const int* tile_off, int E, int n_slabs) {
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (tile_off[mid] * n_slabs <= t) lo = mid; else hi = mid - 1;
+    }
+    Tile tl;
+    tl.e = lo;
+    const int mt = tile_off[lo + 1] - tile_off[lo];
+    const int local = t - tile_off[lo] * n_slabs;
+    tl.s = local / mt;
+    tl.m = local % mt;
+    tl.row0 = (tile_off[lo] + tl.m) * kTok;
+    return tl;
+}
+
+// 4 int8 codes (one 32-bit word) -> 2 f16x2 words, exactly: u = q ^ 0x80 = q + 128 placed as
+// the mantissa of f16 1024 gives 1152 + q; subtracting 1152 leaves q.
+__device__ __forceinline__ void int8x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    const uint32_t u = w ^ 0x80808080u;
+    const uint32_t a = __byte_perm(u, 0x64646464u, 0x5140);  // bytes u0, 0x64, u1, 0x64
+    const uint32_t b = __byte_perm(u, 0x64646464u, 0x7362);  // bytes u2, 0x64, u3, 0x64
+    const __half2 off = __half2half2(__ushort_as_half((unsigned short)0x6480));  // 1152
+    const __half2 ra = __hsub2(*reinterpret_cast<const __half2*>(&a), off);
+    const __half2 rb = __hsub2(*reinterpret_cast<const __half2*>(&b), off);
+    lo = *reinterpret_cast<const uint32_t*>(&ra);
+    hi = *reinterpret_cast<const uint32_t*>(&rb);
+}
+
+// Expand weight row r's 64 int8 codes from the raw tile (64-byte rows, 64-byte swizzle: chunk
+// index ^= address bits 7-8) into f16 row r of a 128-byte-swizzled K-major tile.
+__device__ __forceinline__ void convert_row(const uint8_t* raw_tile, uint8_t* tile, int r) {
+    const uint8_t* row = raw_tile + r * 64;
+    const int x = (r >> 1) & 3;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint4 c = *reinterpret_cast<const uint4*>(row + ((q ^ x) << 4));  // 16 codes
+        uint32_t o[8];
+        int8x4_to_f16(c.x, o[0], o[1]);
+        int8x4_to_f16(c.y, o[2], o[3]);
+        int8x4_to_f16(c.z, o[4], o[5]);
+        int8x4_to_f16(c.w, o[6], o[7]);
+        const int ch0 = 2 * q, ch1 = 2 * q + 1;  // 8 f16 per 16-byte chunk
+        *reinterpret_cast<uint4*>(tile + r * 128 + ((ch0 ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(tile + r * 128 + ((ch1 ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+}
+
+__device__ __forceinline__ int exact_int(uint32_t hi_bits, uint32_t lo_bits) {
+    return 16 * __float2int_rn(__uint_as_float(hi_bits)) + __float2int_rn(__uint_as_float(lo_bits));
+}
+
+template <bool kL1>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_int8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, I8Args args) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_base = smem_u32(smem_raw);
+    const uint32_t base = (raw_base + 1023u) & ~1023u;
+    uint8_t* smem = smem_raw + (base - raw_base);
+    const uint32_t bars = base + kBarOff;
+    auto raw_full = [&](int i) { return bars + 8u * i; };
+    auto raw_empty = [&](int i) { return bars + 8u * (kRawStages + i); };
+    auto hf_full = [&](int i) { return bars + 8u * (2 * kRawStages + i); };
+    auto hf_empty = [&](int i) { return bars + 8u * (2 * kRawStages + kHfStages + i); };
+    constexpr int kTokBar = 2 * (kRawStages + kHfStages);
+    auto tok_full = [&](int i) { return bars + 8u * (kTokBar + i); };
+    auto tok_empty = [&](int i) { return bars + 8u * (kTokBar + kTokStages + i); };
+    const uint32_t acc_full = bars + 8u * (kTokBar + 2 * kTokStages);
+    const uint32_t acc_empty = acc_full + 8u;
+    const uint32_t drain_bar = acc_full + 16u;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kMiscOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
+    int* tile_off = reinterpret_cast<int*>(smem + kTileOffOff);
+
+    const Plan& p = args.p;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i <= p.E; i += kThreads) tile_off[i] = p.tile_off[i];
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kRawStages; ++i) {
+            mbar_init(raw_full(i), 1);
+            mbar_init(raw_empty(i), 128);
+        }
+        for (int i = 0; i < kHfStages; ++i) {
+            mbar_init(hf_full(i), 128);  // the 128 converter threads
+            mbar_init(hf_empty(i), 1);
+        }
+        for (int i = 0; i < kTokStages; ++i) {
+            mbar_init(tok_full(i), 1);   // the token TMA (arrive + bytes)
+            mbar_init(tok_empty(i), 1);
+        }
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, 4);
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) tmem_alloc(smem_u32(tmem_holder), 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    const int total = tile_off[p.E] * args.n_slabs;
+    const int KB = args.k_blocks;
+    const int I = p.I, H = p.H;
+    auto wrow = [&](const Tile& tl, int blk) {
+        if (kL1) return tl.e * args.n_out + (blk ? I : 0) + tl.s * kWR;
+        return tl.e * args.n_out + tl.s * 2 * kWR + blk * kWR;
+    };
+
+    if (warp == 0) {
+        // ---------------- raw weight TMA ----------------
+        if (lane == 0) {
+            int it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                const Tile tl = decode(t, tile_off, p.E, args.n_slabs);
+                const int w0 = wrow(tl, 0), w1 = wrow(tl, 1);
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const int r = it % kRawStages;
+                    if (!mbar_wait(raw_empty(r), ((uint32_t)(it / kRawStages) & 1u) ^ 1u, p.hdr, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t dst = base + kRawOff + r * kRawBytes;
+                    mbar_arrive_expect_tx(raw_full(r), kRawBytes);
+                    tma_load_2d(dst, &tmW, kb * kBK, w0, raw_full(r));
+                    tma_load_2d(dst + kWR * kBK, &tmW, kb * kBK, w1, raw_full(r));
+                }
+            }
+            for (int j = it - kRawStages < 0 ? 0 : it - kRawStages; j < it; ++j)
+                mbar_drain(raw_full(j % kRawStages), (uint32_t)(j / kRawStages) & 1u, p.hdr);
+        }
+    } else if (warp == 10) {
+        // ---------------- token TMA: hi plane rows, then lo plane rows ----------------
+        if (lane == 0) {
+            int it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                const Tile tl = decode(t, tile_off, p.E, args.n_slabs);
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const int b = it % kTokStages;
+                    if (!mbar_wait(tok_empty(b), ((uint32_t)(it / kTokStages) & 1u) ^ 1u, p.hdr, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t dst = base + kTokOff + b * kTokBytes;
+                    mbar_arrive_expect_tx(tok_full(b), (uint32_t)kTokBytes);
+                    for (int pl = 0; pl < 2; ++pl)
+                        for (int i = 0; i < kTok / kTokBox; ++i)
+                            tma_load_2d(dst + (pl * kTok + i * kTokBox) * 128, &tmX, kb * kBK,
+                                        (int)(pl * p.pool_rows) + tl.row0 + i * kTokBox, tok_full(b));
+                }
+            }
+            for (int j = it - kTokStages < 0 ? 0 : it - kTokStages; j < it; ++j)
+                mbar_drain(tok_full(j % kTokStages), (uint32_t)(j / kTokStages) & 1u, p.hdr);
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            int it = 0, tc = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tc) {
+                if (!mbar_wait(acc_empty, ((uint32_t)tc & 1u) ^ 1u, p.hdr, abort_flag)) break;
+                tc_fence_after();
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const int b = it % kHfStages, tb = it % kTokStages;
+                    if (!mbar_wait(hf_full(b), (uint32_t)(it / kHfStages) & 1u, p.hdr, abort_flag) ||
+                        !mbar_wait(tok_full(tb), (uint32_t)(it / kTokStages) & 1u, p.hdr, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa0 = base + kHfOff + b * kABytes, sa1 = sa0 + kWR * 128;
+                    const uint32_t sb = base + kTokOff + tb * kTokBytes;
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                        const uint64_t bd = kmajor_desc(sb, kk);
+                        tc_mma(tmem_base, kmajor_desc(sa0, kk), bd, kIdesc, (kb | kk) != 0);
+                        tc_mma(tmem_base + 256, kmajor_desc(sa1, kk), bd, kIdesc, (kb | kk) != 0);
+                    }
+                    tc_commit(hf_empty(b));
+                    tc_commit(tok_empty(tb));
+                }
+                if (ok) tc_commit(acc_full);
+            }
+            tc_commit(drain_bar);
+            mbar_drain(drain_bar, 0, p.hdr);
+        }
+    } else if (warp >= 6) {
+        // ---------------- weight converters ----------------
+        const int c = threadIdx.x - 192;  // row of each 128-row weight block
+        int it = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            for (int kb = 0; kb < KB; ++kb, ++it) {
+                const int r = it % kRawStages, b = it % kHfStages;
+                bool w_ok = mbar_wait(raw_full(r), (uint32_t)(it / kRawStages) & 1u, p.hdr, abort_flag);
+                w_ok = w_ok && mbar_wait(hf_empty(b), ((uint32_t)(it / kHfStages) & 1u) ^ 1u, p.hdr, abort_flag);
+                if (!__all_sync(0xffffffffu, w_ok)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t* rw = smem + kRawOff + r * kRawBytes;
+                uint8_t* dst = smem + kHfOff + b * kABytes;
+                convert_row(rw, dst, c);
+                convert_row(rw + kWR * kBK, dst + kWR * 128, c);
+                fence_proxy_async_smem();
+                mbar_arrive(raw_empty(r));
+                mbar_arrive(hf_full(b));
+            }
+        }
+    } else {
+        // ---------------- epilogue (warps 2..5) ----------------
+        const int q = warp & 3;
+        int tc = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x, ++tc) {
+            const bool w_ok = mbar_wait(acc_full, (uint32_t)tc & 1u, p.hdr, abort_flag);
+            if (!__all_sync(0xffffffffu, w_ok)) break;
+            tc_fence_after();
+            const Tile tl = decode(t, tile_off, p.E, args.n_slabs);
+            const int n_valid = min(kTok, p.counts[tl.e] - tl.m * kTok);
+            const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16);
+            if constexpr (kL1) {
+                // C = 16 D_hi + D_lo; H = (C * s^W1) * s^X; A = SiLU(H_gate) * H_up, all 128 tokens
+                // (padding tokens come out finite and are never read back as results)
+                const int j = tl.s * kWR + q * 32 + lane;
+                const float* s1 = args.w_scale + (int64_t)tl.e * 2 * I;
+                const float sg = s1[j], su = s1[I + j];
+                for (int c0 = 0; c0 < kTok; c0 += 32) {
+                    const float sx_l = reinterpret_cast<const float*>(p.x_pool_scale)[tl.row0 + c0 + lane];
+                    uint32_t hi[32], lo[32];
+                    float hg[32];
+                    tmem_ld32(tb + c0, hi);
+                    tmem_ld32(tb + kTok + c0, lo);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int tt = 0; tt < 32; ++tt) hg[tt] = __int2float_rn(exact_int(hi[tt], lo[tt]));
+                    tmem_ld32(tb + 256 + c0, hi);
+                    tmem_ld32(tb + 256 + kTok + c0, lo);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int tt = 0; tt < 32; ++tt) {
+                        const float sx = __shfl_sync(0xffffffffu, sx_l, tt);
+                        const float Hg = __fmul_rn(__fmul_rn(hg[tt], sg), sx);
+                        const float Hu = __fmul_rn(__fmul_rn(__int2float_rn(exact_int(hi[tt], lo[tt])), su), sx);
+                        p.a_f32[(int64_t)(tl.row0 + c0 + tt) * I + j] = silu(Hg) * Hu;
+                    }
+                }
+            } else {
+                // D = 16 D_hi + D_lo; Y = (D * s^W2) * s^A; c = bf16(G * Y) to the combine row
+                for (int c0 = 0; c0 < n_valid; c0 += 32) {
+                    const int src_l = c0 + lane < n_valid ? p.pool_src[tl.row0 + c0 + lane] : -1;
+                    const float g_l = src_l >= 0 ? args.topk_weights[src_l] : 0.0f;
+                    const float sa_l = reinterpret_cast<const float*>(p.a_pool_scale)[tl.row0 + c0 + lane];
+#pragma unroll 1
+                    for (int blk = 0; blk < 2; ++blk) {
+                        const int h = tl.s * 2 * kWR + blk * kWR + q * 32 + lane;
+                        const float s2 = args.w_scale[(int64_t)tl.e * H + h];
+                        uint32_t hi[32], lo[32];
+                        tmem_ld32(tb + blk * 256 + c0, hi);
+                        tmem_ld32(tb + blk * 256 + kTok + c0, lo);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int tt = 0; tt < 32; ++tt) {
+                            if (c0 + tt >= n_valid) break;  // uniform across the warp
+                            const int src = __shfl_sync(0xffffffffu, src_l, tt);
+                            const float gw = __shfl_sync(0xffffffffu, g_l, tt);
+                            const float sa = __shfl_sync(0xffffffffu, sa_l, tt);
+                            const float y = __fmul_rn(__fmul_rn(__int2float_rn(exact_int(hi[tt], lo[tt])), s2), sa);
+                            if (src >= 0) p.comb[(int64_t)src * H + h] = float_to_bf16_bits(__fmul_rn(gw, y));
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, 512);
+}
+
+template <bool kL1>
+cudaError_t launch_int8(const Plan& p, const void* w, const void* w_scale, const float* topk_weights, cudaStream_t s) {
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(tc_int8_kernel<kL1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    const int n_out = kL1 ? 2 * p.I : p.H;
+    const int kin = kL1 ? p.H : p.I;
+    CUtensorMap tmW, tmX;
+    if (!tc_make_map_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w, (uint64_t)kin, (uint64_t)p.E * n_out, kBK, kWR,
+                        CU_TENSOR_MAP_SWIZZLE_64B))
+        return cudaErrorInvalidValue;
+    if (!tc_make_map_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, kL1 ? (const void*)p.x_planes : (const void*)p.a_planes,
+                        (uint64_t)kin, 2 * (uint64_t)p.pool_rows, kBK, kTokBox, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    I8Args args{p, static_cast<const float*>(w_scale), topk_weights, kL1 ? p.I / kWR : p.H / (2 * kWR), kin / kBK,
+                n_out};
+    const int64_t max_tiles = (p.pool_rows / kTok) * args.n_slabs;
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(max_tiles, tc_num_sms()));
+    tc_int8_kernel<kL1><<<grid, kThreads, kSmem, s>>>(tmW, tmX, args);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool int8_tc_supported(const Plan& p, int stage) {
+    if (p.mode != MOE_A8W8_INT8 || p.E > kMaxExperts || !tc_encode_available()) return false;
+    if (stage == 1) return p.I % kWR == 0 && p.H % kBK == 0;
+    return p.H % (2 * kWR) == 0 && p.I % kBK == 0;
+}
+
+cudaError_t launch_l1_int8_tc(const Plan& p, const void* w1, const void* w1_scale, cudaStream_t s) {
+    return launch_int8<true>(p, w1, w1_scale, nullptr, s);
+}
+
+cudaError_t launch_l2_int8_tc(const Plan& p, const void* w2, const void* w2_scale, const float* topk_weights,
+                              cudaStream_t s) {
+    return launch_int8<false>(p, w2, w2_scale, topk_weights, s);
+}
+
+}  // namespace moe
