@@ -207,23 +207,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ---------------- TMA producer: weights (two 64-row boxes) and tokens ----------------
         if (lane == 0) {
-            // the weight boxes are also prefetched into L2 two rings' depth ahead of the loads
-            int pt = blockIdx.x, pkb = 0;
-            Tile ptl = tile_of(pt < total ? pt : 0);
-            auto prefetch_next = [&]() {
-                if (pt >= total) return;
-                const int na = atoms_of(pkb);
-                for (int at = 0; at < na; ++at) {
-                    tma_prefetch_2d(&tmW, pkb * kBK + at * kAtomK, wrow(ptl, 0));
-                    tma_prefetch_2d(&tmW, pkb * kBK + at * kAtomK, wrow(ptl, 1));
-                }
-                if (++pkb == KB) {
-                    pkb = 0;
-                    pt += gridDim.x;
-                    if (pt < total) ptl = tile_of(pt);
-                }
-            };
-            for (int i = 0; i < 2 * kStages; ++i) prefetch_next();
             int it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
@@ -231,7 +214,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int n = (tl.n_valid + 15) & ~15;
                 const int w0 = wrow(tl, 0), w1 = wrow(tl, 1);
                 for (int kb = 0; kb < KB; ++kb, ++it) {
-                    prefetch_next();
                     const int s = it % kStages;
                     if (!mbar_wait(empty_bar(s), ((uint32_t)(it / kStages) & 1u) ^ 1u, p.hdr, abort_flag)) {
                         ok = false;

@@ -47,7 +47,6 @@ constexpr int kStageBytes = kABytes + kBBytes; // 48 KB
 constexpr int kThreads = 192;
 constexpr int kTmemCols = 512;                 // two 256-column fp32 accumulators
 constexpr int kMaxExperts = 1024;
-constexpr int kPrefetch = 8;                   // k-blocks of weights prefetched into L2 ahead of the loads
 
 // Instruction descriptor of tcgen05.mma.kind::f16: D fp32 (bits 4-5 = 1), A bf16 (bits 7-9 =
 // 1), B bf16 (bits 10-12 = 1), A K-major (bit 15 = 0), B MN-major (bit 16 = 1), N >> 3 in
@@ -151,36 +150,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         if (lane == 0) {
             // ---------------- TMA producer ----------------
-            // weight boxes are also prefetched into L2 kPrefetch k-blocks ahead of the ring
-            int pt = blockIdx.x, pkb = 0;
-            Tile ptl = decode_tile(pt < total ? pt : 0, tile_off, p.E, args.n_tiles);
-            auto prefetch_next = [&]() {
-                if (pt >= total) return;
-                const int y = ptl.e * args.k_rows + pkb * kBK;
-                if (kL1) {
-                    const int g0 = ptl.n * 128, u0 = p.I + ptl.n * 128;
-                    tma_prefetch_2d(&tmB, g0, y);
-                    tma_prefetch_2d(&tmB, g0 + 64, y);
-                    tma_prefetch_2d(&tmB, u0, y);
-                    tma_prefetch_2d(&tmB, u0 + 64, y);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) tma_prefetch_2d(&tmB, ptl.n * kBN + j * 64, y);
-                }
-                if (++pkb == KB) {
-                    pkb = 0;
-                    pt += gridDim.x;
-                    if (pt < total) ptl = decode_tile(pt, tile_off, p.E, args.n_tiles);
-                }
-            };
-            for (int i = 0; i < kPrefetch; ++i) prefetch_next();
             int it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 const Tile tl = decode_tile(t, tile_off, p.E, args.n_tiles);
                 const int wrow = tl.e * args.k_rows;
                 for (int kb = 0; kb < KB; ++kb, ++it) {
-                    prefetch_next();
                     const int s = it % kStages;
                     const uint32_t ph = (uint32_t)(it / kStages) & 1u;
                     if (!mbar_wait(empty_bar(s), ph ^ 1u, p.hdr, abort_flag)) {
