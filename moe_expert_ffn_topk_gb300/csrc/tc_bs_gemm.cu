@@ -19,9 +19,12 @@
 //
 // Operand staging: weights by TMA with 128-byte swizzle (e2m1 through the 16U4_ALIGN16B element
 // type, which expands each packed 8-byte group of 16 codes into a 16-byte slot: the 4-bit
-// operand layout of kind::mxf8f6f4; its transaction count is the packed size); tokens by TMA of
-// the pool's e4m3 codes in boxes of 16 rows; scales by four "scale warps" that write the stage's
-// UE8M0 bytes into tensor memory with tcgen05.st. Layout the MMA reads (measured on this GPU):
+// operand layout of kind::mxf8f6f4; its transaction count is the packed size), one copy per K
+// atom for all 128 rows (L1: a 4-D box [K][64 rows][gate, up][expert]); tokens by one TMA copy
+// per K atom of the sub-tile's kNT pool rows (e4m3 codes; rows past the sub-tile feed no MMA
+// column); scales by four "scale warps" that write the stage's UE8M0 bytes into tensor memory
+// with one tcgen05.st per K atom. Each TMA instruction costs the producer about 75 cycles to
+// issue (measured), so a stage is moved in as few copies as the layout allows. Layout the MMA reads (measured on this GPU):
 // the scale of A row r is in TMEM lane r, column base + r/32, byte = the K group (a_sf_id); the
 // scale of B row n is in lane 32*q + n%32 of every lane quarter q, column base + n/32, byte =
 // b_sf_id; one 32-bit word holds a row's 4 scales of a stage.
@@ -47,13 +50,11 @@ using namespace tc;
 constexpr int kWR = 128;          // weight rows per tile (MMA M)
 constexpr int kHalf = 64;         // L1: gate rows, then up rows
 constexpr int kAtomK = 128;       // K of one 128-byte swizzle atom (a stage holds kAtoms of them)
-constexpr int kTokBox = 16;       // token rows per TMA box
 constexpr int kThreads = 320;
 constexpr int kMaxExperts = 1024;
 constexpr int kABytes = kWR * 128;
 constexpr int kSfCol0 = 256;      // first TMEM column of the scale ring
 constexpr int kSfColsPerStage = 16;  // per K atom: SFA 4 columns, SFB up to 4 columns
-constexpr int kLookahead = 3;     // scale loads issued this many stages ahead
 constexpr int kEpiBar = 1;        // named barrier of the 4 epilogue warps
 
 template <int kNT, int kStages, int kAtoms>
@@ -61,13 +62,15 @@ struct BsCfg {
     static constexpr int kBBytes = kNT * 128;                          // one K atom of tokens
     static constexpr int kStageBytes = kAtoms * (kABytes + kBBytes);   // [A atoms][B atoms]
     static constexpr int kBarOff = kStages * kStageBytes;
-    static constexpr int kNumBars = 2 * kStages + 4 + 1;
-    static constexpr int kXbufOff = kBarOff + 8 * kNumBars;           // 32 tokens x 64 up values (fp32)
+    static constexpr int kNumBars = 2 * kStages + 4 + 1 + 2;  // + two token-scale buffers
+    static constexpr int kXbufOff = kBarOff + 8 * kNumBars;           // 2 x 16 tokens x 64 outputs (fp32)
     static constexpr int kMiscOff = kXbufOff + 32 * kHalf * 4;
     static constexpr int kTileOffOff = kMiscOff + 16;                 // int[E+1] 128-row tiles per expert
     static constexpr int kSubOffOff = kTileOffOff + 4 * (kMaxExperts + 1);   // int[E+1] kNT sub-tiles
     static constexpr int kCountsOff = kSubOffOff + 4 * (kMaxExperts + 1);    // int[E]
-    static constexpr size_t kSmem = 1024 + (size_t)kCountsOff + 4 * kMaxExperts;
+    static constexpr int kTokWords = kNT < 32 ? 1 : kNT / 32;                 // token scale words per lane
+    static constexpr int kTokSfOff = (kCountsOff + 4 * kMaxExperts + 15) & ~15;  // u32[2][kTokWords][8][32]
+    static constexpr size_t kSmem = 1024 + (size_t)kTokSfOff + 2 * kTokWords * 8 * 32 * 4;
     static_assert(kSmem <= 232448, "shared memory");
     static_assert(2 * kNT <= kSfCol0 && kSfCol0 + kStages * kSfColsPerStage <= 512, "tensor memory");
     static_assert(kAtoms == 1 || kAtoms == 2, "atoms per stage");
@@ -122,8 +125,12 @@ __device__ __forceinline__ void tc_mma_bs(uint32_t d, uint64_t adesc, uint64_t b
         : "memory");
 }
 
-__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+// 8 consecutive columns of the warp's 32 lanes, one 32-bit word per lane and column
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t a4,
+                                         uint32_t a5, uint32_t a6, uint32_t a7) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr), "r"(a0),
+                 "r"(a1), "r"(a2), "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
+                 : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync %0, 128;" ::"n"(kEpiBar) : "memory"); }
@@ -146,6 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto acc_full = [&](int a) { return bars + 8u * (2 * kStages + a); };
     auto acc_empty = [&](int a) { return bars + 8u * (2 * kStages + 2 + a); };
     const uint32_t drain_bar = bars + 8u * (2 * kStages + 4);
+    auto tok_bar = [&](int b) { return bars + 8u * (2 * kStages + 5 + b); };
     float* xbuf = reinterpret_cast<float*>(smem + Cfg::kXbufOff);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kMiscOff + 4);
@@ -176,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (threadIdx.x == 32) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(full_bar(s), 1 + 128);  // TMA (arrive + bytes) + 128 scale writers
+            mbar_init(full_bar(s), 1 + 4);  // TMA (arrive + bytes) + the 4 scale-writer warps
             mbar_init(empty_bar(s), 1);
         }
         for (int a = 0; a < 2; ++a) {
@@ -184,6 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(acc_empty(a), 4);
         }
         mbar_init(drain_bar, 1);
+        for (int b = 0; b < 2; ++b) mbar_init(tok_bar(b), 4);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -211,8 +220,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 const Tile tl = tile_of(t);
-                const int n = (tl.n_valid + 15) & ~15;
-                const int w0 = wrow(tl, 0), w1 = wrow(tl, 1);
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int s = it % kStages;
                     if (!mbar_wait(empty_bar(s), ((uint32_t)(it / kStages) & 1u) ^ 1u, p.hdr, abort_flag)) {
@@ -221,14 +228,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const uint32_t sa = base + s * Cfg::kStageBytes, sb = sa + kAtoms * kABytes;
                     const int na = atoms_of(kb);
-                    mbar_arrive_expect_tx(full_bar(s), (uint32_t)na * (2 * kABoxTx + (uint32_t)n * 128u));
+                    mbar_arrive_expect_tx(full_bar(s), (uint32_t)na * (2 * kABoxTx + (uint32_t)Cfg::kBBytes));
                     for (int at = 0; at < na; ++at) {
                         const int x = kb * kBK + at * kAtomK;
-                        tma_load_2d(sa + at * kABytes, &tmW, x, w0, full_bar(s));
-                        tma_load_2d(sa + at * kABytes + kHalf * 128, &tmW, x, w1, full_bar(s));
-                        for (int i = 0; i < n / kTokBox; ++i)
-                            tma_load_2d(sb + at * Cfg::kBBytes + i * kTokBox * 128, &tmX, x, tl.row0 + i * kTokBox,
-                                        full_bar(s));
+                        if constexpr (kL1)
+                            tma_load_4d(sa + at * kABytes, &tmW, x, tl.s * kHalf, 0, tl.e, full_bar(s));
+                        else
+                            tma_load_2d(sa + at * kABytes, &tmW, x, wrow(tl, 0), full_bar(s));
+                        tma_load_2d(sb + at * Cfg::kBBytes, &tmX, x, tl.row0, full_bar(s));
                     }
                 }
             }
@@ -272,94 +279,135 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp >= 6) {
         // ---------------- scale writers ----------------
+        // Each lane owns weight row r = 32q + lane of the tile and, for the token rows, the group
+        // c = q: rows 32c + lane. The scale words (one per row and 128-element K atom) are read 8
+        // atoms at a time, so the 32 bytes a lane reads fill one sector, and two blocks ahead of
+        // their use, which covers the load latency of a busy memory system. Token words are
+        // needed by all four warps (the MMA reads them in every lane quarter): each warp
+        // publishes its group through shared memory, guarded by an mbarrier per buffer.
         const int q = warp & 3;  // lane quarter this warp writes
         const int spr = args.kin / 32;
         const int r = 32 * q + lane;  // weight row within the tile
-        constexpr int kTokWords = kNT < 32 ? 1 : kNT / 32;
-        struct Words {
-            uint32_t a[kAtoms], b[kAtoms][kTokWords];
+        const int n_words = args.kin / kAtomK;  // scale words per row
+        const int n_blk = (n_words + 7) >> 3;
+        constexpr int kTokWords = Cfg::kTokWords;
+        constexpr int kStagesPerBlk = 8 / kAtoms;
+        const int cq = q % kTokWords;  // token group this warp loads
+        uint32_t* tok_sf = reinterpret_cast<uint32_t*>(smem + Cfg::kTokSfOff);
+        // Raw words only: nothing computed from a load happens before the block is used, so
+        // the loads stay in flight (addresses are clamped into the tensors instead of predicated)
+        struct Blk {
+            uint32_t a[8], b[8];
+            bool tok_valid;
         };
-        // the lookahead tile is decoded once per tile, not once per stage
-        Tile ltile{};
-        const uint32_t* wsrow = nullptr;
-        // word g = the 4 UE8M0 bytes of K atom g (elements 128g .. 128g+127) of a row
-        auto load_words = [&](int kb) {
-            Words w;
-            const Tile& tl = ltile;
-            const int na = atoms_of(kb);
+        auto load_blk = [&](int t, int blk) {
+            Blk w;
+            const Tile tl = tile_of(t);
+            const int wr = wrow(tl, r >= kHalf) + (r & (kHalf - 1));
+            const uint32_t* ws = reinterpret_cast<const uint32_t*>(args.w_scale + (int64_t)wr * spr);
+            const int n = 32 * cq + lane;
+            w.tok_valid = n < tl.n_valid;
+            const int64_t row = tl.row0 + min(n, kNT - 1);  // a pool row of the sub-tile
 #pragma unroll
-            for (int at = 0; at < kAtoms; ++at) {
-                const int g = kb * kAtoms + at;
-                w.a[at] = at < na ? __ldg(wsrow + g) : 0x7f7f7f7fu;
-#pragma unroll
-                for (int c = 0; c < kTokWords; ++c) {
-                    const int n = 32 * c + lane;
-                    uint32_t v = 0x7f7f7f7fu;  // 1.0 for the padding tokens
-                    if (at < na && n < tl.n_valid) {
-                        const int64_t row = tl.row0 + n;
-                        if constexpr (kL1 && kFp4) {
-                            const uint32_t bits =
-                                __float_as_uint(reinterpret_cast<const float*>(p.x_pool_scale)[row * (H / 128) + g]);
-                            v = ((bits >> 23) & 0xffu) * 0x01010101u;  // power-of-two scale -> its UE8M0 byte, x4
-                        } else if constexpr (kL1) {
-                            v = __ldg(reinterpret_cast<const uint32_t*>(p.x_pool_scale + row * (H / 32)) + g);
-                        } else {
-                            v = __ldg(reinterpret_cast<const uint32_t*>(p.a_pool_scale + row * (I / 32)) + g);
-                        }
-                    }
-                    w.b[at][c] = v;
-                }
+            for (int i = 0; i < 8; ++i) {
+                const int g = min(blk * 8 + i, n_words - 1);  // K atom: elements 128g .. 128g+127
+                w.a[i] = __ldg(ws + g);
+                if constexpr (kL1 && kFp4)
+                    w.b[i] = __float_as_uint(__ldg(reinterpret_cast<const float*>(p.x_pool_scale) + row * (H / 128) + g));
+                else if constexpr (kL1)
+                    w.b[i] = __ldg(reinterpret_cast<const uint32_t*>(p.x_pool_scale + row * (H / 32)) + g);
+                else
+                    w.b[i] = __ldg(reinterpret_cast<const uint32_t*>(p.a_pool_scale + row * (I / 32)) + g);
             }
             return w;
         };
-        int lt = blockIdx.x, lkb = 0;  // lookahead iterator over the producer's (tile, k-block) sequence
-        auto set_tile = [&]() {
-            if (lt < total) {
-                ltile = tile_of(lt);
-                const int wr = wrow(ltile, r >= kHalf) + (r & (kHalf - 1));
-                wsrow = reinterpret_cast<const uint32_t*>(args.w_scale + (int64_t)wr * spr);
+        // token word as the MMA reads it: 4 UE8M0 bytes; 1.0 for the padding tokens
+        auto tok_word = [&](const Blk& w, uint32_t raw) -> uint32_t {
+            if (!w.tok_valid) return 0x7f7f7f7fu;
+            if constexpr (kL1 && kFp4) return ((raw >> 23) & 0xffu) * 0x01010101u;  // power-of-two fp32 scale
+            return raw;
+        };
+        // (tile, block) positions in the producer's order: t0 is being written out, t1 and t2 are
+        // in flight
+        auto next_pos = [&](int& t, int& blk) {
+            if (++blk == n_blk) {
+                blk = 0;
+                t += gridDim.x;
             }
         };
-        auto advance = [&]() {
-            if (++lkb == KB) {
-                lkb = 0;
-                lt += gridDim.x;
-                set_tile();
-            }
-        };
-        set_tile();
-        Words ring[kLookahead];
-#pragma unroll
-        for (int i = 0; i < kLookahead; ++i) {
-            if (lt < total) ring[i] = load_words(lkb);
-            advance();
-        }
-        int it = 0;
+        int t0 = blockIdx.x, b0 = 0, t1 = t0, b1 = b0;
+        next_pos(t1, b1);
+        int t2 = t1, b2 = b1;
+        int it = 0, nb = 0;  // stages and blocks done
         bool ok = true;
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            for (int kb = 0; kb < KB; ++kb, ++it) {
-                const Words w = ring[0];
+        // writes out block (t0, b0) from `use` after starting the loads of block (t2, b2) into
+        // `fill`; the three buffers rotate by name, so no register holding a load in flight is copied
+        auto run_block = [&](const Blk& use, Blk& fill) -> bool {
+            if (t0 >= total || !ok) return false;
+            next_pos(t2, b2);
+            if (t2 < total) fill = load_blk(t2, b2);
+            const int buf = nb & 1;
+            if constexpr (kTokWords > 1) {
 #pragma unroll
-                for (int i = 0; i + 1 < kLookahead; ++i) ring[i] = ring[i + 1];
-                if (lt < total) ring[kLookahead - 1] = load_words(lkb);
-                advance();
+                for (int i = 0; i < 8; ++i) tok_sf[((buf * kTokWords + cq) * 8 + i) * 32 + lane] = tok_word(use, use.b[i]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tok_bar(buf));
+                const bool t_ok = mbar_wait(tok_bar(buf), (uint32_t)(nb >> 1) & 1u, p.hdr, abort_flag);
+                if (!__all_sync(0xffffffffu, t_ok)) return ok = false;
+            }
+            // working copy of the block (its loads landed a block ago), shifted by one stage's
+            // words per stage so the rolled loop below indexes registers statically
+            uint32_t wa[8], wb[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                wa[i] = use.a[i];
+                wb[i] = tok_word(use, use.b[i]);
+            }
+#pragma unroll 1
+            for (int j = 0; j < kStagesPerBlk; ++j) {
+                const int kb = b0 * kStagesPerBlk + j;
+                if (kb >= KB) break;  // uniform across the CTA's scale warps
                 const int s = it % kStages;
                 const bool w_ok = mbar_wait(empty_bar(s), ((uint32_t)(it / kStages) & 1u) ^ 1u, p.hdr, abort_flag);
-                if (!__all_sync(0xffffffffu, w_ok)) {
-                    ok = false;
-                    break;
-                }
+                if (!__all_sync(0xffffffffu, w_ok)) return ok = false;
                 const uint32_t sf = tmem_base + ((uint32_t)(32 * q) << 16) + kSfCol0 + s * kSfColsPerStage;
+                // per K atom 8 columns: the A word in columns 0-3 (the MMA reads column q of lane
+                // quarter q), the token words in columns 4.. (unused columns get copies)
 #pragma unroll
                 for (int at = 0; at < kAtoms; ++at) {
-                    tmem_st1(sf + 8 * at + q, w.a[at]);
+                    const int i = j * kAtoms + at;
+                    uint32_t tw[4];
 #pragma unroll
-                    for (int c = 0; c < kTokWords; ++c) tmem_st1(sf + 8 * at + 4 + c, w.b[at][c]);
+                    for (int c = 0; c < 4; ++c) {
+                        if constexpr (kTokWords > 1)
+                            tw[c] = tok_sf[((buf * kTokWords + c % kTokWords) * 8 + i) * 32 + lane];
+                        else
+                            tw[c] = wb[at];
+                    }
+                    tmem_st8(sf + 8 * at, wa[at], wa[at], wa[at], wa[at], tw[0], tw[1], tw[2], tw[3]);
+                }
+#pragma unroll
+                for (int i = 0; i + kAtoms < 8; ++i) {
+                    wa[i] = wa[i + kAtoms];
+                    wb[i] = wb[i + kAtoms];
                 }
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(full_bar(s));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(full_bar(s));
+                ++it;
             }
+            t0 = t1;
+            b0 = b1;
+            t1 = t2;
+            b1 = b2;
+            ++nb;
+            return true;
+        };
+        Blk A{}, B{}, C{};
+        if (t0 < total) A = load_blk(t0, b0);
+        if (t1 < total) B = load_blk(t1, b1);
+        while (run_block(A, C) && run_block(B, A) && run_block(C, B)) {
         }
     } else {
         // ---------------- epilogue (warps 2..5) ----------------
@@ -374,32 +422,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int n = (tl.n_valid + 15) & ~15;
             const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * kNT);
             if constexpr (kL1) {
-                // lanes 0-63: gate rows, lanes 64-127: up rows of the same 64 outputs j
+                // lanes 0-63 hold the gate rows and lanes 64-127 the up rows of the same 64 outputs j.
+                // Of each 32-token chunk the gate warps finish tokens 0-15 and the up warps tokens
+                // 16-31; each hands its partner the other half through xbuf.
                 const bool gate = q < 2;
                 const int jl = 32 * (q & 1) + lane;  // output within the tile
                 const int j = tl.s * kHalf + jl;
+                float* xg = xbuf;               // [16 tokens][64 outputs]: gate values of tokens 16-31
+                float* xu = xbuf + 16 * kHalf;  // [16 tokens][64 outputs]: up values of tokens 0-15
+                // A = SiLU(gate) * up, then MX FP8 (one UE8M0 exponent per 32 outputs of a token)
+                auto finish = [&](int64_t row, float g, float u) {
+                    const float av = silu(g) * u;
+                    const float amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(av))));
+                    const int ex = mx_exponent_e4m3(amax);
+                    p.a_pool[row * I + j] = float_to_e4m3_satfinite(av * exp2_neg_int(ex));
+                    if (lane == 0) p.a_pool_scale[row * (I / 32) + (j >> 5)] = (uint8_t)(ex + 127);
+                };
                 for (int c0 = 0; c0 < n; c0 += 32) {
                     uint32_t v[32];
                     tmem_ld32(tb + c0, v);
                     tmem_ld_wait();
-                    if (!gate) {
-#pragma unroll
-                        for (int tt = 0; tt < 32; ++tt) xbuf[tt * kHalf + jl] = __uint_as_float(v[tt]);
-                    }
-                    epi_sync();
                     if (gate) {
 #pragma unroll
-                        for (int tt = 0; tt < 32; ++tt) {
-                            if (c0 + tt >= n) break;  // uniform across the warp
-                            const float av = silu(__uint_as_float(v[tt])) * xbuf[tt * kHalf + jl];
-                            float amax = fabsf(av);
+                        for (int tt = 0; tt < 16; ++tt) xg[tt * kHalf + jl] = __uint_as_float(v[16 + tt]);
+                    } else {
 #pragma unroll
-                            for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-                            const int ex = mx_exponent_e4m3(amax);
-                            const int64_t row = tl.row0 + c0 + tt;
-                            p.a_pool[row * I + j] = float_to_e4m3_satfinite(av * exp2_neg_int(ex));
-                            if (lane == 0) p.a_pool_scale[row * (I / 32) + (j >> 5)] = (uint8_t)(ex + 127);
-                        }
+                        for (int tt = 0; tt < 16; ++tt) xu[tt * kHalf + jl] = __uint_as_float(v[tt]);
+                    }
+                    epi_sync();
+                    const int64_t row0 = tl.row0 + c0 + (gate ? 0 : 16);
+                    if (gate) {  // n is a multiple of 16: tokens 0-15 of the chunk are all below n
+#pragma unroll
+                        for (int tt = 0; tt < 16; ++tt) finish(row0 + tt, __uint_as_float(v[tt]), xu[tt * kHalf + jl]);
+                    } else if (c0 + 16 < n) {
+#pragma unroll
+                        for (int tt = 0; tt < 16; ++tt) finish(row0 + tt, xg[tt * kHalf + jl], __uint_as_float(v[16 + tt]));
                     }
                     epi_sync();
                 }
@@ -412,8 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld32(tb + c0, y);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int tt = 0; tt < 32; ++tt) {
-                        if (c0 + tt >= tl.n_valid) break;  // uniform across the warp
+                    for (int tt = 0; tt < 32; ++tt) {  // src < 0 beyond the sub-tile's routed rows
                         const int src = __shfl_sync(0xffffffffu, src_l, tt);
                         const float gw = __shfl_sync(0xffffffffu, g_l, tt);
                         if (src >= 0) p.comb[(int64_t)src * H + h] = float_to_bf16_bits(__fmul_rn(gw, __uint_as_float(y[tt])));
@@ -457,18 +513,32 @@ cudaError_t launch_bs(const Plan& p, const void* w, const void* w_scale, const f
     const int n_out = kL1 ? 2 * p.I : p.H;
     const int kin = kL1 ? p.H : p.I;
     CUtensorMap tmW, tmX;
-    const bool ok_w = MODE == MOE_A8W4_FP8_FP4
-                          ? tc_make_map_2d_packed4(&tmW, w, (uint64_t)kin, (uint64_t)p.E * n_out, kAtomK, kHalf)
-                          : tc_make_map_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w, (uint64_t)kin,
-                                           (uint64_t)p.E * n_out, kAtomK, kHalf, CU_TENSOR_MAP_SWIZZLE_128B);
+    constexpr bool kFp4 = MODE == MOE_A8W4_FP8_FP4;
+    const CUtensorMapDataType wtype = kFp4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    const uint64_t pitch = kFp4 ? (uint64_t)kin / 2 : (uint64_t)kin;  // bytes per weight row
+    bool ok_w;
+    if (kL1) {
+        // [K][row within the gate or up half][half][expert]: one box holds a tile's 64 gate and 64 up rows
+        const uint64_t dims[4] = {(uint64_t)kin, (uint64_t)p.I, 2, (uint64_t)p.E};
+        const uint64_t strides[3] = {pitch, pitch * p.I, pitch * 2 * p.I};
+        const uint32_t box[4] = {kAtomK, kHalf, 2, 1};
+        ok_w = tc_make_map_nd(&tmW, wtype, 4, w, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    } else {
+        const uint64_t dims[2] = {(uint64_t)kin, (uint64_t)p.E * n_out};
+        const uint64_t strides[1] = {pitch};
+        const uint32_t box[2] = {kAtomK, kWR};
+        ok_w = tc_make_map_nd(&tmW, wtype, 2, w, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    }
     if (!ok_w) return cudaErrorInvalidValue;
-    if (!tc_make_map_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kL1 ? (const void*)p.x_pool : (const void*)p.a_pool,
-                        (uint64_t)kin, (uint64_t)p.pool_rows, kAtomK, kTokBox, CU_TENSOR_MAP_SWIZZLE_128B))
-        return cudaErrorInvalidValue;
-    BsArgs args{p, static_cast<const uint8_t*>(w_scale), topk_weights, kL1 ? p.I / kHalf : p.H / kWR, 0, n_out, kin};
     // few routed rows per expert: the weights stream from HBM; 16-token sub-tiles and K = 256
     // stages (whole 128-byte lines of every weight row per load)
-    if ((int64_t)p.T * p.K <= (int64_t)16 * p.E) return launch_bs_cfg<MODE, kL1, 16, 5, 2>(p, tmW, tmX, args, s);
+    const bool decode = (int64_t)p.T * p.K <= (int64_t)16 * p.E;
+    // token rows: one copy brings the sub-tile's kNT pool rows
+    if (!tc_make_map_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kL1 ? (const void*)p.x_pool : (const void*)p.a_pool,
+                        (uint64_t)kin, (uint64_t)p.pool_rows, kAtomK, decode ? 16u : 128u, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    BsArgs args{p, static_cast<const uint8_t*>(w_scale), topk_weights, kL1 ? p.I / kHalf : p.H / kWR, 0, n_out, kin};
+    if (decode) return launch_bs_cfg<MODE, kL1, 16, 5, 2>(p, tmW, tmX, args, s);
     return launch_bs_cfg<MODE, kL1, 128, 6, 1>(p, tmW, tmX, args, s);
 }
 

@@ -66,6 +66,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, int w,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+        : "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -150,6 +158,9 @@ int tc_num_sms();
 // Packed e2m1 tensor [outer, inner_elems] (two codes per byte): TMA expands every 8-byte group of
 // 16 codes into a 16-byte slot of the 128-byte-swizzled shared tile (the 4-bit operand layout of
 // kind::mxf8f6f4); the transaction byte count is the packed size.
+// Rank-1..5 tiled map: dims and box in elements (innermost first), strides in bytes of dims 1..rank-1.
+bool tc_make_map_nd(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* ptr, const uint64_t* dims,
+                    const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swizzle);
 bool tc_make_map_2d_packed4(CUtensorMap* map, const void* ptr, uint64_t inner_elems, uint64_t outer,
                             uint32_t box_inner, uint32_t box_outer);
 
