@@ -43,9 +43,12 @@ __device__ __forceinline__ float e4m3_to_float(uint8_t c) {
     return __half2float(__half(h));
 }
 
-// float -> e4m3fn code, round to nearest even, saturating to +-448
+// float -> e4m3fn code, round to nearest even, saturating to +-448 (the PTX conversion: of the
+// two converted operands the second lands in the low byte)
 __device__ __forceinline__ uint8_t float_to_e4m3_satfinite(float v) {
-    return static_cast<uint8_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
+    uint16_t pair;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(0.0f), "f"(v));
+    return static_cast<uint8_t>(pair & 0xffu);
 }
 
 // e2m1 code (low 4 bits) -> float: sign | 2 exponent bits (bias 1) | 1 mantissa bit
@@ -65,12 +68,15 @@ __device__ __forceinline__ float ue8m0_to_float(uint8_t s) {
 // [-127, 127]; amax = 0 gives -127. For emax = 448 = 0.875 * 2^9: with amax = m * 2^x,
 // m in [0.5, 1), amax / 448 lies in (2^(x-10), 2^(x-9)] when m <= 0.875, else in
 // (2^(x-9), 2^(x-8)).
+// Read from the bits: a normal amax has x = (biased exponent) - 126 and m <= 0.875 exactly when
+// its 23 fraction bits are <= 0.75 * 2^23; a subnormal amax gives x <= -125, so e = -127.
 __device__ __forceinline__ int mx_exponent_e4m3(float amax) {
     if (!(amax > 0.0f)) return -127;
-    int x;
-    float m = frexpf(amax, &x);
-    int e = (m <= 0.875f) ? x - 9 : x - 8;
-    return e < -127 ? -127 : (e > 127 ? 127 : e);
+    const uint32_t bits = __float_as_uint(amax);
+    const int be = (int)(bits >> 23);
+    if (be == 0) return -127;
+    const int e = (bits & 0x7fffffu) <= 0x600000u ? be - 126 - 9 : be - 126 - 8;
+    return e > 127 ? 127 : e;
 }
 
 // 2^-e as float for e in [-127, 126] (exact power of two)
@@ -78,8 +84,10 @@ __device__ __forceinline__ float exp2_neg_int(int e) {
     return __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
 }
 
+// SiLU(z) = z / (1 + e^-z) with the approximate exp and divide (a few ulp of fp32, far below
+// the bf16 / e4m3 rounding that follows, and branch-free; for z < -87 the quotient is -0)
 __device__ __forceinline__ float silu(float z) {
-    return z / (1.0f + expf(-z));
+    return __fdividef(z, 1.0f + __expf(-z));
 }
 
 }  // namespace moe

@@ -412,13 +412,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ---------------- epilogue (warps 2..5) ----------------
         const int q = warp & 3;
+        constexpr int kChunks = (kNT + 31) / 32;  // 32-token chunks of a sub-tile
         int tc = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++tc) {
             const int a = tc & 1;
+            const Tile tl = tile_of(t);
+            // L2: destination slot and gate weight of each row, read while the MMAs of this tile
+            // still run (two dependent loads that would otherwise sit on the epilogue's path)
+            int src_l[kChunks];
+            float g_l[kChunks];
+            if constexpr (!kL1) {
+#pragma unroll
+                for (int ci = 0; ci < kChunks; ++ci) {
+                    const int n = 32 * ci + lane;
+                    src_l[ci] = n < tl.n_valid ? __ldg(p.pool_src + tl.row0 + n) : -1;
+                }
+#pragma unroll
+                for (int ci = 0; ci < kChunks; ++ci) g_l[ci] = src_l[ci] >= 0 ? __ldg(args.topk_weights + src_l[ci]) : 0.0f;
+            }
             const bool w_ok = mbar_wait(acc_full(a), (uint32_t)(tc >> 1) & 1u, p.hdr, abort_flag);
             if (!__all_sync(0xffffffffu, w_ok)) break;
             tc_fence_after();
-            const Tile tl = tile_of(t);
             const int n = (tl.n_valid + 15) & ~15;
             const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * kNT);
             if constexpr (kL1) {
@@ -430,14 +444,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int j = tl.s * kHalf + jl;
                 float* xg = xbuf;               // [16 tokens][64 outputs]: gate values of tokens 16-31
                 float* xu = xbuf + 16 * kHalf;  // [16 tokens][64 outputs]: up values of tokens 0-15
-                // A = SiLU(gate) * up, then MX FP8 (one UE8M0 exponent per 32 outputs of a token)
-                auto finish = [&](int64_t row, float g, float u) {
-                    const float av = silu(g) * u;
-                    const float amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(av))));
-                    const int ex = mx_exponent_e4m3(amax);
-                    p.a_pool[row * I + j] = float_to_e4m3_satfinite(av * exp2_neg_int(ex));
-                    if (lane == 0) p.a_pool_scale[row * (I / 32) + (j >> 5)] = (uint8_t)(ex + 127);
-                };
                 for (int c0 = 0; c0 < n; c0 += 32) {
                     uint32_t v[32];
                     tmem_ld32(tb + c0, v);
@@ -450,31 +456,56 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int tt = 0; tt < 16; ++tt) xu[tt * kHalf + jl] = __uint_as_float(v[tt]);
                     }
                     epi_sync();
-                    const int64_t row0 = tl.row0 + c0 + (gate ? 0 : 16);
-                    if (gate) {  // n is a multiple of 16: tokens 0-15 of the chunk are all below n
+                    // n is a multiple of 16: a warp's 16 tokens are all below n or all above
+                    if (gate || c0 + 16 < n) {
+                        const int64_t row0 = tl.row0 + c0 + (gate ? 0 : 16);
+                        uint32_t my_sc = 0;  // lane tt keeps the UE8M0 byte of token tt
+                        // A = SiLU(gate) * up, then MX FP8: one exponent per 32 outputs of a token.
+                        // Branch-free, so the 16 tokens' dependency chains overlap.
 #pragma unroll
-                        for (int tt = 0; tt < 16; ++tt) finish(row0 + tt, __uint_as_float(v[tt]), xu[tt * kHalf + jl]);
-                    } else if (c0 + 16 < n) {
-#pragma unroll
-                        for (int tt = 0; tt < 16; ++tt) finish(row0 + tt, xg[tt * kHalf + jl], __uint_as_float(v[16 + tt]));
+                        for (int tt = 0; tt < 16; ++tt) {
+                            const float gv = gate ? __uint_as_float(v[tt]) : xg[tt * kHalf + jl];
+                            const float uv = gate ? xu[tt * kHalf + jl] : __uint_as_float(v[16 + tt]);
+                            const float av = silu(gv) * uv;
+                            const float amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(av))));
+                            const int ex = mx_exponent_e4m3(amax);
+                            st_global_u8_if(true, p.a_pool + (row0 + tt) * I + j, float_to_e4m3_satfinite(av * exp2_neg_int(ex)));
+                            my_sc = lane == tt ? (uint32_t)(ex + 127) : my_sc;
+                        }
+                        st_global_u8_if(lane < 16, p.a_pool_scale + (row0 + lane) * (I / 32) + (j >> 5), (uint8_t)my_sc);
                     }
                     epi_sync();
                 }
             } else {
                 const int h = tl.s * kWR + q * 32 + lane;
-                for (int c0 = 0; c0 < tl.n_valid; c0 += 32) {
-                    const int src_l = c0 + lane < tl.n_valid ? p.pool_src[tl.row0 + c0 + lane] : -1;
-                    const float g_l = src_l >= 0 ? args.topk_weights[src_l] : 0.0f;
+                // the rows' slots and gate weights as a per-warp table (xbuf is free in L2):
+                // broadcast reads instead of shuffles, and no dependency chain through the stores
+                int* w_src = reinterpret_cast<int*>(xbuf) + q * 2 * kNT;
+                float* w_g = reinterpret_cast<float*>(w_src + kNT);
+#pragma unroll
+                for (int ci = 0; ci < kChunks; ++ci) {
+                    if (32 * ci + lane < kNT) {
+                        w_src[32 * ci + lane] = src_l[ci];
+                        w_g[32 * ci + lane] = g_l[ci];
+                    }
+                }
+                __syncwarp();
+#pragma unroll
+                for (int ci = 0; ci < kChunks; ++ci) {
+                    const int c0 = 32 * ci;
+                    if (c0 >= tl.n_valid) break;  // uniform across the warp
                     uint32_t y[32];
                     tmem_ld32(tb + c0, y);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int tt = 0; tt < 32; ++tt) {  // src < 0 beyond the sub-tile's routed rows
-                        const int src = __shfl_sync(0xffffffffu, src_l, tt);
-                        const float gw = __shfl_sync(0xffffffffu, g_l, tt);
-                        if (src >= 0) p.comb[(int64_t)src * H + h] = float_to_bf16_bits(__fmul_rn(gw, __uint_as_float(y[tt])));
+                    for (int tt = 0; tt < 32 && c0 + tt < kNT; ++tt) {  // src < 0 past the routed rows
+                        const int src = w_src[c0 + tt];
+                        const float gw = w_g[c0 + tt];
+                        st_global_u16_if(src >= 0, p.comb + (int64_t)src * H + h,
+                                         float_to_bf16_bits(__fmul_rn(gw, __uint_as_float(y[tt]))));
                     }
                 }
+                __syncwarp();
             }
             tc_fence_before();
             __syncwarp();

@@ -74,6 +74,17 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// Predicated global stores with no memory clobber: epilogue loops stay branch-free and the
+// compiler may move independent loads across them.
+__device__ __forceinline__ void st_global_u8_if(bool pred, void* ptr, uint8_t v) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %0, 0;\n\t@p st.global.u8 [%1], %2;\n\t}" ::"r"((int)pred), "l"(ptr),
+                 "h"((uint16_t)v));
+}
+__device__ __forceinline__ void st_global_u16_if(bool pred, void* ptr, uint16_t v) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %0, 0;\n\t@p st.global.u16 [%1], %2;\n\t}" ::"r"((int)pred), "l"(ptr),
+                 "h"(v));
+}
+
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
