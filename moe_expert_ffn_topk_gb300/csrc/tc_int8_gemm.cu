@@ -39,7 +39,6 @@ using namespace tc;
 constexpr int kWR = 128;        // weight rows per block (MMA M)
 constexpr int kTok = 128;       // tokens per tile (one route tile)
 constexpr int kBK = 64;         // K per stage: 64 f16 = one 128-byte swizzle row
-constexpr int kTokBox = 16;     // token rows per TMA box
 constexpr int kThreads = 352;
 constexpr int kMaxExperts = 1024;
 constexpr int kRawStages = 3, kHfStages = 2, kTokStages = 3;
@@ -54,7 +53,8 @@ constexpr int kNumBars = 2 * (kRawStages + kHfStages + kTokStages) + 2 + 1;
 constexpr int kMiscOff = kBarOff + 8 * kNumBars;
 constexpr int kTileOffOff = kMiscOff + 16;
 constexpr int kCountsOff = kTileOffOff + 4 * (kMaxExperts + 1);
-constexpr size_t kSmem = 1024 + (size_t)kCountsOff + 4 * kMaxExperts;
+constexpr int kTabOff = kCountsOff + 4 * kMaxExperts;  // L2 epilogue: per warp [slot, gate, s^A] x 128 rows
+constexpr size_t kSmem = 1024 + (size_t)kTabOff + 4 * 3 * 4 * kTok;
 static_assert(kSmem <= 232448, "shared memory");
 
 // kind::f16 instruction descriptor: D fp32 (bits 4-5 = 1), A and B f16 (formats 0), both
@@ -220,10 +220,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const uint32_t dst = base + kTokOff + b * kTokBytes;
                     mbar_arrive_expect_tx(tok_full(b), (uint32_t)kTokBytes);
+                    // one copy per plane: each TMA instruction costs the issuing thread ~75 cycles
                     for (int pl = 0; pl < 2; ++pl)
-                        for (int i = 0; i < kTok / kTokBox; ++i)
-                            tma_load_2d(dst + (pl * kTok + i * kTokBox) * 128, &tmX, kb * kBK,
-                                        (int)(pl * p.pool_rows) + tl.row0 + i * kTokBox, tok_full(b));
+                        tma_load_2d(dst + pl * kTok * 128, &tmX, kb * kBK, (int)(pl * p.pool_rows) + tl.row0, tok_full(b));
                 }
             }
             for (int j = it - kTokStages < 0 ? 0 : it - kTokStages; j < it; ++j)
@@ -286,23 +285,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ---------------- epilogue (warps 2..5) ----------------
+        // The per-row values (token scales, L2 slots and gate weights) and the per-channel weight
+        // scales are read before the accumulator wait, while the tile's MMAs still run: the
+        // accumulator is single-buffered, so the epilogue adds directly to the tile time.
         const int q = warp & 3;
+        int* w_src = reinterpret_cast<int*>(smem + kTabOff) + q * 3 * kTok;
+        float* w_g = reinterpret_cast<float*>(w_src + kTok);
+        float* w_sa = w_g + kTok;
         int tc = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++tc) {
+            const Tile tl = decode(t, tile_off, p.E, args.n_slabs);
+            const int n_valid = min(kTok, p.counts[tl.e] - tl.m * kTok);
+            float sx_l[kTok / 32];
+            float sg = 0.0f, su = 0.0f, s2[2] = {0.0f, 0.0f};
+            if constexpr (kL1) {
+                const int j = tl.s * kWR + q * 32 + lane;
+                const float* s1 = args.w_scale + (int64_t)tl.e * 2 * I;
+                sg = __ldg(s1 + j);
+                su = __ldg(s1 + I + j);
+#pragma unroll
+                for (int ci = 0; ci < kTok / 32; ++ci)
+                    sx_l[ci] = __ldg(reinterpret_cast<const float*>(p.x_pool_scale) + tl.row0 + 32 * ci + lane);
+            } else {
+#pragma unroll
+                for (int blk = 0; blk < 2; ++blk)
+                    s2[blk] = __ldg(args.w_scale + (int64_t)tl.e * H + tl.s * 2 * kWR + blk * kWR + q * 32 + lane);
+                int src[kTok / 32];
+#pragma unroll
+                for (int ci = 0; ci < kTok / 32; ++ci) {
+                    const int n = 32 * ci + lane;
+                    src[ci] = n < n_valid ? __ldg(p.pool_src + tl.row0 + n) : -1;
+                    sx_l[ci] = __ldg(reinterpret_cast<const float*>(p.a_pool_scale) + tl.row0 + n);
+                }
+#pragma unroll
+                for (int ci = 0; ci < kTok / 32; ++ci) {
+                    const float g = src[ci] >= 0 ? __ldg(args.topk_weights + src[ci]) : 0.0f;
+                    w_src[32 * ci + lane] = src[ci];
+                    w_g[32 * ci + lane] = g;
+                    w_sa[32 * ci + lane] = sx_l[ci];
+                }
+                __syncwarp();
+            }
             const bool w_ok = mbar_wait(acc_full, (uint32_t)tc & 1u, p.hdr, abort_flag);
             if (!__all_sync(0xffffffffu, w_ok)) break;
             tc_fence_after();
-            const Tile tl = decode(t, tile_off, p.E, args.n_slabs);
-            const int n_valid = min(kTok, p.counts[tl.e] - tl.m * kTok);
             const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16);
             if constexpr (kL1) {
                 // C = 16 D_hi + D_lo; H = (C * s^W1) * s^X; A = SiLU(H_gate) * H_up, all 128 tokens
                 // (padding tokens come out finite and are never read back as results)
                 const int j = tl.s * kWR + q * 32 + lane;
-                const float* s1 = args.w_scale + (int64_t)tl.e * 2 * I;
-                const float sg = s1[j], su = s1[I + j];
-                for (int c0 = 0; c0 < kTok; c0 += 32) {
-                    const float sx_l = reinterpret_cast<const float*>(p.x_pool_scale)[tl.row0 + c0 + lane];
+#pragma unroll
+                for (int ci = 0; ci < kTok / 32; ++ci) {
+                    const int c0 = 32 * ci;
                     uint32_t hi[32], lo[32];
                     float hg[32];
                     tmem_ld32(tb + c0, hi);
@@ -315,37 +349,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld_wait();
 #pragma unroll
                     for (int tt = 0; tt < 32; ++tt) {
-                        const float sx = __shfl_sync(0xffffffffu, sx_l, tt);
+                        const float sx = __shfl_sync(0xffffffffu, sx_l[ci], tt);
                         const float Hg = __fmul_rn(__fmul_rn(hg[tt], sg), sx);
                         const float Hu = __fmul_rn(__fmul_rn(__int2float_rn(exact_int(hi[tt], lo[tt])), su), sx);
                         p.a_f32[(int64_t)(tl.row0 + c0 + tt) * I + j] = silu(Hg) * Hu;
                     }
                 }
             } else {
-                // D = 16 D_hi + D_lo; Y = (D * s^W2) * s^A; c = bf16(G * Y) to the combine row
-                for (int c0 = 0; c0 < n_valid; c0 += 32) {
-                    const int src_l = c0 + lane < n_valid ? p.pool_src[tl.row0 + c0 + lane] : -1;
-                    const float g_l = src_l >= 0 ? args.topk_weights[src_l] : 0.0f;
-                    const float sa_l = reinterpret_cast<const float*>(p.a_pool_scale)[tl.row0 + c0 + lane];
-#pragma unroll 1
+                // D = 16 D_hi + D_lo; Y = (D * s^W2) * s^A; c = bf16(G * Y) to the combine row.
+                // Branch-free: the slot, gate and s^A of token tt are broadcast reads of the table.
+#pragma unroll
+                for (int ci = 0; ci < kTok / 32; ++ci) {
+                    const int c0 = 32 * ci;
+                    if (c0 >= n_valid) break;  // uniform across the warp
+#pragma unroll
                     for (int blk = 0; blk < 2; ++blk) {
                         const int h = tl.s * 2 * kWR + blk * kWR + q * 32 + lane;
-                        const float s2 = args.w_scale[(int64_t)tl.e * H + h];
                         uint32_t hi[32], lo[32];
                         tmem_ld32(tb + blk * 256 + c0, hi);
                         tmem_ld32(tb + blk * 256 + kTok + c0, lo);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int tt = 0; tt < 32; ++tt) {
-                            if (c0 + tt >= n_valid) break;  // uniform across the warp
-                            const int src = __shfl_sync(0xffffffffu, src_l, tt);
-                            const float gw = __shfl_sync(0xffffffffu, g_l, tt);
-                            const float sa = __shfl_sync(0xffffffffu, sa_l, tt);
-                            const float y = __fmul_rn(__fmul_rn(__int2float_rn(exact_int(hi[tt], lo[tt])), s2), sa);
-                            if (src >= 0) p.comb[(int64_t)src * H + h] = float_to_bf16_bits(__fmul_rn(gw, y));
+                        for (int tt = 0; tt < 32; ++tt) {  // slot < 0 past the routed rows
+                            const int src = w_src[c0 + tt];
+                            const float y = __fmul_rn(__fmul_rn(__int2float_rn(exact_int(hi[tt], lo[tt])), s2[blk]), w_sa[c0 + tt]);
+                            st_global_u16_if(src >= 0, p.comb + (int64_t)src * H + h, float_to_bf16_bits(__fmul_rn(w_g[c0 + tt], y)));
                         }
                     }
                 }
+                __syncwarp();
             }
             tc_fence_before();
             __syncwarp();
@@ -374,7 +406,7 @@ cudaError_t launch_int8(const Plan& p, const void* w, const void* w_scale, const
                         CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
     if (!tc_make_map_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, kL1 ? (const void*)p.x_planes : (const void*)p.a_planes,
-                        (uint64_t)kin, 2 * (uint64_t)p.pool_rows, kBK, kTokBox, CU_TENSOR_MAP_SWIZZLE_128B))
+                        (uint64_t)kin, 2 * (uint64_t)p.pool_rows, kBK, kTok, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     I8Args args{p, static_cast<const float*>(w_scale), topk_weights, kL1 ? p.I / kWR : p.H / (2 * kWR), kin / kBK,
                 n_out};
