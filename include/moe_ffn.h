@@ -96,7 +96,10 @@ typedef struct {
 /* Flags of the GEMM stages. */
 enum {
     MOE_FLAG_NONE = 0u,
-    MOE_FLAG_SIMT = 1u   /* run the CUDA-core reference GEMMs instead of the tensor-core ones */
+    MOE_FLAG_SIMT = 1u,         /* run the CUDA-core reference GEMMs instead of the tensor-core ones */
+    MOE_FLAG_WEIGHT_MAJOR = 2u  /* FP8 modes at prefill sizes: 128 weight rows x 128 tokens per tile
+                                   (the decode-style tile) instead of 128 tokens x 256 weight rows;
+                                   same results up to fp32 summation order, for comparison */
 };
 
 /* Bytes of workspace that moe_plan / moe_forward and the stage calls need for `d` and `m`.

@@ -74,10 +74,16 @@ cudaError_t launch_l2_int8_tc(const Plan& p, const void* w2, const void* w2_scal
                               cudaStream_t s);
 bool int8_tc_supported(const Plan& p, int stage);
 
-// Block-scaled tensor-core path of the FP8 modes (kind::mxf8f6f4.block_scale).
-cudaError_t launch_l1_bs(const Plan& p, const void* w1, const void* w1_scale, cudaStream_t s);
+// Block-scaled tensor-core path of the FP8 modes (kind::mxf8f6f4.block_scale): weight-major
+// tiles for decode-sized experts, token-major tiles for prefill-sized ones (weight-major when
+// `weight_major` is set or the shape has no token-major kernel).
+cudaError_t launch_l1_bs(const Plan& p, const void* w1, const void* w1_scale, bool weight_major, cudaStream_t s);
 cudaError_t launch_l2_bs(const Plan& p, const void* w2, const void* w2_scale, const float* topk_weights,
-                         cudaStream_t s);
+                         bool weight_major, cudaStream_t s);
 bool bs_supported(const Plan& p, int stage);
+cudaError_t launch_l1_bs_tm(const Plan& p, const void* w1, const void* w1_scale, cudaStream_t s);
+cudaError_t launch_l2_bs_tm(const Plan& p, const void* w2, const void* w2_scale, const float* topk_weights,
+                            cudaStream_t s);
+bool bs_tm_supported(const Plan& p, int stage);
 
 }  // namespace moe

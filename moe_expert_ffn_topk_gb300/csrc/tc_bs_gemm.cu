@@ -132,7 +132,6 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, uint32_t a0, uint32_t a
                  "r"(a1), "r"(a2), "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
                  : "memory");
 }
-__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync %0, 128;" ::"n"(kEpiBar) : "memory"); }
 
 template <int MODE, bool kL1, int kNT, int kStages, int kAtoms>
@@ -540,7 +539,8 @@ cudaError_t launch_bs_cfg(const Plan& p, const CUtensorMap& tmW, const CUtensorM
 }
 
 template <int MODE, bool kL1>
-cudaError_t launch_bs(const Plan& p, const void* w, const void* w_scale, const float* topk_weights, cudaStream_t s) {
+cudaError_t launch_bs(const Plan& p, const void* w, const void* w_scale, const float* topk_weights, bool weight_major,
+                      cudaStream_t s) {
     const int n_out = kL1 ? 2 * p.I : p.H;
     const int kin = kL1 ? p.H : p.I;
     CUtensorMap tmW, tmX;
@@ -564,6 +564,8 @@ cudaError_t launch_bs(const Plan& p, const void* w, const void* w_scale, const f
     // few routed rows per expert: the weights stream from HBM; 16-token sub-tiles and K = 256
     // stages (whole 128-byte lines of every weight row per load)
     const bool decode = (int64_t)p.T * p.K <= (int64_t)16 * p.E;
+    if (!decode && !weight_major && bs_tm_supported(p, kL1 ? 1 : 2))
+        return kL1 ? launch_l1_bs_tm(p, w, w_scale, s) : launch_l2_bs_tm(p, w, w_scale, topk_weights, s);
     // token rows: one copy brings the sub-tile's kNT pool rows
     if (!tc_make_map_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kL1 ? (const void*)p.x_pool : (const void*)p.a_pool,
                         (uint64_t)kin, (uint64_t)p.pool_rows, kAtomK, decode ? 16u : 128u, CU_TENSOR_MAP_SWIZZLE_128B))
@@ -582,15 +584,17 @@ bool bs_supported(const Plan& p, int stage) {
     return p.H % kWR == 0 && p.I % kAtomK == 0;
 }
 
-cudaError_t launch_l1_bs(const Plan& p, const void* w1, const void* w1_scale, cudaStream_t s) {
-    if (p.mode == MOE_A8W4_FP8_FP4) return launch_bs<MOE_A8W4_FP8_FP4, true>(p, w1, w1_scale, nullptr, s);
-    if (p.mode == MOE_A8W8_FP8) return launch_bs<MOE_A8W8_FP8, true>(p, w1, w1_scale, nullptr, s);
+cudaError_t launch_l1_bs(const Plan& p, const void* w1, const void* w1_scale, bool weight_major, cudaStream_t s) {
+    if (p.mode == MOE_A8W4_FP8_FP4) return launch_bs<MOE_A8W4_FP8_FP4, true>(p, w1, w1_scale, nullptr, weight_major, s);
+    if (p.mode == MOE_A8W8_FP8) return launch_bs<MOE_A8W8_FP8, true>(p, w1, w1_scale, nullptr, weight_major, s);
     return cudaErrorNotSupported;
 }
 
-cudaError_t launch_l2_bs(const Plan& p, const void* w2, const void* w2_scale, const float* topk_weights, cudaStream_t s) {
-    if (p.mode == MOE_A8W4_FP8_FP4) return launch_bs<MOE_A8W4_FP8_FP4, false>(p, w2, w2_scale, topk_weights, s);
-    if (p.mode == MOE_A8W8_FP8) return launch_bs<MOE_A8W8_FP8, false>(p, w2, w2_scale, topk_weights, s);
+cudaError_t launch_l2_bs(const Plan& p, const void* w2, const void* w2_scale, const float* topk_weights,
+                         bool weight_major, cudaStream_t s) {
+    if (p.mode == MOE_A8W4_FP8_FP4)
+        return launch_bs<MOE_A8W4_FP8_FP4, false>(p, w2, w2_scale, topk_weights, weight_major, s);
+    if (p.mode == MOE_A8W8_FP8) return launch_bs<MOE_A8W8_FP8, false>(p, w2, w2_scale, topk_weights, weight_major, s);
     return cudaErrorNotSupported;
 }
 

@@ -74,6 +74,8 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // Predicated global stores with no memory clobber: epilogue loops stay branch-free and the
 // compiler may move independent loads across them.
 __device__ __forceinline__ void st_global_u8_if(bool pred, void* ptr, uint8_t v) {

@@ -297,3 +297,23 @@ def test_quantised_tensor_core_path_matches_reference_kernels(moe, mode, wl):
     L = outs[0]["layout"]
     c = [region(o["ws"], L, "comb", torch.bfloat16, wl.T * wl.K * wl.H).float().cpu().numpy() for o in outs]
     assert np.abs(c[0] - c[1]).max() <= TOL[mode] * np.abs(c[1]).max()
+
+
+FP8_PREFILL = [(m, w) for m, w in ALL if m in ("a8w8_fp8", "a8w4_fp8_fp4") and w.T * w.K > 16 * w.E]
+
+
+@pytest.mark.parametrize("mode,wl", FP8_PREFILL, ids=[f"{m}-{w.name}" for m, w in FP8_PREFILL])
+def test_token_major_and_weight_major_block_scaled_tiles_agree(moe, mode, wl):
+    """At prefill sizes the FP8 modes run 128-token x 256-weight-row tiles; the flag selects the
+    128-weight-row x 128-token tiles. Both compute the same block-scaled products, so the combine
+    rows and the output agree up to the fp32 summation order (within the mode's tolerance), and
+    the oracle bounds both."""
+    inp = make_inputs(wl, device=DEV)
+    outs = [run_forward(moe, wl, inp, flags=f, stages=True) for f in (0, moe.MOE_FLAG_WEIGHT_MAJOR)]
+    assert all(o["status"] == 0 for o in outs)
+    L = outs[0]["layout"]
+    c = [region(o["ws"], L, "comb", torch.bfloat16, wl.T * wl.K * wl.H).float().cpu().numpy() for o in outs]
+    assert np.abs(c[0] - c[1]).max() <= TOL[mode] * np.abs(c[1]).max()
+    ref = oracle_forward(wl, inp)
+    for o in outs:
+        assert_close(y_numpy(o["y"]), ref, mode)
