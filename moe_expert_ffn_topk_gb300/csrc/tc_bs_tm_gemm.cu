@@ -26,6 +26,11 @@
 // lane 32*q + n%32 of every lane quarter q, column slot + 4 + n/32; byte k of a word is the
 // scale of K group k of the stage.
 //
+// Scale words (4 UE8M0 bytes per row and 128-element K atom; fp32 per atom for the FP8xFP4
+// tokens) come by TMA too, in blocks of 4 atoms (16 bytes of every row) two blocks ahead of their
+// use, into a 4-deep ring: scattered 4-byte loads of them by the scale warps slowed the operand
+// TMA down by a quarter (measured). The scale warps only move them from shared to tensor memory.
+//
 // Warp roles (320 threads): 0 TMA producer, 1 TMEM allocation + MMA issuer, 2-5 epilogue (warp
 // w owns TMEM lanes 32*(w%4) .. +31, i.e. those token rows), 6-9 scale writers. Every wait is
 // bounded; on time-out the CTA records MOE_ERR_TIMEOUT, drains and exits.
@@ -55,13 +60,17 @@ constexpr int kWBytes = kWN * 128;                   // 32 KB in shared memory
 constexpr int kStageBytes = kTokBytes + kWBytes;
 constexpr int kSfCol0 = 256;
 constexpr int kSfColsPerStage = 16;  // SFA 4 columns, SFB 8 columns
-constexpr int kNumBars = 2 * kStages + 2 + 1 + 2;  // full, empty, acc full/empty, drain, 2 weight-scale buffers
-constexpr int kBarOff = kStages * kStageBytes;
+constexpr int kSfBlk = 4;            // K atoms per scale block (16 bytes of a row)
+constexpr int kSfBufs = 4;           // scale ring depth: blocks issued two ahead of their use
+constexpr int kSfWBytes = kWN * 16;  // weight scale words of a block: [256 rows][4 atoms]
+constexpr int kSfTBytes = kTM * 16;  // token scale words of a block: [128 rows][4 atoms]
+constexpr int kSfOff = kStages * kStageBytes;
+constexpr int kBarOff = kSfOff + kSfBufs * (kSfWBytes + kSfTBytes);
+constexpr int kNumBars = 2 * kStages + 2 + 1 + 2 * kSfBufs;  // full, empty, acc full/empty, drain, scale full/empty
 constexpr int kMiscOff = kBarOff + 8 * kNumBars;
 constexpr int kTileOffOff = kMiscOff + 16;
 constexpr int kCountsOff = kTileOffOff + 4 * (kMaxExperts + 1);
-constexpr int kWsfOff = (kCountsOff + 4 * kMaxExperts + 15) & ~15;  // u32 [2][8 groups][8 atoms][32 lanes]
-constexpr size_t kSmem = 1024 + (size_t)kWsfOff + 2 * 8 * 8 * 32 * 4;
+constexpr size_t kSmem = 1024 + (size_t)kCountsOff + 4 * kMaxExperts;
 static_assert(kSmem <= 232448, "shared memory");
 static_assert(kSfCol0 + kStages * kSfColsPerStage <= 512, "tensor memory");
 
@@ -130,6 +139,14 @@ __device__ __forceinline__ void st_global_v4_if(bool pred, void* ptr, uint32_t a
                  "l"(ptr), "r"(a), "r"(b), "r"(c), "r"(d));
 }
 
+// predicated 32-byte global store (sm_100 family); 32-byte aligned address
+__device__ __forceinline__ void st_global_v8_if(bool pred, void* ptr, const uint32_t* v) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %0, 0;\n\t@p st.global.v8.b32 [%1], {%2, %3, %4, %5, %6, %7, %8, %9};\n\t}" ::"r"(
+            (int)pred),
+        "l"(ptr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]));
+}
+
 // two floats -> two e4m3 codes (RN, saturating), the first in the low byte
 __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
     uint16_t pair;
@@ -139,7 +156,8 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
 
 template <int MODE, bool kL1>
 __global__ void __launch_bounds__(kThreads, 1)
-    tc_bs_tm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, TmArgs args) {
+    tc_bs_tm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                    const __grid_constant__ CUtensorMap tmSW, const __grid_constant__ CUtensorMap tmSX, TmArgs args) {
     constexpr bool kFp4 = MODE == MOE_A8W4_FP8_FP4;
     constexpr uint32_t kBfmt = kFp4 ? 5u : 0u;
     constexpr uint32_t kWTx = kFp4 ? kWN * kAtomK / 2 : kWN * kAtomK;  // TMA counts the packed global bytes
@@ -153,12 +171,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t acc_full = bars + 8u * (2 * kStages);
     const uint32_t acc_empty = acc_full + 8u;
     const uint32_t drain_bar = acc_full + 16u;
-    auto wsf_bar = [&](int b) { return bars + 8u * (2 * kStages + 3 + b); };
+    auto sf_full = [&](int b) { return bars + 8u * (2 * kStages + 3 + b); };
+    auto sf_empty = [&](int b) { return bars + 8u * (2 * kStages + 3 + kSfBufs + b); };
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
     int* tile_off = reinterpret_cast<int*>(smem + kTileOffOff);
     int* counts = reinterpret_cast<int*>(smem + kCountsOff);
-    uint32_t* wsf = reinterpret_cast<uint32_t*>(smem + kWsfOff);
 
     const Plan& p = args.p;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -172,7 +190,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, 4);
         mbar_init(drain_bar, 1);
-        for (int b = 0; b < 2; ++b) mbar_init(wsf_bar(b), 4);
+        for (int b = 0; b < kSfBufs; ++b) {
+            mbar_init(sf_full(b), 1);   // the producer (arrive + bytes)
+            mbar_init(sf_empty(b), 4);  // the 4 scale-writer warps
+        }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -199,13 +220,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ---------------- TMA producer: 128 token rows, 256 weight rows per stage ----------------
         if (lane == 0) {
-            int it = 0;
+            const int n_sfb = (KB + kSfBlk - 1) / kSfBlk;  // scale blocks per tile
+            // scale blocks in the order they are used: (tile, block), counted by sj
+            int st_t = blockIdx.x, st_b = 0, sj = 0;
+            Tile st_tl = tile_of(st_t < total ? st_t : 0);  // decoded once per tile
             bool ok = true;
+            auto issue_scales = [&]() {  // the next scale block, if any
+                if (st_t >= total || !ok) return;
+                const int buf = sj % kSfBufs;
+                if (!mbar_wait(sf_empty(buf), ((uint32_t)(sj / kSfBufs) & 1u) ^ 1u, p.hdr, abort_flag)) {
+                    ok = false;
+                    return;
+                }
+                const Tile& tl = st_tl;
+                const uint32_t dw = base + kSfOff + buf * (kSfWBytes + kSfTBytes), dt = dw + kSfWBytes;
+                mbar_arrive_expect_tx(sf_full(buf), (uint32_t)(kSfWBytes + kSfTBytes));
+                const int xw = st_b * kSfBlk * 4;  // byte offset of the block within a row's scales
+                if constexpr (kL1)
+                    tma_load_4d(dw, &tmSW, xw, tl.s * 128, 0, tl.e, sf_full(buf));
+                else
+                    tma_load_2d(dw, &tmSW, xw, wrow(tl, 0), sf_full(buf));
+                tma_load_2d(dt, &tmSX, kL1 && kFp4 ? st_b * kSfBlk : xw, tl.row0, sf_full(buf));
+                ++sj;
+                if (++st_b == n_sfb) {
+                    st_b = 0;
+                    st_t += gridDim.x;
+                    if (st_t < total) st_tl = tile_of(st_t);
+                }
+            };
+            issue_scales();
+            issue_scales();
+            int it = 0;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 const Tile tl = tile_of(t);
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int s = it % kStages;
-                    if (!mbar_wait(empty_bar(s), ((uint32_t)(it / kStages) & 1u) ^ 1u, p.hdr, abort_flag)) {
+                    if (!ok || !mbar_wait(empty_bar(s), ((uint32_t)(it / kStages) & 1u) ^ 1u, p.hdr, abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -217,10 +267,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_load_4d(sb, &tmW, x, tl.s * 128, 0, tl.e, full_bar(s));
                     else
                         tma_load_2d(sb, &tmW, x, wrow(tl, 0), full_bar(s));
+                    // after the stage's operands, which the MMA waits for first: the scale
+                    // block two ahead of the one this stage starts
+                    if (kb % kSfBlk == 0) issue_scales();
                 }
             }
+            // drain: every copy issued has landed (bounded)
             for (int j = it - kStages < 0 ? 0 : it - kStages; j < it; ++j)
                 mbar_drain(full_bar(j % kStages), (uint32_t)(j / kStages) & 1u, p.hdr);
+            for (int j = sj - kSfBufs < 0 ? 0 : sj - kSfBufs; j < sj; ++j)
+                mbar_drain(sf_full(j % kSfBufs), (uint32_t)(j / kSfBufs) & 1u, p.hdr);
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
@@ -252,117 +308,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp >= 6) {
         // ---------------- scale writers ----------------
-        // Lane l of warp q owns token row r = 32q + l (its A scale) and loads the weight rows
-        // 32c + l for c = 2q, 2q+1; the B scales are needed in every lane quarter, so each warp
-        // publishes its two groups through shared memory (an mbarrier per buffer). Scale words
-        // (one per row and 128-element K atom) are read 8 atoms at a time, so a lane's 32 bytes
-        // fill one sector, and two blocks ahead of their use; the loaded words are only
-        // converted when the block is written out, so the loads stay in flight.
+        // Lane l of warp q writes TMEM lane 32q + l: the A word of token row r = 32q + l and the
+        // B words of weight rows 32c + l (c = 0..7), all read from the scale block in shared
+        // memory ([row][4 atoms] words; 4-way bank conflicts at most).
         const int q = warp & 3;
         const int r = 32 * q + lane;
-        const int spr = args.kin / 32;
-        const int n_words = args.kin / kAtomK;
-        const int n_blk = (n_words + 7) >> 3;
-        struct Blk {
-            uint32_t a[8], w0[8], w1[8];
-            bool tok_valid;
-        };
-        auto load_blk = [&](int t, int blk) {
-            Blk w;
-            const Tile tl = tile_of(t);
-            w.tok_valid = r < tl.n_valid;
-            const int64_t row = tl.row0 + r;  // a pool row of the route tile
-            const uint32_t* ws0 = reinterpret_cast<const uint32_t*>(args.w_scale + (int64_t)wrow(tl, 64 * q + lane) * spr);
-            const uint32_t* ws1 =
-                reinterpret_cast<const uint32_t*>(args.w_scale + (int64_t)wrow(tl, 64 * q + 32 + lane) * spr);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int g = min(blk * 8 + i, n_words - 1);  // K atom: elements 128g .. 128g+127
-                if constexpr (kL1 && kFp4)
-                    w.a[i] = __float_as_uint(__ldg(reinterpret_cast<const float*>(p.x_pool_scale) + row * (H / 128) + g));
-                else if constexpr (kL1)
-                    w.a[i] = __ldg(reinterpret_cast<const uint32_t*>(p.x_pool_scale + row * (H / 32)) + g);
-                else
-                    w.a[i] = __ldg(reinterpret_cast<const uint32_t*>(p.a_pool_scale + row * (I / 32)) + g);
-                w.w0[i] = __ldg(ws0 + g);
-                w.w1[i] = __ldg(ws1 + g);
-            }
-            return w;
-        };
-        // token word as the MMA reads it: 4 UE8M0 bytes; 1.0 for the padding rows
-        auto tok_word = [&](const Blk& w, uint32_t raw) -> uint32_t {
-            if (!w.tok_valid) return 0x7f7f7f7fu;
-            if constexpr (kL1 && kFp4) return ((raw >> 23) & 0xffu) * 0x01010101u;  // power-of-two fp32 scale
-            return raw;
-        };
-        auto next_pos = [&](int& t, int& blk) {
-            if (++blk == n_blk) {
-                blk = 0;
-                t += gridDim.x;
-            }
-        };
-        int t0 = blockIdx.x, b0 = 0, t1 = t0, b1 = b0;
-        next_pos(t1, b1);
-        int t2 = t1, b2 = b1;
-        int it = 0, nb = 0;  // stages and blocks done
+        int it = 0, sj = 0;
         bool ok = true;
-        // writes out block (t0, b0) from `use` after starting the loads of block (t2, b2) into
-        // `fill`; the three buffers rotate by name, so no register holding a load in flight is copied
-        auto run_block = [&](const Blk& use, Blk& fill) -> bool {
-            if (t0 >= total || !ok) return false;
-            next_pos(t2, b2);
-            if (t2 < total) fill = load_blk(t2, b2);
-            const int buf = nb & 1;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            const Tile tl = tile_of(t);
+            const bool tok_valid = r < tl.n_valid;
+            for (int kb = 0; kb < KB && ok; kb += kSfBlk) {
+                const int buf = sj % kSfBufs;
+                const bool f_ok = mbar_wait(sf_full(buf), (uint32_t)(sj / kSfBufs) & 1u, p.hdr, abort_flag);
+                if (!__all_sync(0xffffffffu, f_ok)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t* sw = reinterpret_cast<const uint32_t*>(smem + kSfOff + buf * (kSfWBytes + kSfTBytes));
+                const uint32_t* sx = sw + kSfWBytes / 4;
+                for (int i = 0; i < kSfBlk && kb + i < KB; ++i, ++it) {
+                    const int s = it % kStages;
+                    const bool w_ok = mbar_wait(empty_bar(s), ((uint32_t)(it / kStages) & 1u) ^ 1u, p.hdr, abort_flag);
+                    if (!__all_sync(0xffffffffu, w_ok)) {
+                        ok = false;
+                        break;
+                    }
+                    uint32_t ta = sx[r * kSfBlk + i];
+                    if constexpr (kL1 && kFp4) ta = ((ta >> 23) & 0xffu) * 0x01010101u;  // power-of-two fp32 scale
+                    if (!tok_valid) ta = 0x7f7f7f7fu;  // 1.0 for the padding rows
+                    // slot columns: 0-3 the A word (the MMA reads column q of lane quarter q), 4-11
+                    // the B words of weight rows 32c + lane, 12-15 unused
+                    uint32_t v[16];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                wsf[((buf * 8 + 2 * q) * 8 + i) * 32 + lane] = use.w0[i];
-                wsf[((buf * 8 + 2 * q + 1) * 8 + i) * 32 + lane] = use.w1[i];
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(wsf_bar(buf));
-            const bool b_ok = mbar_wait(wsf_bar(buf), (uint32_t)(nb >> 1) & 1u, p.hdr, abort_flag);
-            if (!__all_sync(0xffffffffu, b_ok)) return ok = false;
-            // working copy of the token words (loaded a block ago), shifted one per stage so the
-            // rolled loop below indexes registers statically
-            uint32_t ta[8];
+                    for (int c = 0; c < 4; ++c) v[c] = ta;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) ta[i] = tok_word(use, use.a[i]);
-#pragma unroll 1
-            for (int i = 0; i < 8; ++i) {
-                const int kb = b0 * 8 + i;
-                if (kb >= KB) break;  // uniform across the CTA's scale warps
-                const int s = it % kStages;
-                const bool w_ok = mbar_wait(empty_bar(s), ((uint32_t)(it / kStages) & 1u) ^ 1u, p.hdr, abort_flag);
-                if (!__all_sync(0xffffffffu, w_ok)) return ok = false;
-                // slot columns: 0-3 the A word (the MMA reads column q of lane quarter q), 4-11
-                // the B words of weight rows 32c + lane, 12-15 unused
-                uint32_t v[16];
+                    for (int c = 0; c < 8; ++c) v[4 + c] = sw[(32 * c + lane) * kSfBlk + i];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) v[c] = ta[0];
-#pragma unroll
-                for (int c = 0; c < 8; ++c) v[4 + c] = wsf[((buf * 8 + c) * 8 + i) * 32 + lane];
-#pragma unroll
-                for (int c = 12; c < 16; ++c) v[c] = 0x7f7f7f7fu;
-                tmem_st16(tmem_base + ((uint32_t)(32 * q) << 16) + kSfCol0 + s * kSfColsPerStage, v);
-#pragma unroll
-                for (int j = 0; j < 7; ++j) ta[j] = ta[j + 1];
-                tmem_st_wait();
-                tc_fence_before();
+                    for (int c = 12; c < 16; ++c) v[c] = 0x7f7f7f7fu;
+                    tmem_st16(tmem_base + ((uint32_t)(32 * q) << 16) + kSfCol0 + s * kSfColsPerStage, v);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(full_bar(s));
+                }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(full_bar(s));
-                ++it;
+                if (lane == 0) mbar_arrive(sf_empty(buf));
+                ++sj;
             }
-            t0 = t1;
-            b0 = b1;
-            t1 = t2;
-            b1 = b2;
-            ++nb;
-            return true;
-        };
-        Blk A{}, B{}, C{};
-        if (t0 < total) A = load_blk(t0, b0);
-        if (t1 < total) B = load_blk(t1, b1);
-        while (run_block(A, C) && run_block(B, A) && run_block(C, B)) {
         }
     } else {
         // ---------------- epilogue (warps 2..5): thread = token row ----------------
@@ -414,29 +407,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                         w[k] = e4m3x2(av[4 * k] * inv, av[4 * k + 1] * inv) |
                                (e4m3x2(av[4 * k + 2] * inv, av[4 * k + 3] * inv) << 16);
                     const int j0 = tl.s * 128 + 32 * c;
-                    uint8_t* dst = p.a_pool + row * I + j0;
-                    st_global_v4_if(valid, dst, w[0], w[1], w[2], w[3]);
-                    st_global_v4_if(valid, dst + 16, w[4], w[5], w[6], w[7]);
+                    st_global_v8_if(valid, p.a_pool + row * I + j0, w);
                     st_global_u8_if(valid, p.a_pool_scale + row * (I / 32) + (j0 >> 5), (uint8_t)(ex + 127));
                 }
             } else {
-                // c = bf16(G * y) for hidden columns 256s + 32c .. +31: 64 bytes of the combine row
-#pragma unroll 1
+                // c = bf16(G * y) for the tile's 256 hidden columns: all of them packed into
+                // registers first, so the accumulator is released before the stores (a thread's
+                // 512 bytes go to its own combine row, in 32-byte stores: 32 rows per warp
+                // store instruction make the stores the slow part)
+                uint32_t w[128];
+#pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     uint32_t y[32];
                     tmem_ld32(tb + 32 * c, y);
                     tmem_ld_wait();
-                    if (c == 7) release();
-                    uint32_t w[16];
 #pragma unroll
                     for (int k = 0; k < 16; ++k)
-                        w[k] = (uint32_t)float_to_bf16_bits(__fmul_rn(gw, __uint_as_float(y[2 * k]))) |
-                               ((uint32_t)float_to_bf16_bits(__fmul_rn(gw, __uint_as_float(y[2 * k + 1]))) << 16);
-                    uint16_t* dst = p.comb + (int64_t)(src >= 0 ? src : 0) * H + tl.s * kWN + 32 * c;
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        st_global_v4_if(src >= 0, dst + 8 * k, w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+                        w[16 * c + k] = (uint32_t)float_to_bf16_bits(__fmul_rn(gw, __uint_as_float(y[2 * k]))) |
+                                        ((uint32_t)float_to_bf16_bits(__fmul_rn(gw, __uint_as_float(y[2 * k + 1]))) << 16);
                 }
+                release();
+                uint16_t* dst = p.comb + (int64_t)(src >= 0 ? src : 0) * H + tl.s * kWN;
+#pragma unroll
+                for (int k = 0; k < 16; ++k) st_global_v8_if(src >= 0, dst + 16 * k, w + 8 * k);
             }
         }
     }
@@ -478,11 +471,41 @@ cudaError_t launch_tm(const Plan& p, const void* w, const void* w_scale, const f
     if (!tc_make_map_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kL1 ? (const void*)p.x_pool : (const void*)p.a_pool,
                         (uint64_t)kin, (uint64_t)p.pool_rows, kAtomK, kTM, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
+    // scale words, 16 bytes (4 K atoms) of every row per copy, unswizzled
+    CUtensorMap tmSW, tmSX;
+    const uint64_t sp = (uint64_t)kin / 32;  // scale bytes per weight row
+    if (kL1) {
+        const uint64_t dims[4] = {sp, (uint64_t)p.I, 2, (uint64_t)p.E};
+        const uint64_t strides[3] = {sp, sp * p.I, sp * 2 * p.I};
+        const uint32_t box[4] = {16, 128, 2, 1};
+        ok_w = tc_make_map_nd(&tmSW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, w_scale, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+    } else {
+        const uint64_t dims[2] = {sp, (uint64_t)p.E * n_out};
+        const uint64_t strides[1] = {sp};
+        const uint32_t box[2] = {16, kWN};
+        ok_w = tc_make_map_nd(&tmSW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, w_scale, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+    }
+    if (!ok_w) return cudaErrorInvalidValue;
+    bool ok_x;
+    if (kL1 && kFp4) {  // fp32 per 128 elements of a token row
+        const uint64_t dims[2] = {(uint64_t)kin / 128, (uint64_t)p.pool_rows};
+        const uint64_t strides[1] = {(uint64_t)kin / 128 * 4};
+        const uint32_t box[2] = {4, kTM};
+        ok_x = tc_make_map_nd(&tmSX, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p.x_pool_scale, dims, strides, box,
+                              CU_TENSOR_MAP_SWIZZLE_NONE);
+    } else {  // UE8M0 per 32 elements
+        const uint64_t dims[2] = {sp, (uint64_t)p.pool_rows};
+        const uint64_t strides[1] = {sp};
+        const uint32_t box[2] = {16, kTM};
+        ok_x = tc_make_map_nd(&tmSX, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, kL1 ? (const void*)p.x_pool_scale : (const void*)p.a_pool_scale,
+                              dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+    }
+    if (!ok_x) return cudaErrorInvalidValue;
     TmArgs args{p, static_cast<const uint8_t*>(w_scale), topk_weights, kL1 ? p.I / 128 : p.H / kWN, kin / kAtomK, n_out,
                 kin};
     const int64_t max_tiles = std::max<int64_t>(1, (p.pool_rows / kTM) * args.n_slabs);
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(max_tiles, tc_num_sms()));
-    tc_bs_tm_kernel<MODE, kL1><<<grid, kThreads, kSmem, s>>>(tmW, tmX, args);
+    tc_bs_tm_kernel<MODE, kL1><<<grid, kThreads, kSmem, s>>>(tmW, tmX, tmSW, tmSX, args);
     return cudaGetLastError();
 }
 
@@ -491,8 +514,10 @@ cudaError_t launch_tm(const Plan& p, const void* w, const void* w_scale, const f
 bool bs_tm_supported(const Plan& p, int stage) {
     if ((p.mode != MOE_A8W8_FP8 && p.mode != MOE_A8W4_FP8_FP4) || p.E > kMaxExperts || !tc_encode_available())
         return false;
-    if (stage == 1) return p.I % 128 == 0 && p.H % kAtomK == 0;
-    return p.H % kWN == 0 && p.I % kAtomK == 0;
+    // scale rows by TMA: their byte pitch (K / 32; K / 32 for the fp32 per-128 token scales
+    // too) must be a multiple of 16
+    if (stage == 1) return p.I % 128 == 0 && p.H % 512 == 0;
+    return p.H % kWN == 0 && p.I % 512 == 0;
 }
 
 cudaError_t launch_l1_bs_tm(const Plan& p, const void* w1, const void* w1_scale, cudaStream_t s) {
