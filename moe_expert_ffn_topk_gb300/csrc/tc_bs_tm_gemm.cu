@@ -4,24 +4,26 @@
 // A8W8-FP use case, "DQ_MX ... implicitly performed inside matmul"; DeepGEMM page, section 4,
 // step 5: block-scaled MMA with UE8M0 scale factors in tensor memory).
 //
-// Tile: M = 128 pool rows (one 128-row route tile of an expert) x N = 256 weight rows, K = 128
-// per stage (MMAs of K = 32):
+// Tile: M = 128 pool rows (one 128-row route tile of an expert) x N weight rows, K = 128 per
+// stage (MMAs of K = 32):
 // - L1: the 128 gate rows and the 128 up rows of outputs [128s, 128s + 128) (one 4-D TMA box),
 //   so a thread of the epilogue holds its token's gate and up values of the same outputs and
 //   applies SwiGLU (Ascend page, "SwiGLU Activation") and the MX FP8 re-quantisation of A (one
 //   exponent per 32 outputs) without any exchange between threads;
-// - L2: 256 hidden columns; the epilogue scales the token's row by G and writes its bf16
-//   combine row (Ascend page, "Token Combine") with 16-byte stores.
+// - L2: N = 224 hidden columns when H is a multiple of 224 (else 256); the epilogue scales the
+//   token's row by G and writes its bf16 combine row (Ascend page, "Token Combine").
 // Why this shape: these GEMMs are bound by how fast TMA fills shared memory (about 55-68 bytes
 // per clock per SM measured on this GPU with 192 KB in flight). Per 128-K stage a tile takes
 // 16 KB of tokens and 32 KB of weights (e2m1 occupies a byte per code in the MMA's 4-bit
 // layout) for 128 x 256 x 128 MACs: 24 KB per 128^3, where 128 weight rows x 128 tokens take
-// 32 KB. The price is a single-buffered accumulator: two 256-column accumulators fill the
-// 512 TMEM columns and leave none for the scale factors. The epilogue releases it as soon as
-// its last columns are loaded into registers.
+// 32 KB. With N = 256 the accumulator is single-buffered (two 256-column accumulators fill the
+// 512 TMEM columns and leave none for the scale factors): eight epilogue warps, two per lane
+// quarter, each drain half of its columns and release it as soon as they are in registers.
+// N = 224 (L2) fits two accumulators and the scale ring (2 * 224 + 64 = 512 columns), so the
+// epilogue of a tile overlaps the main loop of the next.
 //
-// TMEM: accumulator in columns 0-255; scale factors in a ring of 16-column slots from column
-// 256, one per stage. Layout the MMA reads (measured on this GPU, M = 128): the scale word of A
+// TMEM: accumulator(s) from column 0; scale factors in a ring of 16-column slots after them, one
+// per stage. Layout the MMA reads (measured on this GPU, M = 128): the scale word of A
 // row r (a token) in lane r, column slot + r/32; the scale word of B row n (a weight row) in
 // lane 32*q + n%32 of every lane quarter q, column slot + 4 + n/32; byte k of a word is the
 // scale of K group k of the stage.
@@ -31,9 +33,10 @@
 // use, into a 4-deep ring: scattered 4-byte loads of them by the scale warps slowed the operand
 // TMA down by a quarter (measured). The scale warps only move them from shared to tensor memory.
 //
-// Warp roles (320 threads): 0 TMA producer, 1 TMEM allocation + MMA issuer, 2-5 epilogue (warp
-// w owns TMEM lanes 32*(w%4) .. +31, i.e. those token rows), 6-9 scale writers. Every wait is
-// bounded; on time-out the CTA records MOE_ERR_TIMEOUT, drains and exits.
+// Warp roles (448 threads): 0 TMA producer, 1 TMEM allocation + MMA issuer, 2-5 and 10-13
+// epilogue (warp w owns TMEM lanes 32*(w%4) .. +31, i.e. those token rows; warps 2-5 take the
+// first half of the columns, 10-13 the second), 6-9 scale writers. Every wait is bounded; on
+// time-out the CTA records MOE_ERR_TIMEOUT, drains and exits.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -50,29 +53,35 @@ namespace {
 using namespace tc;
 
 constexpr int kTM = 128;          // token rows per tile (MMA M)
-constexpr int kWN = 256;          // weight rows per tile (MMA N)
 constexpr int kAtomK = 128;       // K per stage: one 128-byte swizzle atom of e4m3 / expanded e2m1
 constexpr int kStages = 4;
-constexpr int kThreads = 320;
+constexpr int kThreads = 448;
 constexpr int kMaxExperts = 1024;
-constexpr int kTokBytes = kTM * 128;                 // 16 KB
-constexpr int kWBytes = kWN * 128;                   // 32 KB in shared memory
-constexpr int kStageBytes = kTokBytes + kWBytes;
-constexpr int kSfCol0 = 256;
-constexpr int kSfColsPerStage = 16;  // SFA 4 columns, SFB 8 columns
-constexpr int kSfBlk = 4;            // K atoms per scale block (16 bytes of a row)
-constexpr int kSfBufs = 4;           // scale ring depth: blocks issued two ahead of their use
-constexpr int kSfWBytes = kWN * 16;  // weight scale words of a block: [256 rows][4 atoms]
-constexpr int kSfTBytes = kTM * 16;  // token scale words of a block: [128 rows][4 atoms]
-constexpr int kSfOff = kStages * kStageBytes;
-constexpr int kBarOff = kSfOff + kSfBufs * (kSfWBytes + kSfTBytes);
-constexpr int kNumBars = 2 * kStages + 2 + 1 + 2 * kSfBufs;  // full, empty, acc full/empty, drain, scale full/empty
-constexpr int kMiscOff = kBarOff + 8 * kNumBars;
-constexpr int kTileOffOff = kMiscOff + 16;
-constexpr int kCountsOff = kTileOffOff + 4 * (kMaxExperts + 1);
-constexpr size_t kSmem = 1024 + (size_t)kCountsOff + 4 * kMaxExperts;
-static_assert(kSmem <= 232448, "shared memory");
-static_assert(kSfCol0 + kStages * kSfColsPerStage <= 512, "tensor memory");
+constexpr int kTokBytes = kTM * 128;   // 16 KB
+constexpr int kSfColsPerStage = 16;    // SFA 4 columns, SFB N/32 columns
+constexpr int kSfBlk = 4;              // K atoms per scale block (16 bytes of a row)
+constexpr int kSfBufs = 4;             // scale ring depth: blocks issued two ahead of their use
+constexpr int kSfTBytes = kTM * 16;    // token scale words of a block: [128 rows][4 atoms]
+
+template <int kWN>  // weight rows per tile (MMA N): 256, or 224 with two accumulators
+struct TmCfg {
+    static constexpr int kAccs = 2 * kWN + kStages * kSfColsPerStage <= 512 ? 2 : 1;
+    static constexpr int kSfCol0 = kAccs * kWN;
+    static constexpr int kWBytes = kWN * 128;  // in shared memory
+    static constexpr int kStageBytes = kTokBytes + kWBytes;
+    static constexpr int kSfWBytes = kWN * 16;  // weight scale words of a block: [N rows][4 atoms]
+    static constexpr int kSfOff = kStages * kStageBytes;
+    static constexpr int kBarOff = kSfOff + kSfBufs * (kSfWBytes + kSfTBytes);
+    // full, empty, acc full/empty x2, drain, scale full/empty
+    static constexpr int kNumBars = 2 * kStages + 4 + 1 + 2 * kSfBufs;
+    static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
+    static constexpr int kTileOffOff = kMiscOff + 16;
+    static constexpr int kCountsOff = kTileOffOff + 4 * (kMaxExperts + 1);
+    static constexpr size_t kSmem = 1024 + (size_t)kCountsOff + 4 * kMaxExperts;
+    static_assert(kSmem <= 232448, "shared memory");
+    static_assert(kSfCol0 + kStages * kSfColsPerStage <= 512, "tensor memory");
+    static_assert(kWN % 32 == 0 && kWN <= 256 && 4 + kWN / 32 <= kSfColsPerStage, "tile");
+};
 
 struct TmArgs {
     Plan p;
@@ -107,8 +116,8 @@ __device__ __forceinline__ Tile decode_tile(int t, const int* tile_off, const in
 // kind::mxf8f6f4.block_scale instruction descriptor: B scale id (bits 4-5), A type (7-9: e4m3
 // tokens = 0), B type (10-12: e4m3 = 0, e2m1 = 5), both K-major, N >> 3 (17-22), UE8M0 scales
 // (bit 23), M >> 4 (24-28), A scale id (29-30).
-__device__ __forceinline__ uint32_t tm_idesc(uint32_t bfmt, int sf_id) {
-    return ((uint32_t)sf_id << 4) | (0u << 7) | (bfmt << 10) | ((uint32_t)(kWN >> 3) << 17) | (1u << 23) |
+__device__ __forceinline__ uint32_t tm_idesc(uint32_t bfmt, int n, int sf_id) {
+    return ((uint32_t)sf_id << 4) | (0u << 7) | (bfmt << 10) | ((uint32_t)(n >> 3) << 17) | (1u << 23) |
            ((uint32_t)(kTM >> 4) << 24) | ((uint32_t)sf_id << 29);
 }
 
@@ -154,29 +163,32 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
     return pair;
 }
 
-template <int MODE, bool kL1>
+template <int MODE, bool kL1, int kWN>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bs_tm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                     const __grid_constant__ CUtensorMap tmSW, const __grid_constant__ CUtensorMap tmSX, TmArgs args) {
+    using Cfg = TmCfg<kWN>;
     constexpr bool kFp4 = MODE == MOE_A8W4_FP8_FP4;
     constexpr uint32_t kBfmt = kFp4 ? 5u : 0u;
     constexpr uint32_t kWTx = kFp4 ? kWN * kAtomK / 2 : kWN * kAtomK;  // TMA counts the packed global bytes
+    constexpr int kStageBytes = Cfg::kStageBytes, kSfOff = Cfg::kSfOff, kSfWBytes = Cfg::kSfWBytes;
+    constexpr int kSfCol0 = Cfg::kSfCol0, kAccs = Cfg::kAccs;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = smem_u32(smem_raw);
     const uint32_t base = (raw_base + 1023u) & ~1023u;
     uint8_t* smem = smem_raw + (base - raw_base);
-    const uint32_t bars = base + kBarOff;
+    const uint32_t bars = base + Cfg::kBarOff;
     auto full_bar = [&](int s) { return bars + 8u * s; };
     auto empty_bar = [&](int s) { return bars + 8u * (kStages + s); };
-    const uint32_t acc_full = bars + 8u * (2 * kStages);
-    const uint32_t acc_empty = acc_full + 8u;
-    const uint32_t drain_bar = acc_full + 16u;
-    auto sf_full = [&](int b) { return bars + 8u * (2 * kStages + 3 + b); };
-    auto sf_empty = [&](int b) { return bars + 8u * (2 * kStages + 3 + kSfBufs + b); };
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kMiscOff);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
-    int* tile_off = reinterpret_cast<int*>(smem + kTileOffOff);
-    int* counts = reinterpret_cast<int*>(smem + kCountsOff);
+    auto acc_full = [&](int a) { return bars + 8u * (2 * kStages + a); };
+    auto acc_empty = [&](int a) { return bars + 8u * (2 * kStages + 2 + a); };
+    const uint32_t drain_bar = bars + 8u * (2 * kStages + 4);
+    auto sf_full = [&](int b) { return bars + 8u * (2 * kStages + 5 + b); };
+    auto sf_empty = [&](int b) { return bars + 8u * (2 * kStages + 5 + kSfBufs + b); };
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kMiscOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kMiscOff + 4);
+    int* tile_off = reinterpret_cast<int*>(smem + Cfg::kTileOffOff);
+    int* counts = reinterpret_cast<int*>(smem + Cfg::kCountsOff);
 
     const Plan& p = args.p;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -187,8 +199,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(full_bar(s), 1 + 4);  // TMA (arrive + bytes) + the 4 scale-writer warps
             mbar_init(empty_bar(s), 1);
         }
-        mbar_init(acc_full, 1);
-        mbar_init(acc_empty, 4);
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(acc_full(a), 1);
+            mbar_init(acc_empty(a), 8);  // the 8 epilogue warps
+        }
         mbar_init(drain_bar, 1);
         for (int b = 0; b < kSfBufs; ++b) {
             mbar_init(sf_full(b), 1);   // the producer (arrive + bytes)
@@ -284,8 +298,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             int it = 0, tc = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tc) {
-                if (!mbar_wait(acc_empty, ((uint32_t)tc & 1u) ^ 1u, p.hdr, abort_flag)) break;
+                const int a = tc % kAccs;
+                if (!mbar_wait(acc_empty(a), ((uint32_t)(tc / kAccs) & 1u) ^ 1u, p.hdr, abort_flag)) break;
                 tc_fence_after();
+                const uint32_t d = tmem_base + (uint32_t)(a * kWN);
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int s = it % kStages;
                     if (!mbar_wait(full_bar(s), (uint32_t)(it / kStages) & 1u, p.hdr, abort_flag)) {
@@ -297,19 +313,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t sf = tmem_base + kSfCol0 + s * kSfColsPerStage;
 #pragma unroll
                     for (int kk = 0; kk < kAtomK / 32; ++kk)
-                        tm_mma(tmem_base, kmajor_desc(sa, kk), kmajor_desc(sb, kk), tm_idesc(kBfmt, kk), sf, sf + 4,
+                        tm_mma(d, kmajor_desc(sa, kk), kmajor_desc(sb, kk), tm_idesc(kBfmt, kWN, kk), sf, sf + 4,
                                (kb | kk) != 0);
                     tc_commit(empty_bar(s));
                 }
-                if (ok) tc_commit(acc_full);
+                if (ok) tc_commit(acc_full(a));
             }
             tc_commit(drain_bar);
             mbar_drain(drain_bar, 0, p.hdr);
         }
-    } else if (warp >= 6) {
+    } else if (warp >= 6 && warp < 10) {
         // ---------------- scale writers ----------------
         // Lane l of warp q writes TMEM lane 32q + l: the A word of token row r = 32q + l and the
-        // B words of weight rows 32c + l (c = 0..7), all read from the scale block in shared
+        // B words of weight rows 32c + l (c < N/32), all read from the scale block in shared
         // memory ([row][4 atoms] words; 4-way bank conflicts at most).
         const int q = warp & 3;
         const int r = 32 * q + lane;
@@ -337,15 +353,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t ta = sx[r * kSfBlk + i];
                     if constexpr (kL1 && kFp4) ta = ((ta >> 23) & 0xffu) * 0x01010101u;  // power-of-two fp32 scale
                     if (!tok_valid) ta = 0x7f7f7f7fu;  // 1.0 for the padding rows
-                    // slot columns: 0-3 the A word (the MMA reads column q of lane quarter q), 4-11
-                    // the B words of weight rows 32c + lane, 12-15 unused
+                    // slot columns: 0-3 the A word (the MMA reads column q of lane quarter q), then
+                    // the B words of weight rows 32c + lane (c < N/32), the rest unused
                     uint32_t v[16];
 #pragma unroll
                     for (int c = 0; c < 4; ++c) v[c] = ta;
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) v[4 + c] = sw[(32 * c + lane) * kSfBlk + i];
-#pragma unroll
-                    for (int c = 12; c < 16; ++c) v[c] = 0x7f7f7f7fu;
+                    for (int c = 0; c < 12; ++c) v[4 + c] = c < kWN / 32 ? sw[(32 * c + lane) * kSfBlk + i] : 0x7f7f7f7fu;
                     tmem_st16(tmem_base + ((uint32_t)(32 * q) << 16) + kSfCol0 + s * kSfColsPerStage, v);
                     tmem_st_wait();
                     tc_fence_before();
@@ -358,12 +372,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else {
-        // ---------------- epilogue (warps 2..5): thread = token row ----------------
+        // ---------------- epilogue (warps 2..5, 10..13): thread = token row ----------------
         const int q = warp & 3;
+        const int half = warp >= 10;  // which half of the tile's columns this warp drains
         const int r = 32 * q + lane;
-        const uint32_t tb = tmem_base + ((uint32_t)(32 * q) << 16);
         int tc = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++tc) {
+            const int a = tc % kAccs;
+            const uint32_t tb = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(a * kWN);
             const Tile tl = tile_of(t);
             const bool valid = r < tl.n_valid;
             const int64_t row = tl.row0 + r;
@@ -374,24 +390,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 src = valid ? __ldg(p.pool_src + row) : -1;
                 gw = src >= 0 ? __ldg(args.topk_weights + src) : 0.0f;
             }
-            const bool w_ok = mbar_wait(acc_full, (uint32_t)tc & 1u, p.hdr, abort_flag);
+            const bool w_ok = mbar_wait(acc_full(a), (uint32_t)(tc / kAccs) & 1u, p.hdr, abort_flag);
             if (!__all_sync(0xffffffffu, w_ok)) break;
             tc_fence_after();
-            auto release = [&]() {  // every column of the accumulator is in registers
+            auto release = [&]() {  // this warp's columns of the accumulator are in registers
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(acc_empty);
+                if (lane == 0) mbar_arrive(acc_empty(a));
             };
             if constexpr (kL1) {
-                // A = SiLU(gate) * up for outputs 128s + 32c .. +31, then MX FP8: one UE8M0
-                // exponent per 32 outputs of the token, 32 codes as two 16-byte stores
+                // A = SiLU(gate) * up for outputs 128s + 32c .. +31 (c = 2 half, 2 half + 1), then MX
+                // FP8: one UE8M0 exponent per 32 outputs of the token, 32 codes in one 32-byte store
 #pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 2 * half; c < 2 * half + 2; ++c) {
                     uint32_t g[32], u[32];
                     tmem_ld32(tb + 32 * c, g);
                     tmem_ld32(tb + 128 + 32 * c, u);
                     tmem_ld_wait();
-                    if (c == 3) release();
+                    if (c == 2 * half + 1) release();
                     float av[32];
                     float amax = 0.0f;
 #pragma unroll
@@ -411,25 +427,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                     st_global_u8_if(valid, p.a_pool_scale + row * (I / 32) + (j0 >> 5), (uint8_t)(ex + 127));
                 }
             } else {
-                // c = bf16(G * y) for the tile's 256 hidden columns: all of them packed into
+                // c = bf16(G * y) for this warp's half of the tile's hidden columns: packed into
                 // registers first, so the accumulator is released before the stores (a thread's
-                // 512 bytes go to its own combine row, in 32-byte stores: 32 rows per warp
-                // store instruction make the stores the slow part)
-                uint32_t w[128];
+                // bytes go to its own combine row in 32-byte stores; with 32 rows per warp store
+                // instruction the stores are the slow part)
+                constexpr int kChunks = kWN / 32, kMine = (kChunks + 1) / 2;
+                const int c0 = half * kMine, nc = half ? kChunks - kMine : kMine;
+                uint32_t w[16 * kMine];
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    uint32_t y[32];
-                    tmem_ld32(tb + 32 * c, y);
-                    tmem_ld_wait();
+                for (int i = 0; i < kMine; ++i) {
+                    if (i < nc) {
 #pragma unroll
-                    for (int k = 0; k < 16; ++k)
-                        w[16 * c + k] = (uint32_t)float_to_bf16_bits(__fmul_rn(gw, __uint_as_float(y[2 * k]))) |
-                                        ((uint32_t)float_to_bf16_bits(__fmul_rn(gw, __uint_as_float(y[2 * k + 1]))) << 16);
+                        for (int hh = 0; hh < 2; ++hh) {  // 16 columns per load keeps the registers in bounds
+                            uint32_t y[16];
+                            tmem_ld16(tb + 32 * (c0 + i) + 16 * hh, y);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int k = 0; k < 8; ++k)
+                                w[16 * i + 8 * hh + k] =
+                                    (uint32_t)float_to_bf16_bits(__fmul_rn(gw, __uint_as_float(y[2 * k]))) |
+                                    ((uint32_t)float_to_bf16_bits(__fmul_rn(gw, __uint_as_float(y[2 * k + 1]))) << 16);
+                        }
+                    }
                 }
                 release();
-                uint16_t* dst = p.comb + (int64_t)(src >= 0 ? src : 0) * H + tl.s * kWN;
+                uint16_t* dst = p.comb + (int64_t)(src >= 0 ? src : 0) * H + tl.s * kWN + 32 * c0;
 #pragma unroll
-                for (int k = 0; k < 16; ++k) st_global_v8_if(src >= 0, dst + 16 * k, w + 8 * k);
+                for (int k = 0; k < 2 * kMine; ++k)
+                    if (k < 2 * nc) st_global_v8_if(src >= 0, dst + 16 * k, w + 8 * k);
             }
         }
     }
@@ -440,12 +465,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_dealloc(tmem_base, 512);
 }
 
-template <int MODE, bool kL1>
+template <int MODE, bool kL1, int kWN>
 cudaError_t launch_tm(const Plan& p, const void* w, const void* w_scale, const float* topk_weights, cudaStream_t s) {
+    using Cfg = TmCfg<kWN>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(tc_bs_tm_kernel<MODE, kL1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+        attr_err = cudaFuncSetAttribute(tc_bs_tm_kernel<MODE, kL1, kWN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)Cfg::kSmem);
     });
     if (attr_err != cudaSuccess) return attr_err;
     const int n_out = kL1 ? 2 * p.I : p.H;
@@ -505,7 +532,7 @@ cudaError_t launch_tm(const Plan& p, const void* w, const void* w_scale, const f
                 kin};
     const int64_t max_tiles = std::max<int64_t>(1, (p.pool_rows / kTM) * args.n_slabs);
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(max_tiles, tc_num_sms()));
-    tc_bs_tm_kernel<MODE, kL1><<<grid, kThreads, kSmem, s>>>(tmW, tmX, tmSW, tmSX, args);
+    tc_bs_tm_kernel<MODE, kL1, kWN><<<grid, kThreads, Cfg::kSmem, s>>>(tmW, tmX, tmSW, tmSX, args);
     return cudaGetLastError();
 }
 
@@ -517,19 +544,25 @@ bool bs_tm_supported(const Plan& p, int stage) {
     // scale rows by TMA: their byte pitch (K / 32; K / 32 for the fp32 per-128 token scales
     // too) must be a multiple of 16
     if (stage == 1) return p.I % 128 == 0 && p.H % 512 == 0;
-    return p.H % kWN == 0 && p.I % 512 == 0;
+    return (p.H % 224 == 0 || p.H % 256 == 0) && p.I % 512 == 0;
 }
 
 cudaError_t launch_l1_bs_tm(const Plan& p, const void* w1, const void* w1_scale, cudaStream_t s) {
-    if (p.mode == MOE_A8W4_FP8_FP4) return launch_tm<MOE_A8W4_FP8_FP4, true>(p, w1, w1_scale, nullptr, s);
-    if (p.mode == MOE_A8W8_FP8) return launch_tm<MOE_A8W8_FP8, true>(p, w1, w1_scale, nullptr, s);
+    if (p.mode == MOE_A8W4_FP8_FP4) return launch_tm<MOE_A8W4_FP8_FP4, true, 256>(p, w1, w1_scale, nullptr, s);
+    if (p.mode == MOE_A8W8_FP8) return launch_tm<MOE_A8W8_FP8, true, 256>(p, w1, w1_scale, nullptr, s);
     return cudaErrorNotSupported;
 }
 
 cudaError_t launch_l2_bs_tm(const Plan& p, const void* w2, const void* w2_scale, const float* topk_weights,
                             cudaStream_t s) {
-    if (p.mode == MOE_A8W4_FP8_FP4) return launch_tm<MOE_A8W4_FP8_FP4, false>(p, w2, w2_scale, topk_weights, s);
-    if (p.mode == MOE_A8W8_FP8) return launch_tm<MOE_A8W8_FP8, false>(p, w2, w2_scale, topk_weights, s);
+    // N = 224 keeps two accumulators in TMEM (the epilogue overlaps the next tile)
+    const bool n224 = p.H % 224 == 0;
+    if (p.mode == MOE_A8W4_FP8_FP4)
+        return n224 ? launch_tm<MOE_A8W4_FP8_FP4, false, 224>(p, w2, w2_scale, topk_weights, s)
+                    : launch_tm<MOE_A8W4_FP8_FP4, false, 256>(p, w2, w2_scale, topk_weights, s);
+    if (p.mode == MOE_A8W8_FP8)
+        return n224 ? launch_tm<MOE_A8W8_FP8, false, 224>(p, w2, w2_scale, topk_weights, s)
+                    : launch_tm<MOE_A8W8_FP8, false, 256>(p, w2, w2_scale, topk_weights, s);
     return cudaErrorNotSupported;
 }
 

@@ -37,8 +37,11 @@ CASES = {
                   Workload("ragged_int8", "a8w8_int8", 300, 512, 384, 6, 3, 25, 0.05)],
     "a8w4_fp8_fp4": [Workload("tiny_fp4", "a8w4_fp8_fp4", 64, 256, 128, 8, 2, 26, 0.02),
                      Workload("ragged_fp4", "a8w4_fp8_fp4", 300, 512, 384, 6, 2, 27, 0.05),
-                     Workload("skew_fp4", "a8w4_fp8_fp4", 257, 256, 256, 64, 8, 28, 0.05, zipf_s=1.2, zipf_empty=8)],
+                     Workload("skew_fp4", "a8w4_fp8_fp4", 257, 256, 256, 64, 8, 28, 0.05, zipf_s=1.2, zipf_empty=8),
+                     # hidden 3584 = 7 * 512 = 16 * 224: token-major L1 and the 224-column L2 tiles
+                     Workload("n224_fp4", "a8w4_fp8_fp4", 260, 3584, 512, 6, 2, 29, 0.05)],
 }
+CASES["a8w8_fp8"].append(Workload("n224_fp8", "a8w8_fp8", 200, 3584, 512, 5, 2, 30, 0.05))
 ALL = [(m, wl) for m, wls in CASES.items() for wl in wls]
 
 
