@@ -148,14 +148,6 @@ __device__ __forceinline__ void st_global_v4_if(bool pred, void* ptr, uint32_t a
                  "l"(ptr), "r"(a), "r"(b), "r"(c), "r"(d));
 }
 
-// predicated 32-byte global store (sm_100 family); 32-byte aligned address
-__device__ __forceinline__ void st_global_v8_if(bool pred, void* ptr, const uint32_t* v) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %0, 0;\n\t@p st.global.v8.b32 [%1], {%2, %3, %4, %5, %6, %7, %8, %9};\n\t}" ::"r"(
-            (int)pred),
-        "l"(ptr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]));
-}
-
 // two floats -> two e4m3 codes (RN, saturating), the first in the low byte
 __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
     uint16_t pair;

@@ -66,6 +66,13 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, int w,
                                             uint32_t bar) {
     asm volatile(
@@ -81,6 +88,13 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 __device__ __forceinline__ void st_global_u8_if(bool pred, void* ptr, uint8_t v) {
     asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %0, 0;\n\t@p st.global.u8 [%1], %2;\n\t}" ::"r"((int)pred), "l"(ptr),
                  "h"((uint16_t)v));
+}
+// predicated 32-byte global store (sm_100 family); 32-byte aligned address
+__device__ __forceinline__ void st_global_v8_if(bool pred, void* ptr, const uint32_t* v) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %0, 0;\n\t@p st.global.v8.b32 [%1], {%2, %3, %4, %5, %6, %7, %8, %9};\n\t}" ::"r"(
+            (int)pred),
+        "l"(ptr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]));
 }
 __device__ __forceinline__ void st_global_u16_if(bool pred, void* ptr, uint16_t v) {
     asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %0, 0;\n\t@p st.global.u16 [%1], %2;\n\t}" ::"r"((int)pred), "l"(ptr),

@@ -60,6 +60,7 @@ struct TcArgs {
     int n_tiles;                // column blocks per expert
     int k_blocks;               // K / 64
     int k_rows;                 // rows of one expert's weight in its 2-D view (L1: H, L2: I)
+    int b_one_box;              // B map brings a stage's four 64-column blocks in one copy
 };
 
 // A tile: 128 rows x 64 K, K-major, 128-byte swizzle (the TMA box layout). 8-row groups are
@@ -166,7 +167,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive_expect_tx(full_bar(s), kStageBytes);
                     tma_load_2d(sa, &tmA, kb * kBK, tl.row0, full_bar(s));
                     const int y = wrow + kb * kBK;
-                    if (kL1) {
+                    if (args.b_one_box) {
+                        // [64 columns][K row][column block](L1: [gate, up]) in one copy
+                        if (kL1)
+                            tma_load_4d(sb, &tmB, 0, y, 2 * tl.n, 0, full_bar(s));
+                        else
+                            tma_load_3d(sb, &tmB, 0, y, 4 * tl.n, full_bar(s));
+                    } else if (kL1) {
                         const int g0 = tl.n * 128, u0 = p.I + tl.n * 128;
                         tma_load_2d(sb, &tmB, g0, y, full_bar(s));
                         tma_load_2d(sb + kBBoxBytes, &tmB, g0 + 64, y, full_bar(s));
@@ -230,12 +237,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         int tc = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++tc) {
             const int a = tc & 1;
+            const Tile tl = decode_tile(t, tile_off, p.E, args.n_tiles);
+            const int64_t row = tl.row0 + q * 32 + lane;
+            // L2: the row's combine slot and gate weight, read while the tile's MMAs still run
+            int src = -1;
+            float gw = 0.0f;
+            if (!kL1) {
+                src = __ldg(p.pool_src + row);
+                gw = src >= 0 ? __ldg(args.topk_weights + src) : 0.0f;
+            }
             // every lane waits; the warp goes on only if all of them saw the phase complete
             const bool ok = mbar_wait(tfull_bar(a), (uint32_t)(tc >> 1) & 1u, p.hdr, abort_flag);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
-            const Tile tl = decode_tile(t, tile_off, p.E, args.n_tiles);
-            const int64_t row = tl.row0 + q * 32 + lane;
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * kBN);
             if (kL1) {
                 uint16_t* out = reinterpret_cast<uint16_t*>(p.a_pool) + row * p.I + tl.n * 128;
@@ -252,33 +266,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float a1 = silu(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]);
                         packed[j] = (uint32_t)float_to_bf16_bits(a0) | ((uint32_t)float_to_bf16_bits(a1) << 16);
                     }
-                    uint4* dst = reinterpret_cast<uint4*>(out + c * 32);
-#pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+                    st_global_v8_if(true, out + c * 32, packed);
+                    st_global_v8_if(true, out + c * 32 + 16, packed + 8);
                 }
             } else {
-                const int src = p.pool_src[row];
-                const float gw = src >= 0 ? args.topk_weights[src] : 0.0f;
                 uint16_t* out = p.comb + (int64_t)(src >= 0 ? src : 0) * p.H + tl.n * kBN;
 #pragma unroll 1
                 for (int c = 0; c < kBN / 32; ++c) {
                     uint32_t r[32];
                     tmem_ld32(tbase + c * 32, r);
                     tmem_ld_wait();
-                    if (src >= 0) {
-                        uint32_t packed[16];
+                    uint32_t packed[16];
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const float y0 = __fmul_rn(gw, __uint_as_float(r[2 * j]));
-                            const float y1 = __fmul_rn(gw, __uint_as_float(r[2 * j + 1]));
-                            packed[j] = (uint32_t)float_to_bf16_bits(y0) | ((uint32_t)float_to_bf16_bits(y1) << 16);
-                        }
-                        uint4* dst = reinterpret_cast<uint4*>(out + c * 32);
-#pragma unroll
-                        for (int v = 0; v < 4; ++v)
-                            dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+                    for (int j = 0; j < 16; ++j) {
+                        const float y0 = __fmul_rn(gw, __uint_as_float(r[2 * j]));
+                        const float y1 = __fmul_rn(gw, __uint_as_float(r[2 * j + 1]));
+                        packed[j] = (uint32_t)float_to_bf16_bits(y0) | ((uint32_t)float_to_bf16_bits(y1) << 16);
                     }
+                    st_global_v8_if(src >= 0, out + c * 32, packed);
+                    st_global_v8_if(src >= 0, out + c * 32 + 16, packed + 8);
                 }
             }
             tc_fence_before();
@@ -333,19 +339,46 @@ bool tc_supported(const Plan& p, int stage) {
     return p.H % kBN == 0;
 }
 
+// B (weights, N contiguous) as [64 columns][K row][64-column block] (+ [gate, up] for L1), so one
+// box brings a stage's four 8 KB blocks in the MMA's layout: the dimensions are listed in the
+// order the box is written, so their strides do not increase. Falls back to 2-D boxes (four
+// copies a stage) when the driver's encoder does not take such a map.
+bool make_b_map(CUtensorMap* map, const void* w, uint64_t n_cols, uint64_t rows, uint64_t half_cols, bool l1,
+                int* one_box) {
+    const uint64_t pitch = n_cols * 2;
+    bool ok;
+    if (l1) {
+        const uint64_t dims[4] = {64, rows, half_cols / 64, 2};
+        const uint64_t strides[3] = {pitch, 128, half_cols * 2};
+        const uint32_t box[4] = {64, (uint32_t)kBK, 2, 2};
+        ok = tc_make_map_nd(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, w, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    } else {
+        const uint64_t dims[3] = {64, rows, n_cols / 64};
+        const uint64_t strides[2] = {pitch, 128};
+        const uint32_t box[3] = {64, (uint32_t)kBK, 4};
+        ok = tc_make_map_nd(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, w, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    }
+    *one_box = ok ? 1 : 0;
+    return ok || make_map(map, w, n_cols, rows, kBK);
+}
+
 cudaError_t launch_l1_tc(const Plan& p, const void* w1, const void*, cudaStream_t s) {
     CUtensorMap a, b;
+    int one_box = 0;
     if (!make_map(&a, p.x_pool, (uint64_t)p.H, (uint64_t)p.pool_rows, kBM)) return cudaErrorInvalidValue;
-    if (!make_map(&b, w1, (uint64_t)2 * p.I, (uint64_t)p.E * p.H, kBK)) return cudaErrorInvalidValue;
-    TcArgs args{p, nullptr, p.I / 128, p.H / kBK, p.H};
+    if (!make_b_map(&b, w1, (uint64_t)2 * p.I, (uint64_t)p.E * p.H, (uint64_t)p.I, true, &one_box))
+        return cudaErrorInvalidValue;
+    TcArgs args{p, nullptr, p.I / 128, p.H / kBK, p.H, one_box};
     return launch_tc<true>(p, a, b, args, s);
 }
 
 cudaError_t launch_l2_tc(const Plan& p, const void* w2, const void*, const float* topk_weights, cudaStream_t s) {
     CUtensorMap a, b;
+    int one_box = 0;
     if (!make_map(&a, p.a_pool, (uint64_t)p.I, (uint64_t)p.pool_rows, kBM)) return cudaErrorInvalidValue;
-    if (!make_map(&b, w2, (uint64_t)p.H, (uint64_t)p.E * p.I, kBK)) return cudaErrorInvalidValue;
-    TcArgs args{p, topk_weights, p.H / kBN, p.I / kBK, p.I};
+    if (!make_b_map(&b, w2, (uint64_t)p.H, (uint64_t)p.E * p.I, (uint64_t)p.H, false, &one_box))
+        return cudaErrorInvalidValue;
+    TcArgs args{p, topk_weights, p.H / kBN, p.I / kBK, p.I, one_box};
     return launch_tc<false>(p, a, b, args, s);
 }
 
