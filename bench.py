@@ -352,29 +352,54 @@ def run_gb300(args, wl, rank, world, local_rank):
         raise RuntimeError(f"device error in the timed region: {moe.moe_status_string(st)}")
     elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
 
-    # end to end through the public API with host buffers: H2D of the step's inputs from
-    # pinned memory, the forward call, D2H of y
+    # end to end through the public API with host buffers: every step copies its inputs from
+    # pinned host memory, calls moe_forward and copies y back to pinned host memory. The input and
+    # the output copies run on two more streams with double-buffered device inputs and outputs, so
+    # step i+1's input copy and step i-1's y copy overlap step i's compute (events order each
+    # buffer's use; one copy stream would queue step i+1's inputs behind step i's y).
     host_in = {k: inp[k].cpu().pin_memory() for k in ("x", "x_scale", "topk_ids", "topk_weights")
                if inp[k] is not None}
-    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
-    y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    dev_in = [{k: torch.empty_like(v, device=dev) for k, v in host_in.items()} for _ in range(2)]
+    y_dev = [y, torch.empty_like(y)]
+    y_host = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for _ in range(2)]
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
-    d2h = y_host.numel() * y_host.element_size()
+    d2h = y_host[0].numel() * y_host[0].element_size()
+    in_stream, out_stream = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    in_ready, fwd_done, out_read = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+    state = {"i": 0}
 
     def e2e_step():
-        for k, v in host_in.items():
-            dev_in[k].copy_(v, non_blocking=True)
-        moe.moe_forward(dev_in["x"], dev_in.get("x_scale"), dev_in["topk_ids"], dev_in["topk_weights"], inp["w1"],
-                        inp["w1_scale"], inp["w2"], inp["w2_scale"], y, d, wl.mode, ws, args.flags, stream=stream)
-        y_host.copy_(y, non_blocking=True)
+        b = state["i"] & 1
+        state["i"] += 1
+        with torch.cuda.stream(in_stream):
+            in_stream.wait_event(fwd_done[b])  # the forward two steps back has read dev_in[b]
+            for k, v in host_in.items():
+                dev_in[b][k].copy_(v, non_blocking=True)
+            in_ready[b].record(in_stream)
+        stream.wait_event(in_ready[b])
+        stream.wait_event(out_read[b])  # y_dev[b] of two steps back has been copied out
+        di = dev_in[b]
+        moe.moe_forward(di["x"], di.get("x_scale"), di["topk_ids"], di["topk_weights"], inp["w1"], inp["w1_scale"],
+                        inp["w2"], inp["w2_scale"], y_dev[b], d, wl.mode, ws, args.flags, stream=stream)
+        fwd_done[b].record(stream)
+        with torch.cuda.stream(out_stream):
+            out_stream.wait_event(fwd_done[b])
+            y_host[b].copy_(y_dev[b], non_blocking=True)
+            out_read[b].record(out_stream)
 
+    for e in fwd_done + out_read:
+        e.record(stream)
     for _ in range(max(1, args.warmup)):
         e2e_step()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    stream.wait_stream(in_stream)
+    stream.wait_stream(out_stream)
     barrier()
     e0.record(stream)
     for _ in range(args.steps):
         e2e_step()
+    stream.wait_stream(out_stream)  # the last step's y has reached the host buffer
     e1.record(stream)
     barrier()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
