@@ -176,40 +176,65 @@ __global__ void __launch_bounds__(128) dispatch_gather_kernel(const uint4* __res
 // the INT8 mode it also writes the codes as two f16 planes, hi = floor(q/16) and lo = q mod 16
 // (q = 16*hi + lo, both exact in f16), the operand of the INT8 tensor-core GEMM: with them every
 // fp32 partial sum of that GEMM stays an exactly representable integer.
+// Each thread keeps four 16-byte loads in flight before its stores, and the next row's source
+// index is read while the current row is copied (a row costs two dependent loads otherwise).
 template <int MODE>
 __global__ void __launch_bounds__(128) dispatch_gather_q_kernel(const uint8_t* __restrict__ x, const uint8_t* __restrict__ xs,
                                                                 const int32_t* __restrict__ pool_src,
                                                                 const int32_t* __restrict__ hdr, int K, int H,
                                                                 int scale_bytes, int64_t pool_rows, uint8_t* __restrict__ xp,
                                                                 uint8_t* __restrict__ xps, uint16_t* __restrict__ xb) {
+    constexpr int kUnroll = 4;
     const int rows = hdr[kHdrPadRows];
-    for (int r = blockIdx.x; r < rows; r += gridDim.x) {
-        const int src = pool_src[r];
-        if (src < 0) continue;  // padding row: left as it is (rows are independent everywhere)
-        const int64_t tok = src / K;
-        for (int v = threadIdx.x; v < H / 16; v += blockDim.x) {
-            const uint4 c = reinterpret_cast<const uint4*>(x + tok * H)[v];
-            reinterpret_cast<uint4*>(xp + (int64_t)r * H)[v] = c;
-            if constexpr (MODE == MOE_A8W8_INT8) {
-                const uint8_t* b = reinterpret_cast<const uint8_t*>(&c);
-                uint32_t hi[8], lo[8];
+    const int nv = H / 16;                 // 16-byte vectors of a row of codes
+    const int scale_words = scale_bytes / 4;
+    int r = blockIdx.x;
+    int src = r < rows ? __ldg(pool_src + r) : -1;
+    while (r < rows) {
+        const int rn = r + gridDim.x;
+        const int src_next = rn < rows ? __ldg(pool_src + rn) : -1;
+        if (src >= 0) {  // padding rows are left as they are (rows are independent everywhere)
+            const int64_t tok = src / K;
+            const uint4* xs4 = reinterpret_cast<const uint4*>(x + tok * H);
+            uint4* xd = reinterpret_cast<uint4*>(xp + (int64_t)r * H);
+            for (int v0 = threadIdx.x; v0 < nv; v0 += kUnroll * blockDim.x) {
+                uint4 c[kUnroll];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int q0 = (int8_t)b[2 * j], q1 = (int8_t)b[2 * j + 1];
-                    hi[j] = (uint32_t)float_to_f16_bits((float)(q0 >> 4)) |
-                            ((uint32_t)float_to_f16_bits((float)(q1 >> 4)) << 16);
-                    lo[j] = (uint32_t)float_to_f16_bits((float)(q0 & 15)) |
-                            ((uint32_t)float_to_f16_bits((float)(q1 & 15)) << 16);
+                for (int u = 0; u < kUnroll; ++u) {
+                    const int v = v0 + u * blockDim.x;
+                    if (v < nv) c[u] = __ldg(xs4 + v);
                 }
-                uint4* dh = reinterpret_cast<uint4*>(xb + (int64_t)r * H + v * 16);
-                uint4* dl = reinterpret_cast<uint4*>(xb + (pool_rows + r) * H + v * 16);
-                dh[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                dh[1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
-                dl[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                dl[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    const int v = v0 + u * blockDim.x;
+                    if (v >= nv) break;
+                    xd[v] = c[u];
+                    if constexpr (MODE == MOE_A8W8_INT8) {
+                        const uint8_t* b = reinterpret_cast<const uint8_t*>(&c[u]);
+                        uint32_t hi[8], lo[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const int q0 = (int8_t)b[2 * j], q1 = (int8_t)b[2 * j + 1];
+                            hi[j] = (uint32_t)float_to_f16_bits((float)(q0 >> 4)) |
+                                    ((uint32_t)float_to_f16_bits((float)(q1 >> 4)) << 16);
+                            lo[j] = (uint32_t)float_to_f16_bits((float)(q0 & 15)) |
+                                    ((uint32_t)float_to_f16_bits((float)(q1 & 15)) << 16);
+                        }
+                        uint4* dh = reinterpret_cast<uint4*>(xb + (int64_t)r * H + v * 16);
+                        uint4* dl = reinterpret_cast<uint4*>(xb + (pool_rows + r) * H + v * 16);
+                        dh[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                        dh[1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+                        dl[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                        dl[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+                    }
+                }
             }
+            for (int w = threadIdx.x; w < scale_words; w += blockDim.x)
+                reinterpret_cast<uint32_t*>(xps + (int64_t)r * scale_bytes)[w] =
+                    __ldg(reinterpret_cast<const uint32_t*>(xs + tok * scale_bytes) + w);
         }
-        for (int w = threadIdx.x; w < scale_bytes; w += blockDim.x) xps[(int64_t)r * scale_bytes + w] = xs[tok * scale_bytes + w];
+        r = rn;
+        src = src_next;
     }
 }
 

@@ -241,11 +241,15 @@ __global__ void __launch_bounds__(NT) l2_simt_kernel(Plan p, const uint8_t* __re
 __global__ void __launch_bounds__(256) int8_row_quant_kernel(Plan p) {
     __shared__ float red[8];
     const int rows = p.hdr[kHdrPadRows];
-    const int I = p.I;
+    const int I = p.I, nv = p.I / 4;  // float4 vectors of a row
     for (int r = blockIdx.x; r < rows; r += gridDim.x) {
-        const float* a = p.a_f32 + (int64_t)r * I;
+        if (__ldg(p.pool_src + r) < 0) continue;  // padding row (uniform across the block): never read back
+        const float4* a = reinterpret_cast<const float4*>(p.a_f32 + (int64_t)r * I);
         float m = 0.0f;
-        for (int j = threadIdx.x; j < I; j += blockDim.x) m = fmaxf(m, fabsf(a[j]));
+        for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+            const float4 x = a[v];
+            m = fmaxf(m, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
+        }
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
@@ -255,16 +259,25 @@ __global__ void __launch_bounds__(256) int8_row_quant_kernel(Plan p) {
         for (int w = 1; w < 8; ++w) amax = fmaxf(amax, red[w]);
         __syncthreads();
         const float s = fmaxf(__fdiv_rn(amax, 127.0f), 1e-8f);
-        int8_t* q = reinterpret_cast<int8_t*>(p.a_pool) + (int64_t)r * I;
-        uint16_t* hi = p.a_planes + (int64_t)r * I;             // plane 0: floor(q/16), f16
-        uint16_t* lo = p.a_planes + (p.pool_rows + r) * I;      // plane 1: q mod 16, f16
-        for (int j = threadIdx.x; j < I; j += blockDim.x) {
-            float v = rintf(__fdiv_rn(a[j], s));
-            v = fminf(fmaxf(v, -127.0f), 127.0f);
-            const int qi = static_cast<int>(v);
-            q[j] = static_cast<int8_t>(qi);
-            hi[j] = float_to_f16_bits((float)(qi >> 4));
-            lo[j] = float_to_f16_bits((float)(qi & 15));
+        uint32_t* q = reinterpret_cast<uint32_t*>(p.a_pool + (int64_t)r * I);   // 4 codes per word
+        uint2* hi = reinterpret_cast<uint2*>(p.a_planes + (int64_t)r * I);      // plane 0: floor(q/16), f16
+        uint2* lo = reinterpret_cast<uint2*>(p.a_planes + (p.pool_rows + r) * I);  // plane 1: q mod 16, f16
+        for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+            const float4 x = a[v];
+            const float xv[4] = {x.x, x.y, x.z, x.w};
+            uint32_t qw = 0, h[2] = {0, 0}, l[2] = {0, 0};
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float t = rintf(__fdiv_rn(xv[c], s));
+                t = fminf(fmaxf(t, -127.0f), 127.0f);
+                const int qi = static_cast<int>(t);
+                qw |= (uint32_t)(qi & 0xff) << (8 * c);
+                h[c >> 1] |= (uint32_t)float_to_f16_bits((float)(qi >> 4)) << (16 * (c & 1));
+                l[c >> 1] |= (uint32_t)float_to_f16_bits((float)(qi & 15)) << (16 * (c & 1));
+            }
+            q[v] = qw;
+            hi[v] = make_uint2(h[0], h[1]);
+            lo[v] = make_uint2(l[0], l[1]);
         }
         if (threadIdx.x == 0) reinterpret_cast<float*>(p.a_pool_scale)[r] = s;
     }
