@@ -175,19 +175,47 @@ def mx_scale_exponent(amax32: np.ndarray, elem_max: float) -> np.ndarray:
     return out
 
 
-def quant_mx_fp8(a: np.ndarray):
-    """MX quantisation with 1x32 blocks along the last axis to e4m3 + UE8M0 (p1 A8W8-FP
-    "Q_MX"; DeepGEMM §4 step 6 FP8 re-quantisation). The decision runs on fp32 values:
-    a -> fp32, per-block amax, exponent e, codes = e4m3_rne_satfinite(a / 2^e).
-    Returns (codes uint8 [n, I], scale bytes uint8 [n, I/32])."""
+def quant_mx_fp8(a: np.ndarray, block: int = 32):
+    """MX quantisation with 1 x `block` groups along the last axis to e4m3 + a shared
+    power-of-two exponent (p1 A8W8-FP "Q_MX", group size 32; DeepGEMM §4 step 6 FP8
+    re-quantisation). The decision runs on fp32 values: a -> fp32, per-group amax, exponent e,
+    codes = e4m3_rne_satfinite(a / 2^e).
+    Returns (codes uint8 [n, m], exponents as UE8M0 bytes uint8 [n, m/block])."""
     a32 = np.asarray(a, dtype=np.float64).astype(np.float32).astype(np.float64)
-    n, inter = a32.shape
-    blocks = a32.reshape(n, inter // 32, 32)
+    n, m = a32.shape
+    blocks = a32.reshape(n, m // block, block)
     amax = np.max(np.abs(blocks), axis=2)
     e = mx_scale_exponent(amax, codecs.E4M3_MAX)
     scaled = blocks / np.ldexp(1.0, e.astype(np.int32))[:, :, None]
-    codes = codecs.e4m3_encode_rne_satfinite(scaled).reshape(n, inter)
+    codes = codecs.e4m3_encode_rne_satfinite(scaled).reshape(n, m)
     return codes, (e + 127).astype(np.uint8)
+
+
+def quantize_x(mode: str, x_bf16: np.ndarray):
+    """The operator's own quantisation of the bf16 activations before dispatch, to the mode's
+    x format (p1 parameter dispatch_quant_mode):
+      * A8W8-INT (p1 "A8W8-INT Quantization Use Case", "EP Dispatch"): per token
+        s_i = max|X[i,:]| / 127 and q_i = round(X[i,:] / s_i), as quant_int8_rows (fp32
+        decision, scale floored at 1e-8);
+      * A8W8-FP (p1 "A8W8-FP Quantization Use Case", first phase): Q_MX with groups of 32,
+        e4m3 codes and E8M0 scales;
+      * FP8 activations x FP4 weights: the same shared-exponent rule on groups of 128 gives the
+        mode's x format, e4m3 codes with power-of-two fp32 scales (the DeepGEMM page takes
+        FP8 activations with their scales as the input of fp8_fp4_mega_moe).
+    x_bf16: uint16 bf16 codes [T, H]. Returns (x, x_scale) as moe_forward's x operand takes them:
+    bf16 codes and None for A16W16."""
+    x = np.asarray(x_bf16, dtype=np.uint16)
+    if mode == "a16w16":
+        return x, None
+    xv = codecs.bf16_decode(x)
+    if mode == "a8w8_int8":
+        return quant_int8_rows(xv)
+    if mode == "a8w8_fp8":
+        return quant_mx_fp8(xv, 32)
+    if mode == "a8w4_fp8_fp4":
+        codes, sb = quant_mx_fp8(xv, 128)
+        return codes, np.ldexp(np.float32(1.0), sb.astype(np.int32) - 127).astype(np.float32)
+    raise ValueError(mode)
 
 
 def l2_operand(mode: str, a: np.ndarray):

@@ -127,6 +127,63 @@ def test_mx_fp8_quant_properties():
     assert np.all(rel <= 2.0 ** -4 + 1e-12)
 
 
+def _bf16(v):
+    return codecs.bf16_encode(codecs.round_to_bf16(np.asarray(v, dtype=np.float64)))
+
+
+def test_quantize_x_int8_closed_form_and_invariants():
+    # a row of small integers with max 127: s = 1 exactly and q = the row
+    row = np.array([[127.0, -64.0, 1.0, 0.0, -127.0, 3.0, 100.0, -1.0]])
+    q, s = moe.quantize_x("a8w8_int8", _bf16(row))
+    assert s[0] == np.float32(1.0) and np.array_equal(q[0], row[0].astype(np.int8))
+    rng = np.random.default_rng(11)
+    x = _bf16(rng.standard_normal((32, 256)) * rng.uniform(1e-3, 1e3, size=(32, 1)))
+    xv = codecs.bf16_decode(x)
+    q, s = moe.quantize_x("a8w8_int8", x)
+    assert q.min() >= -127 and q.max() <= 127
+    arg = np.argmax(np.abs(xv), axis=1)
+    assert np.all(np.abs(q[np.arange(32), arg]) == 127)
+    # half a step, plus the fp32 rounding of s and of x/s (a quotient next to .5 can round to
+    # the tie and then to the even integer: x = 972, max 1944 gives 63.5 -> 64)
+    assert np.all(np.abs(q * s[:, None].astype(np.float64) - xv) <= s[:, None] * 0.5 * (1 + 1e-5))
+    q, s = moe.quantize_x("a8w8_int8", _bf16(np.zeros((1, 16))))
+    assert np.all(q == 0) and s[0] == np.float32(1e-8)
+
+
+@pytest.mark.parametrize("mode,block", [("a8w8_fp8", 32), ("a8w4_fp8_fp4", 128)])
+def test_quantize_x_fp8_groups(mode, block):
+    rng = np.random.default_rng(12)
+    x = rng.standard_normal((8, 512)) * rng.uniform(1e-2, 1e2, size=(8, 1))
+    x[2, :block] = 0.0
+    xb = _bf16(x)
+    xv = codecs.bf16_decode(xb)
+    codes, sc = moe.quantize_x(mode, xb)
+    scale = codecs.ue8m0_decode(sc) if mode == "a8w8_fp8" else sc.astype(np.float64)
+    assert scale.shape == (8, 512 // block)
+    assert np.all(np.log2(scale[scale > 0]) == np.round(np.log2(scale[scale > 0])))  # powers of two
+    vals = codecs.e4m3_decode(codes)
+    full = np.repeat(scale, block, axis=1)
+    amax = np.abs(xv).reshape(8, -1, block).max(axis=2)
+    nz = amax > 0
+    assert np.all((amax / scale)[nz] > 224.0) and np.all((amax / scale)[nz] <= 448.0)
+    assert np.all(vals[2, :block] == 0.0)
+    rel = np.abs(vals * full - xv) / np.maximum(np.abs(xv), 2.0 ** -6 * full)
+    assert np.all(rel <= 2.0 ** -4 + 1e-12)
+    # values that are e4m3 codes times the group's power of two come back exactly
+    exact = np.resize(codecs.e4m3_decode(np.arange(0x30, 0x7e, dtype=np.uint8)), block) * 2.0 ** 3
+    exact[0] = 448.0 * 2.0 ** 3  # the group's amax sets the exponent to 3
+    c2, s2 = moe.quantize_x(mode, _bf16(np.tile(exact, (1, 512 // block))))
+    s2v = codecs.ue8m0_decode(s2) if mode == "a8w8_fp8" else s2.astype(np.float64)
+    assert np.all(s2v == 8.0)
+    assert np.array_equal(codecs.e4m3_decode(c2) * 8.0, codecs.bf16_decode(_bf16(np.tile(exact, (1, 512 // block)))))
+
+
+def test_quantize_x_a16w16_is_the_input():
+    x = _bf16(np.linspace(-3, 3, 64).reshape(4, 16))
+    xx, sc = moe.quantize_x("a16w16", x)
+    assert sc is None and np.array_equal(xx, x)
+
+
 def test_int32_accumulator_guard():
     q = np.full((1, 200000), 127, dtype=np.int8)
     w = np.full((200000, 1), 127, dtype=np.int8)
