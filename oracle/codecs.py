@@ -97,7 +97,9 @@ _E4M3_POS = E4M3_VALUES[:0x7F]
 
 def e4m3_encode_rne_satfinite(v: np.ndarray) -> np.ndarray:
     """Round float64 values to the nearest e4m3fn code, ties to the even code, and clamp
-    magnitudes above 448 to 448 (saturating finite conversion). Returns uint8 codes."""
+    magnitudes above 448 to 448 (saturating finite conversion). The sign is kept, also when
+    the magnitude rounds to zero (a negative value gives -0, code 0x80, as a rounding
+    conversion does). Returns uint8 codes."""
     v = np.asarray(v, dtype=np.float64)
     mag = np.minimum(np.abs(v), E4M3_MAX)
     # index of the first table magnitude >= mag
@@ -108,7 +110,7 @@ def e4m3_encode_rne_satfinite(v: np.ndarray) -> np.ndarray:
     d_hi = _E4M3_POS[hi] - mag
     pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
     code = np.where(pick_hi, hi, lo).astype(np.uint8)
-    sign = (np.signbit(v) & (code != 0)).astype(np.uint8) << np.uint8(7)
+    sign = np.signbit(v).astype(np.uint8) << np.uint8(7)
     return code | sign
 
 

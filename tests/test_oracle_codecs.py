@@ -34,13 +34,13 @@ def test_e4m3_encode_matches_torch_rne():
                         codecs.E4M3_VALUES[:0x7F], -codecs.E4M3_VALUES[1:0x7F]])
     # midpoints between neighbouring magnitudes: ties must go to the even code
     mids = (codecs.E4M3_VALUES[1:0x7F] + codecs.E4M3_VALUES[0:0x7E]) / 2
-    v = np.concatenate([v, mids, -mids])
+    # values that round to +-0 (below half the smallest subnormal, and exactly half of it)
+    tiny = np.array([2.0 ** -10, 2.0 ** -11, 1e-6, 0.0])
+    v = np.concatenate([v, mids, -mids, tiny, -tiny])
     v = np.clip(v, -448, 448).astype(np.float32).astype(np.float64)
     ref = torch.from_numpy(v).to(torch.float32).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
     ours = codecs.e4m3_encode_rne_satfinite(v)
-    # +0 / -0 may differ in sign bit only
-    same = (ref == ours) | ((ref & 0x7F) == 0) & ((ours & 0x7F) == 0)
-    assert np.all(same)
+    assert np.array_equal(ours, ref)  # including the sign of a zero result
 
 
 def test_e4m3_encode_saturates():
