@@ -97,9 +97,11 @@ typedef struct {
 enum {
     MOE_FLAG_NONE = 0u,
     MOE_FLAG_SIMT = 1u,         /* run the CUDA-core reference GEMMs instead of the tensor-core ones */
-    MOE_FLAG_WEIGHT_MAJOR = 2u  /* FP8 modes at prefill sizes: 128 weight rows x 128 tokens per tile
+    MOE_FLAG_WEIGHT_MAJOR = 2u, /* FP8 modes at prefill sizes: 128 weight rows x 128 tokens per tile
                                    (the decode-style tile) instead of 128 tokens x 256 weight rows;
                                    same results up to fp32 summation order, for comparison */
+    MOE_FLAG_QUANTIZE_X = 4u    /* moe_forward: x.data is bf16 [T,H] (x.scale unused) and the
+                                   dispatch stage quantises it as moe_dispatch_quantize does */
 };
 
 /* Bytes of workspace that moe_plan / moe_forward and the stage calls need for `d` and `m`.
@@ -126,6 +128,18 @@ MOE_API moe_status moe_plan(const int32_t* topk_ids, const moe_dims* d, int32_t*
  *   x  device operand in the mode's x format. */
 MOE_API moe_status moe_dispatch(moe_operand x, const moe_dims* d, moe_dtype_mode m, void* workspace,
                         size_t workspace_bytes, moe_stream_t stream);
+
+/* Stage S2 from bf16 activations, with the operator's own quantisation before dispatch (Ascend
+ * page: parameter dispatch_quant_mode; A8W8-INT use case "EP Dispatch": per token
+ * s_i = max|X[i,:]|/127, q_i = round(X[i,:]/s_i), scale floored at 1e-8; A8W8-FP use case, first
+ * phase: Q_MX with groups of 32, e4m3 codes and E8M0 scales). For A8W4_FP8_FP4 the same
+ * shared-exponent rule on groups of 128 gives e4m3 codes with fp32 power-of-two scales (the
+ * mode's x format); A16W16 is the plain gather. Each token is quantised once and written to its
+ * K pool rows. Every code is decided on fp32 values (IEEE division, round half to even).
+ * Needs moe_plan first.
+ *   x_bf16  device bf16 [T,H], row-major. */
+MOE_API moe_status moe_dispatch_quantize(const void* x_bf16, const moe_dims* d, moe_dtype_mode m, void* workspace,
+                                 size_t workspace_bytes, moe_stream_t stream);
 
 /* Stages S3+S4, L1 grouped GEMM with SwiGLU and the L2-operand re-quantisation fused
  * (Ascend page: "Linear1 Projection", "SwiGLU Activation", and the A8W8 activation

@@ -18,11 +18,11 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "li
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_BAD_ROUTE, MOE_ERR_TIMEOUT, \
     MOE_ERR_WORKSPACE = range(7)
 MODES = {"a16w16": 0, "a8w8_fp8": 1, "a8w8_int8": 2, "a8w4_fp8_fp4": 3}
-MOE_FLAG_NONE, MOE_FLAG_SIMT, MOE_FLAG_WEIGHT_MAJOR = 0, 1, 2
+MOE_FLAG_NONE, MOE_FLAG_SIMT, MOE_FLAG_WEIGHT_MAJOR, MOE_FLAG_QUANTIZE_X = 0, 1, 2, 4
 
 ABI_FUNCTIONS = ("moe_workspace_bytes", "moe_plan", "moe_dispatch", "moe_expert_l1", "moe_expert_l2",
                  "moe_combine", "moe_forward", "moe_check_device_error", "moe_status_string",
-                 "moe_workspace_layout", "moe_debug_bounded_wait", "moe_plan_noalloc")
+                 "moe_workspace_layout", "moe_debug_bounded_wait", "moe_plan_noalloc", "moe_dispatch_quantize")
 
 
 class MoeDims(ctypes.Structure):
@@ -67,6 +67,7 @@ def _load():
         "moe_workspace_layout": (st, [dims_p, st, ctypes.POINTER(MoeWorkspaceLayout)]),
         "moe_debug_bounded_wait": (st, [vp, sz, ctypes.c_uint64, vp]),
         "moe_plan_noalloc": (st, [vp, dims_p, vp, vp, vp, vp]),
+        "moe_dispatch_quantize": (st, [vp, dims_p, st, vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -150,6 +151,13 @@ def moe_dispatch(x, x_scale, d: MoeDims, mode, workspace, stream=None):
     ws, nb = _ws(workspace)
     _check(LIB.moe_dispatch(_operand(x, x_scale, "x"), ctypes.byref(d), _mode(mode), ws, nb, _stream(stream)),
            "moe_dispatch")
+
+
+def moe_dispatch_quantize(x_bf16, d: MoeDims, mode, workspace, stream=None):
+    """S2 from bf16 x with the mode's activation quantisation (x_bf16: bf16 [T, H])."""
+    ws, nb = _ws(workspace)
+    _check(LIB.moe_dispatch_quantize(_ptr(x_bf16, "x_bf16"), ctypes.byref(d), _mode(mode), ws, nb, _stream(stream)),
+           "moe_dispatch_quantize")
 
 
 def moe_expert_l1(w1, w1_scale, d: MoeDims, mode, workspace, flags=0, stream=None):

@@ -162,6 +162,15 @@ moe_status moe_dispatch(moe_operand x, const moe_dims* d, moe_dtype_mode m, void
     return from_cuda(launch_dispatch(p, x.data, x.scale, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+moe_status moe_dispatch_quantize(const void* x_bf16, const moe_dims* d, moe_dtype_mode m, void* workspace,
+                                 size_t workspace_bytes, moe_stream_t stream) {
+    Plan p;
+    moe_status st = make_plan_view(d, m, workspace, workspace_bytes, &p, true);
+    if (st != MOE_OK) return st;
+    if (d->num_tokens > 0 && !x_bf16) return MOE_ERR_INVALID_ARG;
+    return from_cuda(launch_dispatch_quant(p, x_bf16, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 moe_status moe_expert_l1(moe_operand w1, const moe_dims* d, moe_dtype_mode m, uint32_t flags, void* workspace,
                          size_t workspace_bytes, moe_stream_t stream) {
     Plan p;
@@ -220,9 +229,13 @@ moe_status moe_forward(moe_operand x, const int32_t* topk_ids, const float* topk
     const bool q = m != MOE_A16W16;
     if (!operand_ok(w1, q) || !operand_ok(w2, q)) return MOE_ERR_INVALID_ARG;
     if (d->num_tokens == 0) return MOE_OK;
-    if (!operand_ok(x, q) || !topk_ids || !topk_weights || !y) return MOE_ERR_INVALID_ARG;
+    const bool quantize_x = (flags & MOE_FLAG_QUANTIZE_X) != 0;
+    if (!(quantize_x ? x.data != nullptr : operand_ok(x, q)) || !topk_ids || !topk_weights || !y)
+        return MOE_ERR_INVALID_ARG;
     if ((st = moe_plan(topk_ids, d, nullptr, nullptr, nullptr, workspace, workspace_bytes, stream)) != MOE_OK) return st;
-    if ((st = moe_dispatch(x, d, m, workspace, workspace_bytes, stream)) != MOE_OK) return st;
+    st = quantize_x ? moe_dispatch_quantize(x.data, d, m, workspace, workspace_bytes, stream)
+                    : moe_dispatch(x, d, m, workspace, workspace_bytes, stream);
+    if (st != MOE_OK) return st;
     if ((st = moe_expert_l1(w1, d, m, flags, workspace, workspace_bytes, stream)) != MOE_OK) return st;
     if ((st = moe_expert_l2(w2, topk_weights, d, m, flags, workspace, workspace_bytes, stream)) != MOE_OK) return st;
     return moe_combine(y, d, workspace, workspace_bytes, stream);

@@ -59,6 +59,8 @@ cudaError_t launch_l1_simt(const Plan& p, const void* w1, const void* w1_scale, 
 cudaError_t launch_l2_simt(const Plan& p, const void* w2, const void* w2_scale, const float* topk_weights,
                            cudaStream_t s);
 cudaError_t launch_int8_row_quant(const Plan& p, cudaStream_t s);
+// S2 from bf16 x with the mode's activation quantisation (A16W16: the plain gather).
+cudaError_t launch_dispatch_quant(const Plan& p, const void* x_bf16, cudaStream_t s);
 cudaError_t launch_debug_wait(const Plan& p, uint64_t timeout_ns, cudaStream_t s);
 
 // Tensor-core path. Returns cudaErrorNotSupported when the mode / shape has no tcgen05 kernel.

@@ -238,6 +238,92 @@ __global__ void __launch_bounds__(128) dispatch_gather_q_kernel(const uint8_t* _
     }
 }
 
+// S2 with the operator's own activation quantisation (Ascend page, A8W8-INT use case "EP
+// Dispatch": per token s = max|X[i,:]|/127, q = round(X/s); A8W8-FP use case: Q_MX with groups
+// of 32 and E8M0 scales; FP8 activations x FP4 weights: the same shared-exponent rule on groups
+// of 128, fp32 power-of-two scales, the mode's x format). One CTA per token: its bf16 row is
+// quantised once and written to each of its K pool rows. Warp w takes 128-element chunks, 4
+// elements per lane. Every code is decided on fp32 values: IEEE division for the int8 scale
+// and quotient, exact power-of-two scaling before the e4m3 rounding.
+template <int MODE>
+__global__ void __launch_bounds__(256) dispatch_quant_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ slot_row,
+                                                             int T, int K, int H, int64_t pool_rows, uint8_t* __restrict__ xp,
+                                                             uint8_t* __restrict__ xps, uint16_t* __restrict__ xb) {
+    __shared__ float red[8];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int t = blockIdx.x; t < T; t += gridDim.x) {
+        // pool row of slot `lane` (K <= 32), shuffled to all lanes when the chunk is stored
+        const int my_row = lane < K ? __ldg(slot_row + (int64_t)t * K + lane) : -1;
+        const uint2* xr = reinterpret_cast<const uint2*>(x + (int64_t)t * H);  // 4 bf16 per uint2
+        float s_int8 = 0.0f;
+        if constexpr (MODE == MOE_A8W8_INT8) {
+            float m = 0.0f;
+            for (int c = threadIdx.x; c < H / 4; c += blockDim.x) {
+                const uint2 v = __ldg(xr + c);
+                m = fmaxf(m, fmaxf(fmaxf(fabsf(bf16_bits_to_float(v.x & 0xffff)), fabsf(bf16_bits_to_float(v.x >> 16))),
+                                   fmaxf(fabsf(bf16_bits_to_float(v.y & 0xffff)), fabsf(bf16_bits_to_float(v.y >> 16)))));
+            }
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            if (lane == 0) red[warp] = m;
+            __syncthreads();
+            float amax = red[0];
+#pragma unroll
+            for (int w = 1; w < 8; ++w) amax = fmaxf(amax, red[w]);
+            __syncthreads();
+            s_int8 = fmaxf(__fdiv_rn(amax, 127.0f), 1e-8f);
+        }
+        for (int c0 = warp * 128; c0 < H; c0 += 8 * 128) {
+            const uint2 v = __ldg(xr + c0 / 4 + lane);
+            const float f[4] = {bf16_bits_to_float(v.x & 0xffff), bf16_bits_to_float(v.x >> 16),
+                                bf16_bits_to_float(v.y & 0xffff), bf16_bits_to_float(v.y >> 16)};
+            uint32_t code = 0, hi[2] = {0, 0}, lo[2] = {0, 0};
+            int ex = 0;  // FP8 modes: exponent of this lane's group
+            if constexpr (MODE == MOE_A8W8_INT8) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float q = rintf(__fdiv_rn(f[c], s_int8));
+                    q = fminf(fmaxf(q, -127.0f), 127.0f);
+                    const int qi = (int)q;
+                    code |= (uint32_t)(qi & 0xff) << (8 * c);
+                    hi[c >> 1] |= (uint32_t)float_to_f16_bits((float)(qi >> 4)) << (16 * (c & 1));
+                    lo[c >> 1] |= (uint32_t)float_to_f16_bits((float)(qi & 15)) << (16 * (c & 1));
+                }
+            } else {
+                float m = fmaxf(fmaxf(fabsf(f[0]), fabsf(f[1])), fmaxf(fabsf(f[2]), fabsf(f[3])));
+                // group of 32 = 8 lanes (A8W8-FP8) or of 128 = the warp (FP8 x FP4)
+                constexpr int kLanes = MODE == MOE_A8W8_FP8 ? 8 : 32;
+#pragma unroll
+                for (int o = 1; o < kLanes; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                ex = mx_exponent_e4m3(m);
+                const float inv = exp2_neg_int(ex);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) code |= (uint32_t)float_to_e4m3_satfinite(f[c] * inv) << (8 * c);
+            }
+            for (int k = 0; k < K; ++k) {
+                const int prow = __shfl_sync(0xffffffffu, my_row, k);
+                if (prow < 0) continue;  // masked route (uniform across the warp)
+                reinterpret_cast<uint32_t*>(xp + (int64_t)prow * H + c0)[lane] = code;
+                if constexpr (MODE == MOE_A8W8_INT8) {
+                    reinterpret_cast<uint2*>(xb + (int64_t)prow * H + c0)[lane] = make_uint2(hi[0], hi[1]);
+                    reinterpret_cast<uint2*>(xb + (pool_rows + prow) * H + c0)[lane] = make_uint2(lo[0], lo[1]);
+                } else if constexpr (MODE == MOE_A8W8_FP8) {
+                    if ((lane & 7) == 0) xps[(int64_t)prow * (H / 32) + c0 / 32 + lane / 8] = (uint8_t)(ex + 127);
+                } else {
+                    // 2^ex as fp32 (2^-127, a subnormal, for an all-zero group)
+                    if (lane == 0) reinterpret_cast<float*>(xps)[(int64_t)prow * (H / 128) + c0 / 128] = ue8m0_to_float((uint8_t)(ex + 127));
+                }
+            }
+        }
+        if constexpr (MODE == MOE_A8W8_INT8) {
+            if (threadIdx.x < K) {
+                const int prow = my_row;
+                if (prow >= 0) reinterpret_cast<float*>(xps)[prow] = s_int8;
+            }
+        }
+    }
+}
+
 // S6: y[t, 8j..8j+7] = bf16( sum_k comb[t*K+k, 8j..8j+7] ), fp32 sum in slot order.
 __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ comb, const int32_t* __restrict__ slot_row,
                                                       int T, int K, int row_vecs, uint4* __restrict__ y) {
@@ -329,6 +415,29 @@ cudaError_t launch_dispatch(const Plan& p, const void* x, const void* x_scale, c
                                                 p.pool_src, p.hdr, p.K, row_vecs, scale_words,
                                                 reinterpret_cast<uint4*>(p.x_pool),
                                                 reinterpret_cast<uint32_t*>(p.x_pool_scale));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_quant(const Plan& p, const void* x_bf16, cudaStream_t s) {
+    if (p.T == 0) return cudaSuccess;
+    const int grid = (int)std::min<int64_t>(p.T, 152 * 8);
+    const uint16_t* x = static_cast<const uint16_t*>(x_bf16);
+    switch (p.mode) {
+        case MOE_A8W8_FP8:
+            dispatch_quant_kernel<MOE_A8W8_FP8><<<grid, 256, 0, s>>>(x, p.slot_row, p.T, p.K, p.H, p.pool_rows, p.x_pool,
+                                                                     p.x_pool_scale, p.x_planes);
+            break;
+        case MOE_A8W8_INT8:
+            dispatch_quant_kernel<MOE_A8W8_INT8><<<grid, 256, 0, s>>>(x, p.slot_row, p.T, p.K, p.H, p.pool_rows, p.x_pool,
+                                                                      p.x_pool_scale, p.x_planes);
+            break;
+        case MOE_A8W4_FP8_FP4:
+            dispatch_quant_kernel<MOE_A8W4_FP8_FP4><<<grid, 256, 0, s>>>(x, p.slot_row, p.T, p.K, p.H, p.pool_rows,
+                                                                         p.x_pool, p.x_pool_scale, p.x_planes);
+            break;
+        default:  // A16W16: x is already the pool's format
+            return launch_dispatch(p, x_bf16, nullptr, s);
+    }
     return cudaGetLastError();
 }
 

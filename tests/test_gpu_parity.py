@@ -320,3 +320,68 @@ def test_token_major_and_weight_major_block_scaled_tiles_agree(moe, mode, wl):
     ref = oracle_forward(wl, inp)
     for o in outs:
         assert_close(y_numpy(o["y"]), ref, mode)
+
+
+XQ_CASES = [(m, w) for m, w in ALL if m != "a16w16" and w.name in ("tiny_fp8", "ragged_fp8", "tiny_int8", "ragged_int8",
+                                                                    "tiny_fp4", "skew_fp4", "n224_fp4", "n224_fp8")]
+
+
+def _special_rows(x_bf16):
+    """Rows that reach the corners of the quantisers: all zero, tiny, huge, one spike."""
+    x = x_bf16.clone()
+    x[0] = 0.0
+    if x.shape[0] > 3:
+        x[1] = x[1] * 1e-30
+        x[2] = x[2] * 1e30
+        x[3] = 0.0
+        x[3, 5] = -3.0
+    return x.contiguous()
+
+
+@pytest.mark.parametrize("mode,wl", XQ_CASES, ids=[f"{m}-{w.name}" for m, w in XQ_CASES])
+def test_dispatch_quantize_matches_oracle_bit_exactly(moe, mode, wl):
+    """S2 from bf16 x: every routed pool row holds the oracle's quantisation of its token (codes
+    and scales bit-exact: both sides decide in fp32), and the INT8 planes hold its hi/lo split."""
+    inp = make_inputs(wl, device=DEV)
+    xb = _special_rows(inp["x_bf16"])
+    d = moe.dims(wl.T, wl.H, wl.I, wl.E, wl.K)
+    ws = moe.alloc_workspace(d, wl.mode, DEV)
+    moe.moe_plan(inp["topk_ids"], d, ws)
+    moe.moe_dispatch_quantize(xb, d, wl.mode, ws)
+    assert moe.moe_check_device_error(ws) == 0
+    L = moe.moe_workspace_layout(d, wl.mode)
+    R = L["pool_rows"]
+    pool_src = region(ws, L, "pool_src", torch.int32, R).cpu().numpy()
+    rows = np.nonzero(pool_src >= 0)[0]
+    tok = pool_src[rows] // wl.K
+    qx, sx = omoe.quantize_x(mode, to_numpy({"x": xb})["x"])
+    codes = region(ws, L, "x_pool", torch.uint8, R * wl.H).view(R, wl.H).cpu().numpy()[rows]
+    assert np.array_equal(codes, qx.view(np.uint8)[tok]), "codes"
+    if mode == "a8w8_fp8":
+        sc = region(ws, L, "x_pool_scale", torch.uint8, R * (wl.H // 32)).view(R, -1).cpu().numpy()[rows]
+        assert np.array_equal(sc, sx[tok])
+    else:
+        n = wl.H // 128 if mode == "a8w4_fp8_fp4" else 1
+        sc = region(ws, L, "x_pool_scale", torch.float32, R * n).view(R, n).cpu().numpy()[rows]
+        assert np.array_equal(sc.reshape(len(rows), -1), np.asarray(sx, np.float32)[tok].reshape(len(rows), -1))
+    if mode == "a8w8_int8":
+        planes = region(ws, L, "x_pool_planes", torch.float16, 2 * R * wl.H).view(2, R, wl.H).float().cpu().numpy()
+        q = qx.astype(np.int64)[tok]
+        assert np.array_equal(planes[0, rows], np.floor_divide(q, 16)) and np.array_equal(planes[1, rows], q % 16)
+
+
+@pytest.mark.parametrize("mode,wl", XQ_CASES, ids=[f"{m}-{w.name}" for m, w in XQ_CASES])
+def test_forward_quantizing_x_matches_oracle(moe, mode, wl):
+    """moe_forward with MOE_FLAG_QUANTIZE_X on bf16 x equals the oracle on its own quantisation of x."""
+    inp = make_inputs(wl, device=DEV)
+    d = moe.dims(wl.T, wl.H, wl.I, wl.E, wl.K)
+    ws = moe.alloc_workspace(d, wl.mode, DEV)
+    y = torch.full((wl.T, wl.H), float("nan"), dtype=torch.bfloat16, device=DEV)
+    moe.moe_forward(inp["x_bf16"], None, inp["topk_ids"], inp["topk_weights"], inp["w1"], inp["w1_scale"], inp["w2"],
+                    inp["w2_scale"], y, d, wl.mode, ws, moe.MOE_FLAG_QUANTIZE_X)
+    assert moe.moe_check_device_error(ws) == 0
+    h = to_numpy(inp)
+    qx, sx = omoe.quantize_x(mode, h["x_bf16"])
+    ref = omoe.forward(mode, qx, sx, h["topk_ids"], h["topk_weights"], h["w1"], h["w1_scale"], h["w2"], h["w2_scale"],
+                       num_experts=wl.E, inter=wl.I)
+    assert_close(y_numpy(y), ref, mode)

@@ -156,13 +156,15 @@ def make_inputs(wl: Workload, device="cpu", mode: str | None = None):
     """Generate every input of one forward call for workload ``wl`` on ``device``.
 
     Returns a dict of contiguous tensors: x, x_scale, topk_ids, topk_weights, w1, w1_scale,
-    w2, w2_scale (scales are None where the mode has none)."""
+    w2, w2_scale (scales are None where the mode has none), and x_bf16, the bf16 activations
+    (the input of the path on which the operator quantises x itself)."""
     mode = mode or wl.mode
     T, H, I, E, K = wl.T, wl.H, wl.I, wl.E, wl.K
     g = _gen(wl.seed, device)
     ids, gates = routing(T, E, K, g, device, wl.zipf_s, wl.zipf_empty)
     x = torch.randn((T, H), generator=g, device=device, dtype=torch.float32)
-    out = {"topk_ids": ids, "topk_weights": gates}
+    # the bf16 activations, for the path on which the operator quantises x itself
+    out = {"topk_ids": ids, "topk_weights": gates, "x_bf16": x.to(torch.bfloat16)}
 
     # weights are drawn one expert at a time, which keeps the fp32 staging small at full size
     if mode == "a16w16":
