@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", type=int, default=None, help="override the workload's token count")
     ap.add_argument("--experts", type=int, default=None, help="override the workload's expert count")
+    ap.add_argument("--quantize-x", action="store_true",
+                    help="bf16 x in, quantised by the dispatch stage as the mode prescribes (MOE_FLAG_QUANTIZE_X)")
     return ap.parse_args()
 
 
@@ -56,10 +58,13 @@ def peaks():
     return FALLBACK_PEAKS, "fallback"
 
 
-def workload_config(wl):
-    return {"workload": wl.name, "mode": wl.mode, "tokens": wl.T, "hidden": wl.H, "intermediate": wl.I,
-            "experts": wl.E, "topk": wl.K, "routed_rows": wl.routed_rows, "seed": wl.seed,
-            "l2_policy": "inputs larger than L2 (no flush)"}
+def workload_config(wl, quantize_x=False):
+    cfg = {"workload": wl.name, "mode": wl.mode, "tokens": wl.T, "hidden": wl.H, "intermediate": wl.I,
+           "experts": wl.E, "topk": wl.K, "routed_rows": wl.routed_rows, "seed": wl.seed,
+           "l2_policy": "inputs larger than L2 (no flush)"}
+    if quantize_x:
+        cfg["x_input"] = "bf16, quantised by the dispatch stage"
+    return cfg
 
 
 # ---------------------------------------------------------------------------------------
@@ -81,18 +86,22 @@ def oracle_threads():
     return os.cpu_count() or 1
 
 
-def oracle_sample(wl, inp_host, n_tokens, seed):
+def oracle_sample(wl, inp_host, n_tokens, seed, quantize_x=False):
     """Run the oracle, as it stands, on a seeded sample of n_tokens tokens; returns
-    (seconds, routed rows computed)."""
+    (seconds, routed rows computed). With quantize_x the sampled bf16 rows are quantised by the
+    oracle first (the quantisation is per token, so a sample is exact)."""
     import numpy as np
     from oracle import moe as omoe
     rng = np.random.default_rng(seed)
     tokens = np.sort(rng.choice(wl.T, size=n_tokens, replace=False))
     h = inp_host
-    xs = None if h["x_scale"] is None else h["x_scale"][tokens]
     ids = h["topk_ids"][tokens]
     t0 = time.perf_counter()
-    omoe.forward(wl.mode, h["x"][tokens], xs, ids, h["topk_weights"][tokens], h["w1"], h["w1_scale"], h["w2"],
+    if quantize_x:
+        x, xs = omoe.quantize_x(wl.mode, h["x_bf16"][tokens])
+    else:
+        x, xs = h["x"][tokens], None if h["x_scale"] is None else h["x_scale"][tokens]
+    omoe.forward(wl.mode, x, xs, ids, h["topk_weights"][tokens], h["w1"], h["w1_scale"], h["w2"],
                  h["w2_scale"], num_experts=wl.E, inter=wl.I)
     dt = time.perf_counter() - t0
     return dt, int((ids >= 0).sum())
@@ -116,10 +125,10 @@ def run_reference(args, wl, rank, world):
     h = host_inputs(wl)
     n_tok = cpu_tokens_per_sample(wl)
     for w in range(args.warmup):
-        oracle_sample(wl, h, n_tok, seed=1000 + w)
+        oracle_sample(wl, h, n_tok, seed=1000 + w, quantize_x=args.quantize_x)
     total_t, total_rows = 0.0, 0
     for s in range(args.steps):
-        dt, rows = oracle_sample(wl, h, n_tok, seed=2000 + s)
+        dt, rows = oracle_sample(wl, h, n_tok, seed=2000 + s, quantize_x=args.quantize_x)
         total_t += dt
         total_rows += rows
     flops = 6.0 * wl.H * wl.I * total_rows
@@ -130,7 +139,7 @@ def run_reference(args, wl, rank, world):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(wl), "routed_rows_per_s": total_rows / total_t,
+        "config": workload_config(wl, args.quantize_x), "routed_rows_per_s": total_rows / total_t,
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -311,9 +320,14 @@ def run_gb300(args, wl, rank, world, local_rank):
     ws = moe.alloc_workspace(d, wl.mode, dev)
     y = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=dev)
 
+    flags = args.flags | (moe.MOE_FLAG_QUANTIZE_X if args.quantize_x else 0)
+
     def step(ev_l1=None):
         moe.moe_plan(inp["topk_ids"], d, ws, stream=stream)
-        moe.moe_dispatch(inp["x"], inp["x_scale"], d, wl.mode, ws, stream=stream)
+        if args.quantize_x:
+            moe.moe_dispatch_quantize(inp["x_bf16"], d, wl.mode, ws, stream=stream)
+        else:
+            moe.moe_dispatch(inp["x"], inp["x_scale"], d, wl.mode, ws, stream=stream)
         if ev_l1:
             ev_l1[0].record(stream)
         moe.moe_expert_l1(inp["w1"], inp["w1_scale"], d, wl.mode, ws, args.flags, stream=stream)
@@ -357,8 +371,8 @@ def run_gb300(args, wl, rank, world, local_rank):
     # the output copies run on two more streams with double-buffered device inputs and outputs, so
     # step i+1's input copy and step i-1's y copy overlap step i's compute (events order each
     # buffer's use; one copy stream would queue step i+1's inputs behind step i's y).
-    host_in = {k: inp[k].cpu().pin_memory() for k in ("x", "x_scale", "topk_ids", "topk_weights")
-               if inp[k] is not None}
+    x_keys = ("x_bf16",) if args.quantize_x else ("x", "x_scale")
+    host_in = {k: inp[k].cpu().pin_memory() for k in x_keys + ("topk_ids", "topk_weights") if inp[k] is not None}
     dev_in = [{k: torch.empty_like(v, device=dev) for k, v in host_in.items()} for _ in range(2)]
     y_dev = [y, torch.empty_like(y)]
     y_host = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for _ in range(2)]
@@ -380,8 +394,9 @@ def run_gb300(args, wl, rank, world, local_rank):
         stream.wait_event(in_ready[b])
         stream.wait_event(out_read[b])  # y_dev[b] of two steps back has been copied out
         di = dev_in[b]
-        moe.moe_forward(di["x"], di.get("x_scale"), di["topk_ids"], di["topk_weights"], inp["w1"], inp["w1_scale"],
-                        inp["w2"], inp["w2_scale"], y_dev[b], d, wl.mode, ws, args.flags, stream=stream)
+        moe.moe_forward(di["x_bf16"] if args.quantize_x else di["x"], di.get("x_scale"), di["topk_ids"],
+                        di["topk_weights"], inp["w1"], inp["w1_scale"], inp["w2"], inp["w2_scale"], y_dev[b], d,
+                        wl.mode, ws, flags, stream=stream)
         fwd_done[b].record(stream)
         with torch.cuda.stream(out_stream):
             out_stream.wait_event(fwd_done[b])
@@ -418,7 +433,7 @@ def run_gb300(args, wl, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": DTYPE[wl.mode], "data": "synthetic (seeded; random-init weights)",
-        "config": workload_config(wl),
+        "config": workload_config(wl, args.quantize_x),
         "routed_rows_per_s": world * wl.routed_rows * args.steps / (elapsed_ms * 1e-3),
         "roofline": roof,
         "e2e": {"value": whole_job_tflops(flops, args.steps, e2e_ms, world), "unit": "TFLOP/s",
@@ -454,9 +469,9 @@ def main():
         from workloads import to_numpy
         h = to_numpy(inp)
         # size the sample for about 10 s of oracle time from a 2-token probe
-        dt0, _ = oracle_sample(wl, h, min(2, wl.T), seed=6)
+        dt0, _ = oracle_sample(wl, h, min(2, wl.T), seed=6, quantize_x=args.quantize_x)
         n_tok = int(max(2, min(wl.T, 64, round(2 * 10.0 / max(dt0, 1e-3)))))
-        dt, rows = oracle_sample(wl, h, n_tok, seed=7)
+        dt, rows = oracle_sample(wl, h, n_tok, seed=7, quantize_x=args.quantize_x)
         line["cpu_baseline"] = {"value": 6.0 * wl.H * wl.I * rows / dt / 1e12, "unit": "TFLOP/s",
                                 "cores": oracle_threads(), "kind": "oracle",
                                 "sample": f"{n_tok} seeded tokens ({rows} routed rows) of {wl.name}, "
