@@ -385,3 +385,33 @@ def test_forward_quantizing_x_matches_oracle(moe, mode, wl):
     ref = omoe.forward(mode, qx, sx, h["topk_ids"], h["topk_weights"], h["w1"], h["w1_scale"], h["w2"], h["w2_scale"],
                        num_experts=wl.E, inter=wl.I)
     assert_close(y_numpy(y), ref, mode)
+
+
+@pytest.mark.parametrize("name", ["dsv3_fp8fp4_prefill_zipf", "int8_a8w8", "dsv3_fp8fp4_decode"])
+def test_full_size_quantizing_x_sampled(moe, name):
+    """Full-size workload from bf16 x (the dispatch stage quantises it, as the bench's --quantize-x
+    times it): the pool codes of a seeded sample of tokens are bit-exact against the oracle's
+    quantisation, and their outputs match the oracle within the mode's bound."""
+    wl = WORKLOADS[name]
+    inp = make_inputs(wl, device=DEV)
+    d = moe.dims(wl.T, wl.H, wl.I, wl.E, wl.K)
+    ws = moe.alloc_workspace(d, wl.mode, DEV)
+    y = torch.full((wl.T, wl.H), float("nan"), dtype=torch.bfloat16, device=DEV)
+    moe.moe_forward(inp["x_bf16"], None, inp["topk_ids"], inp["topk_weights"], inp["w1"], inp["w1_scale"], inp["w2"],
+                    inp["w2_scale"], y, d, wl.mode, ws, moe.MOE_FLAG_QUANTIZE_X)
+    assert moe.moe_check_device_error(ws) == 0
+    rng = np.random.default_rng(wl.seed + 100)
+    tokens = np.sort(rng.choice(wl.T, size=6, replace=False))
+    h = to_numpy({k: inp[k] for k in ("x_bf16", "topk_ids", "topk_weights", "w1", "w1_scale", "w2", "w2_scale")})
+    qx, sx = omoe.quantize_x(wl.mode, h["x_bf16"][tokens])
+    # the pool rows of the sampled tokens hold their codes
+    L = moe.moe_workspace_layout(d, wl.mode)
+    slot_row = region(ws, L, "slot_row", torch.int32, wl.T * wl.K).view(wl.T, wl.K).cpu().numpy()
+    codes = region(ws, L, "x_pool", torch.uint8, L["pool_rows"] * wl.H).view(L["pool_rows"], wl.H)
+    for j, t in enumerate(tokens):
+        for k in range(wl.K):
+            assert np.array_equal(codes[int(slot_row[t, k])].cpu().numpy(), qx.view(np.uint8)[j]), (t, k)
+    ref = omoe.forward(wl.mode, qx, sx, h["topk_ids"][tokens], h["topk_weights"][tokens], h["w1"], h["w1_scale"],
+                       h["w2"], h["w2_scale"], num_experts=wl.E, inter=wl.I)
+    assert_close(y_numpy(y)[tokens], ref, wl.mode)
+    assert torch.isfinite(y.float()).all()
