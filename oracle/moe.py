@@ -137,8 +137,14 @@ def silu(z: np.ndarray) -> np.ndarray:
         return z / (1.0 + np.exp(-z))
 
 
-def swiglu(h: np.ndarray, inter: int) -> np.ndarray:
-    """A = SiLU(H[:, :I]) * H[:, I:]; gate is the first half of the columns."""
+def swiglu(h: np.ndarray, inter: int, clamp: float | None = None) -> np.ndarray:
+    """A = SiLU(H[:, :I]) * H[:, I:]; gate is the first half of the columns.
+
+    clamp (p1 parameter activation_clamp, "symmetric clamp threshold for the activation
+    function input"): when given, both halves of H, the input of SwiGLU, are first clipped to
+    [-clamp, clamp]."""
+    if clamp is not None:
+        h = np.clip(h, -clamp, clamp)
     return silu(h[:, :inter]) * h[:, inter:]
 
 
@@ -249,7 +255,8 @@ def _int_matmul_checked(q: np.ndarray, w: np.ndarray) -> np.ndarray:
 
 
 def expert_ffn(mode: str, xe: np.ndarray, sx: np.ndarray | None, w1e: np.ndarray,
-               s_w1e: np.ndarray | None, w2e: np.ndarray, s_w2e: np.ndarray | None, inter: int):
+               s_w1e: np.ndarray | None, w2e: np.ndarray, s_w2e: np.ndarray | None, inter: int,
+               clamp: float | None = None):
     """Y_e for the rows X_e of one expert. Returns (Y float64 [n, H], intermediates).
 
     float modes : H = X_e . W1 (float64), A = SwiGLU(H), A~ = requant(A), Y = A~ . W2.
@@ -262,14 +269,14 @@ def expert_ffn(mode: str, xe: np.ndarray, sx: np.ndarray | None, w1e: np.ndarray
         h32 = (c.astype(np.float32) * s_w1e[None, :].astype(np.float32)).astype(np.float32)
         h32 = (h32 * sx[:, None].astype(np.float32)).astype(np.float32)
         h = h32.astype(np.float64)
-        a = swiglu(h, inter)
+        a = swiglu(h, inter, clamp)
         q, rec = l2_operand(mode, a)
         d = _int_matmul_checked(rec["a"], w2e)
         y32 = (d.astype(np.float32) * s_w2e[None, :].astype(np.float32)).astype(np.float32)
         y32 = (y32 * rec["a_scale"][:, None]).astype(np.float32)
         return y32.astype(np.float64), {"h": h, "c": c, "d": d, **rec}
     h = xe @ w1e
-    a = swiglu(h, inter)
+    a = swiglu(h, inter, clamp)
     a_q, rec = l2_operand(mode, a)
     y = a_q @ w2e
     return y, {"h": h, **rec}
@@ -303,8 +310,9 @@ def combine_rows(contrib: np.ndarray) -> np.ndarray:
 
 
 def forward(mode: str, x, x_scale, topk_ids, topk_weights, w1, w1_scale, w2, w2_scale,
-            num_experts: int, inter: int, return_intermediates: bool = False):
-    """Plan -> per-expert L1 -> SwiGLU -> requant -> L2 -> gate -> combine.
+            num_experts: int, inter: int, return_intermediates: bool = False, clamp: float | None = None):
+    """Plan -> per-expert L1 -> SwiGLU (inputs clipped to [-clamp, clamp] when clamp is given)
+    -> requant -> L2 -> gate -> combine.
 
     Returns y as float64 bf16 values [T, H] (and, on request, the plan and per-row
     intermediates keyed by pool position: 'comb' holds the weighted bf16 rows [T*K, H]).
@@ -329,7 +337,7 @@ def forward(mode: str, x, x_scale, topk_ids, topk_weights, w1, w1_scale, w2, w2_
         w2e = decode_weight(mode, w2, w2_scale, e)
         s1 = None if mode != "a8w8_int8" else np.asarray(w1_scale[e], dtype=np.float32)
         s2 = None if mode != "a8w8_int8" else np.asarray(w2_scale[e], dtype=np.float32)
-        y_e, rec = expert_ffn(mode, xe, sx, w1e, s1, w2e, s2, inter)
+        y_e, rec = expert_ffn(mode, xe, sx, w1e, s1, w2e, s2, inter, clamp)
         comb[src] = weighted_rows(g.reshape(-1)[src], y_e)
         if return_intermediates:
             inter_rec[e] = {"src": src, "y": y_e, **rec}
@@ -341,7 +349,7 @@ def forward(mode: str, x, x_scale, topk_ids, topk_weights, w1, w1_scale, w2, w2_
 
 
 def forward_tokens(mode: str, tokens, x, x_scale, topk_ids, topk_weights, w1, w1_scale, w2,
-                   w2_scale, inter: int):
+                   w2_scale, inter: int, clamp: float | None = None):
     """Brute force for a subset of tokens: for each token i and each slot k, evaluate the FFN
     of expert E[i,k] on x_i alone, weight it and sum. No plan and no permutation is used, so
     this checks the pooled path (every row of an expert is computed independently)."""
@@ -364,7 +372,7 @@ def forward_tokens(mode: str, tokens, x, x_scale, topk_ids, topk_weights, w1, w1
             sx = None if mode != "a8w8_int8" else np.asarray(x_scale, dtype=np.float32)[i:i + 1]
             s1 = None if mode != "a8w8_int8" else np.asarray(w1_scale[e], dtype=np.float32)
             s2 = None if mode != "a8w8_int8" else np.asarray(w2_scale[e], dtype=np.float32)
-            y_e, _ = expert_ffn(mode, xi, sx, w1e, s1, w2e, s2, inter)
+            y_e, _ = expert_ffn(mode, xi, sx, w1e, s1, w2e, s2, inter, clamp)
             contrib.append(weighted_rows(g[i, k:k + 1], y_e)[0])
         out.append(combine_rows(np.stack(contrib)))
     return np.stack(out)

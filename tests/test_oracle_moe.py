@@ -207,3 +207,57 @@ def test_fp8_mode_decoding_uses_block_scales():
     xd2 = moe.decode_x("a8w8_fp8", d["x"], sc)
     assert np.array_equal(xd2[0, 32:64], 2 * xd[0, 32:64])
     assert np.array_equal(xd2[0, :32], xd[0, :32]) and np.array_equal(xd2[1:], xd[1:])
+
+
+# ---------------------------------------------------------------------------------------
+# activation_clamp (p1 parameter: symmetric clamp of the activation function's input)
+# ---------------------------------------------------------------------------------------
+
+
+def _h_range(mode, d, wl):
+    _, rec = _forward(mode, d, wl, return_intermediates=True)
+    hs = np.concatenate([np.abs(r["h"]).ravel() for r in rec["experts"].values()])
+    return hs.min(), hs.max()
+
+
+@pytest.mark.parametrize("mode", list(TINY))
+def test_activation_clamp_limits(mode):
+    """A clamp at or above every |H| changes nothing; a clamp of 0 makes every output 0
+    (SiLU(0) * 0 = 0 in every mode, so every requantised A and every Y is 0)."""
+    wl = TINY[mode]
+    d = _np(make_inputs(wl))
+    y = _forward(mode, d, wl)
+    _, hmax = _h_range(mode, d, wl)
+    assert np.array_equal(_forward(mode, d, wl, clamp=float(hmax)), y)
+    assert np.all(_forward(mode, d, wl, clamp=0.0) == 0.0)
+
+
+@pytest.mark.parametrize("mode", ["a16w16", "a8w8_fp8"])
+def test_activation_clamp_saturates(mode):
+    """With the clamp at the smallest |H| every SwiGLU input sits on the clamp, so doubling W1
+    (which doubles H exactly) leaves the output unchanged; without the clamp it changes."""
+    wl = TINY[mode]
+    d = _np(make_inputs(wl))
+    hmin, _ = _h_range(mode, d, wl)
+    assert hmin > 0
+    d2 = dict(d)
+    if mode == "a16w16":
+        d2["w1"] = codecs.bf16_encode(2.0 * codecs.bf16_decode(d["w1"]))
+    else:  # one more unit of the UE8M0 block exponent doubles every weight exactly
+        d2["w1_scale"] = (d["w1_scale"].astype(np.int32) + 1).astype(np.uint8)
+    c = float(hmin)
+    assert np.array_equal(_forward(mode, d, wl, clamp=c), _forward(mode, d2, wl, clamp=c))
+    assert not np.array_equal(_forward(mode, d, wl), _forward(mode, d2, wl))
+
+
+@pytest.mark.parametrize("mode", list(TINY))
+def test_activation_clamp_brute_force_equals_pooled_path(mode):
+    wl = TINY[mode]
+    d = _np(make_inputs(wl))
+    hmin, hmax = _h_range(mode, d, wl)
+    c = float(0.5 * (hmin + hmax) / 4)
+    y = _forward(mode, d, wl, clamp=c)
+    yb = moe.forward_tokens(mode, range(wl.T), d["x"], d["x_scale"], d["topk_ids"], d["topk_weights"],
+                            d["w1"], d["w1_scale"], d["w2"], d["w2_scale"], inter=wl.I, clamp=c)
+    assert np.array_equal(y, yb)
+    assert not np.array_equal(y, _forward(mode, d, wl))
