@@ -169,6 +169,28 @@ MOE_API moe_status moe_forward(moe_operand x, const int32_t* topk_ids, const flo
                        moe_operand w2, void* y, const moe_dims* d, moe_dtype_mode m, uint32_t flags,
                        void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
+/* Options of the _ex entry points; zero-initialise, then set what is used (a null pointer means
+ * all defaults).
+ *   flags                 MOE_FLAG_* as for moe_forward
+ *   has_activation_clamp  nonzero: clip both inputs of SwiGLU (the gate and the up halves of H)
+ *                         to [-activation_clamp, activation_clamp] before SiLU and the product
+ *                         (Ascend page, parameter activation_clamp); activation_clamp must be
+ *                         >= 0 (else MOE_ERR_INVALID_ARG). */
+typedef struct {
+    uint32_t flags;
+    uint32_t has_activation_clamp;
+    float activation_clamp;
+} moe_options;
+
+/* moe_expert_l1 with options. */
+MOE_API moe_status moe_expert_l1_ex(moe_operand w1, const moe_dims* d, moe_dtype_mode m, const moe_options* opt,
+                            void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/* moe_forward with options. */
+MOE_API moe_status moe_forward_ex(moe_operand x, const int32_t* topk_ids, const float* topk_weights, moe_operand w1,
+                          moe_operand w2, void* y, const moe_dims* d, moe_dtype_mode m, const moe_options* opt,
+                          void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
 /* Synchronises `stream`, returns the first device-side error recorded in the workspace
  * (MOE_OK if none) and clears it. */
 MOE_API moe_status moe_check_device_error(void* workspace, moe_stream_t stream);

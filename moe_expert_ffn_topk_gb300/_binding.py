@@ -22,12 +22,18 @@ MOE_FLAG_NONE, MOE_FLAG_SIMT, MOE_FLAG_WEIGHT_MAJOR, MOE_FLAG_QUANTIZE_X = 0, 1,
 
 ABI_FUNCTIONS = ("moe_workspace_bytes", "moe_plan", "moe_dispatch", "moe_expert_l1", "moe_expert_l2",
                  "moe_combine", "moe_forward", "moe_check_device_error", "moe_status_string",
-                 "moe_workspace_layout", "moe_debug_bounded_wait", "moe_plan_noalloc", "moe_dispatch_quantize")
+                 "moe_workspace_layout", "moe_debug_bounded_wait", "moe_plan_noalloc", "moe_dispatch_quantize",
+                 "moe_expert_l1_ex", "moe_forward_ex")
 
 
 class MoeDims(ctypes.Structure):
     _fields_ = [("num_tokens", ctypes.c_int32), ("hidden", ctypes.c_int32), ("intermediate", ctypes.c_int32),
                 ("num_experts", ctypes.c_int32), ("topk", ctypes.c_int32)]
+
+
+class MoeOptions(ctypes.Structure):
+    _fields_ = [("flags", ctypes.c_uint32), ("has_activation_clamp", ctypes.c_uint32),
+                ("activation_clamp", ctypes.c_float)]
 
 
 class MoeOperand(ctypes.Structure):
@@ -68,6 +74,9 @@ def _load():
         "moe_debug_bounded_wait": (st, [vp, sz, ctypes.c_uint64, vp]),
         "moe_plan_noalloc": (st, [vp, dims_p, vp, vp, vp, vp]),
         "moe_dispatch_quantize": (st, [vp, dims_p, st, vp, sz, vp]),
+        "moe_expert_l1_ex": (st, [MoeOperand, dims_p, st, ctypes.POINTER(MoeOptions), vp, sz, vp]),
+        "moe_forward_ex": (st, [MoeOperand, vp, vp, MoeOperand, MoeOperand, vp, dims_p, st, ctypes.POINTER(MoeOptions),
+                                vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -183,6 +192,30 @@ def moe_forward(x, x_scale, topk_ids, topk_weights, w1, w1_scale, w2, w2_scale, 
     _check(LIB.moe_forward(_operand(x, x_scale, "x"), _ptr(topk_ids, "topk_ids"), _ptr(topk_weights, "topk_weights"),
                            _operand(w1, w1_scale, "w1"), _operand(w2, w2_scale, "w2"), _ptr(y, "y"),
                            ctypes.byref(d), _mode(mode), flags, ws, nb, _stream(stream)), "moe_forward")
+
+
+def _options(flags, activation_clamp):
+    return MoeOptions(int(flags), 0 if activation_clamp is None else 1,
+                      0.0 if activation_clamp is None else float(activation_clamp))
+
+
+def moe_expert_l1_ex(w1, w1_scale, d: MoeDims, mode, workspace, flags=0, activation_clamp=None, stream=None):
+    """moe_expert_l1 with options (activation_clamp: None or >= 0)."""
+    ws, nb = _ws(workspace)
+    opt = _options(flags, activation_clamp)
+    _check(LIB.moe_expert_l1_ex(_operand(w1, w1_scale, "w1"), ctypes.byref(d), _mode(mode), ctypes.byref(opt), ws, nb,
+                                _stream(stream)), "moe_expert_l1_ex")
+
+
+def moe_forward_ex(x, x_scale, topk_ids, topk_weights, w1, w1_scale, w2, w2_scale, y, d: MoeDims, mode, workspace,
+                   flags=0, activation_clamp=None, stream=None):
+    """moe_forward with options (activation_clamp: None or >= 0)."""
+    ws, nb = _ws(workspace)
+    opt = _options(flags, activation_clamp)
+    _check(LIB.moe_forward_ex(_operand(x, x_scale, "x"), _ptr(topk_ids, "topk_ids"), _ptr(topk_weights, "topk_weights"),
+                              _operand(w1, w1_scale, "w1"), _operand(w2, w2_scale, "w2"), _ptr(y, "y"),
+                              ctypes.byref(d), _mode(mode), ctypes.byref(opt), ws, nb, _stream(stream)),
+           "moe_forward_ex")
 
 
 def moe_check_device_error(workspace, stream=None) -> int:

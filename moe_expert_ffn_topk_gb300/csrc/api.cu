@@ -2,6 +2,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstring>
 
 #include "internal.h"
@@ -92,6 +93,7 @@ moe_status make_plan_view(const moe_dims* d, moe_dtype_mode m, void* ws, size_t 
     const size_t need = pools ? L.total : L.x_pool;  // x_pool starts where the mode-free part ends
     if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255) || ws_bytes < need) return MOE_ERR_WORKSPACE;
     uint8_t* b = static_cast<uint8_t*>(ws);
+    p->act_clamp = INFINITY;
     p->T = d->num_tokens;
     p->H = d->hidden;
     p->I = d->intermediate;
@@ -171,11 +173,31 @@ moe_status moe_dispatch_quantize(const void* x_bf16, const moe_dims* d, moe_dtyp
     return from_cuda(launch_dispatch_quant(p, x_bf16, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+static moe_status expert_l1(moe_operand w1, const moe_dims* d, moe_dtype_mode m, uint32_t flags, float clamp,
+                            void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
 moe_status moe_expert_l1(moe_operand w1, const moe_dims* d, moe_dtype_mode m, uint32_t flags, void* workspace,
                          size_t workspace_bytes, moe_stream_t stream) {
+    return expert_l1(w1, d, m, flags, INFINITY, workspace, workspace_bytes, stream);
+}
+
+// the options of the _ex entry points: flags, and the activation clamp applied through the plan
+static moe_status read_options(const moe_options* opt, uint32_t* flags, float* clamp) {
+    *flags = opt ? opt->flags : 0u;
+    *clamp = INFINITY;
+    if (opt && opt->has_activation_clamp) {
+        if (!(opt->activation_clamp >= 0.0f)) return MOE_ERR_INVALID_ARG;  // also rejects NaN
+        *clamp = opt->activation_clamp;
+    }
+    return MOE_OK;
+}
+
+static moe_status expert_l1(moe_operand w1, const moe_dims* d, moe_dtype_mode m, uint32_t flags, float clamp,
+                            void* workspace, size_t workspace_bytes, moe_stream_t stream) {
     Plan p;
     moe_status st = make_plan_view(d, m, workspace, workspace_bytes, &p, true);
     if (st != MOE_OK) return st;
+    p.act_clamp = clamp;
     if (!operand_ok(w1, m != MOE_A16W16)) return MOE_ERR_INVALID_ARG;
     if (d->num_tokens == 0) return MOE_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -191,6 +213,15 @@ moe_status moe_expert_l1(moe_operand w1, const moe_dims* d, moe_dtype_mode m, ui
     }
     if (e == cudaSuccess && m == MOE_A8W8_INT8) e = launch_int8_row_quant(p, s);
     return from_cuda(e);
+}
+
+moe_status moe_expert_l1_ex(moe_operand w1, const moe_dims* d, moe_dtype_mode m, const moe_options* opt,
+                            void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+    uint32_t flags;
+    float clamp;
+    const moe_status st = read_options(opt, &flags, &clamp);
+    if (st != MOE_OK) return st;
+    return expert_l1(w1, d, m, flags, clamp, workspace, workspace_bytes, stream);
 }
 
 moe_status moe_expert_l2(moe_operand w2, const float* topk_weights, const moe_dims* d, moe_dtype_mode m,
@@ -220,9 +251,9 @@ moe_status moe_combine(void* y, const moe_dims* d, void* workspace, size_t works
     return from_cuda(launch_combine(p, static_cast<uint16_t*>(y), reinterpret_cast<cudaStream_t>(stream)));
 }
 
-moe_status moe_forward(moe_operand x, const int32_t* topk_ids, const float* topk_weights, moe_operand w1,
-                       moe_operand w2, void* y, const moe_dims* d, moe_dtype_mode m, uint32_t flags,
-                       void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+static moe_status forward(moe_operand x, const int32_t* topk_ids, const float* topk_weights, moe_operand w1,
+                          moe_operand w2, void* y, const moe_dims* d, moe_dtype_mode m, uint32_t flags, float clamp,
+                          void* workspace, size_t workspace_bytes, moe_stream_t stream) {
     Plan p;
     moe_status st = make_plan_view(d, m, workspace, workspace_bytes, &p, true);
     if (st != MOE_OK) return st;
@@ -236,9 +267,25 @@ moe_status moe_forward(moe_operand x, const int32_t* topk_ids, const float* topk
     st = quantize_x ? moe_dispatch_quantize(x.data, d, m, workspace, workspace_bytes, stream)
                     : moe_dispatch(x, d, m, workspace, workspace_bytes, stream);
     if (st != MOE_OK) return st;
-    if ((st = moe_expert_l1(w1, d, m, flags, workspace, workspace_bytes, stream)) != MOE_OK) return st;
+    if ((st = expert_l1(w1, d, m, flags, clamp, workspace, workspace_bytes, stream)) != MOE_OK) return st;
     if ((st = moe_expert_l2(w2, topk_weights, d, m, flags, workspace, workspace_bytes, stream)) != MOE_OK) return st;
     return moe_combine(y, d, workspace, workspace_bytes, stream);
+}
+
+moe_status moe_forward(moe_operand x, const int32_t* topk_ids, const float* topk_weights, moe_operand w1,
+                       moe_operand w2, void* y, const moe_dims* d, moe_dtype_mode m, uint32_t flags,
+                       void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+    return forward(x, topk_ids, topk_weights, w1, w2, y, d, m, flags, INFINITY, workspace, workspace_bytes, stream);
+}
+
+moe_status moe_forward_ex(moe_operand x, const int32_t* topk_ids, const float* topk_weights, moe_operand w1,
+                          moe_operand w2, void* y, const moe_dims* d, moe_dtype_mode m, const moe_options* opt,
+                          void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+    uint32_t flags;
+    float clamp;
+    const moe_status st = read_options(opt, &flags, &clamp);
+    if (st != MOE_OK) return st;
+    return forward(x, topk_ids, topk_weights, w1, w2, y, d, m, flags, clamp, workspace, workspace_bytes, stream);
 }
 
 moe_status moe_check_device_error(void* workspace, moe_stream_t stream) {

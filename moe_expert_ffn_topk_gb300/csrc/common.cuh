@@ -4,6 +4,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
+
+#include <cmath>
 #include <stdint.h>
 
 #include "internal.h"
@@ -88,6 +90,16 @@ __device__ __forceinline__ float exp2_neg_int(int e) {
 // the bf16 / e4m3 rounding that follows, and branch-free; for z < -87 the quotient is -0)
 __device__ __forceinline__ float silu(float z) {
     return __fdividef(z, 1.0f + __expf(-z));
+}
+
+// SwiGLU on one (gate, up) pair with the operator's activation_clamp (Ascend page, parameter
+// activation_clamp: both inputs clipped to [-c, c]; c = +inf leaves them as they are). A select,
+// not a branch, so epilogue loops stay branch-free.
+__device__ __forceinline__ float swiglu1(float g, float u, float c) {
+    const bool on = c < INFINITY;
+    g = on ? fminf(fmaxf(g, -c), c) : g;
+    u = on ? fminf(fmaxf(u, -c), c) : u;
+    return silu(g) * u;
 }
 
 }  // namespace moe

@@ -39,6 +39,7 @@ struct Plan {
     uint16_t* x_planes;    // INT8: f16 [2][pool_rows, H] (hi, lo planes of the codes)
     uint16_t* a_planes;    // INT8: f16 [2][pool_rows, I]
     uint16_t* comb;        // bf16 [T*K, H]
+    float act_clamp;       // SwiGLU inputs clipped to [-act_clamp, act_clamp]; +inf: no clamp
 };
 
 // x / A storage properties per mode

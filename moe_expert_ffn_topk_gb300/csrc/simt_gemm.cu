@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(NT) l1_simt_kernel(Plan p, const uint8_t* __re
         }
         float a[2];
 #pragma unroll
-        for (int c = 0; c < 2; ++c) a[c] = silu(g[c]) * u[c];
+        for (int c = 0; c < 2; ++c) a[c] = swiglu1(g[c], u[c], p.act_clamp);
         if constexpr (MODE == MOE_A16W16) {
             uint16_t* ap = reinterpret_cast<uint16_t*>(p.a_pool);
             ap[row * I + j0] = float_to_bf16_bits(a[0]);

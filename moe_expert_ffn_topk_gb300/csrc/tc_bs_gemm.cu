@@ -465,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int tt = 0; tt < 16; ++tt) {
                             const float gv = gate ? __uint_as_float(v[tt]) : xg[tt * kHalf + jl];
                             const float uv = gate ? xu[tt * kHalf + jl] : __uint_as_float(v[16 + tt]);
-                            const float av = silu(gv) * uv;
+                            const float av = swiglu1(gv, uv, p.act_clamp);
                             const float amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(av))));
                             const int ex = mx_exponent_e4m3(amax);
                             st_global_u8_if(true, p.a_pool + (row0 + tt) * I + j, float_to_e4m3_satfinite(av * exp2_neg_int(ex)));

@@ -141,13 +141,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
         : "memory");
 }
 
-// predicated 16-byte global store (no memory clobber: independent loads may move across it)
-__device__ __forceinline__ void st_global_v4_if(bool pred, void* ptr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %0, 0;\n\t@p st.global.v4.b32 [%1], {%2, %3, %4, %5};\n\t}" ::"r"(
-                     (int)pred),
-                 "l"(ptr), "r"(a), "r"(b), "r"(c), "r"(d));
-}
-
 // two floats -> two e4m3 codes (RN, saturating), the first in the low byte
 __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
     uint16_t pair;
@@ -404,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float amax = 0.0f;
 #pragma unroll
                     for (int jj = 0; jj < 32; ++jj) {
-                        av[jj] = silu(__uint_as_float(g[jj])) * __uint_as_float(u[jj]);
+                        av[jj] = swiglu1(__uint_as_float(g[jj]), __uint_as_float(u[jj]), p.act_clamp);
                         amax = fmaxf(amax, fabsf(av[jj]));
                     }
                     const int ex = mx_exponent_e4m3(amax);

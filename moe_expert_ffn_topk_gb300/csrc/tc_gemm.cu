@@ -262,8 +262,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t packed[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        const float a0 = silu(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]);
-                        const float a1 = silu(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]);
+                        const float a0 = swiglu1(__uint_as_float(g[2 * j]), __uint_as_float(u[2 * j]), p.act_clamp);
+                        const float a1 = swiglu1(__uint_as_float(g[2 * j + 1]), __uint_as_float(u[2 * j + 1]), p.act_clamp);
                         packed[j] = (uint32_t)float_to_bf16_bits(a0) | ((uint32_t)float_to_bf16_bits(a1) << 16);
                     }
                     st_global_v8_if(true, out + c * 32, packed);

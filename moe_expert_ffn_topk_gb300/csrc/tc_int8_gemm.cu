@@ -352,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float sx = __shfl_sync(0xffffffffu, sx_l[ci], tt);
                         const float Hg = __fmul_rn(__fmul_rn(hg[tt], sg), sx);
                         const float Hu = __fmul_rn(__fmul_rn(__int2float_rn(exact_int(hi[tt], lo[tt])), su), sx);
-                        p.a_f32[(int64_t)(tl.row0 + c0 + tt) * I + j] = silu(Hg) * Hu;
+                        p.a_f32[(int64_t)(tl.row0 + c0 + tt) * I + j] = swiglu1(Hg, Hu, p.act_clamp);
                     }
                 }
             } else {

@@ -415,3 +415,50 @@ def test_full_size_quantizing_x_sampled(moe, name):
                        h["w2"], h["w2_scale"], num_experts=wl.E, inter=wl.I)
     assert_close(y_numpy(y)[tokens], ref, wl.mode)
     assert torch.isfinite(y.float()).all()
+
+
+CLAMP_CASES = [(m, w) for m, w in ALL if w.name in ("tiny_bf16", "ragged_bf16", "ragged_fp8", "ragged_int8", "ragged_fp4",
+                                                     "skew_fp4", "n224_fp4")]
+
+
+@pytest.mark.parametrize("mode,wl", CLAMP_CASES, ids=[f"{m}-{w.name}" for m, w in CLAMP_CASES])
+@pytest.mark.parametrize("flags", [0, 1, 2], ids=["default", "simt", "weight_major"])
+def test_activation_clamp_matches_oracle(moe, mode, wl, flags):
+    """moe_forward_ex with activation_clamp: every L1 kernel clips both SwiGLU inputs; the clamp,
+    set near the median |H| (an fp32 value), changes the output and the oracle bounds it."""
+    inp = make_inputs(wl, device=DEV)
+    h = to_numpy(inp)
+    _, rec = omoe.forward(mode, h["x"], h["x_scale"], h["topk_ids"], h["topk_weights"], h["w1"], h["w1_scale"],
+                          h["w2"], h["w2_scale"], num_experts=wl.E, inter=wl.I, return_intermediates=True)
+    hs = np.concatenate([np.abs(r["h"]).ravel() for r in rec["experts"].values()])
+    c = float(np.float32(np.median(hs)))
+    d = moe.dims(wl.T, wl.H, wl.I, wl.E, wl.K)
+    ws = moe.alloc_workspace(d, wl.mode, DEV)
+    y = torch.full((wl.T, wl.H), float("nan"), dtype=torch.bfloat16, device=DEV)
+    moe.moe_forward_ex(inp["x"], inp["x_scale"], inp["topk_ids"], inp["topk_weights"], inp["w1"], inp["w1_scale"],
+                       inp["w2"], inp["w2_scale"], y, d, wl.mode, ws, flags=flags, activation_clamp=c)
+    assert moe.moe_check_device_error(ws) == 0
+    ref = omoe.forward(mode, h["x"], h["x_scale"], h["topk_ids"], h["topk_weights"], h["w1"], h["w1_scale"], h["w2"],
+                       h["w2_scale"], num_experts=wl.E, inter=wl.I, clamp=c)
+    assert_close(y_numpy(y), ref, mode)
+    unclamped = oracle_forward(wl, inp)
+    assert np.abs(ref - unclamped).max() > 10 * TOL[mode] * np.abs(unclamped).max()
+
+
+def test_activation_clamp_rejects_bad_values(moe):
+    wl = WORKLOADS["tiny_bf16"]
+    inp = make_inputs(wl, device=DEV)
+    d = moe.dims(wl.T, wl.H, wl.I, wl.E, wl.K)
+    ws = moe.alloc_workspace(d, wl.mode, DEV)
+    y = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=DEV)
+    for bad in (-1.0, float("nan")):
+        with pytest.raises(moe.MoeError):
+            moe.moe_forward_ex(inp["x"], None, inp["topk_ids"], inp["topk_weights"], inp["w1"], None, inp["w2"], None,
+                               y, d, wl.mode, ws, activation_clamp=bad)
+    # no clamp through the options path is the plain forward, bit for bit
+    y0 = torch.empty_like(y)
+    moe.moe_forward(inp["x"], None, inp["topk_ids"], inp["topk_weights"], inp["w1"], None, inp["w2"], None, y0, d,
+                    wl.mode, ws)
+    moe.moe_forward_ex(inp["x"], None, inp["topk_ids"], inp["topk_weights"], inp["w1"], None, inp["w2"], None, y, d,
+                       wl.mode, ws)
+    assert torch.equal(y.view(torch.int16), y0.view(torch.int16))
