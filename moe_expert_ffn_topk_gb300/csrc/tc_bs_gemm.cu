@@ -2,8 +2,8 @@
 // A8W4: e2m1 weights; e4m3 tokens in both), on tcgen05.mma kind::mxf8f6f4.block_scale: the
 // tensor core consumes the stored codes and applies one UE8M0 scale per 32 elements of K to
 // each operand, so nothing is dequantised in software (the Ascend mega_moe page, A8W8-FP use
-// case: "DQ_MX ... implicitly performed inside matmul"; DeepGEMM page §4 step 5: block-scaled
-// MMA with UE8M0 scale factors in tensor memory).
+// case: the MX dequantisation happens within the matrix multiply; DeepGEMM page §4 step 5:
+// block-scaled MMA with UE8M0 scale factors in tensor memory).
 //
 // Tiles (M = 128 weight rows, N = tokens, K = 128 or 256 per stage, MMAs of K = 32):
 // - L1: the 128 rows are 64 gate rows and the 64 up rows of the same 64 outputs of A, so the

@@ -1,8 +1,8 @@
 // Token-major block-scaled grouped GEMM for the FP8 modes at prefill sizes (A8W8-FP8: e4m3
 // weights, A8W4: e2m1 weights; e4m3 tokens), on tcgen05.mma kind::mxf8f6f4.block_scale with
 // one UE8M0 scale per 32 elements of K applied by the tensor core (the Ascend mega_moe page,
-// A8W8-FP use case, "DQ_MX ... implicitly performed inside matmul"; DeepGEMM page, section 4,
-// step 5: block-scaled MMA with UE8M0 scale factors in tensor memory).
+// A8W8-FP use case: the MX dequantisation happens within the matrix multiply; DeepGEMM page,
+// section 4, step 5: block-scaled MMA with UE8M0 scale factors in tensor memory).
 //
 // Tile: M = 128 pool rows (one 128-row route tile of an expert) x N weight rows, K = 128 per
 // stage (MMAs of K = 32):

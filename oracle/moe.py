@@ -140,9 +140,9 @@ def silu(z: np.ndarray) -> np.ndarray:
 def swiglu(h: np.ndarray, inter: int, clamp: float | None = None) -> np.ndarray:
     """A = SiLU(H[:, :I]) * H[:, I:]; gate is the first half of the columns.
 
-    clamp (p1 parameter activation_clamp, "symmetric clamp threshold for the activation
-    function input"): when given, both halves of H, the input of SwiGLU, are first clipped to
-    [-clamp, clamp]."""
+    clamp (p1 parameter activation_clamp: a threshold t >= 0 that limits the input of the
+    activation function to [-t, t], symmetrically): when given, both halves of H, the input of
+    SwiGLU, are first clipped to [-clamp, clamp]."""
     if clamp is not None:
         h = np.clip(h, -clamp, clamp)
     return silu(h[:, :inter]) * h[:, inter:]
