@@ -149,6 +149,16 @@ def e2m1_unpack_decode(packed: np.ndarray) -> np.ndarray:
     return out
 
 
+def int4_unpack(packed: np.ndarray) -> np.ndarray:
+    """Packed bytes [..., K/2] of signed 4-bit integers (two's complement nibbles, element 2j in
+    the low nibble of byte j) -> int8 values [..., K] in [-8, 7]."""
+    p = np.asarray(packed, dtype=np.uint8)
+    nib = np.empty(p.shape[:-1] + (p.shape[-1] * 2,), dtype=np.int16)
+    nib[..., 0::2] = p & 0xF
+    nib[..., 1::2] = p >> 4
+    return np.where(nib >= 8, nib - 16, nib).astype(np.int8)
+
+
 # ---------------------------------------------------------------------------------------
 # UE8M0 scale byte
 # ---------------------------------------------------------------------------------------

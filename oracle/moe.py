@@ -33,7 +33,8 @@ import numpy as np
 
 from . import codecs
 
-MODES = ("a16w16", "a8w8_fp8", "a8w8_int8", "a8w4_fp8_fp4")
+MODES = ("a16w16", "a8w8_fp8", "a8w8_int8", "a8w4_fp8_fp4", "a8w4_int")
+INT_MODES = ("a8w8_int8", "a8w4_int")  # integer GEMMs with per-token / per-channel fp32 scales
 
 
 # ---------------------------------------------------------------------------------------
@@ -87,6 +88,7 @@ def decode_x(mode: str, x: np.ndarray, x_scale: np.ndarray | None) -> np.ndarray
     a8w8_int8    : x int8 codes q_i; x_scale fp32 [T] = s^X_i. Returns the integer codes;
                    the int8 path keeps q and s^X apart (p1 A8W8-INT).
     a8w4_fp8_fp4 : x e4m3 codes, x_scale fp32 [T, H/128] (1x128 blocks).
+    a8w4_int     : as a8w8_int8 (p1 A8W4-INT: the same per-token int8 quantisation of X).
     """
     if mode == "a16w16":
         return codecs.bf16_decode(x)
@@ -94,7 +96,7 @@ def decode_x(mode: str, x: np.ndarray, x_scale: np.ndarray | None) -> np.ndarray
         v = codecs.e4m3_decode(x)
         s = np.repeat(codecs.ue8m0_decode(x_scale), 32, axis=-1)
         return v * s
-    if mode == "a8w8_int8":
+    if mode in INT_MODES:
         return np.asarray(x, dtype=np.int8).astype(np.float64)
     if mode == "a8w4_fp8_fp4":
         v = codecs.e4m3_decode(x)
@@ -112,6 +114,8 @@ def decode_weight(mode: str, w: np.ndarray, w_scale: np.ndarray | None, e: int) 
     a8w8_int8    : w int8 [E, N_out, K_in]; returns the integer codes (the per-output-channel
                    fp32 scale is applied after the integer GEMM).
     a8w4_fp8_fp4 : w e2m1 packed [E, N_out, K_in/2] with UE8M0 scales [E, N_out, K_in/32].
+    a8w4_int     : w signed int4 packed [E, N_out, K_in/2] (element 2j in the low nibble);
+                   returns the integer codes (per-output-channel fp32 scale as for a8w8_int8).
     """
     if mode == "a16w16":
         return codecs.bf16_decode(w[e])
@@ -120,6 +124,8 @@ def decode_weight(mode: str, w: np.ndarray, w_scale: np.ndarray | None, e: int) 
         return v.T
     if mode == "a8w8_int8":
         return np.asarray(w[e], dtype=np.int8).astype(np.float64).T
+    if mode == "a8w4_int":
+        return codecs.int4_unpack(w[e]).astype(np.float64).T
     if mode == "a8w4_fp8_fp4":
         v = codecs.e2m1_unpack_decode(w[e]) * np.repeat(codecs.ue8m0_decode(w_scale[e]), 32, axis=-1)
         return v.T
@@ -214,7 +220,7 @@ def quantize_x(mode: str, x_bf16: np.ndarray):
     if mode == "a16w16":
         return x, None
     xv = codecs.bf16_decode(x)
-    if mode == "a8w8_int8":
+    if mode in INT_MODES:
         return quant_int8_rows(xv)
     if mode == "a8w8_fp8":
         return quant_mx_fp8(xv, 32)
@@ -233,7 +239,7 @@ def l2_operand(mode: str, a: np.ndarray):
         codes, sc = quant_mx_fp8(a)
         v = codecs.e4m3_decode(codes) * np.repeat(codecs.ue8m0_decode(sc), 32, axis=1)
         return v, {"a": codes, "a_scale": sc}
-    if mode == "a8w8_int8":
+    if mode in INT_MODES:
         q, s = quant_int8_rows(a)
         return q.astype(np.float64), {"a": q, "a_scale": s}
     raise ValueError(mode)
@@ -254,6 +260,25 @@ def _int_matmul_checked(q: np.ndarray, w: np.ndarray) -> np.ndarray:
     return c
 
 
+def msd_int_matmul(q: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """The A8W4-INT product of p1 ("A8W4-INT Quantization Use Case", Expert Compute): the int8
+    activations are split into a signed high nibble q_hi = floor(q / 16) and an offset low
+    nibble q_lo = (q & 0x0F) - 8, each multiplied by the int4 weights, and recombined as
+    16 * (q_hi . W) + (q_lo . W) + bias with the compensation bias = 8 * (1^T . W) that the page
+    defines (computed offline there and passed to the operator). All in int64; the page applies
+    the weight scale before this combination, which in exact arithmetic is the same as applying
+    it to the combined integer, as done by the caller. Equals q . W exactly."""
+    q = q.astype(np.int64)
+    hi = np.floor_divide(q, 16)
+    lo = np.bitwise_and(q, 0x0F) - 8
+    wi = w.astype(np.int64)
+    bias = 8 * wi.sum(axis=0)
+    c = 16 * (hi @ wi) + (lo @ wi) + bias[None, :]
+    if c.size and (c.min() < INT32_MIN or c.max() > INT32_MAX):
+        raise OverflowError("int8 x int4 GEMM accumulator outside int32")
+    return c
+
+
 def expert_ffn(mode: str, xe: np.ndarray, sx: np.ndarray | None, w1e: np.ndarray,
                s_w1e: np.ndarray | None, w2e: np.ndarray, s_w2e: np.ndarray | None, inter: int,
                clamp: float | None = None):
@@ -263,15 +288,17 @@ def expert_ffn(mode: str, xe: np.ndarray, sx: np.ndarray | None, w1e: np.ndarray
     a8w8_int8   : C = Q_e . W1 (int32), H = (C * s^W1) * s^X in fp32 (p1 Linear1),
                   A = SwiGLU(H), (A^int8, s^A) = requant(A),
                   D = A^int8 . W2 (int32), Y = (D * s^W2) * s^A in fp32 (p1 Linear2).
+    a8w4_int    : the same with int4 weights, C and D by the MSD decomposition (msd_int_matmul).
     """
-    if mode == "a8w8_int8":
-        c = _int_matmul_checked(xe, w1e)
+    if mode in INT_MODES:
+        mm = _int_matmul_checked if mode == "a8w8_int8" else msd_int_matmul
+        c = mm(xe, w1e)
         h32 = (c.astype(np.float32) * s_w1e[None, :].astype(np.float32)).astype(np.float32)
         h32 = (h32 * sx[:, None].astype(np.float32)).astype(np.float32)
         h = h32.astype(np.float64)
         a = swiglu(h, inter, clamp)
         q, rec = l2_operand(mode, a)
-        d = _int_matmul_checked(rec["a"], w2e)
+        d = mm(rec["a"], w2e)
         y32 = (d.astype(np.float32) * s_w2e[None, :].astype(np.float32)).astype(np.float32)
         y32 = (y32 * rec["a_scale"][:, None]).astype(np.float32)
         return y32.astype(np.float64), {"h": h, "c": c, "d": d, **rec}
@@ -332,11 +359,11 @@ def forward(mode: str, x, x_scale, topk_ids, topk_weights, w1, w1_scale, w2, w2_
         src = row_src[lo:hi]
         tok = src // K
         xe = xd[tok]
-        sx = None if mode != "a8w8_int8" else np.asarray(x_scale, dtype=np.float32)[tok]
+        sx = None if mode not in INT_MODES else np.asarray(x_scale, dtype=np.float32)[tok]
         w1e = decode_weight(mode, w1, w1_scale, e)
         w2e = decode_weight(mode, w2, w2_scale, e)
-        s1 = None if mode != "a8w8_int8" else np.asarray(w1_scale[e], dtype=np.float32)
-        s2 = None if mode != "a8w8_int8" else np.asarray(w2_scale[e], dtype=np.float32)
+        s1 = None if mode not in INT_MODES else np.asarray(w1_scale[e], dtype=np.float32)
+        s2 = None if mode not in INT_MODES else np.asarray(w2_scale[e], dtype=np.float32)
         y_e, rec = expert_ffn(mode, xe, sx, w1e, s1, w2e, s2, inter, clamp)
         comb[src] = weighted_rows(g.reshape(-1)[src], y_e)
         if return_intermediates:
@@ -369,9 +396,9 @@ def forward_tokens(mode: str, tokens, x, x_scale, topk_ids, topk_weights, w1, w1
             if e not in decoded:
                 decoded[e] = (decode_weight(mode, w1, w1_scale, e), decode_weight(mode, w2, w2_scale, e))
             w1e, w2e = decoded[e]
-            sx = None if mode != "a8w8_int8" else np.asarray(x_scale, dtype=np.float32)[i:i + 1]
-            s1 = None if mode != "a8w8_int8" else np.asarray(w1_scale[e], dtype=np.float32)
-            s2 = None if mode != "a8w8_int8" else np.asarray(w2_scale[e], dtype=np.float32)
+            sx = None if mode not in INT_MODES else np.asarray(x_scale, dtype=np.float32)[i:i + 1]
+            s1 = None if mode not in INT_MODES else np.asarray(w1_scale[e], dtype=np.float32)
+            s2 = None if mode not in INT_MODES else np.asarray(w2_scale[e], dtype=np.float32)
             y_e, _ = expert_ffn(mode, xi, sx, w1e, s1, w2e, s2, inter, clamp)
             contrib.append(weighted_rows(g[i, k:k + 1], y_e)[0])
         out.append(combine_rows(np.stack(contrib)))

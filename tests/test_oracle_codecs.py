@@ -184,6 +184,27 @@ def test_quantize_x_a16w16_is_the_input():
     assert sc is None and np.array_equal(xx, x)
 
 
+def test_int4_pack_round_trip_exhaustive():
+    v0, v1 = np.meshgrid(np.arange(-8, 8), np.arange(-8, 8), indexing="ij")
+    packed = ((v0.ravel() & 0xF) | ((v1.ravel() & 0xF) << 4)).astype(np.uint8)[:, None]
+    out = codecs.int4_unpack(packed)
+    assert np.array_equal(out[:, 0], v0.ravel()) and np.array_equal(out[:, 1], v1.ravel())
+    assert len(np.unique(packed)) == 256
+
+
+def test_msd_split_equals_the_integer_product():
+    """The A8W4-INT decomposition (high nibble, offset low nibble, compensation bias) gives
+    q . W exactly, also at the int8 extremes."""
+    rng = np.random.default_rng(21)
+    q = rng.integers(-127, 128, size=(17, 96)).astype(np.int8)
+    q[0] = 127
+    q[1] = -127
+    q[2, ::2] = -128 + 1
+    w = rng.integers(-8, 8, size=(96, 40)).astype(np.int8)
+    ref = q.astype(np.int64) @ w.astype(np.int64)
+    assert np.array_equal(moe.msd_int_matmul(q, w), ref)
+
+
 def test_int32_accumulator_guard():
     q = np.full((1, 200000), 127, dtype=np.int8)
     w = np.full((200000, 1), 127, dtype=np.int8)

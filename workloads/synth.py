@@ -63,6 +63,8 @@ WORKLOADS = {
     "dsv3_fp8fp4_prefill_zipf": Workload("dsv3_fp8fp4_prefill_zipf", "a8w4_fp8_fp4", 8192, 7168, 2048, 256, 8,
                                          3, 0.02, zipf_s=1.2, zipf_empty=16),
     "int8_a8w8": Workload("int8_a8w8", "a8w8_int8", 2048, 5120, 1536, 64, 6, 4, 0.02),
+    # the A8W8-INT shapes with int4 weights (the A8W4-INT use case)
+    "int4_a8w4": Workload("int4_a8w4", "a8w4_int", 2048, 5120, 1536, 64, 6, 5, 0.02),
 }
 
 
@@ -147,6 +149,17 @@ def int8_per_row(v: torch.Tensor):
     return q.contiguous(), s.float().contiguous()
 
 
+def int4_per_row_packed(v: torch.Tensor):
+    """Symmetric per-row int4: s = max|v|/7 (floored at 1e-8), q = round(v/s) in [-7, 7], packed
+    two per byte (element 2j in the low nibble, two's complement). Returns (packed uint8 [..., n/2],
+    s float32 [...])."""
+    vf = v.float()
+    s = (vf.abs().amax(dim=-1) / 7.0).clamp(min=1e-8)
+    q = torch.round(vf / s[..., None]).clamp(-7, 7).to(torch.int16) & 0xF
+    packed = (q[..., 0::2] | (q[..., 1::2] << 4)).to(torch.uint8)
+    return packed.contiguous(), s.float().contiguous()
+
+
 # ---------------------------------------------------------------------------------------
 # A complete set of inputs
 # ---------------------------------------------------------------------------------------
@@ -196,6 +209,15 @@ def make_inputs(wl: Workload, device="cpu", mode: str | None = None):
                 w = (torch.randn((n_out, k_in), generator=g, device=device) * wl.w_std).to(torch.bfloat16)
                 q[e], sc[e] = int8_per_row(w)  # per output channel: amax over the input dim
             out[name], out[name + "_scale"] = q, sc
+    elif mode == "a8w4_int":
+        out["x"], out["x_scale"] = int8_per_row(x.to(torch.bfloat16))
+        for name, (n_out, k_in) in (("w1", (2 * I, H)), ("w2", (H, I))):
+            packed = torch.empty((E, n_out, k_in // 2), device=device, dtype=torch.uint8)
+            sc = torch.empty((E, n_out), device=device, dtype=torch.float32)
+            for e in range(E):
+                w = (torch.randn((n_out, k_in), generator=g, device=device) * wl.w_std).to(torch.bfloat16)
+                packed[e], sc[e] = int4_per_row_packed(w)  # per output channel: amax over the input dim
+            out[name], out[name + "_scale"] = packed, sc
     elif mode == "a8w4_fp8_fp4":
         xc, xe = to_e4m3_blocks(x, 128)
         out["x"] = xc
