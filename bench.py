@@ -30,8 +30,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "fused MoE FFN TFLOP/s + routed rows/s, % of tensor/HBM roofline, 1xGB300"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-DTYPE = {"a16w16": "bf16", "a8w8_fp8": "e4m3", "a8w8_int8": "int8", "a8w4_fp8_fp4": "e4m3xe2m1"}
-LAUNCHES_PER_STEP = {"a16w16": 7, "a8w8_fp8": 7, "a8w8_int8": 8, "a8w4_fp8_fp4": 7}
+DTYPE = {"a16w16": "bf16", "a8w8_fp8": "e4m3", "a8w8_int8": "int8", "a8w4_fp8_fp4": "e4m3xe2m1", "a8w4_int": "int8xint4"}
+LAUNCHES_PER_STEP = {"a16w16": 7, "a8w8_fp8": 7, "a8w8_int8": 8, "a8w4_fp8_fp4": 7, "a8w4_int": 8}
 
 
 def parse():
@@ -264,8 +264,10 @@ def whole_job_tflops(flops_per_step: float, steps: int, elapsed_ms: float, world
     return world * flops_per_step * steps / (elapsed_ms * 1e-3) / 1e12
 
 
-WEIGHT_BYTES_PER_ELEM = {"a16w16": 2.0, "a8w8_fp8": 1.0 + 1 / 32, "a8w8_int8": 1.0, "a8w4_fp8_fp4": 0.5 + 1 / 32}
-X_BYTES_PER_ELEM = {"a16w16": 2.0, "a8w8_fp8": 1.0 + 1 / 32, "a8w8_int8": 1.0, "a8w4_fp8_fp4": 1.0 + 4 / 128}
+WEIGHT_BYTES_PER_ELEM = {"a16w16": 2.0, "a8w8_fp8": 1.0 + 1 / 32, "a8w8_int8": 1.0, "a8w4_fp8_fp4": 0.5 + 1 / 32,
+                         "a8w4_int": 0.5}
+X_BYTES_PER_ELEM = {"a16w16": 2.0, "a8w8_fp8": 1.0 + 1 / 32, "a8w8_int8": 1.0, "a8w4_fp8_fp4": 1.0 + 4 / 128,
+                    "a8w4_int": 1.0}
 
 
 def is_decode(wl) -> bool:

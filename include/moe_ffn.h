@@ -57,7 +57,7 @@ typedef enum {
     MOE_ERR_WORKSPACE = 6      /* workspace missing, misaligned or too small            */
 } moe_status;
 
-/* Storage formats of the four use cases (Ascend mega_moe page, "Use Case / A / W" table;
+/* Storage formats of the five use cases (Ascend mega_moe page, "Use Case / A / W" table;
  * DeepGEMM page §1 for FP8 x FP4). T tokens, H hidden, I intermediate, E experts.
  *
  * MOE_A16W16        x bf16 [T,H]; w1 bf16 [E,H,2I]; w2 bf16 [E,I,H] (the page's math
@@ -70,13 +70,20 @@ typedef enum {
  * MOE_A8W4_FP8_FP4  x e4m3 [T,H] + fp32 [T,H/128] power-of-two block scales; w1 e2m1
  *                   [E,2I,H/2] + UE8M0 [E,2I,H/32]; w2 e2m1 [E,H,I/2] + UE8M0 [E,H,I/32];
  *                   two e2m1 codes per byte, element 2j in the low nibble.
+ * MOE_A8W4_INT      x as MOE_A8W8_INT8; w1 signed int4 [E,2I,H/2] + fp32 [E,2I]; w2 signed
+ *                   int4 [E,H,I/2] + fp32 [E,H] per output channel; two's-complement codes in
+ *                   [-8,7], two per byte, element 2j in the low nibble. The page's INT4 x INT4
+ *                   MSD split of the activations and its offline bias 8 * (1^T W) are one way
+ *                   to reach the exact integer product Q . W; the library computes that product
+ *                   directly, so no bias input exists (the page's A8W4-INT use case).
  * In every mode the gate columns of w1 are the first I outputs and the up columns the
  * last I; y is bf16 [T,H]. */
 typedef enum {
     MOE_A16W16 = 0,
     MOE_A8W8_FP8 = 1,
     MOE_A8W8_INT8 = 2,
-    MOE_A8W4_FP8_FP4 = 3
+    MOE_A8W4_FP8_FP4 = 3,
+    MOE_A8W4_INT = 4
 } moe_dtype_mode;
 
 typedef struct {
@@ -130,7 +137,7 @@ MOE_API moe_status moe_dispatch(moe_operand x, const moe_dims* d, moe_dtype_mode
                         size_t workspace_bytes, moe_stream_t stream);
 
 /* Stage S2 from bf16 activations, with the operator's own quantisation before dispatch (Ascend
- * page: parameter dispatch_quant_mode; A8W8-INT use case "EP Dispatch": per token
+ * page: parameter dispatch_quant_mode; A8W8-INT and A8W4-INT use cases "EP Dispatch": per token
  * s_i = max|X[i,:]|/127, q_i = round(X[i,:]/s_i), scale floored at 1e-8; A8W8-FP use case, first
  * phase: Q_MX with groups of 32, e4m3 codes and E8M0 scales). For A8W4_FP8_FP4 the same
  * shared-exponent rule on groups of 128 gives e4m3 codes with fp32 power-of-two scales (the
@@ -145,7 +152,8 @@ MOE_API moe_status moe_dispatch_quantize(const void* x_bf16, const moe_dims* d, 
  * (Ascend page: "Linear1 Projection", "SwiGLU Activation", and the A8W8 activation
  * quantisation of "Linear2"; DeepGEMM page §4 step 6). Needs moe_dispatch first.
  *   w1  device operand in the mode's w1 format. Writes the L2 operand A into the workspace:
- *       bf16 (A16W16), e4m3 + UE8M0 per 1x32 (both FP8 modes), int8 + fp32 per row (INT8). */
+ *       bf16 (A16W16), e4m3 + UE8M0 per 1x32 (both FP8 modes), int8 + fp32 per row (INT8,
+ *       A8W4-INT). */
 MOE_API moe_status moe_expert_l1(moe_operand w1, const moe_dims* d, moe_dtype_mode m, uint32_t flags,
                          void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
@@ -214,10 +222,16 @@ typedef struct {
     size_t x_pool_scale;  /* gathered x scales [pool_rows, *] */
     size_t a_pool;        /* L2 operand codes [pool_rows, I] */
     size_t a_pool_scale;  /* L2 operand scales [pool_rows, *] */
-    size_t a_f32;         /* fp32 A [pool_rows, I] (INT8 mode: before the per-row quantisation) */
+    size_t a_f32;         /* fp32 A [pool_rows, I] (integer modes: before the per-row quantisation) */
     size_t x_pool_planes; /* INT8 mode: the gathered x codes as two f16 planes [2][pool_rows, H],
-                             hi = floor(q/16) and lo = q mod 16 (other modes: size 0) */
-    size_t a_pool_planes; /* INT8 mode: the re-quantised A as two f16 planes (hi, lo) [2][pool_rows, I] */
+                             hi = floor(q/16) and lo = q mod 16; A8W4-INT: one plane, the codes
+                             as f16 [pool_rows, H] (other modes: size 0) */
+    size_t a_pool_planes; /* the re-quantised A likewise: [2][pool_rows, I] (INT8), [pool_rows, I]
+                             (A8W4-INT). A8W4-INT stores each group of 8 consecutive codes
+                             q0..q7 in the order q0 q4 q1 q5 q2 q6 q3 q7 (the order its weight
+                             expansion produces) */
+    size_t pool_sums;     /* A8W4-INT: int32 [2][pool_rows], the sum of each pool row's codes:
+                             x rows, then A rows (other modes: size 0) */
     size_t comb;          /* bf16 [T*K, H] weighted rows */
     size_t total;         /* = moe_workspace_bytes() */
     int64_t pool_rows;    /* rows reserved in each pool */

@@ -15,7 +15,8 @@ int x_elem_bytes(int mode) { return mode == MOE_A16W16 ? 2 : 1; }
 int64_t x_scale_row_bytes(int mode, int H) {
     switch (mode) {
         case MOE_A8W8_FP8: return H / 32;                // UE8M0 per 1x32
-        case MOE_A8W8_INT8: return 4;                    // fp32 per token
+        case MOE_A8W8_INT8:
+        case MOE_A8W4_INT: return 4;                     // fp32 per token
         case MOE_A8W4_FP8_FP4: return (int64_t)(H / 128) * 4;  // fp32 per 1x128
         default: return 0;
     }
@@ -27,14 +28,15 @@ int64_t a_scale_row_bytes(int mode, int I) {
     switch (mode) {
         case MOE_A8W8_FP8:
         case MOE_A8W4_FP8_FP4: return I / 32;            // UE8M0 per 1x32
-        case MOE_A8W8_INT8: return 4;                    // fp32 per row
+        case MOE_A8W8_INT8:
+        case MOE_A8W4_INT: return 4;                     // fp32 per row
         default: return 0;
     }
 }
 
 static bool dims_ok(const moe_dims* d, moe_dtype_mode m) {
     if (!d) return false;
-    if (m < MOE_A16W16 || m > MOE_A8W4_FP8_FP4) return false;
+    if (m < MOE_A16W16 || m > MOE_A8W4_INT) return false;
     if (d->num_tokens < 0 || d->topk < 1 || d->topk > 32) return false;
     if (d->num_experts < d->topk || d->num_experts > 1024) return false;
     if (d->hidden < 128 || d->hidden % 128 || d->intermediate < 128 || d->intermediate % 128) return false;
@@ -76,10 +78,11 @@ moe_status layout(const moe_dims* d, moe_dtype_mode m, moe_workspace_layout_t* o
     L.x_pool_scale = take((size_t)pool_rows * x_scale_row_bytes(m, (int)H));
     L.a_pool = take((size_t)pool_rows * I * a_elem_bytes(m));
     L.a_pool_scale = take((size_t)pool_rows * a_scale_row_bytes(m, (int)I));
-    L.a_f32 = take(m == MOE_A8W8_INT8 ? (size_t)pool_rows * I * 4 : 0);
-    const int planes = m == MOE_A8W8_INT8 ? 2 : 0;  // the INT8 tensor-core path's hi / lo operand planes
+    L.a_f32 = take(int_mode(m) ? (size_t)pool_rows * I * 4 : 0);
+    const int planes = int_planes(m);  // the integer tensor-core path's f16 operand planes
     L.x_pool_planes = take((size_t)planes * pool_rows * H * 2);
     L.a_pool_planes = take((size_t)planes * pool_rows * I * 2);
+    L.pool_sums = take(m == MOE_A8W4_INT ? (size_t)2 * pool_rows * 4 : 0);
     L.total = off;
     L.pool_rows = pool_rows;
     *out = L;
@@ -118,6 +121,8 @@ moe_status make_plan_view(const moe_dims* d, moe_dtype_mode m, void* ws, size_t 
     p->a_f32 = reinterpret_cast<float*>(b + L.a_f32);
     p->x_planes = reinterpret_cast<uint16_t*>(b + L.x_pool_planes);
     p->a_planes = reinterpret_cast<uint16_t*>(b + L.a_pool_planes);
+    p->x_sums = reinterpret_cast<int32_t*>(b + L.pool_sums);
+    p->a_sums = p->x_sums + L.pool_rows;
     p->comb = reinterpret_cast<uint16_t*>(b + L.comb);
     return MOE_OK;
 }
@@ -208,10 +213,12 @@ static moe_status expert_l1(moe_operand w1, const moe_dims* d, moe_dtype_mode m,
         e = launch_l1_bs(p, w1.data, w1.scale, (flags & MOE_FLAG_WEIGHT_MAJOR) != 0, s);
     } else if (!(flags & MOE_FLAG_SIMT) && int8_tc_supported(p, 1)) {
         e = launch_l1_int8_tc(p, w1.data, w1.scale, s);
+    } else if (!(flags & MOE_FLAG_SIMT) && w4_tc_supported(p, 1)) {
+        e = launch_l1_w4_tc(p, w1.data, w1.scale, s);
     } else {
         e = launch_l1_simt(p, w1.data, w1.scale, s);
     }
-    if (e == cudaSuccess && m == MOE_A8W8_INT8) e = launch_int8_row_quant(p, s);
+    if (e == cudaSuccess && int_mode(m)) e = launch_int8_row_quant(p, s);
     return from_cuda(e);
 }
 
@@ -239,6 +246,8 @@ moe_status moe_expert_l2(moe_operand w2, const float* topk_weights, const moe_di
         return from_cuda(launch_l2_bs(p, w2.data, w2.scale, topk_weights, (flags & MOE_FLAG_WEIGHT_MAJOR) != 0, s));
     if (!(flags & MOE_FLAG_SIMT) && int8_tc_supported(p, 2))
         return from_cuda(launch_l2_int8_tc(p, w2.data, w2.scale, topk_weights, s));
+    if (!(flags & MOE_FLAG_SIMT) && w4_tc_supported(p, 2))
+        return from_cuda(launch_l2_w4_tc(p, w2.data, w2.scale, topk_weights, s));
     return from_cuda(launch_l2_simt(p, w2.data, w2.scale, topk_weights, s));
 }
 

@@ -16,6 +16,12 @@ constexpr int kHdrPadRows = 2;
 constexpr int kHdrTiles = 3;
 constexpr int kHdrWaitFlag = 8;         // a flag that nothing sets (bounded-wait test hook)
 
+// The integer modes (int8 activations, fp32 per-token / per-channel scales) and the number of
+// f16 operand planes their tensor-core GEMMs read: the int8 codes as hi = floor(q/16) and
+// lo = q mod 16 with int8 weights, the codes themselves with int4 weights.
+__host__ __device__ constexpr bool int_mode(int m) { return m == MOE_A8W8_INT8 || m == MOE_A8W4_INT; }
+__host__ __device__ constexpr int int_planes(int m) { return m == MOE_A8W8_INT8 ? 2 : m == MOE_A8W4_INT ? 1 : 0; }
+
 // Device view of the workspace for one (dims, mode).
 struct Plan {
     int T, H, I, E, K;
@@ -35,9 +41,11 @@ struct Plan {
     uint8_t* x_pool_scale;
     uint8_t* a_pool;       // [pool_rows, I * a elem bytes]
     uint8_t* a_pool_scale;
-    float* a_f32;          // [pool_rows, I] (INT8 mode)
-    uint16_t* x_planes;    // INT8: f16 [2][pool_rows, H] (hi, lo planes of the codes)
-    uint16_t* a_planes;    // INT8: f16 [2][pool_rows, I]
+    float* a_f32;          // [pool_rows, I] (integer modes)
+    uint16_t* x_planes;    // integer modes: f16 [int_planes][pool_rows, H] (INT8: hi, lo of the codes)
+    uint16_t* a_planes;    // integer modes: f16 [int_planes][pool_rows, I]
+    int32_t* x_sums;       // A8W4-INT: sum of each x pool row's codes [pool_rows]
+    int32_t* a_sums;       // A8W4-INT: sum of each A pool row's codes [pool_rows]
     uint16_t* comb;        // bf16 [T*K, H]
     float act_clamp;       // SwiGLU inputs clipped to [-act_clamp, act_clamp]; +inf: no clamp
 };
@@ -70,12 +78,22 @@ cudaError_t launch_l2_tc(const Plan& p, const void* w2, const void* w2_scale, co
                          cudaStream_t s);
 bool tc_supported(const Plan& p, int stage);
 
-// Tensor-core path of the INT8 mode (weights converted to f16 in shared memory, tokens split
-// into exact hi/lo f16 planes).
+// Tensor-core path of the integer modes (int8 or int4 weights converted to f16 in shared
+// memory, the tokens' f16 planes; every partial sum an exact integer).
 cudaError_t launch_l1_int8_tc(const Plan& p, const void* w1, const void* w1_scale, cudaStream_t s);
 cudaError_t launch_l2_int8_tc(const Plan& p, const void* w2, const void* w2_scale, const float* topk_weights,
                               cudaStream_t s);
 bool int8_tc_supported(const Plan& p, int stage);
+
+// Token-major tensor-core path of A8W4-INT (int4 weights expanded to f16 in shared memory).
+cudaError_t launch_l1_w4_tc(const Plan& p, const void* w1, const void* w1_scale, cudaStream_t s);
+cudaError_t launch_l2_w4_tc(const Plan& p, const void* w2, const void* w2_scale, const float* topk_weights,
+                            cudaStream_t s);
+bool w4_tc_supported(const Plan& p, int stage);
+
+// Position of code k of a row in the A8W4-INT f16 operand planes: within each group of 8, code
+// i < 4 goes to position 2i and code 4 + i to position 2i + 1.
+__host__ __device__ constexpr int w4_plane_pos(int k) { return (k & ~7) | ((k & 3) << 1) | ((k >> 2) & 1); }
 
 // Block-scaled tensor-core path of the FP8 modes (kind::mxf8f6f4.block_scale): weight-major
 // tiles for decode-sized experts, token-major tiles for prefill-sized ones (weight-major when

@@ -175,7 +175,9 @@ __global__ void __launch_bounds__(128) dispatch_gather_kernel(const uint4* __res
 // S2 for the quantised modes: copies the codes and scale rows like dispatch_gather_kernel. For
 // the INT8 mode it also writes the codes as two f16 planes, hi = floor(q/16) and lo = q mod 16
 // (q = 16*hi + lo, both exact in f16), the operand of the INT8 tensor-core GEMM: with them every
-// fp32 partial sum of that GEMM stays an exactly representable integer.
+// fp32 partial sum of that GEMM stays an exactly representable integer. For A8W4-INT the plane
+// is the codes themselves as f16 (int8 x int4 products are small enough without the split), in
+// the order of w4_plane_pos, and the row's code sum goes to `sums`.
 // Each thread keeps four 16-byte loads in flight before its stores, and the next row's source
 // index is read while the current row is copied (a row costs two dependent loads otherwise).
 template <int MODE>
@@ -183,8 +185,10 @@ __global__ void __launch_bounds__(128) dispatch_gather_q_kernel(const uint8_t* _
                                                                 const int32_t* __restrict__ pool_src,
                                                                 const int32_t* __restrict__ hdr, int K, int H,
                                                                 int scale_bytes, int64_t pool_rows, uint8_t* __restrict__ xp,
-                                                                uint8_t* __restrict__ xps, uint16_t* __restrict__ xb) {
+                                                                uint8_t* __restrict__ xps, uint16_t* __restrict__ xb,
+                                                                int32_t* __restrict__ sums) {
     constexpr int kUnroll = 4;
+    __shared__ int red[4];
     const int rows = hdr[kHdrPadRows];
     const int nv = H / 16;                 // 16-byte vectors of a row of codes
     const int scale_words = scale_bytes / 4;
@@ -197,6 +201,7 @@ __global__ void __launch_bounds__(128) dispatch_gather_q_kernel(const uint8_t* _
             const int64_t tok = src / K;
             const uint4* xs4 = reinterpret_cast<const uint4*>(x + tok * H);
             uint4* xd = reinterpret_cast<uint4*>(xp + (int64_t)r * H);
+            int row_sum = 0;  // A8W4-INT
             for (int v0 = threadIdx.x; v0 < nv; v0 += kUnroll * blockDim.x) {
                 uint4 c[kUnroll];
 #pragma unroll
@@ -209,7 +214,22 @@ __global__ void __launch_bounds__(128) dispatch_gather_q_kernel(const uint8_t* _
                     const int v = v0 + u * blockDim.x;
                     if (v >= nv) break;
                     xd[v] = c[u];
-                    if constexpr (MODE == MOE_A8W8_INT8) {
+                    if constexpr (MODE == MOE_A8W4_INT) {
+                        const uint8_t* b = reinterpret_cast<const uint8_t*>(&c[u]);
+                        uint32_t f[8];  // word 4g + j: codes 8g + j and 8g + 4 + j
+#pragma unroll
+                        for (int g = 0; g < 2; ++g)
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const int q0 = (int8_t)b[8 * g + j], q1 = (int8_t)b[8 * g + 4 + j];
+                                f[4 * g + j] = (uint32_t)float_to_f16_bits((float)q0) |
+                                               ((uint32_t)float_to_f16_bits((float)q1) << 16);
+                                row_sum += q0 + q1;
+                            }
+                        uint4* d = reinterpret_cast<uint4*>(xb + (int64_t)r * H + v * 16);
+                        d[0] = make_uint4(f[0], f[1], f[2], f[3]);
+                        d[1] = make_uint4(f[4], f[5], f[6], f[7]);
+                    } else if constexpr (MODE == MOE_A8W8_INT8) {
                         const uint8_t* b = reinterpret_cast<const uint8_t*>(&c[u]);
                         uint32_t hi[8], lo[8];
 #pragma unroll
@@ -232,14 +252,22 @@ __global__ void __launch_bounds__(128) dispatch_gather_q_kernel(const uint8_t* _
             for (int w = threadIdx.x; w < scale_words; w += blockDim.x)
                 reinterpret_cast<uint32_t*>(xps + (int64_t)r * scale_bytes)[w] =
                     __ldg(reinterpret_cast<const uint32_t*>(xs + tok * scale_bytes) + w);
+            if constexpr (MODE == MOE_A8W4_INT) {  // src >= 0 is uniform across the block
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1) row_sum += __shfl_xor_sync(0xffffffffu, row_sum, o);
+                if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = row_sum;
+                __syncthreads();
+                if (threadIdx.x == 0) sums[r] = red[0] + red[1] + red[2] + red[3];
+                __syncthreads();
+            }
         }
         r = rn;
         src = src_next;
     }
 }
 
-// S2 with the operator's own activation quantisation (Ascend page, A8W8-INT use case "EP
-// Dispatch": per token s = max|X[i,:]|/127, q = round(X/s); A8W8-FP use case: Q_MX with groups
+// S2 with the operator's own activation quantisation (Ascend page, A8W8-INT and A8W4-INT use
+// cases "EP Dispatch": per token s = max|X[i,:]|/127, q = round(X/s); A8W8-FP use case: Q_MX with groups
 // of 32 and E8M0 scales; FP8 activations x FP4 weights: the same shared-exponent rule on groups
 // of 128, fp32 power-of-two scales, the mode's x format). One CTA per token: its bf16 row is
 // quantised once and written to each of its K pool rows. Warp w takes 128-element chunks, 4
@@ -248,15 +276,17 @@ __global__ void __launch_bounds__(128) dispatch_gather_q_kernel(const uint8_t* _
 template <int MODE>
 __global__ void __launch_bounds__(256) dispatch_quant_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ slot_row,
                                                              int T, int K, int H, int64_t pool_rows, uint8_t* __restrict__ xp,
-                                                             uint8_t* __restrict__ xps, uint16_t* __restrict__ xb) {
+                                                             uint8_t* __restrict__ xps, uint16_t* __restrict__ xb,
+                                                             int32_t* __restrict__ sums) {
     __shared__ float red[8];
+    __shared__ int red_sum[8];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int t = blockIdx.x; t < T; t += gridDim.x) {
         // pool row of slot `lane` (K <= 32), shuffled to all lanes when the chunk is stored
         const int my_row = lane < K ? __ldg(slot_row + (int64_t)t * K + lane) : -1;
         const uint2* xr = reinterpret_cast<const uint2*>(x + (int64_t)t * H);  // 4 bf16 per uint2
         float s_int8 = 0.0f;
-        if constexpr (MODE == MOE_A8W8_INT8) {
+        if constexpr (int_mode(MODE)) {
             float m = 0.0f;
             for (int c = threadIdx.x; c < H / 4; c += blockDim.x) {
                 const uint2 v = __ldg(xr + c);
@@ -273,21 +303,36 @@ __global__ void __launch_bounds__(256) dispatch_quant_kernel(const uint16_t* __r
             __syncthreads();
             s_int8 = fmaxf(__fdiv_rn(amax, 127.0f), 1e-8f);
         }
+        int code_sum = 0;  // A8W4-INT
         for (int c0 = warp * 128; c0 < H; c0 += 8 * 128) {
             const uint2 v = __ldg(xr + c0 / 4 + lane);
             const float f[4] = {bf16_bits_to_float(v.x & 0xffff), bf16_bits_to_float(v.x >> 16),
                                 bf16_bits_to_float(v.y & 0xffff), bf16_bits_to_float(v.y >> 16)};
             uint32_t code = 0, hi[2] = {0, 0}, lo[2] = {0, 0};
             int ex = 0;  // FP8 modes: exponent of this lane's group
-            if constexpr (MODE == MOE_A8W8_INT8) {
+            if constexpr (int_mode(MODE)) {
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     float q = rintf(__fdiv_rn(f[c], s_int8));
                     q = fminf(fmaxf(q, -127.0f), 127.0f);
                     const int qi = (int)q;
                     code |= (uint32_t)(qi & 0xff) << (8 * c);
-                    hi[c >> 1] |= (uint32_t)float_to_f16_bits((float)(qi >> 4)) << (16 * (c & 1));
-                    lo[c >> 1] |= (uint32_t)float_to_f16_bits((float)(qi & 15)) << (16 * (c & 1));
+                    if constexpr (MODE == MOE_A8W8_INT8) {
+                        hi[c >> 1] |= (uint32_t)float_to_f16_bits((float)(qi >> 4)) << (16 * (c & 1));
+                        lo[c >> 1] |= (uint32_t)float_to_f16_bits((float)(qi & 15)) << (16 * (c & 1));
+                    } else {  // A8W4-INT: the codes as one f16 plane (order below)
+                        hi[c >> 1] |= (uint32_t)float_to_f16_bits((float)qi) << (16 * (c & 1));
+                        code_sum += qi;
+                    }
+                }
+                if constexpr (MODE == MOE_A8W4_INT) {
+                    // codes 0-3 of a group of 8 are in an even lane, 4-7 in the next one; the plane
+                    // holds q0 q4 q1 q5 (even lane) and q2 q6 q3 q7 (odd lane)
+                    const bool odd = lane & 1;
+                    const uint32_t got = __shfl_xor_sync(0xffffffffu, odd ? hi[0] : hi[1], 1);
+                    const uint32_t mine = odd ? hi[1] : hi[0];
+                    hi[0] = odd ? (got & 0xffffu) | (mine << 16) : (mine & 0xffffu) | (got << 16);
+                    hi[1] = odd ? (got >> 16) | (mine & 0xffff0000u) : (mine >> 16) | (got & 0xffff0000u);
                 }
             } else {
                 float m = fmaxf(fmaxf(fabsf(f[0]), fabsf(f[1])), fmaxf(fabsf(f[2]), fabsf(f[3])));
@@ -307,6 +352,8 @@ __global__ void __launch_bounds__(256) dispatch_quant_kernel(const uint16_t* __r
                 if constexpr (MODE == MOE_A8W8_INT8) {
                     reinterpret_cast<uint2*>(xb + (int64_t)prow * H + c0)[lane] = make_uint2(hi[0], hi[1]);
                     reinterpret_cast<uint2*>(xb + (pool_rows + prow) * H + c0)[lane] = make_uint2(lo[0], lo[1]);
+                } else if constexpr (MODE == MOE_A8W4_INT) {
+                    reinterpret_cast<uint2*>(xb + (int64_t)prow * H + c0)[lane] = make_uint2(hi[0], hi[1]);
                 } else if constexpr (MODE == MOE_A8W8_FP8) {
                     if ((lane & 7) == 0) xps[(int64_t)prow * (H / 32) + c0 / 32 + lane / 8] = (uint8_t)(ex + 127);
                 } else {
@@ -315,10 +362,23 @@ __global__ void __launch_bounds__(256) dispatch_quant_kernel(const uint16_t* __r
                 }
             }
         }
-        if constexpr (MODE == MOE_A8W8_INT8) {
+        if constexpr (MODE == MOE_A8W4_INT) {
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) code_sum += __shfl_xor_sync(0xffffffffu, code_sum, o);
+            if (lane == 0) red_sum[warp] = code_sum;
+            __syncthreads();
+            code_sum = 0;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) code_sum += red_sum[w];
+            __syncthreads();
+        }
+        if constexpr (int_mode(MODE)) {
             if (threadIdx.x < K) {
                 const int prow = my_row;
-                if (prow >= 0) reinterpret_cast<float*>(xps)[prow] = s_int8;
+                if (prow >= 0) {
+                    reinterpret_cast<float*>(xps)[prow] = s_int8;
+                    if constexpr (MODE == MOE_A8W4_INT) sums[prow] = code_sum;
+                }
             }
         }
     }
@@ -396,7 +456,7 @@ static cudaError_t dispatch_q(const Plan& p, const void* x, const void* x_scale,
     dispatch_gather_q_kernel<MODE><<<grid, 128, 0, s>>>(static_cast<const uint8_t*>(x),
                                                         static_cast<const uint8_t*>(x_scale), p.pool_src, p.hdr, p.K,
                                                         p.H, (int)x_scale_row_bytes(MODE, p.H), p.pool_rows, p.x_pool,
-                                                        p.x_pool_scale, p.x_planes);
+                                                        p.x_pool_scale, p.x_planes, p.x_sums);
     return cudaGetLastError();
 }
 
@@ -405,6 +465,7 @@ cudaError_t launch_dispatch(const Plan& p, const void* x, const void* x_scale, c
     switch (p.mode) {
         case MOE_A8W8_FP8: return dispatch_q<MOE_A8W8_FP8>(p, x, x_scale, s);
         case MOE_A8W8_INT8: return dispatch_q<MOE_A8W8_INT8>(p, x, x_scale, s);
+        case MOE_A8W4_INT: return dispatch_q<MOE_A8W4_INT>(p, x, x_scale, s);
         case MOE_A8W4_FP8_FP4: return dispatch_q<MOE_A8W4_FP8_FP4>(p, x, x_scale, s);
         default: break;
     }
@@ -425,15 +486,19 @@ cudaError_t launch_dispatch_quant(const Plan& p, const void* x_bf16, cudaStream_
     switch (p.mode) {
         case MOE_A8W8_FP8:
             dispatch_quant_kernel<MOE_A8W8_FP8><<<grid, 256, 0, s>>>(x, p.slot_row, p.T, p.K, p.H, p.pool_rows, p.x_pool,
-                                                                     p.x_pool_scale, p.x_planes);
+                                                                     p.x_pool_scale, p.x_planes, p.x_sums);
             break;
         case MOE_A8W8_INT8:
             dispatch_quant_kernel<MOE_A8W8_INT8><<<grid, 256, 0, s>>>(x, p.slot_row, p.T, p.K, p.H, p.pool_rows, p.x_pool,
-                                                                      p.x_pool_scale, p.x_planes);
+                                                                      p.x_pool_scale, p.x_planes, p.x_sums);
+            break;
+        case MOE_A8W4_INT:
+            dispatch_quant_kernel<MOE_A8W4_INT><<<grid, 256, 0, s>>>(x, p.slot_row, p.T, p.K, p.H, p.pool_rows, p.x_pool,
+                                                                     p.x_pool_scale, p.x_planes, p.x_sums);
             break;
         case MOE_A8W4_FP8_FP4:
             dispatch_quant_kernel<MOE_A8W4_FP8_FP4><<<grid, 256, 0, s>>>(x, p.slot_row, p.T, p.K, p.H, p.pool_rows,
-                                                                         p.x_pool, p.x_pool_scale, p.x_planes);
+                                                                         p.x_pool, p.x_pool_scale, p.x_planes, p.x_sums);
             break;
         default:  // A16W16: x is already the pool's format
             return launch_dispatch(p, x_bf16, nullptr, s);

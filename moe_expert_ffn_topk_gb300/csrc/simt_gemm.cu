@@ -38,7 +38,7 @@ __device__ __forceinline__ int expert_of_row(const int32_t* pad_off, int E, int 
 }
 
 template <int MODE>
-using acc_t = typename std::conditional<MODE == MOE_A8W8_INT8, int, float>::type;
+using acc_t = typename std::conditional<int_mode(MODE), int, float>::type;
 
 // Element k of pool row p of the L1 operand (gathered x).
 template <int MODE>
@@ -47,7 +47,7 @@ __device__ __forceinline__ acc_t<MODE> load_x(const uint8_t* xp, const uint8_t* 
         return bf16_bits_to_float(reinterpret_cast<const uint16_t*>(xp)[p * H + k]);
     } else if constexpr (MODE == MOE_A8W8_FP8) {
         return e4m3_to_float(xp[p * H + k]) * ue8m0_to_float(xs[p * (H / 32) + k / 32]);
-    } else if constexpr (MODE == MOE_A8W8_INT8) {
+    } else if constexpr (int_mode(MODE)) {
         return static_cast<int>(reinterpret_cast<const int8_t*>(xp)[p * H + k]);
     } else {
         return e4m3_to_float(xp[p * H + k]) * reinterpret_cast<const float*>(xs)[p * (H / 128) + k / 128];
@@ -66,6 +66,10 @@ __device__ __forceinline__ acc_t<MODE> load_w(const uint8_t* w, const uint8_t* w
         return e4m3_to_float(w[en * Kin + k]) * ue8m0_to_float(ws[en * (Kin / 32) + k / 32]);
     } else if constexpr (MODE == MOE_A8W8_INT8) {
         return static_cast<int>(reinterpret_cast<const int8_t*>(w)[en * Kin + k]);
+    } else if constexpr (MODE == MOE_A8W4_INT) {
+        const uint8_t b = w[en * (Kin / 2) + k / 2];
+        const int n = (k & 1) ? (b >> 4) : (b & 0xF);
+        return n >= 8 ? n - 16 : n;  // two's-complement nibble
     } else {
         const uint8_t b = w[en * (Kin / 2) + k / 2];
         return e2m1_to_float((k & 1) ? (b >> 4) : (b & 0xF)) * ue8m0_to_float(ws[en * (Kin / 32) + k / 32]);
@@ -77,7 +81,7 @@ template <int MODE>
 __device__ __forceinline__ acc_t<MODE> load_a(const uint8_t* ap, const uint8_t* as, int I, int64_t p, int j) {
     if constexpr (MODE == MOE_A16W16) {
         return bf16_bits_to_float(reinterpret_cast<const uint16_t*>(ap)[p * I + j]);
-    } else if constexpr (MODE == MOE_A8W8_INT8) {
+    } else if constexpr (int_mode(MODE)) {
         return static_cast<int>(reinterpret_cast<const int8_t*>(ap)[p * I + j]);
     } else {
         return e4m3_to_float(ap[p * I + j]) * ue8m0_to_float(as[p * (I / 32) + j / 32]);
@@ -132,7 +136,7 @@ __global__ void __launch_bounds__(NT) l1_simt_kernel(Plan p, const uint8_t* __re
         const int64_t row = r0 + ty * 4 + i;
         const int j0 = jb * 32 + tx * 2;
         float g[2], u[2];
-        if constexpr (MODE == MOE_A8W8_INT8) {
+        if constexpr (int_mode(MODE)) {
             const float sx = reinterpret_cast<const float*>(p.x_pool_scale)[row];
             const float* s1 = reinterpret_cast<const float*>(w1s) + (int64_t)e * 2 * I;
 #pragma unroll
@@ -154,7 +158,7 @@ __global__ void __launch_bounds__(NT) l1_simt_kernel(Plan p, const uint8_t* __re
             uint16_t* ap = reinterpret_cast<uint16_t*>(p.a_pool);
             ap[row * I + j0] = float_to_bf16_bits(a[0]);
             ap[row * I + j0 + 1] = float_to_bf16_bits(a[1]);
-        } else if constexpr (MODE == MOE_A8W8_INT8) {
+        } else if constexpr (int_mode(MODE)) {
             p.a_f32[row * I + j0] = a[0];
             p.a_f32[row * I + j0 + 1] = a[1];
         } else {
@@ -222,7 +226,7 @@ __global__ void __launch_bounds__(NT) l2_simt_kernel(Plan p, const uint8_t* __re
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
             float y;
-            if constexpr (MODE == MOE_A8W8_INT8) {
+            if constexpr (int_mode(MODE)) {
                 const float s2 = reinterpret_cast<const float*>(w2s)[(int64_t)e * H + h0 + tx * 4 + c];
                 const float sa = reinterpret_cast<const float*>(p.a_pool_scale)[row];
                 y = __fmul_rn(__fmul_rn(__int2float_rn(acc[i][c]), s2), sa);
@@ -236,10 +240,13 @@ __global__ void __launch_bounds__(NT) l2_simt_kernel(Plan p, const uint8_t* __re
     }
 }
 
-// INT8 mode, Linear2 step (1) of the A8W8-INT use case: s = max|A[row,:]|/127 (floored at
-// 1e-8), q = round-half-even(A/s) clamped to [-127, 127]; fp32 IEEE division throughout.
+// Integer modes, Linear2 step (1) of the A8W8-INT and A8W4-INT use cases: s = max|A[row,:]|/127
+// (floored at 1e-8), q = round-half-even(A/s) clamped to [-127, 127]; fp32 IEEE division
+// throughout. Besides the int8 codes it writes the tensor-core operand planes: hi and lo for
+// INT8; for A8W4-INT the codes as f16 in the order of w4_plane_pos, and the row's code sum.
 __global__ void __launch_bounds__(256) int8_row_quant_kernel(Plan p) {
     __shared__ float red[8];
+    __shared__ int red_sum[8];
     const int rows = p.hdr[kHdrPadRows];
     const int I = p.I, nv = p.I / 4;  // float4 vectors of a row
     for (int r = blockIdx.x; r < rows; r += gridDim.x) {
@@ -262,6 +269,10 @@ __global__ void __launch_bounds__(256) int8_row_quant_kernel(Plan p) {
         uint32_t* q = reinterpret_cast<uint32_t*>(p.a_pool + (int64_t)r * I);   // 4 codes per word
         uint2* hi = reinterpret_cast<uint2*>(p.a_planes + (int64_t)r * I);      // plane 0: floor(q/16), f16
         uint2* lo = reinterpret_cast<uint2*>(p.a_planes + (p.pool_rows + r) * I);  // plane 1: q mod 16, f16
+        const bool split = p.mode == MOE_A8W8_INT8;  // A8W4-INT: plane 0 holds q itself
+        int code_sum = 0;
+        // nv is a multiple of 8 and blockDim even: lanes 2m and 2m + 1 hold the two halves of a
+        // group of 8 codes together
         for (int v = threadIdx.x; v < nv; v += blockDim.x) {
             const float4 x = a[v];
             const float xv[4] = {x.x, x.y, x.z, x.w};
@@ -272,14 +283,38 @@ __global__ void __launch_bounds__(256) int8_row_quant_kernel(Plan p) {
                 t = fminf(fmaxf(t, -127.0f), 127.0f);
                 const int qi = static_cast<int>(t);
                 qw |= (uint32_t)(qi & 0xff) << (8 * c);
-                h[c >> 1] |= (uint32_t)float_to_f16_bits((float)(qi >> 4)) << (16 * (c & 1));
+                h[c >> 1] |= (uint32_t)float_to_f16_bits((float)(split ? qi >> 4 : qi)) << (16 * (c & 1));
                 l[c >> 1] |= (uint32_t)float_to_f16_bits((float)(qi & 15)) << (16 * (c & 1));
             }
             q[v] = qw;
-            hi[v] = make_uint2(h[0], h[1]);
-            lo[v] = make_uint2(l[0], l[1]);
+            if (split) {
+                hi[v] = make_uint2(h[0], h[1]);
+                lo[v] = make_uint2(l[0], l[1]);
+            } else {
+                // q0 q4 q1 q5 from the even lane of the pair, q2 q6 q3 q7 from the odd one
+                const bool odd = threadIdx.x & 1;
+                const uint32_t got = __shfl_xor_sync(0xffffffffu, odd ? h[0] : h[1], 1);
+                const uint32_t mine = odd ? h[1] : h[0];
+                hi[v] = odd ? make_uint2((got & 0xffffu) | (mine << 16), (got >> 16) | (mine & 0xffff0000u))
+                            : make_uint2((mine & 0xffffu) | (got << 16), (mine >> 16) | (got & 0xffff0000u));
+                code_sum += (int)(int8_t)(qw & 0xff) + (int)(int8_t)((qw >> 8) & 0xff) +
+                            (int)(int8_t)((qw >> 16) & 0xff) + (int)(int8_t)(qw >> 24);
+            }
         }
         if (threadIdx.x == 0) reinterpret_cast<float*>(p.a_pool_scale)[r] = s;
+        if (!split) {
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) code_sum += __shfl_xor_sync(0xffffffffu, code_sum, o);
+            if ((threadIdx.x & 31) == 0) red_sum[threadIdx.x >> 5] = code_sum;
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                int t = 0;
+#pragma unroll
+                for (int w = 0; w < 8; ++w) t += red_sum[w];
+                p.a_sums[r] = t;
+            }
+            __syncthreads();
+        }
     }
 }
 
@@ -306,6 +341,7 @@ cudaError_t launch_l1_simt(const Plan& p, const void* w1, const void* w1_scale, 
         case MOE_A8W8_FP8: return l1_launch<MOE_A8W8_FP8>(p, w1, w1_scale, s);
         case MOE_A8W8_INT8: return l1_launch<MOE_A8W8_INT8>(p, w1, w1_scale, s);
         case MOE_A8W4_FP8_FP4: return l1_launch<MOE_A8W4_FP8_FP4>(p, w1, w1_scale, s);
+        case MOE_A8W4_INT: return l1_launch<MOE_A8W4_INT>(p, w1, w1_scale, s);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -318,6 +354,7 @@ cudaError_t launch_l2_simt(const Plan& p, const void* w2, const void* w2_scale, 
         case MOE_A8W8_FP8: return l2_launch<MOE_A8W8_FP8>(p, w2, w2_scale, topk_weights, s);
         case MOE_A8W8_INT8: return l2_launch<MOE_A8W8_INT8>(p, w2, w2_scale, topk_weights, s);
         case MOE_A8W4_FP8_FP4: return l2_launch<MOE_A8W4_FP8_FP4>(p, w2, w2_scale, topk_weights, s);
+        case MOE_A8W4_INT: return l2_launch<MOE_A8W4_INT>(p, w2, w2_scale, topk_weights, s);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -4,14 +4,14 @@
 // sm_103a has no integer tcgen05.mma kind, so the integers travel as f16 (kind::f16, fp32
 // accumulation in TMEM), which is exact as long as every partial sum stays below 2^24:
 // - the token codes are split as q = 16*hi + lo with hi = floor(q/16) in [-8, 7] and
-//   lo = q mod 16 in [0, 15] (the identity of the page's A8W4-INT "MSD" scheme); the dispatch
+//   lo = q mod 16 in [0, 15] (the identity of the page's A8W4-INT MSD scheme); the dispatch
 //   stage (x) and the row quantiser (A) store them as two f16 planes;
 // - the weights stay int8 in HBM; TMA brings them into a staging ring (64-byte swizzle) and four
 //   converter warps expand them to f16 (q ^ 0x80 placed under the exponent of 1024 gives
 //   1152 + q exactly; one f16 subtraction removes the 1152), in the 128-byte-swizzled K-major
 //   layout of the MMA;
 // - one tile is 128 weight rows x 128 tokens; its B tile holds the tokens' hi rows, then their
-//   lo rows (N = 256), so |partial sum| <= 15 * 127 * K < 2^24 for K <= 8800, and the epilogue
+//   lo rows (N = 256), so |partial sum| <= 15 * 128 * K < 2^24 for K <= 8704, and the epilogue
 //   rebuilds the exact accumulator as 16 * D_hi + D_lo in int32 before the fp32 dequantisation.
 // Weight-major orientation as in the block-scaled kernel: M = weight rows; L1 tiles carry the
 // gate block and the up block of the same 128 outputs (two accumulators sharing B), L2 tiles two
@@ -56,6 +56,8 @@ constexpr int kCountsOff = kTileOffOff + 4 * (kMaxExperts + 1);
 constexpr int kTabOff = kCountsOff + 4 * kMaxExperts;  // L2 epilogue: per warp [slot, gate, s^A] x 128 rows
 constexpr size_t kSmem = 1024 + (size_t)kTabOff + 4 * 3 * 4 * kTok;
 static_assert(kSmem <= 232448, "shared memory");
+// largest K with every partial sum below 2^24: |lo * w| <= 15 * 128
+constexpr int kMaxK = 8704;
 
 // kind::f16 instruction descriptor: D fp32 (bits 4-5 = 1), A and B f16 (formats 0), both
 // K-major, N = 256 (>> 3 in bits 17-22), M = 128 (>> 4 in bits 24-28).
@@ -101,20 +103,27 @@ __device__ __forceinline__ void int8x4_to_f16(uint32_t w, uint32_t& lo, uint32_t
     hi = *reinterpret_cast<const uint32_t*>(&rb);
 }
 
-// Expand weight row r's 64 int8 codes from the raw tile (64-byte rows, 64-byte swizzle: chunk
-// index ^= address bits 7-8) into f16 row r of a 128-byte-swizzled K-major tile.
-__device__ __forceinline__ void convert_row(const uint8_t* raw_tile, uint8_t* tile, int r) {
+// Weight row r's 64 int8 codes from the raw tile (64-byte rows, 64-byte swizzle: chunk index
+// ^= address bits 7-8), as four 16-byte chunks in K order. The converters load every chunk of
+// their rows before the first store: the compiler cannot tell the raw and f16 tiles apart, so a
+// load placed after a store would wait for it.
+__device__ __forceinline__ void load_row(const uint8_t* raw_tile, int r, uint4 (&c)[4]) {
     const uint8_t* row = raw_tile + r * 64;
     const int x = (r >> 1) & 3;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const uint4 c = *reinterpret_cast<const uint4*>(row + ((q ^ x) << 4));  // 16 codes
+    for (int q = 0; q < 4; ++q) c[q] = *reinterpret_cast<const uint4*>(row + ((q ^ x) << 4));
+}
+
+// Expand them into f16 row r of a 128-byte-swizzled K-major tile.
+__device__ __forceinline__ void store_row(const uint4 (&c)[4], uint8_t* tile, int r) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {  // 16 codes -> two 16-byte chunks of 8 f16
         uint32_t o[8];
-        int8x4_to_f16(c.x, o[0], o[1]);
-        int8x4_to_f16(c.y, o[2], o[3]);
-        int8x4_to_f16(c.z, o[4], o[5]);
-        int8x4_to_f16(c.w, o[6], o[7]);
-        const int ch0 = 2 * q, ch1 = 2 * q + 1;  // 8 f16 per 16-byte chunk
+        int8x4_to_f16(c[q].x, o[0], o[1]);
+        int8x4_to_f16(c[q].y, o[2], o[3]);
+        int8x4_to_f16(c[q].z, o[4], o[5]);
+        int8x4_to_f16(c[q].w, o[6], o[7]);
+        const int ch0 = 2 * q, ch1 = 2 * q + 1;
         *reinterpret_cast<uint4*>(tile + r * 128 + ((ch0 ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
         *reinterpret_cast<uint4*>(tile + r * 128 + ((ch1 ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
     }
@@ -276,8 +285,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const uint8_t* rw = smem + kRawOff + r * kRawBytes;
                 uint8_t* dst = smem + kHfOff + b * kABytes;
-                convert_row(rw, dst, c);
-                convert_row(rw + kWR * kBK, dst + kWR * 128, c);
+                uint4 r0[4], r1[4];
+                load_row(rw, c, r0);
+                load_row(rw + kWR * kBK, c, r1);
+                store_row(r0, dst, c);
+                store_row(r1, dst + kWR * 128, c);
                 fence_proxy_async_smem();
                 mbar_arrive(raw_empty(r));
                 mbar_arrive(hf_full(b));
@@ -420,8 +432,8 @@ cudaError_t launch_int8(const Plan& p, const void* w, const void* w_scale, const
 
 bool int8_tc_supported(const Plan& p, int stage) {
     if (p.mode != MOE_A8W8_INT8 || p.E > kMaxExperts || !tc_encode_available()) return false;
-    if (stage == 1) return p.I % kWR == 0 && p.H % kBK == 0;
-    return p.H % (2 * kWR) == 0 && p.I % kBK == 0;
+    if (stage == 1) return p.I % kWR == 0 && p.H % kBK == 0 && p.H <= kMaxK;
+    return p.H % (2 * kWR) == 0 && p.I % kBK == 0 && p.I <= kMaxK;
 }
 
 cudaError_t launch_l1_int8_tc(const Plan& p, const void* w1, const void* w1_scale, cudaStream_t s) {

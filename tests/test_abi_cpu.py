@@ -45,7 +45,7 @@ CONFIGS = [(64, 256, 128, 8, 2), (4096, 4096, 14336, 8, 2), (128, 7168, 2048, 25
 
 
 @pytest.mark.parametrize("cfg", CONFIGS)
-@pytest.mark.parametrize("mode", ["a16w16", "a8w8_fp8", "a8w8_int8", "a8w4_fp8_fp4"])
+@pytest.mark.parametrize("mode", ["a16w16", "a8w8_fp8", "a8w8_int8", "a8w4_fp8_fp4", "a8w4_int"])
 def test_workspace_layout(moe, cfg, mode):
     T, H, I, E, K = cfg
     d = moe.dims(*cfg)
@@ -59,6 +59,13 @@ def test_workspace_layout(moe, cfg, mode):
         "comb": 2 * R * H, "x_pool": L["pool_rows"] * H * (2 if mode == "a16w16" else 1),
         "a_pool": L["pool_rows"] * I * (2 if mode == "a16w16" else 1),
     }
+    # the integer modes: fp32 A and the f16 operand planes (two for int8 weights, one for int4)
+    planes = {"a8w8_int8": 2, "a8w4_int": 1}.get(mode, 0)
+    if planes:
+        regions.update(a_f32=4 * L["pool_rows"] * I, x_pool_planes=2 * planes * L["pool_rows"] * H,
+                       a_pool_planes=2 * planes * L["pool_rows"] * I)
+    if mode == "a8w4_int":
+        regions["pool_sums"] = 8 * L["pool_rows"]
     spans = sorted((L[k], L[k] + n) for k, n in regions.items() if n)
     for (a0, a1), (b0, b1) in zip(spans, spans[1:]):
         assert a1 <= b0

@@ -1,14 +1,15 @@
 """GPU parity of every stage of the path against the CPU oracle, through the C ABI.
 
 Bars: counts, offsets and the per-expert multiset of row identities bit-exact; floating
-point within max|y - y_ref| <= tol * max|y_ref| (2e-2 bf16 and INT8, 6e-2 for the FP8/FP4
-modes); INT8 L2 accumulators bit-exact given the kernel's own re-quantised operand.
+point within max|y - y_ref| <= tol * max|y_ref| (2e-2 bf16 and the integer modes, 6e-2 for the
+FP8/FP4 modes); integer L2 accumulators bit-exact given the kernel's own re-quantised operand.
 """
 import numpy as np
 import pytest
 import torch
 
 from gpu_util import TOL, assert_close, lib, region, run_forward, slice_tokens, y_numpy
+from oracle import codecs as ocodecs
 from oracle import moe as omoe
 from workloads import WORKLOADS, Workload, make_inputs, to_numpy
 
@@ -35,6 +36,8 @@ CASES = {
                  Workload("ragged_fp8", "a8w8_fp8", 300, 512, 384, 6, 2, 23, 0.05)],
     "a8w8_int8": [Workload("tiny_int8", "a8w8_int8", 64, 256, 128, 8, 2, 24, 0.02),
                   Workload("ragged_int8", "a8w8_int8", 300, 512, 384, 6, 3, 25, 0.05)],
+    "a8w4_int": [Workload("tiny_w4", "a8w4_int", 64, 256, 128, 8, 2, 37, 0.02),
+                 Workload("ragged_w4", "a8w4_int", 300, 512, 384, 6, 3, 38, 0.05)],
     "a8w4_fp8_fp4": [Workload("tiny_fp4", "a8w4_fp8_fp4", 64, 256, 128, 8, 2, 26, 0.02),
                      Workload("ragged_fp4", "a8w4_fp8_fp4", 300, 512, 384, 6, 2, 27, 0.05),
                      Workload("skew_fp4", "a8w4_fp8_fp4", 257, 256, 256, 64, 8, 28, 0.05, zipf_s=1.2, zipf_empty=8),
@@ -101,11 +104,12 @@ def test_dispatch_gathers_rows(moe):
     assert sorted(int(v) for v in pool_src[:n_pad] if v >= 0) == list(range(wl.T * wl.K))
 
 
-def test_int8_l2_accumulators_exact(moe):
+@pytest.mark.parametrize("mode", ["a8w8_int8", "a8w4_int"])
+def test_int8_l2_accumulators_exact(moe, mode):
     """D = A^int8 . W2 must be the exact integer product: recompute the weighted rows from the
-    kernel's own A^int8 and s^A with the oracle's integer GEMM and the page's fp32 dequant
-    order, and require bit equality."""
-    wl = CASES["a8w8_int8"][1]
+    kernel's own A^int8 and s^A with an integer GEMM and the page's fp32 dequant order, and
+    require bit equality (int8 or int4 weights)."""
+    wl = CASES[mode][1]
     inp = make_inputs(wl, device=DEV)
     out = run_forward(moe, wl, inp, stages=True)
     L = out["layout"]
@@ -120,13 +124,18 @@ def test_int8_l2_accumulators_exact(moe):
     g = h["topk_weights"].reshape(-1)
     n_pad = int(region(ws, L, "header", torch.int32, 16).cpu().numpy()[2])
     assert np.abs(a_q[:n_pad][pool_src[:n_pad] >= 0].astype(np.int32)).max() <= 127
+    if mode == "a8w4_int":  # the row quantiser's plane and code sums of the same codes
+        routed = np.nonzero(pool_src[:n_pad] >= 0)[0]
+        _check_w4_operands(ws, L, "a_pool_planes", 1, rows, wl.I, routed, a_q[routed].astype(np.int64))
+        x_q = region(ws, L, "x_pool", torch.int8, rows * wl.H).view(rows, wl.H).cpu().numpy()
+        _check_w4_operands(ws, L, "x_pool_planes", 0, rows, wl.H, routed, x_q[routed].astype(np.int64))
     for e in range(wl.E):
         lo, hi = pad_off[e], pad_off[e + 1]
         src = pool_src[lo:hi]
         keep = src >= 0
         if not keep.any():
             continue
-        w2 = h["w2"][e].astype(np.int64).T  # [I, H]
+        w2 = (ocodecs.int4_unpack(h["w2"][e]) if mode == "a8w4_int" else h["w2"][e]).astype(np.int64).T  # [I, H]
         d = a_q[lo:hi][keep].astype(np.int64) @ w2
         y32 = (d.astype(np.float32) * h["w2_scale"][e][None, :]).astype(np.float32)
         y32 = (y32 * s_a[lo:hi][keep][:, None]).astype(np.float32)
@@ -202,7 +211,7 @@ def test_bounded_wait_times_out_and_device_stays_usable(moe):
     assert_close(y_numpy(out["y"]), oracle_forward(wl, inp), wl.mode)
 
 
-FULL = ["mixtral_bf16_prefill", "dsv3_fp8fp4_decode", "dsv3_fp8fp4_prefill_zipf", "int8_a8w8"]
+FULL = ["mixtral_bf16_prefill", "dsv3_fp8fp4_decode", "dsv3_fp8fp4_prefill_zipf", "int8_a8w8", "int4_a8w4"]
 
 
 @pytest.mark.parametrize("name", FULL)
@@ -290,6 +299,48 @@ def test_int8_l1_accumulators_exact_on_adversarial_codes(moe):
         assert np.abs(got[~pos]).max(initial=0) < 1e-20 and np.abs(a_ref[~pos]).max(initial=0) < 1e-20
 
 
+def test_int4_l1_accumulators_exact_at_the_largest_k(moe):
+    """A8W4-INT at K = 8704, the largest hidden size of its tensor-core path: x codes +-127,
+    int4 weights +-4, and for expert 0 gate channels of all 7 and up channels of all -8 against
+    rows of all 127. The kernel accumulates (w + 8) * q, which reaches 15 * 127 * 8704 =
+    16,581,120 (between 2^23 and 2^24) on those gate channels. Every sum is a multiple of 1016 (an
+    even count of odd multiples of 508) or of 1778, so SiLU(H) = H exactly for H > 0 and the fp32
+    A must equal the oracle's bit for bit there."""
+    wl = Workload("adv_w4", "a8w4_int", 96, 8704, 256, 2, 1, 52, 0.05)
+    inp = make_inputs(wl, device=DEV)
+    g = torch.Generator(device=DEV).manual_seed(6)
+    sign = lambda shape: torch.randint(0, 2, shape, generator=g, device=DEV) * 2 - 1
+    x = (sign(inp["x"].shape) * 127).to(torch.int8)
+    x[:3] = 127
+    w1 = sign((wl.E, 2 * wl.I, wl.H)) * 4
+    w1[0, :3] = 7
+    w1[0, wl.I:wl.I + 3] = -8
+    nib = (w1 & 0xF).to(torch.uint8)
+    inp["x"], inp["x_scale"] = x, torch.ones_like(inp["x_scale"])
+    inp["w1"] = (nib[..., 0::2] | (nib[..., 1::2] << 4)).contiguous()
+    inp["w1_scale"] = torch.ones_like(inp["w1_scale"])
+    inp["topk_ids"][:3] = 0
+    out = run_forward(moe, wl, inp, stages=True)
+    assert out["status"] == 0
+    L = out["layout"]
+    rows = L["pool_rows"]
+    ws = out["ws"]
+    n_pad = int(region(ws, L, "header", torch.int32, 16).cpu().numpy()[2])
+    pool_src = region(ws, L, "pool_src", torch.int32, rows).cpu().numpy()[:n_pad]
+    a_f32 = region(ws, L, "a_f32", torch.float32, rows * wl.I).view(rows, wl.I).cpu().numpy()
+    _, rec = oracle_forward(wl, inp, return_intermediates=True)
+    got_rows = {int(s): i for i, s in enumerate(pool_src) if s >= 0}
+    for e, r in rec["experts"].items():
+        h = r["h"]
+        if e == 0:
+            assert np.abs(r["c"]).max() > 2 ** 22
+        a_ref = (omoe.swiglu(h, wl.I)).astype(np.float32)
+        got = np.stack([a_f32[got_rows[int(s)]] for s in r["src"]])
+        pos = h[:, :wl.I] > 0
+        assert np.array_equal(got[pos], a_ref[pos]), f"expert {e}: {np.abs(got - a_ref)[pos].max()}"
+        assert np.abs(got[~pos]).max(initial=0) < 1e-20 and np.abs(a_ref[~pos]).max(initial=0) < 1e-20
+
+
 @pytest.mark.parametrize("mode,wl", [(m, w) for m, w in ALL if m != "a16w16"],
                          ids=[f"{m}-{w.name}" for m, w in ALL if m != "a16w16"])
 def test_quantised_tensor_core_path_matches_reference_kernels(moe, mode, wl):
@@ -322,7 +373,22 @@ def test_token_major_and_weight_major_block_scaled_tiles_agree(moe, mode, wl):
         assert_close(y_numpy(o["y"]), ref, mode)
 
 
+W4_ORDER = np.array([0, 4, 1, 5, 2, 6, 3, 7])
+
+
+def _check_w4_operands(ws, L, planes, sums_half, R, n, rows, codes):
+    """A8W4-INT operand rows: plane position 8g + p holds code 8g + W4_ORDER[p] as f16, and the
+    row's code sum is stored beside (x rows in the first half of the sums region, A rows in the
+    second)."""
+    plane = region(ws, L, planes, torch.float16, R * n).view(R, n).float().cpu().numpy()[rows]
+    perm = (np.arange(n) // 8) * 8 + W4_ORDER[np.arange(n) % 8]
+    assert np.array_equal(plane, codes[:, perm].astype(np.float64)), "plane"
+    sums = region(ws, L, "pool_sums", torch.int32, 2 * R).view(2, R).cpu().numpy()[sums_half, rows]
+    assert np.array_equal(sums, codes.sum(axis=1)), "code sums"
+
+
 XQ_CASES = [(m, w) for m, w in ALL if m != "a16w16" and w.name in ("tiny_fp8", "ragged_fp8", "tiny_int8", "ragged_int8",
+                                                                    "tiny_w4", "ragged_w4",
                                                                     "tiny_fp4", "skew_fp4", "n224_fp4", "n224_fp8")]
 
 
@@ -368,6 +434,8 @@ def test_dispatch_quantize_matches_oracle_bit_exactly(moe, mode, wl):
         planes = region(ws, L, "x_pool_planes", torch.float16, 2 * R * wl.H).view(2, R, wl.H).float().cpu().numpy()
         q = qx.astype(np.int64)[tok]
         assert np.array_equal(planes[0, rows], np.floor_divide(q, 16)) and np.array_equal(planes[1, rows], q % 16)
+    if mode == "a8w4_int":  # one plane: the codes themselves, in the expansion's order, and their sums
+        _check_w4_operands(ws, L, "x_pool_planes", 0, R, wl.H, rows, qx.astype(np.int64)[tok])
 
 
 @pytest.mark.parametrize("mode,wl", XQ_CASES, ids=[f"{m}-{w.name}" for m, w in XQ_CASES])
@@ -387,7 +455,7 @@ def test_forward_quantizing_x_matches_oracle(moe, mode, wl):
     assert_close(y_numpy(y), ref, mode)
 
 
-@pytest.mark.parametrize("name", ["dsv3_fp8fp4_prefill_zipf", "int8_a8w8", "dsv3_fp8fp4_decode"])
+@pytest.mark.parametrize("name", ["dsv3_fp8fp4_prefill_zipf", "int8_a8w8", "dsv3_fp8fp4_decode", "int4_a8w4"])
 def test_full_size_quantizing_x_sampled(moe, name):
     """Full-size workload from bf16 x (the dispatch stage quantises it, as the bench's --quantize-x
     times it): the pool codes of a seeded sample of tokens are bit-exact against the oracle's
@@ -418,7 +486,7 @@ def test_full_size_quantizing_x_sampled(moe, name):
 
 
 CLAMP_CASES = [(m, w) for m, w in ALL if w.name in ("tiny_bf16", "ragged_bf16", "ragged_fp8", "ragged_int8", "ragged_fp4",
-                                                     "skew_fp4", "n224_fp4")]
+                                                     "skew_fp4", "n224_fp4", "ragged_w4")]
 
 
 @pytest.mark.parametrize("mode,wl", CLAMP_CASES, ids=[f"{m}-{w.name}" for m, w in CLAMP_CASES])
