@@ -25,7 +25,9 @@ Readings where the pages are silent or disagree (each listed in the design notes
   * the FP8 re-quantisation of A uses blocks of 32 along the intermediate dimension with a
     power-of-two scale 2^ceil(log2(amax/448)) stored as UE8M0;
   * the INT8 re-quantisation of A follows p1's per-row formula with the scale floored at
-    1e-8 (the floor of p1's own weight-quantisation example).
+    1e-8 (the floor of p1's own weight-quantisation example);
+  * a shared expert (DeepGEMM page §6) is computed like a routed one, in the same dtype mode,
+    on every token, with weight 1 in the extra combine slot K + j after the routed slots.
 """
 from __future__ import annotations
 
@@ -336,14 +338,33 @@ def combine_rows(contrib: np.ndarray) -> np.ndarray:
 # ---------------------------------------------------------------------------------------
 
 
+def with_shared_slots(topk_ids, topk_weights, num_experts: int, num_shared: int):
+    """The routing with the shared experts' slots (DeepGEMM page §6, optional shared experts):
+    a shared expert takes no routed id; it sees every token, and its output goes to an extra
+    combine slot after the K routed ones, which the combine sums with them. Shared expert j is
+    expert num_experts + j of the weight tensors; its slot K + j carries weight 1 (the page gives
+    the slot no gate). Returns ids [T, K + S] and weights [T, K + S]."""
+    ids = np.asarray(topk_ids)
+    g = np.asarray(topk_weights, dtype=np.float32)
+    T = ids.shape[0]
+    shared_ids = np.tile(np.arange(num_experts, num_experts + num_shared, dtype=ids.dtype), (T, 1))
+    ones = np.ones((T, num_shared), dtype=np.float32)
+    return np.concatenate([ids, shared_ids], axis=1), np.concatenate([g, ones], axis=1)
+
+
 def forward(mode: str, x, x_scale, topk_ids, topk_weights, w1, w1_scale, w2, w2_scale,
-            num_experts: int, inter: int, return_intermediates: bool = False, clamp: float | None = None):
+            num_experts: int, inter: int, return_intermediates: bool = False, clamp: float | None = None,
+            num_shared: int = 0):
     """Plan -> per-expert L1 -> SwiGLU (inputs clipped to [-clamp, clamp] when clamp is given)
-    -> requant -> L2 -> gate -> combine.
+    -> requant -> L2 -> gate -> combine. With num_shared > 0 the weight tensors hold
+    num_experts routed experts followed by the shared ones (see with_shared_slots).
 
     Returns y as float64 bf16 values [T, H] (and, on request, the plan and per-row
     intermediates keyed by pool position: 'comb' holds the weighted bf16 rows [T*K, H]).
     """
+    if num_shared:
+        topk_ids, topk_weights = with_shared_slots(topk_ids, topk_weights, num_experts, num_shared)
+        num_experts += num_shared
     ids = np.asarray(topk_ids)
     T, K = ids.shape
     g = np.asarray(topk_weights, dtype=np.float32)
@@ -376,10 +397,13 @@ def forward(mode: str, x, x_scale, topk_ids, topk_weights, w1, w1_scale, w2, w2_
 
 
 def forward_tokens(mode: str, tokens, x, x_scale, topk_ids, topk_weights, w1, w1_scale, w2,
-                   w2_scale, inter: int, clamp: float | None = None):
+                   w2_scale, inter: int, clamp: float | None = None, num_experts: int = 0, num_shared: int = 0):
     """Brute force for a subset of tokens: for each token i and each slot k, evaluate the FFN
     of expert E[i,k] on x_i alone, weight it and sum. No plan and no permutation is used, so
-    this checks the pooled path (every row of an expert is computed independently)."""
+    this checks the pooled path (every row of an expert is computed independently). Shared
+    experts (num_shared > 0, after num_experts routed ones) add their slots after the routed."""
+    if num_shared:
+        topk_ids, topk_weights = with_shared_slots(topk_ids, topk_weights, num_experts, num_shared)
     ids = np.asarray(topk_ids)
     T, K = ids.shape
     g = np.asarray(topk_weights, dtype=np.float32)

@@ -1,5 +1,6 @@
 """Pins of the oracle's plan, SwiGLU and forward path against the pages' worked example,
 hand-derived closed forms, invariants, brute force and library routines."""
+import dataclasses
 import json
 import math
 import os
@@ -261,4 +262,61 @@ def test_activation_clamp_brute_force_equals_pooled_path(mode):
     yb = moe.forward_tokens(mode, range(wl.T), d["x"], d["x_scale"], d["topk_ids"], d["topk_weights"],
                             d["w1"], d["w1_scale"], d["w2"], d["w2_scale"], inter=wl.I, clamp=c)
     assert np.array_equal(y, yb)
+    assert not np.array_equal(y, _forward(mode, d, wl))
+
+
+# ---------------------------------------------------------------------------------------
+# Shared experts (DeepGEMM page §6): every token, weight 1, the slot after the routed ones
+# ---------------------------------------------------------------------------------------
+
+
+def test_shared_expert_alone_is_a_dense_ffn():
+    """Routed gates all zero, one shared expert: y = bf16(bf16(SwiGLU(x W1s)) W2s) on every
+    token, computed with torch float64 matmul and torch's SiLU (independent of the oracle)."""
+    wl = Workload("shared_dense", "a16w16", 20, 64, 32, 3, 2, 22, 0.2)
+    inp = make_inputs(wl, shared=1)
+    assert inp["w1"].shape[0] == 4 and inp["w2"].shape[0] == 4
+    inp["topk_weights"] = torch.zeros_like(inp["topk_weights"])
+    d = _np(inp)
+    y = _forward("a16w16", d, wl, num_shared=1)
+    x = inp["x"].double()
+    h = x @ inp["w1"][3].double()
+    a = (torch.nn.functional.silu(h[:, :32]) * h[:, 32:]).to(torch.bfloat16).double()
+    ref = (a @ inp["w2"][3].double()).float().to(torch.bfloat16).double().numpy()
+    assert np.array_equal(y, ref)
+    # masking every routed slot instead of zeroing its gate gives the same output
+    ids_m = np.full_like(d["topk_ids"], -1)
+    assert np.array_equal(_forward("a16w16", dict(d, topk_ids=ids_m), wl, num_shared=1), ref)
+
+
+@pytest.mark.parametrize("mode", list(TINY))
+def test_shared_copy_of_the_routed_expert_doubles_the_output(mode):
+    """Every token routed to expert 0 with gate 1 (K = 1) and a shared expert that is a copy of
+    expert 0: both slots hold the same bf16 row c, so y = bf16(c + c) = 2 y(no shared), exactly."""
+    wl = dataclasses.replace(TINY[mode], K=1)
+    inp = make_inputs(wl, shared=1)
+    for name in ("w1", "w1_scale", "w2", "w2_scale"):
+        if inp[name] is not None:
+            inp[name][wl.E] = inp[name][0]
+    inp["topk_ids"] = torch.zeros_like(inp["topk_ids"])
+    inp["topk_weights"] = torch.ones_like(inp["topk_weights"])
+    d = _np(inp)
+    y0 = _forward(mode, d, wl)
+    y1 = _forward(mode, d, wl, num_shared=1)
+    assert np.abs(y0).max() > 0
+    assert np.array_equal(y1, 2.0 * y0)
+
+
+@pytest.mark.parametrize("mode", list(TINY))
+def test_shared_brute_force_per_token_equals_pooled_path(mode):
+    wl = TINY[mode]
+    d = _np(make_inputs(wl, shared=2))
+    y, rec = _forward(mode, d, wl, num_shared=2, return_intermediates=True)
+    yb = moe.forward_tokens(mode, range(wl.T), d["x"], d["x_scale"], d["topk_ids"], d["topk_weights"],
+                            d["w1"], d["w1_scale"], d["w2"], d["w2_scale"], inter=wl.I,
+                            num_experts=wl.E, num_shared=2)
+    assert np.array_equal(y, yb)
+    # each shared expert sees every token; the routed experts see their routed rows only
+    assert rec["counts"].tolist()[wl.E:] == [wl.T, wl.T]
+    assert sum(rec["counts"].tolist()[:wl.E]) == wl.T * wl.K
     assert not np.array_equal(y, _forward(mode, d, wl))

@@ -165,12 +165,21 @@ def int4_per_row_packed(v: torch.Tensor):
 # ---------------------------------------------------------------------------------------
 
 
-def make_inputs(wl: Workload, device="cpu", mode: str | None = None):
+def make_inputs(wl: Workload, device="cpu", mode: str | None = None, shared: int = 0):
     """Generate every input of one forward call for workload ``wl`` on ``device``.
 
     Returns a dict of contiguous tensors: x, x_scale, topk_ids, topk_weights, w1, w1_scale,
     w2, w2_scale (scales are None where the mode has none), and x_bf16, the bf16 activations
-    (the input of the path on which the operator quantises x itself)."""
+    (the input of the path on which the operator quantises x itself). With ``shared`` > 0 the
+    weight tensors hold the wl.E routed experts (the same as without) followed by ``shared``
+    shared experts drawn from a seed of their own; routing stays over the routed experts."""
+    if shared:
+        out = make_inputs(wl, device, mode)
+        extra = make_inputs(dataclasses.replace(wl, E=shared, K=1, seed=wl.seed + 1000003, zipf_s=None), device, mode)
+        for name in ("w1", "w1_scale", "w2", "w2_scale"):
+            if out[name] is not None:
+                out[name] = torch.cat([out[name], extra[name]]).contiguous()
+        return out
     mode = mode or wl.mode
     T, H, I, E, K = wl.T, wl.H, wl.I, wl.E, wl.K
     g = _gen(wl.seed, device)
