@@ -26,7 +26,7 @@
  *     that ran out) are recorded in the workspace's error word; read them with
  *     moe_check_device_error().
  *   - Limits: 0 <= T, 1 <= K <= 32, K <= E <= 1024, H and I multiples of 128, and
- *     T*K <= 2^24.
+ *     T*K <= 2^24; with S shared experts, K + S <= 32, E + S <= 1024 and T*(K+S) <= 2^24.
  */
 #ifndef MOE_FFN_H
 #define MOE_FFN_H
@@ -90,9 +90,19 @@ typedef struct {
     int32_t num_tokens;    /* T */
     int32_t hidden;        /* H */
     int32_t intermediate;  /* I: the width of A; w1 has 2*I outputs */
-    int32_t num_experts;   /* E */
-    int32_t topk;          /* K */
+    int32_t num_experts;   /* E: routed experts */
+    int32_t topk;          /* K: routed slots per token */
+    int32_t num_shared_experts; /* S >= 0: shared experts (DeepGEMM page §6), see below */
 } moe_dims;
+
+/* Shared experts. Each of the S shared experts runs on every token, in the same mode as the
+ * routed ones, and its output goes to a combine slot after the K routed slots with weight 1;
+ * the combine sums it with them in slot order. The weights (w1, w2 and their scales) then
+ * hold E + S experts: the E routed experts first, shared expert j at index E + j. topk_ids
+ * and topk_weights stay [T,K]; a routed id in [E, E+S) is a bad route. Internally every token
+ * has K + S slots (token i, slot k is row i*(K+S)+k), so the plan covers E + S experts and
+ * T*(K+S) slots: the counts, offsets and row_src that moe_plan writes have E+S, E+S+1 and
+ * T*(K+S) entries. S = 0 is the plain routed layer. */
 
 /* A quantised tensor: its codes and, where the mode has them, its scales (device). */
 typedef struct {
@@ -124,6 +134,7 @@ MOE_API size_t moe_workspace_bytes(const moe_dims* d, moe_dtype_mode m);
  *             expert_token_nums output).
  *   offsets   device int32 [E+1] or NULL: exclusive prefix sum of counts; offsets[E] = R.
  *   row_src   device int32 [T*K] or NULL: row_src[p] = i*K+k for p < R, the (token, slot)
+ *             (with shared experts: E+S, E+S+1 and T*(K+S) entries, slots i*(K+S)+k)
  *             identity of routed row p; rows of expert e fill [offsets[e], offsets[e+1]),
  *             in an order the call does not fix (the page allows any fixed order).
  * The plan is also kept in the workspace for the stages that follow. */
@@ -206,7 +217,8 @@ MOE_API moe_status moe_check_device_error(void* workspace, moe_stream_t stream);
 /* Static text for a status code. */
 MOE_API const char* moe_status_string(moe_status s);
 
-/* Byte offsets of the workspace regions, for inspection of the intermediate stages. Rows of
+/* Byte offsets of the workspace regions, for inspection of the intermediate stages (E and K
+ * below count the shared experts and their slots when S > 0: E + S and K + S). Rows of
  * expert e in the pools start at pad_offsets[e] (a multiple of the 128-row tile) and the
  * pool holds at most pool_rows rows. A region that a mode does not use has size 0. */
 typedef struct {
@@ -218,6 +230,8 @@ typedef struct {
     size_t row_src;       /* int32[T*K] unpadded pool row -> i*K+k */
     size_t pool_src;      /* int32[pool_rows] padded pool row -> i*K+k, -1 for padding */
     size_t slot_row;      /* int32[T*K] i*K+k -> padded pool row, -1 if masked */
+    size_t gates;         /* shared experts: fp32 [T*(K+S)], the routed gates then 1 per shared
+                             slot (written by moe_expert_l2; S = 0: size 0) */
     size_t x_pool;        /* gathered x codes [pool_rows, H] */
     size_t x_pool_scale;  /* gathered x scales [pool_rows, *] */
     size_t a_pool;        /* L2 operand codes [pool_rows, I] */
@@ -245,7 +259,8 @@ MOE_API moe_status moe_workspace_layout(const moe_dims* d, moe_dtype_mode m, moe
  * counterpart of this call; it is an allocation-free variant of moe_plan.)
  *   topk_ids, counts, offsets, row_src  as for moe_plan (device memory, owned by the caller;
  *             counts and offsets are required, row_src is required when T*K > 0).
- *   Limits: T*K <= 65536 and E <= 1024; larger sizes return MOE_ERR_INVALID_ARG and launch
+ *   Limits: T*K <= 65536 and E <= 1024 (T*(K+S) and E+S with shared experts, whose slots the
+ *   plan includes as moe_plan's does); larger sizes return MOE_ERR_INVALID_ARG and launch
  *   nothing. The call allocates nothing: its scratch is one fixed 1,590,272-byte device array
  *   inside the library that every GPU which loads the library holds until the process exits.
  *   The first call on a device looks up that array's device address (cudaGetSymbolAddress)

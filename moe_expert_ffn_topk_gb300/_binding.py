@@ -28,7 +28,7 @@ ABI_FUNCTIONS = ("moe_workspace_bytes", "moe_plan", "moe_dispatch", "moe_expert_
 
 class MoeDims(ctypes.Structure):
     _fields_ = [("num_tokens", ctypes.c_int32), ("hidden", ctypes.c_int32), ("intermediate", ctypes.c_int32),
-                ("num_experts", ctypes.c_int32), ("topk", ctypes.c_int32)]
+                ("num_experts", ctypes.c_int32), ("topk", ctypes.c_int32), ("num_shared_experts", ctypes.c_int32)]
 
 
 class MoeOptions(ctypes.Structure):
@@ -42,7 +42,7 @@ class MoeOperand(ctypes.Structure):
 
 class MoeWorkspaceLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
-        "header", "counts", "offsets", "pad_offsets", "tile_offsets", "row_src", "pool_src", "slot_row",
+        "header", "counts", "offsets", "pad_offsets", "tile_offsets", "row_src", "pool_src", "slot_row", "gates",
         "x_pool", "x_pool_scale", "a_pool", "a_pool_scale", "a_f32", "x_pool_planes", "a_pool_planes", "pool_sums",
         "comb",
         "total")] + \
@@ -93,8 +93,9 @@ LIB = _load()
 # ---------------------------------------------------------------------------------------
 
 
-def dims(T: int, H: int, I: int, E: int, K: int) -> MoeDims:  # noqa: E741
-    return MoeDims(T, H, I, E, K)
+def dims(T: int, H: int, I: int, E: int, K: int, S: int = 0) -> MoeDims:  # noqa: E741
+    """T tokens, hidden H, intermediate I, E routed experts, top-K, S shared experts."""
+    return MoeDims(T, H, I, E, K, S)
 
 
 def _mode(m) -> int:

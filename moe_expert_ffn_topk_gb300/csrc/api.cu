@@ -37,10 +37,11 @@ int64_t a_scale_row_bytes(int mode, int I) {
 static bool dims_ok(const moe_dims* d, moe_dtype_mode m) {
     if (!d) return false;
     if (m < MOE_A16W16 || m > MOE_A8W4_INT) return false;
-    if (d->num_tokens < 0 || d->topk < 1 || d->topk > 32) return false;
-    if (d->num_experts < d->topk || d->num_experts > 1024) return false;
+    const int S = d->num_shared_experts;
+    if (d->num_tokens < 0 || d->topk < 1 || S < 0 || d->topk + S > 32) return false;
+    if (d->num_experts < d->topk || d->num_experts + S > 1024) return false;
     if (d->hidden < 128 || d->hidden % 128 || d->intermediate < 128 || d->intermediate % 128) return false;
-    if ((int64_t)d->num_tokens * d->topk > (int64_t(1) << 24)) return false;
+    if ((int64_t)d->num_tokens * (d->topk + S) > (int64_t(1) << 24)) return false;
     if ((int64_t)d->hidden > (1 << 16) || (int64_t)d->intermediate > (1 << 16)) return false;
     return true;
 }
@@ -49,7 +50,9 @@ static size_t align_up(size_t v) { return (v + 255) & ~size_t(255); }
 
 moe_status layout(const moe_dims* d, moe_dtype_mode m, moe_workspace_layout_t* out) {
     if (!out || !dims_ok(d, m)) return MOE_ERR_INVALID_ARG;
-    const int64_t T = d->num_tokens, H = d->hidden, I = d->intermediate, E = d->num_experts, K = d->topk;
+    // the shared experts are experts E..E+S-1 with one slot per token each
+    const int64_t S = d->num_shared_experts;
+    const int64_t T = d->num_tokens, H = d->hidden, I = d->intermediate, E = d->num_experts + S, K = d->topk + S;
     const int64_t R = T * K;
     const int64_t pool_rows = R + std::min<int64_t>(E, R) * (kTileRows - 1);
     moe_workspace_layout_t L;
@@ -72,6 +75,7 @@ moe_status layout(const moe_dims* d, moe_dtype_mode m, moe_workspace_layout_t* o
     L.row_src = take(sizeof(int32_t) * R);
     L.pool_src = take(sizeof(int32_t) * pool_rows);
     L.slot_row = take(sizeof(int32_t) * R);
+    L.gates = take(S ? sizeof(float) * R : 0);
     L.comb = take((size_t)R * H * 2);
     // everything above is the same for every mode; the pools below depend on it
     L.x_pool = take((size_t)pool_rows * H * x_elem_bytes(m));
@@ -100,8 +104,11 @@ moe_status make_plan_view(const moe_dims* d, moe_dtype_mode m, void* ws, size_t 
     p->T = d->num_tokens;
     p->H = d->hidden;
     p->I = d->intermediate;
-    p->E = d->num_experts;
-    p->K = d->topk;
+    p->E = d->num_experts + d->num_shared_experts;
+    p->K = d->topk + d->num_shared_experts;
+    p->Er = d->num_experts;
+    p->Kr = d->topk;
+    p->gates = reinterpret_cast<float*>(b + L.gates);
     p->mode = m;
     p->pool_rows = L.pool_rows;
     p->hdr = reinterpret_cast<int32_t*>(b + L.header);
@@ -240,6 +247,11 @@ moe_status moe_expert_l2(moe_operand w2, const float* topk_weights, const moe_di
     if (d->num_tokens == 0) return MOE_OK;
     if (!topk_weights) return MOE_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (p.K != p.Kr) {  // shared experts: their slots carry weight 1
+        const cudaError_t e = launch_expand_gates(p, topk_weights, s);
+        if (e != cudaSuccess) return from_cuda(e);
+        topk_weights = p.gates;
+    }
     if (!(flags & MOE_FLAG_SIMT) && tc_supported(p, 2))
         return from_cuda(launch_l2_tc(p, w2.data, w2.scale, topk_weights, s));
     if (!(flags & MOE_FLAG_SIMT) && bs_supported(p, 2))

@@ -24,7 +24,8 @@ __host__ __device__ constexpr int int_planes(int m) { return m == MOE_A8W8_INT8 
 
 // Device view of the workspace for one (dims, mode).
 struct Plan {
-    int T, H, I, E, K;
+    int T, H, I, E, K;     // E, K: all experts and slots, shared ones included
+    int Er, Kr;            // routed experts and slots (E - Er = K - Kr = shared experts)
     int mode;
     int64_t pool_rows;
     int32_t* hdr;
@@ -48,6 +49,7 @@ struct Plan {
     int32_t* a_sums;       // A8W4-INT: sum of each A pool row's codes [pool_rows]
     uint16_t* comb;        // bf16 [T*K, H]
     float act_clamp;       // SwiGLU inputs clipped to [-act_clamp, act_clamp]; +inf: no clamp
+    float* gates;          // shared experts: [T*K] gates, the routed ones then 1 per shared slot
 };
 
 // x / A storage properties per mode
@@ -64,6 +66,8 @@ cudaError_t launch_route(const Plan& p, const int32_t* topk_ids, int32_t* counts
                          int32_t* row_src_out, cudaStream_t s);
 cudaError_t launch_dispatch(const Plan& p, const void* x, const void* x_scale, cudaStream_t s);
 cudaError_t launch_combine(const Plan& p, uint16_t* y, cudaStream_t s);
+// shared experts: p.gates[t*K + k] = k < Kr ? topk_weights[t*Kr + k] : 1
+cudaError_t launch_expand_gates(const Plan& p, const float* topk_weights, cudaStream_t s);
 cudaError_t launch_l1_simt(const Plan& p, const void* w1, const void* w1_scale, cudaStream_t s);
 cudaError_t launch_l2_simt(const Plan& p, const void* w2, const void* w2_scale, const float* topk_weights,
                            cudaStream_t s);

@@ -77,10 +77,12 @@ using namespace moe;
 
 extern "C" MOE_API moe_status moe_plan_noalloc(const int32_t* topk_ids, const moe_dims* d, int32_t* counts,
                                                int32_t* offsets, int32_t* row_src, moe_stream_t stream) {
-    if (!d || d->num_tokens < 0 || d->topk < 1 || d->topk > 32 || d->num_experts < d->topk ||
-        d->num_experts > kNoallocMaxExperts)
+    if (!d || d->num_tokens < 0 || d->topk < 1 || d->num_shared_experts < 0 ||
+        d->topk + d->num_shared_experts > 32 || d->num_experts < d->topk ||
+        d->num_experts + d->num_shared_experts > kNoallocMaxExperts)
         return MOE_ERR_INVALID_ARG;
-    const int64_t ids = (int64_t)d->num_tokens * d->topk;
+    const int E = d->num_experts + d->num_shared_experts, K = d->topk + d->num_shared_experts;
+    const int64_t ids = (int64_t)d->num_tokens * K;  // the shared experts' slots included
     if (ids > kNoallocMaxIds) return MOE_ERR_INVALID_ARG;
     if (!counts || !offsets || (ids > 0 && (!topk_ids || !row_src))) return MOE_ERR_INVALID_ARG;
     int32_t* s = nullptr;
@@ -89,10 +91,12 @@ extern "C" MOE_API moe_status moe_plan_noalloc(const int32_t* topk_ids, const mo
     p.T = d->num_tokens;
     p.H = d->hidden;
     p.I = d->intermediate;
-    p.E = d->num_experts;
-    p.K = d->topk;
+    p.E = E;
+    p.K = K;
+    p.Er = d->num_experts;
+    p.Kr = d->topk;
     p.mode = MOE_A16W16;
-    p.pool_rows = ids + std::min<int64_t>(d->num_experts, ids) * (kTileRows - 1);
+    p.pool_rows = ids + std::min<int64_t>(E, ids) * (kTileRows - 1);
     p.hdr = s + kOffHdr;
     p.claim = s + kOffClaim;
     p.counts = s + kOffCounts;

@@ -21,9 +21,22 @@ constexpr int kRouteThreads = 256;
 constexpr int kRouteItems = 16;                       // ids per thread in the count kernel
 constexpr int kRouteChunk = kRouteThreads * kRouteItems;
 
+// Expert of slot i = t*Kt + k of the plan: the caller's id for the Kr routed slots; shared
+// expert Er + (k - Kr) for the slots after them (DeepGEMM page §6: a shared expert takes every
+// token, in the combine slot after the routed ones). A routed id that names a shared expert is
+// returned as Et = Er + (Kt - Kr), out of range, so that it counts as a bad route.
+__device__ __forceinline__ int route_id(const int32_t* __restrict__ ids, int i, int Kt, int Kr, int Er) {
+    if (Kt == Kr) return ids[i];
+    const int t = i / Kt, k = i - t * Kt;
+    if (k >= Kr) return Er + (k - Kr);
+    const int e = ids[t * Kr + k];
+    return e >= Er ? Er + (Kt - Kr) : e;
+}
+
 // Count ids per expert in shared memory (warp-aggregated), claim each expert's range with a
 // global atomicAdd and record every id's position inside its expert.
 __global__ void __launch_bounds__(kRouteThreads) route_count_claim_kernel(const int32_t* __restrict__ ids, int n_ids,
+                                                                          int Kt, int Kr, int Er,
                                                                           int E, int32_t* __restrict__ claim,
                                                                           int32_t* __restrict__ pos,
                                                                           int32_t* __restrict__ hdr) {
@@ -41,7 +54,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_count_claim_kernel(const 
     for (int j = 0; j < kRouteItems; ++j) {
         const int i = begin + j * kRouteThreads + threadIdx.x;
         const bool in = i < n_ids;
-        int e = in ? ids[i] : -1;
+        int e = in ? route_id(ids, i, Kt, Kr, Er) : -1;
         const bool valid = in && e >= 0 && e < E;
         if (in && !valid && e != -1) record_error(hdr, MOE_ERR_BAD_ROUTE);
         expert[j] = valid ? e : -1;
@@ -132,13 +145,14 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int E, const int32_t* 
 }
 
 // Scatter every routed (i,k) to its pool row and record both directions of the identity map.
-__global__ void route_scatter_kernel(const int32_t* __restrict__ ids, int n_ids, int E, const int32_t* __restrict__ pos,
+__global__ void route_scatter_kernel(const int32_t* __restrict__ ids, int n_ids, int Kt, int Kr, int Er, int E,
+                                     const int32_t* __restrict__ pos,
                                      const int32_t* __restrict__ offsets, const int32_t* __restrict__ pad_off,
                                      int32_t* __restrict__ row_src, int32_t* __restrict__ pool_src,
                                      int32_t* __restrict__ slot_row, int32_t* __restrict__ row_src_out) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n_ids) return;
-    const int e = ids[i];
+    const int e = route_id(ids, i, Kt, Kr, Er);
     const int p = pos[i];
     if (e < 0 || e >= E || p < 0) {
         slot_row[i] = -1;
@@ -411,6 +425,15 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
     y[(size_t)t * row_vecs + v] = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// Gates of the plan's slots with shared experts: the caller's [T, Kr] gates, then 1 for each of
+// the Kt - Kr shared slots of a token.
+__global__ void expand_gates_kernel(const float* __restrict__ g, int n, int Kt, int Kr, float* __restrict__ out) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const int t = i / Kt, k = i - t * Kt;
+    out[i] = k < Kr ? g[t * Kr + k] : 1.0f;
+}
+
 // Waits for hdr[kHdrWaitFlag] to become non-zero, at most timeout_ns; on time-out records
 // MOE_ERR_TIMEOUT and returns.
 __global__ void debug_wait_kernel(int32_t* hdr, uint64_t timeout_ns) {
@@ -438,14 +461,15 @@ cudaError_t launch_route(const Plan& p, const int32_t* topk_ids, int32_t* counts
     if (e != cudaSuccess) return e;
     if (n_ids > 0) {
         const int blocks = (n_ids + kRouteChunk - 1) / kRouteChunk;
-        route_count_claim_kernel<<<blocks, kRouteThreads, 2 * p.E * sizeof(int32_t), s>>>(topk_ids, n_ids, p.E, p.claim,
-                                                                                          p.pos, p.hdr);
+        route_count_claim_kernel<<<blocks, kRouteThreads, 2 * p.E * sizeof(int32_t), s>>>(
+            topk_ids, n_ids, p.K, p.Kr, p.Er, p.E, p.claim, p.pos, p.hdr);
     }
     route_scan_kernel<<<1, 1024, 0, s>>>(p.E, p.claim, p.counts, p.offsets, p.pad_off, p.tile_off, p.pool_src, p.hdr,
                                          counts_out, offsets_out);
     if (n_ids > 0) {
-        route_scatter_kernel<<<(n_ids + 255) / 256, 256, 0, s>>>(topk_ids, n_ids, p.E, p.pos, p.offsets, p.pad_off,
-                                                                 p.row_src, p.pool_src, p.slot_row, row_src_out);
+        route_scatter_kernel<<<(n_ids + 255) / 256, 256, 0, s>>>(topk_ids, n_ids, p.K, p.Kr, p.Er, p.E, p.pos,
+                                                                 p.offsets, p.pad_off, p.row_src, p.pool_src,
+                                                                 p.slot_row, row_src_out);
     }
     return cudaGetLastError();
 }
@@ -519,6 +543,13 @@ cudaError_t launch_debug_wait(const Plan& p, uint64_t timeout_ns, cudaStream_t s
     cudaError_t e = cudaMemsetAsync(p.hdr, 0, sizeof(int32_t) * kHeaderInts, s);
     if (e != cudaSuccess) return e;
     debug_wait_kernel<<<1, 1, 0, s>>>(p.hdr, timeout_ns);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_expand_gates(const Plan& p, const float* topk_weights, cudaStream_t s) {
+    const int n = p.T * p.K;
+    if (n == 0) return cudaSuccess;
+    expand_gates_kernel<<<(n + 255) / 256, 256, 0, s>>>(topk_weights, n, p.K, p.Kr, p.gates);
     return cudaGetLastError();
 }
 

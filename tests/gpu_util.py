@@ -13,17 +13,18 @@ def lib():
     return moe
 
 
-def run_forward(moe, wl, inp, flags=0, stages=False):
-    """One forward pass; returns y (and, with stages=True, the plan and workspace views)."""
+def run_forward(moe, wl, inp, flags=0, stages=False, shared=0):
+    """One forward pass; returns y (and, with stages=True, the plan and workspace views).
+    With shared > 0 the weights hold wl.E routed experts followed by the shared ones."""
     dev = inp["topk_ids"].device
-    d = moe.dims(wl.T, wl.H, wl.I, wl.E, wl.K)
+    d = moe.dims(wl.T, wl.H, wl.I, wl.E, wl.K, shared)
     ws = moe.alloc_workspace(d, wl.mode, dev)
     y = torch.full((wl.T, wl.H), float("nan"), dtype=torch.bfloat16, device=dev)
     if stages:
-        E = wl.E
+        E, K = wl.E + shared, wl.K + shared  # the plan covers the shared experts' slots too
         counts = torch.full((E,), -7, dtype=torch.int32, device=dev)
         offsets = torch.full((E + 1,), -7, dtype=torch.int32, device=dev)
-        row_src = torch.full((max(wl.T * wl.K, 1),), -7, dtype=torch.int32, device=dev)
+        row_src = torch.full((max(wl.T * K, 1),), -7, dtype=torch.int32, device=dev)
         moe.moe_plan(inp["topk_ids"], d, ws, counts, offsets, row_src)
         moe.moe_dispatch(inp["x"], inp["x_scale"], d, wl.mode, ws)
         moe.moe_expert_l1(inp["w1"], inp["w1_scale"], d, wl.mode, ws, flags)
@@ -36,7 +37,7 @@ def run_forward(moe, wl, inp, flags=0, stages=False):
     out = {"y": y, "status": status, "ws": ws, "d": d}
     if stages:
         L = moe.moe_workspace_layout(d, wl.mode)
-        out.update(counts=counts, offsets=offsets, row_src=row_src[:wl.T * wl.K], layout=L)
+        out.update(counts=counts, offsets=offsets, row_src=row_src[:wl.T * (wl.K + shared)], layout=L)
     return out
 
 

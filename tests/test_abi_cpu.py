@@ -74,6 +74,30 @@ def test_workspace_layout(moe, cfg, mode):
         assert L[k] % 256 == 0
 
 
+@pytest.mark.parametrize("shared", [1, 3])
+def test_workspace_layout_with_shared_experts(moe, shared):
+    """S shared experts: the plan regions cover E + S experts and T*(K+S) slots, and the gate
+    region holds T*(K+S) fp32 values."""
+    T, H, I, E, K = 64, 256, 128, 8, 2
+    d = moe.dims(T, H, I, E, K, shared)
+    L = moe.moe_workspace_layout(d, "a16w16")
+    Et, Kt = E + shared, K + shared
+    R = T * Kt
+    assert L["pool_rows"] == R + min(Et, R) * 127
+    regions = {"counts": 4 * Et, "offsets": 4 * (Et + 1), "row_src": 4 * R, "slot_row": 4 * R, "gates": 4 * R,
+               "pool_src": 4 * L["pool_rows"], "comb": 2 * R * H, "x_pool": 2 * L["pool_rows"] * H}
+    spans = sorted((L[k], L[k] + n) for k, n in regions.items())
+    for (a0, a1), (b0, b1) in zip(spans, spans[1:]):
+        assert a1 <= b0
+    assert L["gates"] > 0 and moe.moe_workspace_layout(moe.dims(T, H, I, E, K), "a16w16")["gates"] >= 0
+    assert moe.moe_workspace_bytes(d, "a16w16") > moe.moe_workspace_bytes(moe.dims(T, H, I, E, K), "a16w16")
+
+
+@pytest.mark.parametrize("bad", [(1, 256, 128, 8, 2, -1), (1, 256, 128, 8, 30, 3), (1, 256, 128, 1022, 2, 3)])
+def test_shared_expert_limits(moe, bad):
+    assert moe.moe_workspace_bytes(moe.dims(*bad), "a16w16") == 0
+
+
 @pytest.mark.parametrize("bad", [(1, 100, 128, 8, 2), (1, 256, 96, 8, 2), (1, 256, 128, 8, 0),
                                  (1, 256, 128, 8, 33), (1, 256, 128, 2000, 2), (1, 256, 128, 2, 4),
                                  (-1, 256, 128, 8, 2)])

@@ -530,3 +530,64 @@ def test_activation_clamp_rejects_bad_values(moe):
     moe.moe_forward_ex(inp["x"], None, inp["topk_ids"], inp["topk_weights"], inp["w1"], None, inp["w2"], None, y, d,
                        wl.mode, ws)
     assert torch.equal(y.view(torch.int16), y0.view(torch.int16))
+
+
+# ---------------------------------------------------------------------------------------
+# Shared experts (DeepGEMM page §6): every token, weight 1, the slot after the routed ones
+# ---------------------------------------------------------------------------------------
+
+SHARED_CASES = [(m, w) for m, w in ALL if w.name in ("tiny_bf16", "ragged_bf16", "ragged_fp8", "ragged_int8",
+                                                      "ragged_w4", "ragged_fp4", "skew_fp4", "n224_fp8")]
+
+
+@pytest.mark.parametrize("mode,wl", SHARED_CASES, ids=[f"{m}-{w.name}" for m, w in SHARED_CASES])
+@pytest.mark.parametrize("shared", [1, 2])
+@pytest.mark.parametrize("flags", [0, 1], ids=["default", "simt"])
+def test_shared_experts_match_oracle(moe, mode, wl, shared, flags):
+    inp = make_inputs(wl, device=DEV, shared=shared)
+    out = run_forward(moe, wl, inp, flags=flags, stages=True, shared=shared)
+    assert out["status"] == 0
+    h = to_numpy(inp)
+    ids_ext, _ = omoe.with_shared_slots(h["topk_ids"], h["topk_weights"], wl.E, shared)
+    counts, offsets, row_src = omoe.plan(ids_ext, wl.E + shared)
+    assert out["counts"].cpu().numpy().tolist() == counts.tolist()
+    assert counts[wl.E:].tolist() == [wl.T] * shared
+    assert out["offsets"].cpu().numpy().tolist() == offsets.tolist()
+    got = out["row_src"].cpu().numpy()
+    assert sorted(got.tolist()) == sorted(row_src.tolist())
+    ref = omoe.forward(mode, h["x"], h["x_scale"], h["topk_ids"], h["topk_weights"], h["w1"], h["w1_scale"],
+                       h["w2"], h["w2_scale"], num_experts=wl.E, inter=wl.I, num_shared=shared)
+    assert_close(y_numpy(out["y"]), ref, mode)
+
+
+def test_shared_experts_with_masked_routes_and_quantizing_dispatch(moe):
+    """Every routed slot of half the tokens masked: those tokens get the shared experts alone;
+    the quantising dispatch (row f1) feeds the shared experts' pool rows too."""
+    wl = CASES["a8w8_int8"][1]
+    inp = make_inputs(wl, device=DEV, shared=1)
+    inp["topk_ids"][: wl.T // 2] = -1
+    d = moe.dims(wl.T, wl.H, wl.I, wl.E, wl.K, 1)
+    ws = moe.alloc_workspace(d, wl.mode, DEV)
+    y = torch.full((wl.T, wl.H), float("nan"), dtype=torch.bfloat16, device=DEV)
+    moe.moe_forward(inp["x_bf16"], None, inp["topk_ids"], inp["topk_weights"], inp["w1"], inp["w1_scale"], inp["w2"],
+                    inp["w2_scale"], y, d, wl.mode, ws, moe.MOE_FLAG_QUANTIZE_X)
+    assert moe.moe_check_device_error(ws) == 0
+    h = to_numpy(inp)
+    qx, sx = omoe.quantize_x(wl.mode, h["x_bf16"])
+    ref = omoe.forward(wl.mode, qx, sx, h["topk_ids"], h["topk_weights"], h["w1"], h["w1_scale"], h["w2"],
+                       h["w2_scale"], num_experts=wl.E, inter=wl.I, num_shared=1)
+    assert_close(y_numpy(y), ref, wl.mode)
+
+
+def test_routed_id_naming_a_shared_expert_is_a_bad_route(moe):
+    wl = CASES["a16w16"][0]
+    inp = make_inputs(wl, device=DEV, shared=1)
+    inp["topk_ids"][0, 0] = wl.E  # the shared expert's index: not a routed expert
+    out = run_forward(moe, wl, inp, shared=1)
+    assert out["status"] == 4  # MOE_ERR_BAD_ROUTE
+    ids = inp["topk_ids"].clone()
+    ids[0, 0] = -1  # the kernel skipped the bad route: same as a masked one
+    h = to_numpy(dict(inp, topk_ids=ids))
+    ref = omoe.forward(wl.mode, h["x"], h["x_scale"], h["topk_ids"], h["topk_weights"], h["w1"], h["w1_scale"],
+                       h["w2"], h["w2_scale"], num_experts=wl.E, inter=wl.I, num_shared=1)
+    assert_close(y_numpy(out["y"]), ref, wl.mode)
