@@ -11,6 +11,8 @@ name:
 * BFLOAT16: the upper 16 bits of an IEEE binary32 value.
 * FLOAT8_E4M3FN: 1 sign, 4 exponent bits (bias 7), 3 mantissa bits, no infinities,
   NaN only at S.1111.111, largest finite 448.
+* FLOAT8_E5M2: 1 sign, 5 exponent bits (bias 15), 2 mantissa bits, IEEE-style: exponent field
+  31 holds the infinities (mantissa 0) and NaNs; largest finite 1.75 * 2^15 = 57344.
 * FLOAT4_E2M1 (packed two per byte): 1 sign, 2 exponent bits (bias 1), 1 mantissa bit;
   magnitudes {0, 0.5, 1, 1.5, 2, 3, 4, 6}.
 * FLOAT8_E8M0 / UE8M0 scale: unsigned exponent byte s meaning 2^(s-127); 255 is NaN.
@@ -112,6 +114,53 @@ def e4m3_encode_rne_satfinite(v: np.ndarray) -> np.ndarray:
     code = np.where(pick_hi, hi, lo).astype(np.uint8)
     sign = np.signbit(v).astype(np.uint8) << np.uint8(7)
     return code | sign
+
+
+# ---------------------------------------------------------------------------------------
+# float8 e5m2
+# ---------------------------------------------------------------------------------------
+
+
+def _e5m2_table() -> np.ndarray:
+    """Value of each of the 256 e5m2 codes, built from the field definition."""
+    t = np.empty(256, dtype=np.float64)
+    for c in range(256):
+        s = -1.0 if (c >> 7) & 1 else 1.0
+        e = (c >> 2) & 0x1F
+        m = c & 0x3
+        if e == 0x1F:
+            t[c] = s * np.inf if m == 0 else np.nan
+        elif e == 0:
+            t[c] = s * (m / 4.0) * 2.0 ** (1 - 15)  # subnormal
+        else:
+            t[c] = s * (1.0 + m / 4.0) * 2.0 ** (e - 15)
+    return t
+
+
+E5M2_VALUES = _e5m2_table()
+E5M2_MAX = 57344.0
+
+
+def e5m2_decode(codes: np.ndarray) -> np.ndarray:
+    return E5M2_VALUES[np.asarray(codes, dtype=np.uint8)]
+
+
+# Non-negative finite e5m2 magnitudes in code order 0x00..0x7B (increasing with the code).
+_E5M2_POS = E5M2_VALUES[:0x7C]
+
+
+def e5m2_encode_rne_satfinite(v: np.ndarray) -> np.ndarray:
+    """Round float64 values to the nearest e5m2 code, ties to the even code, magnitudes above
+    57344 clamped to 57344 (saturating finite conversion); the sign is kept, also on zero."""
+    v = np.asarray(v, dtype=np.float64)
+    mag = np.minimum(np.abs(v), E5M2_MAX)
+    hi = np.minimum(np.searchsorted(_E5M2_POS, mag, side="left"), 0x7B)
+    lo = np.maximum(hi - 1, 0)
+    d_lo = mag - _E5M2_POS[lo]
+    d_hi = _E5M2_POS[hi] - mag
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo).astype(np.uint8)
+    return code | (np.signbit(v).astype(np.uint8) << np.uint8(7))
 
 
 # ---------------------------------------------------------------------------------------

@@ -35,7 +35,10 @@ import numpy as np
 
 from . import codecs
 
-MODES = ("a16w16", "a8w8_fp8", "a8w8_int8", "a8w4_fp8_fp4", "a8w4_int")
+MODES = ("a16w16", "a8w8_fp8", "a8w8_int8", "a8w4_fp8_fp4", "a8w4_int", "a8w8_fp8_e5m2")
+# the FP8 element format of each A8W8-FP mode (p1 A8W8-FP: FLOAT8_E4M3FN or FLOAT8_E5M2; x, both
+# weights and the re-quantised A take the same type)
+FP8_FORMAT = {"a8w8_fp8": "e4m3", "a8w8_fp8_e5m2": "e5m2"}
 INT_MODES = ("a8w8_int8", "a8w4_int")  # integer GEMMs with per-token / per-channel fp32 scales
 
 
@@ -82,6 +85,10 @@ def plan(topk_ids: np.ndarray, num_experts: int):
 # ---------------------------------------------------------------------------------------
 
 
+def fp8_decode(fmt: str, codes: np.ndarray) -> np.ndarray:
+    return codecs.e4m3_decode(codes) if fmt == "e4m3" else codecs.e5m2_decode(codes)
+
+
 def decode_x(mode: str, x: np.ndarray, x_scale: np.ndarray | None) -> np.ndarray:
     """Activations [T, H] as exact float64 values.
 
@@ -91,11 +98,12 @@ def decode_x(mode: str, x: np.ndarray, x_scale: np.ndarray | None) -> np.ndarray
                    the int8 path keeps q and s^X apart (p1 A8W8-INT).
     a8w4_fp8_fp4 : x e4m3 codes, x_scale fp32 [T, H/128] (1x128 blocks).
     a8w4_int     : as a8w8_int8 (p1 A8W4-INT: the same per-token int8 quantisation of X).
+    a8w8_fp8_e5m2: as a8w8_fp8 with e5m2 codes.
     """
     if mode == "a16w16":
         return codecs.bf16_decode(x)
-    if mode == "a8w8_fp8":
-        v = codecs.e4m3_decode(x)
+    if mode in FP8_FORMAT:
+        v = fp8_decode(FP8_FORMAT[mode], x)
         s = np.repeat(codecs.ue8m0_decode(x_scale), 32, axis=-1)
         return v * s
     if mode in INT_MODES:
@@ -118,11 +126,12 @@ def decode_weight(mode: str, w: np.ndarray, w_scale: np.ndarray | None, e: int) 
     a8w4_fp8_fp4 : w e2m1 packed [E, N_out, K_in/2] with UE8M0 scales [E, N_out, K_in/32].
     a8w4_int     : w signed int4 packed [E, N_out, K_in/2] (element 2j in the low nibble);
                    returns the integer codes (per-output-channel fp32 scale as for a8w8_int8).
+    a8w8_fp8_e5m2: as a8w8_fp8 with e5m2 codes.
     """
     if mode == "a16w16":
         return codecs.bf16_decode(w[e])
-    if mode == "a8w8_fp8":
-        v = codecs.e4m3_decode(w[e]) * np.repeat(codecs.ue8m0_decode(w_scale[e]), 32, axis=-1)
+    if mode in FP8_FORMAT:
+        v = fp8_decode(FP8_FORMAT[mode], w[e]) * np.repeat(codecs.ue8m0_decode(w_scale[e]), 32, axis=-1)
         return v.T
     if mode == "a8w8_int8":
         return np.asarray(w[e], dtype=np.int8).astype(np.float64).T
@@ -189,19 +198,22 @@ def mx_scale_exponent(amax32: np.ndarray, elem_max: float) -> np.ndarray:
     return out
 
 
-def quant_mx_fp8(a: np.ndarray, block: int = 32):
-    """MX quantisation with 1 x `block` groups along the last axis to e4m3 + a shared
-    power-of-two exponent (p1 A8W8-FP "Q_MX", group size 32; DeepGEMM §4 step 6 FP8
-    re-quantisation). The decision runs on fp32 values: a -> fp32, per-group amax, exponent e,
-    codes = e4m3_rne_satfinite(a / 2^e).
+def quant_mx_fp8(a: np.ndarray, block: int = 32, fmt: str = "e4m3"):
+    """MX quantisation with 1 x `block` groups along the last axis to an FP8 format (e4m3 or
+    e5m2) + a shared power-of-two exponent (p1 A8W8-FP "Q_MX", group size 32, target type
+    FLOAT8_E4M3FN or FLOAT8_E5M2; DeepGEMM §4 step 6 FP8 re-quantisation). The decision runs on
+    fp32 values: a -> fp32, per-group amax, exponent e = the smallest with amax <= max * 2^e
+    (max = the format's largest finite value), codes = rne_satfinite(a / 2^e).
     Returns (codes uint8 [n, m], exponents as UE8M0 bytes uint8 [n, m/block])."""
     a32 = np.asarray(a, dtype=np.float64).astype(np.float32).astype(np.float64)
     n, m = a32.shape
     blocks = a32.reshape(n, m // block, block)
     amax = np.max(np.abs(blocks), axis=2)
-    e = mx_scale_exponent(amax, codecs.E4M3_MAX)
+    elem_max = codecs.E4M3_MAX if fmt == "e4m3" else codecs.E5M2_MAX
+    encode = codecs.e4m3_encode_rne_satfinite if fmt == "e4m3" else codecs.e5m2_encode_rne_satfinite
+    e = mx_scale_exponent(amax, elem_max)
     scaled = blocks / np.ldexp(1.0, e.astype(np.int32))[:, :, None]
-    codes = codecs.e4m3_encode_rne_satfinite(scaled).reshape(n, m)
+    codes = encode(scaled).reshape(n, m)
     return codes, (e + 127).astype(np.uint8)
 
 
@@ -212,7 +224,7 @@ def quantize_x(mode: str, x_bf16: np.ndarray):
         s_i = max|X[i,:]| / 127 and q_i = round(X[i,:] / s_i), as quant_int8_rows (fp32
         decision, scale floored at 1e-8);
       * A8W8-FP (p1 "A8W8-FP Quantization Use Case", first phase): Q_MX with groups of 32,
-        e4m3 codes and E8M0 scales;
+        e4m3 (or, for a8w8_fp8_e5m2, e5m2) codes and E8M0 scales;
       * FP8 activations x FP4 weights: the same shared-exponent rule on groups of 128 gives the
         mode's x format, e4m3 codes with power-of-two fp32 scales (the DeepGEMM page takes
         FP8 activations with their scales as the input of fp8_fp4_mega_moe).
@@ -224,8 +236,8 @@ def quantize_x(mode: str, x_bf16: np.ndarray):
     xv = codecs.bf16_decode(x)
     if mode in INT_MODES:
         return quant_int8_rows(xv)
-    if mode == "a8w8_fp8":
-        return quant_mx_fp8(xv, 32)
+    if mode in FP8_FORMAT:
+        return quant_mx_fp8(xv, 32, FP8_FORMAT[mode])
     if mode == "a8w4_fp8_fp4":
         codes, sb = quant_mx_fp8(xv, 128)
         return codes, np.ldexp(np.float32(1.0), sb.astype(np.int32) - 127).astype(np.float32)
@@ -237,9 +249,10 @@ def l2_operand(mode: str, a: np.ndarray):
     if mode == "a16w16":
         v = codecs.round_to_bf16(a)
         return v, {"a": codecs.bf16_encode(v)}
-    if mode in ("a8w8_fp8", "a8w4_fp8_fp4"):
-        codes, sc = quant_mx_fp8(a)
-        v = codecs.e4m3_decode(codes) * np.repeat(codecs.ue8m0_decode(sc), 32, axis=1)
+    if mode in ("a8w8_fp8", "a8w4_fp8_fp4", "a8w8_fp8_e5m2"):
+        fmt = FP8_FORMAT.get(mode, "e4m3")  # FP8 x FP4 re-quantises A to e4m3 (DeepGEMM §4 step 6)
+        codes, sc = quant_mx_fp8(a, 32, fmt)
+        v = fp8_decode(fmt, codes) * np.repeat(codecs.ue8m0_decode(sc), 32, axis=1)
         return v, {"a": codes, "a_scale": sc}
     if mode in INT_MODES:
         q, s = quant_int8_rows(a)

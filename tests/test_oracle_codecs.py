@@ -48,6 +48,60 @@ def test_e4m3_encode_saturates():
     assert codecs.e4m3_encode_rne_satfinite(np.array([-500.0]))[0] == 0xFE
 
 
+def test_e5m2_table_matches_definition_landmarks():
+    t = codecs.E5M2_VALUES
+    assert t[0x00] == 0.0 and t[0x80] == 0.0
+    assert t[0x01] == 2.0 ** -16          # smallest subnormal: 1/4 * 2^-14
+    assert t[0x04] == 2.0 ** -14          # smallest normal
+    assert t[0x3C] == 1.0                 # exponent field 15 = bias
+    assert t[0x7B] == 57344.0             # largest finite: 1.75 * 2^15
+    assert t[0x7C] == math.inf and t[0xFC] == -math.inf
+    assert math.isnan(t[0x7D]) and math.isnan(t[0xFF])
+
+
+def test_e5m2_table_matches_torch_for_every_code():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e5m2).to(torch.float64).numpy()
+    ours = codecs.E5M2_VALUES
+    both_nan = np.isnan(ref) & np.isnan(ours)
+    assert np.all(both_nan | (ref == ours))
+
+
+def test_e5m2_encode_matches_torch_rne():
+    rng = np.random.default_rng(8)
+    pos = codecs.E5M2_VALUES[:0x7C]
+    v = np.concatenate([rng.standard_normal(20000) * 3000, rng.standard_normal(2000) * 1e-4, pos, -pos[1:]])
+    mids = (pos[1:] + pos[:-1]) / 2  # ties go to the even code
+    tiny = np.array([2.0 ** -17, 2.0 ** -18, 1e-9, 0.0])
+    v = np.concatenate([v, mids, -mids, tiny, -tiny])
+    v = np.clip(v, -57344, 57344).astype(np.float32).astype(np.float64)
+    ref = torch.from_numpy(v).to(torch.float32).to(torch.float8_e5m2).view(torch.uint8).numpy()
+    assert np.array_equal(codecs.e5m2_encode_rne_satfinite(v), ref)
+
+
+def test_e5m2_encode_saturates_to_the_largest_finite():
+    # (torch's own conversion overflows to infinity; the satfinite rule clamps)
+    assert codecs.e5m2_encode_rne_satfinite(np.array([1e9]))[0] == 0x7B
+    assert codecs.e5m2_encode_rne_satfinite(np.array([-61440.0]))[0] == 0xFB
+
+
+def test_mx_e5m2_quant_properties():
+    rng = np.random.default_rng(9)
+    a = rng.standard_normal((6, 128)) * np.exp(rng.standard_normal((6, 1)) * 4)
+    a[0] = 0.0
+    codes, sc = moe.quant_mx_fp8(a, 32, "e5m2")
+    vals = codecs.e5m2_decode(codes) * np.repeat(codecs.ue8m0_decode(sc), 32, axis=1)
+    assert np.all(vals[0] == 0.0) and np.all(sc[0] == 0)
+    blocks = np.abs(a.astype(np.float32).astype(np.float64)).reshape(6, 4, 32).max(axis=2)
+    e = sc.astype(np.int64) - 127
+    ratio = blocks[1:] / np.ldexp(1.0, e[1:])
+    # the largest element of a block lands in the top binade of e5m2: (28672, 57344]
+    assert np.all(ratio > 28672) and np.all(ratio <= 57344)
+    # relative rounding error of e5m2 (2 mantissa bits) is at most 2^-3 of the value's binade
+    err = np.abs(vals[1:] - a[1:]) / np.maximum(np.abs(a[1:]), 2.0 ** -14 * np.ldexp(1.0, np.repeat(e[1:], 32, axis=1)))
+    assert err.max() <= 2.0 ** -3 + 1e-12
+
+
 def test_e2m1_table_is_the_format():
     mags = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
     assert list(codecs.E2M1_VALUES[:8]) == mags
@@ -214,3 +268,17 @@ def test_int32_accumulator_guard():
     q = np.full((1, 5120), -127, dtype=np.int8)
     w = np.full((5120, 1), 127, dtype=np.int8)
     assert moe._int_matmul_checked(q, w)[0, 0] == -5120 * 127 * 127
+
+
+def test_quantize_x_e5m2_round_trip_and_zero_groups():
+    """A8W8-FP with the E5M2 target type (p1 Q_MX): values that are e5m2 codes times the group's
+    power of two come back exactly; a group of zeros gets scale byte 0 and zero codes."""
+    block = 32
+    top = codecs.e5m2_decode(np.arange(0x5C, 0x7C, dtype=np.uint8))  # 32 codes up to 57344
+    exact = np.tile(top, (1, 4)) * 2.0 ** -10   # fits bf16: 3 significant bits
+    x = np.concatenate([exact, np.zeros((1, 128))])
+    codes, sc = moe.quantize_x("a8w8_fp8_e5m2", _bf16(x))
+    assert codes.dtype == np.uint8 and sc.shape == (2, 4)
+    assert np.all(sc[0] == 127 - 10) and np.all(sc[1] == 0) and np.all(codes[1] == 0)
+    back = codecs.e5m2_decode(codes[0]) * 2.0 ** -10
+    assert np.array_equal(back, codecs.bf16_decode(_bf16(exact))[0])

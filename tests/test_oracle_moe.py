@@ -137,6 +137,7 @@ TINY = {
     "a8w8_int8": Workload("t", "a8w8_int8", 12, 96, 64, 4, 3, 13, 0.1),
     "a8w4_fp8_fp4": Workload("t", "a8w4_fp8_fp4", 12, 128, 64, 4, 2, 14, 0.1),
     "a8w4_int": Workload("t", "a8w4_int", 12, 96, 64, 4, 3, 15, 0.1),
+    "a8w8_fp8_e5m2": Workload("t", "a8w8_fp8_e5m2", 12, 128, 64, 4, 2, 16, 0.1),
 }
 
 

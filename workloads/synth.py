@@ -22,6 +22,9 @@ Storage formats per mode (x, w1, w2 and their scales; row-major, contiguous):
   a8w4_fp8_fp4 : x e4m3 [T,H] + fp32 power-of-two scales [T,H/128];
                  w1 e2m1 packed [E,2I,H/2] + UE8M0 [E,2I,H/32];
                  w2 e2m1 packed [E,H,I/2] + UE8M0 [E,H,I/32]; low nibble = even element.
+  a8w4_int     : x as a8w8_int8; w1 int4 packed [E,2I,H/2] + fp32 [E,2I]; w2 int4 packed
+                 [E,H,I/2] + fp32 [E,H] (per-output-channel symmetric, [-7,7]).
+  a8w8_fp8_e5m2: as a8w8_fp8 with e5m2 codes.
 """
 from __future__ import annotations
 
@@ -29,7 +32,7 @@ import dataclasses
 
 import torch
 
-MODES = ("a16w16", "a8w8_fp8", "a8w8_int8", "a8w4_fp8_fp4")
+MODES = ("a16w16", "a8w8_fp8", "a8w8_int8", "a8w4_fp8_fp4", "a8w4_int", "a8w8_fp8_e5m2")
 
 
 @dataclasses.dataclass(frozen=True)
@@ -108,14 +111,15 @@ def _pow2_ceil_exponent(amax: torch.Tensor, elem_max: float) -> torch.Tensor:
     return e.clamp(-127, 127).to(torch.int32)
 
 
-def to_e4m3_blocks(v: torch.Tensor, block: int):
-    """Power-of-two block scales along the last axis, then e4m3 codes (RNE).
+def to_e4m3_blocks(v: torch.Tensor, block: int, fmt: str = "e4m3"):
+    """Power-of-two block scales along the last axis, then e4m3 (or e5m2) codes (RNE).
     Returns (codes uint8, exponent int32 [..., n/block])."""
     shp = v.shape
     b = v.float().reshape(*shp[:-1], shp[-1] // block, block)
-    e = _pow2_ceil_exponent(b.abs().amax(dim=-1), 448.0)
+    top, dt = (448.0, torch.float8_e4m3fn) if fmt == "e4m3" else (57344.0, torch.float8_e5m2)
+    e = _pow2_ceil_exponent(b.abs().amax(dim=-1), top)
     scaled = b / torch.ldexp(torch.ones_like(e, dtype=torch.float32), e.float())[..., None]
-    codes = scaled.clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+    codes = scaled.clamp(-top, top).to(dt).view(torch.uint8)
     return codes.reshape(shp), e
 
 
@@ -198,15 +202,16 @@ def make_inputs(wl: Workload, device="cpu", mode: str | None = None, shared: int
         for e in range(E):
             w2[e] = (torch.randn((I, H), generator=g, device=device) * wl.w_std).to(torch.bfloat16)
         out.update(w1=w1, w1_scale=None, w2=w2, w2_scale=None)
-    elif mode == "a8w8_fp8":
-        xc, xe = to_e4m3_blocks(x, 32)
+    elif mode in ("a8w8_fp8", "a8w8_fp8_e5m2"):
+        fmt = "e4m3" if mode == "a8w8_fp8" else "e5m2"
+        xc, xe = to_e4m3_blocks(x, 32, fmt)
         out["x"], out["x_scale"] = xc, (xe + 127).to(torch.uint8)
         for name, (n_out, k_in) in (("w1", (2 * I, H)), ("w2", (H, I))):
             codes = torch.empty((E, n_out, k_in), device=device, dtype=torch.uint8)
             sc = torch.empty((E, n_out, k_in // 32), device=device, dtype=torch.uint8)
             for e in range(E):
                 w = torch.randn((n_out, k_in), generator=g, device=device) * wl.w_std
-                c, ex = to_e4m3_blocks(w, 32)
+                c, ex = to_e4m3_blocks(w, 32, fmt)
                 codes[e], sc[e] = c, (ex + 127).to(torch.uint8)
             out[name], out[name + "_scale"] = codes, sc
     elif mode == "a8w8_int8":
