@@ -30,8 +30,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "fused MoE FFN TFLOP/s + routed rows/s, % of tensor/HBM roofline, 1xGB300"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-DTYPE = {"a16w16": "bf16", "a8w8_fp8": "e4m3", "a8w8_int8": "int8", "a8w4_fp8_fp4": "e4m3xe2m1", "a8w4_int": "int8xint4"}
-LAUNCHES_PER_STEP = {"a16w16": 7, "a8w8_fp8": 7, "a8w8_int8": 8, "a8w4_fp8_fp4": 7, "a8w4_int": 8}
+DTYPE = {"a16w16": "bf16", "a8w8_fp8": "e4m3", "a8w8_int8": "int8", "a8w4_fp8_fp4": "e4m3xe2m1", "a8w4_int": "int8xint4", "a8w8_fp8_e5m2": "e5m2"}
+LAUNCHES_PER_STEP = {"a16w16": 7, "a8w8_fp8": 7, "a8w8_int8": 8, "a8w4_fp8_fp4": 7, "a8w4_int": 8, "a8w8_fp8_e5m2": 7}
 
 
 def parse():

@@ -76,6 +76,8 @@ typedef enum {
  *                   MSD split of the activations and its offline bias 8 * (1^T W) are one way
  *                   to reach the exact integer product Q . W; the library computes that product
  *                   directly, so no bias input exists (the page's A8W4-INT use case).
+ * MOE_A8W8_FP8_E5M2 as MOE_A8W8_FP8 with FLOAT8_E5M2 codes for x, w1, w2 and the re-quantised
+ *                   A (the page's A8W8-FP use case with the E5M2 target type).
  * In every mode the gate columns of w1 are the first I outputs and the up columns the
  * last I; y is bf16 [T,H]. */
 typedef enum {
@@ -83,7 +85,8 @@ typedef enum {
     MOE_A8W8_FP8 = 1,
     MOE_A8W8_INT8 = 2,
     MOE_A8W4_FP8_FP4 = 3,
-    MOE_A8W4_INT = 4
+    MOE_A8W4_INT = 4,
+    MOE_A8W8_FP8_E5M2 = 5
 } moe_dtype_mode;
 
 typedef struct {
@@ -163,8 +166,8 @@ MOE_API moe_status moe_dispatch_quantize(const void* x_bf16, const moe_dims* d, 
  * (Ascend page: "Linear1 Projection", "SwiGLU Activation", and the A8W8 activation
  * quantisation of "Linear2"; DeepGEMM page §4 step 6). Needs moe_dispatch first.
  *   w1  device operand in the mode's w1 format. Writes the L2 operand A into the workspace:
- *       bf16 (A16W16), e4m3 + UE8M0 per 1x32 (both FP8 modes), int8 + fp32 per row (INT8,
- *       A8W4-INT). */
+ *       bf16 (A16W16), e4m3 + UE8M0 per 1x32 (A8W8_FP8, A8W4_FP8_FP4), e5m2 + UE8M0 per 1x32
+ *       (A8W8_FP8_E5M2), int8 + fp32 per row (INT8, A8W4-INT). */
 MOE_API moe_status moe_expert_l1(moe_operand w1, const moe_dims* d, moe_dtype_mode m, uint32_t flags,
                          void* workspace, size_t workspace_bytes, moe_stream_t stream);
 

@@ -14,7 +14,8 @@ int x_elem_bytes(int mode) { return mode == MOE_A16W16 ? 2 : 1; }
 
 int64_t x_scale_row_bytes(int mode, int H) {
     switch (mode) {
-        case MOE_A8W8_FP8: return H / 32;                // UE8M0 per 1x32
+        case MOE_A8W8_FP8:
+        case MOE_A8W8_FP8_E5M2: return H / 32;           // UE8M0 per 1x32
         case MOE_A8W8_INT8:
         case MOE_A8W4_INT: return 4;                     // fp32 per token
         case MOE_A8W4_FP8_FP4: return (int64_t)(H / 128) * 4;  // fp32 per 1x128
@@ -27,6 +28,7 @@ int a_elem_bytes(int mode) { return mode == MOE_A16W16 ? 2 : 1; }
 int64_t a_scale_row_bytes(int mode, int I) {
     switch (mode) {
         case MOE_A8W8_FP8:
+        case MOE_A8W8_FP8_E5M2:
         case MOE_A8W4_FP8_FP4: return I / 32;            // UE8M0 per 1x32
         case MOE_A8W8_INT8:
         case MOE_A8W4_INT: return 4;                     // fp32 per row
@@ -36,7 +38,7 @@ int64_t a_scale_row_bytes(int mode, int I) {
 
 static bool dims_ok(const moe_dims* d, moe_dtype_mode m) {
     if (!d) return false;
-    if (m < MOE_A16W16 || m > MOE_A8W4_INT) return false;
+    if (m < MOE_A16W16 || m > MOE_A8W8_FP8_E5M2) return false;
     const int S = d->num_shared_experts;
     if (d->num_tokens < 0 || d->topk < 1 || S < 0 || d->topk + S > 32) return false;
     if (d->num_experts < d->topk || d->num_experts + S > 1024) return false;

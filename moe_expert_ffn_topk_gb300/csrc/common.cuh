@@ -81,6 +81,43 @@ __device__ __forceinline__ int mx_exponent_e4m3(float amax) {
     return e > 127 ? 127 : e;
 }
 
+// e5m2 code -> float (exact), via the fp8 conversion of cuda_fp8.h
+__device__ __forceinline__ float e5m2_to_float(uint8_t c) {
+    __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(c), __NV_E5M2);
+    return __half2float(__half(h));
+}
+
+// float -> e5m2 code, round to nearest even, saturating to +-57344 (the PTX conversion)
+__device__ __forceinline__ uint8_t float_to_e5m2_satfinite(float v) {
+    uint16_t pair;
+    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(0.0f), "f"(v));
+    return static_cast<uint8_t>(pair & 0xffu);
+}
+
+// Shared exponent of an MX block for e5m2: the smallest e with amax <= 57344 * 2^e. As
+// 57344 = 448 * 2^7 this is the e4m3 exponent minus 7 (clamped to [-127, 127] the same way).
+__device__ __forceinline__ int mx_exponent_e5m2(float amax) {
+    const int e = mx_exponent_e4m3(amax) - 7;
+    return e < -127 ? -127 : e;
+}
+
+// The FP8 element type of an A8W8-FP mode: e5m2 when kE5, else e4m3.
+template <bool kE5>
+__device__ __forceinline__ float fp8_to_float(uint8_t c) {
+    if constexpr (kE5) return e5m2_to_float(c);
+    else return e4m3_to_float(c);
+}
+template <bool kE5>
+__device__ __forceinline__ uint8_t float_to_fp8_satfinite(float v) {
+    if constexpr (kE5) return float_to_e5m2_satfinite(v);
+    else return float_to_e4m3_satfinite(v);
+}
+template <bool kE5>
+__device__ __forceinline__ int mx_exponent_fp8(float amax) {
+    if constexpr (kE5) return mx_exponent_e5m2(amax);
+    else return mx_exponent_e4m3(amax);
+}
+
 // 2^-e as float for e in [-127, 126] (exact power of two)
 __device__ __forceinline__ float exp2_neg_int(int e) {
     return __uint_as_float(static_cast<uint32_t>(127 - e) << 23);

@@ -351,13 +351,14 @@ __global__ void __launch_bounds__(256) dispatch_quant_kernel(const uint16_t* __r
             } else {
                 float m = fmaxf(fmaxf(fabsf(f[0]), fabsf(f[1])), fmaxf(fabsf(f[2]), fabsf(f[3])));
                 // group of 32 = 8 lanes (A8W8-FP8) or of 128 = the warp (FP8 x FP4)
-                constexpr int kLanes = MODE == MOE_A8W8_FP8 ? 8 : 32;
+                constexpr int kLanes = MODE == MOE_A8W4_FP8_FP4 ? 32 : 8;
+                constexpr bool kE5 = MODE == MOE_A8W8_FP8_E5M2;
 #pragma unroll
                 for (int o = 1; o < kLanes; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-                ex = mx_exponent_e4m3(m);
+                ex = mx_exponent_fp8<kE5>(m);
                 const float inv = exp2_neg_int(ex);
 #pragma unroll
-                for (int c = 0; c < 4; ++c) code |= (uint32_t)float_to_e4m3_satfinite(f[c] * inv) << (8 * c);
+                for (int c = 0; c < 4; ++c) code |= (uint32_t)float_to_fp8_satfinite<kE5>(f[c] * inv) << (8 * c);
             }
             for (int k = 0; k < K; ++k) {
                 const int prow = __shfl_sync(0xffffffffu, my_row, k);
@@ -368,7 +369,7 @@ __global__ void __launch_bounds__(256) dispatch_quant_kernel(const uint16_t* __r
                     reinterpret_cast<uint2*>(xb + (pool_rows + prow) * H + c0)[lane] = make_uint2(lo[0], lo[1]);
                 } else if constexpr (MODE == MOE_A8W4_INT) {
                     reinterpret_cast<uint2*>(xb + (int64_t)prow * H + c0)[lane] = make_uint2(hi[0], hi[1]);
-                } else if constexpr (MODE == MOE_A8W8_FP8) {
+                } else if constexpr (MODE == MOE_A8W8_FP8 || MODE == MOE_A8W8_FP8_E5M2) {
                     if ((lane & 7) == 0) xps[(int64_t)prow * (H / 32) + c0 / 32 + lane / 8] = (uint8_t)(ex + 127);
                 } else {
                     // 2^ex as fp32 (2^-127, a subnormal, for an all-zero group)
@@ -488,6 +489,7 @@ cudaError_t launch_dispatch(const Plan& p, const void* x, const void* x_scale, c
     if (p.T == 0) return cudaSuccess;
     switch (p.mode) {
         case MOE_A8W8_FP8: return dispatch_q<MOE_A8W8_FP8>(p, x, x_scale, s);
+        case MOE_A8W8_FP8_E5M2: return dispatch_q<MOE_A8W8_FP8_E5M2>(p, x, x_scale, s);
         case MOE_A8W8_INT8: return dispatch_q<MOE_A8W8_INT8>(p, x, x_scale, s);
         case MOE_A8W4_INT: return dispatch_q<MOE_A8W4_INT>(p, x, x_scale, s);
         case MOE_A8W4_FP8_FP4: return dispatch_q<MOE_A8W4_FP8_FP4>(p, x, x_scale, s);
@@ -508,6 +510,10 @@ cudaError_t launch_dispatch_quant(const Plan& p, const void* x_bf16, cudaStream_
     const int grid = (int)std::min<int64_t>(p.T, 152 * 8);
     const uint16_t* x = static_cast<const uint16_t*>(x_bf16);
     switch (p.mode) {
+        case MOE_A8W8_FP8_E5M2:
+            dispatch_quant_kernel<MOE_A8W8_FP8_E5M2><<<grid, 256, 0, s>>>(x, p.slot_row, p.T, p.K, p.H, p.pool_rows,
+                                                                          p.x_pool, p.x_pool_scale, p.x_planes, p.x_sums);
+            break;
         case MOE_A8W8_FP8:
             dispatch_quant_kernel<MOE_A8W8_FP8><<<grid, 256, 0, s>>>(x, p.slot_row, p.T, p.K, p.H, p.pool_rows, p.x_pool,
                                                                      p.x_pool_scale, p.x_planes, p.x_sums);

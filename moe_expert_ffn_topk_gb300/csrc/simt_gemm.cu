@@ -45,8 +45,8 @@ template <int MODE>
 __device__ __forceinline__ acc_t<MODE> load_x(const uint8_t* xp, const uint8_t* xs, int H, int64_t p, int k) {
     if constexpr (MODE == MOE_A16W16) {
         return bf16_bits_to_float(reinterpret_cast<const uint16_t*>(xp)[p * H + k]);
-    } else if constexpr (MODE == MOE_A8W8_FP8) {
-        return e4m3_to_float(xp[p * H + k]) * ue8m0_to_float(xs[p * (H / 32) + k / 32]);
+    } else if constexpr (MODE == MOE_A8W8_FP8 || MODE == MOE_A8W8_FP8_E5M2) {
+        return fp8_to_float<MODE == MOE_A8W8_FP8_E5M2>(xp[p * H + k]) * ue8m0_to_float(xs[p * (H / 32) + k / 32]);
     } else if constexpr (int_mode(MODE)) {
         return static_cast<int>(reinterpret_cast<const int8_t*>(xp)[p * H + k]);
     } else {
@@ -62,8 +62,8 @@ __device__ __forceinline__ acc_t<MODE> load_w(const uint8_t* w, const uint8_t* w
     const int64_t en = (int64_t)e * Nout + n;
     if constexpr (MODE == MOE_A16W16) {
         return bf16_bits_to_float(reinterpret_cast<const uint16_t*>(w)[((int64_t)e * Kin + k) * Nout + n]);
-    } else if constexpr (MODE == MOE_A8W8_FP8) {
-        return e4m3_to_float(w[en * Kin + k]) * ue8m0_to_float(ws[en * (Kin / 32) + k / 32]);
+    } else if constexpr (MODE == MOE_A8W8_FP8 || MODE == MOE_A8W8_FP8_E5M2) {
+        return fp8_to_float<MODE == MOE_A8W8_FP8_E5M2>(w[en * Kin + k]) * ue8m0_to_float(ws[en * (Kin / 32) + k / 32]);
     } else if constexpr (MODE == MOE_A8W8_INT8) {
         return static_cast<int>(reinterpret_cast<const int8_t*>(w)[en * Kin + k]);
     } else if constexpr (MODE == MOE_A8W4_INT) {
@@ -84,7 +84,7 @@ __device__ __forceinline__ acc_t<MODE> load_a(const uint8_t* ap, const uint8_t* 
     } else if constexpr (int_mode(MODE)) {
         return static_cast<int>(reinterpret_cast<const int8_t*>(ap)[p * I + j]);
     } else {
-        return e4m3_to_float(ap[p * I + j]) * ue8m0_to_float(as[p * (I / 32) + j / 32]);
+        return fp8_to_float<MODE == MOE_A8W8_FP8_E5M2>(ap[p * I + j]) * ue8m0_to_float(as[p * (I / 32) + j / 32]);
     }
 }
 
@@ -166,9 +166,10 @@ __global__ void __launch_bounds__(NT) l1_simt_kernel(Plan p, const uint8_t* __re
             float amax = fmaxf(fabsf(a[0]), fabsf(a[1]));
 #pragma unroll
             for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-            const int ex = mx_exponent_e4m3(amax);
+            constexpr bool kE5 = MODE == MOE_A8W8_FP8_E5M2;
+            const int ex = mx_exponent_fp8<kE5>(amax);
             const float inv = exp2_neg_int(ex);
-            const uint8_t c0 = float_to_e4m3_satfinite(a[0] * inv), c1 = float_to_e4m3_satfinite(a[1] * inv);
+            const uint8_t c0 = float_to_fp8_satfinite<kE5>(a[0] * inv), c1 = float_to_fp8_satfinite<kE5>(a[1] * inv);
             p.a_pool[row * I + j0] = c0;
             p.a_pool[row * I + j0 + 1] = c1;
             if (tx == 0) p.a_pool_scale[row * (I / 32) + jb] = static_cast<uint8_t>(ex + 127);
@@ -339,6 +340,7 @@ cudaError_t launch_l1_simt(const Plan& p, const void* w1, const void* w1_scale, 
     switch (p.mode) {
         case MOE_A16W16: return l1_launch<MOE_A16W16>(p, w1, w1_scale, s);
         case MOE_A8W8_FP8: return l1_launch<MOE_A8W8_FP8>(p, w1, w1_scale, s);
+        case MOE_A8W8_FP8_E5M2: return l1_launch<MOE_A8W8_FP8_E5M2>(p, w1, w1_scale, s);
         case MOE_A8W8_INT8: return l1_launch<MOE_A8W8_INT8>(p, w1, w1_scale, s);
         case MOE_A8W4_FP8_FP4: return l1_launch<MOE_A8W4_FP8_FP4>(p, w1, w1_scale, s);
         case MOE_A8W4_INT: return l1_launch<MOE_A8W4_INT>(p, w1, w1_scale, s);
@@ -352,6 +354,7 @@ cudaError_t launch_l2_simt(const Plan& p, const void* w2, const void* w2_scale, 
     switch (p.mode) {
         case MOE_A16W16: return l2_launch<MOE_A16W16>(p, w2, w2_scale, topk_weights, s);
         case MOE_A8W8_FP8: return l2_launch<MOE_A8W8_FP8>(p, w2, w2_scale, topk_weights, s);
+        case MOE_A8W8_FP8_E5M2: return l2_launch<MOE_A8W8_FP8_E5M2>(p, w2, w2_scale, topk_weights, s);
         case MOE_A8W8_INT8: return l2_launch<MOE_A8W8_INT8>(p, w2, w2_scale, topk_weights, s);
         case MOE_A8W4_FP8_FP4: return l2_launch<MOE_A8W4_FP8_FP4>(p, w2, w2_scale, topk_weights, s);
         case MOE_A8W4_INT: return l2_launch<MOE_A8W4_INT>(p, w2, w2_scale, topk_weights, s);

@@ -108,10 +108,10 @@ __device__ __forceinline__ Tile decode(int t, const int* sub_off, const int* til
 }
 
 // Instruction descriptor of kind::mxf8f6f4.block_scale: B scale-factor id (bits 4-5), A and B
-// element types (7-9, 10-12: e4m3 = 0, e2m1 = 5), both K-major, N >> 3 (17-22), scale type
-// UE8M0 (bit 23), M >> 4 (24-28), A scale-factor id (29-30).
-__device__ __forceinline__ uint32_t bs_idesc(uint32_t afmt, int n, int sf_id) {
-    return ((uint32_t)sf_id << 4) | (afmt << 7) | (0u << 10) | ((uint32_t)(n >> 3) << 17) | (1u << 23) |
+// element types (7-9, 10-12: e4m3 = 0, e5m2 = 1, e2m1 = 5), both K-major, N >> 3 (17-22), scale
+// type UE8M0 (bit 23), M >> 4 (24-28), A scale-factor id (29-30).
+__device__ __forceinline__ uint32_t bs_idesc(uint32_t afmt, uint32_t bfmt, int n, int sf_id) {
+    return ((uint32_t)sf_id << 4) | (afmt << 7) | (bfmt << 10) | ((uint32_t)(n >> 3) << 17) | (1u << 23) |
            ((uint32_t)(kWR >> 4) << 24) | ((uint32_t)sf_id << 29);
 }
 
@@ -140,7 +140,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     using Cfg = BsCfg<kNT, kStages, kAtoms>;
     constexpr int kBK = kAtoms * kAtomK;  // K per stage
     constexpr bool kFp4 = MODE == MOE_A8W4_FP8_FP4;
-    constexpr uint32_t kAfmt = kFp4 ? 5u : 0u;
+    constexpr bool kE5 = MODE == MOE_A8W8_FP8_E5M2;  // e5m2 weights, tokens and A
+    constexpr uint32_t kBfmt = kE5 ? 1u : 0u;
+    constexpr uint32_t kAfmt = kFp4 ? 5u : kBfmt;
     constexpr uint32_t kABoxTx = kFp4 ? kHalf * kAtomK / 2 : kHalf * kAtomK;  // TMA counts the packed global bytes
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = smem_u32(smem_raw);
@@ -267,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int kk = 0; kk < kAtomK / 32; ++kk)
                             tc_mma_bs(d, kmajor_desc(sa + at * kABytes, kk), kmajor_desc(sb + at * Cfg::kBBytes, kk),
-                                      bs_idesc(kAfmt, n, kk), sf + 8 * at, sf + 8 * at + 4, (kb | at | kk) != 0);
+                                      bs_idesc(kAfmt, kBfmt, n, kk), sf + 8 * at, sf + 8 * at + 4, (kb | at | kk) != 0);
                     }
                     tc_commit(empty_bar(s));
                 }
@@ -467,8 +469,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const float uv = gate ? xu[tt * kHalf + jl] : __uint_as_float(v[16 + tt]);
                             const float av = swiglu1(gv, uv, p.act_clamp);
                             const float amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(av))));
-                            const int ex = mx_exponent_e4m3(amax);
-                            st_global_u8_if(true, p.a_pool + (row0 + tt) * I + j, float_to_e4m3_satfinite(av * exp2_neg_int(ex)));
+                            const int ex = mx_exponent_fp8<kE5>(amax);
+                            st_global_u8_if(true, p.a_pool + (row0 + tt) * I + j, float_to_fp8_satfinite<kE5>(av * exp2_neg_int(ex)));
                             my_sc = lane == tt ? (uint32_t)(ex + 127) : my_sc;
                         }
                         st_global_u8_if(lane < 16, p.a_pool_scale + (row0 + lane) * (I / 32) + (j >> 5), (uint8_t)my_sc);
@@ -578,7 +580,8 @@ cudaError_t launch_bs(const Plan& p, const void* w, const void* w_scale, const f
 }  // namespace
 
 bool bs_supported(const Plan& p, int stage) {
-    if ((p.mode != MOE_A8W8_FP8 && p.mode != MOE_A8W4_FP8_FP4) || p.E > kMaxExperts || !tc_encode_available())
+    if ((p.mode != MOE_A8W8_FP8 && p.mode != MOE_A8W8_FP8_E5M2 && p.mode != MOE_A8W4_FP8_FP4) ||
+        p.E > kMaxExperts || !tc_encode_available())
         return false;
     if (stage == 1) return p.I % kHalf == 0 && p.H % kAtomK == 0;
     return p.H % kWR == 0 && p.I % kAtomK == 0;
@@ -587,6 +590,8 @@ bool bs_supported(const Plan& p, int stage) {
 cudaError_t launch_l1_bs(const Plan& p, const void* w1, const void* w1_scale, bool weight_major, cudaStream_t s) {
     if (p.mode == MOE_A8W4_FP8_FP4) return launch_bs<MOE_A8W4_FP8_FP4, true>(p, w1, w1_scale, nullptr, weight_major, s);
     if (p.mode == MOE_A8W8_FP8) return launch_bs<MOE_A8W8_FP8, true>(p, w1, w1_scale, nullptr, weight_major, s);
+    if (p.mode == MOE_A8W8_FP8_E5M2)
+        return launch_bs<MOE_A8W8_FP8_E5M2, true>(p, w1, w1_scale, nullptr, weight_major, s);
     return cudaErrorNotSupported;
 }
 
@@ -595,6 +600,8 @@ cudaError_t launch_l2_bs(const Plan& p, const void* w2, const void* w2_scale, co
     if (p.mode == MOE_A8W4_FP8_FP4)
         return launch_bs<MOE_A8W4_FP8_FP4, false>(p, w2, w2_scale, topk_weights, weight_major, s);
     if (p.mode == MOE_A8W8_FP8) return launch_bs<MOE_A8W8_FP8, false>(p, w2, w2_scale, topk_weights, weight_major, s);
+    if (p.mode == MOE_A8W8_FP8_E5M2)
+        return launch_bs<MOE_A8W8_FP8_E5M2, false>(p, w2, w2_scale, topk_weights, weight_major, s);
     return cudaErrorNotSupported;
 }
 

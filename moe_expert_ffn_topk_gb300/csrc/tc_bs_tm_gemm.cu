@@ -113,11 +113,11 @@ __device__ __forceinline__ Tile decode_tile(int t, const int* tile_off, const in
     return tl;
 }
 
-// kind::mxf8f6f4.block_scale instruction descriptor: B scale id (bits 4-5), A type (7-9: e4m3
-// tokens = 0), B type (10-12: e4m3 = 0, e2m1 = 5), both K-major, N >> 3 (17-22), UE8M0 scales
-// (bit 23), M >> 4 (24-28), A scale id (29-30).
-__device__ __forceinline__ uint32_t tm_idesc(uint32_t bfmt, int n, int sf_id) {
-    return ((uint32_t)sf_id << 4) | (0u << 7) | (bfmt << 10) | ((uint32_t)(n >> 3) << 17) | (1u << 23) |
+// kind::mxf8f6f4.block_scale instruction descriptor: B scale id (bits 4-5), A type (7-9: the
+// tokens, e4m3 = 0, e5m2 = 1), B type (10-12: e4m3 = 0, e5m2 = 1, e2m1 = 5), both K-major,
+// N >> 3 (17-22), UE8M0 scales (bit 23), M >> 4 (24-28), A scale id (29-30).
+__device__ __forceinline__ uint32_t tm_idesc(uint32_t afmt, uint32_t bfmt, int n, int sf_id) {
+    return ((uint32_t)sf_id << 4) | (afmt << 7) | (bfmt << 10) | ((uint32_t)(n >> 3) << 17) | (1u << 23) |
            ((uint32_t)(kTM >> 4) << 24) | ((uint32_t)sf_id << 29);
 }
 
@@ -141,10 +141,12 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
         : "memory");
 }
 
-// two floats -> two e4m3 codes (RN, saturating), the first in the low byte
-__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+// two floats -> two e4m3 (or e5m2) codes (RN, saturating), the first in the low byte
+template <bool kE5>
+__device__ __forceinline__ uint32_t fp8x2(float lo, float hi) {
     uint16_t pair;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(hi), "f"(lo));
+    if constexpr (kE5) asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(hi), "f"(lo));
+    else asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(hi), "f"(lo));
     return pair;
 }
 
@@ -154,7 +156,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tmSW, const __grid_constant__ CUtensorMap tmSX, TmArgs args) {
     using Cfg = TmCfg<kWN>;
     constexpr bool kFp4 = MODE == MOE_A8W4_FP8_FP4;
-    constexpr uint32_t kBfmt = kFp4 ? 5u : 0u;
+    constexpr bool kE5 = MODE == MOE_A8W8_FP8_E5M2;  // e5m2 tokens, weights and A
+    constexpr uint32_t kAfmt = kE5 ? 1u : 0u;
+    constexpr uint32_t kBfmt = kFp4 ? 5u : kAfmt;
     constexpr uint32_t kWTx = kFp4 ? kWN * kAtomK / 2 : kWN * kAtomK;  // TMA counts the packed global bytes
     constexpr int kStageBytes = Cfg::kStageBytes, kSfOff = Cfg::kSfOff, kSfWBytes = Cfg::kSfWBytes;
     constexpr int kSfCol0 = Cfg::kSfCol0, kAccs = Cfg::kAccs;
@@ -298,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t sf = tmem_base + kSfCol0 + s * kSfColsPerStage;
 #pragma unroll
                     for (int kk = 0; kk < kAtomK / 32; ++kk)
-                        tm_mma(d, kmajor_desc(sa, kk), kmajor_desc(sb, kk), tm_idesc(kBfmt, kWN, kk), sf, sf + 4,
+                        tm_mma(d, kmajor_desc(sa, kk), kmajor_desc(sb, kk), tm_idesc(kAfmt, kBfmt, kWN, kk), sf, sf + 4,
                                (kb | kk) != 0);
                     tc_commit(empty_bar(s));
                 }
@@ -400,13 +404,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         av[jj] = swiglu1(__uint_as_float(g[jj]), __uint_as_float(u[jj]), p.act_clamp);
                         amax = fmaxf(amax, fabsf(av[jj]));
                     }
-                    const int ex = mx_exponent_e4m3(amax);
+                    const int ex = mx_exponent_fp8<kE5>(amax);
                     const float inv = exp2_neg_int(ex);
                     uint32_t w[8];
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
-                        w[k] = e4m3x2(av[4 * k] * inv, av[4 * k + 1] * inv) |
-                               (e4m3x2(av[4 * k + 2] * inv, av[4 * k + 3] * inv) << 16);
+                        w[k] = fp8x2<kE5>(av[4 * k] * inv, av[4 * k + 1] * inv) |
+                               (fp8x2<kE5>(av[4 * k + 2] * inv, av[4 * k + 3] * inv) << 16);
                     const int j0 = tl.s * 128 + 32 * c;
                     st_global_v8_if(valid, p.a_pool + row * I + j0, w);
                     st_global_u8_if(valid, p.a_pool_scale + row * (I / 32) + (j0 >> 5), (uint8_t)(ex + 127));
@@ -524,7 +528,8 @@ cudaError_t launch_tm(const Plan& p, const void* w, const void* w_scale, const f
 }  // namespace
 
 bool bs_tm_supported(const Plan& p, int stage) {
-    if ((p.mode != MOE_A8W8_FP8 && p.mode != MOE_A8W4_FP8_FP4) || p.E > kMaxExperts || !tc_encode_available())
+    if ((p.mode != MOE_A8W8_FP8 && p.mode != MOE_A8W8_FP8_E5M2 && p.mode != MOE_A8W4_FP8_FP4) ||
+        p.E > kMaxExperts || !tc_encode_available())
         return false;
     // scale rows by TMA: their byte pitch (K / 32; K / 32 for the fp32 per-128 token scales
     // too) must be a multiple of 16
@@ -535,6 +540,7 @@ bool bs_tm_supported(const Plan& p, int stage) {
 cudaError_t launch_l1_bs_tm(const Plan& p, const void* w1, const void* w1_scale, cudaStream_t s) {
     if (p.mode == MOE_A8W4_FP8_FP4) return launch_tm<MOE_A8W4_FP8_FP4, true, 256>(p, w1, w1_scale, nullptr, s);
     if (p.mode == MOE_A8W8_FP8) return launch_tm<MOE_A8W8_FP8, true, 256>(p, w1, w1_scale, nullptr, s);
+    if (p.mode == MOE_A8W8_FP8_E5M2) return launch_tm<MOE_A8W8_FP8_E5M2, true, 256>(p, w1, w1_scale, nullptr, s);
     return cudaErrorNotSupported;
 }
 
@@ -548,6 +554,9 @@ cudaError_t launch_l2_bs_tm(const Plan& p, const void* w2, const void* w2_scale,
     if (p.mode == MOE_A8W8_FP8)
         return n224 ? launch_tm<MOE_A8W8_FP8, false, 224>(p, w2, w2_scale, topk_weights, s)
                     : launch_tm<MOE_A8W8_FP8, false, 256>(p, w2, w2_scale, topk_weights, s);
+    if (p.mode == MOE_A8W8_FP8_E5M2)
+        return n224 ? launch_tm<MOE_A8W8_FP8_E5M2, false, 224>(p, w2, w2_scale, topk_weights, s)
+                    : launch_tm<MOE_A8W8_FP8_E5M2, false, 256>(p, w2, w2_scale, topk_weights, s);
     return cudaErrorNotSupported;
 }
 

@@ -3,7 +3,8 @@ back the workspace regions, and compare against the oracle."""
 import numpy as np
 import torch
 
-TOL = {"a16w16": 2e-2, "a8w8_int8": 2e-2, "a8w4_int": 2e-2, "a8w8_fp8": 6e-2, "a8w4_fp8_fp4": 6e-2}
+TOL = {"a16w16": 2e-2, "a8w8_int8": 2e-2, "a8w4_int": 2e-2, "a8w8_fp8": 6e-2, "a8w4_fp8_fp4": 6e-2,
+       "a8w8_fp8_e5m2": 6e-2}
 
 
 def lib():

@@ -45,7 +45,7 @@ CONFIGS = [(64, 256, 128, 8, 2), (4096, 4096, 14336, 8, 2), (128, 7168, 2048, 25
 
 
 @pytest.mark.parametrize("cfg", CONFIGS)
-@pytest.mark.parametrize("mode", ["a16w16", "a8w8_fp8", "a8w8_int8", "a8w4_fp8_fp4", "a8w4_int"])
+@pytest.mark.parametrize("mode", ["a16w16", "a8w8_fp8", "a8w8_int8", "a8w4_fp8_fp4", "a8w4_int", "a8w8_fp8_e5m2"])
 def test_workspace_layout(moe, cfg, mode):
     T, H, I, E, K = cfg
     d = moe.dims(*cfg)

@@ -45,6 +45,9 @@ CASES = {
                      Workload("n224_fp4", "a8w4_fp8_fp4", 260, 3584, 512, 6, 2, 29, 0.05)],
 }
 CASES["a8w8_fp8"].append(Workload("n224_fp8", "a8w8_fp8", 200, 3584, 512, 5, 2, 30, 0.05))
+CASES["a8w8_fp8_e5m2"] = [Workload("tiny_e5m2", "a8w8_fp8_e5m2", 64, 256, 128, 8, 2, 39, 0.02),
+                          Workload("ragged_e5m2", "a8w8_fp8_e5m2", 300, 512, 384, 6, 2, 40, 0.05),
+                          Workload("n224_e5m2", "a8w8_fp8_e5m2", 200, 3584, 512, 5, 2, 41, 0.05)]
 ALL = [(m, wl) for m, wls in CASES.items() for wl in wls]
 
 
@@ -353,7 +356,7 @@ def test_quantised_tensor_core_path_matches_reference_kernels(moe, mode, wl):
     assert np.abs(c[0] - c[1]).max() <= TOL[mode] * np.abs(c[1]).max()
 
 
-FP8_PREFILL = [(m, w) for m, w in ALL if m in ("a8w8_fp8", "a8w4_fp8_fp4") and w.T * w.K > 16 * w.E]
+FP8_PREFILL = [(m, w) for m, w in ALL if m in ("a8w8_fp8", "a8w4_fp8_fp4", "a8w8_fp8_e5m2") and w.T * w.K > 16 * w.E]
 
 
 @pytest.mark.parametrize("mode,wl", FP8_PREFILL, ids=[f"{m}-{w.name}" for m, w in FP8_PREFILL])
@@ -388,7 +391,7 @@ def _check_w4_operands(ws, L, planes, sums_half, R, n, rows, codes):
 
 
 XQ_CASES = [(m, w) for m, w in ALL if m != "a16w16" and w.name in ("tiny_fp8", "ragged_fp8", "tiny_int8", "ragged_int8",
-                                                                    "tiny_w4", "ragged_w4",
+                                                                    "tiny_w4", "ragged_w4", "tiny_e5m2", "ragged_e5m2",
                                                                     "tiny_fp4", "skew_fp4", "n224_fp4", "n224_fp8")]
 
 
@@ -423,7 +426,7 @@ def test_dispatch_quantize_matches_oracle_bit_exactly(moe, mode, wl):
     qx, sx = omoe.quantize_x(mode, to_numpy({"x": xb})["x"])
     codes = region(ws, L, "x_pool", torch.uint8, R * wl.H).view(R, wl.H).cpu().numpy()[rows]
     assert np.array_equal(codes, qx.view(np.uint8)[tok]), "codes"
-    if mode == "a8w8_fp8":
+    if mode in ("a8w8_fp8", "a8w8_fp8_e5m2"):
         sc = region(ws, L, "x_pool_scale", torch.uint8, R * (wl.H // 32)).view(R, -1).cpu().numpy()[rows]
         assert np.array_equal(sc, sx[tok])
     else:
@@ -486,7 +489,7 @@ def test_full_size_quantizing_x_sampled(moe, name):
 
 
 CLAMP_CASES = [(m, w) for m, w in ALL if w.name in ("tiny_bf16", "ragged_bf16", "ragged_fp8", "ragged_int8", "ragged_fp4",
-                                                     "skew_fp4", "n224_fp4", "ragged_w4")]
+                                                     "skew_fp4", "n224_fp4", "ragged_w4", "ragged_e5m2")]
 
 
 @pytest.mark.parametrize("mode,wl", CLAMP_CASES, ids=[f"{m}-{w.name}" for m, w in CLAMP_CASES])
@@ -537,7 +540,7 @@ def test_activation_clamp_rejects_bad_values(moe):
 # ---------------------------------------------------------------------------------------
 
 SHARED_CASES = [(m, w) for m, w in ALL if w.name in ("tiny_bf16", "ragged_bf16", "ragged_fp8", "ragged_int8",
-                                                      "ragged_w4", "ragged_fp4", "skew_fp4", "n224_fp8")]
+                                                      "ragged_w4", "ragged_fp4", "skew_fp4", "n224_fp8", "ragged_e5m2")]
 
 
 @pytest.mark.parametrize("mode,wl", SHARED_CASES, ids=[f"{m}-{w.name}" for m, w in SHARED_CASES])
