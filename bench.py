@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", type=int, default=None, help="override the workload's token count")
     ap.add_argument("--experts", type=int, default=None, help="override the workload's expert count")
+    ap.add_argument("--fused", action="store_true",
+                    help="S3-S5 in one launch (moe_expert_ffn; MOE_FLAG_FUSED end to end), bf16 only")
     ap.add_argument("--quantize-x", action="store_true",
                     help="bf16 x in, quantised by the dispatch stage as the mode prescribes (MOE_FLAG_QUANTIZE_X)")
     return ap.parse_args()
@@ -58,12 +60,14 @@ def peaks():
     return FALLBACK_PEAKS, "fallback"
 
 
-def workload_config(wl, quantize_x=False):
+def workload_config(wl, quantize_x=False, fused=False):
     cfg = {"workload": wl.name, "mode": wl.mode, "tokens": wl.T, "hidden": wl.H, "intermediate": wl.I,
            "experts": wl.E, "topk": wl.K, "routed_rows": wl.routed_rows, "seed": wl.seed,
            "l2_policy": "inputs larger than L2 (no flush)"}
     if quantize_x:
         cfg["x_input"] = "bf16, quantised by the dispatch stage"
+    if fused:
+        cfg["gemm_launch"] = "L1 and L2 in one cooperative launch (moe_expert_ffn)"
     return cfg
 
 
@@ -139,7 +143,7 @@ def run_reference(args, wl, rank, world):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(wl, args.quantize_x), "routed_rows_per_s": total_rows / total_t,
+        "config": workload_config(wl, args.quantize_x, args.fused), "routed_rows_per_s": total_rows / total_t,
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -222,11 +226,11 @@ class ClockSampler:
 # ---------------------------------------------------------------------------------------
 
 
-def dominant_kernel_traffic(workload):
-    """DRAM bytes per launch of the L1 GEMM from the committed ncu summary of this workload,
-    valid only while the kernel sources the counters were taken on are unchanged (the summary
-    lists them and their sha256)."""
-    path = os.path.join(ROOT, "profiles", f"l1_gemm_{workload}.md")
+def dominant_kernel_traffic(workload, prefix="l1_gemm"):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary of this
+    workload, valid only while the kernel sources the counters were taken on are unchanged (the
+    summary lists them and their sha256)."""
+    path = os.path.join(ROOT, "profiles", f"{prefix}_{workload}.md")
     if not os.path.exists(path):
         return None
     txt = open(path).read()
@@ -307,6 +311,19 @@ def l1_roofline(wl, inp, l1_ms, pk, pk_src, sustained):
             "traffic": dominant_kernel_traffic(wl.name)}
 
 
+def fused_roofline(wl, ffn_ms, pk, pk_src, sustained):
+    """Roofline of the fused launch (L1 + SwiGLU + L2 + gate): algorithmic flops 6*H*I per routed
+    row against the dense bf16 peak."""
+    flops = 6.0 * wl.H * wl.I * wl.routed_rows
+    achieved = flops / (ffn_ms * 1e-3) / 1e12
+    peak = float(pk["bf16_tflops_sustained"] if sustained else pk["bf16_tflops"])
+    clock = "sustained" if sustained else "burst"
+    return {"bound": "tensor", "kernel": "L1 + SwiGLU + L2 + gate in one launch (moe_expert_ffn)",
+            "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "peak_source": f"{pk_src} bf16 dense, {clock}", "ffn_ms": ffn_ms,
+            "traffic": dominant_kernel_traffic(wl.name, "ffn_fused")}
+
+
 def run_gb300(args, wl, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -322,7 +339,7 @@ def run_gb300(args, wl, rank, world, local_rank):
     ws = moe.alloc_workspace(d, wl.mode, dev)
     y = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=dev)
 
-    flags = args.flags | (moe.MOE_FLAG_QUANTIZE_X if args.quantize_x else 0)
+    flags = args.flags | (moe.MOE_FLAG_QUANTIZE_X if args.quantize_x else 0) | (moe.MOE_FLAG_FUSED if args.fused else 0)
 
     def step(ev_l1=None):
         moe.moe_plan(inp["topk_ids"], d, ws, stream=stream)
@@ -332,10 +349,17 @@ def run_gb300(args, wl, rank, world, local_rank):
             moe.moe_dispatch(inp["x"], inp["x_scale"], d, wl.mode, ws, stream=stream)
         if ev_l1:
             ev_l1[0].record(stream)
-        moe.moe_expert_l1(inp["w1"], inp["w1_scale"], d, wl.mode, ws, args.flags, stream=stream)
-        if ev_l1:
-            ev_l1[1].record(stream)
-        moe.moe_expert_l2(inp["w2"], inp["w2_scale"], inp["topk_weights"], d, wl.mode, ws, args.flags, stream=stream)
+        if args.fused:  # the events bracket the one launch of S3-S5
+            moe.moe_expert_ffn(inp["w1"], inp["w1_scale"], inp["w2"], inp["w2_scale"], inp["topk_weights"], d, wl.mode,
+                               ws, stream=stream)
+            if ev_l1:
+                ev_l1[1].record(stream)
+        else:
+            moe.moe_expert_l1(inp["w1"], inp["w1_scale"], d, wl.mode, ws, args.flags, stream=stream)
+            if ev_l1:
+                ev_l1[1].record(stream)
+            moe.moe_expert_l2(inp["w2"], inp["w2_scale"], inp["topk_weights"], d, wl.mode, ws, args.flags,
+                              stream=stream)
         moe.moe_combine(y, d, ws, stream=stream)
 
     def barrier():
@@ -430,17 +454,20 @@ def run_gb300(args, wl, rank, world, local_rank):
     # a timed region of a second or more runs at the power-capped clock: sustained peak;
     # a shorter one runs at burst clocks: burst peak
     sustained = elapsed_ms >= 1000.0
-    roof = l1_roofline(wl, inp, l1_ms, pk, pk_src, sustained)
+    if args.fused:
+        roof = fused_roofline(wl, l1_ms, pk, pk_src, sustained)
+    else:
+        roof = l1_roofline(wl, inp, l1_ms, pk, pk_src, sustained)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": DTYPE[wl.mode], "data": "synthetic (seeded; random-init weights)",
-        "config": workload_config(wl, args.quantize_x),
+        "config": workload_config(wl, args.quantize_x, args.fused),
         "routed_rows_per_s": world * wl.routed_rows * args.steps / (elapsed_ms * 1e-3),
         "roofline": roof,
         "e2e": {"value": whole_job_tflops(flops, args.steps, e2e_ms, world), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps},
-        "gpu_launches": LAUNCHES_PER_STEP[wl.mode] * args.steps,
+        "gpu_launches": (LAUNCHES_PER_STEP[wl.mode] - (1 if args.fused else 0)) * args.steps,
         "clocks": clocks.summary(),
     }
     return line, inp

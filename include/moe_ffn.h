@@ -120,8 +120,12 @@ enum {
     MOE_FLAG_WEIGHT_MAJOR = 2u, /* FP8 modes at prefill sizes: 128 weight rows x 128 tokens per tile
                                    (the decode-style tile) instead of 128 tokens x 256 weight rows;
                                    same results up to fp32 summation order, for comparison */
-    MOE_FLAG_QUANTIZE_X = 4u    /* moe_forward: x.data is bf16 [T,H] (x.scale unused) and the
+    MOE_FLAG_QUANTIZE_X = 4u,   /* moe_forward: x.data is bf16 [T,H] (x.scale unused) and the
                                    dispatch stage quantises it as moe_dispatch_quantize does */
+    MOE_FLAG_FUSED = 8u         /* moe_forward: S3-S5 through moe_expert_ffn (one launch, L1 -> L2
+                                   dependency counters). A16W16 only; other modes return
+                                   MOE_ERR_UNSUPPORTED, and with MOE_FLAG_SIMT it is
+                                   MOE_ERR_INVALID_ARG. Same results as the separate stages. */
 };
 
 /* Bytes of workspace that moe_plan / moe_forward and the stage calls need for `d` and `m`.
@@ -179,6 +183,7 @@ MOE_API moe_status moe_expert_l1(moe_operand w1, const moe_dims* d, moe_dtype_mo
 MOE_API moe_status moe_expert_l2(moe_operand w2, const float* topk_weights, const moe_dims* d, moe_dtype_mode m,
                          uint32_t flags, void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
+
 /* Stage S6, combine (Ascend page "Token Combine"): y[i,:] = bf16( sum_{k=0..K-1} c[i,k,:] )
  * summed in fp32 in slot order; masked slots contribute nothing. Needs moe_expert_l2 first.
  *   y  device bf16 [T,H]; every row is written. */
@@ -212,6 +217,18 @@ MOE_API moe_status moe_expert_l1_ex(moe_operand w1, const moe_dims* d, moe_dtype
 MOE_API moe_status moe_forward_ex(moe_operand x, const int32_t* topk_ids, const float* topk_weights, moe_operand w1,
                           moe_operand w2, void* y, const moe_dims* d, moe_dtype_mode m, const moe_options* opt,
                           void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/* Stages S3-S5 in one persistent cooperative launch (the DeepGEMM page's L1 -> L2 dependency
+ * counters, §5): every L1 tile (GEMM + SwiGLU), then every L2 tile (GEMM + gate); an L2 tile
+ * starts once all L1 tiles of its 128-row route tile have published their A rows, which it
+ * waits for with a bounded wait (on time-out MOE_ERR_TIMEOUT goes to the error word). The
+ * results equal moe_expert_l1 followed by moe_expert_l2. Needs moe_dispatch first; opt may be
+ * NULL (its flags are not used; the activation clamp applies). A16W16 with H a multiple of 256
+ * only: other modes and shapes return MOE_ERR_UNSUPPORTED before any launch.
+ *   w1, w2, topk_weights  as for moe_expert_l1 and moe_expert_l2. */
+MOE_API moe_status moe_expert_ffn(moe_operand w1, moe_operand w2, const float* topk_weights, const moe_dims* d,
+                          moe_dtype_mode m, const moe_options* opt, void* workspace, size_t workspace_bytes,
+                          moe_stream_t stream);
 
 /* Synchronises `stream`, returns the first device-side error recorded in the workspace
  * (MOE_OK if none) and clears it. */

@@ -18,12 +18,12 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "li
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_BAD_ROUTE, MOE_ERR_TIMEOUT, \
     MOE_ERR_WORKSPACE = range(7)
 MODES = {"a16w16": 0, "a8w8_fp8": 1, "a8w8_int8": 2, "a8w4_fp8_fp4": 3, "a8w4_int": 4, "a8w8_fp8_e5m2": 5}
-MOE_FLAG_NONE, MOE_FLAG_SIMT, MOE_FLAG_WEIGHT_MAJOR, MOE_FLAG_QUANTIZE_X = 0, 1, 2, 4
+MOE_FLAG_NONE, MOE_FLAG_SIMT, MOE_FLAG_WEIGHT_MAJOR, MOE_FLAG_QUANTIZE_X, MOE_FLAG_FUSED = 0, 1, 2, 4, 8
 
 ABI_FUNCTIONS = ("moe_workspace_bytes", "moe_plan", "moe_dispatch", "moe_expert_l1", "moe_expert_l2",
                  "moe_combine", "moe_forward", "moe_check_device_error", "moe_status_string",
                  "moe_workspace_layout", "moe_debug_bounded_wait", "moe_plan_noalloc", "moe_dispatch_quantize",
-                 "moe_expert_l1_ex", "moe_forward_ex")
+                 "moe_expert_l1_ex", "moe_forward_ex", "moe_expert_ffn")
 
 
 class MoeDims(ctypes.Structure):
@@ -76,6 +76,7 @@ def _load():
         "moe_plan_noalloc": (st, [vp, dims_p, vp, vp, vp, vp]),
         "moe_dispatch_quantize": (st, [vp, dims_p, st, vp, sz, vp]),
         "moe_expert_l1_ex": (st, [MoeOperand, dims_p, st, ctypes.POINTER(MoeOptions), vp, sz, vp]),
+        "moe_expert_ffn": (st, [MoeOperand, MoeOperand, vp, dims_p, st, ctypes.POINTER(MoeOptions), vp, sz, vp]),
         "moe_forward_ex": (st, [MoeOperand, vp, vp, MoeOperand, MoeOperand, vp, dims_p, st, ctypes.POINTER(MoeOptions),
                                 vp, sz, vp]),
     }
@@ -207,6 +208,16 @@ def moe_expert_l1_ex(w1, w1_scale, d: MoeDims, mode, workspace, flags=0, activat
     opt = _options(flags, activation_clamp)
     _check(LIB.moe_expert_l1_ex(_operand(w1, w1_scale, "w1"), ctypes.byref(d), _mode(mode), ctypes.byref(opt), ws, nb,
                                 _stream(stream)), "moe_expert_l1_ex")
+
+
+def moe_expert_ffn(w1, w1_scale, w2, w2_scale, topk_weights, d: MoeDims, mode, workspace, activation_clamp=None,
+                   stream=None):
+    """S3-S5 in one launch (L1 -> L2 dependency counters); needs moe_dispatch first."""
+    ws, nb = _ws(workspace)
+    opt = _options(0, activation_clamp)
+    _check(LIB.moe_expert_ffn(_operand(w1, w1_scale, "w1"), _operand(w2, w2_scale, "w2"),
+                              _ptr(topk_weights, "topk_weights"), ctypes.byref(d), _mode(mode), ctypes.byref(opt),
+                              ws, nb, _stream(stream)), "moe_expert_ffn")
 
 
 def moe_forward_ex(x, x_scale, topk_ids, topk_weights, w1, w1_scale, w2, w2_scale, y, d: MoeDims, mode, workspace,

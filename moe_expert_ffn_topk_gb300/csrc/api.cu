@@ -265,6 +265,27 @@ moe_status moe_expert_l2(moe_operand w2, const float* topk_weights, const moe_di
     return from_cuda(launch_l2_simt(p, w2.data, w2.scale, topk_weights, s));
 }
 
+moe_status moe_expert_ffn(moe_operand w1, moe_operand w2, const float* topk_weights, const moe_dims* d,
+                          moe_dtype_mode m, const moe_options* opt, void* workspace, size_t workspace_bytes,
+                          moe_stream_t stream) {
+    Plan p;
+    moe_status st = make_plan_view(d, m, workspace, workspace_bytes, &p, true);
+    if (st != MOE_OK) return st;
+    uint32_t flags;
+    if ((st = read_options(opt, &flags, &p.act_clamp)) != MOE_OK) return st;
+    if (!operand_ok(w1, m != MOE_A16W16) || !operand_ok(w2, m != MOE_A16W16)) return MOE_ERR_INVALID_ARG;
+    if (!(tc_supported(p, 1) && tc_supported(p, 2))) return MOE_ERR_UNSUPPORTED;
+    if (d->num_tokens == 0) return MOE_OK;
+    if (!topk_weights) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (p.K != p.Kr) {  // shared experts: their slots carry weight 1
+        const cudaError_t e = launch_expand_gates(p, topk_weights, s);
+        if (e != cudaSuccess) return from_cuda(e);
+        topk_weights = p.gates;
+    }
+    return from_cuda(launch_ffn_fused_tc(p, w1.data, w2.data, topk_weights, s));
+}
+
 moe_status moe_combine(void* y, const moe_dims* d, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
     Plan p;
     moe_status st = make_plan_view(d, MOE_A16W16, workspace, workspace_bytes, &p, false);
@@ -286,12 +307,21 @@ static moe_status forward(moe_operand x, const int32_t* topk_ids, const float* t
     const bool quantize_x = (flags & MOE_FLAG_QUANTIZE_X) != 0;
     if (!(quantize_x ? x.data != nullptr : operand_ok(x, q)) || !topk_ids || !topk_weights || !y)
         return MOE_ERR_INVALID_ARG;
+    const bool fused = (flags & MOE_FLAG_FUSED) != 0;
+    if (fused && (flags & MOE_FLAG_SIMT)) return MOE_ERR_INVALID_ARG;
+    if (fused && !(tc_supported(p, 1) && tc_supported(p, 2))) return MOE_ERR_UNSUPPORTED;
     if ((st = moe_plan(topk_ids, d, nullptr, nullptr, nullptr, workspace, workspace_bytes, stream)) != MOE_OK) return st;
     st = quantize_x ? moe_dispatch_quantize(x.data, d, m, workspace, workspace_bytes, stream)
                     : moe_dispatch(x, d, m, workspace, workspace_bytes, stream);
     if (st != MOE_OK) return st;
-    if ((st = expert_l1(w1, d, m, flags, clamp, workspace, workspace_bytes, stream)) != MOE_OK) return st;
-    if ((st = moe_expert_l2(w2, topk_weights, d, m, flags, workspace, workspace_bytes, stream)) != MOE_OK) return st;
+    if (fused) {
+        const moe_options opt{flags, 1u, clamp};
+        if ((st = moe_expert_ffn(w1, w2, topk_weights, d, m, &opt, workspace, workspace_bytes, stream)) != MOE_OK)
+            return st;
+    } else {
+        if ((st = expert_l1(w1, d, m, flags, clamp, workspace, workspace_bytes, stream)) != MOE_OK) return st;
+        if ((st = moe_expert_l2(w2, topk_weights, d, m, flags, workspace, workspace_bytes, stream)) != MOE_OK) return st;
+    }
     return moe_combine(y, d, workspace, workspace_bytes, stream);
 }
 

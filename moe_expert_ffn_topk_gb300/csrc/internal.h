@@ -81,6 +81,9 @@ cudaError_t launch_l1_tc(const Plan& p, const void* w1, const void* w1_scale, cu
 cudaError_t launch_l2_tc(const Plan& p, const void* w2, const void* w2_scale, const float* topk_weights,
                          cudaStream_t s);
 bool tc_supported(const Plan& p, int stage);
+// S3-S5 of the bf16 mode in one cooperative launch (L1 -> L2 dependency counters)
+cudaError_t launch_ffn_fused_tc(const Plan& p, const void* w1, const void* w2, const float* topk_weights,
+                                cudaStream_t s);
 
 // Tensor-core path of the integer modes (int8 or int4 weights converted to f16 in shared
 // memory, the tokens' f16 planes; every partial sum an exact integer).

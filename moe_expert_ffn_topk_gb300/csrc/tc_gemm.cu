@@ -16,6 +16,14 @@
 // H columns; the epilogue multiplies row p by G[row_src[p]] in fp32 and stores bf16 to the
 // combine row of (token, slot).
 //
+// L1 and L2 in one launch (the DeepGEMM page's L1 -> L2 dependency counters, §5): the fused
+// instantiation runs every L1 tile, then every L2 tile, over one static round-robin order, so
+// each CTA finishes its L1 tiles before it starts on L2. An L2 tile needs the A rows of its
+// 128-row route tile from all I/128 L1 tiles of that route tile: the L1 epilogue publishes each
+// finished tile with a release increment of the route tile's counter, and the L2 producer waits
+// (bounded) until the count is complete before its TMA reads A. The launch is cooperative, so
+// every CTA is resident and the L1 tiles an L2 tile waits for are always making progress.
+//
 // Warp roles (192 threads): warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer,
 // warps 2-5 = epilogue (warp w reads TMEM lanes 32*(w%4) .. 32*(w%4)+31).
 // Every mbarrier wait is bounded (2 s); on time-out the CTA records MOE_ERR_TIMEOUT, drains
@@ -61,7 +69,19 @@ struct TcArgs {
     int k_blocks;               // K / 64
     int k_rows;                 // rows of one expert's weight in its 2-D view (L1: H, L2: I)
     int b_one_box;              // B map brings a stage's four 64-column blocks in one copy
+    // fused launch: the L2 stage's figures, and the per-route-tile count of finished L1 tiles
+    int n_tiles2, k_blocks2, k_rows2, b_one_box2;
+    int32_t* l1_done;
 };
+
+constexpr int kL2 = 0, kL1 = 1, kFusedL1L2 = 2;  // what one launch runs
+
+// Count of the finished L1 tiles of a route tile, read with acquire semantics at GPU scope.
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
 
 // A tile: 128 rows x 64 K, K-major, 128-byte swizzle (the TMA box layout). 8-row groups are
 // 1024 bytes apart; the K extent of one MMA (16 elements, 32 bytes) stays inside a swizzle
@@ -96,9 +116,11 @@ __device__ __forceinline__ Tile decode_tile(int t, const int* tile_off, int E, i
     return tl;
 }
 
-template <bool kL1>
+template <int kKind>  // kL1, kL2 or kFusedL1L2
 __global__ void __launch_bounds__(kThreads, 1)
-    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, TcArgs args) {
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2, TcArgs args) {
+    constexpr bool kFused = kKind == kFusedL1L2;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -112,6 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* misc = smem + kStages * kStageBytes + 8 * (2 * kStages + 5);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(misc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
+    int* epi_done = reinterpret_cast<int*>(misc + 8);  // fused: epilogue warps done with L1 tiles
     int* tile_off = reinterpret_cast<int*>(misc + 16);
 
     const Plan& p = args.p;
@@ -128,6 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
+        *epi_done = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
@@ -139,14 +163,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0 && lane == 0) {
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+        if (kFused) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA2)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB2)) : "memory");
+        }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
 
-    const int total = tile_off[p.E] * args.n_tiles;
-    const int KB = args.k_blocks;
+    // tiles [0, total1) are the launch's first stage (L1 when fused), [total1, total) the L2 ones
+    const int total1 = tile_off[p.E] * args.n_tiles;
+    const int total = kFused ? total1 + tile_off[p.E] * args.n_tiles2 : total1;
+    auto is_l1 = [&](int t) { return kKind == kL1 || (kFused && t < total1); };
+    auto tile_of = [&](int t) {
+        return kFused && t >= total1 ? decode_tile(t - total1, tile_off, p.E, args.n_tiles2)
+                                     : decode_tile(t, tile_off, p.E, args.n_tiles);
+    };
+    auto k_blocks_of = [&](int t) { return kFused && t >= total1 ? args.k_blocks2 : args.k_blocks; };
 
     if (warp == 0) {
         if (lane == 0) {
@@ -154,8 +189,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             int it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const Tile tl = decode_tile(t, tile_off, p.E, args.n_tiles);
-                const int wrow = tl.e * args.k_rows;
+                const bool l1 = is_l1(t), second = kFused && !l1;
+                const Tile tl = tile_of(t);
+                const CUtensorMap* mA = second ? &tmA2 : &tmA;
+                const CUtensorMap* mB = second ? &tmB2 : &tmB;
+                const int wrow = tl.e * (second ? args.k_rows2 : args.k_rows);
+                const int one_box = second ? args.b_one_box2 : args.b_one_box;
+                const int KB = k_blocks_of(t);
+                if (second) {
+                    // every L1 tile of this route tile has published its A rows
+                    const int32_t* done = args.l1_done + tile_off[tl.e] + tl.m;
+                    const uint64_t t0 = globaltimer_ns();
+                    while (ld_acquire_gpu(done) < args.n_tiles) {
+                        if (*abort_flag) {
+                            ok = false;
+                            break;
+                        }
+                        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+                            record_error(p.hdr, MOE_ERR_TIMEOUT);
+                            *abort_flag = 1;
+                            ok = false;
+                            break;
+                        }
+                        __nanosleep(64);
+                    }
+                    if (!ok) break;
+                    // those rows were written through the generic proxy; the TMA reads them
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                }
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int s = it % kStages;
                     const uint32_t ph = (uint32_t)(it / kStages) & 1u;
@@ -165,23 +226,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const uint32_t sa = base + s * kStageBytes, sb = sa + kABytes;
                     mbar_arrive_expect_tx(full_bar(s), kStageBytes);
-                    tma_load_2d(sa, &tmA, kb * kBK, tl.row0, full_bar(s));
+                    tma_load_2d(sa, mA, kb * kBK, tl.row0, full_bar(s));
                     const int y = wrow + kb * kBK;
-                    if (args.b_one_box) {
+                    if (one_box) {
                         // [64 columns][K row][column block](L1: [gate, up]) in one copy
-                        if (kL1)
-                            tma_load_4d(sb, &tmB, 0, y, 2 * tl.n, 0, full_bar(s));
+                        if (l1)
+                            tma_load_4d(sb, mB, 0, y, 2 * tl.n, 0, full_bar(s));
                         else
-                            tma_load_3d(sb, &tmB, 0, y, 4 * tl.n, full_bar(s));
-                    } else if (kL1) {
+                            tma_load_3d(sb, mB, 0, y, 4 * tl.n, full_bar(s));
+                    } else if (l1) {
                         const int g0 = tl.n * 128, u0 = p.I + tl.n * 128;
-                        tma_load_2d(sb, &tmB, g0, y, full_bar(s));
-                        tma_load_2d(sb + kBBoxBytes, &tmB, g0 + 64, y, full_bar(s));
-                        tma_load_2d(sb + 2 * kBBoxBytes, &tmB, u0, y, full_bar(s));
-                        tma_load_2d(sb + 3 * kBBoxBytes, &tmB, u0 + 64, y, full_bar(s));
+                        tma_load_2d(sb, mB, g0, y, full_bar(s));
+                        tma_load_2d(sb + kBBoxBytes, mB, g0 + 64, y, full_bar(s));
+                        tma_load_2d(sb + 2 * kBBoxBytes, mB, u0, y, full_bar(s));
+                        tma_load_2d(sb + 3 * kBBoxBytes, mB, u0 + 64, y, full_bar(s));
                     } else {
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) tma_load_2d(sb + j * kBBoxBytes, &tmB, tl.n * kBN + j * 64, y, full_bar(s));
+                        for (int j = 0; j < 4; ++j) tma_load_2d(sb + j * kBBoxBytes, mB, tl.n * kBN + j * 64, y, full_bar(s));
                     }
                 }
             }
@@ -206,6 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!mbar_wait(tempty_bar(a), ((uint32_t)(tc >> 1) & 1u) ^ 1u, p.hdr, abort_flag)) break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(a * kBN);
+                const int KB = k_blocks_of(t);
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int s = it % kStages;
                     if (!mbar_wait(full_bar(s), (uint32_t)(it / kStages) & 1u, p.hdr, abort_flag)) {
@@ -237,12 +299,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         int tc = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++tc) {
             const int a = tc & 1;
-            const Tile tl = decode_tile(t, tile_off, p.E, args.n_tiles);
+            const bool l1 = is_l1(t);
+            const Tile tl = tile_of(t);
             const int64_t row = tl.row0 + q * 32 + lane;
             // L2: the row's combine slot and gate weight, read while the tile's MMAs still run
             int src = -1;
             float gw = 0.0f;
-            if (!kL1) {
+            if (!l1) {
                 src = __ldg(p.pool_src + row);
                 gw = src >= 0 ? __ldg(args.topk_weights + src) : 0.0f;
             }
@@ -251,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * kBN);
-            if (kL1) {
+            if (l1) {
                 uint16_t* out = reinterpret_cast<uint16_t*>(p.a_pool) + row * p.I + tl.n * 128;
 #pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
@@ -268,6 +331,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     st_global_v8_if(true, out + c * 32, packed);
                     st_global_v8_if(true, out + c * 32 + 16, packed + 8);
+                }
+                if (kFused) {
+                    // publish the tile: each warp fences its own stores; the last of the four
+                    // warps to finish counts the tile for its route tile (no warp waits here)
+                    __threadfence();
+                    __syncwarp();
+                    if (lane == 0 && (atomicAdd(epi_done, 1) & 3) == 3) {
+                        __threadfence();
+                        atomicAdd(args.l1_done + tile_off[tl.e] + tl.m, 1);
+                    }
                 }
             } else {
                 uint16_t* out = p.comb + (int64_t)(src >= 0 ? src : 0) * p.H + tl.n * kBN;
@@ -316,18 +389,24 @@ constexpr size_t smem_bytes() {
     return 1024 + (size_t)kStages * kStageBytes + 8 * (2 * kStages + 5) + 16 + 4 * (kMaxExperts + 1);
 }
 
-template <bool kL1>
-cudaError_t launch_tc(const Plan& p, const CUtensorMap& a, const CUtensorMap& b, TcArgs args, cudaStream_t s) {
+template <int kKind>
+cudaError_t set_smem_attr() {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(tc_gemm_kernel<kL1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr_err = cudaFuncSetAttribute(tc_gemm_kernel<kKind>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         (int)smem_bytes());
     });
+    return attr_err;
+}
+
+template <int kKind>
+cudaError_t launch_tc(const Plan& p, const CUtensorMap& a, const CUtensorMap& b, TcArgs args, cudaStream_t s) {
+    const cudaError_t attr_err = set_smem_attr<kKind>();
     if (attr_err != cudaSuccess) return attr_err;
     const int64_t max_tiles = (p.pool_rows / kBM) * args.n_tiles;
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(max_tiles, tc_num_sms()));
-    tc_gemm_kernel<kL1><<<grid, kThreads, smem_bytes(), s>>>(a, b, args);
+    tc_gemm_kernel<kKind><<<grid, kThreads, smem_bytes(), s>>>(a, b, a, b, args);
     return cudaGetLastError();
 }
 
@@ -368,8 +447,8 @@ cudaError_t launch_l1_tc(const Plan& p, const void* w1, const void*, cudaStream_
     if (!make_map(&a, p.x_pool, (uint64_t)p.H, (uint64_t)p.pool_rows, kBM)) return cudaErrorInvalidValue;
     if (!make_b_map(&b, w1, (uint64_t)2 * p.I, (uint64_t)p.E * p.H, (uint64_t)p.I, true, &one_box))
         return cudaErrorInvalidValue;
-    TcArgs args{p, nullptr, p.I / 128, p.H / kBK, p.H, one_box};
-    return launch_tc<true>(p, a, b, args, s);
+    TcArgs args{p, nullptr, p.I / 128, p.H / kBK, p.H, one_box, 0, 0, 0, 0, nullptr};
+    return launch_tc<kL1>(p, a, b, args, s);
 }
 
 cudaError_t launch_l2_tc(const Plan& p, const void* w2, const void*, const float* topk_weights, cudaStream_t s) {
@@ -378,8 +457,46 @@ cudaError_t launch_l2_tc(const Plan& p, const void* w2, const void*, const float
     if (!make_map(&a, p.a_pool, (uint64_t)p.I, (uint64_t)p.pool_rows, kBM)) return cudaErrorInvalidValue;
     if (!make_b_map(&b, w2, (uint64_t)p.H, (uint64_t)p.E * p.I, (uint64_t)p.H, false, &one_box))
         return cudaErrorInvalidValue;
-    TcArgs args{p, topk_weights, p.H / kBN, p.I / kBK, p.I, one_box};
-    return launch_tc<false>(p, a, b, args, s);
+    TcArgs args{p, topk_weights, p.H / kBN, p.I / kBK, p.I, one_box, 0, 0, 0, 0, nullptr};
+    return launch_tc<kL2>(p, a, b, args, s);
+}
+
+cudaError_t launch_ffn_fused_tc(const Plan& p, const void* w1, const void* w2, const float* topk_weights,
+                                cudaStream_t s) {
+    CUtensorMap a1, b1, a2, b2;
+    int one_box1 = 0, one_box2 = 0;
+    if (!make_map(&a1, p.x_pool, (uint64_t)p.H, (uint64_t)p.pool_rows, kBM) ||
+        !make_b_map(&b1, w1, (uint64_t)2 * p.I, (uint64_t)p.E * p.H, (uint64_t)p.I, true, &one_box1) ||
+        !make_map(&a2, p.a_pool, (uint64_t)p.I, (uint64_t)p.pool_rows, kBM) ||
+        !make_b_map(&b2, w2, (uint64_t)p.H, (uint64_t)p.E * p.I, (uint64_t)p.H, false, &one_box2))
+        return cudaErrorInvalidValue;
+    // The L1 -> L2 counters, one per 128-row route tile, live in the plan's position scratch:
+    // it holds T*K ints, at least the route tile count, and nothing reads it once the plan is
+    // built. They start at zero for every launch.
+    const int64_t route_tiles = p.pool_rows / kBM;
+    cudaError_t e = cudaMemsetAsync(p.pos, 0, sizeof(int32_t) * (size_t)route_tiles, s);
+    if (e != cudaSuccess) return e;
+    if ((e = set_smem_attr<kFusedL1L2>()) != cudaSuccess) return e;
+    TcArgs args{p, topk_weights, p.I / 128, p.H / kBK, p.H, one_box1, p.H / kBN, p.I / kBK, p.I, one_box2, p.pos};
+    // every CTA resident at once (cooperative launch): an L2 tile waits only for L1 tiles that
+    // earlier positions of the same round-robin order hold, all of them running
+    int per_sm = 0;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tc_gemm_kernel<kFusedL1L2>, kThreads,
+                                                           smem_bytes())) != cudaSuccess)
+        return e;
+    const int64_t max_tiles = route_tiles * (p.I / 128 + p.H / kBN);
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(max_tiles, (int64_t)tc_num_sms() * std::max(per_sm, 1)));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem_bytes();
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<kFusedL1L2>, a1, b1, a2, b2, args);
 }
 
 }  // namespace moe

@@ -594,3 +594,81 @@ def test_routed_id_naming_a_shared_expert_is_a_bad_route(moe):
     ref = omoe.forward(wl.mode, h["x"], h["x_scale"], h["topk_ids"], h["topk_weights"], h["w1"], h["w1_scale"],
                        h["w2"], h["w2_scale"], num_experts=wl.E, inter=wl.I, num_shared=1)
     assert_close(y_numpy(out["y"]), ref, wl.mode)
+
+
+# ---------------------------------------------------------------------------------------
+# L1 and L2 in one launch (MOE_FLAG_FUSED, §8(f) row f3): the same tiles and arithmetic as the
+# separate stages, so the output is bit-identical to them
+# ---------------------------------------------------------------------------------------
+
+# (shapes with tensor-core tiles for both stages: H a multiple of 256)
+FUSED_CASES = CASES["a16w16"] + [w for w in EDGE if w.mode == "a16w16" and w.H % 256 == 0] + [
+    Workload("fused_one_expert_all_rows", "a16w16", 700, 512, 384, 3, 1, 42, 0.05),
+    Workload("fused_many_tiles", "a16w16", 1500, 1024, 1024, 8, 2, 43, 0.03)]
+
+
+def _forward_flags(moe, wl, inp, flags, shared=0, clamp=None, x=None):
+    d = moe.dims(wl.T, wl.H, wl.I, wl.E, wl.K, shared)
+    ws = moe.alloc_workspace(d, wl.mode, DEV)
+    y = torch.full((wl.T, wl.H), float("nan"), dtype=torch.bfloat16, device=DEV)
+    moe.moe_forward_ex(inp["x"] if x is None else x, inp["x_scale"], inp["topk_ids"], inp["topk_weights"], inp["w1"],
+                       inp["w1_scale"], inp["w2"], inp["w2_scale"], y, d, wl.mode, ws, flags, clamp)
+    return y, moe.moe_check_device_error(ws)
+
+
+@pytest.mark.parametrize("wl", FUSED_CASES, ids=[w.name for w in FUSED_CASES])
+def test_fused_l1_l2_equals_the_separate_stages(moe, wl):
+    inp = make_inputs(wl, device=DEV)
+    if wl.name == "fused_one_expert_all_rows":
+        inp["topk_ids"][:] = 1                  # 700 rows on one expert: 6 route tiles, the last ragged
+        inp["topk_ids"][::7] = -1               # and some masked routes
+    y0, st0 = _forward_flags(moe, wl, inp, 0)
+    y1, st1 = _forward_flags(moe, wl, inp, moe.MOE_FLAG_FUSED)
+    assert st0 == 0 and st1 == 0
+    assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
+    assert_close(y_numpy(y1), oracle_forward(wl, inp), wl.mode)
+
+
+def test_fused_full_size_equals_the_separate_stages(moe):
+    wl = WORKLOADS["mixtral_bf16_prefill"]
+    inp = make_inputs(wl, device=DEV)
+    y0, st0 = _forward_flags(moe, wl, inp, 0)
+    y1, st1 = _forward_flags(moe, wl, inp, moe.MOE_FLAG_FUSED)
+    assert st0 == 0 and st1 == 0
+    assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
+    rng = np.random.default_rng(wl.seed + 7)
+    tokens = sorted(rng.choice(wl.T, size=4, replace=False).tolist())
+    assert_close(y_numpy(y1)[tokens], oracle_forward(wl, slice_tokens(inp, tokens)), wl.mode)
+
+
+def test_fused_with_clamp_shared_experts_and_quantizing_dispatch(moe):
+    wl = CASES["a16w16"][1]
+    inp = make_inputs(wl, device=DEV, shared=1)
+    for flags in (0, moe.MOE_FLAG_QUANTIZE_X):
+        x = inp["x_bf16"] if flags else None
+        y0, st0 = _forward_flags(moe, wl, inp, flags, shared=1, clamp=0.5, x=x)
+        y1, st1 = _forward_flags(moe, wl, inp, flags | moe.MOE_FLAG_FUSED, shared=1, clamp=0.5, x=x)
+        assert st0 == 0 and st1 == 0
+        assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
+    h = to_numpy(inp)
+    ref = omoe.forward(wl.mode, h["x"], h["x_scale"], h["topk_ids"], h["topk_weights"], h["w1"], h["w1_scale"],
+                       h["w2"], h["w2_scale"], num_experts=wl.E, inter=wl.I, num_shared=1, clamp=0.5)
+    assert_close(y_numpy(y1), ref, wl.mode)
+
+
+def test_fused_flag_rejections(moe):
+    wl = CASES["a8w8_fp8"][0]
+    inp = make_inputs(wl, device=DEV)
+    with pytest.raises(moe.MoeError) as err:
+        _forward_flags(moe, wl, inp, moe.MOE_FLAG_FUSED)
+    assert err.value.status == 2  # MOE_ERR_UNSUPPORTED: no fused kernel for this mode
+    wl = EDGE[-1]  # max_topk: H = 128 has no 256-column L2 tile
+    assert wl.name == "max_topk"
+    with pytest.raises(moe.MoeError) as err:
+        _forward_flags(moe, wl, make_inputs(wl, device=DEV), moe.MOE_FLAG_FUSED)
+    assert err.value.status == 2
+    wl = CASES["a16w16"][0]
+    inp = make_inputs(wl, device=DEV)
+    with pytest.raises(moe.MoeError) as err:
+        _forward_flags(moe, wl, inp, moe.MOE_FLAG_FUSED | moe.MOE_FLAG_SIMT)
+    assert err.value.status == 1  # MOE_ERR_INVALID_ARG
