@@ -43,6 +43,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return done != 0;
 }
 
+// Non-blocking test of the phase with the given parity (true once it has completed).
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
 // Bounded wait for the phase of `bar` with the given parity to complete. Returns false when
 // the CTA gave up (this thread timed out, or another role already aborted).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* hdr, volatile int* abort_flag) {
