@@ -122,8 +122,8 @@ enum {
                                    same results up to fp32 summation order, for comparison */
     MOE_FLAG_QUANTIZE_X = 4u,   /* moe_forward: x.data is bf16 [T,H] (x.scale unused) and the
                                    dispatch stage quantises it as moe_dispatch_quantize does */
-    MOE_FLAG_FUSED = 8u         /* moe_forward: S3-S5 through moe_expert_ffn (one launch, L1 -> L2
-                                   dependency counters). A16W16 only; other modes return
+    MOE_FLAG_FUSED = 8u         /* moe_forward: S3-S6 through moe_expert_ffn (one launch: L1 -> L2 ->
+                                   combine dependency counters). A16W16 only; other modes return
                                    MOE_ERR_UNSUPPORTED, and with MOE_FLAG_SIMT it is
                                    MOE_ERR_INVALID_ARG. Same results as the separate stages. */
 };
@@ -218,17 +218,21 @@ MOE_API moe_status moe_forward_ex(moe_operand x, const int32_t* topk_ids, const 
                           moe_operand w2, void* y, const moe_dims* d, moe_dtype_mode m, const moe_options* opt,
                           void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
-/* Stages S3-S5 in one persistent cooperative launch (the DeepGEMM page's L1 -> L2 dependency
- * counters, §5): every L1 tile (GEMM + SwiGLU), then every L2 tile (GEMM + gate); an L2 tile
- * starts once all L1 tiles of its 128-row route tile have published their A rows, which it
- * waits for with a bounded wait (on time-out MOE_ERR_TIMEOUT goes to the error word). The
- * results equal moe_expert_l1 followed by moe_expert_l2. Needs moe_dispatch first; opt may be
- * NULL (its flags are not used; the activation clamp applies). A16W16 with H a multiple of 256
- * only: other modes and shapes return MOE_ERR_UNSUPPORTED before any launch.
- *   w1, w2, topk_weights  as for moe_expert_l1 and moe_expert_l2. */
-MOE_API moe_status moe_expert_ffn(moe_operand w1, moe_operand w2, const float* topk_weights, const moe_dims* d,
-                          moe_dtype_mode m, const moe_options* opt, void* workspace, size_t workspace_bytes,
-                          moe_stream_t stream);
+/* Stages S3-S5, and S6 when y is given, in one persistent cooperative launch (the DeepGEMM
+ * page's single kernel, §5): every L1 tile (GEMM + SwiGLU), then every L2 tile (GEMM + gate),
+ * then the combine of every token. An L2 tile starts once all L1 tiles of its 128-row route
+ * tile have published their A rows; a token's combine starts once every L2 tile holding one of
+ * its rows has published them, so CTAs that finish their L2 tiles early combine while others
+ * are still in L2. Every wait is bounded (on time-out MOE_ERR_TIMEOUT goes to the error word).
+ * The results equal moe_expert_l1, moe_expert_l2 and moe_combine. Needs moe_dispatch first;
+ * opt may be NULL (its flags are not used; the activation clamp applies). A16W16 with H a
+ * multiple of 256 only: other modes and shapes return MOE_ERR_UNSUPPORTED before any launch.
+ *   w1, w2, topk_weights  as for moe_expert_l1 and moe_expert_l2.
+ *   y                     device bf16 [T,H] or NULL (then the combine rows stay in the
+ *                         workspace for moe_combine). */
+MOE_API moe_status moe_expert_ffn(moe_operand w1, moe_operand w2, const float* topk_weights, void* y,
+                          const moe_dims* d, moe_dtype_mode m, const moe_options* opt, void* workspace,
+                          size_t workspace_bytes, moe_stream_t stream);
 
 /* Synchronises `stream`, returns the first device-side error recorded in the workspace
  * (MOE_OK if none) and clears it. */
@@ -267,6 +271,8 @@ typedef struct {
     size_t pool_sums;     /* A8W4-INT: int32 [2][pool_rows], the sum of each pool row's codes:
                              x rows, then A rows (other modes: size 0) */
     size_t comb;          /* bf16 [T*K, H] weighted rows */
+    size_t ffn_counters;  /* int32 [pool_rows/128 + T]: moe_expert_ffn's counts of finished L1 tiles
+                             per 128-row route tile, then of finished combine rows per token */
     size_t total;         /* = moe_workspace_bytes() */
     int64_t pool_rows;    /* rows reserved in each pool */
 } moe_workspace_layout_t;

@@ -44,7 +44,7 @@ class MoeWorkspaceLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
         "header", "counts", "offsets", "pad_offsets", "tile_offsets", "row_src", "pool_src", "slot_row", "gates",
         "x_pool", "x_pool_scale", "a_pool", "a_pool_scale", "a_f32", "x_pool_planes", "a_pool_planes", "pool_sums",
-        "comb",
+        "comb", "ffn_counters",
         "total")] + \
         [("pool_rows", ctypes.c_int64)]
 
@@ -76,7 +76,7 @@ def _load():
         "moe_plan_noalloc": (st, [vp, dims_p, vp, vp, vp, vp]),
         "moe_dispatch_quantize": (st, [vp, dims_p, st, vp, sz, vp]),
         "moe_expert_l1_ex": (st, [MoeOperand, dims_p, st, ctypes.POINTER(MoeOptions), vp, sz, vp]),
-        "moe_expert_ffn": (st, [MoeOperand, MoeOperand, vp, dims_p, st, ctypes.POINTER(MoeOptions), vp, sz, vp]),
+        "moe_expert_ffn": (st, [MoeOperand, MoeOperand, vp, vp, dims_p, st, ctypes.POINTER(MoeOptions), vp, sz, vp]),
         "moe_forward_ex": (st, [MoeOperand, vp, vp, MoeOperand, MoeOperand, vp, dims_p, st, ctypes.POINTER(MoeOptions),
                                 vp, sz, vp]),
     }
@@ -210,14 +210,15 @@ def moe_expert_l1_ex(w1, w1_scale, d: MoeDims, mode, workspace, flags=0, activat
                                 _stream(stream)), "moe_expert_l1_ex")
 
 
-def moe_expert_ffn(w1, w1_scale, w2, w2_scale, topk_weights, d: MoeDims, mode, workspace, activation_clamp=None,
-                   stream=None):
-    """S3-S5 in one launch (L1 -> L2 dependency counters); needs moe_dispatch first."""
+def moe_expert_ffn(w1, w1_scale, w2, w2_scale, topk_weights, d: MoeDims, mode, workspace, y=None,
+                   activation_clamp=None, stream=None):
+    """S3-S5 (and S6 into y when given) in one launch with dependency counters; needs
+    moe_dispatch first."""
     ws, nb = _ws(workspace)
     opt = _options(0, activation_clamp)
     _check(LIB.moe_expert_ffn(_operand(w1, w1_scale, "w1"), _operand(w2, w2_scale, "w2"),
-                              _ptr(topk_weights, "topk_weights"), ctypes.byref(d), _mode(mode), ctypes.byref(opt),
-                              ws, nb, _stream(stream)), "moe_expert_ffn")
+                              _ptr(topk_weights, "topk_weights"), None if y is None else _ptr(y, "y"), ctypes.byref(d),
+                              _mode(mode), ctypes.byref(opt), ws, nb, _stream(stream)), "moe_expert_ffn")
 
 
 def moe_forward_ex(x, x_scale, topk_ids, topk_weights, w1, w1_scale, w2, w2_scale, y, d: MoeDims, mode, workspace,

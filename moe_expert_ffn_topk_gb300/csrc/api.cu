@@ -79,6 +79,7 @@ moe_status layout(const moe_dims* d, moe_dtype_mode m, moe_workspace_layout_t* o
     L.slot_row = take(sizeof(int32_t) * R);
     L.gates = take(S ? sizeof(float) * R : 0);
     L.comb = take((size_t)R * H * 2);
+    L.ffn_counters = take(sizeof(int32_t) * (size_t)(pool_rows / kTileRows + T));
     // everything above is the same for every mode; the pools below depend on it
     L.x_pool = take((size_t)pool_rows * H * x_elem_bytes(m));
     L.x_pool_scale = take((size_t)pool_rows * x_scale_row_bytes(m, (int)H));
@@ -133,6 +134,7 @@ moe_status make_plan_view(const moe_dims* d, moe_dtype_mode m, void* ws, size_t 
     p->x_sums = reinterpret_cast<int32_t*>(b + L.pool_sums);
     p->a_sums = p->x_sums + L.pool_rows;
     p->comb = reinterpret_cast<uint16_t*>(b + L.comb);
+    p->ffn_counters = reinterpret_cast<int32_t*>(b + L.ffn_counters);
     return MOE_OK;
 }
 
@@ -265,7 +267,7 @@ moe_status moe_expert_l2(moe_operand w2, const float* topk_weights, const moe_di
     return from_cuda(launch_l2_simt(p, w2.data, w2.scale, topk_weights, s));
 }
 
-moe_status moe_expert_ffn(moe_operand w1, moe_operand w2, const float* topk_weights, const moe_dims* d,
+moe_status moe_expert_ffn(moe_operand w1, moe_operand w2, const float* topk_weights, void* y, const moe_dims* d,
                           moe_dtype_mode m, const moe_options* opt, void* workspace, size_t workspace_bytes,
                           moe_stream_t stream) {
     Plan p;
@@ -283,7 +285,7 @@ moe_status moe_expert_ffn(moe_operand w1, moe_operand w2, const float* topk_weig
         if (e != cudaSuccess) return from_cuda(e);
         topk_weights = p.gates;
     }
-    return from_cuda(launch_ffn_fused_tc(p, w1.data, w2.data, topk_weights, s));
+    return from_cuda(launch_ffn_fused_tc(p, w1.data, w2.data, topk_weights, static_cast<uint16_t*>(y), s));
 }
 
 moe_status moe_combine(void* y, const moe_dims* d, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
@@ -316,12 +318,10 @@ static moe_status forward(moe_operand x, const int32_t* topk_ids, const float* t
     if (st != MOE_OK) return st;
     if (fused) {
         const moe_options opt{flags, 1u, clamp};
-        if ((st = moe_expert_ffn(w1, w2, topk_weights, d, m, &opt, workspace, workspace_bytes, stream)) != MOE_OK)
-            return st;
-    } else {
-        if ((st = expert_l1(w1, d, m, flags, clamp, workspace, workspace_bytes, stream)) != MOE_OK) return st;
-        if ((st = moe_expert_l2(w2, topk_weights, d, m, flags, workspace, workspace_bytes, stream)) != MOE_OK) return st;
+        return moe_expert_ffn(w1, w2, topk_weights, y, d, m, &opt, workspace, workspace_bytes, stream);
     }
+    if ((st = expert_l1(w1, d, m, flags, clamp, workspace, workspace_bytes, stream)) != MOE_OK) return st;
+    if ((st = moe_expert_l2(w2, topk_weights, d, m, flags, workspace, workspace_bytes, stream)) != MOE_OK) return st;
     return moe_combine(y, d, workspace, workspace_bytes, stream);
 }
 

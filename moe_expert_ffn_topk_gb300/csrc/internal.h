@@ -48,6 +48,7 @@ struct Plan {
     int32_t* x_sums;       // A8W4-INT: sum of each x pool row's codes [pool_rows]
     int32_t* a_sums;       // A8W4-INT: sum of each A pool row's codes [pool_rows]
     uint16_t* comb;        // bf16 [T*K, H]
+    int32_t* ffn_counters; // moe_expert_ffn: [pool_rows/128] route tiles, then [T] tokens
     float act_clamp;       // SwiGLU inputs clipped to [-act_clamp, act_clamp]; +inf: no clamp
     float* gates;          // shared experts: [T*K] gates, the routed ones then 1 per shared slot
 };
@@ -83,7 +84,7 @@ cudaError_t launch_l2_tc(const Plan& p, const void* w2, const void* w2_scale, co
 bool tc_supported(const Plan& p, int stage);
 // S3-S5 of the bf16 mode in one cooperative launch (L1 -> L2 dependency counters)
 cudaError_t launch_ffn_fused_tc(const Plan& p, const void* w1, const void* w2, const float* topk_weights,
-                                cudaStream_t s);
+                                uint16_t* y, cudaStream_t s);
 
 // Tensor-core path of the integer modes (int8 or int4 weights converted to f16 in shared
 // memory, the tokens' f16 planes; every partial sum an exact integer).

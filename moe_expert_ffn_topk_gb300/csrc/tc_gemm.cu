@@ -16,13 +16,17 @@
 // H columns; the epilogue multiplies row p by G[row_src[p]] in fp32 and stores bf16 to the
 // combine row of (token, slot).
 //
-// L1 and L2 in one launch (the DeepGEMM page's L1 -> L2 dependency counters, §5): the fused
-// instantiation runs every L1 tile, then every L2 tile, over one static round-robin order, so
-// each CTA finishes its L1 tiles before it starts on L2. An L2 tile needs the A rows of its
-// 128-row route tile from all I/128 L1 tiles of that route tile: the L1 epilogue publishes each
-// finished tile with a release increment of the route tile's counter, and the L2 producer waits
-// (bounded) until the count is complete before its TMA reads A. The launch is cooperative, so
-// every CTA is resident and the L1 tiles an L2 tile waits for are always making progress.
+// L1, L2 and the combine in one launch (the DeepGEMM page's single kernel with dependency
+// counters, §5): the fused instantiation runs every L1 tile, then every L2 tile, over one
+// static round-robin order, so each CTA finishes its L1 tiles before it starts on L2, and then
+// every warp combines tokens. An L2 tile needs the A rows of its 128-row route tile from all
+// I/128 L1 tiles of that route tile: the L1 epilogue publishes each finished tile with a release
+// increment of the route tile's counter, and the L2 producer waits (bounded) until the count is
+// complete before its TMA reads A. A token's combine needs its routed rows from every L2 column
+// block: each L2 epilogue thread publishes its row with an increment of the token's counter,
+// and the combining warp waits (bounded) for (its unmasked slots) x (column blocks). CTAs whose
+// L2 tiles end early combine while others are still in L2. The launch is cooperative, so every
+// CTA is resident and every wait is on work that earlier positions of the order hold.
 //
 // Warp roles (192 threads): warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer,
 // warps 2-5 = epilogue (warp w reads TMEM lanes 32*(w%4) .. 32*(w%4)+31).
@@ -69,9 +73,12 @@ struct TcArgs {
     int k_blocks;               // K / 64
     int k_rows;                 // rows of one expert's weight in its 2-D view (L1: H, L2: I)
     int b_one_box;              // B map brings a stage's four 64-column blocks in one copy
-    // fused launch: the L2 stage's figures, and the per-route-tile count of finished L1 tiles
+    // fused launch: the L2 stage's figures, the per-route-tile count of finished L1 tiles, and
+    // (when y is given) the per-token count of finished combine rows and the output
     int n_tiles2, k_blocks2, k_rows2, b_one_box2;
     int32_t* l1_done;
+    int32_t* token_done;
+    uint16_t* y;
 };
 
 constexpr int kL2 = 0, kL1 = 1, kFusedL1L2 = 2;  // what one launch runs
@@ -365,10 +372,86 @@ __global__ void __launch_bounds__(kThreads, 1)
                     st_global_v8_if(src >= 0, out + c * 32, packed);
                     st_global_v8_if(src >= 0, out + c * 32 + 16, packed + 8);
                 }
+                if (kFused && args.y != nullptr && src >= 0) {  // publish this combine row's columns
+                    __threadfence();
+                    atomicAdd(args.token_done + src / p.K, 1);
+                }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty_bar(a));
+        }
+    }
+
+    if constexpr (kFused) {
+        if (args.y != nullptr) {
+            // ---------------- combine (S6), every warp ----------------
+            // y[t] = bf16( sum over the unmasked slots k of comb[t*K + k] ), fp32 in slot order (as
+            // the combine kernel); the rows were written by other CTAs, so they are read through
+            // L2 once the token's count is complete
+            __syncwarp();
+            constexpr int kWarps = kThreads / 32;
+            const int K = p.K, row_vecs = p.H / 8;
+            const uint4* comb = reinterpret_cast<const uint4*>(p.comb);
+            uint4* y = reinterpret_cast<uint4*>(args.y);
+            for (int t = blockIdx.x * kWarps + warp; t < p.T && !*abort_flag; t += gridDim.x * kWarps) {
+                const int sr = lane < K ? __ldg(p.slot_row + (int64_t)t * K + lane) : -1;
+                const unsigned valid = __ballot_sync(0xffffffffu, sr >= 0);
+                const int target = __popc(valid) * args.n_tiles2;
+                int ok = 1;
+                if (lane == 0) {
+                    const uint64_t t0 = globaltimer_ns();
+                    while (ld_acquire_gpu(args.token_done + t) < target) {
+                        if (*abort_flag) {
+                            ok = 0;
+                            break;
+                        }
+                        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+                            record_error(p.hdr, MOE_ERR_TIMEOUT);
+                            *abort_flag = 1;
+                            ok = 0;
+                            break;
+                        }
+                        __nanosleep(128);
+                    }
+                }
+                if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+                // four vectors per lane in flight: every slot's load is issued before the adds
+                constexpr int kV = 4;
+                for (int v0 = lane; v0 < row_vecs; v0 += 32 * kV) {
+                    float acc[kV][8];
+#pragma unroll
+                    for (int u = 0; u < kV; ++u)
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) acc[u][j] = 0.0f;
+                    for (int k = 0; k < K; ++k) {
+                        if (!((valid >> k) & 1u)) continue;  // masked route: contributes nothing
+                        const uint4* row = comb + ((int64_t)t * K + k) * row_vecs;
+                        uint4 c[kV];
+#pragma unroll
+                        for (int u = 0; u < kV; ++u) c[u] = v0 + 32 * u < row_vecs ? __ldcg(row + v0 + 32 * u) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                        for (int u = 0; u < kV; ++u) {
+                            const uint32_t w[4] = {c[u].x, c[u].y, c[u].z, c[u].w};
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                acc[u][2 * j] = __fadd_rn(acc[u][2 * j], __uint_as_float(w[j] << 16));
+                                acc[u][2 * j + 1] = __fadd_rn(acc[u][2 * j + 1], __uint_as_float(w[j] & 0xffff0000u));
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < kV; ++u) {
+                        if (v0 + 32 * u >= row_vecs) break;
+                        uint32_t o[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            o[j] = (uint32_t)float_to_bf16_bits(acc[u][2 * j]) |
+                                   ((uint32_t)float_to_bf16_bits(acc[u][2 * j + 1]) << 16);
+                        y[(int64_t)t * row_vecs + v0 + 32 * u] = make_uint4(o[0], o[1], o[2], o[3]);
+                    }
+                }
+            }
         }
     }
 
@@ -453,7 +536,7 @@ cudaError_t launch_l1_tc(const Plan& p, const void* w1, const void*, cudaStream_
     if (!make_map(&a, p.x_pool, (uint64_t)p.H, (uint64_t)p.pool_rows, kBM)) return cudaErrorInvalidValue;
     if (!make_b_map(&b, w1, (uint64_t)2 * p.I, (uint64_t)p.E * p.H, (uint64_t)p.I, true, &one_box))
         return cudaErrorInvalidValue;
-    TcArgs args{p, nullptr, p.I / 128, p.H / kBK, p.H, one_box, 0, 0, 0, 0, nullptr};
+    TcArgs args{p, nullptr, p.I / 128, p.H / kBK, p.H, one_box, 0, 0, 0, 0, nullptr, nullptr, nullptr};
     return launch_tc<kL1>(p, a, b, args, s);
 }
 
@@ -463,12 +546,12 @@ cudaError_t launch_l2_tc(const Plan& p, const void* w2, const void*, const float
     if (!make_map(&a, p.a_pool, (uint64_t)p.I, (uint64_t)p.pool_rows, kBM)) return cudaErrorInvalidValue;
     if (!make_b_map(&b, w2, (uint64_t)p.H, (uint64_t)p.E * p.I, (uint64_t)p.H, false, &one_box))
         return cudaErrorInvalidValue;
-    TcArgs args{p, topk_weights, p.H / kBN, p.I / kBK, p.I, one_box, 0, 0, 0, 0, nullptr};
+    TcArgs args{p, topk_weights, p.H / kBN, p.I / kBK, p.I, one_box, 0, 0, 0, 0, nullptr, nullptr, nullptr};
     return launch_tc<kL2>(p, a, b, args, s);
 }
 
 cudaError_t launch_ffn_fused_tc(const Plan& p, const void* w1, const void* w2, const float* topk_weights,
-                                cudaStream_t s) {
+                                uint16_t* y, cudaStream_t s) {
     CUtensorMap a1, b1, a2, b2;
     int one_box1 = 0, one_box2 = 0;
     if (!make_map(&a1, p.x_pool, (uint64_t)p.H, (uint64_t)p.pool_rows, kBM) ||
@@ -476,14 +559,13 @@ cudaError_t launch_ffn_fused_tc(const Plan& p, const void* w1, const void* w2, c
         !make_map(&a2, p.a_pool, (uint64_t)p.I, (uint64_t)p.pool_rows, kBM) ||
         !make_b_map(&b2, w2, (uint64_t)p.H, (uint64_t)p.E * p.I, (uint64_t)p.H, false, &one_box2))
         return cudaErrorInvalidValue;
-    // The L1 -> L2 counters, one per 128-row route tile, live in the plan's position scratch:
-    // it holds T*K ints, at least the route tile count, and nothing reads it once the plan is
-    // built. They start at zero for every launch.
+    // the counters (one per 128-row route tile, then one per token) start at zero every launch
     const int64_t route_tiles = p.pool_rows / kBM;
-    cudaError_t e = cudaMemsetAsync(p.pos, 0, sizeof(int32_t) * (size_t)route_tiles, s);
+    cudaError_t e = cudaMemsetAsync(p.ffn_counters, 0, sizeof(int32_t) * (size_t)(route_tiles + p.T), s);
     if (e != cudaSuccess) return e;
     if ((e = set_smem_attr<kFusedL1L2>()) != cudaSuccess) return e;
-    TcArgs args{p, topk_weights, p.I / 128, p.H / kBK, p.H, one_box1, p.H / kBN, p.I / kBK, p.I, one_box2, p.pos};
+    TcArgs args{p,          topk_weights, p.I / 128,        p.H / kBK, p.H, one_box1, p.H / kBN, p.I / kBK, p.I,
+                one_box2,   p.ffn_counters, p.ffn_counters + route_tiles, y};
     // every CTA resident at once (cooperative launch): an L2 tile waits only for L1 tiles that
     // earlier positions of the same round-robin order hold, all of them running
     int per_sm = 0;

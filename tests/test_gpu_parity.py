@@ -629,6 +629,27 @@ def test_fused_l1_l2_equals_the_separate_stages(moe, wl):
     assert_close(y_numpy(y1), oracle_forward(wl, inp), wl.mode)
 
 
+def test_fused_launch_without_y_leaves_the_combine_rows(moe):
+    """moe_expert_ffn without y: L1 and L2 in one launch, the combine rows left in the workspace for
+    moe_combine; with y the launch also combines. Both equal the separate stages bit for bit."""
+    wl = FUSED_CASES[1]
+    inp = make_inputs(wl, device=DEV)
+    y_ref, st = _forward_flags(moe, wl, inp, 0)
+    assert st == 0
+    d = moe.dims(wl.T, wl.H, wl.I, wl.E, wl.K)
+    for with_y in (False, True):
+        ws = moe.alloc_workspace(d, wl.mode, DEV)
+        y = torch.full((wl.T, wl.H), float("nan"), dtype=torch.bfloat16, device=DEV)
+        moe.moe_plan(inp["topk_ids"], d, ws)
+        moe.moe_dispatch(inp["x"], inp["x_scale"], d, wl.mode, ws)
+        moe.moe_expert_ffn(inp["w1"], inp["w1_scale"], inp["w2"], inp["w2_scale"], inp["topk_weights"], d, wl.mode, ws,
+                           y=y if with_y else None)
+        if not with_y:
+            moe.moe_combine(y, d, ws)
+        assert moe.moe_check_device_error(ws) == 0
+        assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16)), with_y
+
+
 def test_fused_full_size_equals_the_separate_stages(moe):
     wl = WORKLOADS["mixtral_bf16_prefill"]
     inp = make_inputs(wl, device=DEV)
