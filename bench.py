@@ -111,9 +111,22 @@ def oracle_sample(wl, inp_host, n_tokens, seed, quantize_x=False):
     return dt, int((ids >= 0).sum())
 
 
-def cpu_tokens_per_sample(wl):
-    # a handful of tokens: the oracle's cost is dominated by decoding each touched expert
-    return 2 if wl.H * wl.I >= 4096 * 8192 else 8
+def sample_tokens_for(wl, h, seconds, quantize_x=False, seed=5):
+    """Tokens per oracle sample for about `seconds` of oracle time (at least 1, at most the
+    workload's tokens). The oracle's time is close to a + b*n for n tokens (a: decoding the
+    touched experts' weights, b: the per-token rows), so two probes fix a and b."""
+    n1, n2 = 1, min(8, wl.T)
+    t1, _ = oracle_sample(wl, h, n1, seed=seed, quantize_x=quantize_x)
+    t2, _ = oracle_sample(wl, h, n2, seed=seed + 1, quantize_x=quantize_x)
+    b = max((t2 - t1) / max(n2 - n1, 1), 1e-4)
+    a = max(t1 - b * n1, 0.0)
+    return int(max(1, min(wl.T, (seconds - a) / b)))
+
+
+# whole reference-arm run (warm-up + timed steps): about this many seconds of oracle time
+REFERENCE_RUN_SECONDS = 150.0
+# the cpu_baseline leg of the GB300 arm: one sample of about this many seconds
+CPU_BASELINE_SECONDS = 12.0
 
 
 def host_inputs(wl):
@@ -127,7 +140,8 @@ def run_reference(args, wl, rank, world):
     if rank != 0:
         return None
     h = host_inputs(wl)
-    n_tok = cpu_tokens_per_sample(wl)
+    n_tok = sample_tokens_for(wl, h, REFERENCE_RUN_SECONDS / max(args.steps + args.warmup, 1),
+                              quantize_x=args.quantize_x)
     for w in range(args.warmup):
         oracle_sample(wl, h, n_tok, seed=1000 + w, quantize_x=args.quantize_x)
     total_t, total_rows = 0.0, 0
@@ -498,10 +512,12 @@ def main():
     if line is not None and not args.no_cpu_baseline:
         from workloads import to_numpy
         h = to_numpy(inp)
-        # size the sample for about 10 s of oracle time from a 2-token probe
-        dt0, _ = oracle_sample(wl, h, min(2, wl.T), seed=6, quantize_x=args.quantize_x)
-        n_tok = int(max(2, min(wl.T, 64, round(2 * 10.0 / max(dt0, 1e-3)))))
+        # one sample of about 10-30 s of oracle time; re-sized once if it came out short
+        n_tok = sample_tokens_for(wl, h, CPU_BASELINE_SECONDS, quantize_x=args.quantize_x)
         dt, rows = oracle_sample(wl, h, n_tok, seed=7, quantize_x=args.quantize_x)
+        if dt < 0.6 * CPU_BASELINE_SECONDS and n_tok < wl.T:
+            n_tok = int(min(wl.T, max(n_tok + 1, n_tok * CPU_BASELINE_SECONDS / dt)))
+            dt, rows = oracle_sample(wl, h, n_tok, seed=8, quantize_x=args.quantize_x)
         line["cpu_baseline"] = {"value": 6.0 * wl.H * wl.I * rows / dt / 1e12, "unit": "TFLOP/s",
                                 "cores": oracle_threads(), "kind": "oracle",
                                 "sample": f"{n_tok} seeded tokens ({rows} routed rows) of {wl.name}, "
