@@ -122,10 +122,16 @@ enum {
                                    same results up to fp32 summation order, for comparison */
     MOE_FLAG_QUANTIZE_X = 4u,   /* moe_forward: x.data is bf16 [T,H] (x.scale unused) and the
                                    dispatch stage quantises it as moe_dispatch_quantize does */
-    MOE_FLAG_FUSED = 8u         /* moe_forward: S3-S6 through moe_expert_ffn (one launch: L1 -> L2 ->
+    MOE_FLAG_FUSED = 8u,        /* moe_forward: S3-S6 through moe_expert_ffn (one launch: L1 -> L2 ->
                                    combine dependency counters). A16W16 only; other modes return
                                    MOE_ERR_UNSUPPORTED, and with MOE_FLAG_SIMT it is
                                    MOE_ERR_INVALID_ARG. Same results as the separate stages. */
+    MOE_FLAG_SINGLE_CTA = 16u,  /* A16W16: the L2 GEMM on one-CTA 128-row tiles instead of CTA pairs
+                                   (256-row tiles, tcgen05 cta_group::2); same results bit for bit,
+                                   for comparison. The fused launch always uses one-CTA tiles. */
+    MOE_FLAG_PAIR_L1 = 32u      /* A16W16: the L1 GEMM on CTA pairs too (by default it runs on
+                                   one-CTA tiles, measured faster at the power cap); same results
+                                   bit for bit. Ignored with MOE_FLAG_SINGLE_CTA. */
 };
 
 /* Bytes of workspace that moe_plan / moe_forward and the stage calls need for `d` and `m`.

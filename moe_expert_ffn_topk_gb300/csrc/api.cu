@@ -218,7 +218,9 @@ static moe_status expert_l1(moe_operand w1, const moe_dims* d, moe_dtype_mode m,
     if (d->num_tokens == 0) return MOE_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
-    if (!(flags & MOE_FLAG_SIMT) && tc_supported(p, 1)) {
+    if ((flags & MOE_FLAG_PAIR_L1) && !(flags & (MOE_FLAG_SIMT | MOE_FLAG_SINGLE_CTA)) && pair_supported(p, 1)) {
+        e = launch_l1_pair(p, w1.data, s);
+    } else if (!(flags & MOE_FLAG_SIMT) && tc_supported(p, 1)) {
         e = launch_l1_tc(p, w1.data, w1.scale, s);
     } else if (!(flags & MOE_FLAG_SIMT) && bs_supported(p, 1)) {
         e = launch_l1_bs(p, w1.data, w1.scale, (flags & MOE_FLAG_WEIGHT_MAJOR) != 0, s);
@@ -256,6 +258,8 @@ moe_status moe_expert_l2(moe_operand w2, const float* topk_weights, const moe_di
         if (e != cudaSuccess) return from_cuda(e);
         topk_weights = p.gates;
     }
+    if (!(flags & (MOE_FLAG_SIMT | MOE_FLAG_SINGLE_CTA)) && pair_supported(p, 2))
+        return from_cuda(launch_l2_pair(p, w2.data, topk_weights, s));
     if (!(flags & MOE_FLAG_SIMT) && tc_supported(p, 2))
         return from_cuda(launch_l2_tc(p, w2.data, w2.scale, topk_weights, s));
     if (!(flags & MOE_FLAG_SIMT) && bs_supported(p, 2))

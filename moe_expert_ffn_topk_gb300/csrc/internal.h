@@ -82,6 +82,10 @@ cudaError_t launch_l1_tc(const Plan& p, const void* w1, const void* w1_scale, cu
 cudaError_t launch_l2_tc(const Plan& p, const void* w2, const void* w2_scale, const float* topk_weights,
                          cudaStream_t s);
 bool tc_supported(const Plan& p, int stage);
+// bf16 L1 / L2 on CTA pairs (tcgen05.mma.cta_group::2); same outputs as launch_l1_tc / launch_l2_tc
+bool pair_supported(const Plan& p, int stage);
+cudaError_t launch_l1_pair(const Plan& p, const void* w1, cudaStream_t s);
+cudaError_t launch_l2_pair(const Plan& p, const void* w2, const float* topk_weights, cudaStream_t s);
 // S3-S5 of the bf16 mode in one cooperative launch (L1 -> L2 dependency counters)
 cudaError_t launch_ffn_fused_tc(const Plan& p, const void* w1, const void* w2, const float* topk_weights,
                                 uint16_t* y, cudaStream_t s);

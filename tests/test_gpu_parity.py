@@ -622,7 +622,7 @@ def test_fused_l1_l2_equals_the_separate_stages(moe, wl):
     if wl.name == "fused_one_expert_all_rows":
         inp["topk_ids"][:] = 1                  # 700 rows on one expert: 6 route tiles, the last ragged
         inp["topk_ids"][::7] = -1               # and some masked routes
-    y0, st0 = _forward_flags(moe, wl, inp, 0)
+    y0, st0 = _forward_flags(moe, wl, inp, moe.MOE_FLAG_SINGLE_CTA)
     y1, st1 = _forward_flags(moe, wl, inp, moe.MOE_FLAG_FUSED)
     assert st0 == 0 and st1 == 0
     assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
@@ -634,7 +634,7 @@ def test_fused_launch_without_y_leaves_the_combine_rows(moe):
     moe_combine; with y the launch also combines. Both equal the separate stages bit for bit."""
     wl = FUSED_CASES[1]
     inp = make_inputs(wl, device=DEV)
-    y_ref, st = _forward_flags(moe, wl, inp, 0)
+    y_ref, st = _forward_flags(moe, wl, inp, moe.MOE_FLAG_SINGLE_CTA)
     assert st == 0
     d = moe.dims(wl.T, wl.H, wl.I, wl.E, wl.K)
     for with_y in (False, True):
@@ -653,7 +653,7 @@ def test_fused_launch_without_y_leaves_the_combine_rows(moe):
 def test_fused_full_size_equals_the_separate_stages(moe):
     wl = WORKLOADS["mixtral_bf16_prefill"]
     inp = make_inputs(wl, device=DEV)
-    y0, st0 = _forward_flags(moe, wl, inp, 0)
+    y0, st0 = _forward_flags(moe, wl, inp, moe.MOE_FLAG_SINGLE_CTA)
     y1, st1 = _forward_flags(moe, wl, inp, moe.MOE_FLAG_FUSED)
     assert st0 == 0 and st1 == 0
     assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
@@ -667,7 +667,7 @@ def test_fused_with_clamp_shared_experts_and_quantizing_dispatch(moe):
     inp = make_inputs(wl, device=DEV, shared=1)
     for flags in (0, moe.MOE_FLAG_QUANTIZE_X):
         x = inp["x_bf16"] if flags else None
-        y0, st0 = _forward_flags(moe, wl, inp, flags, shared=1, clamp=0.5, x=x)
+        y0, st0 = _forward_flags(moe, wl, inp, flags | moe.MOE_FLAG_SINGLE_CTA, shared=1, clamp=0.5, x=x)
         y1, st1 = _forward_flags(moe, wl, inp, flags | moe.MOE_FLAG_FUSED, shared=1, clamp=0.5, x=x)
         assert st0 == 0 and st1 == 0
         assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
@@ -693,3 +693,58 @@ def test_fused_flag_rejections(moe):
     with pytest.raises(moe.MoeError) as err:
         _forward_flags(moe, wl, inp, moe.MOE_FLAG_FUSED | moe.MOE_FLAG_SIMT)
     assert err.value.status == 1  # MOE_ERR_INVALID_ARG
+
+
+# ---------------------------------------------------------------------------------------
+# bf16 GEMMs on CTA pairs (the default) against one-CTA tiles (MOE_FLAG_SINGLE_CTA): each
+# output element is the same sequence of 16-K tensor-core products in the same order, so the
+# two are compared bit for bit, and both against the oracle
+# ---------------------------------------------------------------------------------------
+
+def _pair_case_ids(wl, inp):
+    ids = inp["topk_ids"]
+    if wl.name == "pair_odd_tile_then_expert":
+        # expert 0: 300 rows (three route tiles, so its last pair's odd half lies on expert 1's
+        # first tile), expert 1: 130 rows, expert 2: 130 rows
+        ids[:300] = 0
+        ids[300:430] = 1
+        ids[430:] = 2
+    elif wl.name == "pair_odd_tile_last":
+        ids[:130] = 0        # two route tiles, one pair
+        ids[130:] = 1        # three route tiles: the last pair's odd half is past the pool's tiles
+    elif wl.name == "pair_sparse":
+        ids[:, 0] = 5        # two busy experts (three route tiles each), one with a single
+        ids[:, 1] = 7        # tile whose pair's odd half lies on expert 5, the others empty
+        ids[::5, 0] = 1
+        ids[::11, 1] = -1    # masked routes
+    return inp
+
+
+PAIR_CASES = FUSED_CASES + [
+    Workload("pair_odd_tile_then_expert", "a16w16", 560, 512, 384, 3, 1, 44, 0.05),
+    Workload("pair_odd_tile_last", "a16w16", 430, 512, 384, 4, 1, 45, 0.05),
+    Workload("pair_sparse", "a16w16", 333, 768, 256, 12, 2, 46, 0.05)]
+
+
+@pytest.mark.parametrize("wl", PAIR_CASES, ids=[w.name for w in PAIR_CASES])
+def test_pair_tiles_equal_single_cta_tiles(moe, wl):
+    """Default (L2 on pairs) and MOE_FLAG_PAIR_L1 (both stages on pairs) against one-CTA tiles."""
+    inp = _pair_case_ids(wl, make_inputs(wl, device=DEV))
+    y0, st0 = _forward_flags(moe, wl, inp, moe.MOE_FLAG_SINGLE_CTA)
+    assert st0 == 0
+    for flags in (0, moe.MOE_FLAG_PAIR_L1):
+        y1, st1 = _forward_flags(moe, wl, inp, flags)
+        assert st1 == 0
+        assert torch.equal(y0.view(torch.int16), y1.view(torch.int16)), flags
+    assert_close(y_numpy(y1), oracle_forward(wl, inp), wl.mode)
+
+
+def test_pair_tiles_full_size_equal_single_cta_tiles(moe):
+    wl = WORKLOADS["mixtral_bf16_prefill"]
+    inp = make_inputs(wl, device=DEV)
+    y0, st0 = _forward_flags(moe, wl, inp, moe.MOE_FLAG_SINGLE_CTA)
+    assert st0 == 0
+    for flags in (0, moe.MOE_FLAG_PAIR_L1):
+        y1, st1 = _forward_flags(moe, wl, inp, flags)
+        assert st1 == 0
+        assert torch.equal(y0.view(torch.int16), y1.view(torch.int16)), flags
