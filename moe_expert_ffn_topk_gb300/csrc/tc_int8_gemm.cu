@@ -10,9 +10,12 @@
 //   converter warps expand them to f16 (q ^ 0x80 placed under the exponent of 1024 gives
 //   1152 + q exactly; one f16 subtraction removes the 1152), in the 128-byte-swizzled K-major
 //   layout of the MMA;
-// - one tile is 128 weight rows x 128 tokens; its B tile holds the tokens' hi rows, then their
-//   lo rows (N = 256), so |partial sum| <= 15 * 128 * K < 2^24 for K <= 8704, and the epilogue
-//   rebuilds the exact accumulator as 16 * D_hi + D_lo in int32 before the fp32 dequantisation.
+// - one tile is 128 weight rows x the n tokens of one route tile rounded up to 16 (n16 <= 128);
+//   its B tile holds the tokens' hi rows, then their lo rows (N = 2 * n16), so |partial sum| <=
+//   15 * 128 * K < 2^24 for K <= 8704, and the epilogue rebuilds the exact accumulator as
+//   16 * D_hi + D_lo in int32 before the fp32 dequantisation. An expert's last route tile is
+//   usually partial (on average half of it is padding), and its MMAs cover only n16 tokens: full
+//   tiles take the 128-row token box, partial ones n16 / 16 boxes of 16 rows per plane.
 // Weight-major orientation as in the block-scaled kernel: M = weight rows; L1 tiles carry the
 // gate block and the up block of the same 128 outputs (two accumulators sharing B), L2 tiles two
 // 128-row blocks of hidden columns.
@@ -54,14 +57,22 @@ constexpr int kMiscOff = kBarOff + 8 * kNumBars;
 constexpr int kTileOffOff = kMiscOff + 16;
 constexpr int kCountsOff = kTileOffOff + 4 * (kMaxExperts + 1);
 constexpr int kTabOff = kCountsOff + 4 * kMaxExperts;  // L2 epilogue: per warp [slot, gate, s^A] x 128 rows
+constexpr int kTokBox = 16;  // token rows per TMA box of a partial tile
 constexpr size_t kSmem = 1024 + (size_t)kTabOff + 4 * 3 * 4 * kTok;
 static_assert(kSmem <= 232448, "shared memory");
 // largest K with every partial sum below 2^24: |lo * w| <= 15 * 128
 constexpr int kMaxK = 8704;
 
 // kind::f16 instruction descriptor: D fp32 (bits 4-5 = 1), A and B f16 (formats 0), both
-// K-major, N = 256 (>> 3 in bits 17-22), M = 128 (>> 4 in bits 24-28).
-constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(256 >> 3) << 17) | ((uint32_t)(kWR >> 4) << 24);
+// K-major, N = 2 * n16 (>> 3 in bits 17-22, set per tile), M = 128 (>> 4 in bits 24-28).
+constexpr uint32_t kIdescM = (1u << 4) | ((uint32_t)(kWR >> 4) << 24);
+__device__ __forceinline__ uint32_t idesc_n(int n) { return kIdescM | ((uint32_t)(n >> 3) << 17); }
+
+// Tokens of a route tile rounded up to 16 (the B rows of each plane that its MMAs use).
+__device__ __forceinline__ int tile_n16(const int* counts, int e, int m) {
+    const int n = min(kTok, counts[e] - m * kTok);
+    return min(kTok, (n + 15) & ~15);
+}
 
 struct I8Args {
     Plan p;
@@ -135,7 +146,8 @@ __device__ __forceinline__ int exact_int(uint32_t hi_bits, uint32_t lo_bits) {
 
 template <bool kL1>
 __global__ void __launch_bounds__(kThreads, 1)
-    tc_int8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, I8Args args) {
+    tc_int8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                   const __grid_constant__ CUtensorMap tmX16, I8Args args) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = smem_u32(smem_raw);
     const uint32_t base = (raw_base + 1023u) & ~1023u;
@@ -154,10 +166,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
     int* tile_off = reinterpret_cast<int*>(smem + kTileOffOff);
+    int* counts = reinterpret_cast<int*>(smem + kCountsOff);
 
     const Plan& p = args.p;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int i = threadIdx.x; i <= p.E; i += kThreads) tile_off[i] = p.tile_off[i];
+    for (int i = threadIdx.x; i < p.E; i += kThreads) counts[i] = p.counts[i];
     if (threadIdx.x == 0) {
         for (int i = 0; i < kRawStages; ++i) {
             mbar_init(raw_full(i), 1);
@@ -228,10 +242,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     const uint32_t dst = base + kTokOff + b * kTokBytes;
-                    mbar_arrive_expect_tx(tok_full(b), (uint32_t)kTokBytes);
-                    // one copy per plane: each TMA instruction costs the issuing thread ~75 cycles
-                    for (int pl = 0; pl < 2; ++pl)
-                        tma_load_2d(dst + pl * kTok * 128, &tmX, kb * kBK, (int)(pl * p.pool_rows) + tl.row0, tok_full(b));
+                    const int n16 = tile_n16(counts, tl.e, tl.m);
+                    mbar_arrive_expect_tx(tok_full(b), (uint32_t)(2 * n16 * 128));
+                    if (n16 == kTok) {
+                        // one copy per plane: each TMA instruction costs the issuing thread ~75 cycles
+                        for (int pl = 0; pl < 2; ++pl)
+                            tma_load_2d(dst + pl * kTok * 128, &tmX, kb * kBK, (int)(pl * p.pool_rows) + tl.row0,
+                                        tok_full(b));
+                    } else {
+                        // hi rows [0, n16), lo rows [n16, 2 n16): one contiguous B operand of N = 2 n16
+                        for (int pl = 0; pl < 2; ++pl)
+                            for (int j = 0; j < n16; j += kTokBox)
+                                tma_load_2d(dst + (pl * n16 + j) * 128, &tmX16, kb * kBK,
+                                            (int)(pl * p.pool_rows) + tl.row0 + j, tok_full(b));
+                    }
                 }
             }
             for (int j = it - kTokStages < 0 ? 0 : it - kTokStages; j < it; ++j)
@@ -239,30 +263,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
+        // This thread feeds the tensor pipe, so its per-stage work is kept short: a non-blocking
+        // test of each barrier before the bounded wait, ring positions kept as counters, and
+        // descriptors advanced by adding to their address field (start >> 4: +2 per 16 K of a
+        // K-major tile, + the stage's offset >> 4).
         if (lane == 0) {
-            int it = 0, tc = 0;
+            const uint64_t ad0 = kmajor_desc(base + kHfOff, 0), bd0 = kmajor_desc(base + kTokOff, 0);
+            int b = 0, tb = 0, tc = 0;
+            uint32_t hph = 0, tph = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tc) {
                 if (!mbar_wait(acc_empty, ((uint32_t)tc & 1u) ^ 1u, p.hdr, abort_flag)) break;
                 tc_fence_after();
-                for (int kb = 0; kb < KB; ++kb, ++it) {
-                    const int b = it % kHfStages, tb = it % kTokStages;
-                    if (!mbar_wait(hf_full(b), (uint32_t)(it / kHfStages) & 1u, p.hdr, abort_flag) ||
-                        !mbar_wait(tok_full(tb), (uint32_t)(it / kTokStages) & 1u, p.hdr, abort_flag)) {
+                const Tile tl = decode(t, tile_off, p.E, args.n_slabs);
+                const uint32_t idesc = idesc_n(2 * tile_n16(counts, tl.e, tl.m));
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!(mbar_test(hf_full(b), hph) || mbar_wait(hf_full(b), hph, p.hdr, abort_flag)) ||
+                        !(mbar_test(tok_full(tb), tph) || mbar_wait(tok_full(tb), tph, p.hdr, abort_flag))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa0 = base + kHfOff + b * kABytes, sa1 = sa0 + kWR * 128;
-                    const uint32_t sb = base + kTokOff + tb * kTokBytes;
+                    const uint64_t ad = ad0 + (uint64_t)((b * kABytes) >> 4);
+                    const uint64_t bd = bd0 + (uint64_t)((tb * kTokBytes) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
-                        const uint64_t bd = kmajor_desc(sb, kk);
-                        tc_mma(tmem_base, kmajor_desc(sa0, kk), bd, kIdesc, (kb | kk) != 0);
-                        tc_mma(tmem_base + 256, kmajor_desc(sa1, kk), bd, kIdesc, (kb | kk) != 0);
+                        tc_mma(tmem_base, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+                        tc_mma(tmem_base + 256, ad + ((kWR * 128) >> 4) + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
                     }
                     tc_commit(hf_empty(b));
                     tc_commit(tok_empty(tb));
+                    if (++b == kHfStages) b = 0, hph ^= 1u;
+                    if (++tb == kTokStages) tb = 0, tph ^= 1u;
                 }
                 if (ok) tc_commit(acc_full);
             }
@@ -307,7 +339,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int tc = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++tc) {
             const Tile tl = decode(t, tile_off, p.E, args.n_slabs);
-            const int n_valid = min(kTok, p.counts[tl.e] - tl.m * kTok);
+            const int n_valid = min(kTok, counts[tl.e] - tl.m * kTok);
+            const int n16 = min(kTok, (n_valid + 15) & ~15);  // lo plane columns start here
             float sx_l[kTok / 32];
             float sg = 0.0f, su = 0.0f, s2[2] = {0.0f, 0.0f};
             if constexpr (kL1) {
@@ -343,21 +376,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16);
             if constexpr (kL1) {
-                // C = 16 D_hi + D_lo; H = (C * s^W1) * s^X; A = SiLU(H_gate) * H_up, all 128 tokens
-                // (padding tokens come out finite and are never read back as results)
+                // C = 16 D_hi + D_lo; H = (C * s^W1) * s^X; A = SiLU(H_gate) * H_up for the tile's
+                // 32-token chunks up to n16 (the padding rows' values are never read back as results)
                 const int j = tl.s * kWR + q * 32 + lane;
 #pragma unroll
                 for (int ci = 0; ci < kTok / 32; ++ci) {
                     const int c0 = 32 * ci;
+                    if (c0 >= n16) break;  // uniform across the warp
                     uint32_t hi[32], lo[32];
                     float hg[32];
                     tmem_ld32(tb + c0, hi);
-                    tmem_ld32(tb + kTok + c0, lo);
+                    tmem_ld32(tb + n16 + c0, lo);
                     tmem_ld_wait();
 #pragma unroll
                     for (int tt = 0; tt < 32; ++tt) hg[tt] = __int2float_rn(exact_int(hi[tt], lo[tt]));
                     tmem_ld32(tb + 256 + c0, hi);
-                    tmem_ld32(tb + 256 + kTok + c0, lo);
+                    tmem_ld32(tb + 256 + n16 + c0, lo);
                     tmem_ld_wait();
 #pragma unroll
                     for (int tt = 0; tt < 32; ++tt) {
@@ -379,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int h = tl.s * 2 * kWR + blk * kWR + q * 32 + lane;
                         uint32_t hi[32], lo[32];
                         tmem_ld32(tb + blk * 256 + c0, hi);
-                        tmem_ld32(tb + blk * 256 + kTok + c0, lo);
+                        tmem_ld32(tb + blk * 256 + n16 + c0, lo);
                         tmem_ld_wait();
 #pragma unroll
                         for (int tt = 0; tt < 32; ++tt) {  // slot < 0 past the routed rows
@@ -413,18 +447,21 @@ cudaError_t launch_int8(const Plan& p, const void* w, const void* w_scale, const
     if (attr_err != cudaSuccess) return attr_err;
     const int n_out = kL1 ? 2 * p.I : p.H;
     const int kin = kL1 ? p.H : p.I;
-    CUtensorMap tmW, tmX;
+    CUtensorMap tmW, tmX, tmX16;
     if (!tc_make_map_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w, (uint64_t)kin, (uint64_t)p.E * n_out, kBK, kWR,
                         CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
     if (!tc_make_map_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, kL1 ? (const void*)p.x_planes : (const void*)p.a_planes,
-                        (uint64_t)kin, 2 * (uint64_t)p.pool_rows, kBK, kTok, CU_TENSOR_MAP_SWIZZLE_128B))
+                        (uint64_t)kin, 2 * (uint64_t)p.pool_rows, kBK, kTok, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !tc_make_map_2d(&tmX16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                        kL1 ? (const void*)p.x_planes : (const void*)p.a_planes, (uint64_t)kin,
+                        2 * (uint64_t)p.pool_rows, kBK, kTokBox, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     I8Args args{p, static_cast<const float*>(w_scale), topk_weights, kL1 ? p.I / kWR : p.H / (2 * kWR), kin / kBK,
                 n_out};
     const int64_t max_tiles = (p.pool_rows / kTok) * args.n_slabs;
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(max_tiles, tc_num_sms()));
-    tc_int8_kernel<kL1><<<grid, kThreads, kSmem, s>>>(tmW, tmX, args);
+    tc_int8_kernel<kL1><<<grid, kThreads, kSmem, s>>>(tmW, tmX, tmX16, args);
     return cudaGetLastError();
 }
 

@@ -234,29 +234,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
+        // (per-stage work kept short: a non-blocking test of each barrier before the bounded
+        // wait, ring positions kept as counters, descriptors advanced by adding to their address
+        // field: start >> 4, +2 per 16 K of a K-major tile, + the stage's offset >> 4)
         if (lane == 0) {
-            int it = 0, tc = 0;
+            const uint64_t ad0 = kmajor_desc(base + kTokOff, 0), bd0 = kmajor_desc(base + kHfOff, 0);
+            int b = 0, tb = 0, tc = 0;
+            uint32_t hph = 0, tph = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tc) {
                 const int a = tc & 1;
                 if (!mbar_wait(acc_empty(a), ((uint32_t)(tc >> 1) & 1u) ^ 1u, p.hdr, abort_flag)) break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(a * kWN);
-                for (int kb = 0; kb < KB; ++kb, ++it) {
-                    const int b = it % kHfStages, tb = it % kTokStages;
-                    if (!mbar_wait(hf_full(b), (uint32_t)(it / kHfStages) & 1u, p.hdr, abort_flag) ||
-                        !mbar_wait(tok_full(tb), (uint32_t)(it / kTokStages) & 1u, p.hdr, abort_flag)) {
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!(mbar_test(hf_full(b), hph) || mbar_wait(hf_full(b), hph, p.hdr, abort_flag)) ||
+                        !(mbar_test(tok_full(tb), tph) || mbar_wait(tok_full(tb), tph, p.hdr, abort_flag))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = base + kTokOff + tb * kTokBytes;
-                    const uint32_t sb = base + kHfOff + b * kHfBytes;
+                    const uint64_t ad = ad0 + (uint64_t)((tb * kTokBytes) >> 4);
+                    const uint64_t bd = bd0 + (uint64_t)((b * kHfBytes) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk)
-                        tc_mma(d, kmajor_desc(sa, kk), kmajor_desc(sb, kk), kIdesc, (kb | kk) != 0);
+                    for (int kk = 0; kk < kBK / 16; ++kk) tc_mma(d, ad + 2 * kk, bd + 2 * kk, kIdesc, (kb | kk) != 0);
                     tc_commit(hf_empty(b));
                     tc_commit(tok_empty(tb));
+                    if (++b == kHfStages) b = 0, hph ^= 1u;
+                    if (++tb == kTokStages) tb = 0, tph ^= 1u;
                 }
                 if (ok) tc_commit(acc_full(a));
             }
