@@ -245,8 +245,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
+        // At decode sizes this thread sets the pace (eight MMAs of N = 16 per 32 KB stage), so
+        // its per-stage work is kept short: a non-blocking test of the stage before the bounded
+        // wait, the stage position kept as a counter, the tile's four instruction descriptors
+        // made once, and the operand descriptors advanced by adding to their address field
+        // (start >> 4: +2 per 32 K of a K-major atom, + the atom's and the stage's offset >> 4).
         if (lane == 0) {
-            int it = 0, tc = 0;
+            const uint64_t ad0 = kmajor_desc(base, 0), bd0 = kmajor_desc(base + kAtoms * kABytes, 0);
+            int s = 0, tc = 0;
+            uint32_t ph = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tc) {
                 const int a = tc & 1;
@@ -255,23 +262,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const Tile tl = tile_of(t);
                 const int n = (tl.n_valid + 15) & ~15;
                 const uint32_t d = tmem_base + (uint32_t)(a * kNT);
-                for (int kb = 0; kb < KB; ++kb, ++it) {
-                    const int s = it % kStages;
-                    if (!mbar_wait(full_bar(s), (uint32_t)(it / kStages) & 1u, p.hdr, abort_flag)) {
+                uint32_t idesc[kAtomK / 32];
+#pragma unroll
+                for (int kk = 0; kk < kAtomK / 32; ++kk) idesc[kk] = bs_idesc(kAfmt, kBfmt, n, kk);
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!(mbar_test(full_bar(s), ph) || mbar_wait(full_bar(s), ph, p.hdr, abort_flag))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = base + s * Cfg::kStageBytes, sb = sa + kAtoms * kABytes;
+                    const uint64_t so = (uint64_t)((s * Cfg::kStageBytes) >> 4);
                     const uint32_t sf = tmem_base + kSfCol0 + s * kSfColsPerStage;
                     const int na = atoms_of(kb);
                     for (int at = 0; at < na; ++at) {
+                        const uint64_t ad = ad0 + so + (uint64_t)((at * kABytes) >> 4);
+                        const uint64_t bd = bd0 + so + (uint64_t)((at * Cfg::kBBytes) >> 4);
 #pragma unroll
                         for (int kk = 0; kk < kAtomK / 32; ++kk)
-                            tc_mma_bs(d, kmajor_desc(sa + at * kABytes, kk), kmajor_desc(sb + at * Cfg::kBBytes, kk),
-                                      bs_idesc(kAfmt, kBfmt, n, kk), sf + 8 * at, sf + 8 * at + 4, (kb | at | kk) != 0);
+                            tc_mma_bs(d, ad + 2 * kk, bd + 2 * kk, idesc[kk], sf + 8 * at, sf + 8 * at + 4,
+                                      (kb | at | kk) != 0);
                     }
                     tc_commit(empty_bar(s));
+                    if (++s == kStages) s = 0, ph ^= 1u;
                 }
                 if (ok) tc_commit(acc_full(a));
             }

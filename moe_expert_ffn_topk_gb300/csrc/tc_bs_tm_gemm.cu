@@ -283,28 +283,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
+        // (per-stage work kept short: a non-blocking test of the stage before the bounded wait,
+        // the stage position kept as a counter, descriptors advanced by adding to their address
+        // field: start >> 4, +2 per 32 K of a K-major atom, + the stage's offset >> 4)
         if (lane == 0) {
-            int it = 0, tc = 0;
+            const uint64_t ad0 = kmajor_desc(base, 0), bd0 = kmajor_desc(base + kTokBytes, 0);
+            uint32_t idesc[kAtomK / 32];
+#pragma unroll
+            for (int kk = 0; kk < kAtomK / 32; ++kk) idesc[kk] = tm_idesc(kAfmt, kBfmt, kWN, kk);
+            int s = 0, tc = 0;
+            uint32_t ph = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tc) {
                 const int a = tc % kAccs;
                 if (!mbar_wait(acc_empty(a), ((uint32_t)(tc / kAccs) & 1u) ^ 1u, p.hdr, abort_flag)) break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(a * kWN);
-                for (int kb = 0; kb < KB; ++kb, ++it) {
-                    const int s = it % kStages;
-                    if (!mbar_wait(full_bar(s), (uint32_t)(it / kStages) & 1u, p.hdr, abort_flag)) {
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!(mbar_test(full_bar(s), ph) || mbar_wait(full_bar(s), ph, p.hdr, abort_flag))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = base + s * kStageBytes, sb = sa + kTokBytes;
+                    const uint64_t so = (uint64_t)((s * kStageBytes) >> 4);
                     const uint32_t sf = tmem_base + kSfCol0 + s * kSfColsPerStage;
 #pragma unroll
                     for (int kk = 0; kk < kAtomK / 32; ++kk)
-                        tm_mma(d, kmajor_desc(sa, kk), kmajor_desc(sb, kk), tm_idesc(kAfmt, kBfmt, kWN, kk), sf, sf + 4,
-                               (kb | kk) != 0);
+                        tm_mma(d, ad0 + so + 2 * kk, bd0 + so + 2 * kk, idesc[kk], sf, sf + 4, (kb | kk) != 0);
                     tc_commit(empty_bar(s));
+                    if (++s == kStages) s = 0, ph ^= 1u;
                 }
                 if (ok) tc_commit(acc_full(a));
             }
