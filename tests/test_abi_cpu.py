@@ -34,6 +34,20 @@ def test_exports_every_declared_symbol(moe):
         assert hasattr(lib, name), name
 
 
+def _header_enum(prefix):
+    src = open(os.path.join(ROOT, "include", "moe_ffn.h")).read()
+    return {name: int(val) for name, val in re.findall(r"\b(" + prefix + r"\w*)\s*=\s*(\d+)u?\b", src)}
+
+
+def test_binding_constants_match_the_header(moe):
+    """The binding's flag and mode values are the header's enum values (nothing is renumbered)."""
+    flags = _header_enum("MOE_FLAG_")
+    assert flags and all(getattr(moe, name) == val for name, val in flags.items()), flags
+    assert len(set(flags.values())) == len(flags)
+    modes = _header_enum("MOE_A")
+    assert sorted(modes.values()) == sorted(moe.MODES.values()) == list(range(len(modes)))
+
+
 def test_status_strings(moe):
     assert moe.moe_status_string(0) == "ok"
     assert "timed out" in moe.moe_status_string(5)

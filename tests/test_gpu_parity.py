@@ -107,14 +107,36 @@ def test_dispatch_gathers_rows(moe):
     assert sorted(int(v) for v in pool_src[:n_pad] if v >= 0) == list(range(wl.T * wl.K))
 
 
+# Per-expert row counts that put an expert's last route tile at the edges of the INT8 kernel's
+# token granularity (1, 16, 17, 127 tokens; 128, 129 and 255 spill into a second tile).
+TAIL_COUNTS = [1, 16, 17, 127, 128, 129, 255]
+
+
+def _tail_inputs(mode, seed):
+    wl = Workload(f"tail_{mode}", mode, sum(TAIL_COUNTS), 512, 256, len(TAIL_COUNTS), 1, seed, 0.05)
+    inp = make_inputs(wl, device=DEV)
+    inp["topk_ids"] = torch.repeat_interleave(torch.arange(wl.E, dtype=torch.int32),
+                                              torch.tensor(TAIL_COUNTS))[:, None].to(DEV).contiguous()
+    return wl, inp
+
+
 @pytest.mark.parametrize("mode", ["a8w8_int8", "a8w4_int"])
-def test_int8_l2_accumulators_exact(moe, mode):
+@pytest.mark.parametrize("case", ["ragged", "tail_sizes"])
+def test_int8_l2_accumulators_exact(moe, mode, case):
     """D = A^int8 . W2 must be the exact integer product: recompute the weighted rows from the
     kernel's own A^int8 and s^A with an integer GEMM and the page's fp32 dequant order, and
-    require bit equality (int8 or int4 weights)."""
-    wl = CASES[mode][1]
-    inp = make_inputs(wl, device=DEV)
+    require bit equality (int8 or int4 weights). The tail case gives the experts 1, 16, 17, 127,
+    128, 129 and 255 rows, and also checks y against the oracle."""
+    if case == "ragged":
+        wl = CASES[mode][1]
+        inp = make_inputs(wl, device=DEV)
+    else:
+        wl, inp = _tail_inputs(mode, 47)
     out = run_forward(moe, wl, inp, stages=True)
+    assert out["status"] == 0
+    if case == "tail_sizes":
+        check_plan(out, wl, inp["topk_ids"])
+        assert_close(y_numpy(out["y"]), oracle_forward(wl, inp), wl.mode)
     L = out["layout"]
     rows = L["pool_rows"]
     ws = out["ws"]
