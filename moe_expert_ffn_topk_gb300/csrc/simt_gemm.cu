@@ -20,6 +20,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tc_common.cuh"  // tc_num_sms
 
 namespace moe {
 
@@ -245,36 +246,31 @@ __global__ void __launch_bounds__(NT) l2_simt_kernel(Plan p, const uint8_t* __re
 // (floored at 1e-8), q = round-half-even(A/s) clamped to [-127, 127]; fp32 IEEE division
 // throughout. Besides the int8 codes it writes the tensor-core operand planes: hi and lo for
 // INT8; for A8W4-INT the codes as f16 in the order of w4_plane_pos, and the row's code sum.
-__global__ void __launch_bounds__(256) int8_row_quant_kernel(Plan p) {
-    __shared__ float red[8];
-    __shared__ int red_sum[8];
+// One warp per row: the amax and the code sum are warp reductions (no block barrier), and the
+// second pass re-reads the row, which the first pass left in L1.
+constexpr int kRqWarps = 8;
+__global__ void __launch_bounds__(32 * kRqWarps) int8_row_quant_kernel(Plan p) {
     const int rows = p.hdr[kHdrPadRows];
-    const int I = p.I, nv = p.I / 4;  // float4 vectors of a row
-    for (int r = blockIdx.x; r < rows; r += gridDim.x) {
-        if (__ldg(p.pool_src + r) < 0) continue;  // padding row (uniform across the block): never read back
+    const int I = p.I, nv = p.I / 4;  // float4 vectors of a row (a multiple of 32)
+    const int lane = threadIdx.x & 31;
+    const bool split = p.mode == MOE_A8W8_INT8;  // A8W4-INT: plane 0 holds q itself
+    for (int r = blockIdx.x * kRqWarps + (threadIdx.x >> 5); r < rows; r += gridDim.x * kRqWarps) {
+        if (__ldg(p.pool_src + r) < 0) continue;  // padding row (uniform across the warp): never read back
         const float4* a = reinterpret_cast<const float4*>(p.a_f32 + (int64_t)r * I);
         float m = 0.0f;
-        for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+        for (int v = lane; v < nv; v += 32) {
             const float4 x = a[v];
             m = fmaxf(m, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
         }
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
-        __syncthreads();
-        float amax = red[0];
-#pragma unroll
-        for (int w = 1; w < 8; ++w) amax = fmaxf(amax, red[w]);
-        __syncthreads();
-        const float s = fmaxf(__fdiv_rn(amax, 127.0f), 1e-8f);
+        const float s = fmaxf(__fdiv_rn(m, 127.0f), 1e-8f);
         uint32_t* q = reinterpret_cast<uint32_t*>(p.a_pool + (int64_t)r * I);   // 4 codes per word
         uint2* hi = reinterpret_cast<uint2*>(p.a_planes + (int64_t)r * I);      // plane 0: floor(q/16), f16
         uint2* lo = reinterpret_cast<uint2*>(p.a_planes + (p.pool_rows + r) * I);  // plane 1: q mod 16, f16
-        const bool split = p.mode == MOE_A8W8_INT8;  // A8W4-INT: plane 0 holds q itself
         int code_sum = 0;
-        // nv is a multiple of 8 and blockDim even: lanes 2m and 2m + 1 hold the two halves of a
-        // group of 8 codes together
-        for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+        // lanes 2m and 2m + 1 hold the two halves of a group of 8 codes together
+        for (int v = lane; v < nv; v += 32) {
             const float4 x = a[v];
             const float xv[4] = {x.x, x.y, x.z, x.w};
             uint32_t qw = 0, h[2] = {0, 0}, l[2] = {0, 0};
@@ -293,7 +289,7 @@ __global__ void __launch_bounds__(256) int8_row_quant_kernel(Plan p) {
                 lo[v] = make_uint2(l[0], l[1]);
             } else {
                 // q0 q4 q1 q5 from the even lane of the pair, q2 q6 q3 q7 from the odd one
-                const bool odd = threadIdx.x & 1;
+                const bool odd = lane & 1;
                 const uint32_t got = __shfl_xor_sync(0xffffffffu, odd ? h[0] : h[1], 1);
                 const uint32_t mine = odd ? h[1] : h[0];
                 hi[v] = odd ? make_uint2((got & 0xffffu) | (mine << 16), (got >> 16) | (mine & 0xffff0000u))
@@ -302,19 +298,11 @@ __global__ void __launch_bounds__(256) int8_row_quant_kernel(Plan p) {
                             (int)(int8_t)((qw >> 16) & 0xff) + (int)(int8_t)(qw >> 24);
             }
         }
-        if (threadIdx.x == 0) reinterpret_cast<float*>(p.a_pool_scale)[r] = s;
+        if (lane == 0) reinterpret_cast<float*>(p.a_pool_scale)[r] = s;
         if (!split) {
 #pragma unroll
             for (int o = 16; o >= 1; o >>= 1) code_sum += __shfl_xor_sync(0xffffffffu, code_sum, o);
-            if ((threadIdx.x & 31) == 0) red_sum[threadIdx.x >> 5] = code_sum;
-            __syncthreads();
-            if (threadIdx.x == 0) {
-                int t = 0;
-#pragma unroll
-                for (int w = 0; w < 8; ++w) t += red_sum[w];
-                p.a_sums[r] = t;
-            }
-            __syncthreads();
+            if (lane == 0) p.a_sums[r] = code_sum;
         }
     }
 }
@@ -364,8 +352,9 @@ cudaError_t launch_l2_simt(const Plan& p, const void* w2, const void* w2_scale, 
 
 cudaError_t launch_int8_row_quant(const Plan& p, cudaStream_t s) {
     if (p.pool_rows == 0) return cudaSuccess;
-    const int grid = (int)std::min<int64_t>(p.pool_rows, 152 * 8);
-    int8_row_quant_kernel<<<grid, 256, 0, s>>>(p);
+    // a row per warp, 64 rows in flight per SM (8 resident blocks of 8 warps)
+    const int grid = (int)std::min<int64_t>((p.pool_rows + kRqWarps - 1) / kRqWarps, (int64_t)tc_num_sms() * 8);
+    int8_row_quant_kernel<<<grid, 32 * kRqWarps, 0, s>>>(p);
     return cudaGetLastError();
 }
 

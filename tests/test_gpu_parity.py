@@ -149,6 +149,15 @@ def test_int8_l2_accumulators_exact(moe, mode, case):
     g = h["topk_weights"].reshape(-1)
     n_pad = int(region(ws, L, "header", torch.int32, 16).cpu().numpy()[2])
     assert np.abs(a_q[:n_pad][pool_src[:n_pad] >= 0].astype(np.int32)).max() <= 127
+    # the row quantiser, from the kernel's own fp32 A: s = max(amax / 127, 1e-8) and
+    # q = clip(rint(A / s), -127, 127), every step an IEEE fp32 operation (numpy float32 divides
+    # with round-to-nearest-even; rint rounds half to even)
+    routed_rows = np.nonzero(pool_src[:n_pad] >= 0)[0]
+    a32 = region(ws, L, "a_f32", torch.float32, rows * wl.I).view(rows, wl.I).cpu().numpy()[routed_rows]
+    s_ref = np.maximum(np.abs(a32).max(axis=1) / np.float32(127.0), np.float32(1e-8)).astype(np.float32)
+    q_ref = np.clip(np.rint(a32 / s_ref[:, None]), -127, 127).astype(np.int8)
+    assert np.array_equal(s_a[routed_rows], s_ref)
+    assert np.array_equal(a_q[routed_rows], q_ref)
     if mode == "a8w4_int":  # the row quantiser's plane and code sums of the same codes
         routed = np.nonzero(pool_src[:n_pad] >= 0)[0]
         _check_w4_operands(ws, L, "a_pool_planes", 1, rows, wl.I, routed, a_q[routed].astype(np.int64))
