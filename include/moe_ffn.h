@@ -119,7 +119,9 @@ enum {
     MOE_FLAG_SIMT = 1u,         /* run the CUDA-core reference GEMMs instead of the tensor-core ones */
     MOE_FLAG_WEIGHT_MAJOR = 2u, /* FP8 modes at prefill sizes: 128 weight rows x 128 tokens per tile
                                    (the decode-style tile) instead of 128 tokens x 256 weight rows;
-                                   same results up to fp32 summation order, for comparison */
+                                   same results up to fp32 summation order, for comparison.
+                                   A8W4-INT: weight-major tiles (128 weight rows x up to 256 tokens)
+                                   whatever the tile count (see MOE_FLAG_TOKEN_MAJOR); same bits */
     MOE_FLAG_QUANTIZE_X = 4u,   /* moe_forward: x.data is bf16 [T,H] (x.scale unused) and the
                                    dispatch stage quantises it as moe_dispatch_quantize does */
     MOE_FLAG_FUSED = 8u,        /* moe_forward: S3-S6 through moe_expert_ffn (one launch: L1 -> L2 ->
@@ -129,9 +131,13 @@ enum {
     MOE_FLAG_SINGLE_CTA = 16u,  /* A16W16: the L2 GEMM on one-CTA 128-row tiles instead of CTA pairs
                                    (256-row tiles, tcgen05 cta_group::2); same results bit for bit,
                                    for comparison. The fused launch always uses one-CTA tiles. */
-    MOE_FLAG_PAIR_L1 = 32u      /* A16W16: the L1 GEMM on CTA pairs too (by default it runs on
+    MOE_FLAG_PAIR_L1 = 32u,     /* A16W16: the L1 GEMM on CTA pairs too (by default it runs on
                                    one-CTA tiles, measured faster at the power cap); same results
                                    bit for bit. Ignored with MOE_FLAG_SINGLE_CTA. */
+    MOE_FLAG_TOKEN_MAJOR = 64u  /* A8W4-INT: token-major tiles (128 pool rows x 256 weight rows)
+                                   where weight-major ones (128 weight rows x up to 256 tokens) would
+                                   run: experts x weight slabs of at least four rounds of tiles on
+                                   the GPU. Same results bit for bit, for comparison. */
 };
 
 /* Bytes of workspace that moe_plan / moe_forward and the stage calls need for `d` and `m`.

@@ -7,7 +7,7 @@ without the built library raises ImportError: there is no fallback path.
 import torch
 
 from ._binding import (ABI_FUNCTIONS, MODES, MOE_FLAG_FUSED, MOE_FLAG_NONE, MOE_FLAG_PAIR_L1,  # noqa: F401
-                       MOE_FLAG_QUANTIZE_X, MOE_FLAG_SIMT, MOE_FLAG_SINGLE_CTA,
+                       MOE_FLAG_QUANTIZE_X, MOE_FLAG_SIMT, MOE_FLAG_SINGLE_CTA, MOE_FLAG_TOKEN_MAJOR,
                        MOE_FLAG_WEIGHT_MAJOR, MoeDims, MoeError, MoeOptions, dims, moe_check_device_error,
                        moe_combine, moe_debug_bounded_wait, moe_dispatch, moe_dispatch_quantize, moe_expert_l1,
                        moe_expert_l1_ex, moe_expert_l2, moe_expert_ffn, moe_forward, moe_forward_ex, moe_plan, moe_plan_noalloc,

@@ -19,7 +19,7 @@ MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_BAD_ROUT
     MOE_ERR_WORKSPACE = range(7)
 MODES = {"a16w16": 0, "a8w8_fp8": 1, "a8w8_int8": 2, "a8w4_fp8_fp4": 3, "a8w4_int": 4, "a8w8_fp8_e5m2": 5}
 (MOE_FLAG_NONE, MOE_FLAG_SIMT, MOE_FLAG_WEIGHT_MAJOR, MOE_FLAG_QUANTIZE_X, MOE_FLAG_FUSED, MOE_FLAG_SINGLE_CTA,
- MOE_FLAG_PAIR_L1) = 0, 1, 2, 4, 8, 16, 32
+ MOE_FLAG_PAIR_L1, MOE_FLAG_TOKEN_MAJOR) = 0, 1, 2, 4, 8, 16, 32, 64
 
 ABI_FUNCTIONS = ("moe_workspace_bytes", "moe_plan", "moe_dispatch", "moe_expert_l1", "moe_expert_l2",
                  "moe_combine", "moe_forward", "moe_check_device_error", "moe_status_string",

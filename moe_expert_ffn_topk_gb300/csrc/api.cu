@@ -226,6 +226,9 @@ static moe_status expert_l1(moe_operand w1, const moe_dims* d, moe_dtype_mode m,
         e = launch_l1_bs(p, w1.data, w1.scale, (flags & MOE_FLAG_WEIGHT_MAJOR) != 0, s);
     } else if (!(flags & MOE_FLAG_SIMT) && int8_tc_supported(p, 1)) {
         e = launch_l1_int8_tc(p, w1.data, w1.scale, s);
+    } else if (!(flags & (MOE_FLAG_SIMT | MOE_FLAG_TOKEN_MAJOR)) && w4_wm_supported(p, 1) &&
+               ((flags & MOE_FLAG_WEIGHT_MAJOR) || w4_wm_preferred(p, 1))) {
+        e = launch_l1_w4_wm(p, w1.data, w1.scale, s);
     } else if (!(flags & MOE_FLAG_SIMT) && w4_tc_supported(p, 1)) {
         e = launch_l1_w4_tc(p, w1.data, w1.scale, s);
     } else {
@@ -266,6 +269,9 @@ moe_status moe_expert_l2(moe_operand w2, const float* topk_weights, const moe_di
         return from_cuda(launch_l2_bs(p, w2.data, w2.scale, topk_weights, (flags & MOE_FLAG_WEIGHT_MAJOR) != 0, s));
     if (!(flags & MOE_FLAG_SIMT) && int8_tc_supported(p, 2))
         return from_cuda(launch_l2_int8_tc(p, w2.data, w2.scale, topk_weights, s));
+    if (!(flags & (MOE_FLAG_SIMT | MOE_FLAG_TOKEN_MAJOR)) && w4_wm_supported(p, 2) &&
+        ((flags & MOE_FLAG_WEIGHT_MAJOR) || w4_wm_preferred(p, 2)))
+        return from_cuda(launch_l2_w4_wm(p, w2.data, w2.scale, topk_weights, s));
     if (!(flags & MOE_FLAG_SIMT) && w4_tc_supported(p, 2))
         return from_cuda(launch_l2_w4_tc(p, w2.data, w2.scale, topk_weights, s));
     return from_cuda(launch_l2_simt(p, w2.data, w2.scale, topk_weights, s));

@@ -102,6 +102,12 @@ cudaError_t launch_l1_w4_tc(const Plan& p, const void* w1, const void* w1_scale,
 cudaError_t launch_l2_w4_tc(const Plan& p, const void* w2, const void* w2_scale, const float* topk_weights,
                             cudaStream_t s);
 bool w4_tc_supported(const Plan& p, int stage);
+// A8W4-INT weight-major (M = weight rows, N = up to 256 tokens of an expert); same results
+bool w4_wm_supported(const Plan& p, int stage);
+bool w4_wm_preferred(const Plan& p, int stage);
+cudaError_t launch_l1_w4_wm(const Plan& p, const void* w1, const void* w1_scale, cudaStream_t s);
+cudaError_t launch_l2_w4_wm(const Plan& p, const void* w2, const void* w2_scale, const float* topk_weights,
+                            cudaStream_t s);
 
 // Position of code k of a row in the A8W4-INT f16 operand planes: within each group of 8, code
 // i < 4 goes to position 2i and code 4 + i to position 2i + 1.

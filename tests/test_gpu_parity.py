@@ -779,3 +779,26 @@ def test_pair_tiles_full_size_equal_single_cta_tiles(moe):
         y1, st1 = _forward_flags(moe, wl, inp, flags)
         assert st1 == 0
         assert torch.equal(y0.view(torch.int16), y1.view(torch.int16)), flags
+
+
+# ---------------------------------------------------------------------------------------
+# A8W4-INT: weight-major tiles (MOE_FLAG_WEIGHT_MAJOR; the default when the experts' weight slabs
+# fill four rounds of tiles) against token-major ones (MOE_FLAG_TOKEN_MAJOR): both compute the
+# same exact integers and the same fp32 operations, so y is compared bit for bit
+# ---------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("case", ["tiny", "ragged", "tail_sizes", "full_size"])
+def test_w4_weight_major_equals_token_major(moe, case):
+    if case == "tail_sizes":
+        wl, inp = _tail_inputs("a8w4_int", 48)
+    else:
+        wl = {"tiny": CASES["a8w4_int"][0], "ragged": CASES["a8w4_int"][1], "full_size": WORKLOADS["int4_a8w4"]}[case]
+        inp = make_inputs(wl, device=DEV)
+    y0, st0 = _forward_flags(moe, wl, inp, moe.MOE_FLAG_TOKEN_MAJOR)
+    y1, st1 = _forward_flags(moe, wl, inp, moe.MOE_FLAG_WEIGHT_MAJOR)
+    y2, st2 = _forward_flags(moe, wl, inp, 0)  # the tile-count rule's choice
+    assert st0 == 0 and st1 == 0 and st2 == 0
+    assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
+    assert torch.equal(y0.view(torch.int16), y2.view(torch.int16))
+    if case != "full_size":
+        assert_close(y_numpy(y1), oracle_forward(wl, inp), wl.mode)
