@@ -802,3 +802,18 @@ def test_w4_weight_major_equals_token_major(moe, case):
     assert torch.equal(y0.view(torch.int16), y2.view(torch.int16))
     if case != "full_size":
         assert_close(y_numpy(y1), oracle_forward(wl, inp), wl.mode)
+
+
+# The largest expert count the ABI takes (E = 1024) with the largest top-k (K = 32): about two rows
+# per expert, so every kernel's per-expert tables, scans and tile searches run at their limits.
+MAX_E = [Workload(f"max_experts_{m}", m, 64, 256, 128, 1024, 32, 49, 0.05)
+         for m in ("a16w16", "a8w8_fp8", "a8w8_int8", "a8w4_int", "a8w4_fp8_fp4")]
+
+
+@pytest.mark.parametrize("wl", MAX_E, ids=[w.name for w in MAX_E])
+def test_max_experts_and_topk(moe, wl):
+    inp = make_inputs(wl, device=DEV)
+    out = run_forward(moe, wl, inp, stages=True)
+    assert out["status"] == 0
+    check_plan(out, wl, inp["topk_ids"])
+    assert_close(y_numpy(out["y"]), oracle_forward(wl, inp), wl.mode)
