@@ -133,6 +133,17 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, uint32_t a0, uint32_t a
                  : "memory");
 }
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync %0, 128;" ::"n"(kEpiBar) : "memory"); }
+// The same barrier, ANDing `pred` over the four epilogue warps: they leave the tile loop together,
+// since a warp that left alone would keep the others waiting at the next epi_sync.
+__device__ __forceinline__ bool epi_all(bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %1, 0;\n\tbar.red.and.pred q, %2, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((int)pred), "n"(kEpiBar)
+        : "memory");
+    return r != 0;
+}
 
 template <int MODE, bool kL1, int kNT, int kStages, int kAtoms>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -444,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int ci = 0; ci < kChunks; ++ci) g_l[ci] = src_l[ci] >= 0 ? __ldg(args.topk_weights + src_l[ci]) : 0.0f;
             }
             const bool w_ok = mbar_wait(acc_full(a), (uint32_t)(tc >> 1) & 1u, p.hdr, abort_flag);
-            if (!__all_sync(0xffffffffu, w_ok)) break;
+            if (!epi_all(w_ok)) break;  // one decision for the four warps (they share epi_sync)
             tc_fence_after();
             const int n = (tl.n_valid + 15) & ~15;
             const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * kNT);
