@@ -41,7 +41,10 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="mixtral_bf16_prefill")
-    ap.add_argument("--flags", type=int, default=0, help="GEMM stage flags (1 = CUDA-core reference kernels)")
+    ap.add_argument("--flags", type=int, default=0,
+                    help="GEMM stage flags, MOE_FLAG_* of the C ABI: 1 CUDA-core reference kernels, 2 weight-major "
+                         "tiles (FP8 modes at prefill sizes; A8W4-INT at any tile count), 16 one-CTA bf16 L2, "
+                         "32 bf16 L1 on CTA pairs, 64 token-major A8W4-INT")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", type=int, default=None, help="override the workload's token count")
     ap.add_argument("--experts", type=int, default=None, help="override the workload's expert count")
