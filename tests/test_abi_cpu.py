@@ -148,3 +148,35 @@ def test_binding_rejects_host_tensors(moe):
     d = moe.dims(64, 256, 128, 8, 2)
     with pytest.raises(ValueError):
         moe.moe_plan(torch.zeros((64, 2), dtype=torch.int32), d, torch.zeros(1 << 20, dtype=torch.uint8))
+
+
+def test_header_is_a_c_abi(moe, tmp_path):
+    """A C99 program includes include/moe_ffn.h (no CUDA or C++ headers needed), links the library and
+    calls its host-only functions; the workspace size equals the binding's."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "abi.c"
+    src.write_text(
+        '#include "moe_ffn.h"\n#include <stdio.h>\n'
+        "int main(void) {\n"
+        "    moe_dims d = {0};\n"
+        "    d.num_tokens = 300; d.hidden = 512; d.intermediate = 384; d.num_experts = 6; d.topk = 2;\n"
+        "    printf(\"%zu %zu %s\\n\", moe_workspace_bytes(&d, MOE_A16W16), moe_workspace_bytes(&d, MOE_A8W4_INT),\n"
+        "           moe_status_string(MOE_ERR_TIMEOUT));\n"
+        "    return 0;\n}\n")
+    lib_dir = os.path.dirname(moe._binding._LIB_PATH)
+    lib_name = os.path.basename(moe._binding._LIB_PATH)[3:-3]  # libNAME.so -> NAME
+    exe = tmp_path / "abi"
+    cc = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.join(ROOT, "include"),
+                         str(src), "-L", lib_dir, "-l" + lib_name, "-o", str(exe)], capture_output=True, text=True)
+    assert cc.returncode == 0, cc.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True, env=dict(os.environ, LD_LIBRARY_PATH=lib_dir))
+    assert run.returncode == 0, run.stderr
+    bf16, w4, msg = run.stdout.split(maxsplit=2)
+    d = moe.dims(300, 512, 384, 6, 2)
+    assert int(bf16) == moe.moe_workspace_bytes(d, "a16w16")
+    assert int(w4) == moe.moe_workspace_bytes(d, "a8w4_int")
+    assert msg.strip() == moe.moe_status_string(5)
