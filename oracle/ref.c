@@ -1,0 +1,102 @@
+/* Plain C definition of the route plan and of the A16W16 expert feed-forward with top-k combine.
+ *
+ * TEST INFRASTRUCTURE ONLY: a second, independent statement of what oracle/moe.py computes for
+ * the plan and the A16W16 mode, written with plain loops in double precision, which the CPU tests
+ * compare with it. Nothing in the product path links or loads it; it shares no code with the
+ * CUDA path.
+ *
+ * Ascend mega_moe page, "Computation Process", A16W16 use case:
+ *   EP Dispatch: the rows routed to expert e, I_e = {(i, k) : E[i,k] = e}, N_e = |I_e|, stacked in
+ *     ascending i*K + k (a stable counting sort: count, exclusive prefix sum, scatter);
+ *   Linear1: H = X_e . W1[e] (W1[e] is hidden x 2*intermediate);
+ *   SwiGLU: A = SiLU(H[:, :I]) * H[:, I:], SiLU(z) = z / (1 + e^-z);
+ *   Linear2: Y_e = A . W2[e] with A rounded to bf16 (both GEMMs take bf16 operands);
+ *   Token Combine: c[i,k] = bf16(fp32(G[i,k] * Y_e[row(i,k)])), y_i = bf16(sum over k = 0..K-1 of
+ *     c[i,k] in fp32, in slot order). A masked route (id -1) contributes nothing.
+ * Everything else runs in double precision. These are the readings oracle/moe.py states.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+/* Nearest bf16 value (ties to even) of a double, as a double: bf16 keeps 8 significant bits, the
+ * spacing in [2^e, 2^(e+1)) is 2^(e-7), below 2^-126 it stays 2^-133; beyond the largest finite
+ * bf16 (plus half a spacing) the value rounds to infinity. */
+static double round_to_bf16(double v) {
+    if (!isfinite(v)) return v;
+    int ex;
+    frexp(v, &ex); /* |v| in [2^(ex-1), 2^ex) */
+    int e = ex - 1 < -126 ? -126 : ex - 1;
+    const double q = ldexp(1.0, e - 7);
+    const double r = nearbyint(v / q) * q; /* the default rounding mode: half to even */
+    const double bf16_max = (2.0 - ldexp(1.0, -7)) * ldexp(1.0, 127);
+    return fabs(r) > bf16_max ? copysign(INFINITY, v) : r;
+}
+
+/* counts[E], offsets[E+1], row_src[offsets[E]] of the T x K routing ids; returns 0, or -1 when an
+ * id lies outside [-1, E). */
+int oracle_plan(const int32_t* ids, int64_t T, int64_t K, int64_t E, int64_t* counts, int64_t* offsets,
+                int64_t* row_src) {
+    for (int64_t e = 0; e < E; ++e) counts[e] = 0;
+    for (int64_t r = 0; r < T * K; ++r) {
+        if (ids[r] < -1 || ids[r] >= E) return -1;
+        if (ids[r] >= 0) ++counts[ids[r]];
+    }
+    offsets[0] = 0;
+    for (int64_t e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts[e];
+    int64_t* cursor = (int64_t*)malloc(sizeof(int64_t) * (size_t)(E > 0 ? E : 1));
+    if (!cursor) return -2;
+    for (int64_t e = 0; e < E; ++e) cursor[e] = offsets[e];
+    for (int64_t r = 0; r < T * K; ++r)
+        if (ids[r] >= 0) row_src[cursor[ids[r]]++] = r;
+    free(cursor);
+    return 0;
+}
+
+/* y [T, H] (bf16 values as doubles) of the A16W16 layer. x [T, H], w1 [E, H, 2I], w2 [E, I, H] hold
+ * the decoded bf16 operands, g [T*K] the fp32 gate weights. Returns 0, -1 for a bad id, -2 when
+ * memory runs out. */
+int oracle_forward_a16w16(const double* x, const int32_t* ids, const float* g, const double* w1, const double* w2,
+                          int64_t T, int64_t K, int64_t E, int64_t H, int64_t I, double* y) {
+    int64_t* counts = (int64_t*)malloc(sizeof(int64_t) * (size_t)E);
+    int64_t* offsets = (int64_t*)malloc(sizeof(int64_t) * (size_t)(E + 1));
+    int64_t* row_src = (int64_t*)malloc(sizeof(int64_t) * (size_t)(T * K > 0 ? T * K : 1));
+    double* comb = (double*)calloc((size_t)(T * K * H > 0 ? T * K * H : 1), sizeof(double));
+    double* h = (double*)malloc(sizeof(double) * (size_t)(2 * I));
+    double* a = (double*)malloc(sizeof(double) * (size_t)I);
+    int st = (counts && offsets && row_src && comb && h && a) ? 0 : -2;
+    if (st == 0) st = oracle_plan(ids, T, K, E, counts, offsets, row_src);
+    for (int64_t e = 0; st == 0 && e < E; ++e) {
+        const double* w1e = w1 + e * H * 2 * I;
+        const double* w2e = w2 + e * I * H;
+        for (int64_t p = offsets[e]; p < offsets[e + 1]; ++p) {
+            const int64_t src = row_src[p], tok = src / K;
+            const double* xr = x + tok * H;
+            for (int64_t j = 0; j < 2 * I; ++j) { /* Linear1 */
+                double s = 0.0;
+                for (int64_t c = 0; c < H; ++c) s += xr[c] * w1e[c * 2 * I + j];
+                h[j] = s;
+            }
+            for (int64_t j = 0; j < I; ++j) /* SwiGLU, then the bf16 L2 operand */
+                a[j] = round_to_bf16(h[j] / (1.0 + exp(-h[j])) * h[I + j]);
+            for (int64_t c = 0; c < H; ++c) { /* Linear2, gate, the bf16 combine row */
+                double s = 0.0;
+                for (int64_t j = 0; j < I; ++j) s += a[j] * w2e[j * H + c];
+                comb[src * H + c] = round_to_bf16((double)(float)((double)g[src] * s));
+            }
+        }
+    }
+    for (int64_t t = 0; st == 0 && t < T; ++t) /* Token Combine: fp32 in slot order, one bf16 rounding */
+        for (int64_t c = 0; c < H; ++c) {
+            float acc = 0.0f;
+            for (int64_t k = 0; k < K; ++k) acc = acc + (float)comb[(t * K + k) * H + c];
+            y[t * H + c] = round_to_bf16((double)acc);
+        }
+    free(counts);
+    free(offsets);
+    free(row_src);
+    free(comb);
+    free(h);
+    free(a);
+    return st;
+}

@@ -321,3 +321,69 @@ def test_shared_brute_force_per_token_equals_pooled_path(mode):
     assert rec["counts"].tolist()[wl.E:] == [wl.T, wl.T]
     assert sum(rec["counts"].tolist()[:wl.E]) == wl.T * wl.K
     assert not np.array_equal(y, _forward(mode, d, wl))
+
+
+# ---------------------------------------------------------------------------------------
+# The plain C statement of the plan and of the A16W16 layer (oracle/ref.c) against this module:
+# two independent implementations of the same readings
+# ---------------------------------------------------------------------------------------
+
+def _c_oracle():
+    import ctypes
+    import __graft_entry__
+    lib = ctypes.CDLL(__graft_entry__.build_oracle())
+    i64p = ctypes.POINTER(ctypes.c_int64)
+    lib.oracle_plan.restype = ctypes.c_int
+    lib.oracle_plan.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, i64p, i64p, i64p]
+    lib.oracle_forward_a16w16.restype = ctypes.c_int
+    lib.oracle_forward_a16w16.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int64] * 5 + [ctypes.c_void_p]
+    return lib
+
+
+def _c_plan(lib, ids, E):
+    import ctypes
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    T, K = ids.shape
+    counts, offsets = np.zeros(E, np.int64), np.zeros(E + 1, np.int64)
+    row_src = np.zeros(max(T * K, 1), np.int64)
+    p = lambda a: a.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
+    st = lib.oracle_plan(ids.ctypes.data, T, K, E, p(counts), p(offsets), p(row_src))
+    return st, counts, offsets, row_src[:offsets[-1]]
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_c_plan_equals_numpy_plan(seed):
+    lib = _c_oracle()
+    rng = np.random.default_rng(seed)
+    E = 13
+    ids = rng.integers(-1, E, size=(57, 3)).astype(np.int32)  # including masked routes
+    st, counts, offsets, row_src = _c_plan(lib, ids, E)
+    c2, o2, r2 = moe.plan(ids, E)
+    assert st == 0 and counts.tolist() == c2.tolist() and offsets.tolist() == o2.tolist()
+    assert row_src.tolist() == r2.tolist()
+    ids[5, 1] = E  # an id outside [-1, E)
+    assert _c_plan(lib, ids, E)[0] == -1
+
+
+@pytest.mark.parametrize("case", ["tiny", "ragged_masked"])
+def test_c_forward_a16w16_equals_numpy_forward(case):
+    wl = (Workload("tiny_c", "a16w16", 64, 256, 128, 8, 2, 50, 0.05) if case == "tiny"
+          else Workload("ragged_c", "a16w16", 77, 128, 256, 5, 3, 51, 0.05))
+    h = to_numpy(make_inputs(wl, device="cpu"))
+    ids = np.ascontiguousarray(h["topk_ids"], dtype=np.int32)
+    if case == "ragged_masked":
+        ids[::4, 1] = -1
+    g = np.ascontiguousarray(h["topk_weights"], dtype=np.float32)
+    x = np.ascontiguousarray(codecs.bf16_decode(h["x"]))
+    w1 = np.ascontiguousarray(codecs.bf16_decode(h["w1"]))
+    w2 = np.ascontiguousarray(codecs.bf16_decode(h["w2"]))
+    y = np.zeros((wl.T, wl.H), np.float64)
+    st = _c_oracle().oracle_forward_a16w16(x.ctypes.data, ids.ctypes.data, g.ctypes.data, w1.ctypes.data,
+                                           w2.ctypes.data, wl.T, wl.K, wl.E, wl.H, wl.I, y.ctypes.data)
+    assert st == 0
+    ref = moe.forward("a16w16", h["x"], None, ids, g, h["w1"], None, h["w2"], None, num_experts=wl.E, inter=wl.I)
+    # the same rounding points in both; the float64 sums differ only in their order, which moves
+    # a bf16 or fp32 rounding decision only when a value sits within ~1e-16 of a tie
+    same = np.mean(y == ref)
+    assert same >= 0.999, same
+    assert np.abs(y - ref).max() <= 2.0 ** -7 * np.abs(ref).max()
