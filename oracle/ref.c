@@ -1,8 +1,9 @@
-/* Plain C definition of the route plan and of the A16W16 expert feed-forward with top-k combine.
+/* Plain C definition of the route plan and of the A16W16 and A8W8-INT expert feed-forward with
+ * top-k combine.
  *
  * TEST INFRASTRUCTURE ONLY: a second, independent statement of what oracle/moe.py computes for
- * the plan and the A16W16 mode, written with plain loops in double precision, which the CPU tests
- * compare with it. Nothing in the product path links or loads it; it shares no code with the
+ * the plan and the A16W16 and A8W8-INT modes, written with plain loops in double precision (and
+ * the fp32 roundings the readings fix), which the CPU tests compare with it. Nothing in the product path links or loads it; it shares no code with the
  * CUDA path.
  *
  * Ascend mega_moe page, "Computation Process", A16W16 use case:
@@ -32,6 +33,20 @@ static double round_to_bf16(double v) {
     const double bf16_max = (2.0 - ldexp(1.0, -7)) * ldexp(1.0, 127);
     return fabs(r) > bf16_max ? copysign(INFINITY, v) : r;
 }
+
+/* Token Combine: y_t = bf16(sum over the slots k = 0..K-1 of the bf16 rows comb[t*K + k], in fp32 in
+ * slot order); a masked slot's row is zero. */
+static void combine_tokens(const double* comb, int64_t T, int64_t K, int64_t H, double* y) {
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t c = 0; c < H; ++c) {
+            float acc = 0.0f;
+            for (int64_t k = 0; k < K; ++k) acc = acc + (float)comb[(t * K + k) * H + c];
+            y[t * H + c] = round_to_bf16((double)acc);
+        }
+}
+
+/* The weighted combine row of one routed row: bf16(fp32(G * Y)). */
+static double gated(float g, double yv) { return round_to_bf16((double)(float)((double)g * yv)); }
 
 /* counts[E], offsets[E+1], row_src[offsets[E]] of the T x K routing ids; returns 0, or -1 when an
  * id lies outside [-1, E). */
@@ -82,21 +97,87 @@ int oracle_forward_a16w16(const double* x, const int32_t* ids, const float* g, c
             for (int64_t c = 0; c < H; ++c) { /* Linear2, gate, the bf16 combine row */
                 double s = 0.0;
                 for (int64_t j = 0; j < I; ++j) s += a[j] * w2e[j * H + c];
-                comb[src * H + c] = round_to_bf16((double)(float)((double)g[src] * s));
+                comb[src * H + c] = gated(g[src], s);
             }
         }
     }
-    for (int64_t t = 0; st == 0 && t < T; ++t) /* Token Combine: fp32 in slot order, one bf16 rounding */
-        for (int64_t c = 0; c < H; ++c) {
-            float acc = 0.0f;
-            for (int64_t k = 0; k < K; ++k) acc = acc + (float)comb[(t * K + k) * H + c];
-            y[t * H + c] = round_to_bf16((double)acc);
-        }
+    if (st == 0) combine_tokens(comb, T, K, H, y);
     free(counts);
     free(offsets);
     free(row_src);
     free(comb);
     free(h);
     free(a);
+    return st;
+}
+
+/* y [T, H] of the A8W8-INT layer (Ascend mega_moe page, A8W8-INT use case). x int8 [T, H] with the
+ * fp32 per-token scales x_scale [T]; w1 int8 [E, 2I, H] and w2 int8 [E, H, I] (output channel,
+ * then input) with fp32 per-output-channel scales [E, 2I] and [E, H]; g [T*K] fp32.
+ *   Linear1: C = Q . W1 in integers; H = (C * s^W1) * s^X, each product rounded to fp32;
+ *   SwiGLU in double precision on H;
+ *   Linear2 step (1): A rounded to fp32; s^A = max(fp32(max|A| / 127), 1e-8);
+ *     q = clamp(round-half-even(fp32(A / s^A)), -127, 127);
+ *   Linear2: D = q . W2 in integers; Y = (D * s^W2) * s^A, each product rounded to fp32;
+ *   Token Combine as in the A16W16 layer.
+ * Returns 0, -1 for a bad id, -2 when memory runs out. */
+int oracle_forward_int8(const int8_t* x, const float* x_scale, const int32_t* ids, const float* g, const int8_t* w1,
+                        const float* w1_scale, const int8_t* w2, const float* w2_scale, int64_t T, int64_t K, int64_t E,
+                        int64_t H, int64_t I, double* y) {
+    int64_t* counts = (int64_t*)malloc(sizeof(int64_t) * (size_t)E);
+    int64_t* offsets = (int64_t*)malloc(sizeof(int64_t) * (size_t)(E + 1));
+    int64_t* row_src = (int64_t*)malloc(sizeof(int64_t) * (size_t)(T * K > 0 ? T * K : 1));
+    double* comb = (double*)calloc((size_t)(T * K * H > 0 ? T * K * H : 1), sizeof(double));
+    double* h = (double*)malloc(sizeof(double) * (size_t)(2 * I));
+    float* a32 = (float*)malloc(sizeof(float) * (size_t)I);
+    int32_t* q = (int32_t*)malloc(sizeof(int32_t) * (size_t)I);
+    int st = (counts && offsets && row_src && comb && h && a32 && q) ? 0 : -2;
+    if (st == 0) st = oracle_plan(ids, T, K, E, counts, offsets, row_src);
+    for (int64_t e = 0; st == 0 && e < E; ++e) {
+        const int8_t* w1e = w1 + e * 2 * I * H;
+        const int8_t* w2e = w2 + e * H * I;
+        const float* s1 = w1_scale + e * 2 * I;
+        const float* s2 = w2_scale + e * H;
+        for (int64_t p = offsets[e]; p < offsets[e + 1]; ++p) {
+            const int64_t src = row_src[p], tok = src / K;
+            const int8_t* xr = x + tok * H;
+            const float sx = x_scale[tok];
+            for (int64_t j = 0; j < 2 * I; ++j) { /* Linear1 */
+                int64_t c = 0;
+                for (int64_t k = 0; k < H; ++k) c += (int64_t)xr[k] * (int64_t)w1e[j * H + k];
+                float v = (float)c * s1[j];
+                v = v * sx;
+                h[j] = (double)v;
+            }
+            float amax = 0.0f;
+            for (int64_t j = 0; j < I; ++j) { /* SwiGLU, in fp32 for the quantiser */
+                a32[j] = (float)(h[j] / (1.0 + exp(-h[j])) * h[I + j]);
+                const float m = fabsf(a32[j]);
+                amax = m > amax ? m : amax;
+            }
+            float sa = amax / 127.0f;
+            sa = sa > 1e-8f ? sa : 1e-8f;
+            for (int64_t j = 0; j < I; ++j) {
+                float t = rintf(a32[j] / sa);
+                t = t < -127.0f ? -127.0f : (t > 127.0f ? 127.0f : t);
+                q[j] = (int32_t)t;
+            }
+            for (int64_t c = 0; c < H; ++c) { /* Linear2, gate, the bf16 combine row */
+                int64_t d = 0;
+                for (int64_t j = 0; j < I; ++j) d += (int64_t)q[j] * (int64_t)w2e[c * I + j];
+                float v = (float)d * s2[c];
+                v = v * sa;
+                comb[src * H + c] = gated(g[src], (double)v);
+            }
+        }
+    }
+    if (st == 0) combine_tokens(comb, T, K, H, y);
+    free(counts);
+    free(offsets);
+    free(row_src);
+    free(comb);
+    free(h);
+    free(a32);
+    free(q);
     return st;
 }

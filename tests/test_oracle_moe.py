@@ -337,6 +337,8 @@ def _c_oracle():
     lib.oracle_plan.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, i64p, i64p, i64p]
     lib.oracle_forward_a16w16.restype = ctypes.c_int
     lib.oracle_forward_a16w16.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int64] * 5 + [ctypes.c_void_p]
+    lib.oracle_forward_int8.restype = ctypes.c_int
+    lib.oracle_forward_int8.argtypes = [ctypes.c_void_p] * 8 + [ctypes.c_int64] * 5 + [ctypes.c_void_p]
     return lib
 
 
@@ -384,6 +386,30 @@ def test_c_forward_a16w16_equals_numpy_forward(case):
     ref = moe.forward("a16w16", h["x"], None, ids, g, h["w1"], None, h["w2"], None, num_experts=wl.E, inter=wl.I)
     # the same rounding points in both; the float64 sums differ only in their order, which moves
     # a bf16 or fp32 rounding decision only when a value sits within ~1e-16 of a tie
+    same = np.mean(y == ref)
+    assert same >= 0.999, same
+    assert np.abs(y - ref).max() <= 2.0 ** -7 * np.abs(ref).max()
+
+
+@pytest.mark.parametrize("case", ["tiny", "ragged_masked"])
+def test_c_forward_int8_equals_numpy_forward(case):
+    wl = (Workload("tiny_c8", "a8w8_int8", 64, 256, 128, 8, 2, 52, 0.05) if case == "tiny"
+          else Workload("ragged_c8", "a8w8_int8", 77, 128, 256, 5, 3, 53, 0.05))
+    h = to_numpy(make_inputs(wl, device="cpu"))
+    ids = np.ascontiguousarray(h["topk_ids"], dtype=np.int32)
+    if case == "ragged_masked":
+        ids[::4, 1] = -1
+    g = np.ascontiguousarray(h["topk_weights"], dtype=np.float32)
+    arr = {k: np.ascontiguousarray(h[k]) for k in ("x", "x_scale", "w1", "w1_scale", "w2", "w2_scale")}
+    assert arr["x"].dtype == np.int8 and arr["w1"].dtype == np.int8 and arr["x_scale"].dtype == np.float32
+    y = np.zeros((wl.T, wl.H), np.float64)
+    st = _c_oracle().oracle_forward_int8(arr["x"].ctypes.data, arr["x_scale"].ctypes.data, ids.ctypes.data,
+                                         g.ctypes.data, arr["w1"].ctypes.data, arr["w1_scale"].ctypes.data,
+                                         arr["w2"].ctypes.data, arr["w2_scale"].ctypes.data, wl.T, wl.K, wl.E, wl.H,
+                                         wl.I, y.ctypes.data)
+    assert st == 0
+    ref = moe.forward("a8w8_int8", h["x"], h["x_scale"], ids, g, h["w1"], h["w1_scale"], h["w2"], h["w2_scale"],
+                      num_experts=wl.E, inter=wl.I)
     same = np.mean(y == ref)
     assert same >= 0.999, same
     assert np.abs(y - ref).max() <= 2.0 ** -7 * np.abs(ref).max()
