@@ -17,7 +17,7 @@ Parity status of each function (what pins it, in ``tests/test_oracle_*.py``):
   forward         -- brute force per token (no plan) equals the pooled path bit for bit;
                      linearity in the gate weights; masked routes.
 
-``ref.c`` states the plan and the A16W16 and A8W8-INT layers a second time in plain C (loops in double
+``ref.c`` states the plan and the A16W16, A8W8-INT and FP8 x FP4 layers a second time in plain C (loops in double
 precision, the same readings), compiled by ``__graft_entry__.build_oracle()``; the CPU tests
 require the two to agree (the plan exactly, y bit for bit but for ties).
 """

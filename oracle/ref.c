@@ -1,8 +1,8 @@
-/* Plain C definition of the route plan and of the A16W16 and A8W8-INT expert feed-forward with
- * top-k combine.
+/* Plain C definition of the route plan and of the A16W16, A8W8-INT and FP8 x FP4 expert
+ * feed-forward with top-k combine.
  *
  * TEST INFRASTRUCTURE ONLY: a second, independent statement of what oracle/moe.py computes for
- * the plan and the A16W16 and A8W8-INT modes, written with plain loops in double precision (and
+ * the plan and the A16W16, A8W8-INT and FP8 x FP4 modes, written with plain loops in double precision (and
  * the fp32 roundings the readings fix), which the CPU tests compare with it. Nothing in the product path links or loads it; it shares no code with the
  * CUDA path.
  *
@@ -181,3 +181,124 @@ int oracle_forward_int8(const int8_t* x, const float* x_scale, const int32_t* id
     free(q);
     return st;
 }
+
+/* ---- FP8 (e4m3) activations x FP4 (e2m1) weights, block-scaled (DeepGEMM MegaMoE page §4: FP8
+ * activations with 1x128 power-of-two fp32 scales, e2m1 weights with a UE8M0 scale per 32 of K; the
+ * L1 output re-quantised to e4m3 with a UE8M0 exponent per 32, Ascend page "Q_MX") ---- */
+
+/* e4m3fn code -> value: sign, 4 exponent bits (bias 7), 3 mantissa bits; exponent 0 is subnormal;
+ * S.1111.111 is NaN. */
+static double e4m3_value(uint8_t c) {
+    const double s = (c & 0x80) ? -1.0 : 1.0;
+    const int e = (c >> 3) & 0xF, m = c & 7;
+    if (e == 0xF && m == 7) return NAN;
+    if (e == 0) return s * (m / 8.0) * ldexp(1.0, -6);
+    return s * (1.0 + m / 8.0) * ldexp(1.0, e - 7);
+}
+
+/* Nearest e4m3fn code of v, ties to the even code, magnitudes above 448 taken as 448 (a saturating
+ * conversion); the sign bit follows v, also when the magnitude rounds to zero. */
+static uint8_t e4m3_encode(double v) {
+    const uint8_t sign = signbit(v) ? 0x80 : 0;
+    double mag = fabs(v);
+    if (mag > 448.0) mag = 448.0;
+    if (mag < ldexp(1.0, -6)) {  /* subnormal range: spacing 2^-9; 8 * 2^-9 is the smallest normal */
+        const int m = (int)nearbyint(mag / ldexp(1.0, -9));
+        return (uint8_t)(sign | m);
+    }
+    int ex;
+    frexp(mag, &ex);  /* mag in [2^(ex-1), 2^ex) */
+    const int e = ex - 1;
+    int r = (int)nearbyint(mag / ldexp(1.0, e - 3));  /* 8 + mantissa, half to even */
+    int be = e + 7;
+    if (r == 16) r = 8, ++be;
+    return (uint8_t)(sign | (be << 3) | (r - 8));
+}
+
+/* e2m1 code (4 bits) -> value: sign, 2 exponent bits (bias 1), 1 mantissa bit; exponent 0 is
+ * subnormal. */
+static double e2m1_value(int c) {
+    const double s = (c & 8) ? -1.0 : 1.0;
+    const int e = (c >> 1) & 3, m = c & 1;
+    if (e == 0) return s * 0.5 * m;
+    return s * (1.0 + 0.5 * m) * ldexp(1.0, e - 1);
+}
+
+/* UE8M0 scale byte -> 2^(b - 127); 255 is NaN. */
+static double ue8m0_value(uint8_t b) { return b == 255 ? NAN : ldexp(1.0, (int)b - 127); }
+
+/* Element k of a packed e2m1 row (element 2j in the low nibble of byte j) times its UE8M0 scale. */
+static double fp4_weight(const uint8_t* row, const uint8_t* scales, int64_t k) {
+    const int c = (k & 1) ? row[k >> 1] >> 4 : row[k >> 1] & 0xF;
+    return e2m1_value(c) * ue8m0_value(scales[k / 32]);
+}
+
+/* y [T, H] of the FP8 x FP4 layer. x e4m3 [T, H] with fp32 scales [T, H/128]; w1 packed e2m1
+ * [E, 2I, H/2] with UE8M0 [E, 2I, H/32]; w2 packed e2m1 [E, H, I/2] with UE8M0 [E, H, I/32]; g [T*K].
+ *   Linear1: H = X_e . W1[e] on the decoded values, in double precision;
+ *   SwiGLU in double precision;
+ *   re-quantisation of A: A rounded to fp32; per 32 consecutive outputs the exponent e, the
+ *     smallest integer with amax <= 448 * 2^e (clamped to [-127, 127], -127 for amax = 0), and
+ *     codes e4m3(A / 2^e); the L2 operand is their value times 2^e;
+ *   Linear2: Y = A~ . W2[e] in double precision; Token Combine as in the A16W16 layer.
+ * Returns 0, -1 for a bad id, -2 when memory runs out. */
+int oracle_forward_fp8_fp4(const uint8_t* x, const float* x_scale, const int32_t* ids, const float* g,
+                           const uint8_t* w1, const uint8_t* w1_scale, const uint8_t* w2, const uint8_t* w2_scale,
+                           int64_t T, int64_t K, int64_t E, int64_t H, int64_t I, double* y) {
+    int64_t* counts = (int64_t*)malloc(sizeof(int64_t) * (size_t)E);
+    int64_t* offsets = (int64_t*)malloc(sizeof(int64_t) * (size_t)(E + 1));
+    int64_t* row_src = (int64_t*)malloc(sizeof(int64_t) * (size_t)(T * K > 0 ? T * K : 1));
+    double* comb = (double*)calloc((size_t)(T * K * H > 0 ? T * K * H : 1), sizeof(double));
+    double* xv = (double*)malloc(sizeof(double) * (size_t)H);
+    double* h = (double*)malloc(sizeof(double) * (size_t)(2 * I));
+    double* a = (double*)malloc(sizeof(double) * (size_t)I);
+    int st = (counts && offsets && row_src && comb && xv && h && a) ? 0 : -2;
+    if (st == 0) st = oracle_plan(ids, T, K, E, counts, offsets, row_src);
+    for (int64_t e = 0; st == 0 && e < E; ++e) {
+        for (int64_t p = offsets[e]; p < offsets[e + 1]; ++p) {
+            const int64_t src = row_src[p], tok = src / K;
+            for (int64_t k = 0; k < H; ++k)
+                xv[k] = e4m3_value(x[tok * H + k]) * (double)x_scale[tok * (H / 128) + k / 128];
+            for (int64_t j = 0; j < 2 * I; ++j) { /* Linear1 */
+                const uint8_t* wr = w1 + (e * 2 * I + j) * (H / 2);
+                const uint8_t* sr = w1_scale + (e * 2 * I + j) * (H / 32);
+                double s = 0.0;
+                for (int64_t k = 0; k < H; ++k) s += xv[k] * fp4_weight(wr, sr, k);
+                h[j] = s;
+            }
+            for (int64_t j = 0; j < I; ++j) /* SwiGLU, rounded to fp32 for the quantiser */
+                a[j] = (double)(float)(h[j] / (1.0 + exp(-h[j])) * h[I + j]);
+            for (int64_t b = 0; b < I; b += 32) { /* MX e4m3 re-quantisation, blocks of 32 */
+                double amax = 0.0;
+                for (int64_t j = b; j < b + 32; ++j) amax = fabs(a[j]) > amax ? fabs(a[j]) : amax;
+                int ex = -127;
+                if (amax > 0.0) {
+                    int fe;
+                    const double fm = frexp(amax / 448.0, &fe);
+                    ex = fm == 0.5 ? fe - 1 : fe;
+                    ex = ex < -127 ? -127 : (ex > 127 ? 127 : ex);
+                }
+                for (int64_t j = b; j < b + 32; ++j) a[j] = e4m3_value(e4m3_encode(a[j] / ldexp(1.0, ex))) * ldexp(1.0, ex);
+            }
+            for (int64_t c = 0; c < H; ++c) { /* Linear2, gate, the bf16 combine row */
+                const uint8_t* wr = w2 + (e * H + c) * (I / 2);
+                const uint8_t* sr = w2_scale + (e * H + c) * (I / 32);
+                double s = 0.0;
+                for (int64_t j = 0; j < I; ++j) s += a[j] * fp4_weight(wr, sr, j);
+                comb[src * H + c] = gated(g[src], s);
+            }
+        }
+    }
+    if (st == 0) combine_tokens(comb, T, K, H, y);
+    free(counts);
+    free(offsets);
+    free(row_src);
+    free(comb);
+    free(xv);
+    free(h);
+    free(a);
+    return st;
+}
+
+/* The e4m3 encoder on its own, for the codec test. */
+uint8_t oracle_e4m3_encode(double v) { return e4m3_encode(v); }

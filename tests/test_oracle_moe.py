@@ -339,6 +339,8 @@ def _c_oracle():
     lib.oracle_forward_a16w16.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int64] * 5 + [ctypes.c_void_p]
     lib.oracle_forward_int8.restype = ctypes.c_int
     lib.oracle_forward_int8.argtypes = [ctypes.c_void_p] * 8 + [ctypes.c_int64] * 5 + [ctypes.c_void_p]
+    lib.oracle_forward_fp8_fp4.restype = ctypes.c_int
+    lib.oracle_forward_fp8_fp4.argtypes = [ctypes.c_void_p] * 8 + [ctypes.c_int64] * 5 + [ctypes.c_void_p]
     return lib
 
 
@@ -413,3 +415,48 @@ def test_c_forward_int8_equals_numpy_forward(case):
     same = np.mean(y == ref)
     assert same >= 0.999, same
     assert np.abs(y - ref).max() <= 2.0 ** -7 * np.abs(ref).max()
+
+
+@pytest.mark.parametrize("case", ["tiny", "ragged_masked", "skewed"])
+def test_c_forward_fp8_fp4_equals_numpy_forward(case):
+    wl = {"tiny": Workload("tiny_c4", "a8w4_fp8_fp4", 64, 256, 128, 8, 2, 54, 0.02),
+          "ragged_masked": Workload("ragged_c4", "a8w4_fp8_fp4", 77, 256, 256, 5, 3, 55, 0.05),
+          "skewed": Workload("skew_c4", "a8w4_fp8_fp4", 57, 256, 128, 16, 4, 56, 0.05, zipf_s=1.2, zipf_empty=4)}[case]
+    h = to_numpy(make_inputs(wl, device="cpu"))
+    ids = np.ascontiguousarray(h["topk_ids"], dtype=np.int32)
+    if case == "ragged_masked":
+        ids[::4, 1] = -1
+    g = np.ascontiguousarray(h["topk_weights"], dtype=np.float32)
+    arr = {k: np.ascontiguousarray(h[k]) for k in ("x", "x_scale", "w1", "w1_scale", "w2", "w2_scale")}
+    assert arr["x"].dtype == np.uint8 and arr["x_scale"].shape == (wl.T, wl.H // 128)
+    assert arr["w1"].shape == (wl.E, 2 * wl.I, wl.H // 2) and arr["w1_scale"].shape == (wl.E, 2 * wl.I, wl.H // 32)
+    assert arr["w2"].shape == (wl.E, wl.H, wl.I // 2) and arr["w2_scale"].shape == (wl.E, wl.H, wl.I // 32)
+    x_scale = np.ascontiguousarray(arr["x_scale"], dtype=np.float32)
+    y = np.zeros((wl.T, wl.H), np.float64)
+    st = _c_oracle().oracle_forward_fp8_fp4(arr["x"].ctypes.data, x_scale.ctypes.data, ids.ctypes.data,
+                                            g.ctypes.data, arr["w1"].ctypes.data, arr["w1_scale"].ctypes.data,
+                                            arr["w2"].ctypes.data, arr["w2_scale"].ctypes.data, wl.T, wl.K, wl.E,
+                                            wl.H, wl.I, y.ctypes.data)
+    assert st == 0
+    ref = moe.forward("a8w4_fp8_fp4", h["x"], h["x_scale"], ids, g, h["w1"], h["w1_scale"], h["w2"],
+                      h["w2_scale"], num_experts=wl.E, inter=wl.I)
+    same = np.mean(y == ref)
+    assert same >= 0.999, same
+    assert np.abs(y - ref).max() <= 2.0 ** -7 * np.abs(ref).max()
+
+
+def test_c_e4m3_codec_equals_numpy_codec():
+    """The C encoder (nearest value from the format's fields) against the numpy one (table search) on
+    every code's value, every midpoint between neighbours, both signs and values beyond 448."""
+    import ctypes
+    lib = _c_oracle()
+    vals = codecs.E4M3_VALUES[:0x7F]
+    mids = (vals[:-1] + vals[1:]) / 2
+    probe = np.concatenate([vals, mids, mids * (1 + 1e-12), mids * (1 - 1e-12), [448.0, 460.0, 464.0, 500.0, 1e9]])
+    probe = np.concatenate([probe, -probe]).astype(np.float64)
+    want = codecs.e4m3_encode_rne_satfinite(probe)
+    fn = lib.oracle_e4m3_encode
+    fn.restype = ctypes.c_uint8
+    fn.argtypes = [ctypes.c_double]
+    got = np.array([fn(float(v)) for v in probe], dtype=np.uint8)
+    assert np.array_equal(got, want)
