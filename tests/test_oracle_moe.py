@@ -122,6 +122,119 @@ def test_closed_form_int8():
     assert y[0, 0] == pytest.approx(a, rel=2e-7) and y[0, 1] == pytest.approx(-2 * a, rel=2e-7)
 
 
+def _golden_fp8_inputs(g, mode):
+    """Dense operands of a sparse FP8 golden: codes and scale bytes not listed are 0 and 127."""
+    T, H, I, E = g["T"], g["H"], g["I"], g["E"]
+    x = np.zeros((T, H), np.uint8)
+    for t, h, c in g["x_codes"]:
+        x[t, h] = int(c, 16)
+    if mode == "a8w4_fp8_fp4":
+        x_scale = np.array(g["x_scale"], np.float32)
+        w1 = np.zeros((E, 2 * I, H // 2), np.uint8)
+        w2 = np.zeros((E, H, I // 2), np.uint8)
+        for arr, key in ((w1, "w1_codes"), (w2, "w2_codes")):  # two e2m1 codes per byte, element 2j low
+            for e, n, k, c in g[key]:
+                arr[e, n, k // 2] |= np.uint8(int(c, 16) << (4 * (k & 1)))
+    else:
+        x_scale = np.array(g["x_scale_bytes"], np.uint8)
+        w1 = np.zeros((E, 2 * I, H), np.uint8)
+        w2 = np.zeros((E, H, I), np.uint8)
+        for arr, key in ((w1, "w1_codes"), (w2, "w2_codes")):
+            for e, n, k, c in g[key]:
+                arr[e, n, k] = int(c, 16)
+    w1_scale = np.full((E, 2 * I, H // 32), 127, np.uint8)
+    w2_scale = np.full((E, H, I // 32), 127, np.uint8)
+    for arr, key in ((w1_scale, "w1_scale_bytes"), (w2_scale, "w2_scale_bytes")):
+        for e, n, b, v in g[key]:
+            arr[e, n, b] = v
+    return x, x_scale, w1, w1_scale, w2, w2_scale
+
+
+def _dense(pairs, n):
+    v = np.zeros(n)
+    for i, val in pairs:
+        v[i] = float(val) if not isinstance(val, str) else int(val, 16)
+    return v
+
+
+FP8_GOLDENS = [("ffn_closed_form_fp8_e4m3.json", "a8w8_fp8"), ("ffn_closed_form_fp8_e5m2.json", "a8w8_fp8_e5m2"),
+               ("ffn_closed_form_fp8_fp4.json", "a8w4_fp8_fp4")]
+
+
+def _check_fp8_golden(name, mode):
+    """The oracle on a hand-derived FP8 example: H, the re-quantised A (codes and UE8M0 exponent
+    bytes), L2's rows and y, each against the derivation written in the golden file."""
+    g = _load(name)
+    x, xs, w1, s1, w2, s2 = _golden_fp8_inputs(g, mode)
+    y, rec = moe.forward(mode, x, xs, np.array(g["topk_ids"]), np.array(g["topk_weights"], np.float32), w1, s1, w2, s2,
+                         num_experts=g["E"], inter=g["I"], return_intermediates=True)
+    r = rec["experts"][0]
+    assert r["h"][0].tolist() == _dense(g["h_nonzero"], 2 * g["I"]).tolist(), "H"
+    assert r["a"][0].tolist() == _dense(g["a_codes_nonzero"], g["I"]).astype(np.uint8).tolist(), "A codes"
+    assert r["a_scale"][0].tolist() == g["a_scale_bytes"], "A exponents"
+    assert r["y"][0].tolist() == _dense(g["y_row_nonzero"], g["H"]).tolist(), "L2 rows"
+    assert y[0].tolist() == _dense(g["y_nonzero"], g["H"]).tolist(), "y"
+
+
+@pytest.mark.parametrize("name,mode", FP8_GOLDENS, ids=[m for _, m in FP8_GOLDENS])
+def test_closed_form_fp8(name, mode):
+    _check_fp8_golden(name, mode)
+
+
+# Plausible mistakes planted in the oracle (on the CPU): each must fail every FP8 golden, so the
+# goldens are what pins decode_weight, the block scales, the nibble order and the re-quantisation.
+def _decode_weight_untransposed(mode, w, w_scale, e):
+    if mode in moe.FP8_FORMAT:
+        return moe.fp8_decode(moe.FP8_FORMAT[mode], w[e]) * np.repeat(codecs.ue8m0_decode(w_scale[e]), 32, axis=-1)
+    if mode == "a8w4_fp8_fp4":
+        return codecs.e2m1_unpack_decode(w[e]) * np.repeat(codecs.ue8m0_decode(w_scale[e]), 32, axis=-1)
+    raise ValueError(mode)
+
+
+def _decode_weight_per_channel_scale(mode, w, w_scale, e):
+    first = w_scale[e][:, :1]  # the first K block's scale for the whole row
+    if mode in moe.FP8_FORMAT:
+        v = moe.fp8_decode(moe.FP8_FORMAT[mode], w[e]) * codecs.ue8m0_decode(first)
+    else:
+        v = codecs.e2m1_unpack_decode(w[e]) * codecs.ue8m0_decode(first)
+    return v.T
+
+
+def _decode_weight_nibbles_swapped(mode, w, w_scale, e):
+    if mode != "a8w4_fp8_fp4":
+        return ORIG_DECODE_WEIGHT(mode, w, w_scale, e)
+    b = np.asarray(w[e], np.uint8)
+    swapped = ((b >> 4) | (b << 4)).astype(np.uint8)
+    return (codecs.e2m1_unpack_decode(swapped) * np.repeat(codecs.ue8m0_decode(w_scale[e]), 32, axis=-1)).T
+
+
+def _l2_operand_unrounded(mode, a):
+    _, rec = ORIG_L2_OPERAND(mode, a)
+    return a, rec
+
+
+ORIG_DECODE_WEIGHT, ORIG_L2_OPERAND = moe.decode_weight, moe.l2_operand
+MUTATIONS = {"weight_not_transposed": ("decode_weight", _decode_weight_untransposed),
+             "scale_per_output_channel": ("decode_weight", _decode_weight_per_channel_scale),
+             "a_not_requantised": ("l2_operand", _l2_operand_unrounded),
+             "gate_up_swapped": ("swiglu", lambda h, inter, clamp=None: moe.silu(h[:, inter:]) * h[:, :inter])}
+
+
+@pytest.mark.parametrize("mutation", list(MUTATIONS))
+@pytest.mark.parametrize("name,mode", FP8_GOLDENS, ids=[m for _, m in FP8_GOLDENS])
+def test_fp8_goldens_catch_planted_mistakes(monkeypatch, mutation, name, mode):
+    attr, fn = MUTATIONS[mutation]
+    monkeypatch.setattr(moe, attr, fn)
+    with pytest.raises((AssertionError, ValueError)):
+        _check_fp8_golden(name, mode)
+
+
+def test_fp4_golden_catches_swapped_nibbles(monkeypatch):
+    monkeypatch.setattr(moe, "decode_weight", _decode_weight_nibbles_swapped)
+    with pytest.raises(AssertionError):
+        _check_fp8_golden("ffn_closed_form_fp8_fp4.json", "a8w4_fp8_fp4")
+
+
 # ---------------------------------------------------------------------------------------
 # Whole path: brute force, reductions, linearity
 # ---------------------------------------------------------------------------------------
@@ -324,8 +437,8 @@ def test_shared_brute_force_per_token_equals_pooled_path(mode):
 
 
 # ---------------------------------------------------------------------------------------
-# The plain C statement of the plan and of the A16W16 layer (oracle/ref.c) against this module:
-# two independent implementations of the same readings
+# The plain C statement of the plan, the shared slots and every mode's layer (oracle/ref.c) against
+# this module: two independent implementations of the same readings
 # ---------------------------------------------------------------------------------------
 
 def _c_oracle():
@@ -333,14 +446,22 @@ def _c_oracle():
     import __graft_entry__
     lib = ctypes.CDLL(__graft_entry__.build_oracle())
     i64p = ctypes.POINTER(ctypes.c_int64)
-    lib.oracle_plan.restype = ctypes.c_int
-    lib.oracle_plan.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, i64p, i64p, i64p]
-    lib.oracle_forward_a16w16.restype = ctypes.c_int
-    lib.oracle_forward_a16w16.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int64] * 5 + [ctypes.c_void_p]
-    lib.oracle_forward_int8.restype = ctypes.c_int
-    lib.oracle_forward_int8.argtypes = [ctypes.c_void_p] * 8 + [ctypes.c_int64] * 5 + [ctypes.c_void_p]
-    lib.oracle_forward_fp8_fp4.restype = ctypes.c_int
-    lib.oracle_forward_fp8_fp4.argtypes = [ctypes.c_void_p] * 8 + [ctypes.c_int64] * 5 + [ctypes.c_void_p]
+    vp, i64, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    lib.oracle_plan.restype = ci
+    lib.oracle_plan.argtypes = [vp, i64, i64, i64, i64p, i64p, i64p]
+    lib.oracle_forward_a16w16.restype = ci
+    lib.oracle_forward_a16w16.argtypes = [vp] * 5 + [i64] * 5 + [vp]
+    lib.oracle_forward_int.restype = ci
+    lib.oracle_forward_int.argtypes = [ci] + [vp] * 8 + [i64] * 5 + [vp] * 5
+    lib.oracle_forward_fp8.restype = ci
+    lib.oracle_forward_fp8.argtypes = [ci] + [vp] * 8 + [i64] * 5 + [vp] * 3
+    lib.oracle_forward_fp8_fp4.restype = ci
+    lib.oracle_forward_fp8_fp4.argtypes = [vp] * 8 + [i64] * 5 + [vp] * 3
+    lib.oracle_shared_slots.restype = None
+    lib.oracle_shared_slots.argtypes = [vp, vp] + [i64] * 4 + [vp, vp]
+    for name in ("oracle_e4m3_encode", "oracle_e5m2_encode"):
+        getattr(lib, name).restype = ctypes.c_uint8
+        getattr(lib, name).argtypes = [ctypes.c_double]
     return lib
 
 
@@ -369,94 +490,131 @@ def test_c_plan_equals_numpy_plan(seed):
     assert _c_plan(lib, ids, E)[0] == -1
 
 
-@pytest.mark.parametrize("case", ["tiny", "ragged_masked"])
-def test_c_forward_a16w16_equals_numpy_forward(case):
-    wl = (Workload("tiny_c", "a16w16", 64, 256, 128, 8, 2, 50, 0.05) if case == "tiny"
-          else Workload("ragged_c", "a16w16", 77, 128, 256, 5, 3, 51, 0.05))
+def _c_forward(lib, mode, h, ids, g, E, I):
+    """y of the C statement of `mode`, and its per-pool-row records: C, q, s^A, D (integer modes) or the
+    A codes and exponents (FP8 modes)."""
+    c = lambda a: np.ascontiguousarray(a)
+    ids, g = c(np.asarray(ids, np.int32)), c(np.asarray(g, np.float32))
+    T, K = ids.shape
+    H = h["x"].shape[1]
+    R = int((ids >= 0).sum())
+    y = np.zeros((T, H), np.float64)
+    rec = {}
+    if mode == "a16w16":
+        args = [c(codecs.bf16_decode(h[k])) for k in ("x", "w1", "w2")]
+        st = lib.oracle_forward_a16w16(args[0].ctypes.data, ids.ctypes.data, g.ctypes.data, args[1].ctypes.data,
+                                       args[2].ctypes.data, T, K, E, H, I, y.ctypes.data)
+        return st, y, rec
+    arr = {k: c(h[k]) for k in ("x", "x_scale", "w1", "w1_scale", "w2", "w2_scale")}
+    ptrs = [arr[k].ctypes.data for k in ("x", "x_scale")] + [ids.ctypes.data, g.ctypes.data] + \
+           [arr[k].ctypes.data for k in ("w1", "w1_scale", "w2", "w2_scale")]
+    if mode in moe.INT_MODES:
+        rec = {"c": np.zeros((R, 2 * I), np.int64), "a": np.zeros((R, I), np.int32), "a_scale": np.zeros(R, np.float32),
+               "d": np.zeros((R, H), np.int64)}
+        st = lib.oracle_forward_int(8 if mode == "a8w8_int8" else 4, *ptrs, T, K, E, H, I, y.ctypes.data,
+                                    *[rec[k].ctypes.data for k in ("c", "a", "a_scale", "d")])
+    else:
+        rec = {"a": np.zeros((R, I), np.uint8), "a_scale": np.zeros((R, I // 32), np.uint8)}
+        if mode == "a8w4_fp8_fp4":
+            st = lib.oracle_forward_fp8_fp4(*ptrs, T, K, E, H, I, y.ctypes.data, rec["a"].ctypes.data,
+                                            rec["a_scale"].ctypes.data)
+        else:
+            st = lib.oracle_forward_fp8(0 if moe.FP8_FORMAT[mode] == "e4m3" else 1, *ptrs, T, K, E, H, I, y.ctypes.data,
+                                        rec["a"].ctypes.data, rec["a_scale"].ctypes.data)
+    return st, y, rec
+
+
+C_CASES = {
+    "a16w16": [Workload("tiny_c", "a16w16", 64, 256, 128, 8, 2, 50, 0.05),
+               Workload("ragged_c", "a16w16", 77, 128, 256, 5, 3, 51, 0.05)],
+    "a8w8_int8": [Workload("tiny_c8", "a8w8_int8", 64, 256, 128, 8, 2, 52, 0.05),
+                  Workload("ragged_c8", "a8w8_int8", 77, 128, 256, 5, 3, 53, 0.05)],
+    "a8w4_fp8_fp4": [Workload("tiny_c4", "a8w4_fp8_fp4", 64, 256, 128, 8, 2, 54, 0.02),
+                     Workload("ragged_c4", "a8w4_fp8_fp4", 77, 256, 256, 5, 3, 55, 0.05),
+                     Workload("skew_c4", "a8w4_fp8_fp4", 57, 256, 128, 16, 4, 56, 0.05, zipf_s=1.2, zipf_empty=4)],
+    "a8w8_fp8": [Workload("tiny_cf8", "a8w8_fp8", 64, 256, 128, 8, 2, 57, 0.05),
+                 Workload("ragged_cf8", "a8w8_fp8", 77, 128, 192, 5, 3, 58, 0.05)],
+    "a8w8_fp8_e5m2": [Workload("tiny_ce5", "a8w8_fp8_e5m2", 64, 256, 128, 8, 2, 59, 0.05),
+                      Workload("ragged_ce5", "a8w8_fp8_e5m2", 77, 128, 192, 5, 3, 60, 0.05)],
+    "a8w4_int": [Workload("tiny_cw4", "a8w4_int", 64, 256, 128, 8, 2, 61, 0.05),
+                 Workload("ragged_cw4", "a8w4_int", 77, 128, 256, 5, 3, 62, 0.05)],
+}
+C_ALL = [(m, w) for m, ws in C_CASES.items() for w in ws]
+
+
+def _numpy_records(rec, keys):
+    """The numpy oracle's per-expert records stacked in pool order (expert by expert, rows ascending)."""
+    ex = [rec["experts"][e] for e in sorted(rec["experts"])]
+    return {k: np.concatenate([r[k] for r in ex]) for k in keys}
+
+
+@pytest.mark.parametrize("mode,wl", C_ALL, ids=[w.name for _, w in C_ALL])
+def test_c_forward_equals_numpy_forward(mode, wl):
     h = to_numpy(make_inputs(wl, device="cpu"))
     ids = np.ascontiguousarray(h["topk_ids"], dtype=np.int32)
-    if case == "ragged_masked":
-        ids[::4, 1] = -1
+    if wl.name.startswith("ragged"):
+        ids[::4, 1] = -1  # masked routes
     g = np.ascontiguousarray(h["topk_weights"], dtype=np.float32)
-    x = np.ascontiguousarray(codecs.bf16_decode(h["x"]))
-    w1 = np.ascontiguousarray(codecs.bf16_decode(h["w1"]))
-    w2 = np.ascontiguousarray(codecs.bf16_decode(h["w2"]))
-    y = np.zeros((wl.T, wl.H), np.float64)
-    st = _c_oracle().oracle_forward_a16w16(x.ctypes.data, ids.ctypes.data, g.ctypes.data, w1.ctypes.data,
-                                           w2.ctypes.data, wl.T, wl.K, wl.E, wl.H, wl.I, y.ctypes.data)
+    st, y, crec = _c_forward(_c_oracle(), mode, h, ids, g, wl.E, wl.I)
     assert st == 0
-    ref = moe.forward("a16w16", h["x"], None, ids, g, h["w1"], None, h["w2"], None, num_experts=wl.E, inter=wl.I)
-    # the same rounding points in both; the float64 sums differ only in their order, which moves
-    # a bf16 or fp32 rounding decision only when a value sits within ~1e-16 of a tie
+    ref, rec = moe.forward(mode, h["x"], h["x_scale"], ids, g, h["w1"], h["w1_scale"], h["w2"], h["w2_scale"],
+                           num_experts=wl.E, inter=wl.I, return_intermediates=True)
+    if mode in moe.INT_MODES:
+        # integer accumulators and the re-quantised A, decided in fp32 on both sides, are equal
+        nrec = _numpy_records(rec, ("c", "a", "a_scale", "d"))
+        for k in ("c", "a", "a_scale", "d"):
+            assert np.array_equal(crec[k], nrec[k].astype(crec[k].dtype)), k
+        assert np.array_equal(y, ref)  # every later step is the same fp32 arithmetic
+        return
+    if mode != "a16w16":
+        nrec = _numpy_records(rec, ("a", "a_scale"))
+        # the float64 L1 sums differ only in order; a code moves only for a value within ~1e-16 of a tie
+        assert np.mean(crec["a"] == nrec["a"]) >= 0.999 and np.mean(crec["a_scale"] == nrec["a_scale"]) >= 0.999
+    # the same rounding points in both; the float64 sums differ only in their order, which moves a
+    # bf16 or fp32 rounding decision only when a value sits within ~1e-16 of a tie
     same = np.mean(y == ref)
     assert same >= 0.999, same
     assert np.abs(y - ref).max() <= 2.0 ** -7 * np.abs(ref).max()
 
 
-@pytest.mark.parametrize("case", ["tiny", "ragged_masked"])
-def test_c_forward_int8_equals_numpy_forward(case):
-    wl = (Workload("tiny_c8", "a8w8_int8", 64, 256, 128, 8, 2, 52, 0.05) if case == "tiny"
-          else Workload("ragged_c8", "a8w8_int8", 77, 128, 256, 5, 3, 53, 0.05))
-    h = to_numpy(make_inputs(wl, device="cpu"))
+@pytest.mark.parametrize("mode", list(C_CASES))
+def test_c_shared_slots_equal_numpy_shared_slots(mode):
+    """Two shared experts after the routed ones, with masked routes: the C statement of the shared slots
+    and forward against the numpy oracle's."""
+    import ctypes  # noqa: F401
+    wl = C_CASES[mode][0]
+    S = 2
+    h = to_numpy(make_inputs(wl, device="cpu", shared=S))
     ids = np.ascontiguousarray(h["topk_ids"], dtype=np.int32)
-    if case == "ragged_masked":
-        ids[::4, 1] = -1
+    ids[::3, 0] = -1
     g = np.ascontiguousarray(h["topk_weights"], dtype=np.float32)
-    arr = {k: np.ascontiguousarray(h[k]) for k in ("x", "x_scale", "w1", "w1_scale", "w2", "w2_scale")}
-    assert arr["x"].dtype == np.int8 and arr["w1"].dtype == np.int8 and arr["x_scale"].dtype == np.float32
-    y = np.zeros((wl.T, wl.H), np.float64)
-    st = _c_oracle().oracle_forward_int8(arr["x"].ctypes.data, arr["x_scale"].ctypes.data, ids.ctypes.data,
-                                         g.ctypes.data, arr["w1"].ctypes.data, arr["w1_scale"].ctypes.data,
-                                         arr["w2"].ctypes.data, arr["w2_scale"].ctypes.data, wl.T, wl.K, wl.E, wl.H,
-                                         wl.I, y.ctypes.data)
-    assert st == 0
-    ref = moe.forward("a8w8_int8", h["x"], h["x_scale"], ids, g, h["w1"], h["w1_scale"], h["w2"], h["w2_scale"],
-                      num_experts=wl.E, inter=wl.I)
-    same = np.mean(y == ref)
-    assert same >= 0.999, same
-    assert np.abs(y - ref).max() <= 2.0 ** -7 * np.abs(ref).max()
-
-
-@pytest.mark.parametrize("case", ["tiny", "ragged_masked", "skewed"])
-def test_c_forward_fp8_fp4_equals_numpy_forward(case):
-    wl = {"tiny": Workload("tiny_c4", "a8w4_fp8_fp4", 64, 256, 128, 8, 2, 54, 0.02),
-          "ragged_masked": Workload("ragged_c4", "a8w4_fp8_fp4", 77, 256, 256, 5, 3, 55, 0.05),
-          "skewed": Workload("skew_c4", "a8w4_fp8_fp4", 57, 256, 128, 16, 4, 56, 0.05, zipf_s=1.2, zipf_empty=4)}[case]
-    h = to_numpy(make_inputs(wl, device="cpu"))
-    ids = np.ascontiguousarray(h["topk_ids"], dtype=np.int32)
-    if case == "ragged_masked":
-        ids[::4, 1] = -1
-    g = np.ascontiguousarray(h["topk_weights"], dtype=np.float32)
-    arr = {k: np.ascontiguousarray(h[k]) for k in ("x", "x_scale", "w1", "w1_scale", "w2", "w2_scale")}
-    assert arr["x"].dtype == np.uint8 and arr["x_scale"].shape == (wl.T, wl.H // 128)
-    assert arr["w1"].shape == (wl.E, 2 * wl.I, wl.H // 2) and arr["w1_scale"].shape == (wl.E, 2 * wl.I, wl.H // 32)
-    assert arr["w2"].shape == (wl.E, wl.H, wl.I // 2) and arr["w2_scale"].shape == (wl.E, wl.H, wl.I // 32)
-    x_scale = np.ascontiguousarray(arr["x_scale"], dtype=np.float32)
-    y = np.zeros((wl.T, wl.H), np.float64)
-    st = _c_oracle().oracle_forward_fp8_fp4(arr["x"].ctypes.data, x_scale.ctypes.data, ids.ctypes.data,
-                                            g.ctypes.data, arr["w1"].ctypes.data, arr["w1_scale"].ctypes.data,
-                                            arr["w2"].ctypes.data, arr["w2_scale"].ctypes.data, wl.T, wl.K, wl.E,
-                                            wl.H, wl.I, y.ctypes.data)
-    assert st == 0
-    ref = moe.forward("a8w4_fp8_fp4", h["x"], h["x_scale"], ids, g, h["w1"], h["w1_scale"], h["w2"],
-                      h["w2_scale"], num_experts=wl.E, inter=wl.I)
-    same = np.mean(y == ref)
-    assert same >= 0.999, same
-    assert np.abs(y - ref).max() <= 2.0 ** -7 * np.abs(ref).max()
-
-
-def test_c_e4m3_codec_equals_numpy_codec():
-    """The C encoder (nearest value from the format's fields) against the numpy one (table search) on
-    every code's value, every midpoint between neighbours, both signs and values beyond 448."""
-    import ctypes
     lib = _c_oracle()
-    vals = codecs.E4M3_VALUES[:0x7F]
+    ids2 = np.zeros((wl.T, wl.K + S), np.int32)
+    g2 = np.zeros((wl.T, wl.K + S), np.float32)
+    lib.oracle_shared_slots(ids.ctypes.data, g.ctypes.data, wl.T, wl.K, wl.E, S, ids2.ctypes.data, g2.ctypes.data)
+    nid, ng = moe.with_shared_slots(ids, g, wl.E, S)
+    assert np.array_equal(ids2, nid) and np.array_equal(g2, ng)
+    st, y, _ = _c_forward(lib, mode, h, ids2, g2, wl.E + S, wl.I)
+    assert st == 0
+    ref = moe.forward(mode, h["x"], h["x_scale"], ids, g, h["w1"], h["w1_scale"], h["w2"], h["w2_scale"],
+                      num_experts=wl.E, inter=wl.I, num_shared=S)
+    assert np.mean(y == ref) >= 0.999
+    assert np.abs(y - ref).max() <= 2.0 ** -7 * np.abs(ref).max()
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_c_fp8_codec_equals_numpy_codec(fmt):
+    """The C encoders (nearest value from the format's fields) against the numpy ones on every code's value,
+    every midpoint between neighbours, both signs and values beyond the largest finite one."""
+    lib = _c_oracle()
+    if fmt == "e4m3":
+        vals, top, fn, want_fn = codecs.E4M3_VALUES[:0x7F], 448.0, lib.oracle_e4m3_encode, codecs.e4m3_encode_rne_satfinite
+    else:
+        vals = codecs.e5m2_decode(np.arange(0x7C, dtype=np.uint8))  # every finite non-negative code
+        top, fn, want_fn = 57344.0, lib.oracle_e5m2_encode, codecs.e5m2_encode_rne_satfinite
     mids = (vals[:-1] + vals[1:]) / 2
-    probe = np.concatenate([vals, mids, mids * (1 + 1e-12), mids * (1 - 1e-12), [448.0, 460.0, 464.0, 500.0, 1e9]])
+    probe = np.concatenate([vals, mids, mids * (1 + 1e-12), mids * (1 - 1e-12), [top, top * 1.03, top * 1.2, 1e9]])
     probe = np.concatenate([probe, -probe]).astype(np.float64)
-    want = codecs.e4m3_encode_rne_satfinite(probe)
-    fn = lib.oracle_e4m3_encode
-    fn.restype = ctypes.c_uint8
-    fn.argtypes = [ctypes.c_double]
+    want = want_fn(probe)
     got = np.array([fn(float(v)) for v in probe], dtype=np.uint8)
     assert np.array_equal(got, want)
