@@ -54,7 +54,11 @@ typedef enum {
     MOE_ERR_CUDA = 3,          /* a CUDA runtime call or kernel launch failed           */
     MOE_ERR_BAD_ROUTE = 4,     /* device: an expert id outside [-1, E); route skipped   */
     MOE_ERR_TIMEOUT = 5,       /* device: a bounded wait ran out; results are invalid   */
-    MOE_ERR_WORKSPACE = 6      /* workspace missing, misaligned or too small            */
+    MOE_ERR_WORKSPACE = 6,     /* workspace missing, misaligned or too small            */
+    MOE_ERR_BAD_SCALE = 7,     /* device: an FP8 x FP4 x scale that is not a power of two
+                                  2^e, -127 <= e <= 127; the outputs are not defined     */
+    MOE_ERR_BOUNDS = 8         /* device, builds with MOE_DEBUG only: an index outside its
+                                  buffer; the access was skipped, results are invalid   */
 } moe_status;
 
 /* Storage formats of the five use cases (Ascend mega_moe page, "Use Case / A / W" table;
@@ -67,7 +71,10 @@ typedef enum {
  *                   FP8 layout; its (N, K/64, 2) scale shape is this (N, K/32)).
  * MOE_A8W8_INT8     x int8 [T,H] in [-127,127] + fp32 [T] per-token scale; w1 int8
  *                   [E,2I,H] + fp32 [E,2I]; w2 int8 [E,H,I] + fp32 [E,H] per output channel.
- * MOE_A8W4_FP8_FP4  x e4m3 [T,H] + fp32 [T,H/128] power-of-two block scales; w1 e2m1
+ * MOE_A8W4_FP8_FP4  x e4m3 [T,H] + fp32 [T,H/128] power-of-two block scales (2^e with
+ *                   -127 <= e <= 127: the tensor cores take the scale's exponent byte as a UE8M0
+ *                   scale; the dispatch stage checks every scale and records
+ *                   MOE_ERR_BAD_SCALE for any other value); w1 e2m1
  *                   [E,2I,H/2] + UE8M0 [E,2I,H/32]; w2 e2m1 [E,H,I/2] + UE8M0 [E,H,I/32];
  *                   two e2m1 codes per byte, element 2j in the low nibble.
  * MOE_A8W4_INT      x as MOE_A8W8_INT8; w1 signed int4 [E,2I,H/2] + fp32 [E,2I]; w2 signed
@@ -297,12 +304,15 @@ MOE_API moe_status moe_workspace_layout(const moe_dims* d, moe_dtype_mode m, moe
  * counterpart of this call; it is an allocation-free variant of moe_plan.)
  *   topk_ids, counts, offsets, row_src  as for moe_plan (device memory, owned by the caller;
  *             counts and offsets are required, row_src is required when T*K > 0).
+ *   d         checked exactly as moe_plan checks it (hidden and intermediate included), then:
  *   Limits: T*K <= 65536 and E <= 1024 (T*(K+S) and E+S with shared experts, whose slots the
  *   plan includes as moe_plan's does); larger sizes return MOE_ERR_INVALID_ARG and launch
  *   nothing. The call allocates nothing: its scratch is one fixed 1,590,272-byte device array
  *   inside the library that every GPU which loads the library holds until the process exits.
  *   The first call on a device looks up that array's device address (cudaGetSymbolAddress)
- *   with the device current; make that first call before any stream capture.
+ *   with the device current; make that first call before any stream capture. The address
+ *   belongs to the device's current CUDA context: after cudaDeviceReset (or any new context)
+ *   the next call looks it up again, so make that call before a capture too.
  *   Every call shares the array and it keeps the last call's contents (the call clears what
  *   must start at zero itself); calls that overlap on the GPU race on it, so order them on
  *   one stream. Expert ids outside [-1, E) are skipped like masked routes; this call has no

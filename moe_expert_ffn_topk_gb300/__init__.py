@@ -6,6 +6,8 @@ without the built library raises ImportError: there is no fallback path.
 """
 import torch
 
+from ._binding import (MOE_ERR_BAD_ROUTE, MOE_ERR_BAD_SCALE, MOE_ERR_BOUNDS, MOE_ERR_CUDA,  # noqa: F401
+                       MOE_ERR_INVALID_ARG, MOE_ERR_TIMEOUT, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_OK)
 from ._binding import (ABI_FUNCTIONS, MODES, MOE_FLAG_FUSED, MOE_FLAG_NONE, MOE_FLAG_PAIR_L1,  # noqa: F401
                        MOE_FLAG_QUANTIZE_X, MOE_FLAG_SIMT, MOE_FLAG_SINGLE_CTA, MOE_FLAG_TOKEN_MAJOR,
                        MOE_FLAG_WEIGHT_MAJOR, MoeDims, MoeError, MoeOptions, dims, moe_check_device_error,

@@ -13,10 +13,13 @@ import os
 
 import torch
 
-_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libmoe_gb300.so")
+# MOE_GB300_DEBUG=1 loads the bounds-checking build (compiled with -DMOE_DEBUG by build(debug=True)):
+# the same kernels with every data-dependent row index checked on the device (MOE_ERR_BOUNDS)
+_LIB_NAME = "libmoe_gb300_debug.so" if os.environ.get("MOE_GB300_DEBUG") == "1" else "libmoe_gb300.so"
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", _LIB_NAME)
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_BAD_ROUTE, MOE_ERR_TIMEOUT, \
-    MOE_ERR_WORKSPACE = range(7)
+    MOE_ERR_WORKSPACE, MOE_ERR_BAD_SCALE, MOE_ERR_BOUNDS = range(9)
 MODES = {"a16w16": 0, "a8w8_fp8": 1, "a8w8_int8": 2, "a8w4_fp8_fp4": 3, "a8w4_int": 4, "a8w8_fp8_e5m2": 5}
 (MOE_FLAG_NONE, MOE_FLAG_SIMT, MOE_FLAG_WEIGHT_MAJOR, MOE_FLAG_QUANTIZE_X, MOE_FLAG_FUSED, MOE_FLAG_SINGLE_CTA,
  MOE_FLAG_PAIR_L1, MOE_FLAG_TOKEN_MAJOR) = 0, 1, 2, 4, 8, 16, 32, 64

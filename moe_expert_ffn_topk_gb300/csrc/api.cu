@@ -36,7 +36,7 @@ int64_t a_scale_row_bytes(int mode, int I) {
     }
 }
 
-static bool dims_ok(const moe_dims* d, moe_dtype_mode m) {
+bool dims_ok(const moe_dims* d, moe_dtype_mode m) {
     if (!d) return false;
     if (m < MOE_A16W16 || m > MOE_A8W8_FP8_E5M2) return false;
     const int S = d->num_shared_experts;
@@ -371,6 +371,8 @@ const char* moe_status_string(moe_status s) {
         case MOE_ERR_BAD_ROUTE: return "expert id outside [-1, num_experts)";
         case MOE_ERR_TIMEOUT: return "bounded device wait timed out";
         case MOE_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case MOE_ERR_BAD_SCALE: return "FP8 x FP4 activation scale that is not a power of two";
+        case MOE_ERR_BOUNDS: return "index outside its buffer (debug build check)";
         default: return "unknown status";
     }
 }

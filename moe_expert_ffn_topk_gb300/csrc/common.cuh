@@ -19,6 +19,33 @@ __device__ __forceinline__ void record_error(int32_t* hdr, int code) {
     atomicCAS(&hdr[kErrWord], 0, code);
 }
 
+// Index checks of the debug build (compiled with -DMOE_DEBUG): a data-dependent row index outside
+// [-1, n) records MOE_ERR_BOUNDS and comes back as -1, so the caller skips the row as padding. In
+// the default build both helpers return their argument and compile to nothing.
+__device__ __forceinline__ int debug_row(int32_t* hdr, int idx, int64_t n) {
+#ifdef MOE_DEBUG
+    if (idx < -1 || idx >= n) {
+        record_error(hdr, MOE_ERR_BOUNDS);
+        return -1;
+    }
+#else
+    (void)hdr;
+    (void)n;
+#endif
+    return idx;
+}
+
+__device__ __forceinline__ bool debug_ok(int32_t* hdr, bool ok) {
+#ifdef MOE_DEBUG
+    if (!ok) record_error(hdr, MOE_ERR_BOUNDS);
+    return ok;
+#else
+    (void)hdr;
+    (void)ok;
+    return true;
+#endif
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -63,6 +63,9 @@ moe_status layout(const moe_dims* d, moe_dtype_mode m, moe_workspace_layout_t* o
 moe_status make_plan_view(const moe_dims* d, moe_dtype_mode m, void* ws, size_t ws_bytes, Plan* p, bool pools);
 
 // Launchers (each returns cudaGetLastError() of its launches).
+// The shape and mode checks every entry point applies to moe_dims before anything else.
+bool dims_ok(const moe_dims* d, moe_dtype_mode m);
+
 cudaError_t launch_route(const Plan& p, const int32_t* topk_ids, int32_t* counts_out, int32_t* offsets_out,
                          int32_t* row_src_out, cudaStream_t s);
 cudaError_t launch_dispatch(const Plan& p, const void* x, const void* x_scale, cudaStream_t s);

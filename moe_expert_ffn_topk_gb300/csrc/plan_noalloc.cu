@@ -13,6 +13,7 @@
 // different host threads without ordering -- race on the array and give wrong plans.
 //
 // The kernels are the ones moe_plan launches; only the storage differs.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -50,22 +51,57 @@ static __device__ __align__(256) int32_t g_plan_scratch[kNoallocScratchInts];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
-int32_t* g_scratch_ptr[kMaxDevices] = {};
+struct ScratchAddr {
+    unsigned long long ctx_id;  // the context the address belongs to (IDs are never reused)
+    int32_t* ptr;
+};
+ScratchAddr g_scratch[kMaxDevices] = {};
 
-// Device address of g_plan_scratch on the current device, looked up once per device.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// The unique ID of the calling thread's current context, through the driver entry points (no
+// link-time dependency on libcuda).
+cudaError_t current_context_id(unsigned long long* id) {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(p);
+    });
+    if (!get_current || !get_id) return cudaErrorNotSupported;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return cudaErrorDeviceUninitialized;
+    return get_id(ctx, id) == CUDA_SUCCESS ? cudaSuccess : cudaErrorDeviceUninitialized;
+}
+
+// Device address of g_plan_scratch in the current context of the current device. It is looked up
+// once per device and looked up again when that device's context changes (after cudaDeviceReset
+// the old address is no longer mapped). With no context current yet, the lookup itself makes the
+// device's primary context current, and its ID is read afterwards.
 cudaError_t scratch_address(int32_t** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    unsigned long long ctx = 0;
+    const bool have_ctx = current_context_id(&ctx) == cudaSuccess;
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (!g_scratch_ptr[dev]) {
+    if (!have_ctx || !g_scratch[dev].ptr || g_scratch[dev].ctx_id != ctx) {
         void* ptr = nullptr;
         e = cudaGetSymbolAddress(&ptr, g_plan_scratch);
         if (e != cudaSuccess) return e;
-        g_scratch_ptr[dev] = static_cast<int32_t*>(ptr);
+        if ((e = current_context_id(&ctx)) != cudaSuccess) return e;
+        g_scratch[dev] = {ctx, static_cast<int32_t*>(ptr)};
     }
-    *out = g_scratch_ptr[dev];
+    *out = g_scratch[dev].ptr;
     return cudaSuccess;
 }
 
@@ -77,9 +113,8 @@ using namespace moe;
 
 extern "C" MOE_API moe_status moe_plan_noalloc(const int32_t* topk_ids, const moe_dims* d, int32_t* counts,
                                                int32_t* offsets, int32_t* row_src, moe_stream_t stream) {
-    if (!d || d->num_tokens < 0 || d->topk < 1 || d->num_shared_experts < 0 ||
-        d->topk + d->num_shared_experts > 32 || d->num_experts < d->topk ||
-        d->num_experts + d->num_shared_experts > kNoallocMaxExperts)
+    // the same dims checks as moe_plan (which takes them in A16W16 mode), then this call's array limits
+    if (!dims_ok(d, MOE_A16W16) || d->num_experts + d->num_shared_experts > kNoallocMaxExperts)
         return MOE_ERR_INVALID_ARG;
     const int E = d->num_experts + d->num_shared_experts, K = d->topk + d->num_shared_experts;
     const int64_t ids = (int64_t)d->num_tokens * K;  // the shared experts' slots included

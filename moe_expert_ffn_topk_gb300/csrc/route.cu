@@ -149,7 +149,8 @@ __global__ void route_scatter_kernel(const int32_t* __restrict__ ids, int n_ids,
                                      const int32_t* __restrict__ pos,
                                      const int32_t* __restrict__ offsets, const int32_t* __restrict__ pad_off,
                                      int32_t* __restrict__ row_src, int32_t* __restrict__ pool_src,
-                                     int32_t* __restrict__ slot_row, int32_t* __restrict__ row_src_out) {
+                                     int32_t* __restrict__ slot_row, int32_t* __restrict__ row_src_out,
+                                     int32_t* __restrict__ hdr, int64_t pool_rows) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n_ids) return;
     const int e = route_id(ids, i, Kt, Kr, Er);
@@ -160,6 +161,10 @@ __global__ void route_scatter_kernel(const int32_t* __restrict__ ids, int n_ids,
     }
     const int row = offsets[e] + p;
     const int prow = pad_off[e] + p;
+    if (!debug_ok(hdr, row >= 0 && row < n_ids && prow >= 0 && prow < pool_rows)) {
+        slot_row[i] = -1;
+        return;
+    }
     row_src[row] = i;
     if (row_src_out) row_src_out[row] = i;
     pool_src[prow] = i;
@@ -171,12 +176,12 @@ __global__ void route_scatter_kernel(const int32_t* __restrict__ ids, int n_ids,
 // drops the padding rows' results.
 __global__ void __launch_bounds__(128) dispatch_gather_kernel(const uint4* __restrict__ x, const uint32_t* __restrict__ xs,
                                                               const int32_t* __restrict__ pool_src,
-                                                              const int32_t* __restrict__ hdr, int K, int row_vecs,
+                                                              int32_t* __restrict__ hdr, int K, int row_vecs,
                                                               int scale_words, uint4* __restrict__ xp,
-                                                              uint32_t* __restrict__ xps) {
+                                                              uint32_t* __restrict__ xps, int64_t n_ids) {
     const int rows = hdr[kHdrPadRows];
     for (int r = blockIdx.x; r < rows; r += gridDim.x) {
-        const int src = pool_src[r];
+        const int src = debug_row(hdr, pool_src[r], n_ids);
         if (src < 0) continue;  // padding row
         uint4* dst = xp + (size_t)r * row_vecs;
         const uint4* s = x + (size_t)(src / K) * row_vecs;
@@ -197,20 +202,20 @@ __global__ void __launch_bounds__(128) dispatch_gather_kernel(const uint4* __res
 template <int MODE>
 __global__ void __launch_bounds__(128) dispatch_gather_q_kernel(const uint8_t* __restrict__ x, const uint8_t* __restrict__ xs,
                                                                 const int32_t* __restrict__ pool_src,
-                                                                const int32_t* __restrict__ hdr, int K, int H,
+                                                                int32_t* __restrict__ hdr, int K, int H,
                                                                 int scale_bytes, int64_t pool_rows, uint8_t* __restrict__ xp,
                                                                 uint8_t* __restrict__ xps, uint16_t* __restrict__ xb,
-                                                                int32_t* __restrict__ sums) {
+                                                                int32_t* __restrict__ sums, int64_t n_ids) {
     constexpr int kUnroll = 4;
     __shared__ int red[4];
     const int rows = hdr[kHdrPadRows];
     const int nv = H / 16;                 // 16-byte vectors of a row of codes
     const int scale_words = scale_bytes / 4;
     int r = blockIdx.x;
-    int src = r < rows ? __ldg(pool_src + r) : -1;
+    int src = r < rows ? debug_row(hdr, __ldg(pool_src + r), n_ids) : -1;
     while (r < rows) {
         const int rn = r + gridDim.x;
-        const int src_next = rn < rows ? __ldg(pool_src + rn) : -1;
+        const int src_next = rn < rows ? debug_row(hdr, __ldg(pool_src + rn), n_ids) : -1;
         if (src >= 0) {  // padding rows are left as they are (rows are independent everywhere)
             const int64_t tok = src / K;
             const uint4* xs4 = reinterpret_cast<const uint4*>(x + tok * H);
@@ -263,9 +268,18 @@ __global__ void __launch_bounds__(128) dispatch_gather_q_kernel(const uint8_t* _
                     }
                 }
             }
-            for (int w = threadIdx.x; w < scale_words; w += blockDim.x)
-                reinterpret_cast<uint32_t*>(xps + (int64_t)r * scale_bytes)[w] =
-                    __ldg(reinterpret_cast<const uint32_t*>(xs + tok * scale_bytes) + w);
+            for (int w = threadIdx.x; w < scale_words; w += blockDim.x) {
+                const uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(xs + tok * scale_bytes) + w);
+                if constexpr (MODE == MOE_A8W4_FP8_FP4) {
+                    // the block-scaled MMA takes the exponent byte as a UE8M0 scale, so the scale must be
+                    // 2^e with -127 <= e <= 127: a positive normal fp32 with a zero mantissa, or 2^-127
+                    // (the subnormal whose exponent byte is 0)
+                    const uint32_t sexp = v >> 23;  // sign and exponent bits
+                    const bool pow2 = (v & 0x7fffffu) == 0 ? (sexp >= 1 && sexp <= 254) : v == 0x00400000u;
+                    if (!pow2) record_error(hdr, MOE_ERR_BAD_SCALE);
+                }
+                reinterpret_cast<uint32_t*>(xps + (int64_t)r * scale_bytes)[w] = v;
+            }
             if constexpr (MODE == MOE_A8W4_INT) {  // src >= 0 is uniform across the block
 #pragma unroll
                 for (int o = 16; o >= 1; o >>= 1) row_sum += __shfl_xor_sync(0xffffffffu, row_sum, o);
@@ -291,13 +305,13 @@ template <int MODE>
 __global__ void __launch_bounds__(256) dispatch_quant_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ slot_row,
                                                              int T, int K, int H, int64_t pool_rows, uint8_t* __restrict__ xp,
                                                              uint8_t* __restrict__ xps, uint16_t* __restrict__ xb,
-                                                             int32_t* __restrict__ sums) {
+                                                             int32_t* __restrict__ sums, int32_t* __restrict__ hdr) {
     __shared__ float red[8];
     __shared__ int red_sum[8];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int t = blockIdx.x; t < T; t += gridDim.x) {
         // pool row of slot `lane` (K <= 32), shuffled to all lanes when the chunk is stored
-        const int my_row = lane < K ? __ldg(slot_row + (int64_t)t * K + lane) : -1;
+        const int my_row = lane < K ? debug_row(hdr, __ldg(slot_row + (int64_t)t * K + lane), pool_rows) : -1;
         const uint2* xr = reinterpret_cast<const uint2*>(x + (int64_t)t * H);  // 4 bf16 per uint2
         float s_int8 = 0.0f;
         if constexpr (int_mode(MODE)) {
@@ -470,7 +484,7 @@ cudaError_t launch_route(const Plan& p, const int32_t* topk_ids, int32_t* counts
     if (n_ids > 0) {
         route_scatter_kernel<<<(n_ids + 255) / 256, 256, 0, s>>>(topk_ids, n_ids, p.K, p.Kr, p.Er, p.E, p.pos,
                                                                  p.offsets, p.pad_off, p.row_src, p.pool_src,
-                                                                 p.slot_row, row_src_out);
+                                                                 p.slot_row, row_src_out, p.hdr, p.pool_rows);
     }
     return cudaGetLastError();
 }
@@ -481,7 +495,7 @@ static cudaError_t dispatch_q(const Plan& p, const void* x, const void* x_scale,
     dispatch_gather_q_kernel<MODE><<<grid, 128, 0, s>>>(static_cast<const uint8_t*>(x),
                                                         static_cast<const uint8_t*>(x_scale), p.pool_src, p.hdr, p.K,
                                                         p.H, (int)x_scale_row_bytes(MODE, p.H), p.pool_rows, p.x_pool,
-                                                        p.x_pool_scale, p.x_planes, p.x_sums);
+                                                        p.x_pool_scale, p.x_planes, p.x_sums, (int64_t)p.T * p.K);
     return cudaGetLastError();
 }
 
@@ -501,7 +515,7 @@ cudaError_t launch_dispatch(const Plan& p, const void* x, const void* x_scale, c
     dispatch_gather_kernel<<<grid, 128, 0, s>>>(static_cast<const uint4*>(x), static_cast<const uint32_t*>(x_scale),
                                                 p.pool_src, p.hdr, p.K, row_vecs, scale_words,
                                                 reinterpret_cast<uint4*>(p.x_pool),
-                                                reinterpret_cast<uint32_t*>(p.x_pool_scale));
+                                                reinterpret_cast<uint32_t*>(p.x_pool_scale), (int64_t)p.T * p.K);
     return cudaGetLastError();
 }
 
@@ -512,23 +526,23 @@ cudaError_t launch_dispatch_quant(const Plan& p, const void* x_bf16, cudaStream_
     switch (p.mode) {
         case MOE_A8W8_FP8_E5M2:
             dispatch_quant_kernel<MOE_A8W8_FP8_E5M2><<<grid, 256, 0, s>>>(x, p.slot_row, p.T, p.K, p.H, p.pool_rows,
-                                                                          p.x_pool, p.x_pool_scale, p.x_planes, p.x_sums);
+                                                                          p.x_pool, p.x_pool_scale, p.x_planes, p.x_sums, p.hdr);
             break;
         case MOE_A8W8_FP8:
             dispatch_quant_kernel<MOE_A8W8_FP8><<<grid, 256, 0, s>>>(x, p.slot_row, p.T, p.K, p.H, p.pool_rows, p.x_pool,
-                                                                     p.x_pool_scale, p.x_planes, p.x_sums);
+                                                                     p.x_pool_scale, p.x_planes, p.x_sums, p.hdr);
             break;
         case MOE_A8W8_INT8:
             dispatch_quant_kernel<MOE_A8W8_INT8><<<grid, 256, 0, s>>>(x, p.slot_row, p.T, p.K, p.H, p.pool_rows, p.x_pool,
-                                                                      p.x_pool_scale, p.x_planes, p.x_sums);
+                                                                      p.x_pool_scale, p.x_planes, p.x_sums, p.hdr);
             break;
         case MOE_A8W4_INT:
             dispatch_quant_kernel<MOE_A8W4_INT><<<grid, 256, 0, s>>>(x, p.slot_row, p.T, p.K, p.H, p.pool_rows, p.x_pool,
-                                                                     p.x_pool_scale, p.x_planes, p.x_sums);
+                                                                     p.x_pool_scale, p.x_planes, p.x_sums, p.hdr);
             break;
         case MOE_A8W4_FP8_FP4:
             dispatch_quant_kernel<MOE_A8W4_FP8_FP4><<<grid, 256, 0, s>>>(x, p.slot_row, p.T, p.K, p.H, p.pool_rows,
-                                                                         p.x_pool, p.x_pool_scale, p.x_planes, p.x_sums);
+                                                                         p.x_pool, p.x_pool_scale, p.x_planes, p.x_sums, p.hdr);
             break;
         default:  // A16W16: x is already the pool's format
             return launch_dispatch(p, x_bf16, nullptr, s);

@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(NT) l2_simt_kernel(Plan p, const uint8_t* __re
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int64_t row = r0 + ty * 4 + i;
-        const int src = p.pool_src[row];
+        const int src = debug_row(p.hdr, p.pool_src[row], (int64_t)p.T * p.K);
         if (src < 0) continue;  // padding row
         const float g = topk_weights[src];
         uint16_t out[4];
@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(32 * kRqWarps) int8_row_quant_kernel(Plan p) {
     const int lane = threadIdx.x & 31;
     const bool split = p.mode == MOE_A8W8_INT8;  // A8W4-INT: plane 0 holds q itself
     for (int r = blockIdx.x * kRqWarps + (threadIdx.x >> 5); r < rows; r += gridDim.x * kRqWarps) {
-        if (__ldg(p.pool_src + r) < 0) continue;  // padding row (uniform across the warp): never read back
+        if (debug_row(p.hdr, __ldg(p.pool_src + r), (int64_t)p.T * p.K) < 0) continue;  // padding row (uniform across the warp): never read back
         const float4* a = reinterpret_cast<const float4*>(p.a_f32 + (int64_t)r * I);
         float m = 0.0f;
         for (int v = lane; v < nv; v += 32) {

@@ -449,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int ci = 0; ci < kChunks; ++ci) {
                     const int n = 32 * ci + lane;
-                    src_l[ci] = n < tl.n_valid ? __ldg(p.pool_src + tl.row0 + n) : -1;
+                    src_l[ci] = n < tl.n_valid ? debug_row(p.hdr, __ldg(p.pool_src + tl.row0 + n), (int64_t)p.T * p.K) : -1;
                 }
 #pragma unroll
                 for (int ci = 0; ci < kChunks; ++ci) g_l[ci] = src_l[ci] >= 0 ? __ldg(args.topk_weights + src_l[ci]) : 0.0f;

@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int src = -1;
             float gw = 0.0f;
             if (!l1) {
-                src = __ldg(p.pool_src + row);
+                src = debug_row(p.hdr, __ldg(p.pool_src + row), (int64_t)p.T * p.K);
                 gw = src >= 0 ? __ldg(args.topk_weights + src) : 0.0f;
             }
             // every lane waits; the warp goes on only if all of them saw the phase complete

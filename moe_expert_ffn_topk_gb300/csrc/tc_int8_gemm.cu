@@ -359,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int ci = 0; ci < kTok / 32; ++ci) {
                     const int n = 32 * ci + lane;
-                    src[ci] = n < n_valid ? __ldg(p.pool_src + tl.row0 + n) : -1;
+                    src[ci] = n < n_valid ? debug_row(p.hdr, __ldg(p.pool_src + tl.row0 + n), (int64_t)p.T * p.K) : -1;
                     sx_l[ci] = __ldg(reinterpret_cast<const float*>(p.a_pool_scale) + tl.row0 + n);
                 }
 #pragma unroll

@@ -243,7 +243,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             int src = -1;
             float gw = 0.0f;
             if (!kL1 && mine) {
-                src = __ldg(p.pool_src + row);
+                src = debug_row(p.hdr, __ldg(p.pool_src + row), (int64_t)p.T * p.K);
                 gw = src >= 0 ? __ldg(args.topk_weights + src) : 0.0f;
             }
             const bool ok = mbar_wait(tfull_bar(a), (uint32_t)(tc >> 1) & 1u, p.hdr, abort_flag);

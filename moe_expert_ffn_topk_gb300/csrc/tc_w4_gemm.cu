@@ -320,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int src = -1;
             float gw = 0.0f;
             if constexpr (!kL1) {
-                src = valid ? __ldg(p.pool_src + row) : -1;
+                src = valid ? debug_row(p.hdr, __ldg(p.pool_src + row), (int64_t)p.T * p.K) : -1;
                 gw = src >= 0 ? __ldg(args.topk_weights + src) : 0.0f;
             }
             const bool w_ok = mbar_wait(acc_full(a), (uint32_t)(tc >> 1) & 1u, p.hdr, abort_flag);

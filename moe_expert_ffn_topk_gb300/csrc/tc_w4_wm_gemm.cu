@@ -364,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int src = -1;
                 float g = 0.0f;
                 if constexpr (!kL1) {
-                    src = n < tl.n_valid ? __ldg(p.pool_src + row) : -1;
+                    src = n < tl.n_valid ? debug_row(p.hdr, __ldg(p.pool_src + row), (int64_t)p.T * p.K) : -1;
                     g = src >= 0 ? __ldg(args.topk_weights + src) : 0.0f;
                 }
                 w_src[n] = src;

@@ -69,3 +69,59 @@ def slice_tokens(inp, tokens):
     if inp["x_scale"] is not None:
         out["x_scale"] = inp["x_scale"].index_select(0, idx).contiguous()
     return out
+
+
+def covering_tokens(topk_ids, seed, extra=2):
+    """A sample of tokens in which every expert that any token routes to appears at least once
+    (greedy set cover in a seeded order), plus `extra` more seeded tokens. Sorted token indices."""
+    ids = np.asarray(topk_ids)
+    rng = np.random.default_rng(seed)
+    sets = [set(int(e) for e in row if e >= 0) for row in ids]
+    uncovered = set().union(*sets) if sets else set()
+    order = [int(t) for t in rng.permutation(ids.shape[0])]
+    chosen = []
+    while uncovered:
+        best = max(order, key=lambda t: len(sets[t] & uncovered))
+        chosen.append(best)
+        uncovered -= sets[best]
+    chosen += [t for t in order if t not in chosen][:extra]
+    return sorted(chosen)
+
+
+def _oracle_chunk(args):
+    from oracle import moe as omoe
+    mode, h, inter, clamp = args
+    return omoe.forward(mode, h["x"], h["x_scale"], h["topk_ids"], h["topk_weights"], h["w1"], h["w1_scale"],
+                        h["w2"], h["w2_scale"], num_experts=h["w1"].shape[0], inter=inter, clamp=clamp)
+
+
+def oracle_tokens(mode, h, tokens, inter, workers=8, clamp=None):
+    """The oracle's y for a subset of tokens of host inputs h (numpy), computed in `workers` spawned
+    processes: every token is an independent problem and every expert an independent FFN, so each
+    chunk of tokens runs the oracle on the experts it routes to only (their weights sliced out, ids
+    renumbered). Returns y rows in the order of `tokens`."""
+    import concurrent.futures
+    import multiprocessing
+    tokens = list(tokens)
+    chunks = [tokens[i::workers] for i in range(min(workers, len(tokens)))]
+    jobs = []
+    for ch in chunks:
+        ids = h["topk_ids"][ch]
+        used = np.unique(ids[ids >= 0])
+        local = np.full(int(used.max()) + 1 if used.size else 1, -1, np.int64)
+        local[used] = np.arange(used.size)
+        sub = {"x": h["x"][ch], "x_scale": None if h["x_scale"] is None else h["x_scale"][ch],
+               "topk_ids": np.where(ids >= 0, local[np.maximum(ids, 0)], -1).astype(np.int32),
+               "topk_weights": h["topk_weights"][ch]}
+        for k in ("w1", "w1_scale", "w2", "w2_scale"):
+            sub[k] = None if h[k] is None else np.ascontiguousarray(h[k][used])
+        jobs.append((mode, sub, inter, clamp))
+    ctx = multiprocessing.get_context("spawn")  # never fork a process that holds a CUDA context
+    with concurrent.futures.ProcessPoolExecutor(max_workers=len(jobs), mp_context=ctx) as ex:
+        outs = list(ex.map(_oracle_chunk, jobs))
+    y = np.zeros((len(tokens), outs[0].shape[1]))
+    pos = {t: i for i, t in enumerate(tokens)}
+    for ch, out in zip(chunks, outs):
+        for j, t in enumerate(ch):
+            y[pos[t]] = out[j]
+    return y

@@ -52,6 +52,11 @@ def test_status_strings(moe):
     assert moe.moe_status_string(0) == "ok"
     assert "timed out" in moe.moe_status_string(5)
     assert moe.moe_status_string(99) == "unknown status"
+    statuses = _header_enum("MOE_ERR_")
+    assert statuses == {n: getattr(moe, n) for n in statuses} and len(statuses) == 8
+    for v in statuses.values():  # every status has its own message
+        assert moe.moe_status_string(v) != "unknown status"
+    assert len({moe.moe_status_string(v) for v in statuses.values()}) == len(statuses)
 
 
 CONFIGS = [(64, 256, 128, 8, 2), (4096, 4096, 14336, 8, 2), (128, 7168, 2048, 256, 8),

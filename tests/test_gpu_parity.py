@@ -4,11 +4,13 @@ Bars: counts, offsets and the per-expert multiset of row identities bit-exact; f
 point within max|y - y_ref| <= tol * max|y_ref| (2e-2 bf16 and the integer modes, 6e-2 for the
 FP8/FP4 modes); integer L2 accumulators bit-exact given the kernel's own re-quantised operand.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
 
-from gpu_util import TOL, assert_close, lib, region, run_forward, slice_tokens, y_numpy
+from gpu_util import TOL, assert_close, covering_tokens, lib, oracle_tokens, region, run_forward, slice_tokens, y_numpy
 from oracle import codecs as ocodecs
 from oracle import moe as omoe
 from workloads import WORKLOADS, Workload, make_inputs, to_numpy
@@ -224,6 +226,21 @@ def test_bad_route_is_reported_and_skipped(moe):
     assert_close(y_numpy(out["y"]), ref, wl.mode)
 
 
+@pytest.mark.parametrize("bad", [1.5 * 2.0 ** -6, 0.0, -0.25, float("inf"), 3.0])
+def test_fp8_fp4_x_scale_that_is_not_a_power_of_two_is_reported(moe, bad):
+    """The FP8 x FP4 tensor cores take an x scale's exponent byte as its UE8M0 scale, so the scale must be
+    2^e (-127 <= e <= 127): the dispatch stage reads every scale and reports any other value in the error
+    word, with no fault; 2^-127 (a subnormal fp32) and 2^127 are accepted."""
+    wl = CASES["a8w4_fp8_fp4"][0]
+    inp = make_inputs(wl, device=DEV)
+    inp["x_scale"] = inp["x_scale"].clone()
+    inp["x_scale"][3, 1] = bad
+    assert run_forward(moe, wl, inp)["status"] == moe.MOE_ERR_BAD_SCALE
+    inp["x_scale"][3, 1] = 2.0 ** -127
+    inp["x_scale"][5, 0] = 2.0 ** 127
+    assert run_forward(moe, wl, inp)["status"] == 0
+
+
 def test_zero_tokens(moe):
     wl = Workload("empty", "a16w16", 0, 256, 128, 8, 2, 38, 0.05)
     inp = make_inputs(wl, device=DEV)
@@ -248,19 +265,25 @@ def test_bounded_wait_times_out_and_device_stays_usable(moe):
 FULL = ["mixtral_bf16_prefill", "dsv3_fp8fp4_decode", "dsv3_fp8fp4_prefill_zipf", "int8_a8w8", "int4_a8w4"]
 
 
+ORACLE_WORKERS = max(1, min(12, os.cpu_count() or 1))
+
+
 @pytest.mark.parametrize("name", FULL)
 def test_full_size_sampled(moe, name):
-    """Full-size workload in the benchmark's launch configuration; the oracle checks a seeded
-    sample of tokens (every token is an independent problem) and the plan in full."""
+    """Full-size workload in the benchmark's launch configuration; the plan is checked in full and
+    y on a sample of tokens chosen so that every expert any token routes to is computed for at least
+    one sampled token (every token is an independent problem): an error confined to one expert's
+    tiles shows."""
     wl = WORKLOADS[name]
     inp = make_inputs(wl, device=DEV)
     out = run_forward(moe, wl, inp, stages=True)
     assert out["status"] == 0
     check_plan(out, wl, inp["topk_ids"])
-    rng = np.random.default_rng(wl.seed)
-    tokens = sorted(rng.choice(wl.T, size=min(wl.T, 6), replace=False).tolist())
-    sub = slice_tokens(inp, tokens)
-    ref = oracle_forward(wl, sub)
+    h = to_numpy(inp)
+    tokens = covering_tokens(h["topk_ids"], wl.seed)
+    touched = set(h["topk_ids"].ravel().tolist()) - {-1}
+    assert set(h["topk_ids"][tokens].ravel().tolist()) - {-1} == touched
+    ref = oracle_tokens(wl.mode, h, tokens, wl.I, ORACLE_WORKERS)
     got = y_numpy(out["y"])[tokens]
     assert_close(got, ref, wl.mode)
     # every row of the output is written and finite
@@ -492,8 +515,8 @@ def test_forward_quantizing_x_matches_oracle(moe, mode, wl):
 @pytest.mark.parametrize("name", ["dsv3_fp8fp4_prefill_zipf", "int8_a8w8", "dsv3_fp8fp4_decode", "int4_a8w4"])
 def test_full_size_quantizing_x_sampled(moe, name):
     """Full-size workload from bf16 x (the dispatch stage quantises it, as the bench's --quantize-x
-    times it): the pool codes of a seeded sample of tokens are bit-exact against the oracle's
-    quantisation, and their outputs match the oracle within the mode's bound."""
+    times it): on a sample of tokens that covers every routed expert, the pool codes are bit-exact
+    against the oracle's quantisation and the outputs match the oracle within the mode's bound."""
     wl = WORKLOADS[name]
     inp = make_inputs(wl, device=DEV)
     d = moe.dims(wl.T, wl.H, wl.I, wl.E, wl.K)
@@ -502,19 +525,21 @@ def test_full_size_quantizing_x_sampled(moe, name):
     moe.moe_forward(inp["x_bf16"], None, inp["topk_ids"], inp["topk_weights"], inp["w1"], inp["w1_scale"], inp["w2"],
                     inp["w2_scale"], y, d, wl.mode, ws, moe.MOE_FLAG_QUANTIZE_X)
     assert moe.moe_check_device_error(ws) == 0
-    rng = np.random.default_rng(wl.seed + 100)
-    tokens = np.sort(rng.choice(wl.T, size=6, replace=False))
     h = to_numpy({k: inp[k] for k in ("x_bf16", "topk_ids", "topk_weights", "w1", "w1_scale", "w2", "w2_scale")})
+    tokens = covering_tokens(h["topk_ids"], wl.seed + 100)
     qx, sx = omoe.quantize_x(wl.mode, h["x_bf16"][tokens])
     # the pool rows of the sampled tokens hold their codes
     L = moe.moe_workspace_layout(d, wl.mode)
-    slot_row = region(ws, L, "slot_row", torch.int32, wl.T * wl.K).view(wl.T, wl.K).cpu().numpy()
+    slot_row = region(ws, L, "slot_row", torch.int32, wl.T * wl.K).view(wl.T, wl.K)
     codes = region(ws, L, "x_pool", torch.uint8, L["pool_rows"] * wl.H).view(L["pool_rows"], wl.H)
+    rows = slot_row[torch.as_tensor(tokens, device=DEV)].long()
+    got_codes = codes[rows.reshape(-1)].view(len(tokens), wl.K, wl.H).cpu().numpy()
     for j, t in enumerate(tokens):
         for k in range(wl.K):
-            assert np.array_equal(codes[int(slot_row[t, k])].cpu().numpy(), qx.view(np.uint8)[j]), (t, k)
-    ref = omoe.forward(wl.mode, qx, sx, h["topk_ids"][tokens], h["topk_weights"][tokens], h["w1"], h["w1_scale"],
-                       h["w2"], h["w2_scale"], num_experts=wl.E, inter=wl.I)
+            assert np.array_equal(got_codes[j, k], qx.view(np.uint8)[j]), (t, k)
+    sub = {"x": qx, "x_scale": sx, "topk_ids": h["topk_ids"][tokens], "topk_weights": h["topk_weights"][tokens],
+           **{k: h[k] for k in ("w1", "w1_scale", "w2", "w2_scale")}}
+    ref = oracle_tokens(wl.mode, sub, range(len(tokens)), wl.I, ORACLE_WORKERS)
     assert_close(y_numpy(y)[tokens], ref, wl.mode)
     assert torch.isfinite(y.float()).all()
 
