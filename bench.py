@@ -46,6 +46,10 @@ def parse():
                          "tiles (FP8 modes at prefill sizes; A8W4-INT at any tile count), 16 one-CTA bf16 L2, "
                          "32 bf16 L1 on CTA pairs, 64 token-major A8W4-INT")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--configs", default="all", choices=["all", "none"],
+                    help="all: also time the method's other configurations in the same run (each in the line's "
+                         "'configs' object); none: the selected workload only")
+    ap.add_argument("--no-probe", action="store_true", help="skip the tensor-core peak probe")
     ap.add_argument("--tokens", type=int, default=None, help="override the workload's token count")
     ap.add_argument("--experts", type=int, default=None, help="override the workload's expert count")
     ap.add_argument("--fused", action="store_true",
@@ -307,17 +311,94 @@ def is_decode(wl) -> bool:
     return wl.routed_rows / wl.E < 64
 
 
-def l1_roofline(wl, inp, l1_ms, pk, pk_src, sustained):
-    """Roofline of the dominant kernel, the L1 grouped GEMM (2/3 of the flops and of the weight
-    bytes). Tensor-bound workloads: algorithmic flops 4*H*I per routed row against the dense
-    bf16 peak (the tensor-core kind every GEMM here issues). Weight-streaming (decode)
-    workloads: algorithmic bytes = W1 (+ block scales) of every expert with N_e > 0 plus the x
-    rows, against the measured HBM copy bandwidth."""
+# The tcgen05 instruction kind each mode's GEMMs issue (include/moe_peak.h) and how many of its MACs
+# one algorithmic MAC costs: the INT8 GEMM runs every int8 product as two exact f16 products (the
+# hi/lo split of the tokens), A8W4-INT and the float modes one.
+TENSOR_KIND = {"a16w16": ("bf16", 1), "a8w8_fp8": ("e4m3_e4m3", 1), "a8w8_fp8_e5m2": ("e4m3_e4m3", 1),
+               "a8w4_fp8_fp4": ("e4m3_e2m1", 1), "a8w8_int8": ("f16", 2), "a8w4_int": ("f16", 1)}
+PROBE_ITERS = 20000  # about 5 ms of MMA work per CTA at 1.9 GHz
+
+
+def measure_tensor_peaks(moe, dev, kinds, sustained_s=0.0):
+    """The dense rate of each tcgen05 kind in `kinds`, from the library's probe (one CTA per SM issuing
+    back-to-back MMAs on shared-memory operands), timed with events on the launching stream: one launch
+    after a warm-up launch (burst) and, with sustained_s > 0, back-to-back launches for that long
+    (under the power cap). TFLOP/s, with the SM clock sampled during the probes."""
+    import torch
+    stream = torch.cuda.current_stream()
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    out = {}
+    with ClockSampler(dev.index or 0) as clocks:
+        clocks.mark_start()
+        for kind in kinds:
+            moe.moe_tensor_peak_probe(kind, PROBE_ITERS // 10, ws, stream=stream)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            flops = moe.moe_tensor_peak_probe(kind, PROBE_ITERS, ws, stream=stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            rec = {"burst_tflops": flops / (e0.elapsed_time(e1) * 1e-3) / 1e12}
+            if sustained_s > 0:
+                total, n = 0.0, 0
+                e0.record(stream)
+                t_end = time.time() + sustained_s
+                while time.time() < t_end:
+                    total += moe.moe_tensor_peak_probe(kind, PROBE_ITERS, ws, stream=stream)
+                    n += 1
+                    if n % 8 == 0:
+                        torch.cuda.synchronize()  # keep the queue short so the loop lasts sustained_s
+                e1.record(stream)
+                torch.cuda.synchronize()
+                rec["sustained_tflops"] = total / (e0.elapsed_time(e1) * 1e-3) / 1e12
+            out[kind] = rec
+        clocks.mark_end()
+    st = moe.moe_check_device_error(ws)
+    if st != 0:
+        raise RuntimeError(f"tensor peak probe: {moe.moe_status_string(st)}")
+    out["clocks"] = clocks.summary()
+    out["how"] = (f"moe_tensor_peak_probe: one CTA per SM, {PROBE_ITERS} x 4 dense MMAs (M 128, N 256) per CTA on "
+                  "shared-memory operands, CUDA events; burst = one launch after a warm-up launch")
+    return out
+
+
+def tensor_peak(wl, pk, pk_src, probe, sustained):
+    """The peak of the tensor pipe a mode's GEMMs use, in algorithmic TFLOP/s (or TOP/s): the bf16
+    modes take the measured cuBLAS bf16 figure; the others the probe's measured rate of their
+    own instruction kind, divided by the MACs each algorithmic MAC costs (2 for the hi/lo INT8 split)."""
+    clock = "sustained" if sustained else "burst"
+    kind, cost = TENSOR_KIND[wl.mode]
+    if kind == "bf16":
+        return float(pk["bf16_tflops_sustained" if sustained else "bf16_tflops"]), f"{pk_src} bf16 dense (cuBLAS), {clock}"
+    rec = probe.get(kind, {}) if probe else {}
+    key = "sustained_tflops" if sustained and "sustained_tflops" in rec else "burst_tflops"
+    if key in rec:
+        src = f"measured tcgen05 {kind} dense rate (moe_tensor_peak_probe, {key.split('_')[0]})"
+        if cost != 1:
+            src += f" / {cost} (each int8 MAC runs as {cost} exact f16 MACs)"
+        return rec[key] / cost, src
+    # no probe: the bf16 measurement times the nominal dense ratio of the kind
+    ratio = 2.0 if kind.startswith("e4m3") else 1.0
+    bf = float(pk["bf16_tflops_sustained" if sustained else "bf16_tflops"])
+    return bf * ratio / cost, f"{pk_src} bf16 dense ({clock}) x nominal {kind}/bf16 ratio {ratio} / {cost}"
+
+
+def touched_weight_bytes(wl, inp):
+    """W1 and W2 (with their scales) of every expert with N_e > 0, and the number of such experts."""
     import numpy as np
+    ids = inp["topk_ids"].cpu().numpy().reshape(-1)
+    touched = len(np.unique(ids[ids >= 0]))
+    return touched * 3 * wl.I * wl.H * WEIGHT_BYTES_PER_ELEM[wl.mode], touched
+
+
+def l1_roofline(wl, inp, l1_ms, pk, pk_src, probe, sustained):
+    """Roofline of the dominant kernel, the L1 grouped GEMM (2/3 of the flops and of the weight
+    bytes). Tensor-bound workloads: algorithmic flops 4*H*I per routed row against the dense peak of
+    the mode's tensor pipe (tensor_peak). Weight-streaming (decode) workloads: algorithmic bytes = W1
+    (+ block scales) of every expert with N_e > 0 plus the x rows, against the measured HBM copy
+    bandwidth."""
     if is_decode(wl):
-        ids = inp["topk_ids"].cpu().numpy().reshape(-1)
-        touched = len(np.unique(ids[ids >= 0]))
-        nbytes = touched * 2 * wl.I * wl.H * WEIGHT_BYTES_PER_ELEM[wl.mode] + wl.T * wl.H * X_BYTES_PER_ELEM[wl.mode]
+        w_bytes, touched = touched_weight_bytes(wl, inp)
+        nbytes = w_bytes * 2 / 3 + wl.T * wl.H * X_BYTES_PER_ELEM[wl.mode]
         achieved = nbytes / (l1_ms * 1e-3) / 1e9
         peak = float(pk["hbm_gbs"])
         return {"bound": "hbm", "kernel": "L1 grouped GEMM + SwiGLU (moe_expert_l1)", "achieved": achieved,
@@ -326,17 +407,28 @@ def l1_roofline(wl, inp, l1_ms, pk, pk_src, sustained):
                 "traffic": dominant_kernel_traffic(wl.name)}
     l1_flops = 4.0 * wl.H * wl.I * wl.routed_rows
     achieved = l1_flops / (l1_ms * 1e-3) / 1e12
-    bf16_peak = float(pk["bf16_tflops_sustained"] if sustained else pk["bf16_tflops"])
-    clock = "sustained" if sustained else "burst"
-    if wl.mode in ("a8w8_fp8", "a8w4_fp8_fp4"):
-        # block-scaled kind::mxf8f6f4 MMAs: no fp8 peak is measured on this machine, so the bf16
-        # measurement is scaled by the nominal dense ratio 4.5 / 2.25 PFLOP/s
-        peak, src = 2.0 * bf16_peak, f"{pk_src} bf16 dense ({clock}) x nominal fp8/bf16 ratio 2"
-    else:
-        peak, src = bf16_peak, f"{pk_src} bf16 dense, {clock}"
+    peak, src = tensor_peak(wl, pk, pk_src, probe, sustained)
     return {"bound": "tensor", "kernel": "L1 grouped GEMM + SwiGLU (moe_expert_l1)", "achieved": achieved,
             "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": src, "l1_ms": l1_ms,
-            "traffic": dominant_kernel_traffic(wl.name)}
+            "algorithmic_flops": l1_flops, "traffic": dominant_kernel_traffic(wl.name)}
+
+
+def step_roofline(wl, inp, step_ms, pk, pk_src, probe, sustained):
+    """The whole step against the roofline that bounds it: for decode, every algorithmic byte (touched
+    W1 + W2 with scales, x, ids, gates, y) against the HBM copy bandwidth; otherwise 6*H*I flops per
+    routed row against the mode's tensor peak."""
+    if is_decode(wl):
+        w_bytes, touched = touched_weight_bytes(wl, inp)
+        nbytes = (w_bytes + wl.T * wl.H * X_BYTES_PER_ELEM[wl.mode] + wl.T * wl.K * 8 + wl.T * wl.H * 2)
+        achieved = nbytes / (step_ms * 1e-3) / 1e9
+        peak = float(pk["hbm_gbs"])
+        return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "peak_source": f"{pk_src} HBM copy", "algorithmic_bytes": nbytes, "experts_touched": touched,
+                "step_ms": step_ms}
+    achieved = wl.flops / (step_ms * 1e-3) / 1e12
+    peak, src = tensor_peak(wl, pk, pk_src, probe, sustained)
+    return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "peak_source": src, "step_ms": step_ms}
 
 
 def fused_roofline(wl, ffn_ms, pk, pk_src, sustained):
@@ -352,43 +444,43 @@ def fused_roofline(wl, ffn_ms, pk, pk_src, sustained):
             "traffic": dominant_kernel_traffic(wl.name, "ffn_fused")}
 
 
-def run_gb300(args, wl, rank, world, local_rank):
+def measure_workload(args, wl, world, local_rank, fused=False, quantize_x=False, flags=0):
+    """Times args.steps steps of one workload (after args.warmup) through the C ABI with inputs resident
+    in HBM, then the same metric end to end with host buffers twice: copies overlapped with the
+    neighbouring steps on two copy streams, and serial (copy in, forward, copy out on one stream).
+    Returns the raw measurements of rank 0 (None on other ranks) and the inputs."""
     import torch
     import torch.distributed as dist
 
     import moe_expert_ffn_topk_gb300 as moe
     from workloads import make_inputs
 
-    torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     stream = torch.cuda.current_stream()
     inp = make_inputs(wl, device=dev)
     d = moe.dims(wl.T, wl.H, wl.I, wl.E, wl.K)
     ws = moe.alloc_workspace(d, wl.mode, dev)
     y = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=dev)
-
-    flags = args.flags | (moe.MOE_FLAG_QUANTIZE_X if args.quantize_x else 0) | (moe.MOE_FLAG_FUSED if args.fused else 0)
+    fwd_flags = flags | (moe.MOE_FLAG_QUANTIZE_X if quantize_x else 0) | (moe.MOE_FLAG_FUSED if fused else 0)
 
     def step(ev_l1=None):
         moe.moe_plan(inp["topk_ids"], d, ws, stream=stream)
-        if args.quantize_x:
+        if quantize_x:
             moe.moe_dispatch_quantize(inp["x_bf16"], d, wl.mode, ws, stream=stream)
         else:
             moe.moe_dispatch(inp["x"], inp["x_scale"], d, wl.mode, ws, stream=stream)
         if ev_l1:
             ev_l1[0].record(stream)
-        if args.fused:  # the events bracket the one launch of S3-S6
+        if fused:  # the events bracket the one launch of S3-S6
             moe.moe_expert_ffn(inp["w1"], inp["w1_scale"], inp["w2"], inp["w2_scale"], inp["topk_weights"], d, wl.mode,
                                ws, y=y, stream=stream)
             if ev_l1:
                 ev_l1[1].record(stream)
             return
-        else:
-            moe.moe_expert_l1(inp["w1"], inp["w1_scale"], d, wl.mode, ws, args.flags, stream=stream)
-            if ev_l1:
-                ev_l1[1].record(stream)
-            moe.moe_expert_l2(inp["w2"], inp["w2_scale"], inp["topk_weights"], d, wl.mode, ws, args.flags,
-                              stream=stream)
+        moe.moe_expert_l1(inp["w1"], inp["w1_scale"], d, wl.mode, ws, flags, stream=stream)
+        if ev_l1:
+            ev_l1[1].record(stream)
+        moe.moe_expert_l2(inp["w2"], inp["w2_scale"], inp["topk_weights"], d, wl.mode, ws, flags, stream=stream)
         moe.moe_combine(y, d, ws, stream=stream)
 
     def barrier():
@@ -400,7 +492,7 @@ def run_gb300(args, wl, rank, world, local_rank):
         step()
     st = moe.moe_check_device_error(ws)
     if st != 0:
-        raise RuntimeError(f"device error during warm-up: {moe.moe_status_string(st)}")
+        raise RuntimeError(f"{wl.name}: device error during warm-up: {moe.moe_status_string(st)}")
 
     l1_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                  for _ in range(args.steps)]
@@ -418,21 +510,27 @@ def run_gb300(args, wl, rank, world, local_rank):
     l1_ms = statistics.mean(a.elapsed_time(b) for a, b in l1_events)
     st = moe.moe_check_device_error(ws)
     if st != 0:
-        raise RuntimeError(f"device error in the timed region: {moe.moe_status_string(st)}")
+        raise RuntimeError(f"{wl.name}: device error in the timed region: {moe.moe_status_string(st)}")
     elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
 
-    # end to end through the public API with host buffers: every step copies its inputs from
-    # pinned host memory, calls moe_forward and copies y back to pinned host memory. The input and
-    # the output copies run on two more streams with double-buffered device inputs and outputs, so
-    # step i+1's input copy and step i-1's y copy overlap step i's compute (events order each
-    # buffer's use; one copy stream would queue step i+1's inputs behind step i's y).
-    x_keys = ("x_bf16",) if args.quantize_x else ("x", "x_scale")
+    # end to end through the public API with host buffers: every step copies its inputs from pinned host
+    # memory, calls moe_forward and copies y back to pinned host memory
+    x_keys = ("x_bf16",) if quantize_x else ("x", "x_scale")
     host_in = {k: inp[k].cpu().pin_memory() for k in x_keys + ("topk_ids", "topk_weights") if inp[k] is not None}
     dev_in = [{k: torch.empty_like(v, device=dev) for k, v in host_in.items()} for _ in range(2)]
     y_dev = [y, torch.empty_like(y)]
     y_host = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for _ in range(2)]
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
     d2h = y_host[0].numel() * y_host[0].element_size()
+
+    def forward(di, yd):
+        moe.moe_forward(di["x_bf16"] if quantize_x else di["x"], di.get("x_scale"), di["topk_ids"], di["topk_weights"],
+                        inp["w1"], inp["w1_scale"], inp["w2"], inp["w2_scale"], yd, d, wl.mode, ws, fwd_flags,
+                        stream=stream)
+
+    # (a) overlapped: the input and the output copies run on two more streams with double-buffered
+    # device inputs and outputs, so step i+1's input copy and step i-1's y copy overlap step i's compute
+    # (events order each buffer's use), as a serving loop would run
     in_stream, out_stream = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     ev = lambda: torch.cuda.Event()  # noqa: E731
     in_ready, fwd_done, out_read = [ev(), ev()], [ev(), ev()], [ev(), ev()]
@@ -448,10 +546,7 @@ def run_gb300(args, wl, rank, world, local_rank):
             in_ready[b].record(in_stream)
         stream.wait_event(in_ready[b])
         stream.wait_event(out_read[b])  # y_dev[b] of two steps back has been copied out
-        di = dev_in[b]
-        moe.moe_forward(di["x_bf16"] if args.quantize_x else di["x"], di.get("x_scale"), di["topk_ids"],
-                        di["topk_weights"], inp["w1"], inp["w1_scale"], inp["w2"], inp["w2_scale"], y_dev[b], d,
-                        wl.mode, ws, flags, stream=stream)
+        forward(dev_in[b], y_dev[b])
         fwd_done[b].record(stream)
         with torch.cuda.stream(out_stream):
             out_stream.wait_event(fwd_done[b])
@@ -474,33 +569,134 @@ def run_gb300(args, wl, rank, world, local_rank):
     barrier()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
 
-    if rank != 0:
-        return None, None
+    # (b) serial: copy in, forward, copy out, one after the other on one stream (a call that cannot
+    # be overlapped with its neighbours)
+    def serial_step():
+        for k, v in host_in.items():
+            dev_in[0][k].copy_(v, non_blocking=True)
+        forward(dev_in[0], y_dev[0])
+        y_host[0].copy_(y_dev[0], non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        serial_step()
+    barrier()
+    e0.record(stream)
+    for _ in range(args.steps):
+        serial_step()
+    e1.record(stream)
+    barrier()
+    serial_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    st = moe.moe_check_device_error(ws)
+    if st != 0:
+        raise RuntimeError(f"{wl.name}: device error in the end-to-end runs: {moe.moe_status_string(st)}")
+    res = {"elapsed_ms": elapsed_ms, "l1_ms": l1_ms, "e2e_ms": e2e_ms, "serial_ms": serial_ms, "h2d": h2d,
+           "d2h": d2h, "clocks": clocks.summary()}
+    del ws, y, y_dev, dev_in
+    return res, inp
+
+
+def cpu_baseline(wl, inp, seconds, quantize_x=False):
+    """The oracle, as it stands, on one seeded sample of whole tokens sized to about `seconds` on the host
+    cores; re-sized up to four times if it came out short (the oracle's fixed cost grows with the experts a
+    sample touches, so the two-probe fit can come out short)."""
+    from workloads import to_numpy
+    h = to_numpy(inp)
+    n_tok = sample_tokens_for(wl, h, seconds, quantize_x=quantize_x)
+    for attempt in range(5):
+        dt, rows = oracle_sample(wl, h, n_tok, seed=7 + attempt, quantize_x=quantize_x)
+        if dt >= 0.6 * seconds or n_tok >= wl.T or attempt == 4:
+            break
+        n_tok = int(min(wl.T, max(n_tok + 1, n_tok * seconds / max(dt, 1e-3))))
+    return {"value": 6.0 * wl.H * wl.I * rows / dt / 1e12, "unit": "TFLOP/s", "cores": oracle_threads(),
+            "kind": "oracle", "sample": f"{n_tok} seeded tokens ({rows} routed rows) of {wl.name}, {dt:.1f} s, "
+                                        f"float64 numpy oracle"}
+
+
+def is_sustained(res):
+    """The sustained (power-capped) peak when the GPU was at its power cap during the timed region, or
+    the region lasted a second or more; the burst peak for a short, uncapped one."""
+    return res["elapsed_ms"] >= 1000.0 or "sw_power_cap" in (res["clocks"].get("reasons") or [])
+
+
+def result_fields(args, wl, res, inp, world, pk, pk_src, probe, fused, quantize_x):
+    """The per-workload measurements of the JSON line (rank 0)."""
     flops = float(wl.flops)
-    ms_per_step = elapsed_ms / args.steps
-    value = whole_job_tflops(flops, args.steps, elapsed_ms, world)
-    pk, pk_src = peaks()
-    # the sustained (power-capped) peak when the GPU was at its power cap during the timed
-    # region, or the region lasted a second or more; the burst peak for a short, uncapped one
-    clock_summary = clocks.summary()
-    sustained = elapsed_ms >= 1000.0 or "sw_power_cap" in (clock_summary.get("reasons") or [])
-    if args.fused:
-        roof = fused_roofline(wl, l1_ms, pk, pk_src, sustained)
-    else:
-        roof = l1_roofline(wl, inp, l1_ms, pk, pk_src, sustained)
-    line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": DTYPE[wl.mode], "data": "synthetic (seeded; random-init weights)",
-        "config": workload_config(wl, args.quantize_x, args.fused),
-        "routed_rows_per_s": world * wl.routed_rows * args.steps / (elapsed_ms * 1e-3),
+    ms_per_step = res["elapsed_ms"] / args.steps
+    sustained = is_sustained(res)
+    roof = (fused_roofline(wl, res["l1_ms"], pk, pk_src, sustained) if fused
+            else l1_roofline(wl, inp, res["l1_ms"], pk, pk_src, probe, sustained))
+    return {
+        "value": whole_job_tflops(flops, args.steps, res["elapsed_ms"], world), "unit": "TFLOP/s",
+        "ms_per_step": ms_per_step, "dtype": DTYPE[wl.mode], "config": workload_config(wl, quantize_x, fused),
+        "routed_rows_per_s": world * wl.routed_rows * args.steps / (res["elapsed_ms"] * 1e-3),
         "roofline": roof,
-        "e2e": {"value": whole_job_tflops(flops, args.steps, e2e_ms, world), "unit": "TFLOP/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps},
-        "gpu_launches": (LAUNCHES_PER_STEP[wl.mode] - (2 if args.fused else 0)) * args.steps,
-        "clocks": clock_summary,
+        "step_roofline": step_roofline(wl, inp, ms_per_step, pk, pk_src, probe, sustained),
+        "e2e": {"value": whole_job_tflops(flops, args.steps, res["e2e_ms"], world), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
+                "ms_per_step": res["e2e_ms"] / args.steps,
+                "copies": "overlapped: each step's input copy and the previous step's y copy run on two more "
+                          "streams beside the forward (double-buffered)",
+                "serial": {"value": whole_job_tflops(flops, args.steps, res["serial_ms"], world), "unit": "TFLOP/s",
+                           "ms_per_step": res["serial_ms"] / args.steps,
+                           "copies": "copy in, moe_forward, copy out, one after the other on one stream"}},
+        "gpu_launches": (LAUNCHES_PER_STEP[wl.mode] - (2 if fused else 0)) * args.steps,
+        "clocks": res["clocks"],
     }
-    return line, inp
+
+
+# the other configurations of the method's benchmark, measured in the same run (each with the same steps
+# and warm-up), and the oracle's sample length for their cpu_baseline
+OTHER_CONFIGS = ("tiny_bf16", "dsv3_fp8fp4_decode", "dsv3_fp8fp4_prefill_zipf", "int8_a8w8", "int4_a8w4")
+OTHER_CPU_SECONDS = 4.0
+
+
+def run_gb300(args, wl, rank, world, local_rank):
+    import torch
+
+    import moe_expert_ffn_topk_gb300 as moe
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    runs = [(wl, args.fused, args.quantize_x, args.flags)]
+    if args.configs == "all":
+        from workloads import WORKLOADS
+        runs += [(WORKLOADS[n], False, False, 0) for n in OTHER_CONFIGS if n != wl.name]
+    measured = []
+    for w, fused, qx, flags in runs:
+        res, inp = measure_workload(args, w, world, local_rank, fused, qx, flags)
+        cpu = None
+        if rank == 0 and not args.no_cpu_baseline:
+            cpu = cpu_baseline(w, inp, CPU_BASELINE_SECONDS if w is wl else OTHER_CPU_SECONDS, qx)
+        ids = inp["topk_ids"].cpu()
+        measured.append((w, fused, qx, res, {"topk_ids": ids}, cpu))
+        del inp
+        torch.cuda.empty_cache()
+    # the peaks of the tensor pipes the measured modes use, after every timed region (so that the probes'
+    # heat and power do not touch the measurements)
+    kinds = sorted({TENSOR_KIND[w.mode][0] for w, *_ in measured} | {"bf16"})
+    sustained_s = 2.0 if any(is_sustained(r) for _, _, _, r, _, _ in measured) else 0.0
+    probe = measure_tensor_peaks(moe, dev, kinds, sustained_s) if not args.no_probe else None
+    if rank != 0:
+        return None
+    pk, pk_src = peaks()
+    lines = []
+    for w, fused, qx, res, inp, cpu in measured:
+        f = result_fields(args, w, res, inp, world, pk, pk_src, probe, fused, qx)
+        if cpu is not None:
+            f["cpu_baseline"] = cpu
+        lines.append(f)
+    head = lines[0]
+    line = {"metric": METRIC, "value": head["value"], "unit": head["unit"], "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": head["dtype"], "data": "synthetic (seeded; random-init weights)"}
+    line.update({k: v for k, v in head.items() if k not in line})
+    # gpu_launches counts the library kernels of the headline's timed region; each entry of "configs"
+    # counts those of its own timed region
+    if len(lines) > 1:
+        line["configs"] = {f["config"]["workload"]: f for f in lines[1:]}
+    if probe:
+        line["tensor_peaks"] = probe
+    return line
 
 
 def main():
@@ -523,23 +719,7 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
-    line, inp = run_gb300(args, wl, rank, world, local_rank)
-    if line is not None and not args.no_cpu_baseline:
-        from workloads import to_numpy
-        h = to_numpy(inp)
-        # one sample of about 10-30 s of oracle time; re-sized once if it came out short
-        # (the oracle's fixed cost grows with the experts a sample touches, so the fit can
-        # come out short: grow the sample, at most four times, until it lasts long enough)
-        n_tok = sample_tokens_for(wl, h, CPU_BASELINE_SECONDS, quantize_x=args.quantize_x)
-        for attempt in range(5):
-            dt, rows = oracle_sample(wl, h, n_tok, seed=7 + attempt, quantize_x=args.quantize_x)
-            if dt >= 0.6 * CPU_BASELINE_SECONDS or n_tok >= wl.T or attempt == 4:
-                break
-            n_tok = int(min(wl.T, max(n_tok + 1, n_tok * CPU_BASELINE_SECONDS / max(dt, 1e-3))))
-        line["cpu_baseline"] = {"value": 6.0 * wl.H * wl.I * rows / dt / 1e12, "unit": "TFLOP/s",
-                                "cores": oracle_threads(), "kind": "oracle",
-                                "sample": f"{n_tok} seeded tokens ({rows} routed rows) of {wl.name}, "
-                                          f"{dt:.1f} s, float64 numpy oracle"}
+    line = run_gb300(args, wl, rank, world, local_rank)
     if line is not None:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -13,7 +13,8 @@ from ._binding import (ABI_FUNCTIONS, MODES, MOE_FLAG_FUSED, MOE_FLAG_NONE, MOE_
                        MOE_FLAG_WEIGHT_MAJOR, MoeDims, MoeError, MoeOptions, dims, moe_check_device_error,
                        moe_combine, moe_debug_bounded_wait, moe_dispatch, moe_dispatch_quantize, moe_expert_l1,
                        moe_expert_l1_ex, moe_expert_l2, moe_expert_ffn, moe_forward, moe_forward_ex, moe_plan, moe_plan_noalloc,
-                       moe_status_string, moe_workspace_bytes, moe_workspace_layout)
+                       moe_status_string, moe_tensor_peak_probe, moe_workspace_bytes, moe_workspace_layout)
+from ._binding import PEAK_KINDS  # noqa: F401
 
 
 def alloc_workspace(d: MoeDims, mode, device="cuda") -> torch.Tensor:

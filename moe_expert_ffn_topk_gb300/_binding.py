@@ -27,7 +27,9 @@ MODES = {"a16w16": 0, "a8w8_fp8": 1, "a8w8_int8": 2, "a8w4_fp8_fp4": 3, "a8w4_in
 ABI_FUNCTIONS = ("moe_workspace_bytes", "moe_plan", "moe_dispatch", "moe_expert_l1", "moe_expert_l2",
                  "moe_combine", "moe_forward", "moe_check_device_error", "moe_status_string",
                  "moe_workspace_layout", "moe_debug_bounded_wait", "moe_plan_noalloc", "moe_dispatch_quantize",
-                 "moe_expert_l1_ex", "moe_forward_ex", "moe_expert_ffn")
+                 "moe_expert_l1_ex", "moe_forward_ex", "moe_expert_ffn", "moe_tensor_peak_probe")
+# moe_peak_kind (include/moe_peak.h): the tcgen05 instruction kinds the probe measures
+PEAK_KINDS = {"bf16": 0, "f16": 1, "e4m3_e2m1": 2, "e4m3_e4m3": 3}
 
 
 class MoeDims(ctypes.Structure):
@@ -83,6 +85,7 @@ def _load():
         "moe_expert_ffn": (st, [MoeOperand, MoeOperand, vp, vp, dims_p, st, ctypes.POINTER(MoeOptions), vp, sz, vp]),
         "moe_forward_ex": (st, [MoeOperand, vp, vp, MoeOperand, MoeOperand, vp, dims_p, st, ctypes.POINTER(MoeOptions),
                                 vp, sz, vp]),
+        "moe_tensor_peak_probe": (st, [st, ctypes.c_int64, ctypes.c_int, ctypes.POINTER(ctypes.c_double), vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -243,6 +246,17 @@ def moe_check_device_error(workspace, stream=None) -> int:
 def moe_debug_bounded_wait(workspace, timeout_ns: int, stream=None):
     ws, nb = _ws(workspace)
     _check(LIB.moe_debug_bounded_wait(ws, nb, int(timeout_ns), _stream(stream)), "moe_debug_bounded_wait")
+
+
+def moe_tensor_peak_probe(kind, iters_per_cta: int, workspace, grid: int = 0, stream=None) -> float:
+    """Launches the dense tensor-core probe of one instruction kind ("bf16", "f16", "e4m3_e2m1",
+    "e4m3_e4m3"); returns the flops the launch performs (time it with events on `stream`)."""
+    ws, nb = _ws(workspace)
+    flops = ctypes.c_double(0.0)
+    k = PEAK_KINDS[kind] if isinstance(kind, str) else int(kind)
+    _check(LIB.moe_tensor_peak_probe(k, int(iters_per_cta), int(grid), ctypes.byref(flops), ws, nb, _stream(stream)),
+           "moe_tensor_peak_probe")
+    return flops.value
 
 
 def moe_plan_noalloc(topk_ids, d: MoeDims, counts, offsets, row_src, stream=None):

@@ -146,6 +146,14 @@ def test_host_checks_return_before_launch(moe):
     assert lib.moe_expert_l1(w, ctypes.byref(d), 3, 0, ctypes.c_void_p(4096), 1 << 30, None) == 1  # scale needed
     assert lib.moe_forward(op, None, None, w, w, None, ctypes.byref(d), 9, 0, ctypes.c_void_p(4096), 1 << 30,
                            None) == 1  # unknown mode
+    # the tensor-core peak probe: unknown kind, no iterations, no flops output, bad workspace
+    flops = ctypes.c_double(0.0)
+    ws = ctypes.c_void_p(4096)
+    assert lib.moe_tensor_peak_probe(4, 10, 0, ctypes.byref(flops), ws, 256, None) == 1
+    assert lib.moe_tensor_peak_probe(0, 0, 0, ctypes.byref(flops), ws, 256, None) == 1
+    assert lib.moe_tensor_peak_probe(0, 10, 0, None, ws, 256, None) == 1
+    assert lib.moe_tensor_peak_probe(0, 10, 0, ctypes.byref(flops), ctypes.c_void_p(4096 + 8), 256, None) == 6
+    assert lib.moe_tensor_peak_probe(0, 10, 0, ctypes.byref(flops), ws, 128, None) == 6
 
 
 def test_binding_rejects_host_tensors(moe):
@@ -165,7 +173,7 @@ def test_header_is_a_c_abi(moe, tmp_path):
         pytest.skip("no C compiler")
     src = tmp_path / "abi.c"
     src.write_text(
-        '#include "moe_ffn.h"\n#include <stdio.h>\n'
+        '#include "moe_ffn.h"\n#include "moe_peak.h"\n#include <stdio.h>\n'
         "int main(void) {\n"
         "    moe_dims d = {0};\n"
         "    d.num_tokens = 300; d.hidden = 512; d.intermediate = 384; d.num_experts = 6; d.topk = 2;\n"
