@@ -76,7 +76,7 @@ def resident_input_bytes(wl):
     return w + wl.T * wl.H * X_BYTES_PER_ELEM[wl.mode]
 
 
-def workload_config(wl, quantize_x=False, fused=False):
+def workload_config(wl, quantize_x=False, fused=False, flags=0):
     big = resident_input_bytes(wl) > L2_BYTES
     cfg = {"workload": wl.name, "mode": wl.mode, "tokens": wl.T, "hidden": wl.H, "intermediate": wl.I,
            "experts": wl.E, "topk": wl.K, "routed_rows": wl.routed_rows, "seed": wl.seed,
@@ -86,6 +86,13 @@ def workload_config(wl, quantize_x=False, fused=False):
         cfg["x_input"] = "bf16, quantised by the dispatch stage"
     if fused:
         cfg["gemm_launch"] = "L1, L2 and the combine in one cooperative launch (moe_expert_ffn)"
+    if flags & 128:  # MOE_FLAG_PREPARED_WEIGHTS
+        cfg["weights"] = ("prepared once, untimed, by moe_prepare_weights: every int8 code as its exact f16 value "
+                          "(2 bytes per weight in HBM; MOE_FLAG_PREPARED_WEIGHTS)")
+    elif wl.mode == "a8w8_int8":
+        cfg["weights"] = "int8 in HBM, expanded to f16 in shared memory by the GEMM"
+    if flags & ~128:
+        cfg["flags"] = flags & ~128
     return cfg
 
 
@@ -319,27 +326,36 @@ TENSOR_KIND = {"a16w16": ("bf16", 1), "a8w8_fp8": ("e4m3_e4m3", 1), "a8w8_fp8_e5
 PROBE_ITERS = 20000  # about 5 ms of MMA work per CTA at 1.9 GHz
 
 
-def measure_tensor_peaks(moe, dev, kinds, sustained_s=0.0):
+def measure_tensor_peaks(moe, dev, kinds, sustained_s=0.0, repeats=3):
     """The dense rate of each tcgen05 kind in `kinds`, from the library's probe (one CTA per SM issuing
-    back-to-back MMAs on shared-memory operands), timed with events on the launching stream: one launch
-    after a warm-up launch (burst) and, with sustained_s > 0, back-to-back launches for that long
-    (under the power cap). TFLOP/s, with the SM clock sampled during the probes."""
+    back-to-back MMAs on shared-memory operands), timed with events on the launching stream. Burst: the
+    best of `repeats` single launches per kind, the kinds interleaved (each after a warm-up launch), with
+    the SM clock that CTA 0 measured during the launch (cycles over %globaltimer nanoseconds). With
+    sustained_s > 0 also back-to-back launches for that long (under the power cap). TFLOP/s."""
     import torch
     stream = torch.cuda.current_stream()
     ws = torch.zeros(256, dtype=torch.uint8, device=dev)
-    out = {}
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    out = {k: {"burst_tflops": 0.0} for k in kinds}
     with ClockSampler(dev.index or 0) as clocks:
         clocks.mark_start()
-        for kind in kinds:
-            moe.moe_tensor_peak_probe(kind, PROBE_ITERS // 10, ws, stream=stream)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            flops = moe.moe_tensor_peak_probe(kind, PROBE_ITERS, ws, stream=stream)
-            e1.record(stream)
-            torch.cuda.synchronize()
-            rec = {"burst_tflops": flops / (e0.elapsed_time(e1) * 1e-3) / 1e12}
-            if sustained_s > 0:
+        for _ in range(repeats):
+            for kind in kinds:
+                moe.moe_tensor_peak_probe(kind, PROBE_ITERS // 10, ws, stream=stream)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                flops = moe.moe_tensor_peak_probe(kind, PROBE_ITERS, ws, stream=stream)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                cycles, ns = ws[128:144].view(torch.int64).tolist()  # CTA 0's SM cycles and nanoseconds
+                tflops = flops / (e0.elapsed_time(e1) * 1e-3) / 1e12
+                if tflops > out[kind]["burst_tflops"]:
+                    out[kind] = {"burst_tflops": tflops, "sm_mhz": 1e3 * cycles / max(ns, 1),
+                                 "flops_per_sm_cycle": flops / max(cycles * n_sm, 1)}
+        if sustained_s > 0:
+            for kind in kinds:
                 total, n = 0.0, 0
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
                 t_end = time.time() + sustained_s
                 while time.time() < t_end:
@@ -349,15 +365,15 @@ def measure_tensor_peaks(moe, dev, kinds, sustained_s=0.0):
                         torch.cuda.synchronize()  # keep the queue short so the loop lasts sustained_s
                 e1.record(stream)
                 torch.cuda.synchronize()
-                rec["sustained_tflops"] = total / (e0.elapsed_time(e1) * 1e-3) / 1e12
-            out[kind] = rec
+                out[kind]["sustained_tflops"] = total / (e0.elapsed_time(e1) * 1e-3) / 1e12
         clocks.mark_end()
     st = moe.moe_check_device_error(ws)
     if st != 0:
         raise RuntimeError(f"tensor peak probe: {moe.moe_status_string(st)}")
     out["clocks"] = clocks.summary()
     out["how"] = (f"moe_tensor_peak_probe: one CTA per SM, {PROBE_ITERS} x 4 dense MMAs (M 128, N 256) per CTA on "
-                  "shared-memory operands, CUDA events; burst = one launch after a warm-up launch")
+                  f"shared-memory operands, CUDA events; burst = best of {repeats} launches per kind (interleaved, "
+                  "each after a warm-up launch); sm_mhz = CTA 0's clock64 cycles over %globaltimer ns")
     return out
 
 
@@ -459,6 +475,11 @@ def measure_workload(args, wl, world, local_rank, fused=False, quantize_x=False,
     stream = torch.cuda.current_stream()
     inp = make_inputs(wl, device=dev)
     d = moe.dims(wl.T, wl.H, wl.I, wl.E, wl.K)
+    if flags & moe.MOE_FLAG_PREPARED_WEIGHTS:
+        # one-time weight preparation (exact f16 codes of the int8 weights), before and outside every timed region
+        inp = dict(inp, w1=moe.moe_prepare_weights(inp["w1"], d, wl.mode, 1),
+                   w2=moe.moe_prepare_weights(inp["w2"], d, wl.mode, 2))
+        torch.cuda.synchronize()
     ws = moe.alloc_workspace(d, wl.mode, dev)
     y = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=dev)
     fwd_flags = flags | (moe.MOE_FLAG_QUANTIZE_X if quantize_x else 0) | (moe.MOE_FLAG_FUSED if fused else 0)
@@ -618,7 +639,7 @@ def is_sustained(res):
     return res["elapsed_ms"] >= 1000.0 or "sw_power_cap" in (res["clocks"].get("reasons") or [])
 
 
-def result_fields(args, wl, res, inp, world, pk, pk_src, probe, fused, quantize_x):
+def result_fields(args, wl, res, inp, world, pk, pk_src, probe, fused, quantize_x, flags=0):
     """The per-workload measurements of the JSON line (rank 0)."""
     flops = float(wl.flops)
     ms_per_step = res["elapsed_ms"] / args.steps
@@ -627,7 +648,7 @@ def result_fields(args, wl, res, inp, world, pk, pk_src, probe, fused, quantize_
             else l1_roofline(wl, inp, res["l1_ms"], pk, pk_src, probe, sustained))
     return {
         "value": whole_job_tflops(flops, args.steps, res["elapsed_ms"], world), "unit": "TFLOP/s",
-        "ms_per_step": ms_per_step, "dtype": DTYPE[wl.mode], "config": workload_config(wl, quantize_x, fused),
+        "ms_per_step": ms_per_step, "dtype": DTYPE[wl.mode], "config": workload_config(wl, quantize_x, fused, flags),
         "routed_rows_per_s": world * wl.routed_rows * args.steps / (res["elapsed_ms"] * 1e-3),
         "roofline": roof,
         "step_roofline": step_roofline(wl, inp, ms_per_step, pk, pk_src, probe, sustained),
@@ -645,8 +666,12 @@ def result_fields(args, wl, res, inp, world, pk, pk_src, probe, fused, quantize_
 
 
 # the other configurations of the method's benchmark, measured in the same run (each with the same steps
-# and warm-up), and the oracle's sample length for their cpu_baseline
-OTHER_CONFIGS = ("tiny_bf16", "dsv3_fp8fp4_decode", "dsv3_fp8fp4_prefill_zipf", "int8_a8w8", "int4_a8w4")
+# and warm-up): (workload, GEMM flags, key in the line's "configs"), and the oracle's sample length for
+# their cpu_baseline. A8W8-INT runs on prepared weights (MOE_FLAG_PREPARED_WEIGHTS = 128) and, for
+# comparison, on the int8 weights themselves (no cpu_baseline of its own: the same oracle sample).
+OTHER_CONFIGS = (("tiny_bf16", 0, "tiny_bf16"), ("dsv3_fp8fp4_decode", 0, "dsv3_fp8fp4_decode"),
+                 ("dsv3_fp8fp4_prefill_zipf", 0, "dsv3_fp8fp4_prefill_zipf"), ("int8_a8w8", 128, "int8_a8w8"),
+                 ("int8_a8w8", 0, "int8_a8w8[int8 weights]"), ("int4_a8w4", 0, "int4_a8w4"))
 OTHER_CPU_SECONDS = 4.0
 
 
@@ -657,35 +682,36 @@ def run_gb300(args, wl, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    runs = [(wl, args.fused, args.quantize_x, args.flags)]
+    runs = [(wl, args.fused, args.quantize_x, args.flags, wl.name, True)]
     if args.configs == "all":
         from workloads import WORKLOADS
-        runs += [(WORKLOADS[n], False, False, 0) for n in OTHER_CONFIGS if n != wl.name]
+        runs += [(WORKLOADS[n], False, False, f, key, not key.endswith("]")) for n, f, key in OTHER_CONFIGS
+                 if key != wl.name]
     measured = []
-    for w, fused, qx, flags in runs:
+    for w, fused, qx, flags, key, want_cpu in runs:
         res, inp = measure_workload(args, w, world, local_rank, fused, qx, flags)
         cpu = None
-        if rank == 0 and not args.no_cpu_baseline:
+        if rank == 0 and want_cpu and not args.no_cpu_baseline:
             cpu = cpu_baseline(w, inp, CPU_BASELINE_SECONDS if w is wl else OTHER_CPU_SECONDS, qx)
         ids = inp["topk_ids"].cpu()
-        measured.append((w, fused, qx, res, {"topk_ids": ids}, cpu))
+        measured.append((w, fused, qx, flags, key, res, {"topk_ids": ids}, cpu))
         del inp
         torch.cuda.empty_cache()
     # the peaks of the tensor pipes the measured modes use, after every timed region (so that the probes'
     # heat and power do not touch the measurements)
-    kinds = sorted({TENSOR_KIND[w.mode][0] for w, *_ in measured} | {"bf16"})
-    sustained_s = 2.0 if any(is_sustained(r) for _, _, _, r, _, _ in measured) else 0.0
+    kinds = ["bf16", "f16", "e4m3_e2m1", "e4m3_e4m3"]  # every kind the GEMM stages issue
+    sustained_s = 2.0 if any(is_sustained(m[5]) for m in measured) else 0.0
     probe = measure_tensor_peaks(moe, dev, kinds, sustained_s) if not args.no_probe else None
     if rank != 0:
         return None
     pk, pk_src = peaks()
     lines = []
-    for w, fused, qx, res, inp, cpu in measured:
-        f = result_fields(args, w, res, inp, world, pk, pk_src, probe, fused, qx)
+    for w, fused, qx, flags, key, res, inp, cpu in measured:
+        f = result_fields(args, w, res, inp, world, pk, pk_src, probe, fused, qx, flags)
         if cpu is not None:
             f["cpu_baseline"] = cpu
-        lines.append(f)
-    head = lines[0]
+        lines.append((key, f))
+    head = lines[0][1]
     line = {"metric": METRIC, "value": head["value"], "unit": head["unit"], "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": head["dtype"], "data": "synthetic (seeded; random-init weights)"}
@@ -693,7 +719,7 @@ def run_gb300(args, wl, rank, world, local_rank):
     # gpu_launches counts the library kernels of the headline's timed region; each entry of "configs"
     # counts those of its own timed region
     if len(lines) > 1:
-        line["configs"] = {f["config"]["workload"]: f for f in lines[1:]}
+        line["configs"] = {key: f for key, f in lines[1:]}
     if probe:
         line["tensor_peaks"] = probe
     return line

@@ -141,16 +141,39 @@ enum {
     MOE_FLAG_PAIR_L1 = 32u,     /* A16W16: the L1 GEMM on CTA pairs too (by default it runs on
                                    one-CTA tiles, measured faster at the power cap); same results
                                    bit for bit. Ignored with MOE_FLAG_SINGLE_CTA. */
-    MOE_FLAG_TOKEN_MAJOR = 64u  /* A8W4-INT: token-major tiles (128 pool rows x 256 weight rows)
+    MOE_FLAG_TOKEN_MAJOR = 64u, /* A8W4-INT: token-major tiles (128 pool rows x 256 weight rows)
                                    where weight-major ones (128 weight rows x up to 256 tokens) would
                                    run: experts x weight slabs of at least four rounds of tiles on
                                    the GPU. Same results bit for bit, for comparison. */
+    MOE_FLAG_PREPARED_WEIGHTS = 128u /* A8W8-INT: w1.data and w2.data hold the weights as
+                                   moe_prepare_weights wrote them (every int8 code as the exact f16
+                                   value, same [E,N,K] layout; the fp32 scales unchanged). The
+                                   tensor-core GEMMs then load f16 tiles directly instead of
+                                   expanding int8 tiles in shared memory; same results bit for bit.
+                                   Other modes, or with MOE_FLAG_SIMT: MOE_ERR_UNSUPPORTED. */
 };
 
 /* Bytes of workspace that moe_plan / moe_forward and the stage calls need for `d` and `m`.
  * Returns 0 when `d` is outside the limits above. The caller allocates it (device memory,
  * 256-byte aligned); its contents need no initialisation. */
 MOE_API size_t moe_workspace_bytes(const moe_dims* d, moe_dtype_mode m);
+
+/* One-time weight preparation, outside the timed path (the DeepGEMM page, §3 host preparation,
+ * transforms its weights offline the same way; the Ascend page's A8W8-INT use case fixes the
+ * values: int8 codes with fp32 per-output-channel scales). For MOE_A8W8_INT8 it writes every int8
+ * code of w1 (layer 1, [E,2I,H]) or w2 (layer 2, [E,H,I]) as the exact f16 value of the code, in
+ * the same layout: the operand the INT8 tensor-core GEMMs take with MOE_FLAG_PREPARED_WEIGHTS, which
+ * then need no conversion in shared memory. E counts the shared experts too.
+ *   moe_prepared_weights_bytes  bytes of the prepared tensor (2 per weight); 0 when d is outside
+ *             the limits, layer is not 1 or 2, or the mode has no prepared form (modes other than
+ *             MOE_A8W8_INT8).
+ *   w         device int8 weights of the layer (read-only); out: device buffer of at least that
+ *             many bytes, 16-byte aligned, owned by the caller.
+ * Errors: MOE_ERR_UNSUPPORTED for other modes; MOE_ERR_INVALID_ARG for a bad layer, d, pointer,
+ * size or alignment (nothing launched). Asynchronous on `stream`. */
+MOE_API size_t moe_prepared_weights_bytes(const moe_dims* d, moe_dtype_mode m, int layer);
+MOE_API moe_status moe_prepare_weights(const void* w, const moe_dims* d, moe_dtype_mode m, int layer, void* out,
+                                       size_t out_bytes, moe_stream_t stream);
 
 /* Stage S1, route metadata (Ascend page, A16W16 "EP Dispatch": I_e, N_e = |I_e|, row(i,k);
  * metadata page §1 and §3: count -> prefix sum -> scatter).

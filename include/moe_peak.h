@@ -33,7 +33,10 @@ typedef enum {
  *   flops_out  host pointer: 2 * M * N * K * MMAs, all CTAs (required).
  *   workspace  device memory of at least 256 bytes, 256-byte aligned (its error word records
  *              MOE_ERR_TIMEOUT if the one bounded wait, for the last MMAs, ran out; read it with
- *              moe_check_device_error). Nothing else in it is touched.
+ *              moe_check_device_error). Bytes [128, 144) receive two int64: the SM clock cycles
+ *              and the nanoseconds (%globaltimer) of CTA 0 from its first MMA issue to the
+ *              completion of its last, i.e. the SM clock during the probe. Nothing else in it is
+ *              touched.
  * Asynchronous on `stream`; allocates nothing. */
 MOE_API moe_status moe_tensor_peak_probe(moe_peak_kind kind, int64_t iters_per_cta, int grid, double* flops_out,
                                          void* workspace, size_t workspace_bytes, moe_stream_t stream);

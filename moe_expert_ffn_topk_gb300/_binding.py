@@ -22,12 +22,13 @@ MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_BAD_ROUT
     MOE_ERR_WORKSPACE, MOE_ERR_BAD_SCALE, MOE_ERR_BOUNDS = range(9)
 MODES = {"a16w16": 0, "a8w8_fp8": 1, "a8w8_int8": 2, "a8w4_fp8_fp4": 3, "a8w4_int": 4, "a8w8_fp8_e5m2": 5}
 (MOE_FLAG_NONE, MOE_FLAG_SIMT, MOE_FLAG_WEIGHT_MAJOR, MOE_FLAG_QUANTIZE_X, MOE_FLAG_FUSED, MOE_FLAG_SINGLE_CTA,
- MOE_FLAG_PAIR_L1, MOE_FLAG_TOKEN_MAJOR) = 0, 1, 2, 4, 8, 16, 32, 64
+ MOE_FLAG_PAIR_L1, MOE_FLAG_TOKEN_MAJOR, MOE_FLAG_PREPARED_WEIGHTS) = 0, 1, 2, 4, 8, 16, 32, 64, 128
 
 ABI_FUNCTIONS = ("moe_workspace_bytes", "moe_plan", "moe_dispatch", "moe_expert_l1", "moe_expert_l2",
                  "moe_combine", "moe_forward", "moe_check_device_error", "moe_status_string",
                  "moe_workspace_layout", "moe_debug_bounded_wait", "moe_plan_noalloc", "moe_dispatch_quantize",
-                 "moe_expert_l1_ex", "moe_forward_ex", "moe_expert_ffn", "moe_tensor_peak_probe")
+                 "moe_expert_l1_ex", "moe_forward_ex", "moe_expert_ffn", "moe_tensor_peak_probe",
+                 "moe_prepared_weights_bytes", "moe_prepare_weights")
 # moe_peak_kind (include/moe_peak.h): the tcgen05 instruction kinds the probe measures
 PEAK_KINDS = {"bf16": 0, "f16": 1, "e4m3_e2m1": 2, "e4m3_e4m3": 3}
 
@@ -86,6 +87,8 @@ def _load():
         "moe_forward_ex": (st, [MoeOperand, vp, vp, MoeOperand, MoeOperand, vp, dims_p, st, ctypes.POINTER(MoeOptions),
                                 vp, sz, vp]),
         "moe_tensor_peak_probe": (st, [st, ctypes.c_int64, ctypes.c_int, ctypes.POINTER(ctypes.c_double), vp, sz, vp]),
+        "moe_prepared_weights_bytes": (sz, [dims_p, st, ctypes.c_int]),
+        "moe_prepare_weights": (st, [vp, dims_p, st, ctypes.c_int, vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -246,6 +249,25 @@ def moe_check_device_error(workspace, stream=None) -> int:
 def moe_debug_bounded_wait(workspace, timeout_ns: int, stream=None):
     ws, nb = _ws(workspace)
     _check(LIB.moe_debug_bounded_wait(ws, nb, int(timeout_ns), _stream(stream)), "moe_debug_bounded_wait")
+
+
+def moe_prepared_weights_bytes(d: MoeDims, mode, layer: int) -> int:
+    return LIB.moe_prepared_weights_bytes(ctypes.byref(d), _mode(mode), int(layer))
+
+
+def moe_prepare_weights(w, d: MoeDims, mode, layer: int, out=None, stream=None):
+    """The layer's weights in the prepared form the GEMMs take with MOE_FLAG_PREPARED_WEIGHTS (A8W8-INT:
+    every int8 code as its exact f16 value, same layout); writes `out` (allocated here when None) and
+    returns it."""
+    n = moe_prepared_weights_bytes(d, mode, layer)
+    if out is None:
+        if n == 0:
+            raise MoeError(MOE_ERR_UNSUPPORTED if _mode(mode) != MODES["a8w8_int8"] else MOE_ERR_INVALID_ARG,
+                           "moe_prepare_weights")
+        out = torch.empty(n // 2, dtype=torch.float16, device=w.device)
+    _check(LIB.moe_prepare_weights(_ptr(w, "w"), ctypes.byref(d), _mode(mode), int(layer), _ptr(out, "out"),
+                                   out.numel() * out.element_size(), _stream(stream)), "moe_prepare_weights")
+    return out
 
 
 def moe_tensor_peak_probe(kind, iters_per_cta: int, workspace, grid: int = 0, stream=None) -> float:

@@ -218,6 +218,12 @@ static moe_status expert_l1(moe_operand w1, const moe_dims* d, moe_dtype_mode m,
     if (d->num_tokens == 0) return MOE_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
+    if (flags & MOE_FLAG_PREPARED_WEIGHTS) {  // f16 codes from moe_prepare_weights: the INT8 tensor cores only
+        if (m != MOE_A8W8_INT8 || (flags & MOE_FLAG_SIMT) || !int8_tc_supported(p, 1)) return MOE_ERR_UNSUPPORTED;
+        e = launch_l1_int8_tc(p, w1.data, w1.scale, true, s);
+        if (e == cudaSuccess) e = launch_int8_row_quant(p, s);
+        return from_cuda(e);
+    }
     if ((flags & MOE_FLAG_PAIR_L1) && !(flags & (MOE_FLAG_SIMT | MOE_FLAG_SINGLE_CTA)) && pair_supported(p, 1)) {
         e = launch_l1_pair(p, w1.data, s);
     } else if (!(flags & MOE_FLAG_SIMT) && tc_supported(p, 1)) {
@@ -225,7 +231,7 @@ static moe_status expert_l1(moe_operand w1, const moe_dims* d, moe_dtype_mode m,
     } else if (!(flags & MOE_FLAG_SIMT) && bs_supported(p, 1)) {
         e = launch_l1_bs(p, w1.data, w1.scale, (flags & MOE_FLAG_WEIGHT_MAJOR) != 0, s);
     } else if (!(flags & MOE_FLAG_SIMT) && int8_tc_supported(p, 1)) {
-        e = launch_l1_int8_tc(p, w1.data, w1.scale, s);
+        e = launch_l1_int8_tc(p, w1.data, w1.scale, false, s);
     } else if (!(flags & (MOE_FLAG_SIMT | MOE_FLAG_TOKEN_MAJOR)) && w4_wm_supported(p, 1) &&
                ((flags & MOE_FLAG_WEIGHT_MAJOR) || w4_wm_preferred(p, 1))) {
         e = launch_l1_w4_wm(p, w1.data, w1.scale, s);
@@ -253,6 +259,9 @@ moe_status moe_expert_l2(moe_operand w2, const float* topk_weights, const moe_di
     moe_status st = make_plan_view(d, m, workspace, workspace_bytes, &p, true);
     if (st != MOE_OK) return st;
     if (!operand_ok(w2, m != MOE_A16W16)) return MOE_ERR_INVALID_ARG;
+    const bool prepared = (flags & MOE_FLAG_PREPARED_WEIGHTS) != 0;
+    if (prepared && (m != MOE_A8W8_INT8 || (flags & MOE_FLAG_SIMT) || !int8_tc_supported(p, 2)))
+        return MOE_ERR_UNSUPPORTED;
     if (d->num_tokens == 0) return MOE_OK;
     if (!topk_weights) return MOE_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -267,8 +276,8 @@ moe_status moe_expert_l2(moe_operand w2, const float* topk_weights, const moe_di
         return from_cuda(launch_l2_tc(p, w2.data, w2.scale, topk_weights, s));
     if (!(flags & MOE_FLAG_SIMT) && bs_supported(p, 2))
         return from_cuda(launch_l2_bs(p, w2.data, w2.scale, topk_weights, (flags & MOE_FLAG_WEIGHT_MAJOR) != 0, s));
-    if (!(flags & MOE_FLAG_SIMT) && int8_tc_supported(p, 2))
-        return from_cuda(launch_l2_int8_tc(p, w2.data, w2.scale, topk_weights, s));
+    if (prepared || (!(flags & MOE_FLAG_SIMT) && int8_tc_supported(p, 2)))
+        return from_cuda(launch_l2_int8_tc(p, w2.data, w2.scale, topk_weights, prepared, s));
     if (!(flags & (MOE_FLAG_SIMT | MOE_FLAG_TOKEN_MAJOR)) && w4_wm_supported(p, 2) &&
         ((flags & MOE_FLAG_WEIGHT_MAJOR) || w4_wm_preferred(p, 2)))
         return from_cuda(launch_l2_w4_wm(p, w2.data, w2.scale, topk_weights, s));
@@ -360,6 +369,23 @@ moe_status moe_check_device_error(void* workspace, moe_stream_t stream) {
     const int32_t zero = 0;
     if (cudaMemcpy(workspace, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return MOE_ERR_CUDA;
     return static_cast<moe_status>(err);
+}
+
+size_t moe_prepared_weights_bytes(const moe_dims* d, moe_dtype_mode m, int layer) {
+    if (!dims_ok(d, m) || (layer != 1 && layer != 2) || m != MOE_A8W8_INT8) return 0;
+    const int64_t E = d->num_experts + d->num_shared_experts;
+    return sizeof(uint16_t) * (size_t)(E * (layer == 1 ? 2 * (int64_t)d->intermediate : (int64_t)d->hidden) *
+                                       (layer == 1 ? (int64_t)d->hidden : (int64_t)d->intermediate));
+}
+
+moe_status moe_prepare_weights(const void* w, const moe_dims* d, moe_dtype_mode m, int layer, void* out,
+                               size_t out_bytes, moe_stream_t stream) {
+    if (!dims_ok(d, m) || (layer != 1 && layer != 2)) return MOE_ERR_INVALID_ARG;
+    if (m != MOE_A8W8_INT8) return MOE_ERR_UNSUPPORTED;
+    const size_t need = moe_prepared_weights_bytes(d, m, layer);
+    if (!w || !out || out_bytes < need || (reinterpret_cast<uintptr_t>(w) & 15) || (reinterpret_cast<uintptr_t>(out) & 15))
+        return MOE_ERR_INVALID_ARG;
+    return from_cuda(launch_prepare_int8(w, out, (int64_t)(need / 2), reinterpret_cast<cudaStream_t>(stream)));
 }
 
 const char* moe_status_string(moe_status s) {

@@ -95,9 +95,11 @@ cudaError_t launch_ffn_fused_tc(const Plan& p, const void* w1, const void* w2, c
 
 // Tensor-core path of the integer modes (int8 or int4 weights converted to f16 in shared
 // memory, the tokens' f16 planes; every partial sum an exact integer).
-cudaError_t launch_l1_int8_tc(const Plan& p, const void* w1, const void* w1_scale, cudaStream_t s);
+cudaError_t launch_l1_int8_tc(const Plan& p, const void* w1, const void* w1_scale, bool prepared, cudaStream_t s);
 cudaError_t launch_l2_int8_tc(const Plan& p, const void* w2, const void* w2_scale, const float* topk_weights,
-                              cudaStream_t s);
+                              bool prepared, cudaStream_t s);
+// int8 codes [n] -> the same values as f16 [n] (n a multiple of 16)
+cudaError_t launch_prepare_int8(const void* w, void* out, int64_t n, cudaStream_t s);
 bool int8_tc_supported(const Plan& p, int stage);
 
 // Token-major tensor-core path of A8W4-INT (int4 weights expanded to f16 in shared memory).

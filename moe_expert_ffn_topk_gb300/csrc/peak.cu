@@ -24,6 +24,7 @@ constexpr int kABytes = kM * 128, kBBytes = kN * 128;  // one 128-byte swizzle r
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCol = 256;  // scale-factor columns after the 256 accumulator columns
 constexpr size_t kSmem = 1024 + kABytes + kBBytes + 64;
+constexpr int kProbeRecordOffset = 128;  // workspace bytes [128, 144): CTA 0's cycles and nanoseconds
 
 __device__ __forceinline__ uint32_t mix32(uint32_t x) {
     x ^= x >> 16;
@@ -121,6 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1) tensor_peak_kernel(int64_t iters,
     tc_fence_after();
 
     if (warp == 0 && lane == 0) {
+        const uint64_t c0 = clock64(), t0 = globaltimer_ns();
         const uint32_t a = smem_u32(tiles);
         const uint64_t ad = kmajor_desc(a, 0), bd = kmajor_desc(a + kABytes, 0);
         uint32_t idesc[4];
@@ -138,6 +140,11 @@ __global__ void __launch_bounds__(kThreads, 1) tensor_peak_kernel(int64_t iters,
         }
         tc_commit(smem_u32(bar));
         mbar_drain(smem_u32(bar), 0, hdr);  // bounded; the MMAs in flight take microseconds
+        if (blockIdx.x == 0) {  // SM clock cycles and nanoseconds of CTA 0's MMA stream
+            int64_t* rec = reinterpret_cast<int64_t*>(hdr + kProbeRecordOffset / 4);
+            rec[0] = (int64_t)(clock64() - c0);
+            rec[1] = (int64_t)(globaltimer_ns() - t0);
+        }
     }
     tc_fence_before();
     __syncthreads();

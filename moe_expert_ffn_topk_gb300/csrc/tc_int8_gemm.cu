@@ -44,22 +44,30 @@ constexpr int kTok = 128;       // tokens per tile (one route tile)
 constexpr int kBK = 64;         // K per stage: 64 f16 = one 128-byte swizzle row
 constexpr int kThreads = 352;
 constexpr int kMaxExperts = 1024;
-constexpr int kRawStages = 3, kHfStages = 2, kTokStages = 3;
 constexpr int kABytes = 2 * kWR * 128;   // two f16 weight blocks
 constexpr int kTokBytes = 2 * kTok * 128;  // hi rows, then lo rows
 constexpr int kRawBytes = 2 * kWR * kBK;   // two int8 weight blocks
-constexpr int kHfOff = 0;
-constexpr int kTokOff = kHfOff + kHfStages * kABytes;
-constexpr int kRawOff = kTokOff + kTokStages * kTokBytes;
-constexpr int kBarOff = kRawOff + kRawStages * kRawBytes;
-constexpr int kNumBars = 2 * (kRawStages + kHfStages + kTokStages) + 2 + 1;
-constexpr int kMiscOff = kBarOff + 8 * kNumBars;
-constexpr int kTileOffOff = kMiscOff + 16;
-constexpr int kCountsOff = kTileOffOff + 4 * (kMaxExperts + 1);
-constexpr int kTabOff = kCountsOff + 4 * kMaxExperts;  // L2 epilogue: per warp [slot, gate, s^A] x 128 rows
 constexpr int kTokBox = 16;  // token rows per TMA box of a partial tile
-constexpr size_t kSmem = 1024 + (size_t)kTabOff + 4 * 3 * 4 * kTok;
-static_assert(kSmem <= 232448, "shared memory");
+
+// Shared-memory layout. Int8 weights: TMA fills a ring of raw int8 tiles that the converter warps
+// expand into a ring of f16 tiles. Prepared weights (exact f16 codes written once by
+// moe_prepare_weights): TMA fills the f16 ring directly, which takes the raw ring's space as a
+// third stage, and the converter warps stay idle.
+template <bool kPrep>
+struct Layout {
+    static constexpr int kRawStages = kPrep ? 0 : 3, kHfStages = kPrep ? 3 : 2, kTokStages = 3;
+    static constexpr int kHfOff = 0;
+    static constexpr int kTokOff = kHfOff + kHfStages * kABytes;
+    static constexpr int kRawOff = kTokOff + kTokStages * kTokBytes;
+    static constexpr int kBarOff = kRawOff + kRawStages * kRawBytes;
+    static constexpr int kNumBars = 2 * (kRawStages + kHfStages + kTokStages) + 2 + 1;
+    static constexpr int kMiscOff = kBarOff + 8 * kNumBars;
+    static constexpr int kTileOffOff = kMiscOff + 16;
+    static constexpr int kCountsOff = kTileOffOff + 4 * (kMaxExperts + 1);
+    static constexpr int kTabOff = kCountsOff + 4 * kMaxExperts;  // L2 epilogue: per warp [slot, gate, s^A] x 128 rows
+    static constexpr size_t kSmem = 1024 + (size_t)kTabOff + 4 * 3 * 4 * kTok;
+    static_assert(kSmem <= 232448, "shared memory");
+};
 // largest K with every partial sum below 2^24: |lo * w| <= 15 * 128
 constexpr int kMaxK = 8704;
 
@@ -144,10 +152,15 @@ __device__ __forceinline__ int exact_int(uint32_t hi_bits, uint32_t lo_bits) {
     return 16 * __float2int_rn(__uint_as_float(hi_bits)) + __float2int_rn(__uint_as_float(lo_bits));
 }
 
-template <bool kL1>
+template <bool kL1, bool kPrep>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_int8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const __grid_constant__ CUtensorMap tmX16, I8Args args) {
+    using L = Layout<kPrep>;
+    constexpr int kRawStages = L::kRawStages, kHfStages = L::kHfStages, kTokStages = L::kTokStages;
+    constexpr int kHfOff = L::kHfOff, kTokOff = L::kTokOff, kRawOff = L::kRawOff, kBarOff = L::kBarOff;
+    constexpr int kMiscOff = L::kMiscOff, kTileOffOff = L::kTileOffOff, kCountsOff = L::kCountsOff;
+    constexpr int kTabOff = L::kTabOff;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = smem_u32(smem_raw);
     const uint32_t base = (raw_base + 1023u) & ~1023u;
@@ -178,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(raw_empty(i), 128);
         }
         for (int i = 0; i < kHfStages; ++i) {
-            mbar_init(hf_full(i), 128);  // the 128 converter threads
+            mbar_init(hf_full(i), kPrep ? 1 : 128);  // the weight TMA (arrive + bytes), or the 128 converter threads
             mbar_init(hf_empty(i), 1);
         }
         for (int i = 0; i < kTokStages; ++i) {
@@ -206,8 +219,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     if (warp == 0) {
-        // ---------------- raw weight TMA ----------------
-        if (lane == 0) {
+        if constexpr (kPrep) {
+            if (lane == 0) {
+                // ---------------- f16 weight TMA straight into the MMA's ring ----------------
+                int it = 0;
+                bool ok = true;
+                for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                    const Tile tl = decode(t, tile_off, p.E, args.n_slabs);
+                    const int w0 = wrow(tl, 0), w1 = wrow(tl, 1);
+                    for (int kb = 0; kb < KB; ++kb, ++it) {
+                        const int b = it % kHfStages;
+                        if (!mbar_wait(hf_empty(b), ((uint32_t)(it / kHfStages) & 1u) ^ 1u, p.hdr, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t dst = base + kHfOff + b * kABytes;
+                        mbar_arrive_expect_tx(hf_full(b), kABytes);
+                        tma_load_2d(dst, &tmW, kb * kBK, w0, hf_full(b));
+                        tma_load_2d(dst + kWR * 128, &tmW, kb * kBK, w1, hf_full(b));
+                    }
+                }
+                for (int j = it - kHfStages < 0 ? 0 : it - kHfStages; j < it; ++j)
+                    mbar_drain(hf_full(j % kHfStages), (uint32_t)(j / kHfStages) & 1u, p.hdr);
+            }
+        } else if (lane == 0) {
+            // ---------------- raw weight TMA ----------------
             int it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
@@ -302,32 +338,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_drain(drain_bar, 0, p.hdr);
         }
     } else if (warp >= 6) {
-        // ---------------- weight converters ----------------
-        const int c = threadIdx.x - 192;  // row of each 128-row weight block
-        int it = 0;
-        bool ok = true;
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            for (int kb = 0; kb < KB; ++kb, ++it) {
-                const int r = it % kRawStages, b = it % kHfStages;
-                bool w_ok = mbar_wait(raw_full(r), (uint32_t)(it / kRawStages) & 1u, p.hdr, abort_flag);
-                w_ok = w_ok && mbar_wait(hf_empty(b), ((uint32_t)(it / kHfStages) & 1u) ^ 1u, p.hdr, abort_flag);
-                if (!__all_sync(0xffffffffu, w_ok)) {
-                    ok = false;
-                    break;
+        if constexpr (!kPrep) {
+            // ---------------- weight converters ----------------
+            const int c = threadIdx.x - 192;  // row of each 128-row weight block
+            int it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const int r = it % kRawStages, b = it % kHfStages;
+                    bool w_ok = mbar_wait(raw_full(r), (uint32_t)(it / kRawStages) & 1u, p.hdr, abort_flag);
+                    w_ok = w_ok && mbar_wait(hf_empty(b), ((uint32_t)(it / kHfStages) & 1u) ^ 1u, p.hdr, abort_flag);
+                    if (!__all_sync(0xffffffffu, w_ok)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint8_t* rw = smem + kRawOff + r * kRawBytes;
+                    uint8_t* dst = smem + kHfOff + b * kABytes;
+                    uint4 r0[4], r1[4];
+                    load_row(rw, c, r0);
+                    load_row(rw + kWR * kBK, c, r1);
+                    store_row(r0, dst, c);
+                    store_row(r1, dst + kWR * 128, c);
+                    fence_proxy_async_smem();
+                    mbar_arrive(raw_empty(r));
+                    mbar_arrive(hf_full(b));
                 }
-                const uint8_t* rw = smem + kRawOff + r * kRawBytes;
-                uint8_t* dst = smem + kHfOff + b * kABytes;
-                uint4 r0[4], r1[4];
-                load_row(rw, c, r0);
-                load_row(rw + kWR * kBK, c, r1);
-                store_row(r0, dst, c);
-                store_row(r1, dst + kWR * 128, c);
-                fence_proxy_async_smem();
-                mbar_arrive(raw_empty(r));
-                mbar_arrive(hf_full(b));
             }
         }
-    } else {
+    } else if (warp >= 2 && warp < 6) {
         // ---------------- epilogue (warps 2..5) ----------------
         // The per-row values (token scales, L2 slots and gate weights) and the per-channel weight
         // scales are read before the accumulator wait, while the tile's MMAs still run: the
@@ -437,20 +475,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_dealloc(tmem_base, 512);
 }
 
-template <bool kL1>
+template <bool kL1, bool kPrep>
 cudaError_t launch_int8(const Plan& p, const void* w, const void* w_scale, const float* topk_weights, cudaStream_t s) {
+    using L = Layout<kPrep>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(tc_int8_kernel<kL1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+        attr_err = cudaFuncSetAttribute(tc_int8_kernel<kL1, kPrep>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)L::kSmem);
     });
     if (attr_err != cudaSuccess) return attr_err;
     const int n_out = kL1 ? 2 * p.I : p.H;
     const int kin = kL1 ? p.H : p.I;
     CUtensorMap tmW, tmX, tmX16;
-    if (!tc_make_map_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w, (uint64_t)kin, (uint64_t)p.E * n_out, kBK, kWR,
-                        CU_TENSOR_MAP_SWIZZLE_64B))
-        return cudaErrorInvalidValue;
+    const bool w_ok = kPrep ? tc_make_map_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w, (uint64_t)kin,
+                                             (uint64_t)p.E * n_out, kBK, kWR, CU_TENSOR_MAP_SWIZZLE_128B)
+                            : tc_make_map_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w, (uint64_t)kin,
+                                             (uint64_t)p.E * n_out, kBK, kWR, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (!w_ok) return cudaErrorInvalidValue;
     if (!tc_make_map_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, kL1 ? (const void*)p.x_planes : (const void*)p.a_planes,
                         (uint64_t)kin, 2 * (uint64_t)p.pool_rows, kBK, kTok, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !tc_make_map_2d(&tmX16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
@@ -461,8 +503,23 @@ cudaError_t launch_int8(const Plan& p, const void* w, const void* w_scale, const
                 n_out};
     const int64_t max_tiles = (p.pool_rows / kTok) * args.n_slabs;
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(max_tiles, tc_num_sms()));
-    tc_int8_kernel<kL1><<<grid, kThreads, kSmem, s>>>(tmW, tmX, tmX16, args);
+    tc_int8_kernel<kL1, kPrep><<<grid, kThreads, L::kSmem, s>>>(tmW, tmX, tmX16, args);
     return cudaGetLastError();
+}
+
+// One-time preparation of int8 weights for the f16 tensor-core GEMM: every code q becomes the f16
+// value q (exact), 16 codes per thread and step.
+__global__ void prepare_int8_kernel(const uint4* __restrict__ w, uint4* __restrict__ out, int64_t n16) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n16; i += (int64_t)gridDim.x * blockDim.x) {
+        const uint4 c = __ldg(w + i);
+        uint32_t o[8];
+        int8x4_to_f16(c.x, o[0], o[1]);
+        int8x4_to_f16(c.y, o[2], o[3]);
+        int8x4_to_f16(c.z, o[4], o[5]);
+        int8x4_to_f16(c.w, o[6], o[7]);
+        out[2 * i] = make_uint4(o[0], o[1], o[2], o[3]);
+        out[2 * i + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
 }
 
 }  // namespace
@@ -473,13 +530,23 @@ bool int8_tc_supported(const Plan& p, int stage) {
     return p.H % (2 * kWR) == 0 && p.I % kBK == 0 && p.I <= kMaxK;
 }
 
-cudaError_t launch_l1_int8_tc(const Plan& p, const void* w1, const void* w1_scale, cudaStream_t s) {
-    return launch_int8<true>(p, w1, w1_scale, nullptr, s);
+cudaError_t launch_l1_int8_tc(const Plan& p, const void* w1, const void* w1_scale, bool prepared, cudaStream_t s) {
+    return prepared ? launch_int8<true, true>(p, w1, w1_scale, nullptr, s)
+                    : launch_int8<true, false>(p, w1, w1_scale, nullptr, s);
 }
 
 cudaError_t launch_l2_int8_tc(const Plan& p, const void* w2, const void* w2_scale, const float* topk_weights,
-                              cudaStream_t s) {
-    return launch_int8<false>(p, w2, w2_scale, topk_weights, s);
+                              bool prepared, cudaStream_t s) {
+    return prepared ? launch_int8<false, true>(p, w2, w2_scale, topk_weights, s)
+                    : launch_int8<false, false>(p, w2, w2_scale, topk_weights, s);
+}
+
+cudaError_t launch_prepare_int8(const void* w, void* out, int64_t n, cudaStream_t s) {
+    if (n <= 0) return cudaSuccess;
+    const int64_t n16 = n / 16;  // the caller guarantees n % 16 == 0 (K is a multiple of 128)
+    const int grid = (int)std::min<int64_t>((n16 + 255) / 256, (int64_t)tc_num_sms() * 8);
+    prepare_int8_kernel<<<grid, 256, 0, s>>>(static_cast<const uint4*>(w), static_cast<uint4*>(out), n16);
+    return cudaGetLastError();
 }
 
 }  // namespace moe

@@ -146,6 +146,20 @@ def test_host_checks_return_before_launch(moe):
     assert lib.moe_expert_l1(w, ctypes.byref(d), 3, 0, ctypes.c_void_p(4096), 1 << 30, None) == 1  # scale needed
     assert lib.moe_forward(op, None, None, w, w, None, ctypes.byref(d), 9, 0, ctypes.c_void_p(4096), 1 << 30,
                            None) == 1  # unknown mode
+    # weight preparation: modes without a prepared form, bad layer, missing pointers, short output
+    d8 = moe.dims(64, 256, 128, 8, 2)
+    assert moe.moe_prepared_weights_bytes(d8, "a8w8_int8", 1) == 2 * 8 * 256 * 256
+    assert moe.moe_prepared_weights_bytes(d8, "a8w8_int8", 2) == 2 * 8 * 256 * 128
+    assert moe.moe_prepared_weights_bytes(moe.dims(64, 256, 128, 8, 2, 1), "a8w8_int8", 2) == 2 * 9 * 256 * 128
+    for mode in ("a16w16", "a8w8_fp8", "a8w4_fp8_fp4", "a8w4_int", "a8w8_fp8_e5m2"):
+        assert moe.moe_prepared_weights_bytes(d8, mode, 1) == 0
+        assert lib.moe_prepare_weights(ctypes.c_void_p(4096), ctypes.byref(d8), moe.MODES[mode], 1,
+                                       ctypes.c_void_p(8192), 1 << 30, None) == 2
+    assert moe.moe_prepared_weights_bytes(d8, "a8w8_int8", 3) == 0
+    assert lib.moe_prepare_weights(ctypes.c_void_p(4096), ctypes.byref(d8), 2, 3, ctypes.c_void_p(8192), 1 << 30, None) == 1
+    assert lib.moe_prepare_weights(None, ctypes.byref(d8), 2, 1, ctypes.c_void_p(8192), 1 << 30, None) == 1
+    assert lib.moe_prepare_weights(ctypes.c_void_p(4096), ctypes.byref(d8), 2, 1, ctypes.c_void_p(8192), 1024, None) == 1
+    assert lib.moe_prepare_weights(ctypes.c_void_p(4096), ctypes.byref(d8), 2, 1, ctypes.c_void_p(8200), 1 << 30, None) == 1
     # the tensor-core peak probe: unknown kind, no iterations, no flops output, bad workspace
     flops = ctypes.c_double(0.0)
     ws = ctypes.c_void_p(4096)

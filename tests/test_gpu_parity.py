@@ -317,11 +317,12 @@ def test_tensor_core_stages_match_reference_kernels(moe, wl):
     assert np.abs(c[0] - c[1]).max() <= 2e-2 * np.abs(c[1]).max()
 
 
-def test_int8_l1_accumulators_exact_on_adversarial_codes(moe):
+@pytest.mark.parametrize("prepared", [False, True], ids=["int8_weights", "prepared_weights"])
+def test_int8_l1_accumulators_exact_on_adversarial_codes(moe, prepared):
     """Every x and W1 code is +-127 and K = 5120, so the int32 accumulators reach 5120*127^2
     = 82,580,480 > 2^24: a plain fp32 accumulation would round, the exact integer GEMM must
     not. With unit scales H = C exactly and SiLU(H) is H or 0, so the fp32 A of the kernel must
-    equal the oracle's bit for bit."""
+    equal the oracle's bit for bit (int8 weights, or the f16 codes of moe_prepare_weights)."""
     wl = Workload("adv_int8", "a8w8_int8", 96, 5120, 256, 2, 1, 51, 0.05)
     inp = make_inputs(wl, device=DEV)
     g = torch.Generator(device=DEV).manual_seed(5)
@@ -334,7 +335,7 @@ def test_int8_l1_accumulators_exact_on_adversarial_codes(moe):
     inp["w1"][0, wl.I:wl.I + 3] = 127
     inp["w1_scale"] = torch.ones_like(inp["w1_scale"])
     inp["topk_ids"][:3] = 0
-    out = run_forward(moe, wl, inp, stages=True)
+    out = (run_prepared(moe, wl, inp) if prepared else run_forward(moe, wl, inp, stages=True))
     assert out["status"] == 0
     L = out["layout"]
     rows = L["pool_rows"]
@@ -354,6 +355,55 @@ def test_int8_l1_accumulators_exact_on_adversarial_codes(moe):
         pos = h[:, :wl.I] > 0
         assert np.array_equal(got[pos], a_ref[pos]), f"expert {e}: {np.abs(got - a_ref)[pos].max()}"
         assert np.abs(got[~pos]).max(initial=0) < 1e-20 and np.abs(a_ref[~pos]).max(initial=0) < 1e-20
+
+
+def run_prepared(moe, wl, inp, **kw):
+    """run_forward with the A8W8-INT weights prepared once as exact f16 codes (moe_prepare_weights)
+    and MOE_FLAG_PREPARED_WEIGHTS."""
+    d = moe.dims(wl.T, wl.H, wl.I, wl.E, wl.K)
+    w1p = moe.moe_prepare_weights(inp["w1"], d, wl.mode, 1)
+    w2p = moe.moe_prepare_weights(inp["w2"], d, wl.mode, 2)
+    assert torch.equal(w1p.float(), inp["w1"].float()) and torch.equal(w2p.float(), inp["w2"].float())
+    return run_forward(moe, wl, dict(inp, w1=w1p, w2=w2p), flags=moe.MOE_FLAG_PREPARED_WEIGHTS, stages=True, **kw)
+
+
+@pytest.mark.parametrize("case", ["tiny", "ragged", "tail_sizes", "full_size"])
+def test_int8_prepared_weights_equal_int8_weights(moe, case):
+    """The INT8 GEMMs on weights prepared once as exact f16 codes give the same combine rows and y,
+    bit for bit, as on the int8 weights (both accumulate the exact integer products); the tail case
+    puts experts at the 16-token and 128-row edges of the tiles."""
+    if case == "tail_sizes":
+        wl, inp = _tail_inputs("a8w8_int8", 48)
+    else:
+        wl = {"tiny": CASES["a8w8_int8"][0], "ragged": CASES["a8w8_int8"][1], "full_size": WORKLOADS["int8_a8w8"]}[case]
+        inp = make_inputs(wl, device=DEV)
+    a = run_forward(moe, wl, inp, stages=True)
+    b = run_prepared(moe, wl, inp)
+    assert a["status"] == 0 and b["status"] == 0
+    L = a["layout"]
+    ca = region(a["ws"], L, "comb", torch.int16, wl.T * wl.K * wl.H)
+    cb = region(b["ws"], L, "comb", torch.int16, wl.T * wl.K * wl.H)
+    assert torch.equal(ca, cb)
+    assert torch.equal(a["y"].view(torch.int16), b["y"].view(torch.int16))
+    if case != "full_size":
+        assert_close(y_numpy(b["y"]), oracle_forward(wl, inp), wl.mode)
+
+
+def test_prepared_weights_rejections(moe):
+    wl = CASES["a16w16"][0]
+    inp = make_inputs(wl, device=DEV)
+    d = moe.dims(wl.T, wl.H, wl.I, wl.E, wl.K)
+    with pytest.raises(moe.MoeError) as err:
+        moe.moe_prepare_weights(inp["w1"], d, wl.mode, 1)
+    assert err.value.status == moe.MOE_ERR_UNSUPPORTED
+    with pytest.raises(moe.MoeError) as err:  # the flag belongs to the A8W8-INT GEMMs only
+        run_forward(moe, wl, inp, flags=moe.MOE_FLAG_PREPARED_WEIGHTS)
+    assert err.value.status == moe.MOE_ERR_UNSUPPORTED
+    wl8 = CASES["a8w8_int8"][0]
+    inp8 = make_inputs(wl8, device=DEV)
+    with pytest.raises(moe.MoeError) as err:  # no CUDA-core kernel takes prepared weights
+        run_forward(moe, wl8, inp8, flags=moe.MOE_FLAG_PREPARED_WEIGHTS | moe.MOE_FLAG_SIMT)
+    assert err.value.status == moe.MOE_ERR_UNSUPPORTED
 
 
 def test_int4_l1_accumulators_exact_at_the_largest_k(moe):
@@ -377,7 +427,7 @@ def test_int4_l1_accumulators_exact_at_the_largest_k(moe):
     inp["w1"] = (nib[..., 0::2] | (nib[..., 1::2] << 4)).contiguous()
     inp["w1_scale"] = torch.ones_like(inp["w1_scale"])
     inp["topk_ids"][:3] = 0
-    out = run_forward(moe, wl, inp, stages=True)
+    out = (run_prepared(moe, wl, inp) if prepared else run_forward(moe, wl, inp, stages=True))
     assert out["status"] == 0
     L = out["layout"]
     rows = L["pool_rows"]
