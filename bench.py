@@ -475,10 +475,11 @@ def measure_workload(args, wl, world, local_rank, fused=False, quantize_x=False,
     stream = torch.cuda.current_stream()
     inp = make_inputs(wl, device=dev)
     d = moe.dims(wl.T, wl.H, wl.I, wl.E, wl.K)
+    w1, w2 = inp["w1"], inp["w2"]  # the GEMMs' weight operands (inp keeps the stored codes for the oracle)
     if flags & moe.MOE_FLAG_PREPARED_WEIGHTS:
         # one-time weight preparation (exact f16 codes of the int8 weights), before and outside every timed region
-        inp = dict(inp, w1=moe.moe_prepare_weights(inp["w1"], d, wl.mode, 1),
-                   w2=moe.moe_prepare_weights(inp["w2"], d, wl.mode, 2))
+        w1 = moe.moe_prepare_weights(inp["w1"], d, wl.mode, 1)
+        w2 = moe.moe_prepare_weights(inp["w2"], d, wl.mode, 2)
         torch.cuda.synchronize()
     ws = moe.alloc_workspace(d, wl.mode, dev)
     y = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=dev)
@@ -493,15 +494,15 @@ def measure_workload(args, wl, world, local_rank, fused=False, quantize_x=False,
         if ev_l1:
             ev_l1[0].record(stream)
         if fused:  # the events bracket the one launch of S3-S6
-            moe.moe_expert_ffn(inp["w1"], inp["w1_scale"], inp["w2"], inp["w2_scale"], inp["topk_weights"], d, wl.mode,
+            moe.moe_expert_ffn(w1, inp["w1_scale"], w2, inp["w2_scale"], inp["topk_weights"], d, wl.mode,
                                ws, y=y, stream=stream)
             if ev_l1:
                 ev_l1[1].record(stream)
             return
-        moe.moe_expert_l1(inp["w1"], inp["w1_scale"], d, wl.mode, ws, flags, stream=stream)
+        moe.moe_expert_l1(w1, inp["w1_scale"], d, wl.mode, ws, flags, stream=stream)
         if ev_l1:
             ev_l1[1].record(stream)
-        moe.moe_expert_l2(inp["w2"], inp["w2_scale"], inp["topk_weights"], d, wl.mode, ws, flags, stream=stream)
+        moe.moe_expert_l2(w2, inp["w2_scale"], inp["topk_weights"], d, wl.mode, ws, flags, stream=stream)
         moe.moe_combine(y, d, ws, stream=stream)
 
     def barrier():
@@ -546,7 +547,7 @@ def measure_workload(args, wl, world, local_rank, fused=False, quantize_x=False,
 
     def forward(di, yd):
         moe.moe_forward(di["x_bf16"] if quantize_x else di["x"], di.get("x_scale"), di["topk_ids"], di["topk_weights"],
-                        inp["w1"], inp["w1_scale"], inp["w2"], inp["w2_scale"], yd, d, wl.mode, ws, fwd_flags,
+                        w1, inp["w1_scale"], w2, inp["w2_scale"], yd, d, wl.mode, ws, fwd_flags,
                         stream=stream)
 
     # (a) overlapped: the input and the output copies run on two more streams with double-buffered
@@ -612,7 +613,7 @@ def measure_workload(args, wl, world, local_rank, fused=False, quantize_x=False,
         raise RuntimeError(f"{wl.name}: device error in the end-to-end runs: {moe.moe_status_string(st)}")
     res = {"elapsed_ms": elapsed_ms, "l1_ms": l1_ms, "e2e_ms": e2e_ms, "serial_ms": serial_ms, "h2d": h2d,
            "d2h": d2h, "clocks": clocks.summary()}
-    del ws, y, y_dev, dev_in
+    del ws, y, y_dev, dev_in, w1, w2
     return res, inp
 
 
@@ -687,12 +688,19 @@ def run_gb300(args, wl, rank, world, local_rank):
         from workloads import WORKLOADS
         runs += [(WORKLOADS[n], False, False, f, key, not key.endswith("]")) for n, f, key in OTHER_CONFIGS
                  if key != wl.name]
-    measured = []
-    for w, fused, qx, flags, key, want_cpu in runs:
-        res, inp = measure_workload(args, w, world, local_rank, fused, qx, flags)
-        cpu = None
-        if rank == 0 and want_cpu and not args.no_cpu_baseline:
-            cpu = cpu_baseline(w, inp, CPU_BASELINE_SECONDS if w is wl else OTHER_CPU_SECONDS, qx)
+    measured, failed = [], {}
+    for i, (w, fused, qx, flags, key, want_cpu) in enumerate(runs):
+        try:
+            res, inp = measure_workload(args, w, world, local_rank, fused, qx, flags)
+            cpu = None
+            if rank == 0 and want_cpu and not args.no_cpu_baseline:
+                cpu = cpu_baseline(w, inp, CPU_BASELINE_SECONDS if w is wl else OTHER_CPU_SECONDS, qx)
+        except Exception as exc:  # an extra configuration that fails is reported, not fatal
+            if i == 0:
+                raise
+            failed[key] = {"error": f"{type(exc).__name__}: {exc}"[:500]}
+            torch.cuda.synchronize()
+            continue
         ids = inp["topk_ids"].cpu()
         measured.append((w, fused, qx, flags, key, res, {"topk_ids": ids}, cpu))
         del inp
@@ -718,8 +726,9 @@ def run_gb300(args, wl, rank, world, local_rank):
     line.update({k: v for k, v in head.items() if k not in line})
     # gpu_launches counts the library kernels of the headline's timed region; each entry of "configs"
     # counts those of its own timed region
-    if len(lines) > 1:
+    if len(lines) > 1 or failed:
         line["configs"] = {key: f for key, f in lines[1:]}
+        line["configs"].update(failed)
     if probe:
         line["tensor_peaks"] = probe
     return line

@@ -264,7 +264,7 @@ def moe_prepare_weights(w, d: MoeDims, mode, layer: int, out=None, stream=None):
         if n == 0:
             raise MoeError(MOE_ERR_UNSUPPORTED if _mode(mode) != MODES["a8w8_int8"] else MOE_ERR_INVALID_ARG,
                            "moe_prepare_weights")
-        out = torch.empty(n // 2, dtype=torch.float16, device=w.device)
+        out = torch.empty(w.shape, dtype=torch.float16, device=w.device)  # the same layout as the int8 codes
     _check(LIB.moe_prepare_weights(_ptr(w, "w"), ctypes.byref(d), _mode(mode), int(layer), _ptr(out, "out"),
                                    out.numel() * out.element_size(), _stream(stream)), "moe_prepare_weights")
     return out
