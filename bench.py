@@ -668,11 +668,11 @@ def result_fields(args, wl, res, inp, world, pk, pk_src, probe, fused, quantize_
 
 # the other configurations of the method's benchmark, measured in the same run (each with the same steps
 # and warm-up): (workload, GEMM flags, key in the line's "configs"), and the oracle's sample length for
-# their cpu_baseline. A8W8-INT runs on prepared weights (MOE_FLAG_PREPARED_WEIGHTS = 128) and, for
-# comparison, on the int8 weights themselves (no cpu_baseline of its own: the same oracle sample).
+# their cpu_baseline. A8W8-INT runs on its int8 weights and, for comparison, on weights prepared once as
+# exact f16 codes (MOE_FLAG_PREPARED_WEIGHTS = 128; no cpu_baseline of its own: the same oracle sample).
 OTHER_CONFIGS = (("tiny_bf16", 0, "tiny_bf16"), ("dsv3_fp8fp4_decode", 0, "dsv3_fp8fp4_decode"),
-                 ("dsv3_fp8fp4_prefill_zipf", 0, "dsv3_fp8fp4_prefill_zipf"), ("int8_a8w8", 128, "int8_a8w8"),
-                 ("int8_a8w8", 0, "int8_a8w8[int8 weights]"), ("int4_a8w4", 0, "int4_a8w4"))
+                 ("dsv3_fp8fp4_prefill_zipf", 0, "dsv3_fp8fp4_prefill_zipf"), ("int8_a8w8", 0, "int8_a8w8"),
+                 ("int8_a8w8", 128, "int8_a8w8[prepared f16 weights]"), ("int4_a8w4", 0, "int4_a8w4"))
 OTHER_CPU_SECONDS = 4.0
 
 

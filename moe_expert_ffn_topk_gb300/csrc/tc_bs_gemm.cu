@@ -29,14 +29,9 @@
 // scale of B row n is in lane 32*q + n%32 of every lane quarter q, column base + n/32, byte =
 // b_sf_id; one 32-bit word holds a row's 4 scales of a stage.
 //
-// Warp roles (352 threads): 0 TMA producer, 1 TMEM allocation + MMA issuer, 2-5 epilogue,
-// 6-9 scale writers, 10 the second MMA issuer of two-atom stages. At decode sizes one issuing
-// thread sets the pace (per stage: a barrier wait, one tcgen05.mma per 32 K, a commit, the loop;
-// about 900 cycles per 16 KB of e2m1 weights against ~64 cycles of tensor work), so two threads
-// on different schedulers share each stage: thread 1 issues its first K atom into one
-// accumulator, thread 10 its second atom into another, both commit to the stage's empty barrier
-// (two arrivals), and the epilogue adds the two fp32 partial sums. Every wait is bounded; on
-// time-out the CTA records MOE_ERR_TIMEOUT, drains and exits.
+// Warp roles (320 threads): 0 TMA producer, 1 TMEM allocation + MMA issuer, 2-5 epilogue,
+// 6-9 scale writers. Every wait is bounded; on time-out the CTA records MOE_ERR_TIMEOUT, drains
+// and exits.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -55,7 +50,7 @@ using namespace tc;
 constexpr int kWR = 128;          // weight rows per tile (MMA M)
 constexpr int kHalf = 64;         // L1: gate rows, then up rows
 constexpr int kAtomK = 128;       // K of one 128-byte swizzle atom (a stage holds kAtoms of them)
-constexpr int kThreads = 352;
+constexpr int kThreads = 320;
 constexpr int kMaxExperts = 1024;
 constexpr int kABytes = kWR * 128;
 constexpr int kSfCol0 = 256;      // first TMEM column of the scale ring
@@ -67,7 +62,7 @@ struct BsCfg {
     static constexpr int kBBytes = kNT * 128;                          // one K atom of tokens
     static constexpr int kStageBytes = kAtoms * (kABytes + kBBytes);   // [A atoms][B atoms]
     static constexpr int kBarOff = kStages * kStageBytes;
-    static constexpr int kNumBars = 2 * kStages + 4 + 1 + 2 + 1;  // + two token-scale buffers, second drain
+    static constexpr int kNumBars = 2 * kStages + 4 + 1 + 2;  // + two token-scale buffers
     static constexpr int kXbufOff = kBarOff + 8 * kNumBars;           // 2 x 16 tokens x 64 outputs (fp32)
     static constexpr int kMiscOff = kXbufOff + 32 * kHalf * 4;
     static constexpr int kTileOffOff = kMiscOff + 16;                 // int[E+1] 128-row tiles per expert
@@ -77,7 +72,7 @@ struct BsCfg {
     static constexpr int kTokSfOff = (kCountsOff + 4 * kMaxExperts + 15) & ~15;  // u32[2][kTokWords][8][32]
     static constexpr size_t kSmem = 1024 + (size_t)kTokSfOff + 2 * kTokWords * 8 * 32 * 4;
     static_assert(kSmem <= 232448, "shared memory");
-    static_assert((kAtoms == 2 ? 4 : 2) * kNT <= kSfCol0 && kSfCol0 + kStages * kSfColsPerStage <= 512, "tensor memory");
+    static_assert(2 * kNT <= kSfCol0 && kSfCol0 + kStages * kSfColsPerStage <= 512, "tensor memory");
     static_assert(kAtoms == 1 || kAtoms == 2, "atoms per stage");
 };
 
@@ -171,10 +166,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto acc_empty = [&](int a) { return bars + 8u * (2 * kStages + 2 + a); };
     const uint32_t drain_bar = bars + 8u * (2 * kStages + 4);
     auto tok_bar = [&](int b) { return bars + 8u * (2 * kStages + 5 + b); };
-    const uint32_t drain_bar2 = bars + 8u * (2 * kStages + 7);
-    // two issuers (one K atom of each stage each, separate accumulators) when every tile has two atoms
-    const bool dual = kAtoms == 2 && args.kin >= 2 * kAtomK;
-    const uint32_t n_issuers = dual ? 2u : 1u;
     float* xbuf = reinterpret_cast<float*>(smem + Cfg::kXbufOff);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kMiscOff + 4);
@@ -206,14 +197,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 32) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(full_bar(s), 1 + 4);  // TMA (arrive + bytes) + the 4 scale-writer warps
-            mbar_init(empty_bar(s), n_issuers);
+            mbar_init(empty_bar(s), 1);
         }
         for (int a = 0; a < 2; ++a) {
-            mbar_init(acc_full(a), n_issuers);
+            mbar_init(acc_full(a), 1);
             mbar_init(acc_empty(a), 4);
         }
         mbar_init(drain_bar, 1);
-        mbar_init(drain_bar2, 1);
         for (int b = 0; b < 2; ++b) mbar_init(tok_bar(b), 4);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -264,16 +254,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = it - kStages < 0 ? 0 : it - kStages; j < it; ++j)
                 mbar_drain(full_bar(j % kStages), (uint32_t)(j / kStages) & 1u, p.hdr);
         }
-    } else if (warp == 1 || warp == 10) {
-        // ---------------- MMA issuers ----------------
-        // At decode sizes these threads set the pace, so their per-stage work is kept short: a
-        // non-blocking test of the stage before the bounded wait, the stage position kept as a
-        // counter, the tile's four instruction descriptors made once, and the operand descriptors
-        // advanced by adding to their address field (start >> 4: +2 per 32 K of a K-major atom, +
-        // the atom's and the stage's offset >> 4). With two issuers, thread 1 takes atom 0 of each
-        // stage into accumulator columns [a * kNT, ...) and thread 10 atom 1 into [2 kNT + a * kNT, ...).
-        const int my_at = warp == 1 ? 0 : 1;
-        if (lane == 0 && (my_at == 0 || dual)) {
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        // At decode sizes this thread sets the pace (eight MMAs of N = 16 per 32 KB stage), so
+        // its per-stage work is kept short: a non-blocking test of the stage before the bounded
+        // wait, the stage position kept as a counter, the tile's four instruction descriptors
+        // made once, and the operand descriptors advanced by adding to their address field
+        // (start >> 4: +2 per 32 K of a K-major atom, + the atom's and the stage's offset >> 4).
+        if (lane == 0) {
             const uint64_t ad0 = kmajor_desc(base, 0), bd0 = kmajor_desc(base + kAtoms * kABytes, 0);
             int s = 0, tc = 0;
             uint32_t ph = 0;
@@ -284,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const Tile tl = tile_of(t);
                 const int n = (tl.n_valid + 15) & ~15;
-                const uint32_t d = tmem_base + (uint32_t)(a * kNT + my_at * 2 * kNT);
+                const uint32_t d = tmem_base + (uint32_t)(a * kNT);
                 uint32_t idesc[kAtomK / 32];
 #pragma unroll
                 for (int kk = 0; kk < kAtomK / 32; ++kk) idesc[kk] = bs_idesc(kAfmt, kBfmt, n, kk);
@@ -297,23 +285,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t so = (uint64_t)((s * Cfg::kStageBytes) >> 4);
                     const uint32_t sf = tmem_base + kSfCol0 + s * kSfColsPerStage;
                     const int na = atoms_of(kb);
-                    for (int at = dual ? my_at : 0; at < (dual ? min(na, my_at + 1) : na); ++at) {
+                    for (int at = 0; at < na; ++at) {
                         const uint64_t ad = ad0 + so + (uint64_t)((at * kABytes) >> 4);
                         const uint64_t bd = bd0 + so + (uint64_t)((at * Cfg::kBBytes) >> 4);
-                        const int first = dual ? kb : (kb | at);  // the accumulator's first MMA overwrites it
 #pragma unroll
                         for (int kk = 0; kk < kAtomK / 32; ++kk)
                             tc_mma_bs(d, ad + 2 * kk, bd + 2 * kk, idesc[kk], sf + 8 * at, sf + 8 * at + 4,
-                                      (first | kk) != 0);
+                                      (kb | at | kk) != 0);
                     }
                     tc_commit(empty_bar(s));
                     if (++s == kStages) s = 0, ph ^= 1u;
                 }
                 if (ok) tc_commit(acc_full(a));
             }
-            const uint32_t my_drain = my_at ? drain_bar2 : drain_bar;
-            tc_commit(my_drain);
-            mbar_drain(my_drain, 0, p.hdr);
+            tc_commit(drain_bar);
+            mbar_drain(drain_bar, 0, p.hdr);
         }
     } else if (warp >= 6) {
         // ---------------- scale writers ----------------
@@ -485,13 +471,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c0 = 0; c0 < n; c0 += 32) {
                     uint32_t v[32];
                     tmem_ld32(tb + c0, v);
-                    if (dual) {  // the second issuer's partial sums (uniform across the CTA)
-                        uint32_t v2[32];
-                        tmem_ld32(tb + 2 * kNT + c0, v2);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) + __uint_as_float(v2[i]));
-                    }
                     tmem_ld_wait();
                     if (gate) {
 #pragma unroll
@@ -541,13 +520,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (c0 >= tl.n_valid) break;  // uniform across the warp
                     uint32_t y[32];
                     tmem_ld32(tb + c0, y);
-                    if (dual) {  // the second issuer's partial sums
-                        uint32_t y2[32];
-                        tmem_ld32(tb + 2 * kNT + c0, y2);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) y[i] = __float_as_uint(__uint_as_float(y[i]) + __uint_as_float(y2[i]));
-                    }
                     tmem_ld_wait();
 #pragma unroll
                     for (int tt = 0; tt < 32 && c0 + tt < kNT; ++tt) {  // src < 0 past the routed rows

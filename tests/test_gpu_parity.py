@@ -427,7 +427,7 @@ def test_int4_l1_accumulators_exact_at_the_largest_k(moe):
     inp["w1"] = (nib[..., 0::2] | (nib[..., 1::2] << 4)).contiguous()
     inp["w1_scale"] = torch.ones_like(inp["w1_scale"])
     inp["topk_ids"][:3] = 0
-    out = (run_prepared(moe, wl, inp) if prepared else run_forward(moe, wl, inp, stages=True))
+    out = run_forward(moe, wl, inp, stages=True)
     assert out["status"] == 0
     L = out["layout"]
     rows = L["pool_rows"]
