@@ -229,7 +229,7 @@ static moe_status expert_l1(moe_operand w1, const moe_dims* d, moe_dtype_mode m,
     } else if (!(flags & MOE_FLAG_SIMT) && tc_supported(p, 1)) {
         e = launch_l1_tc(p, w1.data, w1.scale, s);
     } else if (!(flags & MOE_FLAG_SIMT) && bs_supported(p, 1)) {
-        e = launch_l1_bs(p, w1.data, w1.scale, (flags & MOE_FLAG_WEIGHT_MAJOR) != 0, s);
+        e = launch_l1_bs(p, w1.data, w1.scale, flags, s);
     } else if (!(flags & MOE_FLAG_SIMT) && int8_tc_supported(p, 1)) {
         e = launch_l1_int8_tc(p, w1.data, w1.scale, false, s);
     } else if (!(flags & (MOE_FLAG_SIMT | MOE_FLAG_TOKEN_MAJOR)) && w4_wm_supported(p, 1) &&
@@ -275,7 +275,7 @@ moe_status moe_expert_l2(moe_operand w2, const float* topk_weights, const moe_di
     if (!(flags & MOE_FLAG_SIMT) && tc_supported(p, 2))
         return from_cuda(launch_l2_tc(p, w2.data, w2.scale, topk_weights, s));
     if (!(flags & MOE_FLAG_SIMT) && bs_supported(p, 2))
-        return from_cuda(launch_l2_bs(p, w2.data, w2.scale, topk_weights, (flags & MOE_FLAG_WEIGHT_MAJOR) != 0, s));
+        return from_cuda(launch_l2_bs(p, w2.data, w2.scale, topk_weights, flags, s));
     if (prepared || (!(flags & MOE_FLAG_SIMT) && int8_tc_supported(p, 2)))
         return from_cuda(launch_l2_int8_tc(p, w2.data, w2.scale, topk_weights, prepared, s));
     if (!(flags & (MOE_FLAG_SIMT | MOE_FLAG_TOKEN_MAJOR)) && w4_wm_supported(p, 2) &&

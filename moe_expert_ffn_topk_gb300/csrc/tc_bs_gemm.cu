@@ -564,8 +564,9 @@ cudaError_t launch_bs_cfg(const Plan& p, const CUtensorMap& tmW, const CUtensorM
 }
 
 template <int MODE, bool kL1>
-cudaError_t launch_bs(const Plan& p, const void* w, const void* w_scale, const float* topk_weights, bool weight_major,
+cudaError_t launch_bs(const Plan& p, const void* w, const void* w_scale, const float* topk_weights, uint32_t flags,
                       cudaStream_t s) {
+    const bool weight_major = (flags & MOE_FLAG_WEIGHT_MAJOR) != 0;
     const int n_out = kL1 ? 2 * p.I : p.H;
     const int kin = kL1 ? p.H : p.I;
     CUtensorMap tmW, tmX;
@@ -589,6 +590,10 @@ cudaError_t launch_bs(const Plan& p, const void* w, const void* w_scale, const f
     // few routed rows per expert: the weights stream from HBM; 16-token sub-tiles and K = 256
     // stages (whole 128-byte lines of every weight row per load)
     const bool decode = (int64_t)p.T * p.K <= (int64_t)16 * p.E;
+    // prefill sizes: weight-major tiles on CTA pairs (M = 256 weight rows, tokens as N), or with
+    // MOE_FLAG_TOKEN_MAJOR the one-CTA token-major tiles
+    if (!decode && !weight_major && !(flags & MOE_FLAG_TOKEN_MAJOR) && bs_pair_supported(p, kL1 ? 1 : 2))
+        return kL1 ? launch_l1_bs_pair(p, w, w_scale, s) : launch_l2_bs_pair(p, w, w_scale, topk_weights, s);
     if (!decode && !weight_major && bs_tm_supported(p, kL1 ? 1 : 2))
         return kL1 ? launch_l1_bs_tm(p, w, w_scale, s) : launch_l2_bs_tm(p, w, w_scale, topk_weights, s);
     // token rows: one copy brings the sub-tile's kNT pool rows
@@ -610,21 +615,18 @@ bool bs_supported(const Plan& p, int stage) {
     return p.H % kWR == 0 && p.I % kAtomK == 0;
 }
 
-cudaError_t launch_l1_bs(const Plan& p, const void* w1, const void* w1_scale, bool weight_major, cudaStream_t s) {
-    if (p.mode == MOE_A8W4_FP8_FP4) return launch_bs<MOE_A8W4_FP8_FP4, true>(p, w1, w1_scale, nullptr, weight_major, s);
-    if (p.mode == MOE_A8W8_FP8) return launch_bs<MOE_A8W8_FP8, true>(p, w1, w1_scale, nullptr, weight_major, s);
-    if (p.mode == MOE_A8W8_FP8_E5M2)
-        return launch_bs<MOE_A8W8_FP8_E5M2, true>(p, w1, w1_scale, nullptr, weight_major, s);
+cudaError_t launch_l1_bs(const Plan& p, const void* w1, const void* w1_scale, uint32_t flags, cudaStream_t s) {
+    if (p.mode == MOE_A8W4_FP8_FP4) return launch_bs<MOE_A8W4_FP8_FP4, true>(p, w1, w1_scale, nullptr, flags, s);
+    if (p.mode == MOE_A8W8_FP8) return launch_bs<MOE_A8W8_FP8, true>(p, w1, w1_scale, nullptr, flags, s);
+    if (p.mode == MOE_A8W8_FP8_E5M2) return launch_bs<MOE_A8W8_FP8_E5M2, true>(p, w1, w1_scale, nullptr, flags, s);
     return cudaErrorNotSupported;
 }
 
-cudaError_t launch_l2_bs(const Plan& p, const void* w2, const void* w2_scale, const float* topk_weights,
-                         bool weight_major, cudaStream_t s) {
-    if (p.mode == MOE_A8W4_FP8_FP4)
-        return launch_bs<MOE_A8W4_FP8_FP4, false>(p, w2, w2_scale, topk_weights, weight_major, s);
-    if (p.mode == MOE_A8W8_FP8) return launch_bs<MOE_A8W8_FP8, false>(p, w2, w2_scale, topk_weights, weight_major, s);
-    if (p.mode == MOE_A8W8_FP8_E5M2)
-        return launch_bs<MOE_A8W8_FP8_E5M2, false>(p, w2, w2_scale, topk_weights, weight_major, s);
+cudaError_t launch_l2_bs(const Plan& p, const void* w2, const void* w2_scale, const float* topk_weights, uint32_t flags,
+                         cudaStream_t s) {
+    if (p.mode == MOE_A8W4_FP8_FP4) return launch_bs<MOE_A8W4_FP8_FP4, false>(p, w2, w2_scale, topk_weights, flags, s);
+    if (p.mode == MOE_A8W8_FP8) return launch_bs<MOE_A8W8_FP8, false>(p, w2, w2_scale, topk_weights, flags, s);
+    if (p.mode == MOE_A8W8_FP8_E5M2) return launch_bs<MOE_A8W8_FP8_E5M2, false>(p, w2, w2_scale, topk_weights, flags, s);
     return cudaErrorNotSupported;
 }
 

@@ -464,20 +464,48 @@ FP8_PREFILL = [(m, w) for m, w in ALL if m in ("a8w8_fp8", "a8w4_fp8_fp4", "a8w8
 
 
 @pytest.mark.parametrize("mode,wl", FP8_PREFILL, ids=[f"{m}-{w.name}" for m, w in FP8_PREFILL])
-def test_token_major_and_weight_major_block_scaled_tiles_agree(moe, mode, wl):
-    """At prefill sizes the FP8 modes run 128-token x 256-weight-row tiles; the flag selects the
-    128-weight-row x 128-token tiles. Both compute the same block-scaled products, so the combine
-    rows and the output agree up to the fp32 summation order (within the mode's tolerance), and
-    the oracle bounds both."""
+def test_block_scaled_tile_choices_agree(moe, mode, wl):
+    """At prefill sizes the FP8 modes run weight-major tiles on CTA pairs (256 weight rows x up to
+    224 tokens) where the shape allows; MOE_FLAG_TOKEN_MAJOR selects 128-token x 256-weight-row
+    tiles and MOE_FLAG_WEIGHT_MAJOR one-CTA 128-weight-row x 128-token tiles. All compute the same
+    block-scaled products, so the combine rows and the output agree up to the fp32 summation order
+    (within the mode's tolerance), and the oracle bounds each."""
     inp = make_inputs(wl, device=DEV)
-    outs = [run_forward(moe, wl, inp, flags=f, stages=True) for f in (0, moe.MOE_FLAG_WEIGHT_MAJOR)]
+    flags = (0, moe.MOE_FLAG_TOKEN_MAJOR, moe.MOE_FLAG_WEIGHT_MAJOR)
+    outs = [run_forward(moe, wl, inp, flags=f, stages=True) for f in flags]
     assert all(o["status"] == 0 for o in outs)
     L = outs[0]["layout"]
     c = [region(o["ws"], L, "comb", torch.bfloat16, wl.T * wl.K * wl.H).float().cpu().numpy() for o in outs]
-    assert np.abs(c[0] - c[1]).max() <= TOL[mode] * np.abs(c[1]).max()
+    for other in c[1:]:
+        assert np.abs(c[0] - other).max() <= TOL[mode] * np.abs(other).max()
     ref = oracle_forward(wl, inp)
     for o in outs:
         assert_close(y_numpy(o["y"]), ref, mode)
+
+
+# Per-expert token counts at the edges of the pair tiles' granularities: 16-token MMA columns, 16-row
+# token boxes of a partial tile, the 112 rows a CTA stages, the 224 tokens of a full tile.
+PAIR_COUNTS = [1, 15, 16, 17, 111, 112, 113, 223, 224, 225, 447, 449]
+
+
+@pytest.mark.parametrize("mode", ["a8w4_fp8_fp4", "a8w8_fp8", "a8w8_fp8_e5m2"])
+def test_pair_tiles_at_token_count_edges(moe, mode):
+    """The CTA-pair weight-major kernel (both GEMMs: H 512, I 512) against the oracle and against the
+    token-major tiles with experts of 1 to 449 routed tokens."""
+    wl = Workload(f"pair_edges_{mode}", mode, sum(PAIR_COUNTS), 512, 512, len(PAIR_COUNTS), 1, 77, 0.05)
+    inp = make_inputs(wl, device=DEV)
+    inp["topk_ids"] = torch.repeat_interleave(torch.arange(wl.E, dtype=torch.int32),
+                                              torch.tensor(PAIR_COUNTS))[:, None].to(DEV).contiguous()
+    a = run_forward(moe, wl, inp, stages=True)
+    b = run_forward(moe, wl, inp, flags=moe.MOE_FLAG_TOKEN_MAJOR, stages=True)
+    assert a["status"] == 0 and b["status"] == 0
+    check_plan(a, wl, inp["topk_ids"])
+    ref, rec = oracle_forward(wl, inp, return_intermediates=True)
+    L = a["layout"]
+    comb = region(a["ws"], L, "comb", torch.bfloat16, wl.T * wl.K * wl.H).view(wl.T * wl.K, wl.H)
+    assert_close(y_numpy(comb), rec["comb"], mode, "combine rows")
+    assert_close(y_numpy(a["y"]), ref, mode)
+    assert_close(y_numpy(b["y"]), ref, mode)
 
 
 W4_ORDER = np.array([0, 4, 1, 5, 2, 6, 3, 7])
