@@ -145,6 +145,14 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
         : "memory");
 }
 
+// Arrive on the even CTA's barrier (given by its shared::cluster address) without a release fence.
+// The scale writers use it after tcgen05.wait::st, which already blocks until their tensor-memory
+// writes are complete, so no ordering is left for a fence to provide; a cluster-scope release fence
+// per stage and warp stalled the writers (~2000 cycles a stage, measured) and with them the MMA.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync %0, 128;" ::"n"(kEpiBar) : "memory"); }
 // The same barrier, ANDing `pred` over the four epilogue warps: they leave the tile loop together.
 __device__ __forceinline__ bool epi_all(bool pred) {
@@ -402,7 +410,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     tmem_st_wait();
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive_cluster(mapa_shared(full_bar(s), 0));
+                    if (lane == 0) {
+                        if (even) mbar_arrive(full_bar(s));
+                        else mbar_arrive_cluster_relaxed(mapa_shared(full_bar(s), 0));
+                    }
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(sf_empty(buf));
