@@ -147,7 +147,7 @@ enum {
                                    the GPU. Same results bit for bit, for comparison.
                                    FP8 modes at prefill sizes: one-CTA token-major tiles (128 tokens
                                    x 256 weight rows) instead of the weight-major tiles on CTA pairs
-                                   (256 weight rows x up to 224 tokens, tcgen05 cta_group::2); same
+                                   (256 weight rows x up to 192 tokens, tcgen05 cta_group::2); same
                                    results up to fp32 summation order, for comparison. */
     MOE_FLAG_PREPARED_WEIGHTS = 128u /* A8W8-INT: w1.data and w2.data hold the weights as
                                    moe_prepare_weights wrote them (every int8 code as the exact f16

@@ -5,12 +5,13 @@
 // the matrix multiply; DeepGEMM page §4 step 5: L1 on 2-CTA block-scaled MMAs).
 //
 // Weight-major pair tiles: M = 256 weight rows, 128 in each CTA of a cluster of two; N = up to
-// 224 tokens of one expert (rounded up to 16), each CTA staging half of them; K = 128 per stage.
+// 192 tokens of one expert (rounded up to 16), each CTA staging half of them; K = 128 per stage.
 // Per SM and stage that is 16 KB of weights (e2m1 takes a byte per code in the MMA's operand
-// layout) and 14 KB of tokens for 128 x 224 x 128 MACs: 17 KB per 128^3 against 24 KB for the
+// layout) and 12 KB of tokens for 128 x 192 x 128 MACs: 18.7 KB per 128^3 against 24 KB for the
 // single-CTA token-major tile (128 tokens x 256 weight rows), and shared-memory fill by TMA is what
-// bounds that tile. Tokens are the N side, so an expert's last tile is padded to 16 tokens, not to
-// 128 rows.
+// bounds that tile; six stages keep 168 KB in flight per SM (the fill rate is the bytes in flight
+// over a load latency of 1.5-2.5 us). Tokens are the N side, so an expert's last tile is padded to 16
+// tokens, not to 128 rows.
 // - L1: the pair's 256 rows are the gate and up rows of 128 outputs; CTA c holds the 64 gate and 64
 //   up rows of outputs [128 s + 64 c, +64), so its epilogue pairs lane r (gate) with lane r + 64
 //   (up) through shared memory, applies SwiGLU (Ascend page, "SwiGLU Activation") and the MX FP8
@@ -29,7 +30,8 @@
 // Synchronisation (as in the bf16 pair kernel):
 //   full[s]   (even CTA): both CTAs' TMA loads of stage s complete on it (the even CTA's producer
 //             arrives with both CTAs' byte count) and the four scale-writer warps of each CTA arrive
-//             on it when the stage's scale words are in tensor memory;
+//             on it when the stage's scale words are in tensor memory (the odd CTA's without a
+//             release fence, see mbar_arrive_cluster_relaxed);
 //   empty[s]  (each CTA): the MMA commit arrives on both CTAs' barriers;
 //   acc_full[a] (each CTA): commit to both; acc_empty[a] (even CTA): the four epilogue warps of
 //             both CTAs.
@@ -55,10 +57,10 @@ using namespace tc;
 
 constexpr int kHM = 128;      // weight rows per CTA (the pair MMA has M = 256)
 constexpr int kHalf = 64;     // L1: a CTA's gate rows, then its up rows
-constexpr int kNT = 224;      // tokens per tile at most (MMA N)
+constexpr int kNT = 192;      // tokens per tile at most (MMA N)
 constexpr int kHT = kNT / 2;  // token rows staged per CTA
 constexpr int kAtomK = 128;   // K per stage: one 128-byte swizzle atom
-constexpr int kStages = 4;
+constexpr int kStages = 6;
 constexpr int kThreads = 320;
 constexpr int kMaxExperts = 1024;
 constexpr int kABytes = kHM * 128;           // 16 KB
@@ -68,9 +70,9 @@ constexpr int kTokBox = 16;                  // token rows per TMA box of a part
 constexpr int kSfBlk = 4;                    // K atoms per scale block (16 bytes of a row)
 constexpr int kSfBufs = 4;
 constexpr int kSfWBytes = kHM * 16;          // weight scale words of a block: [128 rows][4 atoms]
-constexpr int kSfTBytes = kNT * 16;          // token scale words of a block: [224 rows][4 atoms]
-constexpr int kSfCol0 = 2 * kNT;             // two 224-column accumulators, then the scale ring
-constexpr int kSfColsPerStage = 16;          // A word in columns 0-3, token words in 4..10
+constexpr int kSfTBytes = kNT * 16;          // token scale words of a block: [kNT rows][4 atoms]
+constexpr int kSfCol0 = 2 * kNT;             // two 192-column accumulators, then the scale ring
+constexpr int kSfColsPerStage = 16;          // A word in columns 0-3, token words in 4..9
 constexpr int kEpiBar = 1;                   // named barrier of the 4 epilogue warps
 constexpr int kSfOff = kStages * kStageBytes;
 constexpr int kBarOff = kSfOff + kSfBufs * (kSfWBytes + kSfTBytes);
@@ -604,7 +606,7 @@ cudaError_t launch_bs_pair_t(const Plan& p, const void* w, const void* w_scale, 
     }
     if (!ok) return cudaErrorInvalidValue;
     PairBsArgs args{p, topk_weights, kL1 ? p.I / 128 : p.H / 256, kin / kAtomK, kin};
-    // at most one tile per 224 routed rows plus one per expert, per slab
+    // at most one tile per kNT routed rows plus one per expert, per slab
     const int64_t max_tiles = ((int64_t)p.T * p.K / kNT + p.E + 1) * args.n_slabs;
     const int clusters = (int)std::max<int64_t>(1, std::min<int64_t>(max_tiles, resident_clusters<MODE, kL1>()));
     tc_bs_pair_kernel<MODE, kL1><<<2 * clusters, kThreads, kSmem, s>>>(tmW, tmX, tmX16, tmSW, tmSX, args);

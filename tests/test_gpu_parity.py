@@ -466,7 +466,7 @@ FP8_PREFILL = [(m, w) for m, w in ALL if m in ("a8w8_fp8", "a8w4_fp8_fp4", "a8w8
 @pytest.mark.parametrize("mode,wl", FP8_PREFILL, ids=[f"{m}-{w.name}" for m, w in FP8_PREFILL])
 def test_block_scaled_tile_choices_agree(moe, mode, wl):
     """At prefill sizes the FP8 modes run weight-major tiles on CTA pairs (256 weight rows x up to
-    224 tokens) where the shape allows; MOE_FLAG_TOKEN_MAJOR selects 128-token x 256-weight-row
+    192 tokens) where the shape allows; MOE_FLAG_TOKEN_MAJOR selects 128-token x 256-weight-row
     tiles and MOE_FLAG_WEIGHT_MAJOR one-CTA 128-weight-row x 128-token tiles. All compute the same
     block-scaled products, so the combine rows and the output agree up to the fp32 summation order
     (within the mode's tolerance), and the oracle bounds each."""
@@ -484,8 +484,8 @@ def test_block_scaled_tile_choices_agree(moe, mode, wl):
 
 
 # Per-expert token counts at the edges of the pair tiles' granularities: 16-token MMA columns, 16-row
-# token boxes of a partial tile, the 112 rows a CTA stages, the 224 tokens of a full tile.
-PAIR_COUNTS = [1, 15, 16, 17, 111, 112, 113, 223, 224, 225, 447, 449]
+# token boxes of a partial tile, the 96 rows a CTA stages, the 192 tokens of a full tile.
+PAIR_COUNTS = [1, 15, 16, 17, 95, 96, 97, 191, 192, 193, 383, 449]
 
 
 @pytest.mark.parametrize("mode", ["a8w4_fp8_fp4", "a8w8_fp8", "a8w8_fp8_e5m2"])
