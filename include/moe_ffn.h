@@ -125,8 +125,8 @@ enum {
     MOE_FLAG_NONE = 0u,
     MOE_FLAG_SIMT = 1u,         /* run the CUDA-core reference GEMMs instead of the tensor-core ones */
     MOE_FLAG_WEIGHT_MAJOR = 2u, /* FP8 modes at prefill sizes: one-CTA tiles of 128 weight rows x 128
-                                   tokens (the decode-style tile) instead of the CTA-pair tiles;
-                                   same results up to fp32 summation order, for comparison.
+                                   tokens (the decode-style tile) instead of 128 tokens x 256 weight
+                                   rows; same results up to fp32 summation order, for comparison.
                                    A8W4-INT: weight-major tiles (128 weight rows x up to 256 tokens)
                                    whatever the tile count (see MOE_FLAG_TOKEN_MAJOR); same bits */
     MOE_FLAG_QUANTIZE_X = 4u,   /* moe_forward: x.data is bf16 [T,H] (x.scale unused) and the
@@ -140,15 +140,16 @@ enum {
                                    for comparison. The fused launch always uses one-CTA tiles. */
     MOE_FLAG_PAIR_L1 = 32u,     /* A16W16: the L1 GEMM on CTA pairs too (by default it runs on
                                    one-CTA tiles, measured faster at the power cap); same results
-                                   bit for bit. Ignored with MOE_FLAG_SINGLE_CTA. */
+                                   bit for bit. Ignored with MOE_FLAG_SINGLE_CTA.
+                                   FP8 modes at prefill sizes: both GEMMs on weight-major tiles on
+                                   CTA pairs (256 weight rows x up to 192 tokens, tcgen05
+                                   cta_group::2, where H and I allow) instead of the token-major
+                                   tiles; same results up to fp32 summation order, for comparison
+                                   (measured slower). */
     MOE_FLAG_TOKEN_MAJOR = 64u, /* A8W4-INT: token-major tiles (128 pool rows x 256 weight rows)
                                    where weight-major ones (128 weight rows x up to 256 tokens) would
                                    run: experts x weight slabs of at least four rounds of tiles on
-                                   the GPU. Same results bit for bit, for comparison.
-                                   FP8 modes at prefill sizes: one-CTA token-major tiles (128 tokens
-                                   x 256 weight rows) instead of the weight-major tiles on CTA pairs
-                                   (256 weight rows x up to 192 tokens, tcgen05 cta_group::2); same
-                                   results up to fp32 summation order, for comparison. */
+                                   the GPU. Same results bit for bit, for comparison. */
     MOE_FLAG_PREPARED_WEIGHTS = 128u /* A8W8-INT: w1.data and w2.data hold the weights as
                                    moe_prepare_weights wrote them (every int8 code as the exact f16
                                    value, same [E,N,K] layout; the fp32 scales unchanged). The

@@ -119,8 +119,8 @@ cudaError_t launch_l2_w4_wm(const Plan& p, const void* w2, const void* w2_scale,
 __host__ __device__ constexpr int w4_plane_pos(int k) { return (k & ~7) | ((k & 3) << 1) | ((k >> 2) & 1); }
 
 // Block-scaled tensor-core path of the FP8 modes (kind::mxf8f6f4.block_scale): weight-major
-// tiles for decode-sized experts; for prefill-sized ones weight-major tiles on CTA pairs, or with
-// MOE_FLAG_TOKEN_MAJOR in `flags` token-major tiles, or with MOE_FLAG_WEIGHT_MAJOR one-CTA
+// tiles for decode-sized experts; for prefill-sized ones token-major tiles, or with
+// MOE_FLAG_PAIR_L1 in `flags` weight-major tiles on CTA pairs, or with MOE_FLAG_WEIGHT_MAJOR one-CTA
 // weight-major tiles (each where the shape has that kernel).
 cudaError_t launch_l1_bs(const Plan& p, const void* w1, const void* w1_scale, uint32_t flags, cudaStream_t s);
 cudaError_t launch_l2_bs(const Plan& p, const void* w2, const void* w2_scale, const float* topk_weights,

@@ -590,9 +590,9 @@ cudaError_t launch_bs(const Plan& p, const void* w, const void* w_scale, const f
     // few routed rows per expert: the weights stream from HBM; 16-token sub-tiles and K = 256
     // stages (whole 128-byte lines of every weight row per load)
     const bool decode = (int64_t)p.T * p.K <= (int64_t)16 * p.E;
-    // prefill sizes: weight-major tiles on CTA pairs (M = 256 weight rows, tokens as N), or with
-    // MOE_FLAG_TOKEN_MAJOR the one-CTA token-major tiles
-    if (!decode && !weight_major && !(flags & MOE_FLAG_TOKEN_MAJOR) && bs_pair_supported(p, kL1 ? 1 : 2))
+    // prefill sizes: token-major tiles, or with MOE_FLAG_PAIR_L1 weight-major tiles on CTA pairs (M = 256
+    // weight rows, tokens as N; measured slower: Zipf prefill L1 2.48 against 1.50 ms)
+    if (!decode && !weight_major && (flags & MOE_FLAG_PAIR_L1) && bs_pair_supported(p, kL1 ? 1 : 2))
         return kL1 ? launch_l1_bs_pair(p, w, w_scale, s) : launch_l2_bs_pair(p, w, w_scale, topk_weights, s);
     if (!decode && !weight_major && bs_tm_supported(p, kL1 ? 1 : 2))
         return kL1 ? launch_l1_bs_tm(p, w, w_scale, s) : launch_l2_bs_tm(p, w, w_scale, topk_weights, s);

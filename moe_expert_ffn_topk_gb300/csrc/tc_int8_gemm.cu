@@ -20,10 +20,8 @@
 // gate block and the up block of the same 128 outputs (two accumulators sharing B), L2 tiles two
 // 128-row blocks of hidden columns.
 //
-// Warp roles (480 threads): warp 0 TMA of raw weights, warp 1 TMEM allocation + MMA issue,
-// warps 2-5 epilogue, warps 6-13 weight converters (one row of one 128-row block each: with four
-// warps converting two rows a thread, the conversion took 900-1050 cycles a stage against 1024 of
-// MMA work), warp 14 TMA of the token tiles.
+// Warp roles (352 threads): warp 0 TMA of raw weights, warp 1 TMEM allocation + MMA issue,
+// warps 2-5 epilogue, warps 6-9 weight converters, warp 10 TMA of the token tiles.
 // Every wait is bounded; on time-out the CTA records MOE_ERR_TIMEOUT, drains and exits.
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -44,8 +42,7 @@ using namespace tc;
 constexpr int kWR = 128;        // weight rows per block (MMA M)
 constexpr int kTok = 128;       // tokens per tile (one route tile)
 constexpr int kBK = 64;         // K per stage: 64 f16 = one 128-byte swizzle row
-constexpr int kThreads = 480;
-constexpr int kConvThreads = 256;  // warps 6-13: one weight row of one 128-row block each
+constexpr int kThreads = 352;
 constexpr int kMaxExperts = 1024;
 constexpr int kABytes = 2 * kWR * 128;   // two f16 weight blocks
 constexpr int kTokBytes = 2 * kTok * 128;  // hi rows, then lo rows
@@ -191,10 +188,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < kRawStages; ++i) {
             mbar_init(raw_full(i), 1);
-            mbar_init(raw_empty(i), kConvThreads);
+            mbar_init(raw_empty(i), 128);
         }
         for (int i = 0; i < kHfStages; ++i) {
-            mbar_init(hf_full(i), kPrep ? 1 : kConvThreads);  // the weight TMA (arrive + bytes), or the converters
+            mbar_init(hf_full(i), kPrep ? 1 : 128);  // the weight TMA (arrive + bytes), or the 128 converter threads
             mbar_init(hf_empty(i), 1);
         }
         for (int i = 0; i < kTokStages; ++i) {
@@ -267,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = it - kRawStages < 0 ? 0 : it - kRawStages; j < it; ++j)
                 mbar_drain(raw_full(j % kRawStages), (uint32_t)(j / kRawStages) & 1u, p.hdr);
         }
-    } else if (warp == 14) {
+    } else if (warp == 10) {
         // ---------------- token TMA: hi plane rows, then lo plane rows ----------------
         if (lane == 0) {
             int it = 0;
@@ -343,8 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp >= 6) {
         if constexpr (!kPrep) {
             // ---------------- weight converters ----------------
-            const int c = threadIdx.x - 192;  // block c / 128 (gate / up, or the two hidden blocks), row c % 128
-            const int blk = c >> 7, row = c & (kWR - 1);
+            const int c = threadIdx.x - 192;  // row of each 128-row weight block
             int it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
@@ -358,9 +354,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const uint8_t* rw = smem + kRawOff + r * kRawBytes;
                     uint8_t* dst = smem + kHfOff + b * kABytes;
-                    uint4 r0[4];
-                    load_row(rw + blk * kWR * kBK, row, r0);
-                    store_row(r0, dst + blk * kWR * 128, row);
+                    uint4 r0[4], r1[4];
+                    load_row(rw, c, r0);
+                    load_row(rw + kWR * kBK, c, r1);
+                    store_row(r0, dst, c);
+                    store_row(r1, dst + kWR * 128, c);
                     fence_proxy_async_smem();
                     mbar_arrive(raw_empty(r));
                     mbar_arrive(hf_full(b));
@@ -421,27 +419,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int j = tl.s * kWR + q * 32 + lane;
 #pragma unroll
                 for (int ci = 0; ci < kTok / 32; ++ci) {
+                    const int c0 = 32 * ci;
+                    if (c0 >= n16) break;  // uniform across the warp
+                    uint32_t hi[32], lo[32];
+                    float hg[32];
+                    tmem_ld32(tb + c0, hi);
+                    tmem_ld32(tb + n16 + c0, lo);
+                    tmem_ld_wait();
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {  // 16 tokens at a time keeps the registers in bounds
-                        const int cc = 32 * ci + 16 * hh;
-                        if (cc >= n16) break;  // uniform across the warp
-                        uint32_t hi[16], lo[16];
-                        float hg[16];
-                        tmem_ld16(tb + cc, hi);
-                        tmem_ld16(tb + n16 + cc, lo);
-                        tmem_ld_wait();
+                    for (int tt = 0; tt < 32; ++tt) hg[tt] = __int2float_rn(exact_int(hi[tt], lo[tt]));
+                    tmem_ld32(tb + 256 + c0, hi);
+                    tmem_ld32(tb + 256 + n16 + c0, lo);
+                    tmem_ld_wait();
 #pragma unroll
-                        for (int tt = 0; tt < 16; ++tt) hg[tt] = __int2float_rn(exact_int(hi[tt], lo[tt]));
-                        tmem_ld16(tb + 256 + cc, hi);
-                        tmem_ld16(tb + 256 + n16 + cc, lo);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int tt = 0; tt < 16; ++tt) {
-                            const float sx = __shfl_sync(0xffffffffu, sx_l[ci], 16 * hh + tt);
-                            const float Hg = __fmul_rn(__fmul_rn(hg[tt], sg), sx);
-                            const float Hu = __fmul_rn(__fmul_rn(__int2float_rn(exact_int(hi[tt], lo[tt])), su), sx);
-                            p.a_f32[(int64_t)(tl.row0 + cc + tt) * I + j] = swiglu1(Hg, Hu, p.act_clamp);
-                        }
+                    for (int tt = 0; tt < 32; ++tt) {
+                        const float sx = __shfl_sync(0xffffffffu, sx_l[ci], tt);
+                        const float Hg = __fmul_rn(__fmul_rn(hg[tt], sg), sx);
+                        const float Hu = __fmul_rn(__fmul_rn(__int2float_rn(exact_int(hi[tt], lo[tt])), su), sx);
+                        p.a_f32[(int64_t)(tl.row0 + c0 + tt) * I + j] = swiglu1(Hg, Hu, p.act_clamp);
                     }
                 }
             } else {
@@ -454,20 +449,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int blk = 0; blk < 2; ++blk) {
                         const int h = tl.s * 2 * kWR + blk * kWR + q * 32 + lane;
+                        uint32_t hi[32], lo[32];
+                        tmem_ld32(tb + blk * 256 + c0, hi);
+                        tmem_ld32(tb + blk * 256 + n16 + c0, lo);
+                        tmem_ld_wait();
 #pragma unroll
-                        for (int hh = 0; hh < 2; ++hh) {
-                            const int cc = c0 + 16 * hh;
-                            if (cc >= n16) break;  // uniform across the warp
-                            uint32_t hi[16], lo[16];
-                            tmem_ld16(tb + blk * 256 + cc, hi);
-                            tmem_ld16(tb + blk * 256 + n16 + cc, lo);
-                            tmem_ld_wait();
-#pragma unroll
-                            for (int tt = 0; tt < 16; ++tt) {  // slot < 0 past the routed rows
-                                const int src = w_src[cc + tt];
-                                const float y = __fmul_rn(__fmul_rn(__int2float_rn(exact_int(hi[tt], lo[tt])), s2[blk]), w_sa[cc + tt]);
-                                st_global_u16_if(src >= 0, p.comb + (int64_t)src * H + h, float_to_bf16_bits(__fmul_rn(w_g[cc + tt], y)));
-                            }
+                        for (int tt = 0; tt < 32; ++tt) {  // slot < 0 past the routed rows
+                            const int src = w_src[c0 + tt];
+                            const float y = __fmul_rn(__fmul_rn(__int2float_rn(exact_int(hi[tt], lo[tt])), s2[blk]), w_sa[c0 + tt]);
+                            st_global_u16_if(src >= 0, p.comb + (int64_t)src * H + h, float_to_bf16_bits(__fmul_rn(w_g[c0 + tt], y)));
                         }
                     }
                 }

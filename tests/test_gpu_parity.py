@@ -465,13 +465,13 @@ FP8_PREFILL = [(m, w) for m, w in ALL if m in ("a8w8_fp8", "a8w4_fp8_fp4", "a8w8
 
 @pytest.mark.parametrize("mode,wl", FP8_PREFILL, ids=[f"{m}-{w.name}" for m, w in FP8_PREFILL])
 def test_block_scaled_tile_choices_agree(moe, mode, wl):
-    """At prefill sizes the FP8 modes run weight-major tiles on CTA pairs (256 weight rows x up to
-    192 tokens) where the shape allows; MOE_FLAG_TOKEN_MAJOR selects 128-token x 256-weight-row
-    tiles and MOE_FLAG_WEIGHT_MAJOR one-CTA 128-weight-row x 128-token tiles. All compute the same
-    block-scaled products, so the combine rows and the output agree up to the fp32 summation order
-    (within the mode's tolerance), and the oracle bounds each."""
+    """At prefill sizes the FP8 modes run 128-token x 256-weight-row tiles; MOE_FLAG_PAIR_L1 selects
+    weight-major tiles on CTA pairs (256 weight rows x up to 192 tokens) where the shape allows and
+    MOE_FLAG_WEIGHT_MAJOR one-CTA 128-weight-row x 128-token tiles. All compute the same block-scaled
+    products, so the combine rows and the output agree up to the fp32 summation order (within the
+    mode's tolerance), and the oracle bounds each."""
     inp = make_inputs(wl, device=DEV)
-    flags = (0, moe.MOE_FLAG_TOKEN_MAJOR, moe.MOE_FLAG_WEIGHT_MAJOR)
+    flags = (0, moe.MOE_FLAG_PAIR_L1, moe.MOE_FLAG_WEIGHT_MAJOR)
     outs = [run_forward(moe, wl, inp, flags=f, stages=True) for f in flags]
     assert all(o["status"] == 0 for o in outs)
     L = outs[0]["layout"]
@@ -490,14 +490,14 @@ PAIR_COUNTS = [1, 15, 16, 17, 95, 96, 97, 191, 192, 193, 383, 449]
 
 @pytest.mark.parametrize("mode", ["a8w4_fp8_fp4", "a8w8_fp8", "a8w8_fp8_e5m2"])
 def test_pair_tiles_at_token_count_edges(moe, mode):
-    """The CTA-pair weight-major kernel (both GEMMs: H 512, I 512) against the oracle and against the
-    token-major tiles with experts of 1 to 449 routed tokens."""
+    """The CTA-pair weight-major kernel (MOE_FLAG_PAIR_L1; both GEMMs: H 512, I 512) against the oracle
+    and against the token-major tiles with experts of 1 to 449 routed tokens."""
     wl = Workload(f"pair_edges_{mode}", mode, sum(PAIR_COUNTS), 512, 512, len(PAIR_COUNTS), 1, 77, 0.05)
     inp = make_inputs(wl, device=DEV)
     inp["topk_ids"] = torch.repeat_interleave(torch.arange(wl.E, dtype=torch.int32),
                                               torch.tensor(PAIR_COUNTS))[:, None].to(DEV).contiguous()
-    a = run_forward(moe, wl, inp, stages=True)
-    b = run_forward(moe, wl, inp, flags=moe.MOE_FLAG_TOKEN_MAJOR, stages=True)
+    a = run_forward(moe, wl, inp, flags=moe.MOE_FLAG_PAIR_L1, stages=True)
+    b = run_forward(moe, wl, inp, stages=True)
     assert a["status"] == 0 and b["status"] == 0
     check_plan(a, wl, inp["topk_ids"])
     ref, rec = oracle_forward(wl, inp, return_intermediates=True)
