@@ -32,6 +32,8 @@ METRIC = "fused MoE FFN TFLOP/s + routed rows/s, % of tensor/HBM roofline, 1xGB3
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 DTYPE = {"a16w16": "bf16", "a8w8_fp8": "e4m3", "a8w8_int8": "int8", "a8w4_fp8_fp4": "e4m3xe2m1", "a8w4_int": "int8xint4", "a8w8_fp8_e5m2": "e5m2"}
 LAUNCHES_PER_STEP = {"a16w16": 7, "a8w8_fp8": 7, "a8w8_int8": 8, "a8w4_fp8_fp4": 7, "a8w4_int": 8, "a8w8_fp8_e5m2": 7}
+# launches the fused launch replaces: A16W16 runs L1, L2 and the combine in it, the FP8 modes L1 and L2
+FUSED_SAVES = {"a16w16": 2}
 
 
 def parse():
@@ -53,7 +55,7 @@ def parse():
     ap.add_argument("--tokens", type=int, default=None, help="override the workload's token count")
     ap.add_argument("--experts", type=int, default=None, help="override the workload's expert count")
     ap.add_argument("--fused", action="store_true",
-                    help="S3-S5 in one launch (moe_expert_ffn; MOE_FLAG_FUSED end to end), bf16 only")
+                    help="S3-S5 in one launch (moe_expert_ffn; MOE_FLAG_FUSED end to end); A16W16 and FP8 modes")
     ap.add_argument("--quantize-x", action="store_true",
                     help="bf16 x in, quantised by the dispatch stage as the mode prescribes (MOE_FLAG_QUANTIZE_X)")
     return ap.parse_args()
@@ -85,7 +87,8 @@ def workload_config(wl, quantize_x=False, fused=False, flags=0):
     if quantize_x:
         cfg["x_input"] = "bf16, quantised by the dispatch stage"
     if fused:
-        cfg["gemm_launch"] = "L1, L2 and the combine in one cooperative launch (moe_expert_ffn)"
+        cfg["gemm_launch"] = ("L1, L2 and the combine in one cooperative launch (moe_expert_ffn)" if wl.mode == "a16w16"
+                              else "L1 and L2 in one cooperative launch, the combine after it (moe_expert_ffn)")
     if flags & 128:  # MOE_FLAG_PREPARED_WEIGHTS
         cfg["weights"] = ("prepared once, untimed, by moe_prepare_weights: every int8 code as its exact f16 value "
                           "(2 bytes per weight in HBM; MOE_FLAG_PREPARED_WEIGHTS)")
@@ -447,16 +450,27 @@ def step_roofline(wl, inp, step_ms, pk, pk_src, probe, sustained):
             "peak_source": src, "step_ms": step_ms}
 
 
-def fused_roofline(wl, ffn_ms, pk, pk_src, sustained):
-    """Roofline of the fused launch (L1 + SwiGLU + L2 + gate + combine): algorithmic flops 6*H*I
-    per routed row against the dense bf16 peak."""
+def fused_roofline(wl, inp, ffn_ms, pk, pk_src, probe, sustained):
+    """Roofline of the fused launch (moe_expert_ffn: L1 + SwiGLU + L2 + gate, and for A16W16 the combine).
+    Weight-streaming (decode) workloads: algorithmic bytes = W1 + W2 (+ block scales) of every expert with
+    N_e > 0, the x rows read and the bf16 combine rows written, against the measured HBM copy bandwidth.
+    Otherwise algorithmic flops 6*H*I per routed row against the dense peak of the mode's tensor pipe."""
+    kernel = ("L1 + SwiGLU + L2 + gate + combine in one launch (moe_expert_ffn)" if wl.mode == "a16w16"
+              else "L1 + SwiGLU + L2 + gate in one launch (moe_expert_ffn; the combine is a second launch)")
+    if is_decode(wl):
+        w_bytes, touched = touched_weight_bytes(wl, inp)
+        nbytes = w_bytes + wl.T * wl.H * X_BYTES_PER_ELEM[wl.mode] + wl.routed_rows * wl.H * 2
+        achieved = nbytes / (ffn_ms * 1e-3) / 1e9
+        peak = float(pk["hbm_gbs"])
+        return {"bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "peak_source": f"{pk_src} HBM copy", "ffn_ms": ffn_ms,
+                "algorithmic_bytes": nbytes, "experts_touched": touched,
+                "traffic": dominant_kernel_traffic(wl.name, "ffn_fused")}
     flops = 6.0 * wl.H * wl.I * wl.routed_rows
     achieved = flops / (ffn_ms * 1e-3) / 1e12
-    peak = float(pk["bf16_tflops_sustained"] if sustained else pk["bf16_tflops"])
-    clock = "sustained" if sustained else "burst"
-    return {"bound": "tensor", "kernel": "L1 + SwiGLU + L2 + gate + combine in one launch (moe_expert_ffn)",
-            "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-            "peak_source": f"{pk_src} bf16 dense, {clock}", "ffn_ms": ffn_ms,
+    peak, src = tensor_peak(wl, pk, pk_src, probe, sustained)
+    return {"bound": "tensor", "kernel": kernel, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "peak_source": src, "ffn_ms": ffn_ms, "algorithmic_flops": flops,
             "traffic": dominant_kernel_traffic(wl.name, "ffn_fused")}
 
 
@@ -645,7 +659,7 @@ def result_fields(args, wl, res, inp, world, pk, pk_src, probe, fused, quantize_
     flops = float(wl.flops)
     ms_per_step = res["elapsed_ms"] / args.steps
     sustained = is_sustained(res)
-    roof = (fused_roofline(wl, res["l1_ms"], pk, pk_src, sustained) if fused
+    roof = (fused_roofline(wl, inp, res["l1_ms"], pk, pk_src, probe, sustained) if fused
             else l1_roofline(wl, inp, res["l1_ms"], pk, pk_src, probe, sustained))
     return {
         "value": whole_job_tflops(flops, args.steps, res["elapsed_ms"], world), "unit": "TFLOP/s",
@@ -661,7 +675,7 @@ def result_fields(args, wl, res, inp, world, pk, pk_src, probe, fused, quantize_
                 "serial": {"value": whole_job_tflops(flops, args.steps, res["serial_ms"], world), "unit": "TFLOP/s",
                            "ms_per_step": res["serial_ms"] / args.steps,
                            "copies": "copy in, moe_forward, copy out, one after the other on one stream"}},
-        "gpu_launches": (LAUNCHES_PER_STEP[wl.mode] - (2 if fused else 0)) * args.steps,
+        "gpu_launches": (LAUNCHES_PER_STEP[wl.mode] - (FUSED_SAVES.get(wl.mode, 1) if fused else 0)) * args.steps,
         "clocks": res["clocks"],
     }
 
@@ -670,9 +684,12 @@ def result_fields(args, wl, res, inp, world, pk, pk_src, probe, fused, quantize_
 # and warm-up): (workload, GEMM flags, key in the line's "configs"), and the oracle's sample length for
 # their cpu_baseline. A8W8-INT runs on its int8 weights and, for comparison, on weights prepared once as
 # exact f16 codes (MOE_FLAG_PREPARED_WEIGHTS = 128; no cpu_baseline of its own: the same oracle sample).
+# FP8 x FP4 decode also runs L1 and L2 in one cooperative launch (MOE_FLAG_FUSED = 8, through moe_expert_ffn).
 OTHER_CONFIGS = (("tiny_bf16", 0, "tiny_bf16"), ("dsv3_fp8fp4_decode", 0, "dsv3_fp8fp4_decode"),
+                 ("dsv3_fp8fp4_decode", 8, "dsv3_fp8fp4_decode[fused L1+L2 launch]"),
                  ("dsv3_fp8fp4_prefill_zipf", 0, "dsv3_fp8fp4_prefill_zipf"), ("int8_a8w8", 0, "int8_a8w8"),
                  ("int8_a8w8", 128, "int8_a8w8[prepared f16 weights]"), ("int4_a8w4", 0, "int4_a8w4"))
+FLAG_FUSED = 8
 OTHER_CPU_SECONDS = 4.0
 
 
@@ -686,8 +703,8 @@ def run_gb300(args, wl, rank, world, local_rank):
     runs = [(wl, args.fused, args.quantize_x, args.flags, wl.name, True)]
     if args.configs == "all":
         from workloads import WORKLOADS
-        runs += [(WORKLOADS[n], False, False, f, key, not key.endswith("]")) for n, f, key in OTHER_CONFIGS
-                 if key != wl.name]
+        runs += [(WORKLOADS[n], bool(f & FLAG_FUSED), False, f & ~FLAG_FUSED, key, not key.endswith("]"))
+                 for n, f, key in OTHER_CONFIGS if key != wl.name]
     measured, failed = [], {}
     for i, (w, fused, qx, flags, key, want_cpu) in enumerate(runs):
         try:

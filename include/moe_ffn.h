@@ -131,10 +131,11 @@ enum {
                                    whatever the tile count (see MOE_FLAG_TOKEN_MAJOR); same bits */
     MOE_FLAG_QUANTIZE_X = 4u,   /* moe_forward: x.data is bf16 [T,H] (x.scale unused) and the
                                    dispatch stage quantises it as moe_dispatch_quantize does */
-    MOE_FLAG_FUSED = 8u,        /* moe_forward: S3-S6 through moe_expert_ffn (one launch: L1 -> L2 ->
-                                   combine dependency counters). A16W16 only; other modes return
-                                   MOE_ERR_UNSUPPORTED, and with MOE_FLAG_SIMT it is
-                                   MOE_ERR_INVALID_ARG. Same results as the separate stages. */
+    MOE_FLAG_FUSED = 8u,        /* moe_forward: S3-S6 through moe_expert_ffn (one launch with
+                                   L1 -> L2 dependency counters; A16W16 also combines in it). A16W16
+                                   and the FP8 modes; the integer modes return MOE_ERR_UNSUPPORTED,
+                                   and with MOE_FLAG_SIMT it is MOE_ERR_INVALID_ARG. Same results as
+                                   the separate stages (FP8: on weight-major tiles) bit for bit. */
     MOE_FLAG_SINGLE_CTA = 16u,  /* A16W16: the L2 GEMM on one-CTA 128-row tiles instead of CTA pairs
                                    (256-row tiles, tcgen05 cta_group::2); same results bit for bit,
                                    for comparison. The fused launch always uses one-CTA tiles. */
@@ -272,8 +273,13 @@ MOE_API moe_status moe_forward_ex(moe_operand x, const int32_t* topk_ids, const 
  * its rows has published them, so CTAs that finish their L2 tiles early combine while others
  * are still in L2. Every wait is bounded (on time-out MOE_ERR_TIMEOUT goes to the error word).
  * The results equal moe_expert_l1, moe_expert_l2 and moe_combine. Needs moe_dispatch first;
- * opt may be NULL (its flags are not used; the activation clamp applies). A16W16 with H a
- * multiple of 256 only: other modes and shapes return MOE_ERR_UNSUPPORTED before any launch.
+ * opt may be NULL (its flags are not used; the activation clamp applies).
+ * A16W16 needs H a multiple of 256. The FP8 modes (A8W8-FP8 e4m3 or e5m2, FP8 x FP4) run S3 and
+ * S4 on the weight-major block-scaled tiles in one launch (L2 tiles waiting on the same
+ * per-route-tile counters; at decode sizes 16-token sub-tiles, else 128-token ones) and S6 as a
+ * second launch when y is given; they need the shapes moe_expert_l1 and moe_expert_l2 accept on
+ * tensor cores (I a multiple of 64, H and I multiples of 128). The integer modes and other shapes
+ * return MOE_ERR_UNSUPPORTED before any launch.
  *   w1, w2, topk_weights  as for moe_expert_l1 and moe_expert_l2.
  *   y                     device bf16 [T,H] or NULL (then the combine rows stay in the
  *                         workspace for moe_combine). */

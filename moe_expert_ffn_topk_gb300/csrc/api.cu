@@ -295,7 +295,8 @@ moe_status moe_expert_ffn(moe_operand w1, moe_operand w2, const float* topk_weig
     uint32_t flags;
     if ((st = read_options(opt, &flags, &p.act_clamp)) != MOE_OK) return st;
     if (!operand_ok(w1, m != MOE_A16W16) || !operand_ok(w2, m != MOE_A16W16)) return MOE_ERR_INVALID_ARG;
-    if (!(tc_supported(p, 1) && tc_supported(p, 2))) return MOE_ERR_UNSUPPORTED;
+    const bool block_scaled = bs_supported(p, 1) && bs_supported(p, 2);
+    if (!(block_scaled || (tc_supported(p, 1) && tc_supported(p, 2)))) return MOE_ERR_UNSUPPORTED;
     if (d->num_tokens == 0) return MOE_OK;
     if (!topk_weights) return MOE_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -304,7 +305,12 @@ moe_status moe_expert_ffn(moe_operand w1, moe_operand w2, const float* topk_weig
         if (e != cudaSuccess) return from_cuda(e);
         topk_weights = p.gates;
     }
-    return from_cuda(launch_ffn_fused_tc(p, w1.data, w2.data, topk_weights, static_cast<uint16_t*>(y), s));
+    if (!block_scaled)
+        return from_cuda(launch_ffn_fused_tc(p, w1.data, w2.data, topk_weights, static_cast<uint16_t*>(y), s));
+    // FP8 modes: L1 and L2 in one launch, the combine after it
+    const cudaError_t e = launch_ffn_fused_bs(p, w1.data, w1.scale, w2.data, w2.scale, topk_weights, s);
+    if (e != cudaSuccess || !y) return from_cuda(e);
+    return from_cuda(launch_combine(p, static_cast<uint16_t*>(y), s));
 }
 
 moe_status moe_combine(void* y, const moe_dims* d, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
@@ -330,7 +336,8 @@ static moe_status forward(moe_operand x, const int32_t* topk_ids, const float* t
         return MOE_ERR_INVALID_ARG;
     const bool fused = (flags & MOE_FLAG_FUSED) != 0;
     if (fused && (flags & MOE_FLAG_SIMT)) return MOE_ERR_INVALID_ARG;
-    if (fused && !(tc_supported(p, 1) && tc_supported(p, 2))) return MOE_ERR_UNSUPPORTED;
+    if (fused && !((tc_supported(p, 1) && tc_supported(p, 2)) || (bs_supported(p, 1) && bs_supported(p, 2))))
+        return MOE_ERR_UNSUPPORTED;
     if ((st = moe_plan(topk_ids, d, nullptr, nullptr, nullptr, workspace, workspace_bytes, stream)) != MOE_OK) return st;
     st = quantize_x ? moe_dispatch_quantize(x.data, d, m, workspace, workspace_bytes, stream)
                     : moe_dispatch(x, d, m, workspace, workspace_bytes, stream);

@@ -126,6 +126,11 @@ cudaError_t launch_l1_bs(const Plan& p, const void* w1, const void* w1_scale, ui
 cudaError_t launch_l2_bs(const Plan& p, const void* w2, const void* w2_scale, const float* topk_weights,
                          uint32_t flags, cudaStream_t s);
 bool bs_supported(const Plan& p, int stage);
+// S3 and S4 of the FP8 modes in one cooperative launch of the weight-major block-scaled kernel:
+// L1 tiles first, L2 tiles after them, each L2 tile waiting (bounded) on a per-route-tile counter of
+// finished L1 tiles in p.ffn_counters; L2 writes comb, which the combine stage then reduces
+cudaError_t launch_ffn_fused_bs(const Plan& p, const void* w1, const void* w1_scale, const void* w2,
+                                const void* w2_scale, const float* topk_weights, cudaStream_t s);
 cudaError_t launch_l1_bs_tm(const Plan& p, const void* w1, const void* w1_scale, cudaStream_t s);
 cudaError_t launch_l2_bs_tm(const Plan& p, const void* w2, const void* w2_scale, const float* topk_weights,
                             cudaStream_t s);

@@ -81,7 +81,28 @@ struct BsArgs {
     const uint8_t* w_scale;     // UE8M0 [E*n_out][kin/32]
     const float* topk_weights;  // L2
     int n_slabs, k_blocks, n_out, kin;  // k_blocks = stages per tile; the last may hold one atom
+    // the fused launch (L1 then L2 in one launch): the fields above describe its L1, these its L2
+    const uint8_t* w_scale2;
+    int n_slabs2, k_blocks2, n_out2, kin2;
+    int32_t* l1_done;           // finished L1 tiles per 128-row route tile (zeroed before the launch)
+    int32_t* l1_total;          // finished L1 tiles of the whole launch (zeroed before the launch)
 };
+
+constexpr int kL2 = 0, kL1 = 1, kFusedL1L2 = 2;  // what one launch runs
+
+// Count of finished L1 tiles, read with acquire semantics at GPU scope.
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// A 32-bit load through the coherent path (data another CTA of the same launch wrote).
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const void* p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
 
 struct Tile {
     int e, s, row0, n_valid;
@@ -145,10 +166,12 @@ __device__ __forceinline__ bool epi_all(bool pred) {
     return r != 0;
 }
 
-template <int MODE, bool kL1, int kNT, int kStages, int kAtoms>
+template <int MODE, int kKind, int kNT, int kStages, int kAtoms>
 __global__ void __launch_bounds__(kThreads, 1)
-    tc_bs_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, BsArgs args) {
+    tc_bs_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                 const __grid_constant__ CUtensorMap tmW2, const __grid_constant__ CUtensorMap tmX2, BsArgs args) {
     using Cfg = BsCfg<kNT, kStages, kAtoms>;
+    constexpr bool kFused = kKind == kFusedL1L2;
     constexpr int kBK = kAtoms * kAtomK;  // K per stage
     constexpr bool kFp4 = MODE == MOE_A8W4_FP8_FP4;
     constexpr bool kE5 = MODE == MOE_A8W8_FP8_E5M2;  // e5m2 weights, tokens and A
@@ -214,24 +237,65 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
 
-    const int total = sub_off[p.E] * args.n_slabs;
-    const int KB = args.k_blocks;
+    // tiles [0, total1) are the launch's first stage (L1 when fused), [total1, total) the L2 ones
+    const int total1 = sub_off[p.E] * args.n_slabs;
+    const int total = kFused ? total1 + sub_off[p.E] * args.n_slabs2 : total1;
     const int I = p.I, H = p.H;
-    auto atoms_of = [&](int kb) { return min(kAtoms, (args.kin - kb * kBK) / kAtomK); };
-    auto tile_of = [&](int t) { return decode<kNT>(t, sub_off, tile_off, counts, p.E, args.n_slabs); };
+    auto is_l1 = [&](int t) { return kKind == kL1 || (kFused && t < total1); };
+    auto second = [&](int t) { return kFused && t >= total1; };  // an L2 tile of the fused launch
+    auto tile_of = [&](int t) {
+        return second(t) ? decode<kNT>(t - total1, sub_off, tile_off, counts, p.E, args.n_slabs2)
+                         : decode<kNT>(t, sub_off, tile_off, counts, p.E, args.n_slabs);
+    };
+    auto kin_of = [&](int t) { return second(t) ? args.kin2 : args.kin; };
+    auto kb_of = [&](int t) { return second(t) ? args.k_blocks2 : args.k_blocks; };
+    auto atoms_of = [&](int kb, int kin) { return min(kAtoms, (kin - kb * kBK) / kAtomK); };
     // first global weight row of each 64-row half of the tile
-    auto wrow = [&](const Tile& tl, int half) {
-        if (kL1) return tl.e * args.n_out + (half ? I : 0) + tl.s * kHalf;
-        return tl.e * args.n_out + tl.s * kWR + half * kHalf;
+    auto wrow = [&](const Tile& tl, int half, bool l1, int n_out) {
+        if (l1) return tl.e * n_out + (half ? I : 0) + tl.s * kHalf;
+        return tl.e * n_out + tl.s * kWR + half * kHalf;
+    };
+    auto nout_of = [&](int t) { return second(t) ? args.n_out2 : args.n_out; };
+    // fused launch: the route-tile counter an L2 tile of sub-tile row row0 waits on, and its target
+    // (every L1 weight slab of every sub-tile of that route tile)
+    auto dep_of = [&](const Tile& tl, int* target) {
+        const int m = (tl.row0 - tile_off[tl.e] * 128) / 128;
+        const int rows = min(128, counts[tl.e] - m * 128);
+        *target = (rows + kNT - 1) / kNT * args.n_slabs;
+        return args.l1_done + tile_off[tl.e] + m;
     };
 
     if (warp == 0) {
         // ---------------- TMA producer: weights (two 64-row boxes) and tokens ----------------
         if (lane == 0) {
             int it = 0;
-            bool ok = true;
+            bool ok = true, all_l1 = false;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 const Tile tl = tile_of(t);
+                const bool l1 = is_l1(t), sec = second(t);
+                const int KB = kb_of(t), kin = kin_of(t);
+                const CUtensorMap* mW = sec ? &tmW2 : &tmW;
+                const CUtensorMap* mX = sec ? &tmX2 : &tmX;
+                if (sec && !all_l1) {
+                    // every L1 tile of this route tile has published its A rows (bounded wait);
+                    // once every L1 tile of the launch has, no later L2 tile needs a check
+                    all_l1 = ld_acquire_gpu(args.l1_total) >= total1;
+                    int target;
+                    const int32_t* done = dep_of(tl, &target);
+                    const uint64_t t0 = globaltimer_ns();
+                    while (!all_l1 && ld_acquire_gpu(done) < target) {
+                        if (*abort_flag || globaltimer_ns() - t0 > kWaitTimeoutNs) {
+                            if (!*abort_flag) record_error(p.hdr, MOE_ERR_TIMEOUT);
+                            *abort_flag = 1;
+                            ok = false;
+                            break;
+                        }
+                        __nanosleep(64);
+                    }
+                    if (!ok) break;
+                    // those rows were written through the generic proxy; the TMA reads them
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                }
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int s = it % kStages;
                     if (!mbar_wait(empty_bar(s), ((uint32_t)(it / kStages) & 1u) ^ 1u, p.hdr, abort_flag)) {
@@ -239,15 +303,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     const uint32_t sa = base + s * Cfg::kStageBytes, sb = sa + kAtoms * kABytes;
-                    const int na = atoms_of(kb);
+                    const int na = atoms_of(kb, kin);
                     mbar_arrive_expect_tx(full_bar(s), (uint32_t)na * (2 * kABoxTx + (uint32_t)Cfg::kBBytes));
                     for (int at = 0; at < na; ++at) {
                         const int x = kb * kBK + at * kAtomK;
-                        if constexpr (kL1)
-                            tma_load_4d(sa + at * kABytes, &tmW, x, tl.s * kHalf, 0, tl.e, full_bar(s));
+                        if (l1)
+                            tma_load_4d(sa + at * kABytes, mW, x, tl.s * kHalf, 0, tl.e, full_bar(s));
                         else
-                            tma_load_2d(sa + at * kABytes, &tmW, x, wrow(tl, 0), full_bar(s));
-                        tma_load_2d(sb + at * Cfg::kBBytes, &tmX, x, tl.row0, full_bar(s));
+                            tma_load_2d(sa + at * kABytes, mW, x, wrow(tl, 0, false, nout_of(t)), full_bar(s));
+                        tma_load_2d(sb + at * Cfg::kBBytes, mX, x, tl.row0, full_bar(s));
                     }
                 }
             }
@@ -272,6 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const Tile tl = tile_of(t);
                 const int n = (tl.n_valid + 15) & ~15;
+                const int KB = kb_of(t), kin = kin_of(t);
                 const uint32_t d = tmem_base + (uint32_t)(a * kNT);
                 uint32_t idesc[kAtomK / 32];
 #pragma unroll
@@ -284,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     const uint64_t so = (uint64_t)((s * Cfg::kStageBytes) >> 4);
                     const uint32_t sf = tmem_base + kSfCol0 + s * kSfColsPerStage;
-                    const int na = atoms_of(kb);
+                    const int na = atoms_of(kb, kin);
                     for (int at = 0; at < na; ++at) {
                         const uint64_t ad = ad0 + so + (uint64_t)((at * kABytes) >> 4);
                         const uint64_t bd = bd0 + so + (uint64_t)((at * Cfg::kBBytes) >> 4);
@@ -310,51 +375,70 @@ __global__ void __launch_bounds__(kThreads, 1)
         // needed by all four warps (the MMA reads them in every lane quarter): each warp
         // publishes its group through shared memory, guarded by an mbarrier per buffer.
         const int q = warp & 3;  // lane quarter this warp writes
-        const int spr = args.kin / 32;
         const int r = 32 * q + lane;  // weight row within the tile
-        const int n_words = args.kin / kAtomK;  // scale words per row
-        const int n_blk = (n_words + 7) >> 3;
+        auto n_blk_of = [&](int t) { return (kin_of(t) / kAtomK + 7) >> 3; };  // 8-word blocks per row
         constexpr int kTokWords = Cfg::kTokWords;
         constexpr int kStagesPerBlk = 8 / kAtoms;
         const int cq = q % kTokWords;  // token group this warp loads
         uint32_t* tok_sf = reinterpret_cast<uint32_t*>(smem + Cfg::kTokSfOff);
         // Raw words only: nothing computed from a load happens before the block is used, so
-        // the loads stay in flight (addresses are clamped into the tensors instead of predicated)
+        // the loads stay in flight (addresses are clamped into the tensors instead of predicated).
+        // Fused launch: the token words of an L2 tile are A's scales, written by L1 tiles of this
+        // launch; they are loaded ahead only when the tile's L1 tiles are already counted, else
+        // the block is marked lazy and loaded when it is written out (never waiting ahead of work
+        // this CTA still owes).
         struct Blk {
             uint32_t a[8], b[8];
-            bool tok_valid;
+            bool tok_valid, lazy;
+        };
+        bool all_l1 = false;  // fused launch: every L1 tile of the launch seen finished
+        auto tok_ptr = [&](int t, const Tile& tl, int g) -> const uint32_t* {
+            const int n = 32 * cq + lane;
+            const int64_t row = tl.row0 + min(n, kNT - 1);  // a pool row of the sub-tile
+            if (is_l1(t)) {
+                if constexpr (kFp4) return reinterpret_cast<const uint32_t*>(p.x_pool_scale) + row * (H / 128) + g;
+                return reinterpret_cast<const uint32_t*>(p.x_pool_scale + row * (H / 32)) + g;
+            }
+            return reinterpret_cast<const uint32_t*>(p.a_pool_scale + row * (I / 32)) + g;
         };
         auto load_blk = [&](int t, int blk) {
             Blk w;
             const Tile tl = tile_of(t);
-            const int wr = wrow(tl, r >= kHalf) + (r & (kHalf - 1));
-            const uint32_t* ws = reinterpret_cast<const uint32_t*>(args.w_scale + (int64_t)wr * spr);
-            const int n = 32 * cq + lane;
-            w.tok_valid = n < tl.n_valid;
-            const int64_t row = tl.row0 + min(n, kNT - 1);  // a pool row of the sub-tile
+            const bool l1 = is_l1(t);
+            const int kin = kin_of(t), n_words = kin / kAtomK;
+            const int wr = wrow(tl, r >= kHalf, l1, nout_of(t)) + (r & (kHalf - 1));
+            const uint32_t* ws = reinterpret_cast<const uint32_t*>((second(t) ? args.w_scale2 : args.w_scale) +
+                                                                   (int64_t)wr * (kin / 32));
+            w.tok_valid = 32 * cq + lane < tl.n_valid;
+            w.lazy = false;
+            if (second(t) && !all_l1) {  // warp-uniform decisions: each lane loads after its own acquire
+                all_l1 = __all_sync(0xffffffffu, ld_acquire_gpu(args.l1_total) >= total1);
+                int target;
+                w.lazy = !all_l1 && !__all_sync(0xffffffffu, ld_acquire_gpu(dep_of(tl, &target)) >= target);
+            }
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int g = min(blk * 8 + i, n_words - 1);  // K atom: elements 128g .. 128g+127
                 w.a[i] = __ldg(ws + g);
-                if constexpr (kL1 && kFp4)
-                    w.b[i] = __float_as_uint(__ldg(reinterpret_cast<const float*>(p.x_pool_scale) + row * (H / 128) + g));
-                else if constexpr (kL1)
-                    w.b[i] = __ldg(reinterpret_cast<const uint32_t*>(p.x_pool_scale + row * (H / 32)) + g);
+                if (second(t))
+                    w.b[i] = w.lazy ? 0u : ld_relaxed_gpu(tok_ptr(t, tl, g));
+                else if (is_l1(t) && kFp4)
+                    w.b[i] = __float_as_uint(__ldg(reinterpret_cast<const float*>(tok_ptr(t, tl, g))));
                 else
-                    w.b[i] = __ldg(reinterpret_cast<const uint32_t*>(p.a_pool_scale + row * (I / 32)) + g);
+                    w.b[i] = __ldg(tok_ptr(t, tl, g));
             }
             return w;
         };
         // token word as the MMA reads it: 4 UE8M0 bytes; 1.0 for the padding tokens
-        auto tok_word = [&](const Blk& w, uint32_t raw) -> uint32_t {
+        auto tok_word = [&](const Blk& w, uint32_t raw, bool l1) -> uint32_t {
             if (!w.tok_valid) return 0x7f7f7f7fu;
-            if constexpr (kL1 && kFp4) return ((raw >> 23) & 0xffu) * 0x01010101u;  // power-of-two fp32 scale
+            if (kFp4 && l1) return ((raw >> 23) & 0xffu) * 0x01010101u;  // power-of-two fp32 scale
             return raw;
         };
         // (tile, block) positions in the producer's order: t0 is being written out, t1 and t2 are
         // in flight
         auto next_pos = [&](int& t, int& blk) {
-            if (++blk == n_blk) {
+            if (++blk == n_blk_of(t)) {
                 blk = 0;
                 t += gridDim.x;
             }
@@ -371,9 +455,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             next_pos(t2, b2);
             if (t2 < total) fill = load_blk(t2, b2);
             const int buf = nb & 1;
+            const bool l1 = is_l1(t0);
+            const int KB = kb_of(t0);
+            uint32_t ub[8];  // the block's token words (a lazy block loads them now)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ub[i] = use.b[i];
+            if (use.lazy) {
+                // every block before this one is written out: wait (bounded) for the tile's L1 tiles
+                const Tile tl = tile_of(t0);
+                int target;
+                const int32_t* done = dep_of(tl, &target);
+                const uint64_t w0 = globaltimer_ns();
+                bool d_ok = true;
+                while (ld_acquire_gpu(done) < target) {
+                    if (*abort_flag || globaltimer_ns() - w0 > kWaitTimeoutNs) {
+                        if (!*abort_flag) record_error(p.hdr, MOE_ERR_TIMEOUT);
+                        *abort_flag = 1;
+                        d_ok = false;
+                        break;
+                    }
+                    __nanosleep(64);
+                }
+                if (!__all_sync(0xffffffffu, d_ok)) return ok = false;
+                const int n_words = kin_of(t0) / kAtomK;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) ub[i] = ld_relaxed_gpu(tok_ptr(t0, tl, min(b0 * 8 + i, n_words - 1)));
+            }
             if constexpr (kTokWords > 1) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) tok_sf[((buf * kTokWords + cq) * 8 + i) * 32 + lane] = tok_word(use, use.b[i]);
+                for (int i = 0; i < 8; ++i) tok_sf[((buf * kTokWords + cq) * 8 + i) * 32 + lane] = tok_word(use, ub[i], l1);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(tok_bar(buf));
                 const bool t_ok = mbar_wait(tok_bar(buf), (uint32_t)(nb >> 1) & 1u, p.hdr, abort_flag);
@@ -385,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 wa[i] = use.a[i];
-                wb[i] = tok_word(use, use.b[i]);
+                wb[i] = tok_word(use, ub[i], l1);
             }
 #pragma unroll 1
             for (int j = 0; j < kStagesPerBlk; ++j) {
@@ -441,11 +551,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++tc) {
             const int a = tc & 1;
             const Tile tl = tile_of(t);
+            const bool l1 = is_l1(t);
             // L2: destination slot and gate weight of each row, read while the MMAs of this tile
             // still run (two dependent loads that would otherwise sit on the epilogue's path)
             int src_l[kChunks];
             float g_l[kChunks];
-            if constexpr (!kL1) {
+            if (!l1) {
 #pragma unroll
                 for (int ci = 0; ci < kChunks; ++ci) {
                     const int n = 32 * ci + lane;
@@ -459,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const int n = (tl.n_valid + 15) & ~15;
             const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * kNT);
-            if constexpr (kL1) {
+            if (l1) {
                 // lanes 0-63 hold the gate rows and lanes 64-127 the up rows of the same 64 outputs j.
                 // Of each 32-token chunk the gate warps finish tokens 0-15 and the up warps tokens
                 // 16-31; each hands its partner the other half through xbuf.
@@ -499,6 +610,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                         st_global_u8_if(lane < 16, p.a_pool_scale + (row0 + lane) * (I / 32) + (j >> 5), (uint8_t)my_sc);
                     }
                     epi_sync();
+                }
+                if (kFused) {
+                    // publish the tile's A rows and scales (an L2 tile's TMA reads the rows, its
+                    // scale writers the scales): every thread orders its own stores before the
+                    // async proxy's later reads and fences them, the four warps meet, and one thread
+                    // fences again and counts the tile for its route tile (no one waits here)
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                    __threadfence();
+                    epi_sync();
+                    if (q == 0 && lane == 0) {
+                        int target;
+                        __threadfence();
+                        atomicAdd(dep_of(tl, &target), 1);
+                        atomicAdd(args.l1_total, 1);
+                    }
                 }
             } else {
                 const int h = tl.s * kWR + q * 32 + lane;
@@ -543,66 +669,152 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_dealloc(tmem_base, 512);
 }
 
-template <int MODE, bool kL1, int kNT, int kStages, int kAtoms>
+template <int MODE, int kKind, int kNT, int kStages, int kAtoms>
+cudaError_t set_bs_smem_attr() {
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(tc_bs_kernel<MODE, kKind, kNT, kStages, kAtoms>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)BsCfg<kNT, kStages, kAtoms>::kSmem);
+    });
+    return attr_err;
+}
+
+// sub-tiles of kNT rows: at most one per routed row, and 128/kNT per 128-row route tile
+template <int kNT>
+int64_t max_sub_tiles(const Plan& p) {
+    return std::max<int64_t>(1, std::min<int64_t>((int64_t)p.T * p.K, (p.pool_rows / 128) * (128 / kNT)));
+}
+
+template <int MODE, int kKind, int kNT, int kStages, int kAtoms>
 cudaError_t launch_bs_cfg(const Plan& p, const CUtensorMap& tmW, const CUtensorMap& tmX, BsArgs args,
                           cudaStream_t s) {
     using Cfg = BsCfg<kNT, kStages, kAtoms>;
     args.k_blocks = (args.kin + kAtoms * kAtomK - 1) / (kAtoms * kAtomK);
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(tc_bs_kernel<MODE, kL1, kNT, kStages, kAtoms>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmem);
-    });
+    const cudaError_t attr_err = set_bs_smem_attr<MODE, kKind, kNT, kStages, kAtoms>();
     if (attr_err != cudaSuccess) return attr_err;
-    // sub-tiles: at most one per routed row, and one per 128-row tile times 128/kNT
-    const int64_t max_sub = std::min<int64_t>((int64_t)p.T * p.K, (p.pool_rows / 128) * (128 / kNT));
-    const int64_t max_tiles = std::max<int64_t>(1, max_sub) * args.n_slabs;
+    const int64_t max_tiles = max_sub_tiles<kNT>(p) * args.n_slabs;
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(max_tiles, tc_num_sms()));
-    tc_bs_kernel<MODE, kL1, kNT, kStages, kAtoms><<<grid, kThreads, Cfg::kSmem, s>>>(tmW, tmX, args);
+    tc_bs_kernel<MODE, kKind, kNT, kStages, kAtoms><<<grid, kThreads, Cfg::kSmem, s>>>(tmW, tmX, tmW, tmX, args);
     return cudaGetLastError();
 }
 
-template <int MODE, bool kL1>
-cudaError_t launch_bs(const Plan& p, const void* w, const void* w_scale, const float* topk_weights, uint32_t flags,
-                      cudaStream_t s) {
-    const bool weight_major = (flags & MOE_FLAG_WEIGHT_MAJOR) != 0;
-    const int n_out = kL1 ? 2 * p.I : p.H;
-    const int kin = kL1 ? p.H : p.I;
-    CUtensorMap tmW, tmX;
+// L1 then L2 in one cooperative launch: every CTA is resident, so an L2 tile waits (bounded) only
+// for L1 tiles that earlier positions of the same round-robin order hold, all of them running
+template <int MODE, int kNT, int kStages, int kAtoms>
+cudaError_t launch_bs_fused_cfg(const Plan& p, const CUtensorMap& tmW1, const CUtensorMap& tmX1,
+                                const CUtensorMap& tmW2, const CUtensorMap& tmX2, BsArgs args, cudaStream_t s) {
+    using Cfg = BsCfg<kNT, kStages, kAtoms>;
+    constexpr int kBK = kAtoms * kAtomK;
+    args.k_blocks = (args.kin + kBK - 1) / kBK;
+    args.k_blocks2 = (args.kin2 + kBK - 1) / kBK;
+    cudaError_t e = set_bs_smem_attr<MODE, kFusedL1L2, kNT, kStages, kAtoms>();
+    if (e != cudaSuccess) return e;
+    // the counters (one per 128-row route tile) start at zero every launch
+    // (the launch-wide count follows the route tiles' counts)
+    if ((e = cudaMemsetAsync(args.l1_done, 0, sizeof(int32_t) * (size_t)(p.pool_rows / 128 + 1), s)) != cudaSuccess)
+        return e;
+    int per_sm = 0;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tc_bs_kernel<MODE, kFusedL1L2, kNT, kStages, kAtoms>,
+                                                           kThreads, Cfg::kSmem)) != cudaSuccess)
+        return e;
+    if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
+    const int64_t max_tiles = max_sub_tiles<kNT>(p) * (args.n_slabs + args.n_slabs2);
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(max_tiles, (int64_t)tc_num_sms() * per_sm));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Cfg::kSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tc_bs_kernel<MODE, kFusedL1L2, kNT, kStages, kAtoms>, tmW1, tmX1, tmW2, tmX2, args);
+}
+
+// W1 as [K][row within the gate or up half][half][expert] (one box holds a tile's 64 gate and 64
+// up rows), W2 as [K][expert * H]; e2m1 weights packed two to a byte
+template <int MODE>
+bool make_w_map(CUtensorMap* m, const Plan& p, const void* w, bool l1) {
     constexpr bool kFp4 = MODE == MOE_A8W4_FP8_FP4;
     const CUtensorMapDataType wtype = kFp4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    const int kin = l1 ? p.H : p.I;
     const uint64_t pitch = kFp4 ? (uint64_t)kin / 2 : (uint64_t)kin;  // bytes per weight row
-    bool ok_w;
-    if (kL1) {
-        // [K][row within the gate or up half][half][expert]: one box holds a tile's 64 gate and 64 up rows
+    if (l1) {
         const uint64_t dims[4] = {(uint64_t)kin, (uint64_t)p.I, 2, (uint64_t)p.E};
         const uint64_t strides[3] = {pitch, pitch * p.I, pitch * 2 * p.I};
         const uint32_t box[4] = {kAtomK, kHalf, 2, 1};
-        ok_w = tc_make_map_nd(&tmW, wtype, 4, w, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
-    } else {
-        const uint64_t dims[2] = {(uint64_t)kin, (uint64_t)p.E * n_out};
-        const uint64_t strides[1] = {pitch};
-        const uint32_t box[2] = {kAtomK, kWR};
-        ok_w = tc_make_map_nd(&tmW, wtype, 2, w, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+        return tc_make_map_nd(m, wtype, 4, w, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
     }
-    if (!ok_w) return cudaErrorInvalidValue;
-    // few routed rows per expert: the weights stream from HBM; 16-token sub-tiles and K = 256
-    // stages (whole 128-byte lines of every weight row per load)
-    const bool decode = (int64_t)p.T * p.K <= (int64_t)16 * p.E;
+    const uint64_t dims[2] = {(uint64_t)kin, (uint64_t)p.E * p.H};
+    const uint64_t strides[1] = {pitch};
+    const uint32_t box[2] = {kAtomK, kWR};
+    return tc_make_map_nd(m, wtype, 2, w, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// token rows (x_pool for L1, a_pool for L2): one copy brings a sub-tile's rows
+bool make_x_map(CUtensorMap* m, const Plan& p, bool l1, int rows) {
+    return tc_make_map_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, l1 ? (const void*)p.x_pool : (const void*)p.a_pool,
+                          (uint64_t)(l1 ? p.H : p.I), (uint64_t)p.pool_rows, kAtomK, (uint32_t)rows,
+                          CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// few routed rows per expert: the weights stream from HBM; 16-token sub-tiles and K = 256 stages
+// (whole 128-byte lines of every weight row per load)
+bool is_decode(const Plan& p) { return (int64_t)p.T * p.K <= (int64_t)16 * p.E; }
+
+template <int MODE, bool kIsL1>
+cudaError_t launch_bs(const Plan& p, const void* w, const void* w_scale, const float* topk_weights, uint32_t flags,
+                      cudaStream_t s) {
+    const bool weight_major = (flags & MOE_FLAG_WEIGHT_MAJOR) != 0;
+    const bool decode = is_decode(p);
     // prefill sizes: token-major tiles, or with MOE_FLAG_PAIR_L1 weight-major tiles on CTA pairs (M = 256
     // weight rows, tokens as N; measured slower: Zipf prefill L1 2.48 against 1.50 ms)
-    if (!decode && !weight_major && (flags & MOE_FLAG_PAIR_L1) && bs_pair_supported(p, kL1 ? 1 : 2))
-        return kL1 ? launch_l1_bs_pair(p, w, w_scale, s) : launch_l2_bs_pair(p, w, w_scale, topk_weights, s);
-    if (!decode && !weight_major && bs_tm_supported(p, kL1 ? 1 : 2))
-        return kL1 ? launch_l1_bs_tm(p, w, w_scale, s) : launch_l2_bs_tm(p, w, w_scale, topk_weights, s);
-    // token rows: one copy brings the sub-tile's kNT pool rows
-    if (!tc_make_map_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kL1 ? (const void*)p.x_pool : (const void*)p.a_pool,
-                        (uint64_t)kin, (uint64_t)p.pool_rows, kAtomK, decode ? 16u : 128u, CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!decode && !weight_major && (flags & MOE_FLAG_PAIR_L1) && bs_pair_supported(p, kIsL1 ? 1 : 2))
+        return kIsL1 ? launch_l1_bs_pair(p, w, w_scale, s) : launch_l2_bs_pair(p, w, w_scale, topk_weights, s);
+    if (!decode && !weight_major && bs_tm_supported(p, kIsL1 ? 1 : 2))
+        return kIsL1 ? launch_l1_bs_tm(p, w, w_scale, s) : launch_l2_bs_tm(p, w, w_scale, topk_weights, s);
+    CUtensorMap tmW, tmX;
+    if (!make_w_map<MODE>(&tmW, p, w, kIsL1) || !make_x_map(&tmX, p, kIsL1, decode ? 16 : 128))
         return cudaErrorInvalidValue;
-    BsArgs args{p, static_cast<const uint8_t*>(w_scale), topk_weights, kL1 ? p.I / kHalf : p.H / kWR, 0, n_out, kin};
-    if (decode) return launch_bs_cfg<MODE, kL1, 16, 5, 2>(p, tmW, tmX, args, s);
-    return launch_bs_cfg<MODE, kL1, 128, 6, 1>(p, tmW, tmX, args, s);
+    BsArgs args{};
+    args.p = p;
+    args.w_scale = static_cast<const uint8_t*>(w_scale);
+    args.topk_weights = topk_weights;
+    args.n_slabs = kIsL1 ? p.I / kHalf : p.H / kWR;
+    args.n_out = kIsL1 ? 2 * p.I : p.H;
+    args.kin = kIsL1 ? p.H : p.I;
+    constexpr int kKind = kIsL1 ? kL1 : kL2;
+    if (decode) return launch_bs_cfg<MODE, kKind, 16, 5, 2>(p, tmW, tmX, args, s);
+    return launch_bs_cfg<MODE, kKind, 128, 6, 1>(p, tmW, tmX, args, s);
+}
+
+template <int MODE>
+cudaError_t launch_fused(const Plan& p, const void* w1, const void* w1_scale, const void* w2, const void* w2_scale,
+                         const float* topk_weights, cudaStream_t s) {
+    const bool decode = is_decode(p);
+    CUtensorMap tmW1, tmX1, tmW2, tmX2;
+    if (!make_w_map<MODE>(&tmW1, p, w1, true) || !make_x_map(&tmX1, p, true, decode ? 16 : 128) ||
+        !make_w_map<MODE>(&tmW2, p, w2, false) || !make_x_map(&tmX2, p, false, decode ? 16 : 128))
+        return cudaErrorInvalidValue;
+    BsArgs args{};
+    args.p = p;
+    args.w_scale = static_cast<const uint8_t*>(w1_scale);
+    args.topk_weights = topk_weights;
+    args.n_slabs = p.I / kHalf;
+    args.n_out = 2 * p.I;
+    args.kin = p.H;
+    args.w_scale2 = static_cast<const uint8_t*>(w2_scale);
+    args.n_slabs2 = p.H / kWR;
+    args.n_out2 = p.H;
+    args.kin2 = p.I;
+    args.l1_done = p.ffn_counters;
+    args.l1_total = p.ffn_counters + p.pool_rows / 128;
+    if (decode) return launch_bs_fused_cfg<MODE, 16, 5, 2>(p, tmW1, tmX1, tmW2, tmX2, args, s);
+    return launch_bs_fused_cfg<MODE, 128, 6, 1>(p, tmW1, tmX1, tmW2, tmX2, args, s);
 }
 
 }  // namespace
@@ -627,6 +839,15 @@ cudaError_t launch_l2_bs(const Plan& p, const void* w2, const void* w2_scale, co
     if (p.mode == MOE_A8W4_FP8_FP4) return launch_bs<MOE_A8W4_FP8_FP4, false>(p, w2, w2_scale, topk_weights, flags, s);
     if (p.mode == MOE_A8W8_FP8) return launch_bs<MOE_A8W8_FP8, false>(p, w2, w2_scale, topk_weights, flags, s);
     if (p.mode == MOE_A8W8_FP8_E5M2) return launch_bs<MOE_A8W8_FP8_E5M2, false>(p, w2, w2_scale, topk_weights, flags, s);
+    return cudaErrorNotSupported;
+}
+
+cudaError_t launch_ffn_fused_bs(const Plan& p, const void* w1, const void* w1_scale, const void* w2,
+                                const void* w2_scale, const float* topk_weights, cudaStream_t s) {
+    if (p.mode == MOE_A8W4_FP8_FP4) return launch_fused<MOE_A8W4_FP8_FP4>(p, w1, w1_scale, w2, w2_scale, topk_weights, s);
+    if (p.mode == MOE_A8W8_FP8) return launch_fused<MOE_A8W8_FP8>(p, w1, w1_scale, w2, w2_scale, topk_weights, s);
+    if (p.mode == MOE_A8W8_FP8_E5M2)
+        return launch_fused<MOE_A8W8_FP8_E5M2>(p, w1, w1_scale, w2, w2_scale, topk_weights, s);
     return cudaErrorNotSupported;
 }
 

@@ -811,8 +811,85 @@ def test_fused_with_clamp_shared_experts_and_quantizing_dispatch(moe):
     assert_close(y_numpy(y1), ref, wl.mode)
 
 
+# FP8 modes: L1 and L2 in one cooperative launch of the weight-major block-scaled kernel (the
+# combine after it), so the output equals the separate stages on weight-major tiles bit for bit.
+# Decode-shaped cases (at most 16 routed rows per expert on average) run 16-token sub-tiles, the
+# others 128-token ones; several route tiles per expert, ragged last sub-tiles, masked routes and
+# empty experts are all exercised.
+FUSED_BS_CASES = [w for m in ("a8w8_fp8", "a8w8_fp8_e5m2", "a8w4_fp8_fp4") for w in CASES[m]] + [
+    w for w in EDGE if w.mode in ("a8w8_fp8", "a8w4_fp8_fp4")] + [
+    Workload("fused_bs_one_expert_all_rows", "a8w4_fp8_fp4", 700, 512, 384, 3, 1, 53, 0.05),
+    Workload("fused_bs_decode_deep_expert", "a8w4_fp8_fp4", 200, 512, 512, 16, 1, 54, 0.05),
+    Workload("fused_bs_decode_e4m3", "a8w8_fp8", 96, 1024, 256, 64, 8, 55, 0.05)]
+
+
+def _fused_bs_ids(wl, inp):
+    if wl.name == "fused_bs_one_expert_all_rows":
+        inp["topk_ids"][:] = 1          # 700 rows on one expert: 6 route tiles, the last ragged
+        inp["topk_ids"][::7] = -1       # and some masked routes
+    elif wl.name == "fused_bs_decode_deep_expert":
+        inp["topk_ids"][:150] = 0       # 150 rows on expert 0: route tiles of 128 and 22 rows
+        inp["topk_ids"][150:] = torch.arange(50, device=inp["topk_ids"].device).view(50, 1) % 15 + 1
+    return inp
+
+
+@pytest.mark.parametrize("wl", FUSED_BS_CASES, ids=[w.name for w in FUSED_BS_CASES])
+def test_fused_block_scaled_equals_the_separate_stages(moe, wl):
+    inp = _fused_bs_ids(wl, make_inputs(wl, device=DEV))
+    assert moe.MOE_FLAG_FUSED & moe.MOE_FLAG_WEIGHT_MAJOR == 0
+    y0, st0 = _forward_flags(moe, wl, inp, moe.MOE_FLAG_WEIGHT_MAJOR)
+    y1, st1 = _forward_flags(moe, wl, inp, moe.MOE_FLAG_FUSED)
+    assert st0 == 0 and st1 == 0
+    assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
+    assert_close(y_numpy(y1), oracle_forward(wl, inp), wl.mode)
+
+
+def test_fused_block_scaled_shared_experts_clamp_and_quantizing_dispatch(moe):
+    wl = CASES["a8w4_fp8_fp4"][1]
+    inp = make_inputs(wl, device=DEV, shared=1)
+    for flags in (0, moe.MOE_FLAG_QUANTIZE_X):
+        x = inp["x_bf16"] if flags else None
+        y0, st0 = _forward_flags(moe, wl, inp, flags | moe.MOE_FLAG_WEIGHT_MAJOR, shared=1, clamp=0.5, x=x)
+        y1, st1 = _forward_flags(moe, wl, inp, flags | moe.MOE_FLAG_FUSED, shared=1, clamp=0.5, x=x)
+        assert st0 == 0 and st1 == 0
+        assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
+    h = to_numpy(inp)
+    ref = omoe.forward(wl.mode, h["x"], h["x_scale"], h["topk_ids"], h["topk_weights"], h["w1"], h["w1_scale"],
+                       h["w2"], h["w2_scale"], num_experts=wl.E, inter=wl.I, num_shared=1, clamp=0.5)
+    assert_close(y_numpy(y1), ref, wl.mode)
+
+
+def test_fused_block_scaled_without_y_leaves_the_combine_rows(moe):
+    wl = CASES["a8w8_fp8"][1]
+    inp = make_inputs(wl, device=DEV)
+    y_ref, st = _forward_flags(moe, wl, inp, moe.MOE_FLAG_WEIGHT_MAJOR)
+    assert st == 0
+    d = moe.dims(wl.T, wl.H, wl.I, wl.E, wl.K)
+    for with_y in (False, True):
+        ws = moe.alloc_workspace(d, wl.mode, DEV)
+        y = torch.full((wl.T, wl.H), float("nan"), dtype=torch.bfloat16, device=DEV)
+        moe.moe_plan(inp["topk_ids"], d, ws)
+        moe.moe_dispatch(inp["x"], inp["x_scale"], d, wl.mode, ws)
+        moe.moe_expert_ffn(inp["w1"], inp["w1_scale"], inp["w2"], inp["w2_scale"], inp["topk_weights"], d, wl.mode, ws,
+                           y=y if with_y else None)
+        if not with_y:
+            moe.moe_combine(y, d, ws)
+        assert moe.moe_check_device_error(ws) == 0
+        assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16)), with_y
+
+
+@pytest.mark.parametrize("name", ["dsv3_fp8fp4_decode", "dsv3_fp8fp4_prefill_zipf"])
+def test_fused_block_scaled_full_size_equals_the_separate_stages(moe, name):
+    wl = WORKLOADS[name]
+    inp = make_inputs(wl, device=DEV)
+    y0, st0 = _forward_flags(moe, wl, inp, moe.MOE_FLAG_WEIGHT_MAJOR)
+    y1, st1 = _forward_flags(moe, wl, inp, moe.MOE_FLAG_FUSED)
+    assert st0 == 0 and st1 == 0
+    assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
+
+
 def test_fused_flag_rejections(moe):
-    wl = CASES["a8w8_fp8"][0]
+    wl = CASES["a8w8_int8"][0]
     inp = make_inputs(wl, device=DEV)
     with pytest.raises(moe.MoeError) as err:
         _forward_flags(moe, wl, inp, moe.MOE_FLAG_FUSED)
