@@ -684,11 +684,14 @@ def result_fields(args, wl, res, inp, world, pk, pk_src, probe, fused, quantize_
 # and warm-up): (workload, GEMM flags, key in the line's "configs"), and the oracle's sample length for
 # their cpu_baseline. A8W8-INT runs on its int8 weights and, for comparison, on weights prepared once as
 # exact f16 codes (MOE_FLAG_PREPARED_WEIGHTS = 128; no cpu_baseline of its own: the same oracle sample).
-# FP8 x FP4 decode also runs L1 and L2 in one cooperative launch (MOE_FLAG_FUSED = 8, through moe_expert_ffn).
+# FP8 x FP4 decode and the integer modes also run L1 and L2 in one cooperative launch (MOE_FLAG_FUSED = 8,
+# through moe_expert_ffn).
 OTHER_CONFIGS = (("tiny_bf16", 0, "tiny_bf16"), ("dsv3_fp8fp4_decode", 0, "dsv3_fp8fp4_decode"),
                  ("dsv3_fp8fp4_decode", 8, "dsv3_fp8fp4_decode[fused L1+L2 launch]"),
                  ("dsv3_fp8fp4_prefill_zipf", 0, "dsv3_fp8fp4_prefill_zipf"), ("int8_a8w8", 0, "int8_a8w8"),
-                 ("int8_a8w8", 128, "int8_a8w8[prepared f16 weights]"), ("int4_a8w4", 0, "int4_a8w4"))
+                 ("int8_a8w8", 128, "int8_a8w8[prepared f16 weights]"),
+                 ("int8_a8w8", 8, "int8_a8w8[fused L1+L2 launch]"), ("int4_a8w4", 0, "int4_a8w4"),
+                 ("int4_a8w4", 8, "int4_a8w4[fused L1+L2 launch]"))
 FLAG_FUSED = 8
 OTHER_CPU_SECONDS = 4.0
 

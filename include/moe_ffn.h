@@ -132,10 +132,11 @@ enum {
     MOE_FLAG_QUANTIZE_X = 4u,   /* moe_forward: x.data is bf16 [T,H] (x.scale unused) and the
                                    dispatch stage quantises it as moe_dispatch_quantize does */
     MOE_FLAG_FUSED = 8u,        /* moe_forward: S3-S6 through moe_expert_ffn (one launch with
-                                   L1 -> L2 dependency counters; A16W16 also combines in it). A16W16
-                                   and the FP8 modes; the integer modes return MOE_ERR_UNSUPPORTED,
-                                   and with MOE_FLAG_SIMT it is MOE_ERR_INVALID_ARG. Same results as
-                                   the separate stages (FP8: on weight-major tiles) bit for bit. */
+                                   L1 -> L2 dependency counters; A16W16 also combines in it). Every
+                                   mode, on the shapes moe_expert_ffn lists (else
+                                   MOE_ERR_UNSUPPORTED); with MOE_FLAG_SIMT it is
+                                   MOE_ERR_INVALID_ARG. Same results as the separate stages (FP8 and
+                                   A8W4-INT: on weight-major tiles) bit for bit. */
     MOE_FLAG_SINGLE_CTA = 16u,  /* A16W16: the L2 GEMM on one-CTA 128-row tiles instead of CTA pairs
                                    (256-row tiles, tcgen05 cta_group::2); same results bit for bit,
                                    for comparison. The fused launch always uses one-CTA tiles. */
@@ -273,13 +274,18 @@ MOE_API moe_status moe_forward_ex(moe_operand x, const int32_t* topk_ids, const 
  * its rows has published them, so CTAs that finish their L2 tiles early combine while others
  * are still in L2. Every wait is bounded (on time-out MOE_ERR_TIMEOUT goes to the error word).
  * The results equal moe_expert_l1, moe_expert_l2 and moe_combine. Needs moe_dispatch first;
- * opt may be NULL (its flags are not used; the activation clamp applies).
+ * opt may be NULL (of its flags only MOE_FLAG_PREPARED_WEIGHTS is read; the activation clamp
+ * applies).
  * A16W16 needs H a multiple of 256. The FP8 modes (A8W8-FP8 e4m3 or e5m2, FP8 x FP4) run S3 and
  * S4 on the weight-major block-scaled tiles in one launch (L2 tiles waiting on the same
  * per-route-tile counters; at decode sizes 16-token sub-tiles, else 128-token ones) and S6 as a
- * second launch when y is given; they need the shapes moe_expert_l1 and moe_expert_l2 accept on
- * tensor cores (I a multiple of 64, H and I multiples of 128). The integer modes and other shapes
- * return MOE_ERR_UNSUPPORTED before any launch.
+ * second launch when y is given; they need I a multiple of 64 and H and I multiples of 128. The
+ * integer modes (A8W8-INT, A8W4-INT on weight-major tiles) run S3, the per-row re-quantisation
+ * of A and S4 in one launch: the last L1 tile of each 128-row route tile to finish re-quantises
+ * that route tile's rows, and its L2 tiles wait for that; S6 follows as a second launch. They
+ * need I a multiple of 128, H a multiple of 256 and H, I <= 8704; A8W8-INT also takes weights
+ * from moe_prepare_weights with MOE_FLAG_PREPARED_WEIGHTS in opt. Other shapes, and prepared
+ * weights in another mode, return MOE_ERR_UNSUPPORTED before any launch.
  *   w1, w2, topk_weights  as for moe_expert_l1 and moe_expert_l2.
  *   y                     device bf16 [T,H] or NULL (then the combine rows stay in the
  *                         workspace for moe_combine). */
@@ -324,8 +330,12 @@ typedef struct {
     size_t pool_sums;     /* A8W4-INT: int32 [2][pool_rows], the sum of each pool row's codes:
                              x rows, then A rows (other modes: size 0) */
     size_t comb;          /* bf16 [T*K, H] weighted rows */
-    size_t ffn_counters;  /* int32 [pool_rows/128 + T]: moe_expert_ffn's counts of finished L1 tiles
-                             per 128-row route tile, then of finished combine rows per token */
+    size_t ffn_counters;  /* int32 [5 * pool_rows/128 + 3 + T]: moe_expert_ffn's counters. Per
+                             128-row route tile the finished L1 tiles; then A16W16: per token the
+                             finished combine rows; FP8 modes: the launch's finished L1 tiles;
+                             integer modes (each route tile also counts its finished
+                             re-quantisation jobs): jobs finished, queue head, queue tail and
+                             4 job slots per route tile */
     size_t total;         /* = moe_workspace_bytes() */
     int64_t pool_rows;    /* rows reserved in each pool */
 } moe_workspace_layout_t;

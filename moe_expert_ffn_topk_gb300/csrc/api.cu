@@ -79,7 +79,7 @@ moe_status layout(const moe_dims* d, moe_dtype_mode m, moe_workspace_layout_t* o
     L.slot_row = take(sizeof(int32_t) * R);
     L.gates = take(S ? sizeof(float) * R : 0);
     L.comb = take((size_t)R * H * 2);
-    L.ffn_counters = take(sizeof(int32_t) * (size_t)(pool_rows / kTileRows + T));
+    L.ffn_counters = take(sizeof(int32_t) * (size_t)ffn_counter_ints(pool_rows / kTileRows, T));
     // everything above is the same for every mode; the pools below depend on it
     L.x_pool = take((size_t)pool_rows * H * x_elem_bytes(m));
     L.x_pool_scale = take((size_t)pool_rows * x_scale_row_bytes(m, (int)H));
@@ -295,8 +295,12 @@ moe_status moe_expert_ffn(moe_operand w1, moe_operand w2, const float* topk_weig
     uint32_t flags;
     if ((st = read_options(opt, &flags, &p.act_clamp)) != MOE_OK) return st;
     if (!operand_ok(w1, m != MOE_A16W16) || !operand_ok(w2, m != MOE_A16W16)) return MOE_ERR_INVALID_ARG;
+    const bool prepared = (flags & MOE_FLAG_PREPARED_WEIGHTS) != 0;
+    const bool bf16 = tc_supported(p, 1) && tc_supported(p, 2);
     const bool block_scaled = bs_supported(p, 1) && bs_supported(p, 2);
-    if (!(block_scaled || (tc_supported(p, 1) && tc_supported(p, 2)))) return MOE_ERR_UNSUPPORTED;
+    const bool int8 = int8_tc_supported(p, 1) && int8_tc_supported(p, 2);
+    const bool w4 = w4_wm_supported(p, 1) && w4_wm_supported(p, 2);
+    if (!(bf16 || block_scaled || int8 || w4) || (prepared && !int8)) return MOE_ERR_UNSUPPORTED;
     if (d->num_tokens == 0) return MOE_OK;
     if (!topk_weights) return MOE_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -305,10 +309,13 @@ moe_status moe_expert_ffn(moe_operand w1, moe_operand w2, const float* topk_weig
         if (e != cudaSuccess) return from_cuda(e);
         topk_weights = p.gates;
     }
-    if (!block_scaled)
-        return from_cuda(launch_ffn_fused_tc(p, w1.data, w2.data, topk_weights, static_cast<uint16_t*>(y), s));
-    // FP8 modes: L1 and L2 in one launch, the combine after it
-    const cudaError_t e = launch_ffn_fused_bs(p, w1.data, w1.scale, w2.data, w2.scale, topk_weights, s);
+    if (bf16) return from_cuda(launch_ffn_fused_tc(p, w1.data, w2.data, topk_weights, static_cast<uint16_t*>(y), s));
+    // FP8 and integer modes: L1 and L2 in one launch (the integer modes re-quantise A inside it),
+    // the combine after it
+    const cudaError_t e =
+        block_scaled ? launch_ffn_fused_bs(p, w1.data, w1.scale, w2.data, w2.scale, topk_weights, s)
+        : int8       ? launch_ffn_fused_int8(p, w1.data, w1.scale, w2.data, w2.scale, topk_weights, prepared, s)
+                     : launch_ffn_fused_w4_wm(p, w1.data, w1.scale, w2.data, w2.scale, topk_weights, s);
     if (e != cudaSuccess || !y) return from_cuda(e);
     return from_cuda(launch_combine(p, static_cast<uint16_t*>(y), s));
 }
@@ -336,7 +343,9 @@ static moe_status forward(moe_operand x, const int32_t* topk_ids, const float* t
         return MOE_ERR_INVALID_ARG;
     const bool fused = (flags & MOE_FLAG_FUSED) != 0;
     if (fused && (flags & MOE_FLAG_SIMT)) return MOE_ERR_INVALID_ARG;
-    if (fused && !((tc_supported(p, 1) && tc_supported(p, 2)) || (bs_supported(p, 1) && bs_supported(p, 2))))
+    if (fused && !((tc_supported(p, 1) && tc_supported(p, 2)) || (bs_supported(p, 1) && bs_supported(p, 2)) ||
+                   (int8_tc_supported(p, 1) && int8_tc_supported(p, 2)) ||
+                   (w4_wm_supported(p, 1) && w4_wm_supported(p, 2))))
         return MOE_ERR_UNSUPPORTED;
     if ((st = moe_plan(topk_ids, d, nullptr, nullptr, nullptr, workspace, workspace_bytes, stream)) != MOE_OK) return st;
     st = quantize_x ? moe_dispatch_quantize(x.data, d, m, workspace, workspace_bytes, stream)

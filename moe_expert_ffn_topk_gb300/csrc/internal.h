@@ -15,6 +15,12 @@ constexpr int kHdrRows = 1;
 constexpr int kHdrPadRows = 2;
 constexpr int kHdrTiles = 3;
 constexpr int kHdrWaitFlag = 8;         // a flag that nothing sets (bounded-wait test hook)
+// moe_expert_ffn of the integer modes: re-quantisation jobs per 128-row route tile, and the int32
+// counters its launch uses (per route tile, then the job queue: jobs finished, head, tail, a slot
+// per job); the workspace's ffn_counters region holds the largest need of any mode
+constexpr int kQuantJobs = 4;
+constexpr long long fused_int_counters(long long route_tiles) { return route_tiles * (1 + kQuantJobs) + 3; }
+constexpr long long ffn_counter_ints(long long route_tiles, long long T) { return fused_int_counters(route_tiles) + T; }
 
 // The integer modes (int8 activations, fp32 per-token / per-channel scales) and the number of
 // f16 operand planes their tensor-core GEMMs read: the int8 codes as hi = floor(q/16) and
@@ -99,6 +105,12 @@ cudaError_t launch_l1_int8_tc(const Plan& p, const void* w1, const void* w1_scal
 cudaError_t launch_l2_int8_tc(const Plan& p, const void* w2, const void* w2_scale, const float* topk_weights,
                               bool prepared, cudaStream_t s);
 // int8 codes [n] -> the same values as f16 [n] (n a multiple of 16)
+// S3 and S4 of the integer modes in one cooperative launch (weight-major tiles): each route tile's
+// last L1 tile re-quantises its rows of A (quant_a_row) before its L2 tiles start
+cudaError_t launch_ffn_fused_int8(const Plan& p, const void* w1, const void* w1_scale, const void* w2,
+                                  const void* w2_scale, const float* topk_weights, bool prepared, cudaStream_t s);
+cudaError_t launch_ffn_fused_w4_wm(const Plan& p, const void* w1, const void* w1_scale, const void* w2,
+                                   const void* w2_scale, const float* topk_weights, cudaStream_t s);
 cudaError_t launch_prepare_int8(const void* w, void* out, int64_t n, cudaStream_t s);
 bool int8_tc_supported(const Plan& p, int stage);
 

@@ -242,69 +242,14 @@ __global__ void __launch_bounds__(NT) l2_simt_kernel(Plan p, const uint8_t* __re
     }
 }
 
-// Integer modes, Linear2 step (1) of the A8W8-INT and A8W4-INT use cases: s = max|A[row,:]|/127
-// (floored at 1e-8), q = round-half-even(A/s) clamped to [-127, 127]; fp32 IEEE division
-// throughout. Besides the int8 codes it writes the tensor-core operand planes: hi and lo for
-// INT8; for A8W4-INT the codes as f16 in the order of w4_plane_pos, and the row's code sum.
-// One warp per row: the amax and the code sum are warp reductions (no block barrier), and the
-// second pass re-reads the row, which the first pass left in L1.
+// Integer modes, Linear2 step (1) of the A8W8-INT and A8W4-INT use cases (quant_a_row): one warp
+// per pool row, 64 rows in flight per SM.
 constexpr int kRqWarps = 8;
 __global__ void __launch_bounds__(32 * kRqWarps) int8_row_quant_kernel(Plan p) {
     const int rows = p.hdr[kHdrPadRows];
-    const int I = p.I, nv = p.I / 4;  // float4 vectors of a row (a multiple of 32)
     const int lane = threadIdx.x & 31;
-    const bool split = p.mode == MOE_A8W8_INT8;  // A8W4-INT: plane 0 holds q itself
-    for (int r = blockIdx.x * kRqWarps + (threadIdx.x >> 5); r < rows; r += gridDim.x * kRqWarps) {
-        if (debug_row(p.hdr, __ldg(p.pool_src + r), (int64_t)p.T * p.K) < 0) continue;  // padding row (uniform across the warp): never read back
-        const float4* a = reinterpret_cast<const float4*>(p.a_f32 + (int64_t)r * I);
-        float m = 0.0f;
-        for (int v = lane; v < nv; v += 32) {
-            const float4 x = a[v];
-            m = fmaxf(m, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
-        }
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        const float s = fmaxf(__fdiv_rn(m, 127.0f), 1e-8f);
-        uint32_t* q = reinterpret_cast<uint32_t*>(p.a_pool + (int64_t)r * I);   // 4 codes per word
-        uint2* hi = reinterpret_cast<uint2*>(p.a_planes + (int64_t)r * I);      // plane 0: floor(q/16), f16
-        uint2* lo = reinterpret_cast<uint2*>(p.a_planes + (p.pool_rows + r) * I);  // plane 1: q mod 16, f16
-        int code_sum = 0;
-        // lanes 2m and 2m + 1 hold the two halves of a group of 8 codes together
-        for (int v = lane; v < nv; v += 32) {
-            const float4 x = a[v];
-            const float xv[4] = {x.x, x.y, x.z, x.w};
-            uint32_t qw = 0, h[2] = {0, 0}, l[2] = {0, 0};
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                float t = rintf(__fdiv_rn(xv[c], s));
-                t = fminf(fmaxf(t, -127.0f), 127.0f);
-                const int qi = static_cast<int>(t);
-                qw |= (uint32_t)(qi & 0xff) << (8 * c);
-                h[c >> 1] |= (uint32_t)float_to_f16_bits((float)(split ? qi >> 4 : qi)) << (16 * (c & 1));
-                l[c >> 1] |= (uint32_t)float_to_f16_bits((float)(qi & 15)) << (16 * (c & 1));
-            }
-            q[v] = qw;
-            if (split) {
-                hi[v] = make_uint2(h[0], h[1]);
-                lo[v] = make_uint2(l[0], l[1]);
-            } else {
-                // q0 q4 q1 q5 from the even lane of the pair, q2 q6 q3 q7 from the odd one
-                const bool odd = lane & 1;
-                const uint32_t got = __shfl_xor_sync(0xffffffffu, odd ? h[0] : h[1], 1);
-                const uint32_t mine = odd ? h[1] : h[0];
-                hi[v] = odd ? make_uint2((got & 0xffffu) | (mine << 16), (got >> 16) | (mine & 0xffff0000u))
-                            : make_uint2((mine & 0xffffu) | (got << 16), (mine >> 16) | (got & 0xffff0000u));
-                code_sum += (int)(int8_t)(qw & 0xff) + (int)(int8_t)((qw >> 8) & 0xff) +
-                            (int)(int8_t)((qw >> 16) & 0xff) + (int)(int8_t)(qw >> 24);
-            }
-        }
-        if (lane == 0) reinterpret_cast<float*>(p.a_pool_scale)[r] = s;
-        if (!split) {
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) code_sum += __shfl_xor_sync(0xffffffffu, code_sum, o);
-            if (lane == 0) p.a_sums[r] = code_sum;
-        }
-    }
+    for (int r = blockIdx.x * kRqWarps + (threadIdx.x >> 5); r < rows; r += gridDim.x * kRqWarps)
+        quant_a_row<false, 16>(p, r, lane);
 }
 
 template <int MODE>

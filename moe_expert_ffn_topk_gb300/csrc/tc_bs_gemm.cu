@@ -90,20 +90,6 @@ struct BsArgs {
 
 constexpr int kL2 = 0, kL1 = 1, kFusedL1L2 = 2;  // what one launch runs
 
-// Count of finished L1 tiles, read with acquire semantics at GPU scope.
-__device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-// A 32-bit load through the coherent path (data another CTA of the same launch wrote).
-__device__ __forceinline__ uint32_t ld_relaxed_gpu(const void* p) {
-    uint32_t v;
-    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
 struct Tile {
     int e, s, row0, n_valid;
 };
@@ -153,18 +139,10 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, uint32_t a0, uint32_t a
                  "r"(a1), "r"(a2), "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
                  : "memory");
 }
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync %0, 128;" ::"n"(kEpiBar) : "memory"); }
+__device__ __forceinline__ void epi_sync() { bar_sync128<kEpiBar>(); }
 // The same barrier, ANDing `pred` over the four epilogue warps: they leave the tile loop together,
 // since a warp that left alone would keep the others waiting at the next epi_sync.
-__device__ __forceinline__ bool epi_all(bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %1, 0;\n\tbar.red.and.pred q, %2, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"((int)pred), "n"(kEpiBar)
-        : "memory");
-    return r != 0;
-}
+__device__ __forceinline__ bool epi_all(bool pred) { return bar_all128<kEpiBar>(pred); }
 
 template <int MODE, int kKind, int kNT, int kStages, int kAtoms>
 __global__ void __launch_bounds__(kThreads, 1)

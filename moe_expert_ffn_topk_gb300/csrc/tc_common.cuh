@@ -284,7 +284,155 @@ __device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity, int32_
     return true;
 }
 
+// ---------------------------------------------------------------------------------------
+// Counters between the tiles of one cooperative launch (every CTA resident): a producer tile
+// fences its stores and increments a counter; a dependent tile polls it with acquire loads.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// A 32-bit load through the coherent path (data another CTA of the same launch wrote).
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const void* p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Polls until *c >= target (acquire loads, __nanosleep between), at most kWaitTimeoutNs; on
+// time-out (or when another role of the CTA already gave up) records MOE_ERR_TIMEOUT once, sets
+// the CTA's abort flag and returns false.
+__device__ __forceinline__ bool wait_count(const int32_t* c, int target, int32_t* hdr, volatile int* abort_flag) {
+    const uint64_t t0 = globaltimer_ns();
+    while (ld_acquire_gpu(c) < target) {
+        if (*abort_flag || globaltimer_ns() - t0 > kWaitTimeoutNs) {
+            if (!*abort_flag) record_error(hdr, MOE_ERR_TIMEOUT);
+            *abort_flag = 1;
+            return false;
+        }
+        __nanosleep(64);
+    }
+    return true;
+}
+
+// Named barrier kBar over 128 threads (four warps), and the same barrier ANDing a predicate: the
+// warps that share it leave their loop together.
+template <int kBar>
+__device__ __forceinline__ void bar_sync128() {
+    asm volatile("bar.sync %0, 128;" ::"n"(kBar) : "memory");
+}
+template <int kBar>
+__device__ __forceinline__ bool bar_all128(bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %1, 0;\n\tbar.red.and.pred q, %2, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((int)pred), "n"(kBar)
+        : "memory");
+    return r != 0;
+}
+
+// ---------------------------------------------------------------------------------------
+// Re-quantisation jobs of a fused integer launch. A's per-row scale needs whole rows, so the
+// route tile's last L1 tile pushes kQuantJobs jobs of kQuantRows rows; the epilogue warps of any
+// CTA pop and run them while they would otherwise wait (for their next accumulator, or for an L2
+// tile's rows). Pops never wait: a slot that is reserved but not yet written, or taken by
+// another CTA first, is left for the next try. Counters live in the workspace, zeroed per launch.
+// ---------------------------------------------------------------------------------------
+constexpr int kQuantRows = 128 / kQuantJobs;  // rows of A per job
+
+struct QuantQueue {
+    int32_t* dep;        // per route tile: finished L1 tiles, then finished jobs
+    int32_t* jobs_done;  // jobs finished in the whole launch
+    int32_t* head;       // next slot to pop
+    int32_t* tail;       // next slot to reserve
+    int32_t* slots;      // job + 1 per slot (0: not yet written)
+    int n_jobs;          // kQuantJobs x the route tiles that hold rows
+
+    // one thread, after its acquire of the route tile's count: the tile's jobs become visible
+    __device__ __forceinline__ void push(int g) const {
+        const int s = atomicAdd(tail, kQuantJobs);
+        for (int c = 0; c < kQuantJobs; ++c)
+            asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(slots + s + c), "r"(g * kQuantJobs + c + 1)
+                         : "memory");
+    }
+    // one thread: a job (its acquire covers the job's rows of A), or -1
+    __device__ __forceinline__ int try_pop() const {
+        const int h = (int)ld_relaxed_gpu(head);
+        if (h >= n_jobs) return -1;
+        const int v = ld_acquire_gpu(slots + h);
+        if (v == 0 || atomicCAS(head, h, h + 1) != h) return -1;
+        return v - 1;
+    }
+};
+
+// The four epilogue warps (128 threads sharing named barrier kBar; the leader is thread 0 of the
+// first) run one job: kQuantRows / 4 rows per warp, then every thread fences its stores (for the L2 tiles' TMA
+// and loads), the warps meet and the leader counts the job for its route tile and the launch.
+// (not inlined: the epilogue keeps its registers for its own tiles, the job gets its own)
+template <int kBar, int kRegVec>
+__device__ __noinline__ void run_quant_job(const QuantQueue& qq, const Plan& p, int job, int q, int lane, bool leader) {
+    const int g = job / kQuantJobs;
+    const int r0 = g * 128 + (job % kQuantJobs) * kQuantRows;
+    for (int r = q; r < kQuantRows; r += 4) quant_a_row<true, kRegVec>(p, r0 + r, lane);
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    __threadfence();
+    bar_sync128<kBar>();
+    if (leader) {
+        __threadfence();
+        atomicAdd(qq.dep + g, 1);
+        atomicAdd(qq.jobs_done, 1);
+    }
+}
+
+// The four epilogue warps wait until ready() (evaluated by the leader alone) holds, running jobs
+// meanwhile; with kOneJob they stop after one job, or at once when none is available (the caller
+// then waits in the usual way: a job started late would hold up the MMA that waits for the
+// epilogue). The leader's decision reaches the others through `word` (shared memory) between
+// two barriers, so all four leave together. At most kWaitTimeoutNs from the first try (a job in
+// progress finishes first); on time-out records MOE_ERR_TIMEOUT, sets the abort flag and returns
+// false. Loads after a true return are ordered after the leader's acquire in ready().
+template <int kBar, int kRegVec, bool kOneJob, class Ready>
+__device__ __forceinline__ bool idle_with_jobs(const QuantQueue& qq, const Plan& p, volatile int* word,
+                                               volatile int* abort_flag, int q, int lane, Ready ready) {
+    const bool leader = q == 0 && lane == 0;
+    const uint64_t t0 = leader ? globaltimer_ns() : 0;
+    for (;;) {
+        if (leader) {
+            int v = -1;  // -1 ready (kOneJob: or no job), >= 0 a job, -2 nothing to do yet, -3 give up
+            if (!ready()) {
+                v = qq.try_pop();
+                if (v < 0 && kOneJob) v = -1;
+                if (v < 0 && !kOneJob) {
+                    v = -2;
+                    if (*abort_flag || globaltimer_ns() - t0 > kWaitTimeoutNs) {
+                        if (!*abort_flag) record_error(p.hdr, MOE_ERR_TIMEOUT);
+                        *abort_flag = 1;
+                        v = -3;
+                    }
+                }
+            }
+            *word = v;
+        }
+        bar_sync128<kBar>();
+        const int v = *word;
+        bar_sync128<kBar>();  // every thread has read it before the leader writes the next
+        if (v == -1) return true;
+        if (v == -3) return false;
+        if (v == -2) {
+            __nanosleep(256);
+            continue;
+        }
+        run_quant_job<kBar, kRegVec>(qq, p, v, q, lane, leader);
+        if (kOneJob) return true;
+    }
+}
+
 }  // namespace tc
+
+
 
 // Host helpers (tc_host.cu).
 bool tc_make_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes, const void* ptr, uint64_t inner,

@@ -87,7 +87,15 @@ struct I8Args {
     const float* w_scale;       // fp32 per output channel [E*n_out]
     const float* topk_weights;  // L2
     int n_slabs, k_blocks, n_out;
+    // the fused launch (L1 then L2 in one launch): the fields above describe its L1, these its L2
+    const float* w_scale2;
+    int n_slabs2, k_blocks2;
+    int32_t* ctr;  // the workspace's counters: per route tile, then the re-quantisation job queue
 };
+
+constexpr int kL2 = 0, kL1 = 1, kFusedL1L2 = 2;  // what one launch runs
+constexpr int kEpiBar = 1;                       // named barrier of the 4 epilogue warps
+constexpr int kQuantRegVec = 12;  // fused launch: rows of A up to 1536 elements re-quantised from registers
 
 struct Tile {
     int e, s, m, row0;
@@ -152,10 +160,13 @@ __device__ __forceinline__ int exact_int(uint32_t hi_bits, uint32_t lo_bits) {
     return 16 * __float2int_rn(__uint_as_float(hi_bits)) + __float2int_rn(__uint_as_float(lo_bits));
 }
 
-template <bool kL1, bool kPrep>
+template <int kKind, bool kPrep>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_int8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                   const __grid_constant__ CUtensorMap tmX16, I8Args args) {
+                   const __grid_constant__ CUtensorMap tmX16, const __grid_constant__ CUtensorMap tmW2,
+                   const __grid_constant__ CUtensorMap tmX2, const __grid_constant__ CUtensorMap tmX16_2,
+                   I8Args args) {
+    constexpr bool kFused = kKind == kFusedL1L2;
     using L = Layout<kPrep>;
     constexpr int kRawStages = L::kRawStages, kHfStages = L::kHfStages, kTokStages = L::kTokStages;
     constexpr int kHfOff = L::kHfOff, kTokOff = L::kTokOff, kRawOff = L::kRawOff, kBarOff = L::kBarOff;
@@ -178,6 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t drain_bar = acc_full + 16u;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
+    volatile int* job_word = reinterpret_cast<volatile int*>(smem + kMiscOff + 8);  // fused: the epilogue leader's decision
     int* tile_off = reinterpret_cast<int*>(smem + kTileOffOff);
     int* counts = reinterpret_cast<int*>(smem + kCountsOff);
 
@@ -210,13 +222,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
 
-    const int total = tile_off[p.E] * args.n_slabs;
-    const int KB = args.k_blocks;
+    // tiles [0, total1) are the launch's first stage (L1 when fused), [total1, total) the L2 ones;
+    // every L1 tile precedes every L2 tile in the round-robin order
+    const int n_route = tile_off[p.E];
+    const int total1 = n_route * args.n_slabs;
+    const int total = kFused ? total1 + n_route * args.n_slabs2 : total1;
     const int I = p.I, H = p.H;
-    auto wrow = [&](const Tile& tl, int blk) {
-        if (kL1) return tl.e * args.n_out + (blk ? I : 0) + tl.s * kWR;
-        return tl.e * args.n_out + tl.s * 2 * kWR + blk * kWR;
+    auto is_l1 = [&](int t) { return kKind == kL1 || (kFused && t < total1); };
+    auto second = [&](int t) { return kFused && t >= total1; };  // an L2 tile of the fused launch
+    auto tile_of = [&](int t) {
+        return second(t) ? decode(t - total1, tile_off, p.E, args.n_slabs2) : decode(t, tile_off, p.E, args.n_slabs);
     };
+    auto kb_of = [&](int t) { return second(t) ? args.k_blocks2 : args.k_blocks; };
+    auto wrow = [&](const Tile& tl, int blk, bool l1) {
+        if (l1) return tl.e * 2 * I + (blk ? I : 0) + tl.s * kWR;
+        return tl.e * H + tl.s * 2 * kWR + blk * kWR;
+    };
+    // fused launch: per route tile the count of its finished L1 tiles, then of its finished
+    // re-quantisation jobs (an L2 tile waits for dep_target); then the job queue
+    const int route_tiles = (int)(p.pool_rows / kTok);
+    const QuantQueue qq{args.ctr, args.ctr + route_tiles, args.ctr + route_tiles + 1, args.ctr + route_tiles + 2,
+                        args.ctr + route_tiles + 3, kQuantJobs * n_route};
+    const int dep_target = args.n_slabs + kQuantJobs;
 
     if (warp == 0) {
         if constexpr (kPrep) {
@@ -225,8 +252,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int it = 0;
                 bool ok = true;
                 for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                    const Tile tl = decode(t, tile_off, p.E, args.n_slabs);
-                    const int w0 = wrow(tl, 0), w1 = wrow(tl, 1);
+                    const Tile tl = tile_of(t);
+                    const bool l1 = is_l1(t);
+                    const int w0 = wrow(tl, 0, l1), w1 = wrow(tl, 1, l1), KB = kb_of(t);
+                    const CUtensorMap* mW = second(t) ? &tmW2 : &tmW;
                     for (int kb = 0; kb < KB; ++kb, ++it) {
                         const int b = it % kHfStages;
                         if (!mbar_wait(hf_empty(b), ((uint32_t)(it / kHfStages) & 1u) ^ 1u, p.hdr, abort_flag)) {
@@ -235,8 +264,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         const uint32_t dst = base + kHfOff + b * kABytes;
                         mbar_arrive_expect_tx(hf_full(b), kABytes);
-                        tma_load_2d(dst, &tmW, kb * kBK, w0, hf_full(b));
-                        tma_load_2d(dst + kWR * 128, &tmW, kb * kBK, w1, hf_full(b));
+                        tma_load_2d(dst, mW, kb * kBK, w0, hf_full(b));
+                        tma_load_2d(dst + kWR * 128, mW, kb * kBK, w1, hf_full(b));
                     }
                 }
                 for (int j = it - kHfStages < 0 ? 0 : it - kHfStages; j < it; ++j)
@@ -247,8 +276,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             int it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const Tile tl = decode(t, tile_off, p.E, args.n_slabs);
-                const int w0 = wrow(tl, 0), w1 = wrow(tl, 1);
+                const Tile tl = tile_of(t);
+                const bool l1 = is_l1(t);
+                const int w0 = wrow(tl, 0, l1), w1 = wrow(tl, 1, l1), KB = kb_of(t);
+                const CUtensorMap* mW = second(t) ? &tmW2 : &tmW;
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int r = it % kRawStages;
                     if (!mbar_wait(raw_empty(r), ((uint32_t)(it / kRawStages) & 1u) ^ 1u, p.hdr, abort_flag)) {
@@ -257,8 +288,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const uint32_t dst = base + kRawOff + r * kRawBytes;
                     mbar_arrive_expect_tx(raw_full(r), kRawBytes);
-                    tma_load_2d(dst, &tmW, kb * kBK, w0, raw_full(r));
-                    tma_load_2d(dst + kWR * kBK, &tmW, kb * kBK, w1, raw_full(r));
+                    tma_load_2d(dst, mW, kb * kBK, w0, raw_full(r));
+                    tma_load_2d(dst + kWR * kBK, mW, kb * kBK, w1, raw_full(r));
                 }
             }
             for (int j = it - kRawStages < 0 ? 0 : it - kRawStages; j < it; ++j)
@@ -268,9 +299,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------- token TMA: hi plane rows, then lo plane rows ----------------
         if (lane == 0) {
             int it = 0;
-            bool ok = true;
+            bool ok = true, all_q = false;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const Tile tl = decode(t, tile_off, p.E, args.n_slabs);
+                const Tile tl = tile_of(t);
+                const int KB = kb_of(t);
+                const CUtensorMap* mX = second(t) ? &tmX2 : &tmX;
+                const CUtensorMap* mX16 = second(t) ? &tmX16_2 : &tmX16;
+                if (second(t) && !all_q) {
+                    // the route tile's rows are re-quantised (bounded wait); once every job of the
+                    // launch is finished, no later L2 tile needs a check
+                    all_q = ld_acquire_gpu(qq.jobs_done) >= qq.n_jobs;
+                    if (!all_q && !wait_count(qq.dep + tile_off[tl.e] + tl.m, dep_target, p.hdr, abort_flag))
+                        break;
+                    // the planes were written through the generic proxy; the TMA reads them
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                }
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int b = it % kTokStages;
                     if (!mbar_wait(tok_empty(b), ((uint32_t)(it / kTokStages) & 1u) ^ 1u, p.hdr, abort_flag)) {
@@ -283,13 +326,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (n16 == kTok) {
                         // one copy per plane: each TMA instruction costs the issuing thread ~75 cycles
                         for (int pl = 0; pl < 2; ++pl)
-                            tma_load_2d(dst + pl * kTok * 128, &tmX, kb * kBK, (int)(pl * p.pool_rows) + tl.row0,
+                            tma_load_2d(dst + pl * kTok * 128, mX, kb * kBK, (int)(pl * p.pool_rows) + tl.row0,
                                         tok_full(b));
                     } else {
                         // hi rows [0, n16), lo rows [n16, 2 n16): one contiguous B operand of N = 2 n16
                         for (int pl = 0; pl < 2; ++pl)
                             for (int j = 0; j < n16; j += kTokBox)
-                                tma_load_2d(dst + (pl * n16 + j) * 128, &tmX16, kb * kBK,
+                                tma_load_2d(dst + (pl * n16 + j) * 128, mX16, kb * kBK,
                                             (int)(pl * p.pool_rows) + tl.row0 + j, tok_full(b));
                     }
                 }
@@ -311,8 +354,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tc) {
                 if (!mbar_wait(acc_empty, ((uint32_t)tc & 1u) ^ 1u, p.hdr, abort_flag)) break;
                 tc_fence_after();
-                const Tile tl = decode(t, tile_off, p.E, args.n_slabs);
+                const Tile tl = tile_of(t);
                 const uint32_t idesc = idesc_n(2 * tile_n16(counts, tl.e, tl.m));
+                const int KB = kb_of(t);
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!(mbar_test(hf_full(b), hph) || mbar_wait(hf_full(b), hph, p.hdr, abort_flag)) ||
                         !(mbar_test(tok_full(tb), tph) || mbar_wait(tok_full(tb), tph, p.hdr, abort_flag))) {
@@ -344,6 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                const int KB = kb_of(t);
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int r = it % kRawStages, b = it % kHfStages;
                     bool w_ok = mbar_wait(raw_full(r), (uint32_t)(it / kRawStages) & 1u, p.hdr, abort_flag);
@@ -375,13 +420,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         float* w_g = reinterpret_cast<float*>(w_src + kTok);
         float* w_sa = w_g + kTok;
         int tc = 0;
+        const bool leader = q == 0 && lane == 0;
+        bool all_q = false;  // (the leader's) fused launch: every job of the launch seen finished
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++tc) {
-            const Tile tl = decode(t, tile_off, p.E, args.n_slabs);
+            const Tile tl = tile_of(t);
+            const bool l1 = is_l1(t);
             const int n_valid = min(kTok, counts[tl.e] - tl.m * kTok);
             const int n16 = min(kTok, (n_valid + 15) & ~15);  // lo plane columns start here
             float sx_l[kTok / 32];
             float sg = 0.0f, su = 0.0f, s2[2] = {0.0f, 0.0f};
-            if constexpr (kL1) {
+            bool dep_ok = true;
+            if (second(t)) {
+                // s^A of the route tile's rows comes from its re-quantisation in this launch (jobs
+                // run meanwhile); the loads below follow the leader's acquire through the barrier
+                const int32_t* dep = qq.dep + tile_off[tl.e] + tl.m;
+                dep_ok = idle_with_jobs<kEpiBar, kQuantRegVec, false>(qq, p, job_word, abort_flag, q, lane, [&] {
+                    if (!all_q) all_q = ld_acquire_gpu(qq.jobs_done) >= qq.n_jobs;
+                    return all_q || ld_acquire_gpu(dep) >= dep_target;
+                });
+            }
+            if (l1) {
                 const int j = tl.s * kWR + q * 32 + lane;
                 const float* s1 = args.w_scale + (int64_t)tl.e * 2 * I;
                 sg = __ldg(s1 + j);
@@ -390,15 +448,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int ci = 0; ci < kTok / 32; ++ci)
                     sx_l[ci] = __ldg(reinterpret_cast<const float*>(p.x_pool_scale) + tl.row0 + 32 * ci + lane);
             } else {
+                const float* ws2 = second(t) ? args.w_scale2 : args.w_scale;
 #pragma unroll
                 for (int blk = 0; blk < 2; ++blk)
-                    s2[blk] = __ldg(args.w_scale + (int64_t)tl.e * H + tl.s * 2 * kWR + blk * kWR + q * 32 + lane);
+                    s2[blk] = __ldg(ws2 + (int64_t)tl.e * H + tl.s * 2 * kWR + blk * kWR + q * 32 + lane);
                 int src[kTok / 32];
 #pragma unroll
                 for (int ci = 0; ci < kTok / 32; ++ci) {
                     const int n = 32 * ci + lane;
                     src[ci] = n < n_valid ? debug_row(p.hdr, __ldg(p.pool_src + tl.row0 + n), (int64_t)p.T * p.K) : -1;
-                    sx_l[ci] = __ldg(reinterpret_cast<const float*>(p.a_pool_scale) + tl.row0 + n);
+                    const float* sa = reinterpret_cast<const float*>(p.a_pool_scale) + tl.row0 + n;
+                    sx_l[ci] = second(t) ? __uint_as_float(ld_relaxed_gpu(sa)) : __ldg(sa);
                 }
 #pragma unroll
                 for (int ci = 0; ci < kTok / 32; ++ci) {
@@ -409,11 +469,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 __syncwarp();
             }
-            const bool w_ok = mbar_wait(acc_full, (uint32_t)tc & 1u, p.hdr, abort_flag);
-            if (!__all_sync(0xffffffffu, w_ok)) break;
+            if (kFused && dep_ok)  // a re-quantisation job while this tile's MMAs run, if there is one
+                dep_ok = idle_with_jobs<kEpiBar, kQuantRegVec, true>(qq, p, job_word, abort_flag, q, lane,
+                                                                     [&] { return mbar_test(acc_full, (uint32_t)tc & 1u); });
+            const bool w_ok = dep_ok && mbar_wait(acc_full, (uint32_t)tc & 1u, p.hdr, abort_flag);
+            if (!bar_all128<kEpiBar>(w_ok)) break;  // one decision for the four warps (they share kEpiBar)
             tc_fence_after();
             const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16);
-            if constexpr (kL1) {
+            if (l1) {
                 // C = 16 D_hi + D_lo; H = (C * s^W1) * s^X; A = SiLU(H_gate) * H_up for the tile's
                 // 32-token chunks up to n16 (the padding rows' values are never read back as results)
                 const int j = tl.s * kWR + q * 32 + lane;
@@ -466,6 +529,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acc_empty);
+            if (kFused && l1) {
+                // The accumulator is free for the next tile. Publish this tile's rows of A: every
+                // thread fences its own stores, the four warps meet, the leader counts the tile for
+                // its route tile; the route tile's last L1 tile queues its re-quantisation jobs
+                // (whole rows of A are needed), which any CTA's epilogue then runs.
+                const int g = tile_off[tl.e] + tl.m;
+                __threadfence();
+                bar_sync128<kEpiBar>();
+                if (leader) {
+                    __threadfence();
+                    if (atomicAdd(qq.dep + g, 1) == args.n_slabs - 1) {
+                        __threadfence();
+                        qq.push(g);
+                    }
+                }
+            }
         }
     }
 
@@ -475,36 +554,103 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_dealloc(tmem_base, 512);
 }
 
-template <bool kL1, bool kPrep>
-cudaError_t launch_int8(const Plan& p, const void* w, const void* w_scale, const float* topk_weights, cudaStream_t s) {
-    using L = Layout<kPrep>;
+template <int kKind, bool kPrep>
+cudaError_t set_int8_smem_attr() {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(tc_int8_kernel<kL1, kPrep>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)L::kSmem);
+        attr_err = cudaFuncSetAttribute(tc_int8_kernel<kKind, kPrep>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)Layout<kPrep>::kSmem);
     });
-    if (attr_err != cudaSuccess) return attr_err;
-    const int n_out = kL1 ? 2 * p.I : p.H;
-    const int kin = kL1 ? p.H : p.I;
-    CUtensorMap tmW, tmX, tmX16;
-    const bool w_ok = kPrep ? tc_make_map_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w, (uint64_t)kin,
+    return attr_err;
+}
+
+// Weights of one stage (int8 bytes in 64-byte-swizzled boxes of 128 rows x 64 K, or prepared f16
+// codes in 128-byte-swizzled ones) and its token operand: the f16 planes (x for L1, A for L2) in
+// 128-row boxes and 16-row boxes for a route tile's ragged end.
+template <bool kPrep>
+bool make_int8_maps(const Plan& p, const void* w, bool l1, CUtensorMap* tmW, CUtensorMap* tmX, CUtensorMap* tmX16) {
+    const int n_out = l1 ? 2 * p.I : p.H;
+    const int kin = l1 ? p.H : p.I;
+    const bool w_ok = kPrep ? tc_make_map_2d(tmW, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w, (uint64_t)kin,
                                              (uint64_t)p.E * n_out, kBK, kWR, CU_TENSOR_MAP_SWIZZLE_128B)
-                            : tc_make_map_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w, (uint64_t)kin,
+                            : tc_make_map_2d(tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w, (uint64_t)kin,
                                              (uint64_t)p.E * n_out, kBK, kWR, CU_TENSOR_MAP_SWIZZLE_64B);
-    if (!w_ok) return cudaErrorInvalidValue;
-    if (!tc_make_map_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, kL1 ? (const void*)p.x_planes : (const void*)p.a_planes,
-                        (uint64_t)kin, 2 * (uint64_t)p.pool_rows, kBK, kTok, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !tc_make_map_2d(&tmX16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
-                        kL1 ? (const void*)p.x_planes : (const void*)p.a_planes, (uint64_t)kin,
-                        2 * (uint64_t)p.pool_rows, kBK, kTokBox, CU_TENSOR_MAP_SWIZZLE_128B))
-        return cudaErrorInvalidValue;
-    I8Args args{p, static_cast<const float*>(w_scale), topk_weights, kL1 ? p.I / kWR : p.H / (2 * kWR), kin / kBK,
-                n_out};
+    const void* planes = l1 ? (const void*)p.x_planes : (const void*)p.a_planes;
+    return w_ok &&
+           tc_make_map_2d(tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, planes, (uint64_t)kin, 2 * (uint64_t)p.pool_rows, kBK,
+                          kTok, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           tc_make_map_2d(tmX16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, planes, (uint64_t)kin, 2 * (uint64_t)p.pool_rows,
+                          kBK, kTokBox, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+template <bool kIsL1, bool kPrep>
+cudaError_t launch_int8(const Plan& p, const void* w, const void* w_scale, const float* topk_weights, cudaStream_t s) {
+    using L = Layout<kPrep>;
+    constexpr int kKind = kIsL1 ? kL1 : kL2;
+    const cudaError_t attr_err = set_int8_smem_attr<kKind, kPrep>();
+    if (attr_err != cudaSuccess) return attr_err;
+    CUtensorMap tmW, tmX, tmX16;
+    if (!make_int8_maps<kPrep>(p, w, kIsL1, &tmW, &tmX, &tmX16)) return cudaErrorInvalidValue;
+    I8Args args{};
+    args.p = p;
+    args.w_scale = static_cast<const float*>(w_scale);
+    args.topk_weights = topk_weights;
+    args.n_slabs = kIsL1 ? p.I / kWR : p.H / (2 * kWR);
+    args.k_blocks = (kIsL1 ? p.H : p.I) / kBK;
+    args.n_out = kIsL1 ? 2 * p.I : p.H;
     const int64_t max_tiles = (p.pool_rows / kTok) * args.n_slabs;
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(max_tiles, tc_num_sms()));
-    tc_int8_kernel<kL1, kPrep><<<grid, kThreads, L::kSmem, s>>>(tmW, tmX, tmX16, args);
+    tc_int8_kernel<kKind, kPrep><<<grid, kThreads, L::kSmem, s>>>(tmW, tmX, tmX16, tmW, tmX, tmX16, args);
     return cudaGetLastError();
+}
+
+// L1 then L2 in one cooperative launch: every CTA is resident, so an L2 tile waits (bounded) only
+// on L1 tiles and re-quantisations that earlier positions of the same round-robin order hold
+template <bool kPrep>
+cudaError_t launch_int8_fused(const Plan& p, const void* w1, const void* w1_scale, const void* w2,
+                              const void* w2_scale, const float* topk_weights, cudaStream_t s) {
+    using L = Layout<kPrep>;
+    cudaError_t e = set_int8_smem_attr<kFusedL1L2, kPrep>();
+    if (e != cudaSuccess) return e;
+    CUtensorMap tmW1, tmX1, tmX16_1, tmW2, tmX2, tmX16_2;
+    if (!make_int8_maps<kPrep>(p, w1, true, &tmW1, &tmX1, &tmX16_1) ||
+        !make_int8_maps<kPrep>(p, w2, false, &tmW2, &tmX2, &tmX16_2))
+        return cudaErrorInvalidValue;
+    const int64_t route_tiles = p.pool_rows / kTok;
+    // the counters (one per route tile, then the job queue's) start at zero every launch
+    if ((e = cudaMemsetAsync(p.ffn_counters, 0, sizeof(int32_t) * (size_t)fused_int_counters(route_tiles), s)) !=
+        cudaSuccess)
+        return e;
+    I8Args args{};
+    args.p = p;
+    args.w_scale = static_cast<const float*>(w1_scale);
+    args.topk_weights = topk_weights;
+    args.n_slabs = p.I / kWR;
+    args.k_blocks = p.H / kBK;
+    args.n_out = 2 * p.I;
+    args.w_scale2 = static_cast<const float*>(w2_scale);
+    args.n_slabs2 = p.H / (2 * kWR);
+    args.k_blocks2 = p.I / kBK;
+    args.ctr = p.ffn_counters;
+    int per_sm = 0;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tc_int8_kernel<kFusedL1L2, kPrep>, kThreads,
+                                                           L::kSmem)) != cudaSuccess)
+        return e;
+    if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
+    const int64_t max_tiles = route_tiles * (args.n_slabs + args.n_slabs2);
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(max_tiles, (int64_t)tc_num_sms() * per_sm));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = L::kSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tc_int8_kernel<kFusedL1L2, kPrep>, tmW1, tmX1, tmX16_1, tmW2, tmX2, tmX16_2, args);
 }
 
 // One-time preparation of int8 weights for the f16 tensor-core GEMM: every code q becomes the f16
@@ -539,6 +685,12 @@ cudaError_t launch_l2_int8_tc(const Plan& p, const void* w2, const void* w2_scal
                               bool prepared, cudaStream_t s) {
     return prepared ? launch_int8<false, true>(p, w2, w2_scale, topk_weights, s)
                     : launch_int8<false, false>(p, w2, w2_scale, topk_weights, s);
+}
+
+cudaError_t launch_ffn_fused_int8(const Plan& p, const void* w1, const void* w1_scale, const void* w2,
+                                  const void* w2_scale, const float* topk_weights, bool prepared, cudaStream_t s) {
+    return prepared ? launch_int8_fused<true>(p, w1, w1_scale, w2, w2_scale, topk_weights, s)
+                    : launch_int8_fused<false>(p, w1, w1_scale, w2, w2_scale, topk_weights, s);
 }
 
 cudaError_t launch_prepare_int8(const void* w, void* out, int64_t n, cudaStream_t s) {

@@ -87,7 +87,17 @@ struct W4WmArgs {
     const float* row_scale;     // s^X or s^A per pool row
     const int32_t* row_sums;    // code sums per pool row
     int n_slabs, k_blocks, n_out;
+    // the fused launch (L1 then L2 in one launch): the fields above describe its L1, these its L2
+    const float* w_scale2;
+    const float* row_scale2;
+    const int32_t* row_sums2;
+    int n_slabs2, k_blocks2;
+    int32_t* ctr;  // the workspace's counters: per route tile, then the re-quantisation job queue
 };
+
+constexpr int kL2 = 0, kL1 = 1, kFusedL1L2 = 2;  // what one launch runs
+constexpr int kEpiBar = 1;                       // named barrier of the 4 epilogue warps
+constexpr int kQuantRegVec = 12;  // fused launch: rows of A up to 1536 elements re-quantised from registers
 
 struct Tile {
     int e, s, row0, n_valid, n16;
@@ -151,10 +161,13 @@ __device__ __forceinline__ float exact_c(uint32_t bits, int sum8) {
     return __int2float_rn((int)((uint32_t)__float2int_rn(__uint_as_float(bits) * 16777216.0f) - (uint32_t)sum8));
 }
 
-template <bool kL1>
+template <int kKind>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_w4_wm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                    const __grid_constant__ CUtensorMap tmX16, W4WmArgs args) {
+                    const __grid_constant__ CUtensorMap tmX16, const __grid_constant__ CUtensorMap tmW2,
+                    const __grid_constant__ CUtensorMap tmX2, const __grid_constant__ CUtensorMap tmX16_2,
+                    W4WmArgs args) {
+    constexpr bool kFused = kKind == kFusedL1L2;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = smem_u32(smem_raw);
     const uint32_t base = (raw_base + 1023u) & ~1023u;
@@ -172,6 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t drain_bar = acc_full + 16u;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
+    volatile int* job_word = reinterpret_cast<volatile int*>(smem + kMiscOff + 8);  // fused: the epilogue leader's decision
     int* tile_off = reinterpret_cast<int*>(smem + kTileOffOff);
     int* chunk_off = reinterpret_cast<int*>(smem + kChunkOffOff);
     int* counts = reinterpret_cast<int*>(smem + kCountsOff);
@@ -222,14 +236,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
 
-    const int total = chunk_off[p.E] * args.n_slabs;
-    const int KB = args.k_blocks;
+    // tiles [0, total1) are the launch's first stage (L1 when fused), [total1, total) the L2 ones;
+    // every L1 tile precedes every L2 tile in the round-robin order
+    const int n_route = tile_off[p.E];
+    const int total1 = chunk_off[p.E] * args.n_slabs;
+    const int total = kFused ? total1 + chunk_off[p.E] * args.n_slabs2 : total1;
     const int I = p.I, H = p.H;
-    auto tile_of = [&](int t) { return decode_tile(t, tile_off, chunk_off, counts, p.E, args.n_slabs); };
+    auto is_l1 = [&](int t) { return kKind == kL1 || (kFused && t < total1); };
+    auto second = [&](int t) { return kFused && t >= total1; };  // an L2 tile of the fused launch
+    auto tile_of = [&](int t) {
+        return second(t) ? decode_tile(t - total1, tile_off, chunk_off, counts, p.E, args.n_slabs2)
+                         : decode_tile(t, tile_off, chunk_off, counts, p.E, args.n_slabs);
+    };
+    auto kb_of = [&](int t) { return second(t) ? args.k_blocks2 : args.k_blocks; };
     // first weight row of block `blk` of the tile (L1: gate rows, then the up rows of the same outputs)
-    auto wrow = [&](const Tile& tl, int blk) {
-        if (kL1) return tl.e * args.n_out + (blk ? I : 0) + tl.s * kWR;
-        return tl.e * args.n_out + tl.s * 2 * kWR + blk * kWR;
+    auto wrow = [&](const Tile& tl, int blk, bool l1) {
+        if (l1) return tl.e * 2 * I + (blk ? I : 0) + tl.s * kWR;
+        return tl.e * H + tl.s * 2 * kWR + blk * kWR;
+    };
+    // fused launch: per route tile the count of its finished L1 tiles, then of its finished
+    // re-quantisation jobs (an L2 tile waits for dep_target on each route tile of its token chunk);
+    // then the job queue
+    const int route_tiles = (int)(p.pool_rows / kRouteRows);
+    const QuantQueue qq{args.ctr, args.ctr + route_tiles, args.ctr + route_tiles + 1, args.ctr + route_tiles + 2,
+                        args.ctr + route_tiles + 3, kQuantJobs * n_route};
+    const int dep_target = args.n_slabs + kQuantJobs;
+    auto chunk_ready = [&](const Tile& tl) {  // acquire loads
+        const int g = tl.row0 / kRouteRows;
+        return ld_acquire_gpu(qq.dep + g) >= dep_target &&
+               (tl.n_valid <= kRouteRows || ld_acquire_gpu(qq.dep + g + 1) >= dep_target);
+    };
+    auto wait_chunk = [&](const Tile& tl) {  // bounded
+        const int g = tl.row0 / kRouteRows;
+        return wait_count(qq.dep + g, dep_target, p.hdr, abort_flag) &&
+               (tl.n_valid <= kRouteRows || wait_count(qq.dep + g + 1, dep_target, p.hdr, abort_flag));
     };
 
     if (warp == 0) {
@@ -239,7 +279,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 const Tile tl = tile_of(t);
-                const int w0 = wrow(tl, 0), w1 = wrow(tl, 1);
+                const bool l1 = is_l1(t);
+                const int w0 = wrow(tl, 0, l1), w1 = wrow(tl, 1, l1), KB = kb_of(t);
+                const CUtensorMap* mW = second(t) ? &tmW2 : &tmW;
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int r = it % kRawStages;
                     if (!mbar_wait(raw_empty(r), ((uint32_t)(it / kRawStages) & 1u) ^ 1u, p.hdr, abort_flag)) {
@@ -248,8 +290,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const uint32_t dst = base + kRawOff + r * kRawBytes;
                     mbar_arrive_expect_tx(raw_full(r), kRawBytes);
-                    tma_load_2d(dst, &tmW, kb * kRawRow, w0, raw_full(r));
-                    tma_load_2d(dst + kWR * kRawRow, &tmW, kb * kRawRow, w1, raw_full(r));
+                    tma_load_2d(dst, mW, kb * kRawRow, w0, raw_full(r));
+                    tma_load_2d(dst + kWR * kRawRow, mW, kb * kRawRow, w1, raw_full(r));
                 }
             }
             for (int j = it - kRawStages < 0 ? 0 : it - kRawStages; j < it; ++j)
@@ -259,9 +301,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------- token TMA: the tile's n16 rows (128-row boxes, then 16-row boxes) ----------------
         if (lane == 0) {
             int it = 0;
-            bool ok = true;
+            bool ok = true, all_q = false;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 const Tile tl = tile_of(t);
+                const int KB = kb_of(t);
+                const CUtensorMap* mX = second(t) ? &tmX2 : &tmX;
+                const CUtensorMap* mX16 = second(t) ? &tmX16_2 : &tmX16;
+                if (second(t) && !all_q) {
+                    // once every job of the launch is finished, no later L2 tile needs a check
+                    all_q = ld_acquire_gpu(qq.jobs_done) >= qq.n_jobs;
+                    if (!all_q && !wait_chunk(tl)) break;
+                    // the plane was written through the generic proxy; the TMA reads it
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                }
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int b = it % kTokStages;
                     if (!mbar_wait(tok_empty(b), ((uint32_t)(it / kTokStages) & 1u) ^ 1u, p.hdr, abort_flag)) {
@@ -272,9 +324,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive_expect_tx(tok_full(b), (uint32_t)(tl.n16 * 128));
                     int j = 0;
                     for (; j + kRouteRows <= tl.n16; j += kRouteRows)
-                        tma_load_2d(dst + j * 128, &tmX, kb * kBK, tl.row0 + j, tok_full(b));
+                        tma_load_2d(dst + j * 128, mX, kb * kBK, tl.row0 + j, tok_full(b));
                     for (; j < tl.n16; j += kTokBox)
-                        tma_load_2d(dst + j * 128, &tmX16, kb * kBK, tl.row0 + j, tok_full(b));
+                        tma_load_2d(dst + j * 128, mX16, kb * kBK, tl.row0 + j, tok_full(b));
                 }
             }
             for (int j = it - kTokStages < 0 ? 0 : it - kTokStages; j < it; ++j)
@@ -294,6 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!mbar_wait(acc_empty, ((uint32_t)tc & 1u) ^ 1u, p.hdr, abort_flag)) break;
                 tc_fence_after();
                 const uint32_t idesc = idesc_n(tile_of(t).n16);
+                const int KB = kb_of(t);
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!(mbar_test(hf_full(b), hph) || mbar_wait(hf_full(b), hph, p.hdr, abort_flag)) ||
                         !(mbar_test(tok_full(tb), tph) || mbar_wait(tok_full(tb), tph, p.hdr, abort_flag))) {
@@ -324,6 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int it = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            const int KB = kb_of(t);
             for (int kb = 0; kb < KB; ++kb, ++it) {
                 const int r = it % kRawStages, b = it % kHfStages;
                 bool w_ok = mbar_wait(raw_full(r), (uint32_t)(it / kRawStages) & 1u, p.hdr, abort_flag);
@@ -355,39 +409,62 @@ __global__ void __launch_bounds__(kThreads, 1)
         float* w_s = w_g + kTokMax;                            // s^X or s^A
         int* w_sum8 = reinterpret_cast<int*>(w_s + kTokMax);   // 8 * code sum
         int tc = 0;
+        const bool leader = q == 0 && lane == 0;
+        bool all_q = false;  // (the leader's) fused launch: every job of the launch seen finished
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++tc) {
             const Tile tl = tile_of(t);
+            const bool l1 = is_l1(t), sec = second(t);
+            bool dep_ok = true;
+            if (sec) {
+                // s^A and the code sums of the chunk's rows come from their re-quantisation in this
+                // launch (jobs run meanwhile); the loads below follow the leader's acquire through
+                // the barrier
+                dep_ok = idle_with_jobs<kEpiBar, kQuantRegVec, false>(qq, p, job_word, abort_flag, q, lane, [&] {
+                    if (!all_q) all_q = ld_acquire_gpu(qq.jobs_done) >= qq.n_jobs;
+                    return all_q || chunk_ready(tl);
+                });
+            }
+            const float* row_scale = sec ? args.row_scale2 : args.row_scale;
+            const int32_t* row_sums = sec ? args.row_sums2 : args.row_sums;
 #pragma unroll 1
             for (int n = lane; n < kTokMax; n += 32) {
                 const int64_t row = tl.row0 + n;
                 const bool in = n < tl.n16;  // rows of the tile's route tiles
                 int src = -1;
                 float g = 0.0f;
-                if constexpr (!kL1) {
+                if (!l1) {
                     src = n < tl.n_valid ? debug_row(p.hdr, __ldg(p.pool_src + row), (int64_t)p.T * p.K) : -1;
                     g = src >= 0 ? __ldg(args.topk_weights + src) : 0.0f;
                 }
                 w_src[n] = src;
                 w_g[n] = g;
-                w_s[n] = in ? __ldg(args.row_scale + row) : 0.0f;
-                w_sum8[n] = in ? (int)(8u * (uint32_t)__ldg(args.row_sums + row)) : 0;
+                if (sec) {
+                    w_s[n] = in ? __uint_as_float(ld_relaxed_gpu(row_scale + row)) : 0.0f;
+                    w_sum8[n] = in ? (int)(8u * ld_relaxed_gpu(row_sums + row)) : 0;
+                } else {
+                    w_s[n] = in ? __ldg(row_scale + row) : 0.0f;
+                    w_sum8[n] = in ? (int)(8u * (uint32_t)__ldg(row_sums + row)) : 0;
+                }
             }
             __syncwarp();
             float sw0, sw1;  // per-channel weight scales of this thread's rows in the two blocks
-            if constexpr (kL1) {
+            if (l1) {
                 const float* s1 = args.w_scale + (int64_t)tl.e * 2 * I + tl.s * kWR + q * 32 + lane;
                 sw0 = __ldg(s1);      // gate
                 sw1 = __ldg(s1 + I);  // up
             } else {
-                const float* s2 = args.w_scale + (int64_t)tl.e * H + tl.s * 2 * kWR + q * 32 + lane;
+                const float* s2 = (sec ? args.w_scale2 : args.w_scale) + (int64_t)tl.e * H + tl.s * 2 * kWR + q * 32 + lane;
                 sw0 = __ldg(s2);
                 sw1 = __ldg(s2 + kWR);
             }
-            const bool w_ok = mbar_wait(acc_full, (uint32_t)tc & 1u, p.hdr, abort_flag);
-            if (!__all_sync(0xffffffffu, w_ok)) break;
+            if (kFused && dep_ok)  // a re-quantisation job while this tile's MMAs run, if there is one
+                dep_ok = idle_with_jobs<kEpiBar, kQuantRegVec, true>(qq, p, job_word, abort_flag, q, lane,
+                                                                     [&] { return mbar_test(acc_full, (uint32_t)tc & 1u); });
+            const bool w_ok = dep_ok && mbar_wait(acc_full, (uint32_t)tc & 1u, p.hdr, abort_flag);
+            if (!bar_all128<kEpiBar>(w_ok)) break;  // one decision for the four warps (they share kEpiBar)
             tc_fence_after();
             const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16);
-            if constexpr (kL1) {
+            if (l1) {
                 // H = (C * s^W1) * s^X; A[token, j] = SiLU(H_gate) * H_up for output j
                 const int j = tl.s * kWR + q * 32 + lane;
 #pragma unroll 1
@@ -432,6 +509,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acc_empty);
+            if (kFused && l1) {
+                // The accumulator is free for the next tile. Publish this tile's rows of A (one or
+                // two route tiles): every thread fences its own stores, the four warps meet, the
+                // leader counts the tile for each route tile; a route tile's last L1 tile queues its
+                // re-quantisation jobs (whole rows of A are needed), which any CTA's epilogue runs.
+                const int g = tl.row0 / kRouteRows;
+                const int n_rt = tl.n_valid > kRouteRows ? 2 : 1;
+                __threadfence();
+                bar_sync128<kEpiBar>();
+                if (leader) {
+                    __threadfence();
+                    for (int h = 0; h < n_rt; ++h)
+                        if (atomicAdd(qq.dep + g + h, 1) == args.n_slabs - 1) {
+                            __threadfence();
+                            qq.push(g + h);
+                        }
+                }
+            }
         }
     }
 
@@ -441,41 +536,103 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_dealloc(tmem_base, 512);
 }
 
-template <bool kL1>
-cudaError_t launch_w4_wm(const Plan& p, const void* w, const void* w_scale, const float* topk_weights,
-                         cudaStream_t s) {
+template <int kKind>
+cudaError_t set_w4_wm_smem_attr() {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(tc_w4_wm_kernel<kL1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+        attr_err = cudaFuncSetAttribute(tc_w4_wm_kernel<kKind>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
     });
+    return attr_err;
+}
+
+// packed weights as bytes [E * n_out, kin / 2] in boxes of 128 rows x 32 bytes; the f16 token
+// plane (x for L1, A for L2) in 128-row boxes and 16-row boxes for a tile's ragged end
+bool make_w4_wm_maps(const Plan& p, const void* w, bool l1, CUtensorMap* tmW, CUtensorMap* tmX, CUtensorMap* tmX16) {
+    const int n_out = l1 ? 2 * p.I : p.H;
+    const int kin = l1 ? p.H : p.I;
+    const uint16_t* planes = l1 ? p.x_planes : p.a_planes;
+    return tc_make_map_2d(tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w, (uint64_t)kin / 2, (uint64_t)p.E * n_out, kRawRow,
+                          kWR, CU_TENSOR_MAP_SWIZZLE_32B) &&
+           tc_make_map_2d(tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, planes, (uint64_t)kin, (uint64_t)p.pool_rows, kBK,
+                          kRouteRows, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           tc_make_map_2d(tmX16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, planes, (uint64_t)kin, (uint64_t)p.pool_rows, kBK,
+                          kTokBox, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// at most (route tiles + experts) / 2 token chunks per weight slab
+int64_t max_chunks(const Plan& p) { return (p.pool_rows / kRouteRows + p.E) / 2 + 1; }
+
+template <bool kIsL1>
+cudaError_t launch_w4_wm(const Plan& p, const void* w, const void* w_scale, const float* topk_weights,
+                         cudaStream_t s) {
+    constexpr int kKind = kIsL1 ? kL1 : kL2;
+    const cudaError_t attr_err = set_w4_wm_smem_attr<kKind>();
     if (attr_err != cudaSuccess) return attr_err;
-    const int n_out = kL1 ? 2 * p.I : p.H;
-    const int kin = kL1 ? p.H : p.I;
     CUtensorMap tmW, tmX, tmX16;
-    // packed weights as bytes [E * n_out, kin / 2], boxes of 128 rows x 32 bytes
-    if (!tc_make_map_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w, (uint64_t)kin / 2, (uint64_t)p.E * n_out, kRawRow,
-                        kWR, CU_TENSOR_MAP_SWIZZLE_32B))
-        return cudaErrorInvalidValue;
-    const uint16_t* planes = kL1 ? p.x_planes : p.a_planes;
-    if (!tc_make_map_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, planes, (uint64_t)kin, (uint64_t)p.pool_rows, kBK,
-                        kRouteRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !tc_make_map_2d(&tmX16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, planes, (uint64_t)kin, (uint64_t)p.pool_rows, kBK,
-                        kTokBox, CU_TENSOR_MAP_SWIZZLE_128B))
-        return cudaErrorInvalidValue;
-    W4WmArgs args{p,
-                  static_cast<const float*>(w_scale),
-                  topk_weights,
-                  reinterpret_cast<const float*>(kL1 ? p.x_pool_scale : p.a_pool_scale),
-                  kL1 ? p.x_sums : p.a_sums,
-                  kL1 ? p.I / kWR : p.H / (2 * kWR),
-                  kin / kBK,
-                  n_out};
-    // at most (route tiles + experts) / 2 token chunks per weight slab
-    const int64_t max_tiles = ((p.pool_rows / kRouteRows + p.E) / 2 + 1) * args.n_slabs;
+    if (!make_w4_wm_maps(p, w, kIsL1, &tmW, &tmX, &tmX16)) return cudaErrorInvalidValue;
+    W4WmArgs args{};
+    args.p = p;
+    args.w_scale = static_cast<const float*>(w_scale);
+    args.topk_weights = topk_weights;
+    args.row_scale = reinterpret_cast<const float*>(kIsL1 ? p.x_pool_scale : p.a_pool_scale);
+    args.row_sums = kIsL1 ? p.x_sums : p.a_sums;
+    args.n_slabs = kIsL1 ? p.I / kWR : p.H / (2 * kWR);
+    args.k_blocks = (kIsL1 ? p.H : p.I) / kBK;
+    args.n_out = kIsL1 ? 2 * p.I : p.H;
+    const int64_t max_tiles = max_chunks(p) * args.n_slabs;
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(max_tiles, tc_num_sms()));
-    tc_w4_wm_kernel<kL1><<<grid, kThreads, kSmem, s>>>(tmW, tmX, tmX16, args);
+    tc_w4_wm_kernel<kKind><<<grid, kThreads, kSmem, s>>>(tmW, tmX, tmX16, tmW, tmX, tmX16, args);
     return cudaGetLastError();
+}
+
+// L1 then L2 in one cooperative launch: every CTA is resident, so an L2 tile waits (bounded) only
+// on L1 tiles and re-quantisations that earlier positions of the same round-robin order hold
+cudaError_t launch_w4_wm_fused(const Plan& p, const void* w1, const void* w1_scale, const void* w2,
+                               const void* w2_scale, const float* topk_weights, cudaStream_t s) {
+    cudaError_t e = set_w4_wm_smem_attr<kFusedL1L2>();
+    if (e != cudaSuccess) return e;
+    CUtensorMap tmW1, tmX1, tmX16_1, tmW2, tmX2, tmX16_2;
+    if (!make_w4_wm_maps(p, w1, true, &tmW1, &tmX1, &tmX16_1) || !make_w4_wm_maps(p, w2, false, &tmW2, &tmX2, &tmX16_2))
+        return cudaErrorInvalidValue;
+    const int64_t route_tiles = p.pool_rows / kRouteRows;
+    // the counters (one per route tile, then the job queue's) start at zero every launch
+    if ((e = cudaMemsetAsync(p.ffn_counters, 0, sizeof(int32_t) * (size_t)fused_int_counters(route_tiles), s)) !=
+        cudaSuccess)
+        return e;
+    W4WmArgs args{};
+    args.p = p;
+    args.w_scale = static_cast<const float*>(w1_scale);
+    args.topk_weights = topk_weights;
+    args.row_scale = reinterpret_cast<const float*>(p.x_pool_scale);
+    args.row_sums = p.x_sums;
+    args.n_slabs = p.I / kWR;
+    args.k_blocks = p.H / kBK;
+    args.n_out = 2 * p.I;
+    args.w_scale2 = static_cast<const float*>(w2_scale);
+    args.row_scale2 = reinterpret_cast<const float*>(p.a_pool_scale);
+    args.row_sums2 = p.a_sums;
+    args.n_slabs2 = p.H / (2 * kWR);
+    args.k_blocks2 = p.I / kBK;
+    args.ctr = p.ffn_counters;
+    int per_sm = 0;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tc_w4_wm_kernel<kFusedL1L2>, kThreads, kSmem)) !=
+        cudaSuccess)
+        return e;
+    if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
+    const int64_t max_tiles = max_chunks(p) * (args.n_slabs + args.n_slabs2);
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(max_tiles, (int64_t)tc_num_sms() * per_sm));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tc_w4_wm_kernel<kFusedL1L2>, tmW1, tmX1, tmX16_1, tmW2, tmX2, tmX16_2, args);
 }
 
 }  // namespace
@@ -500,6 +657,11 @@ cudaError_t launch_l1_w4_wm(const Plan& p, const void* w1, const void* w1_scale,
 cudaError_t launch_l2_w4_wm(const Plan& p, const void* w2, const void* w2_scale, const float* topk_weights,
                             cudaStream_t s) {
     return launch_w4_wm<false>(p, w2, w2_scale, topk_weights, s);
+}
+
+cudaError_t launch_ffn_fused_w4_wm(const Plan& p, const void* w1, const void* w1_scale, const void* w2,
+                                   const void* w2_scale, const float* topk_weights, cudaStream_t s) {
+    return launch_w4_wm_fused(p, w1, w1_scale, w2, w2_scale, topk_weights, s);
 }
 
 }  // namespace moe

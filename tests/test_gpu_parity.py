@@ -888,12 +888,103 @@ def test_fused_block_scaled_full_size_equals_the_separate_stages(moe, name):
     assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
 
 
+# Integer modes: L1, the per-row re-quantisation of A (by each route tile's last L1 tile) and L2
+# in one cooperative launch of the weight-major kernels, the combine after it; bit-identical to the
+# separate stages on weight-major tiles (A8W4-INT: MOE_FLAG_WEIGHT_MAJOR; A8W8-INT has no other).
+# A8W4-INT tiles take up to two route tiles, so an expert with more than 128 rows exercises a tile
+# that publishes and waits on two route-tile counters.
+FUSED_INT_CASES = CASES["a8w8_int8"] + CASES["a8w4_int"] + [
+    Workload("fused_int8_one_expert_all_rows", "a8w8_int8", 700, 512, 256, 3, 1, 56, 0.05),
+    Workload("fused_w4_one_expert_all_rows", "a8w4_int", 700, 512, 256, 3, 1, 57, 0.05),
+    Workload("fused_w4_many_experts", "a8w4_int", 300, 768, 384, 24, 4, 58, 0.05)]
+
+
+@pytest.mark.parametrize("wl", FUSED_INT_CASES, ids=[w.name for w in FUSED_INT_CASES])
+def test_fused_integer_equals_the_separate_stages(moe, wl):
+    inp = make_inputs(wl, device=DEV)
+    if wl.name.endswith("one_expert_all_rows"):
+        inp["topk_ids"][:] = 1          # 700 rows on one expert: 6 route tiles, the last ragged
+        inp["topk_ids"][::7] = -1       # and some masked routes
+    y0, st0 = _forward_flags(moe, wl, inp, moe.MOE_FLAG_WEIGHT_MAJOR)
+    y1, st1 = _forward_flags(moe, wl, inp, moe.MOE_FLAG_FUSED)
+    assert st0 == 0 and st1 == 0
+    assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
+    assert_close(y_numpy(y1), oracle_forward(wl, inp), wl.mode)
+
+
+def test_fused_integer_pools_equal_the_separate_stages(moe):
+    """The fused launch leaves the same re-quantised A (codes and row scales of every routed slot's
+    pool row) and the same combine rows in the workspace as the separate stages. The plan places an
+    expert's rows in the order its claims land, which may differ between runs, so the pool rows are
+    compared through each slot's row (slot_row)."""
+    for wl in (CASES["a8w8_int8"][1], CASES["a8w4_int"][1], FUSED_INT_CASES[-1]):
+        inp = make_inputs(wl, device=DEV)
+        sep = run_forward(moe, wl, inp, flags=moe.MOE_FLAG_WEIGHT_MAJOR, stages=True)
+        assert sep["status"] == 0
+        d, L = sep["d"], sep["layout"]
+        ws = moe.alloc_workspace(d, wl.mode, DEV)
+        moe.moe_plan(inp["topk_ids"], d, ws)
+        moe.moe_dispatch(inp["x"], inp["x_scale"], d, wl.mode, ws)
+        moe.moe_expert_ffn(inp["w1"], inp["w1_scale"], inp["w2"], inp["w2_scale"], inp["topk_weights"], d, wl.mode, ws)
+        assert moe.moe_check_device_error(ws) == 0
+        rows, R = L["pool_rows"], wl.T * wl.K
+        slot_f = region(ws, L, "slot_row", torch.int32, R).long()
+        slot_s = region(sep["ws"], L, "slot_row", torch.int32, R).long()
+        assert bool((slot_f >= 0).all()) and bool((slot_s >= 0).all())  # no masked routes in these cases
+        for name, dtype, n in (("x_pool", torch.int8, wl.H), ("a_pool", torch.int8, wl.I),
+                               ("a_pool_scale", torch.int32, 1)):
+            got = region(ws, L, name, dtype, rows * n).view(rows, n)[slot_f]
+            ref = region(sep["ws"], L, name, dtype, rows * n).view(rows, n)[slot_s]
+            assert torch.equal(got, ref), (wl.name, name)
+        assert torch.equal(region(ws, L, "comb", torch.int16, R * wl.H),
+                           region(sep["ws"], L, "comb", torch.int16, R * wl.H)), wl.name
+
+
+def test_fused_integer_shared_experts_clamp_quantizing_dispatch_and_prepared_weights(moe):
+    for wl in (CASES["a8w8_int8"][1], CASES["a8w4_int"][1]):
+        inp = make_inputs(wl, device=DEV, shared=1)
+        for flags in (0, moe.MOE_FLAG_QUANTIZE_X):
+            x = inp["x_bf16"] if flags else None
+            y0, st0 = _forward_flags(moe, wl, inp, flags | moe.MOE_FLAG_WEIGHT_MAJOR, shared=1, clamp=0.5, x=x)
+            y1, st1 = _forward_flags(moe, wl, inp, flags | moe.MOE_FLAG_FUSED, shared=1, clamp=0.5, x=x)
+            assert st0 == 0 and st1 == 0
+            assert torch.equal(y0.view(torch.int16), y1.view(torch.int16)), (wl.name, flags)
+        h = to_numpy(inp)
+        ref = omoe.forward(wl.mode, h["x"], h["x_scale"], h["topk_ids"], h["topk_weights"], h["w1"], h["w1_scale"],
+                           h["w2"], h["w2_scale"], num_experts=wl.E, inter=wl.I, num_shared=1, clamp=0.5)
+        assert_close(y_numpy(y1), ref, wl.mode)
+    wl = CASES["a8w8_int8"][1]
+    inp = make_inputs(wl, device=DEV)
+    y0, st0 = _forward_flags(moe, wl, inp, 0)
+    d = moe.dims(wl.T, wl.H, wl.I, wl.E, wl.K)
+    prep = dict(inp, w1=moe.moe_prepare_weights(inp["w1"], d, wl.mode, 1),
+                w2=moe.moe_prepare_weights(inp["w2"], d, wl.mode, 2))
+    y1, st1 = _forward_flags(moe, wl, prep, moe.MOE_FLAG_FUSED | moe.MOE_FLAG_PREPARED_WEIGHTS)
+    assert st0 == 0 and st1 == 0
+    assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
+
+
+@pytest.mark.parametrize("name", ["int8_a8w8", "int4_a8w4"])
+def test_fused_integer_full_size_equals_the_separate_stages(moe, name):
+    wl = WORKLOADS[name]
+    inp = make_inputs(wl, device=DEV)
+    y0, st0 = _forward_flags(moe, wl, inp, moe.MOE_FLAG_WEIGHT_MAJOR)
+    y1, st1 = _forward_flags(moe, wl, inp, moe.MOE_FLAG_FUSED)
+    assert st0 == 0 and st1 == 0
+    assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
+
+
 def test_fused_flag_rejections(moe):
-    wl = CASES["a8w8_int8"][0]
+    wl = Workload("fused_int8_h384", "a8w8_int8", 32, 384, 128, 4, 2, 59, 0.05)
     inp = make_inputs(wl, device=DEV)
     with pytest.raises(moe.MoeError) as err:
         _forward_flags(moe, wl, inp, moe.MOE_FLAG_FUSED)
-    assert err.value.status == 2  # MOE_ERR_UNSUPPORTED: no fused kernel for this mode
+    assert err.value.status == 2  # MOE_ERR_UNSUPPORTED: H = 384 has no 256-row L2 weight tile
+    wl = CASES["a8w8_fp8"][0]
+    inp = make_inputs(wl, device=DEV)
+    with pytest.raises(moe.MoeError) as err:  # prepared weights are the INT8 mode's only
+        _forward_flags(moe, wl, inp, moe.MOE_FLAG_FUSED | moe.MOE_FLAG_PREPARED_WEIGHTS)
+    assert err.value.status == 2
     wl = EDGE[-1]  # max_topk: H = 128 has no 256-column L2 tile
     assert wl.name == "max_topk"
     with pytest.raises(moe.MoeError) as err:
