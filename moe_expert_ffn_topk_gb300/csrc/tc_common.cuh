@@ -358,10 +358,13 @@ struct QuantQueue {
             asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(slots + s + c), "r"(g * kQuantJobs + c + 1)
                          : "memory");
     }
-    // one thread: a job (its acquire covers the job's rows of A), or -1
-    __device__ __forceinline__ int try_pop() const {
+    // one thread: a job (its acquire covers the job's rows of A), or -1; `drained` (the caller's,
+    // initially false) remembers that every job was taken, so later calls cost no load
+    __device__ __forceinline__ int try_pop(bool& drained) const {
+        if (drained) return -1;
         const int h = (int)ld_relaxed_gpu(head);
-        if (h >= n_jobs) return -1;
+        drained = h >= n_jobs;
+        if (drained) return -1;
         const int v = ld_acquire_gpu(slots + h);
         if (v == 0 || atomicCAS(head, h, h + 1) != h) return -1;
         return v - 1;
@@ -393,17 +396,19 @@ __device__ __noinline__ void run_quant_job(const QuantQueue& qq, const Plan& p, 
 // epilogue). The leader's decision reaches the others through `word` (shared memory) between
 // two barriers, so all four leave together. At most kWaitTimeoutNs from the first try (a job in
 // progress finishes first); on time-out records MOE_ERR_TIMEOUT, sets the abort flag and returns
-// false. Loads after a true return are ordered after the leader's acquire in ready().
+// false. Loads after a true return are ordered after the leader's acquire in ready(). `drained`
+// is the leader's QuantQueue::try_pop flag.
 template <int kBar, int kRegVec, bool kOneJob, class Ready>
 __device__ __forceinline__ bool idle_with_jobs(const QuantQueue& qq, const Plan& p, volatile int* word,
-                                               volatile int* abort_flag, int q, int lane, Ready ready) {
+                                               volatile int* abort_flag, bool* drained, int q, int lane,
+                                               Ready ready) {
     const bool leader = q == 0 && lane == 0;
     const uint64_t t0 = leader ? globaltimer_ns() : 0;
     for (;;) {
         if (leader) {
             int v = -1;  // -1 ready (kOneJob: or no job), >= 0 a job, -2 nothing to do yet, -3 give up
             if (!ready()) {
-                v = qq.try_pop();
+                v = qq.try_pop(*drained);
                 if (v < 0 && kOneJob) v = -1;
                 if (v < 0 && !kOneJob) {
                     v = -2;

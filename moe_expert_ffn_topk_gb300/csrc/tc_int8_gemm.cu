@@ -422,6 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int tc = 0;
         const bool leader = q == 0 && lane == 0;
         bool all_q = false;  // (the leader's) fused launch: every job of the launch seen finished
+        bool drained = false;  // (the leader's) fused launch: every job of the launch taken
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++tc) {
             const Tile tl = tile_of(t);
             const bool l1 = is_l1(t);
@@ -434,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // s^A of the route tile's rows comes from its re-quantisation in this launch (jobs
                 // run meanwhile); the loads below follow the leader's acquire through the barrier
                 const int32_t* dep = qq.dep + tile_off[tl.e] + tl.m;
-                dep_ok = idle_with_jobs<kEpiBar, kQuantRegVec, false>(qq, p, job_word, abort_flag, q, lane, [&] {
+                dep_ok = idle_with_jobs<kEpiBar, kQuantRegVec, false>(qq, p, job_word, abort_flag, &drained, q, lane, [&] {
                     if (!all_q) all_q = ld_acquire_gpu(qq.jobs_done) >= qq.n_jobs;
                     return all_q || ld_acquire_gpu(dep) >= dep_target;
                 });
@@ -470,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
             }
             if (kFused && dep_ok)  // a re-quantisation job while this tile's MMAs run, if there is one
-                dep_ok = idle_with_jobs<kEpiBar, kQuantRegVec, true>(qq, p, job_word, abort_flag, q, lane,
+                dep_ok = idle_with_jobs<kEpiBar, kQuantRegVec, true>(qq, p, job_word, abort_flag, &drained, q, lane,
                                                                      [&] { return mbar_test(acc_full, (uint32_t)tc & 1u); });
             const bool w_ok = dep_ok && mbar_wait(acc_full, (uint32_t)tc & 1u, p.hdr, abort_flag);
             if (!bar_all128<kEpiBar>(w_ok)) break;  // one decision for the four warps (they share kEpiBar)

@@ -411,6 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int tc = 0;
         const bool leader = q == 0 && lane == 0;
         bool all_q = false;  // (the leader's) fused launch: every job of the launch seen finished
+        bool drained = false;  // (the leader's) fused launch: every job of the launch taken
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++tc) {
             const Tile tl = tile_of(t);
             const bool l1 = is_l1(t), sec = second(t);
@@ -419,31 +420,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // s^A and the code sums of the chunk's rows come from their re-quantisation in this
                 // launch (jobs run meanwhile); the loads below follow the leader's acquire through
                 // the barrier
-                dep_ok = idle_with_jobs<kEpiBar, kQuantRegVec, false>(qq, p, job_word, abort_flag, q, lane, [&] {
+                dep_ok = idle_with_jobs<kEpiBar, kQuantRegVec, false>(qq, p, job_word, abort_flag, &drained, q, lane, [&] {
                     if (!all_q) all_q = ld_acquire_gpu(qq.jobs_done) >= qq.n_jobs;
                     return all_q || chunk_ready(tl);
                 });
             }
             const float* row_scale = sec ? args.row_scale2 : args.row_scale;
             const int32_t* row_sums = sec ? args.row_sums2 : args.row_sums;
-#pragma unroll 1
-            for (int n = lane; n < kTokMax; n += 32) {
-                const int64_t row = tl.row0 + n;
-                const bool in = n < tl.n16;  // rows of the tile's route tiles
-                int src = -1;
-                float g = 0.0f;
-                if (!l1) {
-                    src = n < tl.n_valid ? debug_row(p.hdr, __ldg(p.pool_src + row), (int64_t)p.T * p.K) : -1;
-                    g = src >= 0 ? __ldg(args.topk_weights + src) : 0.0f;
+            {
+                // every load of the table in flight at once (rows beyond the tile read row0's
+                // values, which are discarded), then the dependent gate loads, then the stores
+                constexpr int kC = kTokMax / 32;
+                int src[kC];
+                uint32_t sv[kC], sm[kC];
+#pragma unroll
+                for (int i = 0; i < kC; ++i) {
+                    const int n = 32 * i + lane;
+                    const int64_t row = tl.row0 + (n < tl.n16 ? n : 0);
+                    src[i] = (!l1 && n < tl.n_valid) ? __ldg(p.pool_src + row) : -1;
+                    sv[i] = sec ? ld_relaxed_gpu(row_scale + row) : __float_as_uint(__ldg(row_scale + row));
+                    sm[i] = sec ? ld_relaxed_gpu(row_sums + row) : (uint32_t)__ldg(row_sums + row);
                 }
-                w_src[n] = src;
-                w_g[n] = g;
-                if (sec) {
-                    w_s[n] = in ? __uint_as_float(ld_relaxed_gpu(row_scale + row)) : 0.0f;
-                    w_sum8[n] = in ? (int)(8u * ld_relaxed_gpu(row_sums + row)) : 0;
-                } else {
-                    w_s[n] = in ? __ldg(row_scale + row) : 0.0f;
-                    w_sum8[n] = in ? (int)(8u * (uint32_t)__ldg(row_sums + row)) : 0;
+                float g[kC];
+#pragma unroll
+                for (int i = 0; i < kC; ++i) {
+                    src[i] = src[i] >= 0 ? debug_row(p.hdr, src[i], (int64_t)p.T * p.K) : -1;
+                    g[i] = src[i] >= 0 ? __ldg(args.topk_weights + src[i]) : 0.0f;
+                }
+#pragma unroll
+                for (int i = 0; i < kC; ++i) {
+                    const int n = 32 * i + lane;
+                    const bool in = n < tl.n16;  // rows of the tile's route tiles
+                    w_src[n] = src[i];
+                    w_g[n] = g[i];
+                    w_s[n] = in ? __uint_as_float(sv[i]) : 0.0f;
+                    w_sum8[n] = in ? (int)(8u * sm[i]) : 0;
                 }
             }
             __syncwarp();
@@ -458,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sw1 = __ldg(s2 + kWR);
             }
             if (kFused && dep_ok)  // a re-quantisation job while this tile's MMAs run, if there is one
-                dep_ok = idle_with_jobs<kEpiBar, kQuantRegVec, true>(qq, p, job_word, abort_flag, q, lane,
+                dep_ok = idle_with_jobs<kEpiBar, kQuantRegVec, true>(qq, p, job_word, abort_flag, &drained, q, lane,
                                                                      [&] { return mbar_test(acc_full, (uint32_t)tc & 1u); });
             const bool w_ok = dep_ok && mbar_wait(acc_full, (uint32_t)tc & 1u, p.hdr, abort_flag);
             if (!bar_all128<kEpiBar>(w_ok)) break;  // one decision for the four warps (they share kEpiBar)
