@@ -358,16 +358,23 @@ struct QuantQueue {
             asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(slots + s + c), "r"(g * kQuantJobs + c + 1)
                          : "memory");
     }
-    // one thread: a job (its acquire covers the job's rows of A), or -1; `drained` (the caller's,
-    // initially false) remembers that every job was taken, so later calls cost no load
+    // one thread: a job (its acquire covers the job's rows of A), or -1 when none is written yet;
+    // a slot lost to another CTA moves on to the next (a bounded number of times: many CTAs pop at
+    // once when a round of L1 tiles ends). `drained` (the caller's, initially false) remembers that
+    // every job was taken, so later calls cost no load.
     __device__ __forceinline__ int try_pop(bool& drained) const {
         if (drained) return -1;
-        const int h = (int)ld_relaxed_gpu(head);
-        drained = h >= n_jobs;
-        if (drained) return -1;
-        const int v = ld_acquire_gpu(slots + h);
-        if (v == 0 || atomicCAS(head, h, h + 1) != h) return -1;
-        return v - 1;
+        int h = (int)ld_relaxed_gpu(head);
+        for (int tries = 0; tries < 64; ++tries) {
+            drained = h >= n_jobs;
+            if (drained) return -1;
+            const int v = ld_acquire_gpu(slots + h);
+            if (v == 0) return -1;
+            const int old = atomicCAS(head, h, h + 1);
+            if (old == h) return v - 1;
+            h = old;  // taken: the head has moved on
+        }
+        return -1;
     }
 };
 
