@@ -171,18 +171,20 @@ __global__ void route_scatter_kernel(const int32_t* __restrict__ ids, int n_ids,
     slot_row[i] = prow;
 }
 
-// S2: copy x row (token = src / K) and its scale row into the pool row of every routed (i, k).
-// Padding rows are left as they are: every consumer computes rows (tokens) independently and
-// drops the padding rows' results.
+// S2: copy x row (token = i / K) and its scale row into the pool row of every routed slot i
+// (slot_row; -1 for a masked route). Iterating the slots rather than the pool rows skips the
+// padding rows without reading them (at decode sizes most pool rows are padding). Padding rows are
+// left as they are: every consumer computes rows (tokens) independently and drops their results.
 __global__ void __launch_bounds__(128) dispatch_gather_kernel(const uint4* __restrict__ x, const uint32_t* __restrict__ xs,
-                                                              const int32_t* __restrict__ pool_src,
+                                                              const int32_t* __restrict__ slot_row,
                                                               int32_t* __restrict__ hdr, int K, int row_vecs,
                                                               int scale_words, uint4* __restrict__ xp,
-                                                              uint32_t* __restrict__ xps, int64_t n_ids) {
-    const int rows = hdr[kHdrPadRows];
-    for (int r = blockIdx.x; r < rows; r += gridDim.x) {
-        const int src = debug_row(hdr, pool_src[r], n_ids);
-        if (src < 0) continue;  // padding row
+                                                              uint32_t* __restrict__ xps, int64_t n_ids,
+                                                              int64_t pool_rows) {
+    for (int64_t i = blockIdx.x; i < n_ids; i += gridDim.x) {
+        const int r = debug_row(hdr, slot_row[i], pool_rows);
+        if (r < 0) continue;  // masked route
+        const int64_t src = i;
         uint4* dst = xp + (size_t)r * row_vecs;
         const uint4* s = x + (size_t)(src / K) * row_vecs;
         for (int v = threadIdx.x; v < row_vecs; v += blockDim.x) dst[v] = s[v];
@@ -197,27 +199,27 @@ __global__ void __launch_bounds__(128) dispatch_gather_kernel(const uint4* __res
 // fp32 partial sum of that GEMM stays an exactly representable integer. For A8W4-INT the plane
 // is the codes themselves as f16 (int8 x int4 products are small enough without the split), in
 // the order of w4_plane_pos, and the row's code sum goes to `sums`.
-// Each thread keeps four 16-byte loads in flight before its stores, and the next row's source
-// index is read while the current row is copied (a row costs two dependent loads otherwise).
+// Each thread keeps four 16-byte loads in flight before its stores, and the next slot's pool row
+// is read while the current row is copied (a row costs two dependent loads otherwise). Like
+// dispatch_gather_kernel it iterates the routed slots (slot_row), so padding rows cost nothing.
 template <int MODE>
 __global__ void __launch_bounds__(128) dispatch_gather_q_kernel(const uint8_t* __restrict__ x, const uint8_t* __restrict__ xs,
-                                                                const int32_t* __restrict__ pool_src,
+                                                                const int32_t* __restrict__ slot_row,
                                                                 int32_t* __restrict__ hdr, int K, int H,
                                                                 int scale_bytes, int64_t pool_rows, uint8_t* __restrict__ xp,
                                                                 uint8_t* __restrict__ xps, uint16_t* __restrict__ xb,
                                                                 int32_t* __restrict__ sums, int64_t n_ids) {
     constexpr int kUnroll = 4;
     __shared__ int red[4];
-    const int rows = hdr[kHdrPadRows];
     const int nv = H / 16;                 // 16-byte vectors of a row of codes
     const int scale_words = scale_bytes / 4;
-    int r = blockIdx.x;
-    int src = r < rows ? debug_row(hdr, __ldg(pool_src + r), n_ids) : -1;
-    while (r < rows) {
-        const int rn = r + gridDim.x;
-        const int src_next = rn < rows ? debug_row(hdr, __ldg(pool_src + rn), n_ids) : -1;
-        if (src >= 0) {  // padding rows are left as they are (rows are independent everywhere)
-            const int64_t tok = src / K;
+    int64_t i = blockIdx.x;
+    int r = i < n_ids ? debug_row(hdr, __ldg(slot_row + i), pool_rows) : -1;
+    while (i < n_ids) {
+        const int64_t in = i + gridDim.x;
+        const int r_next = in < n_ids ? debug_row(hdr, __ldg(slot_row + in), pool_rows) : -1;
+        if (r >= 0) {  // a masked route writes nothing; padding rows are left as they are
+            const int64_t tok = i / K;
             const uint4* xs4 = reinterpret_cast<const uint4*>(x + tok * H);
             uint4* xd = reinterpret_cast<uint4*>(xp + (int64_t)r * H);
             int row_sum = 0;  // A8W4-INT
@@ -280,7 +282,7 @@ __global__ void __launch_bounds__(128) dispatch_gather_q_kernel(const uint8_t* _
                 }
                 reinterpret_cast<uint32_t*>(xps + (int64_t)r * scale_bytes)[w] = v;
             }
-            if constexpr (MODE == MOE_A8W4_INT) {  // src >= 0 is uniform across the block
+            if constexpr (MODE == MOE_A8W4_INT) {  // r >= 0 is uniform across the block
 #pragma unroll
                 for (int o = 16; o >= 1; o >>= 1) row_sum += __shfl_xor_sync(0xffffffffu, row_sum, o);
                 if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = row_sum;
@@ -289,8 +291,8 @@ __global__ void __launch_bounds__(128) dispatch_gather_q_kernel(const uint8_t* _
                 __syncthreads();
             }
         }
-        r = rn;
-        src = src_next;
+        i = in;
+        r = r_next;
     }
 }
 
@@ -491,9 +493,9 @@ cudaError_t launch_route(const Plan& p, const int32_t* topk_ids, int32_t* counts
 
 template <int MODE>
 static cudaError_t dispatch_q(const Plan& p, const void* x, const void* x_scale, cudaStream_t s) {
-    const int grid = (int)std::min<int64_t>(p.pool_rows, 152 * 16);
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)p.T * p.K, 152 * 16));
     dispatch_gather_q_kernel<MODE><<<grid, 128, 0, s>>>(static_cast<const uint8_t*>(x),
-                                                        static_cast<const uint8_t*>(x_scale), p.pool_src, p.hdr, p.K,
+                                                        static_cast<const uint8_t*>(x_scale), p.slot_row, p.hdr, p.K,
                                                         p.H, (int)x_scale_row_bytes(MODE, p.H), p.pool_rows, p.x_pool,
                                                         p.x_pool_scale, p.x_planes, p.x_sums, (int64_t)p.T * p.K);
     return cudaGetLastError();
@@ -511,11 +513,12 @@ cudaError_t launch_dispatch(const Plan& p, const void* x, const void* x_scale, c
     }
     const int row_vecs = p.H * x_elem_bytes(p.mode) / 16;
     const int scale_words = (int)(x_scale_row_bytes(p.mode, p.H) / 4);
-    const int grid = (int)std::min<int64_t>(p.pool_rows, 152 * 16);
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)p.T * p.K, 152 * 16));
     dispatch_gather_kernel<<<grid, 128, 0, s>>>(static_cast<const uint4*>(x), static_cast<const uint32_t*>(x_scale),
-                                                p.pool_src, p.hdr, p.K, row_vecs, scale_words,
+                                                p.slot_row, p.hdr, p.K, row_vecs, scale_words,
                                                 reinterpret_cast<uint4*>(p.x_pool),
-                                                reinterpret_cast<uint32_t*>(p.x_pool_scale), (int64_t)p.T * p.K);
+                                                reinterpret_cast<uint32_t*>(p.x_pool_scale), (int64_t)p.T * p.K,
+                                                p.pool_rows);
     return cudaGetLastError();
 }
 
