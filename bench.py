@@ -32,8 +32,9 @@ METRIC = "fused MoE FFN TFLOP/s + routed rows/s, % of tensor/HBM roofline, 1xGB3
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 DTYPE = {"a16w16": "bf16", "a8w8_fp8": "e4m3", "a8w8_int8": "int8", "a8w4_fp8_fp4": "e4m3xe2m1", "a8w4_int": "int8xint4", "a8w8_fp8_e5m2": "e5m2"}
 LAUNCHES_PER_STEP = {"a16w16": 7, "a8w8_fp8": 7, "a8w8_int8": 8, "a8w4_fp8_fp4": 7, "a8w4_int": 8, "a8w8_fp8_e5m2": 7}
-# launches the fused launch replaces: A16W16 runs L1, L2 and the combine in it, the FP8 modes L1 and L2
-FUSED_SAVES = {"a16w16": 2}
+# launches the fused launch replaces: A16W16 runs L1, L2 and the combine in it, the FP8 modes L1 and L2,
+# the integer modes L1, the re-quantisation of A and L2
+FUSED_SAVES = {"a16w16": 2, "a8w8_int8": 2, "a8w4_int": 2}
 
 
 def parse():
