@@ -122,6 +122,75 @@ def test_closed_form_int8():
     assert y[0, 0] == pytest.approx(a, rel=2e-7) and y[0, 1] == pytest.approx(-2 * a, rel=2e-7)
 
 
+def _check_a8w4_golden():
+    """Hand-derived A8W4-INT layer (tests/golden/ffn_closed_form_a8w4_int.json): the int4 packing, the
+    MSD split of negative codes and codes >= 16, the compensation bias, C, H, the requantised A and D
+    are exact; y equals its closed form within the fp32 rounding of s^A."""
+    g = _load("ffn_closed_form_a8w4_int.json")
+    w1 = np.array([[int(b, 16) for b in g["w1_packed_hex"]]], np.uint8).reshape(1, 4, 1)
+    w2 = np.array([[int(b, 16) for b in g["w2_packed_hex"]]], np.uint8).reshape(1, 2, 1)
+    w1m = moe.decode_weight("a8w4_int", w1, None, 0)   # math orientation [H, 2I]
+    w2m = moe.decode_weight("a8w4_int", w2, None, 0)   # [I, H]
+    assert w1m.T.tolist() == g["w1_int4"] and w2m.T.tolist() == g["w2_int4"]
+    assert w1m.shape == (2, 4)  # a transposed decode would be (4, 2)
+    q = np.array(g["q"], np.int64)
+    assert np.floor_divide(q, 16).tolist() == g["q_hi"]
+    assert (np.bitwise_and(q, 0x0F) - 8).tolist() == g["q_lo_offset"]
+    assert (8 * w1m.astype(np.int64).sum(axis=0)).tolist() == g["bias1"]
+    assert moe.msd_int_matmul(q, w1m).tolist() == g["c"]
+    y, rec = moe.expert_ffn("a8w4_int", q.astype(np.float64), np.array(g["x_scale"], np.float32), w1m,
+                            np.array(g["w1_scale"], np.float32), w2m, np.array(g["w2_scale"], np.float32), inter=2)
+    assert rec["c"].tolist() == g["c"] and rec["h"].tolist() == g["h"]
+    assert rec["a"].tolist() == g["a_codes"] and rec["d"].tolist() == g["d"]
+    s_a = float(np.float32(np.float32(6122.34375) / np.float32(127.0)))
+    assert y[0, 0] == pytest.approx(762 * s_a, rel=2e-7) and y[0, 1] == pytest.approx(-127 * s_a, rel=2e-7)
+    assert y[0, 1] == pytest.approx(-6122.34375, rel=2.0 ** -22)
+
+
+def test_a8w4_int_closed_form_golden():
+    _check_a8w4_golden()
+
+
+# Plausible mistakes planted in the A8W4-INT oracle: each must fail the golden.
+def _msd_without_bias(q, w):
+    q = q.astype(np.int64)
+    wi = w.astype(np.int64)
+    return 16 * (np.floor_divide(q, 16) @ wi) + ((np.bitwise_and(q, 0x0F) - 8) @ wi)
+
+
+def _msd_low_nibble_not_offset(q, w):  # q_lo = q & 0x0F (the -8 dropped) while the bias stays
+    q = q.astype(np.int64)
+    wi = w.astype(np.int64)
+    return 16 * (np.floor_divide(q, 16) @ wi) + (np.bitwise_and(q, 0x0F) @ wi) + 8 * wi.sum(axis=0)[None, :]
+
+
+def _decode_int4_untransposed(mode, w, w_scale, e):
+    if mode == "a8w4_int":
+        return codecs.int4_unpack(w[e]).astype(np.float64)
+    return ORIG_DECODE_WEIGHT(mode, w, w_scale, e)
+
+
+def _decode_int4_nibbles_swapped(mode, w, w_scale, e):
+    if mode == "a8w4_int":
+        b = np.asarray(w[e], np.uint8)
+        return codecs.int4_unpack(((b >> 4) | (b << 4)).astype(np.uint8)).astype(np.float64).T
+    return ORIG_DECODE_WEIGHT(mode, w, w_scale, e)
+
+
+A8W4_MUTATIONS = {"msd_bias_dropped": ("msd_int_matmul", _msd_without_bias),
+                  "msd_low_nibble_not_offset": ("msd_int_matmul", _msd_low_nibble_not_offset),
+                  "int4_not_transposed": ("decode_weight", _decode_int4_untransposed),
+                  "int4_nibbles_swapped": ("decode_weight", _decode_int4_nibbles_swapped)}
+
+
+@pytest.mark.parametrize("mutation", list(A8W4_MUTATIONS))
+def test_a8w4_int_golden_catches_planted_mistakes(monkeypatch, mutation):
+    attr, fn = A8W4_MUTATIONS[mutation]
+    monkeypatch.setattr(moe, attr, fn)
+    with pytest.raises((AssertionError, ValueError)):
+        _check_a8w4_golden()
+
+
 def _golden_fp8_inputs(g, mode):
     """Dense operands of a sparse FP8 golden: codes and scale bytes not listed are 0 and 127."""
     T, H, I, E = g["T"], g["H"], g["I"], g["E"]
