@@ -144,6 +144,101 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int E, const int32_t* 
     }
 }
 
+// S1 in one CTA for up to kSmallIds ids and 1024 experts (decode steps): the same count
+// (warp-aggregated shared-memory atomics), scan and scatter as the three kernels above, with every
+// id's expert and rank kept in registers between the phases, so one launch replaces three. Measured:
+// the decode step (1024 ids) 9 us shorter; with 8192-12288 ids the one CTA's atomics (a few experts
+// take many ids) made the step slower than the multi-CTA count, hence the bound.
+constexpr int kSmallThreads = 1024, kSmallItems = 4, kSmallIds = kSmallThreads * kSmallItems;
+__global__ void __launch_bounds__(kSmallThreads) route_small_kernel(const int32_t* __restrict__ ids, int n_ids, int Kt,
+                                                                   int Kr, int Er, int E, int32_t* __restrict__ counts,
+                                                                   int32_t* __restrict__ offsets,
+                                                                   int32_t* __restrict__ pad_off,
+                                                                   int32_t* __restrict__ tile_off,
+                                                                   int32_t* __restrict__ row_src,
+                                                                   int32_t* __restrict__ pool_src,
+                                                                   int32_t* __restrict__ slot_row,
+                                                                   int32_t* __restrict__ hdr,
+                                                                   int32_t* __restrict__ counts_out,
+                                                                   int32_t* __restrict__ offsets_out,
+                                                                   int32_t* __restrict__ row_src_out, int64_t pool_rows) {
+    __shared__ int hist[1024];   // ids per expert, then (after the scan) each expert's first row
+    __shared__ int pad_s[1024];  // each expert's first padded pool row
+    __shared__ int warp_sums[32];
+    __shared__ int total_rows, total_tiles;
+    const int lane = threadIdx.x & 31;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+    __syncthreads();
+    int expert[kSmallItems];
+    int rank[kSmallItems];
+#pragma unroll
+    for (int j = 0; j < kSmallItems; ++j) {
+        const int i = j * kSmallThreads + threadIdx.x;
+        const bool in = i < n_ids;
+        const int e = in ? route_id(ids, i, Kt, Kr, Er) : -1;
+        const bool valid = in && e >= 0 && e < E;
+        if (in && !valid && e != -1) record_error(hdr, MOE_ERR_BAD_ROUTE);
+        expert[j] = valid ? e : -1;
+        rank[j] = -1;
+        const unsigned active = __ballot_sync(0xffffffffu, valid);
+        if (valid) {
+            const unsigned peers = __match_any_sync(active, e);  // lanes routed to the same expert
+            const int leader = __ffs(peers) - 1;
+            int b = 0;
+            if (lane == leader) b = atomicAdd(&hist[e], __popc(peers));
+            b = __shfl_sync(peers, b, leader);
+            rank[j] = b + __popc(peers & ((1u << lane) - 1u));
+        }
+    }
+    __syncthreads();
+    // counts -> offsets, padded offsets and tile offsets (one expert per thread)
+    const int me = threadIdx.x;
+    const int c = me < E ? hist[me] : 0;
+    const int off = block_exclusive_scan(c, warp_sums, &total_rows);
+    const int toff = block_exclusive_scan((c + kTileRows - 1) / kTileRows, warp_sums, &total_tiles);
+    if (me < E) {
+        counts[me] = c;
+        offsets[me] = off;
+        tile_off[me] = toff;
+        pad_off[me] = toff * kTileRows;
+        hist[me] = off;
+        pad_s[me] = toff * kTileRows;
+        if (counts_out) counts_out[me] = c;
+        if (offsets_out) offsets_out[me] = off;
+    }
+    if (me == 0) {
+        offsets[E] = total_rows;
+        tile_off[E] = total_tiles;
+        pad_off[E] = total_tiles * kTileRows;
+        if (offsets_out) offsets_out[E] = total_rows;
+        hdr[kHdrRows] = total_rows;
+        hdr[kHdrPadRows] = total_tiles * kTileRows;
+        hdr[kHdrTiles] = total_tiles;
+    }
+    __syncthreads();
+    // scatter, both directions of the identity map
+#pragma unroll
+    for (int j = 0; j < kSmallItems; ++j) {
+        const int i = j * kSmallThreads + threadIdx.x;
+        if (i >= n_ids) continue;
+        const int e = expert[j];
+        if (e < 0) {
+            slot_row[i] = -1;
+            continue;
+        }
+        const int row = hist[e] + rank[j];
+        const int prow = pad_s[e] + rank[j];
+        if (!debug_ok(hdr, row >= 0 && row < n_ids && prow >= 0 && prow < pool_rows)) {
+            slot_row[i] = -1;
+            continue;
+        }
+        row_src[row] = i;
+        if (row_src_out) row_src_out[row] = i;
+        pool_src[prow] = i;
+        slot_row[i] = prow;
+    }
+}
+
 // Scatter every routed (i,k) to its pool row and record both directions of the identity map.
 __global__ void route_scatter_kernel(const int32_t* __restrict__ ids, int n_ids, int Kt, int Kr, int Er, int E,
                                      const int32_t* __restrict__ pos,
@@ -415,9 +510,12 @@ __global__ void __launch_bounds__(256) dispatch_quant_kernel(const uint16_t* __r
     }
 }
 
-// S6: y[t, 8j..8j+7] = bf16( sum_k comb[t*K+k, 8j..8j+7] ), fp32 sum in slot order.
+// S6: y[t, 8j..8j+7] = bf16( sum_k comb[t*K+k, 8j..8j+7] ), fp32 sum in slot order. The slots are
+// read eight at a time, all loads in flight before the first add (a masked slot's row is read, it
+// lies inside comb, and skipped), so a thread waits for one memory round trip per eight slots.
 __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ comb, const int32_t* __restrict__ slot_row,
                                                       int T, int K, int row_vecs, uint4* __restrict__ y) {
+    constexpr int kSlots = 8;
     const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= (int64_t)T * row_vecs) return;
     const int t = (int)(idx / row_vecs);
@@ -425,14 +523,24 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
     float acc[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
-    for (int k = 0; k < K; ++k) {
-        if (slot_row[t * K + k] < 0) continue;   // masked route: contributes nothing
-        const uint4 c = comb[((size_t)t * K + k) * row_vecs + v];
-        const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+    for (int k0 = 0; k0 < K; k0 += kSlots) {
+        uint4 c[kSlots];
+        int r[kSlots];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            acc[2 * j] = __fadd_rn(acc[2 * j], __uint_as_float(w[j] << 16));
-            acc[2 * j + 1] = __fadd_rn(acc[2 * j + 1], __uint_as_float(w[j] & 0xffff0000u));
+        for (int u = 0; u < kSlots; ++u) {
+            const int k = k0 + u;
+            r[u] = k < K ? __ldg(slot_row + t * K + k) : -1;
+            if (k < K) c[u] = __ldg(comb + ((size_t)t * K + k) * row_vecs + v);
+        }
+#pragma unroll
+        for (int u = 0; u < kSlots; ++u) {
+            if (r[u] < 0) continue;  // masked route (or past K): contributes nothing
+            const uint32_t w[4] = {c[u].x, c[u].y, c[u].z, c[u].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                acc[2 * j] = __fadd_rn(acc[2 * j], __uint_as_float(w[j] << 16));
+                acc[2 * j + 1] = __fadd_rn(acc[2 * j + 1], __uint_as_float(w[j] & 0xffff0000u));
+            }
         }
     }
     uint32_t o[4];
@@ -476,6 +584,12 @@ cudaError_t launch_route(const Plan& p, const int32_t* topk_ids, int32_t* counts
     if (e != cudaSuccess) return e;
     e = cudaMemsetAsync(p.pool_src, 0xff, sizeof(int32_t) * (size_t)p.pool_rows, s);  // -1: padding row
     if (e != cudaSuccess) return e;
+    if (n_ids <= kSmallIds && p.E <= kSmallThreads) {  // one launch for the whole stage
+        route_small_kernel<<<1, kSmallThreads, 0, s>>>(topk_ids, n_ids, p.K, p.Kr, p.Er, p.E, p.counts, p.offsets,
+                                                       p.pad_off, p.tile_off, p.row_src, p.pool_src, p.slot_row, p.hdr,
+                                                       counts_out, offsets_out, row_src_out, p.pool_rows);
+        return cudaGetLastError();
+    }
     if (n_ids > 0) {
         const int blocks = (n_ids + kRouteChunk - 1) / kRouteChunk;
         route_count_claim_kernel<<<blocks, kRouteThreads, 2 * p.E * sizeof(int32_t), s>>>(
