@@ -18,7 +18,7 @@ namespace moe {
 namespace {
 
 constexpr int kRouteThreads = 256;
-constexpr int kRouteItems = 16;                       // ids per thread in the count kernel
+constexpr int kRouteItems = 4;                        // ids per thread in the count kernel
 constexpr int kRouteChunk = kRouteThreads * kRouteItems;
 
 // Expert of slot i = t*Kt + k of the plan: the caller's id for the Kr routed slots; shared
