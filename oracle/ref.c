@@ -356,18 +356,25 @@ int oracle_forward_fp8_fp4(const uint8_t* x, const float* x_scale, const int32_t
     double* xv = (double*)malloc(sizeof(double) * (size_t)H);
     double* h = (double*)malloc(sizeof(double) * (size_t)(2 * I));
     double* a = (double*)malloc(sizeof(double) * (size_t)I);
-    int st = (counts && offsets && row_src && comb && xv && h && a) ? 0 : -2;
+    double* w1d = (double*)malloc(sizeof(double) * (size_t)(2 * I * H)); /* the expert's weights, decoded */
+    double* w2d = (double*)malloc(sizeof(double) * (size_t)(H * I));
+    int st = (counts && offsets && row_src && comb && xv && h && a && w1d && w2d) ? 0 : -2;
     if (st == 0) st = oracle_plan(ids, T, K, E, counts, offsets, row_src);
     for (int64_t e = 0; st == 0 && e < E; ++e) {
+        if (offsets[e + 1] == offsets[e]) continue; /* no rows */
+        for (int64_t j = 0; j < 2 * I; ++j)         /* decode W1[e] and W2[e] to their values once */
+            for (int64_t k = 0; k < H; ++k)
+                w1d[j * H + k] = fp4_weight(w1 + (e * 2 * I + j) * (H / 2), w1_scale + (e * 2 * I + j) * (H / 32), k);
+        for (int64_t c = 0; c < H; ++c)
+            for (int64_t j = 0; j < I; ++j)
+                w2d[c * I + j] = fp4_weight(w2 + (e * H + c) * (I / 2), w2_scale + (e * H + c) * (I / 32), j);
         for (int64_t p = offsets[e]; p < offsets[e + 1]; ++p) {
             const int64_t src = row_src[p], tok = src / K;
             for (int64_t k = 0; k < H; ++k)
                 xv[k] = e4m3_value(x[tok * H + k]) * (double)x_scale[tok * (H / 128) + k / 128];
             for (int64_t j = 0; j < 2 * I; ++j) { /* Linear1 */
-                const uint8_t* wr = w1 + (e * 2 * I + j) * (H / 2);
-                const uint8_t* sr = w1_scale + (e * 2 * I + j) * (H / 32);
                 double s = 0.0;
-                for (int64_t k = 0; k < H; ++k) s += xv[k] * fp4_weight(wr, sr, k);
+                for (int64_t k = 0; k < H; ++k) s += xv[k] * w1d[j * H + k];
                 h[j] = s;
             }
             for (int64_t j = 0; j < I; ++j) /* SwiGLU */
@@ -375,10 +382,8 @@ int oracle_forward_fp8_fp4(const uint8_t* x, const float* x_scale, const int32_t
             /* the e4m3 re-quantisation of A, blocks of 32 */
             mx_requant(a, I, 0, a_codes_out ? a_codes_out + p * I : NULL, a_exp_out ? a_exp_out + p * (I / 32) : NULL);
             for (int64_t c = 0; c < H; ++c) { /* Linear2, gate, the bf16 combine row */
-                const uint8_t* wr = w2 + (e * H + c) * (I / 2);
-                const uint8_t* sr = w2_scale + (e * H + c) * (I / 32);
                 double s = 0.0;
-                for (int64_t j = 0; j < I; ++j) s += a[j] * fp4_weight(wr, sr, j);
+                for (int64_t j = 0; j < I; ++j) s += a[j] * w2d[c * I + j];
                 comb[src * H + c] = gated(g[src], s);
             }
         }
@@ -391,6 +396,8 @@ int oracle_forward_fp8_fp4(const uint8_t* x, const float* x_scale, const int32_t
     free(xv);
     free(h);
     free(a);
+    free(w1d);
+    free(w2d);
     return st;
 }
 
@@ -415,28 +422,34 @@ int oracle_forward_fp8(int fmt, const uint8_t* x, const uint8_t* x_scale, const 
     double* xv = (double*)malloc(sizeof(double) * (size_t)H);
     double* h = (double*)malloc(sizeof(double) * (size_t)(2 * I));
     double* a = (double*)malloc(sizeof(double) * (size_t)I);
-    int st = (counts && offsets && row_src && comb && xv && h && a) ? 0 : -2;
+    double* w1d = (double*)malloc(sizeof(double) * (size_t)(2 * I * H)); /* the expert's weights, decoded */
+    double* w2d = (double*)malloc(sizeof(double) * (size_t)(H * I));
+    int st = (counts && offsets && row_src && comb && xv && h && a && w1d && w2d) ? 0 : -2;
     if (st == 0) st = oracle_plan(ids, T, K, E, counts, offsets, row_src);
     for (int64_t e = 0; st == 0 && e < E; ++e) {
+        if (offsets[e + 1] == offsets[e]) continue; /* no rows */
+        for (int64_t j = 0; j < 2 * I; ++j)         /* decode W1[e] and W2[e] to their values once */
+            for (int64_t k = 0; k < H; ++k)
+                w1d[j * H + k] = fp8_value(fmt, w1[(e * 2 * I + j) * H + k]) *
+                                 ue8m0_value(w1_scale[(e * 2 * I + j) * (H / 32) + k / 32]);
+        for (int64_t c = 0; c < H; ++c)
+            for (int64_t j = 0; j < I; ++j)
+                w2d[c * I + j] = fp8_value(fmt, w2[(e * H + c) * I + j]) * ue8m0_value(w2_scale[(e * H + c) * (I / 32) + j / 32]);
         for (int64_t p = offsets[e]; p < offsets[e + 1]; ++p) {
             const int64_t src = row_src[p], tok = src / K;
             for (int64_t k = 0; k < H; ++k)
                 xv[k] = fp8_value(fmt, x[tok * H + k]) * ue8m0_value(x_scale[tok * (H / 32) + k / 32]);
             for (int64_t j = 0; j < 2 * I; ++j) { /* GMM1 */
-                const uint8_t* wr = w1 + (e * 2 * I + j) * H;
-                const uint8_t* sr = w1_scale + (e * 2 * I + j) * (H / 32);
                 double s = 0.0;
-                for (int64_t k = 0; k < H; ++k) s += xv[k] * (fp8_value(fmt, wr[k]) * ue8m0_value(sr[k / 32]));
+                for (int64_t k = 0; k < H; ++k) s += xv[k] * w1d[j * H + k];
                 h[j] = s;
             }
             for (int64_t j = 0; j < I; ++j) /* SwiGLU */
                 a[j] = h[j] / (1.0 + exp(-h[j])) * h[I + j];
             mx_requant(a, I, fmt, a_codes_out ? a_codes_out + p * I : NULL, a_exp_out ? a_exp_out + p * (I / 32) : NULL);
             for (int64_t c = 0; c < H; ++c) { /* GMM2, gate, the bf16 combine row */
-                const uint8_t* wr = w2 + (e * H + c) * I;
-                const uint8_t* sr = w2_scale + (e * H + c) * (I / 32);
                 double s = 0.0;
-                for (int64_t j = 0; j < I; ++j) s += a[j] * (fp8_value(fmt, wr[j]) * ue8m0_value(sr[j / 32]));
+                for (int64_t j = 0; j < I; ++j) s += a[j] * w2d[c * I + j];
                 comb[src * H + c] = gated(g[src], s);
             }
         }
@@ -449,6 +462,8 @@ int oracle_forward_fp8(int fmt, const uint8_t* x, const uint8_t* x_scale, const 
     free(xv);
     free(h);
     free(a);
+    free(w1d);
+    free(w2d);
     return st;
 }
 
